@@ -1,0 +1,176 @@
+"""Python binding of libgdn, the Gated DeltaNet layer for GB300 (sm_103a).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls (include/gdn.h), turns torch tensors into device pointers and
+the current torch stream into a cudaStream_t, and raises ``GdnError`` on a
+non-OK status.  All arithmetic runs in the CUDA kernels of libgdn.so; there
+is no CPU path.  If libgdn.so has not been built, loading fails loudly.
+
+Shapes (see include/gdn.h for the full contract):
+  qkv [T, Cc] bf16 (Cc = 2 h_k 128 + h_v 128), z [T, h_v, 128] bf16,
+  a, b [T, h_v] bf16, A_log, dt_bias [h_v] fp32, conv_w [Cc, 4] bf16,
+  norm_w [128] fp32, conv_state [N, 3, Cc] fp32, ssm_state [N, h_v, 128, 128]
+  fp32, out [T, h_v, 128].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libgdn.so")
+
+GDN_OK = 0
+GDN_DTYPE_BF16 = 0
+GDN_DTYPE_F32 = 1
+STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
+                3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT",
+                6: "GDN_ERR_DEVICE_BOUNDS"}
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gdn_status_string(status)}")
+
+
+class Dims(ctypes.Structure):
+    """gdn_dims."""
+    _fields_ = [("h_k", ctypes.c_int), ("h_v", ctypes.c_int), ("d_k", ctypes.c_int),
+                ("d_v", ctypes.c_int), ("conv_w", ctypes.c_int), ("chunk", ctypes.c_int),
+                ("l2_eps", ctypes.c_float), ("rms_eps", ctypes.c_float)]
+
+
+def make_dims(h_k=16, h_v=32, d_k=128, d_v=128, conv_w=4, chunk=64, l2_eps=1e-6,
+              rms_eps=1e-6) -> Dims:
+    return Dims(h_k, h_v, d_k, d_v, conv_w, chunk, l2_eps, rms_eps)
+
+
+_lib = None
+_lock = threading.Lock()
+_P = ctypes.c_void_p
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libgdn.so (raises if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            DP = ctypes.POINTER(Dims)
+            L.gdn_version.restype = ctypes.c_int
+            L.gdn_version.argtypes = []
+            L.gdn_status_string.restype = ctypes.c_char_p
+            L.gdn_status_string.argtypes = [ctypes.c_int]
+            L.gdn_state_bytes.restype = ctypes.c_size_t
+            L.gdn_state_bytes.argtypes = [DP]
+            L.gdn_workspace_bytes.restype = ctypes.c_size_t
+            L.gdn_workspace_bytes.argtypes = [DP, ctypes.c_int, ctypes.c_longlong]
+            L.gdn_prefill.restype = ctypes.c_int
+            L.gdn_prefill.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
+                [_P] * 4 + [ctypes.c_size_t, _P]
+            L.gdn_decode_step.restype = ctypes.c_int
+            L.gdn_decode_step.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_int] + \
+                [_P] * 3 + [ctypes.c_int, _P, _P]
+            L.gdn_read_device_status.restype = ctypes.c_int
+            L.gdn_read_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
+            _lib = L
+    return _lib
+
+
+def gdn_version() -> int:
+    return lib().gdn_version()
+
+
+def gdn_status_string(status: int) -> str:
+    return lib().gdn_status_string(int(status)).decode()
+
+
+def gdn_state_bytes(dims: Dims) -> int:
+    return lib().gdn_state_bytes(ctypes.byref(dims))
+
+
+def gdn_workspace_bytes(dims: Dims, n_seqs: int, total_tokens: int) -> int:
+    return lib().gdn_workspace_bytes(ctypes.byref(dims), int(n_seqs), int(total_tokens))
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _ptr(t, dtype, name, numel=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return t                       # a raw device address, passed through
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: want a contiguous CUDA {dtype} tensor, "
+                         f"got {t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: want {numel} elements, got {t.numel()}")
+    return t.data_ptr()
+
+
+def _check(status: int, where: str):
+    if status != GDN_OK:
+        raise GdnError(status, where)
+
+
+def gdn_prefill(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, cu_seqlens,
+                conv_state, ssm_state, out, workspace, stream=None, n_seqs=None,
+                total_tokens=None):
+    """Chunked prefill over cu_seqlens-packed sequences (states updated in place)."""
+    bf, f32 = torch.bfloat16, torch.float32
+    N = int(n_seqs if n_seqs is not None else cu_seqlens.numel() - 1)
+    T = int(total_tokens if total_tokens is not None else qkv.shape[0])
+    Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib().gdn_prefill(
+        ctypes.byref(dims), _ptr(qkv, bf, "qkv", T * Cc), _ptr(z, bf, "z", T * dims.h_v * dims.d_v),
+        _ptr(a, bf, "a", T * dims.h_v), _ptr(b, bf, "b", T * dims.h_v),
+        _ptr(A_log, f32, "A_log", dims.h_v), _ptr(dt_bias, f32, "dt_bias", dims.h_v),
+        _ptr(conv_w, bf, "conv_w", Cc * dims.conv_w), _ptr(norm_w, f32, "norm_w", dims.d_v),
+        _ptr(cu_seqlens, torch.int32, "cu_seqlens", N + 1), N, T,
+        _ptr(conv_state, f32, "conv_state", N * (dims.conv_w - 1) * Cc),
+        _ptr(ssm_state, f32, "ssm_state", N * dims.h_v * dims.d_v * dims.d_k),
+        _ptr(out, bf, "out", T * dims.h_v * dims.d_v), _ptr(workspace, workspace.dtype, "workspace"),
+        ws_bytes, _stream(stream))
+    _check(st, "gdn_prefill")
+
+
+def gdn_decode_step(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,
+                    conv_state, ssm_state, out, device_status=None, stream=None, batch=None):
+    """One decode step for ``batch`` sequences (states updated in place)."""
+    bf, f32 = torch.bfloat16, torch.float32
+    B = int(batch if batch is not None else qkv.shape[0])
+    Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
+    out_dtype = GDN_DTYPE_F32 if out.dtype == f32 else GDN_DTYPE_BF16
+    st = lib().gdn_decode_step(
+        ctypes.byref(dims), _ptr(qkv, bf, "qkv", B * Cc), _ptr(z, bf, "z", B * dims.h_v * dims.d_v),
+        _ptr(a, bf, "a", B * dims.h_v), _ptr(b, bf, "b", B * dims.h_v),
+        _ptr(A_log, f32, "A_log", dims.h_v), _ptr(dt_bias, f32, "dt_bias", dims.h_v),
+        _ptr(conv_w, bf, "conv_w", Cc * dims.conv_w), _ptr(norm_w, f32, "norm_w", dims.d_v),
+        _ptr(slot, torch.int32, "slot", B), int(n_slots),
+        B, _ptr(conv_state, f32, "conv_state", int(n_slots) * (dims.conv_w - 1) * Cc),
+        _ptr(ssm_state, f32, "ssm_state", int(n_slots) * dims.h_v * dims.d_v * dims.d_k),
+        _ptr(out, out.dtype, "out", B * dims.h_v * dims.d_v), out_dtype,
+        _ptr(device_status, torch.int32, "device_status", 1), _stream(stream))
+    _check(st, "gdn_decode_step")
+
+
+def gdn_read_device_status(status_word, stream=None) -> int:
+    """Waits for the stream and returns the device status word's value."""
+    code = ctypes.c_int32(0)
+    addr = status_word.data_ptr() if isinstance(status_word, torch.Tensor) else status_word
+    _check(lib().gdn_read_device_status(addr, _stream(stream), ctypes.byref(code)),
+           "gdn_read_device_status")
+    return code.value

@@ -1,0 +1,181 @@
+// gdn_api.cu -- the extern "C" surface of libgdn: validation and launch.
+//
+// Every entry point validates its arguments on the host before it touches
+// the device; on any failure it returns a status and launches nothing.
+// Checks that need device data (cu_seqlens contents, slot indices) run in
+// the kernels and report through a device status word.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+#include "gdn_common.cuh"
+#include "gdn_launch.h"
+
+namespace {
+
+constexpr int kVersion = 100;  // 0.1.0
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool ptr_ok(const void* p) { return p != nullptr && aligned16(p); }
+
+// Shape sanity (INVALID_ARG) first, then the compiled fast path (UNSUPPORTED).
+gdn_status check_dims(const gdn_dims* d) {
+  if (!d) return GDN_ERR_INVALID_ARG;
+  if (d->h_k <= 0 || d->h_v <= 0 || d->h_v % d->h_k != 0 || d->d_k <= 0 ||
+      d->d_v <= 0 || d->conv_w <= 0 || d->chunk <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (!(d->l2_eps >= 0.0f) || !(d->rms_eps >= 0.0f) || !isfinite(d->l2_eps) ||
+      !isfinite(d->rms_eps))
+    return GDN_ERR_INVALID_ARG;
+  const int G = d->h_v / d->h_k;
+  if (d->d_k != gdn::kD || d->d_v != gdn::kD || d->conv_w != gdn::kConvW ||
+      d->chunk != gdn::kChunk || !(G == 1 || G == 2 || G == 4) || d->h_k > 64)
+    return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
+long long channels(const gdn_dims* d) {
+  return 2LL * d->h_k * d->d_k + (long long)d->h_v * d->d_v;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_version(void) { return kVersion; }
+
+const char* gdn_status_string(gdn_status s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null or misaligned pointer, bad size or inconsistent dims";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED: dims outside the compiled fast path (d_k = d_v = 128, conv_w = 4, chunk = 64, h_v/h_k in {1,2,4}, h_k <= 64)";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: workspace missing or smaller than gdn_workspace_bytes()";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA runtime call failed";
+    case GDN_ERR_DEVICE_TIMEOUT: return "GDN_ERR_DEVICE_TIMEOUT: a bounded device-side wait gave up";
+    case GDN_ERR_DEVICE_BOUNDS: return "GDN_ERR_DEVICE_BOUNDS: cu_seqlens or a slot index out of range";
+  }
+  return "unknown gdn_status";
+}
+
+size_t gdn_state_bytes(const gdn_dims* d) {
+  if (!d || d->h_k <= 0 || d->h_v <= 0 || d->d_k <= 0 || d->d_v <= 0 || d->conv_w <= 0 ||
+      d->h_v % d->h_k != 0)
+    return 0;
+  const size_t ssm = (size_t)d->h_v * d->d_v * d->d_k * sizeof(float);
+  const size_t conv = (size_t)(d->conv_w - 1) * (size_t)channels(d) * sizeof(float);
+  return ssm + conv;
+}
+
+size_t gdn_workspace_bytes(const gdn_dims* d, int n_seqs, long long total_tokens) {
+  if (check_dims(d) != GDN_OK || n_seqs < 0 || total_tokens < 0) return 0;
+  return 256 + gdn::prefill_scratch_bytes(n_seqs, d->h_k, d->h_v, total_tokens);
+}
+
+gdn_status gdn_prefill(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
+                       const void* b, const float* A_log, const float* dt_bias,
+                       const void* conv_w, const float* norm_w, const int32_t* cu_seqlens,
+                       int n_seqs, long long total_tokens, float* conv_state,
+                       float* ssm_state, void* out, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (n_seqs < 0 || total_tokens < 0 || total_tokens > (1LL << 31) - 1)
+    return GDN_ERR_INVALID_ARG;
+  if (n_seqs == 0 || total_tokens == 0) return GDN_OK;
+  if (!ptr_ok(qkv) || !ptr_ok(z) || !ptr_ok(a) || !ptr_ok(b) || !ptr_ok(A_log) ||
+      !ptr_ok(dt_bias) || !ptr_ok(conv_w) || !ptr_ok(norm_w) || !ptr_ok(cu_seqlens) ||
+      !ptr_ok(conv_state) || !ptr_ok(ssm_state) || !ptr_ok(out))
+    return GDN_ERR_INVALID_ARG;
+  const size_t need = gdn_workspace_bytes(dims, n_seqs, total_tokens);
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+    return GDN_ERR_WORKSPACE;
+
+  gdn::PrefillArgs p;
+  p.qkv = static_cast<const uint16_t*>(qkv);
+  p.z = static_cast<const uint16_t*>(z);
+  p.a = static_cast<const uint16_t*>(a);
+  p.b = static_cast<const uint16_t*>(b);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.conv_w = static_cast<const uint16_t*>(conv_w);
+  p.norm_w = norm_w;
+  p.cu_seqlens = cu_seqlens;
+  p.conv_state = conv_state;
+  p.ssm_state = ssm_state;
+  p.out = static_cast<uint16_t*>(out);
+  p.status = static_cast<int32_t*>(workspace);
+  p.scratch = static_cast<char*>(workspace) + 256;
+  p.scratch_bytes = workspace_bytes - 256;
+  p.n_seqs = n_seqs;
+  p.h_k = dims->h_k;
+  p.h_v = dims->h_v;
+  p.total_tokens = total_tokens;
+  p.l2_eps = dims->l2_eps;
+  p.rms_eps = dims->rms_eps;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(workspace, 0, 256, s) != cudaSuccess) return GDN_ERR_CUDA;
+  return gdn::launch_prefill(p, s) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const void* conv_w, const float* norm_w,
+                           const int32_t* slot, int n_slots, int batch, float* conv_state,
+                           float* ssm_state, void* out, int out_dtype,
+                           int32_t* device_status, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (batch < 0 || n_slots < 0 || (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32))
+    return GDN_ERR_INVALID_ARG;
+  if (batch == 0) return GDN_OK;
+  if ((long long)batch * dims->h_k > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
+  if (n_slots < 1 || (!slot && n_slots < batch)) return GDN_ERR_INVALID_ARG;
+  if (!ptr_ok(qkv) || !ptr_ok(z) || !ptr_ok(a) || !ptr_ok(b) || !ptr_ok(A_log) ||
+      !ptr_ok(dt_bias) || !ptr_ok(conv_w) || !ptr_ok(norm_w) || !ptr_ok(conv_state) ||
+      !ptr_ok(ssm_state) || !ptr_ok(out))
+    return GDN_ERR_INVALID_ARG;
+  if (slot && !aligned16(slot)) return GDN_ERR_INVALID_ARG;
+  if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
+    return GDN_ERR_INVALID_ARG;
+
+  gdn::DecodeArgs p;
+  p.qkv = static_cast<const uint16_t*>(qkv);
+  p.z = static_cast<const uint16_t*>(z);
+  p.a = static_cast<const uint16_t*>(a);
+  p.b = static_cast<const uint16_t*>(b);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.conv_w = static_cast<const uint16_t*>(conv_w);
+  p.norm_w = norm_w;
+  p.slot = slot;
+  p.conv_state = conv_state;
+  p.ssm_state = ssm_state;
+  p.out = out;
+  p.status = device_status;
+  p.n_slots = n_slots;
+  p.batch = batch;
+  p.h_k = dims->h_k;
+  p.h_v = dims->h_v;
+  p.l2_eps = dims->l2_eps;
+  p.rms_eps = dims->rms_eps;
+  return gdn::launch_decode(p, out_dtype == GDN_DTYPE_F32, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_read_device_status(const void* status_word, void* stream, int32_t* code) {
+  if (!status_word || !code || (reinterpret_cast<uintptr_t>(status_word) & 3u))
+    return GDN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, status_word, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
+  *code = v;
+  return GDN_OK;
+}
+
+}  // extern "C"

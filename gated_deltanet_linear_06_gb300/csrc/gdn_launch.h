@@ -1,0 +1,55 @@
+// gdn_launch.h -- argument packs and launchers of the libgdn kernels
+// (internal to the library; the public surface is include/gdn.h).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct DecodeArgs {
+  const uint16_t* qkv;     // bf16 [batch][Cc]
+  const uint16_t* z;       // bf16 [batch][h_v][128]
+  const uint16_t* a;       // bf16 [batch][h_v]
+  const uint16_t* b;       // bf16 [batch][h_v]
+  const float* A_log;      // [h_v]
+  const float* dt_bias;    // [h_v]
+  const uint16_t* conv_w;  // bf16 [Cc][4]
+  const float* norm_w;     // [128]
+  const int32_t* slot;     // nullable [batch]
+  float* conv_state;       // [n_slots][3][Cc]
+  float* ssm_state;        // [n_slots][h_v][128][128]
+  void* out;               // [batch][h_v][128], bf16 or fp32
+  int32_t* status;         // nullable device word
+  int n_slots, batch, h_k, h_v;
+  float l2_eps, rms_eps;
+};
+
+struct PrefillArgs {
+  const uint16_t* qkv;     // bf16 [T][Cc]
+  const uint16_t* z;       // bf16 [T][h_v][128]
+  const uint16_t* a;       // bf16 [T][h_v]
+  const uint16_t* b;       // bf16 [T][h_v]
+  const float* A_log;
+  const float* dt_bias;
+  const uint16_t* conv_w;  // bf16 [Cc][4]
+  const float* norm_w;
+  const int32_t* cu_seqlens;  // device [n_seqs + 1]
+  float* conv_state;       // [n_seqs][3][Cc]
+  float* ssm_state;        // [n_seqs][h_v][128][128]
+  uint16_t* out;           // bf16 [T][h_v][128]
+  int32_t* status;         // device word (workspace offset 0)
+  void* scratch;           // workspace beyond the status word
+  size_t scratch_bytes;
+  int n_seqs, h_k, h_v;
+  long long total_tokens;
+  float l2_eps, rms_eps;
+};
+
+// Host launchers: enqueue on `stream`, return the launch error (or
+// cudaSuccess).  Dims are validated by the caller.
+cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream);
+size_t prefill_scratch_bytes(int n_seqs, int h_k, int h_v, long long total_tokens);
+
+}  // namespace gdn

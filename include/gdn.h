@@ -1,0 +1,177 @@
+/*
+ * gdn.h -- C ABI of libgdn, the Gated DeltaNet layer on NVIDIA GB300 (sm_103a).
+ *
+ * The layer.  The source pages name it as the linear-attention layer of
+ * hybrid Qwen3.x-style models ("Serving large language models on our own
+ * stack", section "Qwen3.5-35B-A3B from a real GGUF"; "Our own inference
+ * runtime", section "What it is") and fix its serving properties: a
+ * fixed-size recurrent state per sequence, constant regardless of position
+ * (llmxabe README, architecture paragraph: ~60 MiB per sequence over 30
+ * layers, i.e. 2 MiB fp32 per layer at 32 x 128 x 128), carried across
+ * chunked prefill and decode (llmxabe README, the worker diagram:
+ * "chunked-prefill scheduler"), and a decode that is bit-identical whether a
+ * sequence runs alone or batched with others (llmxabe README, status and
+ * "Accuracy is a hard gate" paragraphs).  The pages print no formula; the
+ * layer computed here is the gated delta rule, per token t of a sequence:
+ *
+ *   y_t   = silu(causal depthwise conv_W(x)_t)      over the mixed q|k|v channels
+ *   q^    = q / sqrt(|q|^2 + l2_eps) / sqrt(d_k),    k^ = k / sqrt(|k|^2 + l2_eps)
+ *   g     = -exp(A_log[h]) * softplus(a_t[h] + dt_bias[h]),   beta = sigmoid(b_t[h])
+ *   S_t   = exp(g) S_{t-1} (I - beta k^ k^T) + beta v k^T     (S: d_v x d_k, fp32)
+ *   o_t   = S_t q^
+ *   out_t = o_t / sqrt(mean(o_t^2) + rms_eps) * norm_w * silu(z_t[h])
+ *
+ * Value head h reads key head h / (h_v / h_k).  The conv weight w[c][W-1]
+ * multiplies the current token and w[c][0] the oldest; there is no conv bias.
+ *
+ * Conventions for every call:
+ *   - The caller owns all memory.  The library never allocates, frees or
+ *     synchronises (gdn_read_device_status is the one call that waits).
+ *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *     void*; NULL = the legacy default stream).  The returned status covers
+ *     host-side validation and the launch only.  Device-side checks
+ *     (cu_seqlens contents, slot indices, bounded waits) write a code into a
+ *     device status word instead of faulting; read it with
+ *     gdn_read_device_status.
+ *   - On any non-OK status nothing was launched and no buffer was touched.
+ *   - All device pointers must be 16-byte aligned.  Tensors are dense and
+ *     row-major in the shapes given below.
+ *   - Activations (qkv, z, a, b), conv weights and the prefill output are
+ *     bf16 (raw uint16 bit patterns).  A_log, dt_bias, norm_w and both
+ *     states are fp32.
+ *   - The only dims compiled are d_k = d_v = 128, conv_w = 4, chunk = 64,
+ *     h_v / h_k in {1, 2, 4}, h_k <= 64; anything else returns
+ *     GDN_ERR_UNSUPPORTED.
+ *   - No exception crosses this boundary.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1,    /* null or misaligned pointer, bad size, inconsistent dims */
+  GDN_ERR_UNSUPPORTED = 2,    /* dims outside the compiled fast path */
+  GDN_ERR_WORKSPACE = 3,      /* workspace missing or smaller than gdn_workspace_bytes */
+  GDN_ERR_CUDA = 4,           /* a CUDA runtime call failed (launch, attribute, copy) */
+  GDN_ERR_DEVICE_TIMEOUT = 5, /* device word: a bounded device-side wait gave up */
+  GDN_ERR_DEVICE_BOUNDS = 6   /* device word: cu_seqlens or a slot index out of range */
+} gdn_status;
+
+/* Layer dimensions.  d_k / d_v: key / value head size; conv_w: conv width;
+ * chunk: prefill chunk length; the epsilons of the two norms. */
+typedef struct gdn_dims {
+  int h_k;
+  int h_v;
+  int d_k;
+  int d_v;
+  int conv_w;
+  int chunk;
+  float l2_eps;
+  float rms_eps;
+} gdn_dims;
+
+enum { GDN_DTYPE_BF16 = 0, GDN_DTYPE_F32 = 1 };
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* gdn_status_string(gdn_status status);
+
+/* Bytes of carried state per sequence: the fp32 SSM state
+ * [h_v][d_v][d_k] plus the fp32 conv state [conv_w - 1][Cc], with
+ * Cc = 2 h_k d_k + h_v d_v.  A snapshot of a sequence is a copy of these
+ * bytes (the pages' state "snapshot banks": "Our own inference runtime",
+ * section "What it is").  Returns 0 for invalid dims. */
+size_t gdn_state_bytes(const gdn_dims* dims);
+
+/* Device workspace gdn_prefill needs for this problem (>= 256 bytes; holds
+ * the device status word at offset 0).  Returns 0 for invalid arguments. */
+size_t gdn_workspace_bytes(const gdn_dims* dims, int n_seqs, long long total_tokens);
+
+/*
+ * Chunked prefill over cu_seqlens-packed variable-length sequences.
+ *
+ * Runs the layer over every token of n_seqs sequences packed back to back
+ * (no padding), each starting from its carried states, and leaves the
+ * states after its last token in place -- so a long prompt can be fed in
+ * segments, as a chunked-prefill scheduler does (llmxabe README, worker
+ * diagram), and a segment continues exactly where the previous one stopped.
+ *
+ *   qkv        bf16 [total_tokens][Cc]            channel order q | k | v (input)
+ *   z          bf16 [total_tokens][h_v][d_v]      output-gate input (input)
+ *   a, b       bf16 [total_tokens][h_v]           decay / write-gate inputs (input)
+ *   A_log      fp32 [h_v];  dt_bias fp32 [h_v]    (input)
+ *   conv_w     bf16 [Cc][conv_w]                  (input)
+ *   norm_w     fp32 [d_v]                         RMSNorm weight, shared by heads (input)
+ *   cu_seqlens int32 [n_seqs + 1], DEVICE memory, cu_seqlens[0] = 0,
+ *              non-decreasing, cu_seqlens[n_seqs] = total_tokens.  Violations
+ *              are caught on the device: the call then writes nothing and sets
+ *              GDN_ERR_DEVICE_BOUNDS in the status word.
+ *   conv_state fp32 [n_seqs][conv_w - 1][Cc]      in/out: raw inputs of the last
+ *              conv_w - 1 tokens, oldest first (zeros = fresh sequence)
+ *   ssm_state  fp32 [n_seqs][h_v][d_v][d_k]       in/out (zeros = fresh sequence)
+ *   out        bf16 [total_tokens][h_v][d_v]      (output)
+ *   workspace  device buffer of >= gdn_workspace_bytes(dims, n_seqs,
+ *              total_tokens) bytes, 256-byte aligned; its status word is reset
+ *              by the call itself.
+ * Empty sequences are allowed and leave their states unchanged.  n_seqs = 0
+ * or total_tokens = 0 launches nothing and returns GDN_OK.
+ */
+gdn_status gdn_prefill(const gdn_dims* dims, const void* qkv, const void* z,
+                       const void* a, const void* b, const float* A_log,
+                       const float* dt_bias, const void* conv_w,
+                       const float* norm_w, const int32_t* cu_seqlens,
+                       int n_seqs, long long total_tokens, float* conv_state,
+                       float* ssm_state, void* out, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * One decode step for a batch of sequences, one token each.
+ *
+ * Per sequence this is the same arithmetic in the same order whatever the
+ * batch size or the batch's other members: a sequence decodes bit-identically
+ * alone or batched (llmxabe README, "Accuracy is a hard gate" paragraph).
+ *
+ *   qkv  bf16 [batch][Cc];  z bf16 [batch][h_v][d_v];  a, b bf16 [batch][h_v]
+ *   A_log, dt_bias, conv_w, norm_w   as for gdn_prefill
+ *   slot       NULL: batch entry i uses state i of the arrays below.
+ *              Else int32 [batch] DEVICE memory: entry i uses state slot[i],
+ *              0 <= slot[i] < n_slots, all distinct.  An out-of-range entry
+ *              is skipped on the device (its out row is left untouched) and
+ *              GDN_ERR_DEVICE_BOUNDS is written to *device_status if given.
+ *   n_slots    number of states in the arrays (>= batch when slot is NULL).
+ *   conv_state fp32 [n_slots][conv_w - 1][Cc]   in/out
+ *   ssm_state  fp32 [n_slots][h_v][d_v][d_k]    in/out
+ *   out        [batch][h_v][d_v], bf16 or fp32 per out_dtype (output)
+ *   device_status  NULL or a device int32 word that device checks write into
+ *              (never cleared by this call).
+ * batch = 0 launches nothing and returns GDN_OK.
+ */
+gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const void* conv_w,
+                           const float* norm_w, const int32_t* slot,
+                           int n_slots, int batch, float* conv_state,
+                           float* ssm_state, void* out, int out_dtype,
+                           int32_t* device_status, void* stream);
+
+/* Waits for the stream, then reads a device status word (the first 4 bytes
+ * of a prefill workspace, or a decode device_status word) into *code:
+ * GDN_OK or the first device-side error recorded.  Returns GDN_ERR_CUDA if
+ * the copy or the wait failed. */
+gdn_status gdn_read_device_status(const void* status_word, void* stream,
+                                  int32_t* code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,149 @@
+"""Host-side checks of the C ABI: the library loads, exports what the header
+declares, and rejects bad arguments before it touches a device.
+
+No call here reaches the GPU: every call either returns from host-side
+validation or launches nothing (empty batch), so these run without a device.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_deltanet_linear_06_gb300 as gdn
+from gated_deltanet_linear_06_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+FAKE = 0x10000          # a 16-byte-aligned address that is never dereferenced on this path
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return gdn.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gdn_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for want in ("gdn_prefill", "gdn_decode_step", "gdn_workspace_bytes", "gdn_state_bytes",
+                 "gdn_read_device_status", "gdn_status_string", "gdn_version"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", gdn.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (gdn_[a-z_]+)\b", out))
+    assert set(_declared_functions()) <= exported
+
+
+def test_version_and_status_strings(L):
+    assert gdn.gdn_version() >= 100
+    for code in range(7):
+        s = gdn.gdn_status_string(code)
+        assert s.startswith(gdn.STATUS_NAMES[code])
+    assert "unknown" in gdn.gdn_status_string(99)
+
+
+def test_state_bytes_matches_the_pages_state_size(L):
+    # 32 value heads x 128 x 128 fp32 = 2 MiB of SSM state per layer; over
+    # 30 Gated DeltaNet layers that is the ~60 MiB per sequence the llmxabe
+    # README states.  The conv state adds 3 rows of 8192 fp32 channels.
+    d = gdn.make_dims()
+    assert gdn.gdn_state_bytes(d) == 2 * 2**20 + 3 * 8192 * 4
+    assert 30 * 32 * 128 * 128 * 4 == 60 * 2**20
+    assert gdn.gdn_state_bytes(gdn.make_dims(h_k=0)) == 0
+
+
+def test_workspace_bytes(L):
+    d = gdn.make_dims()
+    assert gdn.gdn_workspace_bytes(d, 1, 4096) >= 256
+    assert gdn.gdn_workspace_bytes(d, -1, 4096) == 0
+    assert gdn.gdn_workspace_bytes(gdn.make_dims(d_k=64), 1, 64) == 0
+
+
+def _decode(L, dims, **kw):
+    args = dict(qkv=FAKE, z=FAKE, a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE, conv_w=FAKE,
+                norm_w=FAKE, slot=None, n_slots=4, batch=4, conv_state=FAKE, ssm_state=FAKE,
+                out=FAKE, out_dtype=0, status=None, stream=None)
+    args.update(kw)
+    return L.gdn_decode_step(ctypes.byref(dims) if dims is not None else None, args["qkv"],
+                             args["z"], args["a"], args["b"], args["A_log"], args["dt_bias"],
+                             args["conv_w"], args["norm_w"], args["slot"], args["n_slots"],
+                             args["batch"], args["conv_state"], args["ssm_state"], args["out"],
+                             args["out_dtype"], args["status"], args["stream"])
+
+
+def _prefill(L, dims, **kw):
+    args = dict(qkv=FAKE, z=FAKE, a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE, conv_w=FAKE,
+                norm_w=FAKE, cu=FAKE, n_seqs=2, T=100, conv_state=FAKE, ssm_state=FAKE,
+                out=FAKE, ws=0x100000, ws_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return L.gdn_prefill(ctypes.byref(dims) if dims is not None else None, args["qkv"],
+                         args["z"], args["a"], args["b"], args["A_log"], args["dt_bias"],
+                         args["conv_w"], args["norm_w"], args["cu"], args["n_seqs"], args["T"],
+                         args["conv_state"], args["ssm_state"], args["out"], args["ws"],
+                         args["ws_bytes"], args["stream"])
+
+
+OK, INVALID, UNSUP, WS = 0, 1, 2, 3
+
+
+def test_decode_rejects_bad_dims(L):
+    assert _decode(L, None) == INVALID
+    assert _decode(L, gdn.make_dims(h_k=3, h_v=32)) == INVALID        # h_v % h_k
+    assert _decode(L, gdn.make_dims(h_k=0)) == INVALID
+    assert _decode(L, gdn.make_dims(l2_eps=-1.0)) == INVALID
+    assert _decode(L, gdn.make_dims(l2_eps=float("nan"))) == INVALID
+    assert _decode(L, gdn.make_dims(d_k=64, d_v=64)) == UNSUP
+    assert _decode(L, gdn.make_dims(conv_w=3)) == UNSUP
+    assert _decode(L, gdn.make_dims(h_k=4, h_v=32)) == UNSUP           # G = 8
+    assert _decode(L, gdn.make_dims(h_k=128, h_v=128)) == UNSUP        # h_k > 64
+
+
+def test_decode_rejects_bad_pointers_and_sizes(L):
+    d = gdn.make_dims()
+    assert _decode(L, d, qkv=None) == INVALID
+    assert _decode(L, d, ssm_state=FAKE + 4) == INVALID               # misaligned
+    assert _decode(L, d, out=FAKE + 8) == INVALID
+    assert _decode(L, d, slot=FAKE + 4) == INVALID
+    assert _decode(L, d, status=FAKE + 2) == INVALID
+    assert _decode(L, d, batch=-1) == INVALID
+    assert _decode(L, d, n_slots=3) == INVALID                         # fewer states than batch
+    assert _decode(L, d, out_dtype=7) == INVALID
+    assert _decode(L, d, batch=0) == OK                                # nothing to launch
+
+
+def test_prefill_rejects_bad_arguments(L):
+    d = gdn.make_dims()
+    assert _prefill(L, None) == INVALID
+    assert _prefill(L, gdn.make_dims(chunk=32)) == UNSUP
+    assert _prefill(L, d, cu=None) == INVALID
+    assert _prefill(L, d, z=FAKE + 2) == INVALID
+    assert _prefill(L, d, n_seqs=-1) == INVALID
+    assert _prefill(L, d, T=-5) == INVALID
+    assert _prefill(L, d, T=1 << 31) == INVALID
+    assert _prefill(L, d, ws=None) == WS
+    assert _prefill(L, d, ws=0x100010) == WS                           # not 256-aligned
+    assert _prefill(L, d, ws_bytes=16) == WS
+    assert _prefill(L, d, n_seqs=0) == OK                              # nothing to launch
+    assert _prefill(L, d, T=0) == OK
+
+
+def test_binding_checks_tensor_arguments(L):
+    import torch
+    d = gdn.make_dims()
+    cpu = torch.zeros(4, 8192, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gdn.gdn_decode_step(d, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, None, 4, cpu, cpu,
+                            torch.zeros(4, 32, 128), stream=0)
