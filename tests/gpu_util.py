@@ -48,3 +48,20 @@ def oracle_layer(sh: gi.Shape, tok: dict, params: dict, cu, conv_state=None, ssm
 
 def to_dev(d: dict) -> dict:
     return {k: v.to(DEV) for k, v in d.items()}
+
+
+def assert_bf16_close(got_bf16, ref, tol=DECODE_TOL):
+    """bf16 output check: |got - ref| <= 1 bf16 ulp of ref + tol * max|ref|.
+
+    A bf16 result of an fp32 computation that meets ``tol`` differs from the
+    exact value by its rounding (at most one ulp once the fp32 error can push
+    it across a rounding boundary) plus the fp32 error itself; near-zero
+    outputs are dominated by the second term."""
+    got = got_bf16.detach().float().cpu().double().numpy() if isinstance(got_bf16, torch.Tensor) \
+        else np.asarray(got_bf16, np.float64)
+    ref = np.asarray(ref, np.float64)
+    bound = bf16_ulp(ref) + tol * np.abs(ref).max()
+    excess = np.abs(got - ref) - bound
+    worst_ulps = float((np.abs(got - bf16_round(ref)) / bf16_ulp(ref)).max())
+    assert np.all(excess <= 0), f"bf16 output off by up to {worst_ulps:.1f} ulp beyond the bound"
+    return worst_ulps

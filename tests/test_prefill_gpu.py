@@ -1,0 +1,171 @@
+"""GPU parity of gdn_prefill against the fp64 oracle, through the C ABI.
+
+Bar: max |gpu - oracle| / max |oracle| <= 1e-2 over the bf16 output and over
+the fp32 final state (bf16 tensor-core operands, fp32 accumulation); the
+conv state, a copy of raw inputs, must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_deltanet_linear_06_gb300 as gdn
+import gdn_inputs as gi
+from gpu_util import DECODE_TOL, DEV, PREFILL_TOL, dims_of, oracle_layer, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+SH = gi.LAYER
+
+
+def _inputs(sh, lengths, seed, slow=False, ssm_std=0.0, conv_std=0.0, norm_w="ones"):
+    T = sum(lengths)
+    params = gi.make_params(sh, seed, norm_w=norm_w)
+    tok = gi.make_tokens(sh, T, seed)
+    if slow:
+        gc = gi.gate_controlled(sh, T, seed)
+        tok["a"], tok["b"] = gc["a"], gc["b"]
+        params["A_log"], params["dt_bias"] = gc["A_log"], gc["dt_bias"]
+    st = gi.make_states(sh, len(lengths), seed, ssm_std=ssm_std, conv_std=conv_std)
+    return params, tok, st
+
+
+def _run(sh, lengths, params, tok, st, out_fill=None):
+    dims = dims_of(sh)
+    N, T = len(lengths), sum(lengths)
+    conv = st["conv_state"].clone().to(DEV)
+    ssm = st["ssm_state"].clone().to(DEV)
+    out = torch.empty(T, sh.h_v, sh.d_v, dtype=torch.bfloat16, device=DEV)
+    if out_fill is not None:
+        out.fill_(out_fill)
+    ws = torch.empty(gdn.gdn_workspace_bytes(dims, N, T), dtype=torch.uint8, device=DEV)
+    pd, td = to_dev(params), to_dev(tok)
+    gdn.gdn_prefill(dims, td["qkv"], td["z"], td["a"], td["b"], pd["A_log"], pd["dt_bias"],
+                    pd["conv_w"], pd["norm_w"], gi.cu_seqlens(lengths).to(DEV), conv, ssm, out, ws)
+    status = gdn.gdn_read_device_status(ws)
+    return out, conv, ssm, status
+
+
+def _check(sh, lengths, params, tok, st, head_mask=None, tol=PREFILL_TOL):
+    out, conv, ssm, status = _run(sh, lengths, params, tok, st)
+    assert status == 0
+    ref, ref_conv, ref_ssm = oracle_layer(sh, tok, params, gi.cu_seqlens(lengths),
+                                          conv_state=st["conv_state"], ssm_state=st["ssm_state"],
+                                          head_mask=head_mask)
+    heads = slice(None) if head_mask is None else [i for i, m in enumerate(head_mask) if m]
+    e_out = rel_err(out[:, heads], ref[:, heads])
+    e_ssm = rel_err(ssm[:, heads], ref_ssm[:, heads])
+    np.testing.assert_array_equal(conv.cpu().double().numpy(), ref_conv)
+    assert e_out <= tol and e_ssm <= tol, (e_out, e_ssm)
+    return e_out, e_ssm
+
+
+@pytest.mark.parametrize("slow", [False, True])
+def test_prefill_varlen_ragged_short_and_empty(slow):
+    lengths = [70, 33, 1, 2, 128, 0, 64, 200]
+    params, tok, st = _inputs(SH, lengths, 5, slow=slow, ssm_std=0.1 ** 0.5, conv_std=1.0,
+                              norm_w="uniform")
+    e = _check(SH, lengths, params, tok, st)
+    print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
+
+
+def test_prefill_single_sequence_4096():
+    # T = 4096, zero initial state, seed 2
+    params, tok, st = _inputs(SH, [4096], 2)
+    e = _check(SH, [4096], params, tok, st)
+    print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
+
+
+def test_prefill_long_varlen_with_carried_segments():
+    # packed {32768, 8192, 2048, 512, 131072 split into 4 x 32768 segments
+    # carrying state}, seed 3.  Call 1 packs the four sequences and the first
+    # segment; calls 2-4 continue the segmented sequence from its states.  The
+    # outputs and the final states are compared with the oracle run on the
+    # unsegmented sequences, on a sample of value heads.
+    seg = 32768
+    lengths = [32768, 8192, 2048, 512, 4 * seg]
+    params, tok, st = _inputs(SH, lengths, 3)
+    mask = [1 if h in (0, 13, 31) else 0 for h in range(SH.h_v)]
+    heads = [0, 13, 31]
+    ref, ref_conv, ref_ssm = oracle_layer(SH, tok, params, gi.cu_seqlens(lengths),
+                                          conv_state=st["conv_state"], ssm_state=st["ssm_state"],
+                                          head_mask=mask)
+    T1 = sum(lengths[:4]) + seg
+    first = {k: v[:T1] for k, v in tok.items()}
+    out1, conv, ssm, status = _run(SH, lengths[:4] + [seg], params, first, st)
+    assert status == 0
+    outs = [out1[:, heads].float().cpu()]
+    for k in range(1, 4):
+        part = {kk: v[T1 + (k - 1) * seg:T1 + k * seg] for kk, v in tok.items()}
+        sk = {"conv_state": conv[4:5].cpu(), "ssm_state": ssm[4:5].cpu()}
+        o, c, s, status = _run(SH, [seg], params, part, sk)
+        assert status == 0
+        outs.append(o[:, heads].float().cpu())
+        conv[4:5], ssm[4:5] = c, s
+    got = torch.cat(outs)
+    e_out = rel_err(got, ref[:, heads])
+    e_ssm = rel_err(ssm[:, heads], ref_ssm[:, heads])
+    np.testing.assert_array_equal(conv.cpu().double().numpy(), ref_conv)
+    print(f"rel err out {e_out:.2e} state {e_ssm:.2e}")
+    assert e_out <= PREFILL_TOL and e_ssm <= PREFILL_TOL
+
+
+def test_prefill_then_decode_equals_longer_prefill():
+    T = 77
+    params, tok, st = _inputs(SH, [T + 1], 6, slow=True, ssm_std=0.3, conv_std=1.0)
+    ref, ref_conv, ref_ssm = oracle_layer(SH, tok, params, gi.cu_seqlens([T + 1]),
+                                          conv_state=st["conv_state"], ssm_state=st["ssm_state"])
+    head = {k: v[:T] for k, v in tok.items()}
+    out, conv, ssm, status = _run(SH, [T], params, head, st)
+    assert status == 0
+    last = to_dev({k: v[T:] for k, v in tok.items()})
+    pd = to_dev(params)
+    o1 = torch.empty(1, SH.h_v, SH.d_v, device=DEV)
+    gdn.gdn_decode_step(dims_of(SH), last["qkv"], last["z"], last["a"], last["b"], pd["A_log"],
+                        pd["dt_bias"], pd["conv_w"], pd["norm_w"], None, 1, conv, ssm, o1)
+    assert rel_err(out, ref[:T]) <= PREFILL_TOL
+    assert rel_err(o1, ref[T:]) <= PREFILL_TOL
+    assert rel_err(ssm, ref_ssm) <= PREFILL_TOL
+    np.testing.assert_array_equal(conv.cpu().double().numpy(), ref_conv)
+
+
+@pytest.mark.parametrize("h_k,h_v", [(32, 32), (8, 32), (2, 4)])
+def test_prefill_other_head_groupings(h_k, h_v):
+    sh = gi.Shape(h_k=h_k, h_v=h_v)
+    lengths = [100, 7, 64]
+    params, tok, st = _inputs(sh, lengths, 7, ssm_std=0.3, conv_std=1.0, norm_w="uniform")
+    _check(sh, lengths, params, tok, st)
+
+
+def test_prefill_extreme_decay_stays_finite():
+    # a = 30 gives g ~ -30 exp(A_log) per token: the cumulative decay of a
+    # chunk is far below fp32's range, and every exponential must stay finite
+    lengths = [130]
+    params, tok, st = _inputs(SH, lengths, 8, ssm_std=0.3)
+    tok["a"] = torch.full_like(tok["a"], 30.0)
+    _check(SH, lengths, params, tok, st)
+
+
+def test_prefill_bad_cu_seqlens_writes_nothing():
+    lengths = [40, 24]
+    params, tok, st = _inputs(SH, lengths, 9, ssm_std=0.3, conv_std=1.0)
+    dims = dims_of(SH)
+    conv, ssm = st["conv_state"].clone().to(DEV), st["ssm_state"].clone().to(DEV)
+    out = torch.full((64, SH.h_v, SH.d_v), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(gdn.gdn_workspace_bytes(dims, 2, 64), dtype=torch.uint8, device=DEV)
+    pd, td = to_dev(params), to_dev(tok)
+    for bad in ([0, 50, 40], [0, 40, 65], [1, 40, 64]):
+        gdn.gdn_prefill(dims, td["qkv"], td["z"], td["a"], td["b"], pd["A_log"], pd["dt_bias"],
+                        pd["conv_w"], pd["norm_w"], torch.tensor(bad, dtype=torch.int32, device=DEV),
+                        conv, ssm, out, ws)
+        assert gdn.gdn_read_device_status(ws) == 6
+        assert torch.isnan(out.float()).all()
+        assert torch.equal(ssm.cpu(), st["ssm_state"]) and torch.equal(conv.cpu(), st["conv_state"])
+
+
+def test_prefill_writes_every_output_and_is_deterministic():
+    lengths = [65, 3, 190]
+    params, tok, st = _inputs(SH, lengths, 10, ssm_std=0.3, conv_std=1.0)
+    a = _run(SH, lengths, params, tok, st, out_fill=float("nan"))
+    b = _run(SH, lengths, params, tok, st, out_fill=0.0)
+    assert not torch.isnan(a[0].float()).any()
+    for x, y in zip(a[:3], b[:3]):
+        assert torch.equal(x, y)
