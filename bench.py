@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Throughput of the Gated DeltaNet layer's hot path on GB300, one JSON line.
+
+One step = one gdn_prefill of a single 32,768-token sequence (16 key / 32
+value heads, d = 128, seed 3) followed by 16 gdn_decode_step calls over a
+batch of 256 sequences (seed 4, exp(g) ~ U(0.5, 1)), all inputs seeded and
+synthetic and resident in HBM before the timed region.  Both inputs exceed
+the 129 MB L2 (prefill activations 0.77 GB, decode state 0.54 GB), so no L2
+flush is needed between iterations.
+
+  value            prefill tokens/s, summed over ranks (device time of the
+                   gdn_prefill calls, CUDA events on the launching stream)
+  decode           seq-steps/s of the decode calls, same clock
+  roofline         prefill: HBM-bound (arithmetic intensity below the ridge);
+                   the tensor-core fraction of the effective FLOPs rides along
+  e2e              the same metrics through the C ABI with host buffers: the
+                   pinned host->device copy of each call's inputs and the
+                   device->host copy of its outputs are inside the timed region
+  cpu_baseline     the fp64 oracle on this host's cores, on a bounded sample
+
+``--impl reference`` times the oracle itself (the only reference there is) on
+the same workload, one bounded sample per step.  Under torchrun every rank
+runs its own replica (weak scaling); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN prefill tokens/s (T=32K) & decode seq-steps/s (B=256); % TC/HBM roofline"
+PREFILL_T, PREFILL_SEED = 32768, 3
+DECODE_B, DECODE_CALLS, DECODE_SEED = 256, 16, 4
+H_K, H_V, D = 16, 32, 128
+CC = 2 * H_K * D + H_V * D
+# effective FLOPs of the chunked form (C = 64) per token: per value head
+# 2C(3 d_k + 2 d_v) + 6 d_k d_v = 180,224
+FLOP_PER_TOKEN = (2 * 64 * (3 * D + 2 * D) + 6 * D * D) * H_V
+# minimum HBM bytes per prefill token: qkv 16,384 + z 8,192 + a,b 128 + out 8,192
+PREFILL_BYTES_PER_TOKEN = CC * 2 + H_V * D * 2 + 2 * H_V * 2 + H_V * D * 2
+STATE_BYTES = H_V * D * D * 4 + 3 * CC * 4          # per sequence (ssm + conv)
+# per decode seq-step: state read + write, activations, output
+DECODE_BYTES_PER_SEQSTEP = 2 * STATE_BYTES + CC * 2 + H_V * D * 2 + 2 * H_V * 2 + H_V * D * 2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _src_hash(name: str) -> str:
+    with open(os.path.join(ROOT, "gated_deltanet_linear_06_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _traffic(kernel: str, src: str):
+    """DRAM bytes per launch from the committed ncu summary, or None if the
+    kernel source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel)
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("src_sha256_16") != _src_hash(src):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    """(rank, world, local_rank); initialises a gloo group for timing only."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("gloo")
+    return rank, world, local
+
+
+def aggregate_max(value: float, world: int) -> float:
+    """Max of a per-rank number over all ranks (the slowest rank sets the time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---- CPU baseline: the oracle, as it stands, on a bounded sample -------------
+
+def _prefill_workload_cpu(T: int):
+    import gdn_inputs as gi
+    sh = gi.LAYER
+    return sh, gi.make_params(sh, PREFILL_SEED), gi.make_tokens(sh, T, PREFILL_SEED)
+
+
+def oracle_prefill_sample(tokens: int, threads: int) -> tuple[float, float]:
+    """Runs the oracle over the first ``tokens`` tokens of the prefill workload,
+    all value heads; returns (tokens/s, seconds)."""
+    import oracle
+    sh, p, tok = _prefill_workload_cpu(tokens)
+    t0 = time.perf_counter()
+    oracle.layer(h_k=sh.h_k, h_v=sh.h_v, d_k=sh.d_k, d_v=sh.d_v, qkv=tok["qkv"], z=tok["z"],
+                 a=tok["a"], b=tok["b"], cu_seqlens=[0, tokens], n_threads=threads, **p)
+    dt = time.perf_counter() - t0
+    return tokens / dt, dt
+
+
+def oracle_decode_sample(batch: int, threads: int) -> tuple[float, float]:
+    """One oracle decode step over ``batch`` sequences (carried states);
+    returns (seq-steps/s, seconds)."""
+    import oracle
+    import gdn_inputs as gi
+    sh = gi.LAYER
+    p = gi.make_params(sh, DECODE_SEED)
+    st = gi.make_states(sh, batch, DECODE_SEED, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    tok = gi.make_tokens(sh, batch, DECODE_SEED)
+    t0 = time.perf_counter()
+    oracle.layer(h_k=sh.h_k, h_v=sh.h_v, d_k=sh.d_k, d_v=sh.d_v, qkv=tok["qkv"], z=tok["z"],
+                 a=tok["a"], b=tok["b"], cu_seqlens=list(range(batch + 1)), n_threads=threads,
+                 conv_state=st["conv_state"], ssm_state=st["ssm_state"], **p)
+    dt = time.perf_counter() - t0
+    return batch / dt, dt
+
+
+def cpu_baseline() -> dict:
+    import oracle
+    threads = os.cpu_count() or 1
+    oracle.build()
+    pre_tps, pre_s = oracle_prefill_sample(4096, threads)
+    dec_sps, dec_s = oracle_decode_sample(64, threads)
+    return {"value": round(pre_tps, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"prefill: first 4096 tokens of the 32768-token sequence, all 32 value heads "
+                      f"({pre_s:.1f} s); decode: one step of 64 of the 256 sequences "
+                      f"({dec_s:.1f} s) = {dec_sps:.1f} seq-steps/s",
+            "decode_value": round(dec_sps, 2), "decode_unit": "seq-steps/s"}
+
+
+# ---- our arm --------------------------------------------------------------------
+
+def run_ours(args) -> dict | None:
+    import torch
+
+    import gated_deltanet_linear_06_gb300 as gdn
+    import gdn_inputs as gi
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sh = gi.LAYER
+    dims = gdn.make_dims(h_k=sh.h_k, h_v=sh.h_v)
+    peaks, peak_src = _peaks()
+
+    # prefill workload (host copies kept pinned for the end-to-end leg)
+    p_host = gi.make_params(sh, PREFILL_SEED)
+    x_host = gi.make_tokens(sh, PREFILL_T, PREFILL_SEED)
+    params = {k: v.to(dev) for k, v in p_host.items()}
+    x_dev = {k: v.to(dev) for k, v in x_host.items()}
+    cu = gi.cu_seqlens([PREFILL_T]).to(dev)
+    conv = torch.zeros(1, 3, sh.cc, device=dev)
+    ssm = torch.zeros(1, sh.h_v, D, D, device=dev)
+    out = torch.empty(PREFILL_T, sh.h_v, D, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(gdn.gdn_workspace_bytes(dims, 1, PREFILL_T), dtype=torch.uint8, device=dev)
+
+    # decode workload: 256 carried states, 16 token sets
+    dp_host = gi.make_params(sh, DECODE_SEED)
+    gc = gi.gate_controlled(sh, 1, DECODE_SEED)
+    dp_host["A_log"], dp_host["dt_bias"] = gc["A_log"], gc["dt_bias"]
+    dparams = {k: v.to(dev) for k, v in dp_host.items()}
+    st = gi.make_states(sh, DECODE_B, DECODE_SEED, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    dconv, dssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
+    dtok_host = []
+    for j in range(DECODE_CALLS):
+        t = gi.make_tokens(sh, DECODE_B, DECODE_SEED, offset=j * DECODE_B)
+        g = gi.gate_controlled(sh, DECODE_B, DECODE_SEED, decay=(0.5, 1.0), beta=(0.0, 1.0), offset=j)
+        t["a"], t["b"] = g["a"], g["b"]
+        dtok_host.append(t)
+    dtok = [{k: v.to(dev) for k, v in t.items()} for t in dtok_host]
+    dout = torch.empty(DECODE_B, sh.h_v, D, dtype=torch.bfloat16, device=dev)
+
+    stream = torch.cuda.current_stream(dev)
+
+    def prefill():
+        gdn.gdn_prefill(dims, x_dev["qkv"], x_dev["z"], x_dev["a"], x_dev["b"], params["A_log"],
+                        params["dt_bias"], params["conv_w"], params["norm_w"], cu, conv, ssm, out,
+                        ws, stream=stream)
+
+    def decode(j):
+        t = dtok[j]
+        gdn.gdn_decode_step(dims, t["qkv"], t["z"], t["a"], t["b"], dparams["A_log"],
+                            dparams["dt_bias"], dparams["conv_w"], dparams["norm_w"], None,
+                            DECODE_B, dconv, dssm, dout, stream=stream)
+
+    def step():
+        prefill()
+        for j in range(DECODE_CALLS):
+            decode(j)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    status = gdn.gdn_read_device_status(ws)
+    if status != 0:
+        raise RuntimeError(f"prefill device status {gdn.STATUS_NAMES.get(status, status)}")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        t_all0.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            prefill()
+            ev[k][1].record(stream)
+            ev[k][2].record(stream)
+            for j in range(DECODE_CALLS):
+                decode(j)
+            ev[k][3].record(stream)
+        t_all1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    total_ms = aggregate_max(t_all0.elapsed_time(t_all1), world)
+    pre_ms = aggregate_max(sum(e[0].elapsed_time(e[1]) for e in ev) / K, world)
+    dec_ms = aggregate_max(sum(e[2].elapsed_time(e[3]) for e in ev) / K, world)
+
+    # ---- end to end through host buffers ----
+    pin = lambda t: t.pin_memory()
+    x_pin = {k: pin(v) for k, v in x_host.items()}
+    out_pin = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    ssm_pin = torch.empty(ssm.shape, dtype=ssm.dtype).pin_memory()
+    conv_pin = torch.empty(conv.shape, dtype=conv.dtype).pin_memory()
+    dtok_pin = [{k: pin(v) for k, v in t.items()} for t in dtok_host]
+    dout_pin = torch.empty(dout.shape, dtype=dout.dtype).pin_memory()
+    h2d_pre = sum(v.numel() * v.element_size() for v in x_pin.values())
+    d2h_pre = sum(t.numel() * t.element_size() for t in (out_pin, ssm_pin, conv_pin))
+    h2d_dec = sum(v.numel() * v.element_size() for t in dtok_pin for v in t.values())
+    d2h_dec = DECODE_CALLS * dout_pin.numel() * dout_pin.element_size()
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    for k in range(K):
+        e2e_ev[k][0].record(stream)
+        for name in ("qkv", "z", "a", "b"):
+            x_dev[name].copy_(x_pin[name], non_blocking=True)
+        prefill()
+        out_pin.copy_(out, non_blocking=True)
+        ssm_pin.copy_(ssm, non_blocking=True)
+        conv_pin.copy_(conv, non_blocking=True)
+        e2e_ev[k][1].record(stream)
+        e2e_ev[k][2].record(stream)
+        for j in range(DECODE_CALLS):
+            for name in ("qkv", "z", "a", "b"):
+                dtok[j][name].copy_(dtok_pin[j][name], non_blocking=True)
+            decode(j)
+            dout_pin.copy_(dout, non_blocking=True)
+        e2e_ev[k][3].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_pre_ms = aggregate_max(sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / K, world)
+    e2e_dec_ms = aggregate_max(sum(e[2].elapsed_time(e[3]) for e in e2e_ev) / K, world)
+    if rank != 0:
+        return None
+
+    hbm = float(peaks["hbm_gbs"])
+    tc_peak = float(peaks["bf16_tflops"])
+    pre_bytes = PREFILL_T * PREFILL_BYTES_PER_TOKEN + 2 * STATE_BYTES
+    pre_gbs = pre_bytes / (pre_ms * 1e-3) / 1e9
+    pre_tflops = PREFILL_T * FLOP_PER_TOKEN / (pre_ms * 1e-3) / 1e12
+    dec_bytes = DECODE_B * DECODE_BYTES_PER_SEQSTEP
+    dec_gbs = dec_bytes / (dec_ms / DECODE_CALLS * 1e-3) / 1e9
+    cpu = cpu_baseline() if world == 1 or rank == 0 else None
+    line = {
+        "metric": METRIC,
+        "value": round(world * PREFILL_T / (pre_ms * 1e-3), 1),
+        "unit": "tokens/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "prefill 1 x 32768 tokens + 16 decode steps x 256 sequences",
+                   "h_k": H_K, "h_v": H_V, "d_k": D, "d_v": D, "conv_w": 4, "chunk": 64,
+                   "prefill_tokens": PREFILL_T, "decode_batch": DECODE_B,
+                   "decode_calls_per_step": DECODE_CALLS,
+                   "arith": "bf16 tensor-core operands (fp16 for the q/k Gram), fp32 accumulation and state",
+                   "l2": "no flush: prefill inputs 0.77 GB and decode state 0.54 GB exceed the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": hbm, "unit": "GB/s",
+                     "frac": round(pre_gbs / hbm, 4), "traffic": _traffic("prefill", "gdn_prefill.cu"),
+                     "kernel": "gdn_prefill (prefill_kernel + conv_state_kernel)",
+                     "algorithmic_bytes_per_launch": pre_bytes,
+                     "peak_source": f"{peak_src} hbm_gbs",
+                     "tensor": {"achieved": round(pre_tflops, 2), "peak": tc_peak, "unit": "TFLOP/s",
+                                "frac": round(pre_tflops / tc_peak, 4),
+                                "flop_per_token": FLOP_PER_TOKEN,
+                                "peak_source": f"{peak_src} bf16_tflops (burst)"}},
+        "decode": {"value": round(world * DECODE_B * DECODE_CALLS / (dec_ms * 1e-3), 1),
+                   "unit": "seq-steps/s", "ms_per_call": round(dec_ms / DECODE_CALLS, 4),
+                   "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm,
+                                "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
+                                "traffic": _traffic("decode", "gdn_decode.cu"),
+                                "algorithmic_bytes_per_launch": dec_bytes},
+                   "e2e": {"value": round(world * DECODE_B * DECODE_CALLS / (e2e_dec_ms * 1e-3), 1),
+                           "unit": "seq-steps/s", "h2d_bytes_per_step": h2d_dec,
+                           "d2h_bytes_per_step": d2h_dec}},
+        "e2e": {"value": round(world * PREFILL_T / (e2e_pre_ms * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre},
+        "gpu_launches": K * (2 + DECODE_CALLS),
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+# ---- reference arm: the oracle on the host cores ---------------------------------
+
+def run_reference(args) -> dict | None:
+    rank, world, _ = _dist()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    sample = 2048
+    for _ in range(args.warmup):
+        oracle_prefill_sample(256, threads)
+    times = []
+    for _ in range(args.steps):
+        _, dt = oracle_prefill_sample(sample, threads)
+        times.append(dt)
+    mean = sum(times) / len(times)
+    value = sample / mean
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(mean * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "prefill 1 x 32768 tokens + 16 decode steps x 256 sequences",
+                   "h_k": H_K, "h_v": H_V, "d_k": D, "d_v": D, "conv_w": 4, "chunk": 64},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: the first {sample} tokens of the 32768-token "
+                                   "prefill sequence, all 32 value heads, fp64 sequential recurrence"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

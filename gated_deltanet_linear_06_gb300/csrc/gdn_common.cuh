@@ -1,6 +1,7 @@
 // gdn_common.cuh -- small device helpers shared by the libgdn kernels.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,6 +23,11 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return static_cast<uint32_t>(f32_to_bf16(lo)) |
          (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
+         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }

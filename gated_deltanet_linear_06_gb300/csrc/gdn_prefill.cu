@@ -19,6 +19,13 @@
 // then the gated RMSNorm epilogue writes bf16 out.  Every exponential is of a
 // non-positive difference, so a chunk whose decay underflows fp32 stays finite.
 //
+// The Gram product takes its operands in fp16, all others in bf16.  q^ and k^
+// are unit-bounded, so fp16 cannot overflow there, and its 3 extra mantissa
+// bits matter: when q^_t . k^_t nearly cancels, a token's output is small and
+// the RMSNorm magnifies the rounding of these dot products (bf16 Gram operands
+// alone put the 4096-token output error at ~9e-3 of its maximum; fp16 halves
+// it).
+//
 // Operands are bf16 tiles in shared memory with the 128-byte swizzle; the
 // accumulators are fp32 in tensor memory (512 columns: Gram 64, W 64, U/Vn
 // 64, O1 64, O2 64, S 128).  The K^ tile serves both as a K-major operand
@@ -50,6 +57,8 @@ constexpr uint32_t OFF_VNS = 114688;  // Vn^T diag(e^{gamma_C - gamma}) [d_v][t]
 constexpr uint32_t OFF_TB = 131072;   // T diag(beta) [t][s]
 constexpr uint32_t OFF_TW = 139264;   // T diag(beta e^gamma) [t][s]
 constexpr uint32_t OFF_P = 147456;    // P [t][s]
+constexpr uint32_t OFF_KQ16 = OFF_VN; // fp16 copy of the KQ tile for the Gram MMA; aliases Vn^T
+                                      // and its scaled copy, which are dead while it is live
 constexpr uint32_t OFF_F32 = 155648;  // fp32: A [64][65] + T [64][65], or O staging [64][129]
 constexpr int LDA = 65, LDO = 129;
 constexpr uint32_t F32_BYTES = 2 * 64 * LDA * 4;
@@ -67,6 +76,7 @@ constexpr uint64_t D_K = tc::sdesc_sw128(16, 1024);         // K-major tiles
 constexpr uint64_t D_MN_KQ = tc::sdesc_sw128(16384, 1024);  // K^ read MN-major
 constexpr uint64_t D_MN_V = tc::sdesc_sw128(8192, 1024);    // V read MN-major
 constexpr uint32_t ID_KK = tc::idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t ID_GRAM = tc::idesc_f16(128, 64, 0, 0);
 constexpr uint32_t ID_MN_A = tc::idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_MN_B = tc::idesc_bf16(128, 128, 0, 1);
 
@@ -83,6 +93,14 @@ __device__ __forceinline__ void store_bf16x4(uint8_t* tile, uint32_t off, float 
   uint2 v;
   v.x = pack_bf16x2(a, b);
   v.y = pack_bf16x2(c, d);
+  *reinterpret_cast<uint2*>(tile + off) = v;
+}
+
+__device__ __forceinline__ void store_f16x4(uint8_t* tile, uint32_t off, float a, float b, float c,
+                                            float d) {
+  uint2 v;
+  v.x = pack_f16x2(a, b);
+  v.y = pack_f16x2(c, d);
   *reinterpret_cast<uint2*>(tile + off) = v;
 }
 
@@ -299,6 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
       store_bf16x4(sm.base + OFF_KQ, tc::sw128_off(t, 4 * lane, 16384), y[1][0], y[1][1], y[1][2], y[1][3]);
       store_bf16x4(sm.base + OFF_KQ + 8192, tc::sw128_off(t, 4 * lane, 16384), y[0][0], y[0][1], y[0][2], y[0][3]);
       store_bf16x4(sm.base + OFF_V, tc::sw128_off(t, 4 * lane, 8192), y[2][0], y[2][1], y[2][2], y[2][3]);
+      store_f16x4(sm.base + OFF_KQ16, tc::sw128_off(t, 4 * lane, 16384), y[1][0], y[1][1], y[1][2], y[1][3]);
+      store_f16x4(sm.base + OFF_KQ16 + 8192, tc::sw128_off(t, 4 * lane, 16384), y[0][0], y[0][1], y[0][2], y[0][3]);
     }
     sync_for_mma();
 
@@ -307,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-        const uint32_t a = sm.addr + OFF_KQ + kb * 16384 + ks;
-        tc::mma_bf16(tmem + TM_G, tc::sdesc_at(D_K, a), tc::sdesc_at(D_K, a), ID_KK, k > 0);
+        const uint32_t a = sm.addr + OFF_KQ16 + kb * 16384 + ks;
+        tc::mma_bf16(tmem + TM_G, tc::sdesc_at(D_K, a), tc::sdesc_at(D_K, a), ID_GRAM, k > 0);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {

@@ -1,0 +1,83 @@
+"""A small, self-contained case of one kernel, for profilers.
+
+  python -m gated_deltanet_linear_06_gb300.profile_case --kernel prefill --tokens 8192
+  python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode --batch 128
+
+Builds seeded synthetic inputs (the same distributions as the benchmark),
+runs the kernel ``--warmup`` times, then ``--iters`` times, and prints the
+mean device time per call (CUDA events).  Sized by default so the inputs
+exceed the 129 MB L2 while the whole case holds well under 1 GB of device
+memory, which keeps an ncu capture short.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main():
+    import torch
+
+    import gated_deltanet_linear_06_gb300 as gdn
+    import gdn_inputs as gi
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--kernel", choices=["prefill", "decode"], required=True)
+    ap.add_argument("--tokens", type=int, default=8192, help="prefill: tokens of one sequence")
+    ap.add_argument("--seqs", type=int, default=1, help="prefill: equal-length sequences")
+    ap.add_argument("--batch", type=int, default=128, help="decode: sequences")
+    ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+
+    dev = torch.device("cuda:0")
+    sh = gi.LAYER
+    dims = gdn.make_dims(h_k=sh.h_k, h_v=sh.h_v)
+    stream = torch.cuda.current_stream(dev)
+    if args.kernel == "prefill":
+        N, T = args.seqs, args.seqs * args.tokens
+        p = {k: v.to(dev) for k, v in gi.make_params(sh, 3).items()}
+        x = {k: v.to(dev) for k, v in gi.make_tokens(sh, T, 3).items()}
+        cu = gi.cu_seqlens([args.tokens] * N).to(dev)
+        conv = torch.zeros(N, 3, sh.cc, device=dev)
+        ssm = torch.zeros(N, sh.h_v, 128, 128, device=dev)
+        out = torch.empty(T, sh.h_v, 128, dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(gdn.gdn_workspace_bytes(dims, N, T), dtype=torch.uint8, device=dev)
+
+        def call():
+            gdn.gdn_prefill(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
+                            p["conv_w"], p["norm_w"], cu, conv, ssm, out, ws, stream=stream)
+        unit, per_call = "tokens", T
+    else:
+        B = args.batch
+        p = {k: v.to(dev) for k, v in gi.make_params(sh, 4).items()}
+        st = gi.make_states(sh, B, 4, ssm_std=0.1 ** 0.5, conv_std=1.0)
+        conv, ssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
+        x = {k: v.to(dev) for k, v in gi.make_tokens(sh, B, 4).items()}
+        out = torch.empty(B, sh.h_v, 128, dtype=torch.bfloat16, device=dev)
+
+        def call():
+            gdn.gdn_decode_step(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
+                                p["conv_w"], p["norm_w"], None, B, conv, ssm, out, stream=stream)
+        unit, per_call = "seq-steps", B
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.iters):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / args.iters
+    print(f"{args.kernel}: {ms:.4f} ms per call, {per_call / (ms * 1e-3):.4g} {unit}/s")
+
+
+if __name__ == "__main__":
+    main()
