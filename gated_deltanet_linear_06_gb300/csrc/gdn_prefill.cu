@@ -36,6 +36,9 @@
 // The conv state is rewritten by a second, small kernel after this one, so no
 // CTA overwrites conv-state rows that another CTA of the same sequence still
 // reads.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
@@ -51,21 +54,36 @@ constexpr int C = kChunk;
 constexpr uint32_t OFF_KQ = 0;        // [kb0: K^ | Q^][kb1: K^ | Q^], 8 KB each (64 rows x 128 B)
 constexpr uint32_t OFF_V = 32768;     // V [t][d_v], 64-column blocks 8 KB apart
 constexpr uint32_t OFF_S = 49152;     // S bf16 [d_v][d_k], K blocks 16 KB apart
-constexpr uint32_t OFF_WN = 81920;    // -W [t][d_k], K blocks 8 KB apart
-constexpr uint32_t OFF_VN = 98304;    // Vn^T [d_v][t]
-constexpr uint32_t OFF_VNS = 114688;  // Vn^T diag(e^{gamma_C - gamma}) [d_v][t]
+constexpr uint32_t OFF_VN = 81920;    // Vn^T [d_v][t]
+constexpr uint32_t OFF_VNS = 98304;   // Vn^T diag(e^{gamma_C - gamma}) [d_v][t]
+constexpr uint32_t OFF_KQ16 = OFF_VN; // fp16 copy of the KQ tile for the Gram MMA; aliases Vn^T
+                                      // and its scaled copy, which are dead while it is live
+constexpr uint32_t OFF_WN = 114688;   // -W [t][d_k], K blocks 8 KB apart
 constexpr uint32_t OFF_TB = 131072;   // T diag(beta) [t][s]
 constexpr uint32_t OFF_TW = 139264;   // T diag(beta e^gamma) [t][s]
 constexpr uint32_t OFF_P = 147456;    // P [t][s]
-constexpr uint32_t OFF_KQ16 = OFF_VN; // fp16 copy of the KQ tile for the Gram MMA; aliases Vn^T
-                                      // and its scaled copy, which are dead while it is live
-constexpr uint32_t OFF_F32 = 155648;  // fp32: A [64][65] + T [64][65], or O staging [64][129]
-constexpr int LDA = 65, LDO = 129;
+constexpr uint32_t OFF_F32 = 155648;  // fp32: A [64][65] + T [64][65]
+constexpr int LDA = 65, LDO = 128;
 constexpr uint32_t F32_BYTES = 2 * 64 * LDA * 4;
 constexpr uint32_t OFF_CW = OFF_F32 + F32_BYTES;  // conv weights fp32 [3][128][4]
 constexpr uint32_t OFF_NW = OFF_CW + 3 * 128 * 4 * 4;
 constexpr uint32_t OFF_GATE = OFF_NW + 128 * 4;   // gam, beta, e^gam, e^{gamC-gam}: 4 x 64 fp32
 constexpr uint32_t SMEM_USED = OFF_GATE + 4 * 64 * 4;
+// Staging of a chunk's raw inputs, loaded by TMA (2-D tensor maps over qkv and z):
+// the raw q, k and v rows of tokens t0-3 .. t0+63 (bf16, one [67][128] box per
+// block) land over -W, T, P and the fp32 area, which are dead from the last MMA of
+// the previous chunk to the end of this chunk's conv stage; z ([64][128]) lands in
+// the fp32 area's tail between the state-correction MMA and the epilogue.
+constexpr uint32_t RAW_BOX_ROWS = C + kConvW - 1;     // a chunk and its 3-token halo
+constexpr uint32_t RAW_BLK = RAW_BOX_ROWS * 256;       // one channel block: [67 rows][128 bf16]
+constexpr uint32_t OFF_RAW = OFF_WN;                   // [q | k | v blocks]
+constexpr uint32_t RAW_END = OFF_RAW + 3 * RAW_BLK;
+constexpr uint32_t OFF_OST = OFF_VN;  // O staging fp32 [64][128], after the Vn tiles are consumed
+constexpr uint32_t OFF_Z = RAW_END;   // z bf16 [64][128], in the fp32 area's tail
+static_assert(RAW_END <= OFF_F32 + F32_BYTES, "raw staging past the fp32 area");
+static_assert(OFF_RAW % 128 == 0 && RAW_BLK % 128 == 0 && RAW_END % 128 == 0, "TMA destinations need 128-B alignment");
+static_assert(OFF_Z + 64 * 128 * 2 <= OFF_CW, "z staging overlaps the conv weights");
+static_assert(OFF_OST + 64 * LDO * 4 <= OFF_WN, "O staging overlaps -W");
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024
 
 // ---- tensor memory columns ----
@@ -113,6 +131,51 @@ __device__ __forceinline__ void store_bf16x8(uint8_t* tile, uint32_t off, const 
   *reinterpret_cast<uint4*>(tile + off) = v;
 }
 
+// Four SiLUs with one reciprocal: with d_i = 1 + e^{-x_i}, 1/d_1 =
+// d_2 d_3 d_4 / (d_1 d_2 d_3 d_4), and so on.  Inputs are clamped at -20 so the
+// product stays below 2^126 (|silu(x)| < 4.2e-8 for x < -20, which the clamp
+// replaces by silu(-20)); this takes the special-function unit from two
+// operations per SiLU to 1.25.
+__device__ __forceinline__ void silu4(float (&x)[4]) {
+  float d[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = 1.0f + __expf(-fmaxf(x[i], -20.0f));
+  const float d01 = d[0] * d[1], d23 = d[2] * d[3];
+  const float r = __fdividef(1.0f, d01 * d23);   // approximate reciprocal (product < 2^126)
+  const float r01 = r * d23, r23 = r * d01;   // 1/(d0 d1), 1/(d2 d3)
+  x[0] *= r01 * d[1];
+  x[1] *= r01 * d[0];
+  x[2] *= r23 * d[3];
+  x[3] *= r23 * d[2];
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(mbar)), "r"(bytes)
+               : "memory");
+}
+
+// One 2-D TMA tile load: the box at column x, row y of the tensor map lands at
+// smem_dst and reports its bytes to mbar.  Rows outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* tm, int x, int y, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(tc::smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(tc::smem_u32(mbar))
+      : "memory");
+}
+
+// One thread: the raw q, k and v rows of tokens t0-3 .. t0+63 of a sequence
+// starting at packed row `start` (rows before the sequence are fetched too and
+// ignored: the conv reads the carried conv state for them).
+__device__ __forceinline__ void stage_raw(const CUtensorMap* tm_qkv, uint8_t* raw, uint64_t* mbar, int start,
+                                          int t0, int kh, int h, int Cq) {
+  mbar_expect_tx(mbar, 3 * RAW_BLK);
+  const int y = start + t0 - (kConvW - 1);
+  tma_load_2d(raw, tm_qkv, kh * kD, y, mbar);
+  tma_load_2d(raw + RAW_BLK, tm_qkv, Cq + kh * kD, y, mbar);
+  tma_load_2d(raw + 2 * RAW_BLK, tm_qkv, 2 * Cq + h * kD, y, mbar);
+}
+
 // Every thread calls this; all agree on the verdict.
 __device__ bool cu_seqlens_valid(const PrefillArgs& p) {
   int bad = 0;
@@ -135,9 +198,13 @@ __device__ __forceinline__ void sync_for_mma() {
   tc::fence_after_sync();
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv,
+                   const __grid_constant__ CUtensorMap tm_z) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t mbar;
+  __shared__ __align__(8) uint64_t mbar;      // MMA completion
+  __shared__ __align__(8) uint64_t mbar_raw;  // raw q|k|v rows of a chunk landed
+  __shared__ __align__(8) uint64_t mbar_z;    // z of a chunk landed
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -159,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
     sm.base = smem_raw + pad;
     sm.addr = raw + pad;
   }
-  float* cw = sm.f32(OFF_CW);      // [blk][i][4]
+  float* cw = sm.f32(OFF_CW);      // [blk][tap][i]
   float* nw = sm.f32(OFF_NW);
   float* gam = sm.f32(OFF_GATE);
   float* bet = gam + 64;
@@ -167,18 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
   float* egc = gam + 192;
   float* Af = sm.f32(OFF_F32);
   float* Tf = Af + 64 * LDA;
-  float* Ost = Af;                  // aliases A and T (used at different times)
+  float* Ost = sm.f32(OFF_OST);     // aliases the Vn tiles (used after them)
 
-  if (tid == 0) tc::mbar_init(&mbar, 1);
+  if (tid == 0) {
+    tc::mbar_init(&mbar, 1);
+    tc::mbar_init(&mbar_raw, 1);
+    tc::mbar_init(&mbar_z, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   if (warp == 0) tc::tmem_alloc(&tmem_base_s, TM_COLS);
-  for (int e = tid; e < 3 * kD; e += kThreads) {
+  for (int e = tid; e < 3 * kD; e += kThreads) {   // tap-major: cw[blk][tap][channel]
     const int blk = e / kD, i = e % kD;
     const int ch = blk == 0 ? kh * kD + i : blk == 1 ? Cq + kh * kD + i : 2 * Cq + h * kD + i;
     const uint2 w = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)ch * kConvW);
-    cw[e * 4 + 0] = bf16_to_f32(w.x & 0xffffu);
-    cw[e * 4 + 1] = bf16_to_f32(w.x >> 16);
-    cw[e * 4 + 2] = bf16_to_f32(w.y & 0xffffu);
-    cw[e * 4 + 3] = bf16_to_f32(w.y >> 16);
+    cw[(blk * 4 + 0) * kD + i] = bf16_to_f32(w.x & 0xffffu);
+    cw[(blk * 4 + 1) * kD + i] = bf16_to_f32(w.x >> 16);
+    cw[(blk * 4 + 2) * kD + i] = bf16_to_f32(w.y & 0xffffu);
+    cw[(blk * 4 + 3) * kD + i] = bf16_to_f32(w.y >> 16);
   }
   if (tid < kD) nw[tid] = p.norm_w[tid];
   tc::fence_before_sync();
@@ -208,6 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
     }
   }
 
+  float4 cwr[3][kConvW];   // this lane's 4 channels of each block, per tap
+#pragma unroll
+  for (int blk = 0; blk < 3; ++blk)
+#pragma unroll
+    for (int j = 0; j < kConvW; ++j) cwr[blk][j] = reinterpret_cast<const float4*>(cw + (blk * 4 + j) * kD)[lane];
   const float A_exp = __expf(p.A_log[h]);
   const float dtb = p.dt_bias[h];
   const float qscale = rsqrtf((float)kD);
@@ -222,7 +299,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
     return all_ok;
   };
 
-  for (int t0 = 0; t0 < len && !aborted; t0 += C) {
+  if (tid == 32) stage_raw(&tm_qkv, sm.base + OFF_RAW, &mbar_raw, start, 0, kh, h, Cq);
+  // gate inputs of the next chunk, prefetched into warp 0's registers
+  float a_nx[2] = {0.0f, 0.0f}, b_nx[2] = {0.0f, 0.0f};
+  if (warp == 0) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int t = lane + 32 * u;
+      if (t < len) {
+        const size_t pidx = (size_t)(start + t) * p.h_v + h;
+        a_nx[u] = bf16_to_f32(p.a[pidx]);
+        b_nx[u] = bf16_to_f32(p.b[pidx]);
+      }
+    }
+  }
+  uint32_t chunk_parity = 0;
+  // bulk copies in flight (uniform across the CTA), waited for on the time-out path
+  bool raw_pending = true, z_pending = false;
+  for (int t0 = 0; t0 < len && !aborted; t0 += C, chunk_parity ^= 1u) {
     const int L = min(C, len - t0);
 
     // ---- gates and their cumulative sums (warp 0) ----
@@ -231,12 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int t = lane + 32 * u;
-        g2[u] = 0.0f;
-        b2[u] = 0.0f;
-        if (t < L) {
-          const size_t pidx = (size_t)(start + t0 + t) * p.h_v + h;
-          g2[u] = -A_exp * softplus(bf16_to_f32(p.a[pidx]) + dtb);
-          b2[u] = sigmoid(bf16_to_f32(p.b[pidx]));
+        g2[u] = t < L ? -A_exp * softplus(a_nx[u] + dtb) : 0.0f;
+        b2[u] = t < L ? sigmoid(b_nx[u]) : 0.0f;
+      }
+      // prefetch the next chunk's gate inputs
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int t = t0 + C + lane + 32 * u;
+        if (t < len) {
+          const size_t pidx = (size_t)(start + t) * p.h_v + h;
+          a_nx[u] = bf16_to_f32(p.a[pidx]);
+          b_nx[u] = bf16_to_f32(p.b[pidx]);
         }
       }
 #pragma unroll
@@ -259,66 +358,83 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
       }
     }
 
-    // ---- conv + SiLU + L2 norms -> K^, Q^, V tiles (all warps) ----
-    for (int t = warp; t < C; t += kThreads / 32) {
-      float y[3][4];
-      if (t < L) {
+    if (!__syncthreads_and(tc::mbar_wait(&mbar_raw, chunk_parity, kWaitBudget))) { aborted = true; break; }
+    raw_pending = false;
+
+    // ---- conv + SiLU + L2 norms -> K^, Q^, V tiles (all warps, a token per warp step,
+    //      two tokens in flight per warp) ----
+#pragma unroll 1
+    for (int tb = warp; tb < C; tb += 2 * (kThreads / 32)) {
+      float y[2][3][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int t = tb + u * (kThreads / 32);
 #pragma unroll
         for (int blk = 0; blk < 3; ++blk)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) y[blk][e] = 0.0f;
+          for (int e = 0; e < 4; ++e) y[u][blk][e] = 0.0f;
+        if (t >= L) continue;
 #pragma unroll
         for (int j = 0; j < kConvW; ++j) {
           const int tau = t0 + t - (kConvW - 1) + j;   // position in the sequence
 #pragma unroll
           for (int blk = 0; blk < 3; ++blk) {
-            const int ch = (blk == 0 ? kh * kD : blk == 1 ? Cq + kh * kD : 2 * Cq + h * kD) + 4 * lane;
             float x[4];
             if (tau >= 0) {
-              const uint2 r = *reinterpret_cast<const uint2*>(p.qkv + (size_t)(start + tau) * Cc + ch);
+              const uint2 r = *reinterpret_cast<const uint2*>(sm.base + OFF_RAW + blk * RAW_BLK +
+                                                              (t + j) * 256 + lane * 8);
               x[0] = bf16_to_f32(r.x & 0xffffu); x[1] = bf16_to_f32(r.x >> 16);
               x[2] = bf16_to_f32(r.y & 0xffffu); x[3] = bf16_to_f32(r.y >> 16);
             } else {
+              const int ch = (blk == 0 ? kh * kD : blk == 1 ? Cq + kh * kD : 2 * Cq + h * kD) + 4 * lane;
               const float4 r = *reinterpret_cast<const float4*>(
                   p.conv_state + ((size_t)n * (kConvW - 1) + (kConvW - 1 + tau)) * Cc + ch);
               x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
             }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float w = cw[(blk * kD + 4 * lane + e) * 4 + j];
-              y[blk][e] = j == 0 ? w * x[e] : fmaf(w, x[e], y[blk][e]);
-            }
+            const float4 w4 = cwr[blk][j];
+            y[u][blk][0] = fmaf(w4.x, x[0], y[u][blk][0]);
+            y[u][blk][1] = fmaf(w4.y, x[1], y[u][blk][1]);
+            y[u][blk][2] = fmaf(w4.z, x[2], y[u][blk][2]);
+            y[u][blk][3] = fmaf(w4.w, x[3], y[u][blk][3]);
           }
         }
 #pragma unroll
-        for (int blk = 0; blk < 3; ++blk)
+        for (int blk = 0; blk < 3; ++blk) silu4(y[u][blk]);
+      }
+      float ss[2][2];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) y[blk][e] = silu(y[blk][e]);
-        float sq = y[0][0] * y[0][0], sk = y[1][0] * y[1][0];
+      for (int u = 0; u < 2; ++u) {
+        ss[u][0] = y[u][0][0] * y[u][0][0];
+        ss[u][1] = y[u][1][0] * y[u][1][0];
 #pragma unroll
         for (int e = 1; e < 4; ++e) {
-          sq = fmaf(y[0][e], y[0][e], sq);
-          sk = fmaf(y[1][e], y[1][e], sk);
+          ss[u][0] = fmaf(y[u][0][e], y[u][0][e], ss[u][0]);
+          ss[u][1] = fmaf(y[u][1][e], y[u][1][e], ss[u][1]);
         }
-        sq = warp_sum(sq);
-        sk = warp_sum(sk);
-        const float rq = rsqrtf(sq + p.l2_eps) * qscale, rk = rsqrtf(sk + p.l2_eps);
+      }
+#pragma unroll
+      for (int m = 16; m >= 1; m >>= 1)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          ss[u][0] += __shfl_xor_sync(0xffffffffu, ss[u][0], m);
+          ss[u][1] += __shfl_xor_sync(0xffffffffu, ss[u][1], m);
+        }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int t = tb + u * (kThreads / 32);
+        const float rq = rsqrtf(ss[u][0] + p.l2_eps) * qscale, rk = rsqrtf(ss[u][1] + p.l2_eps);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          y[0][e] *= rq;
-          y[1][e] *= rk;
+          y[u][0][e] *= rq;
+          y[u][1][e] *= rk;
         }
-      } else {
-#pragma unroll
-        for (int blk = 0; blk < 3; ++blk)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) y[blk][e] = 0.0f;
+        const uint32_t o16 = tc::sw128_off(t, 4 * lane, 16384), o8 = tc::sw128_off(t, 4 * lane, 8192);
+        store_bf16x4(sm.base + OFF_KQ, o16, y[u][1][0], y[u][1][1], y[u][1][2], y[u][1][3]);
+        store_bf16x4(sm.base + OFF_KQ + 8192, o16, y[u][0][0], y[u][0][1], y[u][0][2], y[u][0][3]);
+        store_bf16x4(sm.base + OFF_V, o8, y[u][2][0], y[u][2][1], y[u][2][2], y[u][2][3]);
+        store_f16x4(sm.base + OFF_KQ16, o16, y[u][1][0], y[u][1][1], y[u][1][2], y[u][1][3]);
+        store_f16x4(sm.base + OFF_KQ16 + 8192, o16, y[u][0][0], y[u][0][1], y[u][0][2], y[u][0][3]);
       }
-      store_bf16x4(sm.base + OFF_KQ, tc::sw128_off(t, 4 * lane, 16384), y[1][0], y[1][1], y[1][2], y[1][3]);
-      store_bf16x4(sm.base + OFF_KQ + 8192, tc::sw128_off(t, 4 * lane, 16384), y[0][0], y[0][1], y[0][2], y[0][3]);
-      store_bf16x4(sm.base + OFF_V, tc::sw128_off(t, 4 * lane, 8192), y[2][0], y[2][1], y[2][2], y[2][3]);
-      store_f16x4(sm.base + OFF_KQ16, tc::sw128_off(t, 4 * lane, 16384), y[1][0], y[1][1], y[1][2], y[1][3]);
-      store_f16x4(sm.base + OFF_KQ16 + 8192, tc::sw128_off(t, 4 * lane, 16384), y[0][0], y[0][1], y[0][2], y[0][3]);
     }
     sync_for_mma();
 
@@ -353,31 +469,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
     }
     if (!wait_mma()) { aborted = true; break; }
 
-    // ---- A (fp32, warps 0-1) and P (bf16 tile, warps 2-3) from the Gram rows ----
-    if (warp < 4) {
+    // ---- A (fp32, lanes 0-63) and P (bf16 tile, lanes 64-127) from the Gram rows;
+    //      warps w and w+4 share a lane quarter and split its 64 columns ----
+    {
       float v[32];
       const int t = row & 63;
       const float gt = gam[t];
+      const int c0 = half * 32;
+      tc::tmem_ld32(tmem + lane_base + TM_G + c0, v);
+      if ((warp & 3) < 2) {
+        const float bt = bet[t];
 #pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
-        tc::tmem_ld32(tmem + lane_base + TM_G + c32 * 32, v);
-        if (warp < 2) {
-          const float bt = bet[t];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int s = c32 * 32 + i;
-            Af[t * LDA + s] = s < t ? bt * __expf(gt - gam[s]) * v[i] : 0.0f;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int s = c32 * 32 + i;
-            v[i] = s <= t ? v[i] * __expf(gt - gam[s]) : 0.0f;
-          }
-#pragma unroll
-          for (int m = 0; m < 4; ++m)
-            store_bf16x8(sm.base + OFF_P, tc::sw128_off(t, c32 * 32 + 8 * m, 0), v + 8 * m);
+        for (int i = 0; i < 32; ++i) {
+          const int s = c0 + i;
+          Af[t * LDA + s] = s < t ? bt * __expf(gt - gam[s]) * v[i] : 0.0f;
         }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int s = c0 + i;
+          v[i] = s <= t ? v[i] * __expf(gt - gam[s]) : 0.0f;
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          store_bf16x8(sm.base + OFF_P, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
       }
     }
     __syncthreads();
@@ -493,6 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
     }
     if (!wait_mma()) { aborted = true; break; }
 
+    // ---- z of the chunk -> smem (bulk copies; read by the epilogue) ----
+    if (tid == 32) {
+      mbar_expect_tx(&mbar_z, 64 * 256);
+      tma_load_2d(sm.base + OFF_Z, &tm_z, h * kD, start + t0, &mbar_z);
+    }
+    z_pending = true;
+
     // ---- Vn^T tiles (plain and decay-weighted), row = d_v index ----
     {
       float v[32], vs[32];
@@ -523,6 +645,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
       tc::mma_commit(&mbar);
     }
     if (!wait_mma()) { aborted = true; break; }
+    // the next chunk's raw rows land while this chunk finishes
+    if (tid == 32 && t0 + C < len) stage_raw(&tm_qkv, sm.base + OFF_RAW, &mbar_raw, start, t0 + C, kh, h, Cq);
+    raw_pending = t0 + C < len;
 
     // ---- new S -> bf16 operand tile; O = e^gamma O1 + O2 -> fp32 staging ----
     {
@@ -543,32 +668,36 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(PrefillArgs p) {
         Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
       }
     }
-    __syncthreads();
+    if (!__syncthreads_and(tc::mbar_wait(&mbar_z, chunk_parity, kWaitBudget))) { aborted = true; break; }
+    z_pending = false;
 
-    // ---- gated RMSNorm epilogue: warp per token ----
+    // ---- gated RMSNorm epilogue: warp per token, 4 channels per lane ----
     for (int t = warp; t < L; t += kThreads / 32) {
-      float o[4];
-      float ss = 0.0f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        o[e] = Ost[t * LDO + lane + 32 * e];
-        ss = fmaf(o[e], o[e], ss);
-      }
+      const float4 o4 = reinterpret_cast<const float4*>(Ost + t * LDO)[lane];
+      float ss = o4.x * o4.x;
+      ss = fmaf(o4.y, o4.y, ss);
+      ss = fmaf(o4.z, o4.z, ss);
+      ss = fmaf(o4.w, o4.w, ss);
       ss = warp_sum(ss);
       const float rstd = rsqrtf(ss * (1.0f / kD) + p.rms_eps);
-      const size_t obase = ((size_t)(start + t0 + t) * p.h_v + h) * kD;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = lane + 32 * e;
-        const float zz = bf16_to_f32(p.z[obase + i]);
-        p.out[obase + i] = f32_to_bf16(o[e] * rstd * nw[i] * silu(zz));
-      }
+      const uint2 zr = *reinterpret_cast<const uint2*>(sm.base + OFF_Z + t * 256 + lane * 8);
+      const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
+      float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
+                    bf16_to_f32(zr.y >> 16)};
+      silu4(g);
+      uint2 o;
+      o.x = pack_bf16x2(o4.x * rstd * w4.x * g[0], o4.y * rstd * w4.y * g[1]);
+      o.y = pack_bf16x2(o4.z * rstd * w4.z * g[2], o4.w * rstd * w4.w * g[3]);
+      *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0 + t) * p.h_v + h) * kD + 4 * lane) = o;
     }
     __syncthreads();
   }
 
   if (aborted) {
     if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+    // let this CTA's own bulk copies finish (bounded) before its smem goes away
+    if (raw_pending) tc::mbar_wait(&mbar_raw, chunk_parity, kWaitBudget);
+    if (z_pending) tc::mbar_wait(&mbar_z, chunk_parity, kWaitBudget);
   } else {
     // final state back to global memory
     float4* dst = reinterpret_cast<float4*>(S_glob + (size_t)row * kD + half * 64);
@@ -608,11 +737,47 @@ __global__ void __launch_bounds__(256) conv_state_kernel(PrefillArgs p) {
 
 size_t prefill_scratch_bytes(int, int, int, long long) { return 0; }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows][cols] array, box [box_rows][box_cols].
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                 uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  prefill_kernel<<<(unsigned)(p.n_seqs * p.h_v), kThreads, SMEM_BYTES, stream>>>(p);
+  const int Cc_ = 2 * p.h_k * kD + p.h_v * kD;
+  CUtensorMap tm_qkv, tm_z;
+  if (!make_map_2d(&tm_qkv, p.qkv, (uint64_t)Cc_, (uint64_t)p.total_tokens, kD, RAW_BOX_ROWS) ||
+      !make_map_2d(&tm_z, p.z, (uint64_t)p.h_v * kD, (uint64_t)p.total_tokens, kD, C))
+    return cudaErrorInvalidValue;
+  prefill_kernel<<<(unsigned)(p.n_seqs * p.h_v), kThreads, SMEM_BYTES, stream>>>(p, tm_qkv, tm_z);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int Cc = 2 * p.h_k * kD + p.h_v * kD;
