@@ -41,6 +41,11 @@ struct PrefillArgs {
   int32_t* status;         // device word (workspace offset 0)
   void* scratch;           // workspace beyond the status word
   size_t scratch_bytes;
+  // set by the launcher, inside the scratch area:
+  int seg_tokens;          // segment length (sequences up to this long are one segment)
+  int* seg_list;           // [count, pad x3][units][8]: the segments of every sequence
+  int* multi_list;         // [count, pad x3][slots][4]: sequences longer than one segment
+  float* xfer;             // per boundary slot and value head: transfer map, end state, initial state
   int n_seqs, h_k, h_v;
   long long total_tokens;
   float l2_eps, rms_eps;

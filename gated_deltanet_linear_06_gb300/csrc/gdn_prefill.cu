@@ -49,26 +49,44 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int C = kChunk;
+constexpr int kSegTokens = 1024;   // segment length when long sequences are split (see launch_prefill)
 
-// ---- shared memory map (bytes from a 1024-aligned base) ----
-constexpr uint32_t OFF_KQ = 0;        // [kb0: K^ | Q^][kb1: K^ | Q^], 8 KB each (64 rows x 128 B)
-constexpr uint32_t OFF_V = 32768;     // V [t][d_v], 64-column blocks 8 KB apart
-constexpr uint32_t OFF_S = 49152;     // S bf16 [d_v][d_k], K blocks 16 KB apart
-constexpr uint32_t OFF_VN = 81920;    // Vn^T [d_v][t]
-constexpr uint32_t OFF_VNS = 98304;   // Vn^T diag(e^{gamma_C - gamma}) [d_v][t]
-constexpr uint32_t OFF_KQ16 = OFF_VN; // fp16 copy of the KQ tile for the Gram MMA; aliases Vn^T
-                                      // and its scaled copy, which are dead while it is live
-constexpr uint32_t OFF_WN = 114688;   // -W [t][d_k], K blocks 8 KB apart
-constexpr uint32_t OFF_TB = 131072;   // T diag(beta) [t][s]
-constexpr uint32_t OFF_TW = 139264;   // T diag(beta e^gamma) [t][s]
-constexpr uint32_t OFF_P = 147456;    // P [t][s]
-constexpr uint32_t OFF_F32 = 155648;  // fp32: A [64][65] + T [64][65]
+// ---- shared memory maps (bytes from a 1024-aligned base), per pass ----
+// Output pass: the layer over a token range, from a given state.
+// Transfer pass: the same chunk algebra run twice side by side with no
+// output -- S from 0 with the real inputs and X from the identity with v = 0 --
+// which yields the range's affine state map S_end = S_start X_end + S_end(0).
+template <bool kXfer> struct Lay;
+template <> struct Lay<false> {
+  static constexpr uint32_t KQ = 0;        // [kb0: K^ | Q^][kb1: K^ | Q^], 8 KB each (64 rows x 128 B)
+  static constexpr uint32_t V = 32768;     // V [t][d_v], 64-column blocks 8 KB apart
+  static constexpr uint32_t S = 49152;     // S bf16 [d_v][d_k], K blocks 16 KB apart
+  static constexpr uint32_t X = 0;         // (unused)
+  static constexpr uint32_t VN = 81920;    // Vn^T [d_v][t]
+  static constexpr uint32_t VNS = 98304;   // Vn^T diag(e^{gamma_C - gamma}) [d_v][t]
+  static constexpr uint32_t KQ16 = VN;     // fp16 copy of KQ for the Gram MMA (dead before Vn^T is written)
+  static constexpr uint32_t WN = 114688;   // -W [t][d_k], K blocks 8 KB apart
+  static constexpr uint32_t TB = 131072;   // T diag(beta) [t][s]
+  static constexpr uint32_t TW = 139264;   // T diag(beta e^gamma) [t][s]
+  static constexpr uint32_t P = 147456;    // P [t][s]
+  static constexpr uint32_t F32 = 155648;  // fp32: A [64][65] + T [64][65]
+};
+template <> struct Lay<true> {
+  static constexpr uint32_t KQ = 0;        // K^ as above (the Q^ halves are not written)
+  static constexpr uint32_t V = 32768;
+  static constexpr uint32_t S = 49152;
+  static constexpr uint32_t X = 81920;     // X bf16 [d_k][d_k]
+  static constexpr uint32_t VN = 114688;   // Vn_X^T diag(e^{gamma_C - gamma})
+  static constexpr uint32_t VNS = 131072;  // Vn_S^T diag(e^{gamma_C - gamma})
+  static constexpr uint32_t KQ16 = VN;
+  static constexpr uint32_t WN = 147456;
+  static constexpr uint32_t TB = 163840;
+  static constexpr uint32_t TW = 172032;
+  static constexpr uint32_t P = 0;         // (unused)
+  static constexpr uint32_t F32 = 180224;
+};
 constexpr int LDA = 65, LDO = 128;
 constexpr uint32_t F32_BYTES = 2 * 64 * LDA * 4;
-constexpr uint32_t OFF_CW = OFF_F32 + F32_BYTES;  // conv weights fp32 [3][128][4]
-constexpr uint32_t OFF_NW = OFF_CW + 3 * 128 * 4 * 4;
-constexpr uint32_t OFF_GATE = OFF_NW + 128 * 4;   // gam, beta, e^gam, e^{gamC-gam}: 4 x 64 fp32
-constexpr uint32_t SMEM_USED = OFF_GATE + 4 * 64 * 4;
 // Staging of a chunk's raw inputs, loaded by TMA (2-D tensor maps over qkv and z):
 // the raw q, k and v rows of tokens t0-3 .. t0+63 (bf16, one [67][128] box per
 // block) land over -W, T, P and the fp32 area, which are dead from the last MMA of
@@ -76,18 +94,27 @@ constexpr uint32_t SMEM_USED = OFF_GATE + 4 * 64 * 4;
 // the fp32 area's tail between the state-correction MMA and the epilogue.
 constexpr uint32_t RAW_BOX_ROWS = C + kConvW - 1;     // a chunk and its 3-token halo
 constexpr uint32_t RAW_BLK = RAW_BOX_ROWS * 256;       // one channel block: [67 rows][128 bf16]
-constexpr uint32_t OFF_RAW = OFF_WN;                   // [q | k | v blocks]
-constexpr uint32_t RAW_END = OFF_RAW + 3 * RAW_BLK;
-constexpr uint32_t OFF_OST = OFF_VN;  // O staging fp32 [64][128], after the Vn tiles are consumed
-constexpr uint32_t OFF_Z = RAW_END;   // z bf16 [64][128], in the fp32 area's tail
-static_assert(RAW_END <= OFF_F32 + F32_BYTES, "raw staging past the fp32 area");
-static_assert(OFF_RAW % 128 == 0 && RAW_BLK % 128 == 0 && RAW_END % 128 == 0, "TMA destinations need 128-B alignment");
-static_assert(OFF_Z + 64 * 128 * 2 <= OFF_CW, "z staging overlaps the conv weights");
-static_assert(OFF_OST + 64 * LDO * 4 <= OFF_WN, "O staging overlaps -W");
-constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;  // slack to align the base to 1024
+template <bool kXfer> struct Map : Lay<kXfer> {
+  using L_ = Lay<kXfer>;
+  static constexpr uint32_t CW = L_::F32 + F32_BYTES;   // conv weights fp32 [3][tap][128]
+  static constexpr uint32_t NW = CW + 3 * 128 * 4 * 4;
+  static constexpr uint32_t GATE = NW + 128 * 4;        // gam, beta, e^gam, e^{gamC-gam}
+  static constexpr uint32_t USED = GATE + 4 * 64 * 4;
+  static constexpr uint32_t BYTES = USED + 1024;        // slack to align the base to 1024
+  static constexpr uint32_t RAW = L_::WN;               // [q | k | v blocks]
+  static constexpr uint32_t RAW_END = RAW + 3 * RAW_BLK;
+  static constexpr uint32_t OST = L_::VN;               // O staging fp32 [64][128] (output pass)
+  static constexpr uint32_t Z = RAW_END;                // z bf16 [64][128] (output pass)
+  static_assert(RAW_END <= L_::F32 + F32_BYTES, "raw staging past the fp32 area");
+  static_assert(RAW % 128 == 0 && RAW_BLK % 128 == 0 && RAW_END % 128 == 0, "TMA destinations need 128-B alignment");
+  static_assert(kXfer || Z + 64 * 128 * 2 <= CW, "z staging overlaps the conv weights");
+  static_assert(kXfer || OST + 64 * LDO * 4 <= L_::WN, "O staging overlaps -W");
+  static_assert(BYTES <= 227 * 1024, "shared memory");
+};
 
 // ---- tensor memory columns ----
 constexpr uint32_t TM_G = 0, TM_W = 64, TM_U = 128, TM_O1 = 192, TM_O2 = 256, TM_Z = 384;
+constexpr uint32_t TM_VX = 192, TM_ZX = 256;          // transfer pass: X's Vn^T and X itself
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint64_t D_K = tc::sdesc_sw128(16, 1024);         // K-major tiles
@@ -168,10 +195,10 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
 // starting at packed row `start` (rows before the sequence are fetched too and
 // ignored: the conv reads the carried conv state for them).
 __device__ __forceinline__ void stage_raw(const CUtensorMap* tm_qkv, uint8_t* raw, uint64_t* mbar, int start,
-                                          int t0, int kh, int h, int Cq) {
-  mbar_expect_tx(mbar, 3 * RAW_BLK);
+                                          int t0, int kh, int h, int Cq, bool with_q) {
+  mbar_expect_tx(mbar, (with_q ? 3 : 2) * RAW_BLK);
   const int y = start + t0 - (kConvW - 1);
-  tma_load_2d(raw, tm_qkv, kh * kD, y, mbar);
+  if (with_q) tma_load_2d(raw, tm_qkv, kh * kD, y, mbar);
   tma_load_2d(raw + RAW_BLK, tm_qkv, Cq + kh * kD, y, mbar);
   tma_load_2d(raw + 2 * RAW_BLK, tm_qkv, 2 * Cq + h * kD, y, mbar);
 }
@@ -198,9 +225,29 @@ __device__ __forceinline__ void sync_for_mma() {
   tc::fence_after_sync();
 }
 
+// One segment of the work list (built on the device from cu_seqlens).
+struct Seg {
+  int n, begin, len, sigma, nsig, k0;   // sequence, token range within it, segment index/count,
+                                        // the sequence's first boundary slot
+};
+
+__device__ __forceinline__ Seg load_seg(const int* list, int u) {
+  const int* e = list + 4 + 8 * u;
+  return Seg{e[0], e[1], e[2], e[3], e[4], e[5]};
+}
+
+// Transfer matrices of boundary slot k, value head h: X (the map), S (end state
+// from zero, overwritten by the combine pass with the true start state of the
+// next segment), and the sequence's initial state (first slot only).
+__device__ __forceinline__ float* xfer_ptr(const PrefillArgs& p, int k, int h, int part) {
+  return p.xfer + (((size_t)k * p.h_v + h) * 3 + part) * (size_t)(kD * kD);
+}
+
+template <bool kXfer>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv,
-                   const __grid_constant__ CUtensorMap tm_z) {
+    chunk_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv,
+                 const __grid_constant__ CUtensorMap tm_z) {
+  using M = Map<kXfer>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mbar;      // MMA completion
   __shared__ __align__(8) uint64_t mbar_raw;  // raw q|k|v rows of a chunk landed
@@ -208,16 +255,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (!cu_seqlens_valid(p)) {
-    if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_BOUNDS);
-    return;
-  }
-  const int n = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
+  const int u = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
+  if (u >= p.seg_list[0]) return;
+  const Seg sg = load_seg(p.seg_list, u);
+  if (kXfer && sg.sigma == sg.nsig - 1) return;   // the last segment needs no transfer map
+  const int n = sg.n;
   const int G = p.h_v / p.h_k, kh = h / G;
   const int start = p.cu_seqlens[n];
-  const int len = p.cu_seqlens[n + 1] - start;
-  if (len <= 0) return;
+  const int seg_end = sg.begin + sg.len;          // token positions within the sequence
   const int Cq = p.h_k * kD, Cc = 2 * Cq + p.h_v * kD;
+
+  // where the state comes from and goes to
+  const float* S_init = nullptr;
+  float* S_final = nullptr;
+  float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
+  if (!kXfer) {
+    if (sg.nsig == 1) {
+      S_init = ssm;
+      S_final = ssm;
+    } else {
+      S_init = sg.sigma == 0 ? xfer_ptr(p, sg.k0, h, 2) : xfer_ptr(p, sg.k0 + sg.sigma - 1, h, 1);
+      S_final = sg.sigma == sg.nsig - 1 ? ssm : nullptr;
+    }
+  }
 
   Smem sm;
   {
@@ -226,15 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.base = smem_raw + pad;
     sm.addr = raw + pad;
   }
-  float* cw = sm.f32(OFF_CW);      // [blk][tap][i]
-  float* nw = sm.f32(OFF_NW);
-  float* gam = sm.f32(OFF_GATE);
+  float* cw = sm.f32(M::CW);      // [blk][tap][i]
+  float* nw = sm.f32(M::NW);
+  float* gam = sm.f32(M::GATE);
   float* bet = gam + 64;
   float* eg = gam + 128;
   float* egc = gam + 192;
-  float* Af = sm.f32(OFF_F32);
+  float* Af = sm.f32(M::F32);
   float* Tf = Af + 64 * LDA;
-  float* Ost = sm.f32(OFF_OST);     // aliases the Vn tiles (used after them)
+  float* Ost = sm.f32(M::OST);      // output pass: aliases the Vn tiles (used after them)
 
   if (tid == 0) {
     tc::mbar_init(&mbar, 1);
@@ -261,22 +321,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
   const int half = warp >> 2;               // which half of the columns
 
-  float* S_glob = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
-  // initial state: fp32 into TMEM, bf16 into the S operand tile
-  {
-    const float4* src = reinterpret_cast<const float4*>(S_glob + (size_t)row * kD + half * 64);
+  // initial state(s): fp32 into TMEM, bf16 into the operand tile(s)
 #pragma unroll
-    for (int c32 = 0; c32 < 2; ++c32) {
-      float v[32];
+  for (int c32 = 0; c32 < 2; ++c32) {
+    const int col0 = half * 64 + c32 * 32;
+    float v[32];
+    if (!kXfer) {
+      const float4* src = reinterpret_cast<const float4*>(S_init + (size_t)row * kD + col0);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float4 x = src[c32 * 8 + q];
+        const float4 x = src[q];
         v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
       }
-      tc::tmem_st32(tmem + lane_base + TM_Z + half * 64 + c32 * 32, v);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+    tc::tmem_st32(tmem + lane_base + TM_Z + col0, v);
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+      store_bf16x8(sm.base + M::S, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
+    if (kXfer) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = (col0 + i == row) ? 1.0f : 0.0f;
+      tc::tmem_st32(tmem + lane_base + TM_ZX + col0, v);
 #pragma unroll
       for (int m = 0; m < 4; ++m)
-        store_bf16x8(sm.base + OFF_S, tc::sw128_off(row, half * 64 + c32 * 32 + 8 * m, 16384), v + 8 * m);
+        store_bf16x8(sm.base + M::X, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
     }
   }
 
@@ -299,62 +370,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     return all_ok;
   };
 
-  if (tid == 32) stage_raw(&tm_qkv, sm.base + OFF_RAW, &mbar_raw, start, 0, kh, h, Cq);
+  if (tid == 32) stage_raw(&tm_qkv, sm.base + M::RAW, &mbar_raw, start, sg.begin, kh, h, Cq, !kXfer);
   // gate inputs of the next chunk, prefetched into warp 0's registers
   float a_nx[2] = {0.0f, 0.0f}, b_nx[2] = {0.0f, 0.0f};
   if (warp == 0) {
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int t = lane + 32 * u;
-      if (t < len) {
+    for (int uu = 0; uu < 2; ++uu) {
+      const int t = sg.begin + lane + 32 * uu;
+      if (t < seg_end) {
         const size_t pidx = (size_t)(start + t) * p.h_v + h;
-        a_nx[u] = bf16_to_f32(p.a[pidx]);
-        b_nx[u] = bf16_to_f32(p.b[pidx]);
+        a_nx[uu] = bf16_to_f32(p.a[pidx]);
+        b_nx[uu] = bf16_to_f32(p.b[pidx]);
       }
     }
   }
   uint32_t chunk_parity = 0;
   // bulk copies in flight (uniform across the CTA), waited for on the time-out path
   bool raw_pending = true, z_pending = false;
-  for (int t0 = 0; t0 < len && !aborted; t0 += C, chunk_parity ^= 1u) {
-    const int L = min(C, len - t0);
+  for (int t0 = sg.begin; t0 < seg_end && !aborted; t0 += C, chunk_parity ^= 1u) {
+    const int L = min(C, seg_end - t0);
 
     // ---- gates and their cumulative sums (warp 0) ----
     if (warp == 0) {
       float g2[2], b2[2];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int t = lane + 32 * u;
-        g2[u] = t < L ? -A_exp * softplus(a_nx[u] + dtb) : 0.0f;
-        b2[u] = t < L ? sigmoid(b_nx[u]) : 0.0f;
+      for (int uu = 0; uu < 2; ++uu) {
+        const int t = lane + 32 * uu;
+        g2[uu] = t < L ? -A_exp * softplus(a_nx[uu] + dtb) : 0.0f;
+        b2[uu] = t < L ? sigmoid(b_nx[uu]) : 0.0f;
       }
       // prefetch the next chunk's gate inputs
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int t = t0 + C + lane + 32 * u;
-        if (t < len) {
+      for (int uu = 0; uu < 2; ++uu) {
+        const int t = t0 + C + lane + 32 * uu;
+        if (t < seg_end) {
           const size_t pidx = (size_t)(start + t) * p.h_v + h;
-          a_nx[u] = bf16_to_f32(p.a[pidx]);
-          b_nx[u] = bf16_to_f32(p.b[pidx]);
+          a_nx[uu] = bf16_to_f32(p.a[pidx]);
+          b_nx[uu] = bf16_to_f32(p.b[pidx]);
         }
       }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
+      for (int uu = 0; uu < 2; ++uu) {
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, g2[u], off);
-          if (lane >= off) g2[u] += y;
+          const float y = __shfl_up_sync(0xffffffffu, g2[uu], off);
+          if (lane >= off) g2[uu] += y;
         }
       }
       g2[1] += __shfl_sync(0xffffffffu, g2[0], 31);
       const float gC = __shfl_sync(0xffffffffu, g2[1], 31);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int t = lane + 32 * u;
-        gam[t] = g2[u];
-        bet[t] = b2[u];
-        eg[t] = __expf(g2[u]);
-        egc[t] = __expf(gC - g2[u]);
+      for (int uu = 0; uu < 2; ++uu) {
+        const int t = lane + 32 * uu;
+        gam[t] = g2[uu];
+        bet[t] = b2[uu];
+        eg[t] = __expf(g2[uu]);
+        egc[t] = __expf(gC - g2[uu]);
       }
     }
 
@@ -362,26 +433,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     raw_pending = false;
 
     // ---- conv + SiLU + L2 norms -> K^, Q^, V tiles (all warps, a token per warp step,
-    //      two tokens in flight per warp) ----
+    //      two tokens in flight per warp); the transfer pass needs no q ----
+    constexpr int kB0 = kXfer ? 1 : 0;
 #pragma unroll 1
     for (int tb = warp; tb < C; tb += 2 * (kThreads / 32)) {
       float y[2][3][4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int t = tb + u * (kThreads / 32);
+      for (int uu = 0; uu < 2; ++uu) {
+        const int t = tb + uu * (kThreads / 32);
 #pragma unroll
         for (int blk = 0; blk < 3; ++blk)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) y[u][blk][e] = 0.0f;
+          for (int e = 0; e < 4; ++e) y[uu][blk][e] = 0.0f;
         if (t >= L) continue;
 #pragma unroll
         for (int j = 0; j < kConvW; ++j) {
           const int tau = t0 + t - (kConvW - 1) + j;   // position in the sequence
 #pragma unroll
-          for (int blk = 0; blk < 3; ++blk) {
+          for (int blk = kB0; blk < 3; ++blk) {
             float x[4];
             if (tau >= 0) {
-              const uint2 r = *reinterpret_cast<const uint2*>(sm.base + OFF_RAW + blk * RAW_BLK +
+              const uint2 r = *reinterpret_cast<const uint2*>(sm.base + M::RAW + blk * RAW_BLK +
                                                               (t + j) * 256 + lane * 8);
               x[0] = bf16_to_f32(r.x & 0xffffu); x[1] = bf16_to_f32(r.x >> 16);
               x[2] = bf16_to_f32(r.y & 0xffffu); x[3] = bf16_to_f32(r.y >> 16);
@@ -392,86 +464,93 @@ __global__ void __launch_bounds__(kThreads, 1)
               x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
             }
             const float4 w4 = cwr[blk][j];
-            y[u][blk][0] = fmaf(w4.x, x[0], y[u][blk][0]);
-            y[u][blk][1] = fmaf(w4.y, x[1], y[u][blk][1]);
-            y[u][blk][2] = fmaf(w4.z, x[2], y[u][blk][2]);
-            y[u][blk][3] = fmaf(w4.w, x[3], y[u][blk][3]);
+            y[uu][blk][0] = fmaf(w4.x, x[0], y[uu][blk][0]);
+            y[uu][blk][1] = fmaf(w4.y, x[1], y[uu][blk][1]);
+            y[uu][blk][2] = fmaf(w4.z, x[2], y[uu][blk][2]);
+            y[uu][blk][3] = fmaf(w4.w, x[3], y[uu][blk][3]);
           }
         }
 #pragma unroll
-        for (int blk = 0; blk < 3; ++blk) silu4(y[u][blk]);
+        for (int blk = kB0; blk < 3; ++blk) silu4(y[uu][blk]);
       }
       float ss[2][2];
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        ss[u][0] = y[u][0][0] * y[u][0][0];
-        ss[u][1] = y[u][1][0] * y[u][1][0];
+      for (int uu = 0; uu < 2; ++uu) {
+        ss[uu][0] = y[uu][0][0] * y[uu][0][0];
+        ss[uu][1] = y[uu][1][0] * y[uu][1][0];
 #pragma unroll
         for (int e = 1; e < 4; ++e) {
-          ss[u][0] = fmaf(y[u][0][e], y[u][0][e], ss[u][0]);
-          ss[u][1] = fmaf(y[u][1][e], y[u][1][e], ss[u][1]);
+          ss[uu][0] = fmaf(y[uu][0][e], y[uu][0][e], ss[uu][0]);
+          ss[uu][1] = fmaf(y[uu][1][e], y[uu][1][e], ss[uu][1]);
         }
       }
 #pragma unroll
       for (int m = 16; m >= 1; m >>= 1)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          ss[u][0] += __shfl_xor_sync(0xffffffffu, ss[u][0], m);
-          ss[u][1] += __shfl_xor_sync(0xffffffffu, ss[u][1], m);
+        for (int uu = 0; uu < 2; ++uu) {
+          if (!kXfer) ss[uu][0] += __shfl_xor_sync(0xffffffffu, ss[uu][0], m);
+          ss[uu][1] += __shfl_xor_sync(0xffffffffu, ss[uu][1], m);
         }
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int t = tb + u * (kThreads / 32);
-        const float rq = rsqrtf(ss[u][0] + p.l2_eps) * qscale, rk = rsqrtf(ss[u][1] + p.l2_eps);
+      for (int uu = 0; uu < 2; ++uu) {
+        const int t = tb + uu * (kThreads / 32);
+        const float rq = rsqrtf(ss[uu][0] + p.l2_eps) * qscale, rk = rsqrtf(ss[uu][1] + p.l2_eps);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          y[u][0][e] *= rq;
-          y[u][1][e] *= rk;
+          y[uu][0][e] *= rq;
+          y[uu][1][e] *= rk;
         }
         const uint32_t o16 = tc::sw128_off(t, 4 * lane, 16384), o8 = tc::sw128_off(t, 4 * lane, 8192);
-        store_bf16x4(sm.base + OFF_KQ, o16, y[u][1][0], y[u][1][1], y[u][1][2], y[u][1][3]);
-        store_bf16x4(sm.base + OFF_KQ + 8192, o16, y[u][0][0], y[u][0][1], y[u][0][2], y[u][0][3]);
-        store_bf16x4(sm.base + OFF_V, o8, y[u][2][0], y[u][2][1], y[u][2][2], y[u][2][3]);
-        store_f16x4(sm.base + OFF_KQ16, o16, y[u][1][0], y[u][1][1], y[u][1][2], y[u][1][3]);
-        store_f16x4(sm.base + OFF_KQ16 + 8192, o16, y[u][0][0], y[u][0][1], y[u][0][2], y[u][0][3]);
+        store_bf16x4(sm.base + M::KQ, o16, y[uu][1][0], y[uu][1][1], y[uu][1][2], y[uu][1][3]);
+        store_bf16x4(sm.base + M::V, o8, y[uu][2][0], y[uu][2][1], y[uu][2][2], y[uu][2][3]);
+        store_f16x4(sm.base + M::KQ16, o16, y[uu][1][0], y[uu][1][1], y[uu][1][2], y[uu][1][3]);
+        if (!kXfer) {
+          store_bf16x4(sm.base + M::KQ + 8192, o16, y[uu][0][0], y[uu][0][1], y[uu][0][2], y[uu][0][3]);
+          store_f16x4(sm.base + M::KQ16 + 8192, o16, y[uu][0][0], y[uu][0][1], y[uu][0][2], y[uu][0][3]);
+        }
       }
     }
     sync_for_mma();
 
-    // ---- Gram matrices [K; Q] K^T and O1 = S0 Q^T ----
+    // ---- Gram matrices [K; Q] K^T (fp16) and, in the output pass, O1 = S0 Q^T ----
     if (tid == 0) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-        const uint32_t a = sm.addr + OFF_KQ16 + kb * 16384 + ks;
+        const uint32_t a = sm.addr + M::KQ16 + kb * 16384 + ks;
         tc::mma_bf16(tmem + TM_G, tc::sdesc_at(D_K, a), tc::sdesc_at(D_K, a), ID_GRAM, k > 0);
       }
+      if (!kXfer) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-        tc::mma_bf16(tmem + TM_O1, tc::sdesc_at(D_K, sm.addr + OFF_S + kb * 16384 + ks),
-                     tc::sdesc_at(D_K, sm.addr + OFF_KQ + kb * 16384 + 8192 + ks), ID_KK, k > 0);
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TM_O1, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                       tc::sdesc_at(D_K, sm.addr + M::KQ + kb * 16384 + 8192 + ks), ID_KK, k > 0);
+        }
       }
       tc::mma_commit(&mbar);
     }
-    // meanwhile: pre-scale the fp32 state by the chunk's total decay
+    // meanwhile: pre-scale the fp32 state(s) by the chunk's total decay
     {
       const float dC = eg[C - 1];
 #pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
-        float v[32];
-        const uint32_t ta = tmem + lane_base + TM_Z + half * 64 + c32 * 32;
-        tc::tmem_ld32(ta, v);
+      for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= dC;
-        tc::tmem_st32(ta, v);
+        for (int c32 = 0; c32 < 2; ++c32) {
+          float v[32];
+          const uint32_t ta = tmem + lane_base + (zz ? TM_ZX : TM_Z) + half * 64 + c32 * 32;
+          tc::tmem_ld32(ta, v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= dC;
+          tc::tmem_st32(ta, v);
+        }
       }
     }
     if (!wait_mma()) { aborted = true; break; }
 
     // ---- A (fp32, lanes 0-63) and P (bf16 tile, lanes 64-127) from the Gram rows;
     //      warps w and w+4 share a lane quarter and split its 64 columns ----
-    {
+    if (!kXfer || (warp & 3) < 2) {
       float v[32];
       const int t = row & 63;
       const float gt = gam[t];
@@ -492,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int m = 0; m < 4; ++m)
-          store_bf16x8(sm.base + OFF_P, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
+          store_bf16x8(sm.base + M::P, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
       }
     }
     __syncthreads();
@@ -529,11 +608,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         for (int kb = j; kb < i; ++kb) {
 #pragma unroll
-          for (int s = 0; s < 16; ++s) {
-            const float tv = Tf[(16 * kb + s) * LDA + 16 * j + c];
+          for (int s2 = 0; s2 < 16; ++s2) {
+            const float tv = Tf[(16 * kb + s2) * LDA + 16 * j + c];
 #pragma unroll
             for (int r = 0; r < 4; ++r)
-              m[r] = fmaf(Af[(16 * i + 4 * qr + r) * LDA + 16 * kb + s], tv, m[r]);
+              m[r] = fmaf(Af[(16 * i + 4 * qr + r) * LDA + 16 * kb + s2], tv, m[r]);
           }
         }
         float mf[16];
@@ -562,8 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         xb[q] = tv * bet[c8 + q];
         xw[q] = xb[q] * eg[c8 + q];
       }
-      store_bf16x8(sm.base + OFF_TB, tc::sw128_off(t, c8, 0), xb);
-      store_bf16x8(sm.base + OFF_TW, tc::sw128_off(t, c8, 0), xw);
+      store_bf16x8(sm.base + M::TB, tc::sw128_off(t, c8, 0), xb);
+      store_bf16x8(sm.base + M::TW, tc::sw128_off(t, c8, 0), xw);
     }
     sync_for_mma();
 
@@ -571,13 +650,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid == 0) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        tc::mma_bf16(tmem + TM_W, tc::sdesc_at(D_MN_KQ, sm.addr + OFF_KQ + k * 2048),
-                     tc::sdesc_at(D_K, sm.addr + OFF_TW + k * 32), ID_MN_A, k > 0);
+        tc::mma_bf16(tmem + TM_W, tc::sdesc_at(D_MN_KQ, sm.addr + M::KQ + k * 2048),
+                     tc::sdesc_at(D_K, sm.addr + M::TW + k * 32), ID_MN_A, k > 0);
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        tc::mma_bf16(tmem + TM_U, tc::sdesc_at(D_MN_V, sm.addr + OFF_V + k * 2048),
-                     tc::sdesc_at(D_K, sm.addr + OFF_TB + k * 32), ID_MN_A, k > 0);
+        tc::mma_bf16(tmem + TM_U, tc::sdesc_at(D_MN_V, sm.addr + M::V + k * 2048),
+                     tc::sdesc_at(D_K, sm.addr + M::TB + k * 32), ID_MN_A, k > 0);
       }
       tc::mma_commit(&mbar);
     }
@@ -587,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
       float v[32];
       tc::tmem_ld32(tmem + lane_base + TM_W + half * 32, v);
-      uint8_t* wn = sm.base + OFF_WN;
+      uint8_t* wn = sm.base + M::WN;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int t = half * 32 + i;
@@ -596,24 +675,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     sync_for_mma();
 
-    // ---- Vn^T = U^T - S0 W^T ----
+    // ---- Vn^T = U^T - S0 W^T  (transfer pass also: Vn_X^T = -X W^T) ----
     if (tid == 0) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-        tc::mma_bf16(tmem + TM_U, tc::sdesc_at(D_K, sm.addr + OFF_S + kb * 16384 + ks),
-                     tc::sdesc_at(D_K, sm.addr + OFF_WN + kb * 8192 + ks), ID_KK, 1u);
+        tc::mma_bf16(tmem + TM_U, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                     tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
+      }
+      if (kXfer) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TM_VX, tc::sdesc_at(D_K, sm.addr + M::X + kb * 16384 + ks),
+                       tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, k > 0);
+        }
       }
       tc::mma_commit(&mbar);
     }
     if (!wait_mma()) { aborted = true; break; }
 
-    // ---- z of the chunk -> smem (bulk copies; read by the epilogue) ----
-    if (tid == 32) {
-      mbar_expect_tx(&mbar_z, 64 * 256);
-      tma_load_2d(sm.base + OFF_Z, &tm_z, h * kD, start + t0, &mbar_z);
+    if (!kXfer) {
+      // ---- z of the chunk -> smem (TMA; read by the epilogue) ----
+      if (tid == 32) {
+        mbar_expect_tx(&mbar_z, 64 * 256);
+        tma_load_2d(sm.base + M::Z, &tm_z, h * kD, start + t0, &mbar_z);
+      }
+      z_pending = true;
     }
-    z_pending = true;
 
     // ---- Vn^T tiles (plain and decay-weighted), row = d_v index ----
     {
@@ -621,52 +710,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_ld32(tmem + lane_base + TM_U + half * 32, v);
 #pragma unroll
       for (int i = 0; i < 32; ++i) vs[i] = v[i] * egc[half * 32 + i];
+      if (kXfer) {
+        tc::tmem_ld32(tmem + lane_base + TM_VX + half * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= egc[half * 32 + i];
+      }
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const uint32_t off = tc::sw128_off(row, half * 32 + 8 * m, 0);
-        store_bf16x8(sm.base + OFF_VN, off, v + 8 * m);
-        store_bf16x8(sm.base + OFF_VNS, off, vs + 8 * m);
+        store_bf16x8(sm.base + M::VN, off, v + 8 * m);
+        store_bf16x8(sm.base + M::VNS, off, vs + 8 * m);
       }
     }
     sync_for_mma();
 
-    // ---- O2 = Vn^T P^T and S += Vn^T diag(e^{gC-g}) K ----
+    // ---- O2 = Vn^T P^T and S += Vn^T diag(e^{gC-g}) K  (transfer: S and X updates) ----
     if (tid == 0) {
+      if (!kXfer) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        tc::mma_bf16(tmem + TM_O2, tc::sdesc_at(D_K, sm.addr + OFF_VN + k * 32),
-                     tc::sdesc_at(D_K, sm.addr + OFF_P + k * 32), ID_KK, k > 0);
+        for (int k = 0; k < 4; ++k) {
+          tc::mma_bf16(tmem + TM_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
+                       tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          tc::mma_bf16(tmem + TM_ZX, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
+                       tc::sdesc_at(D_MN_KQ, sm.addr + M::KQ + k * 2048), ID_MN_B, 1u);
+        }
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        tc::mma_bf16(tmem + TM_Z, tc::sdesc_at(D_K, sm.addr + OFF_VNS + k * 32),
-                     tc::sdesc_at(D_MN_KQ, sm.addr + OFF_KQ + k * 2048), ID_MN_B, 1u);
+        tc::mma_bf16(tmem + TM_Z, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
+                     tc::sdesc_at(D_MN_KQ, sm.addr + M::KQ + k * 2048), ID_MN_B, 1u);
       }
       tc::mma_commit(&mbar);
     }
     if (!wait_mma()) { aborted = true; break; }
     // the next chunk's raw rows land while this chunk finishes
-    if (tid == 32 && t0 + C < len) stage_raw(&tm_qkv, sm.base + OFF_RAW, &mbar_raw, start, t0 + C, kh, h, Cq);
-    raw_pending = t0 + C < len;
+    if (tid == 32 && t0 + C < seg_end) stage_raw(&tm_qkv, sm.base + M::RAW, &mbar_raw, start, t0 + C, kh, h, Cq, !kXfer);
+    raw_pending = t0 + C < seg_end;
 
-    // ---- new S -> bf16 operand tile; O = e^gamma O1 + O2 -> fp32 staging ----
+    // ---- new state(s) -> bf16 operand tiles; output pass: O = e^gamma O1 + O2 -> fp32 staging ----
     {
 #pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
-        float v[32];
-        tc::tmem_ld32(tmem + lane_base + TM_Z + half * 64 + c32 * 32, v);
+      for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          store_bf16x8(sm.base + OFF_S, tc::sw128_off(row, half * 64 + c32 * 32 + 8 * m, 16384), v + 8 * m);
-      }
-      float o1[32], o2[32];
-      tc::tmem_ld32(tmem + lane_base + TM_O1 + half * 32, o1);
-      tc::tmem_ld32(tmem + lane_base + TM_O2 + half * 32, o2);
+        for (int c32 = 0; c32 < 2; ++c32) {
+          float v[32];
+          tc::tmem_ld32(tmem + lane_base + (zz ? TM_ZX : TM_Z) + half * 64 + c32 * 32, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int t = half * 32 + i;
-        Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
+          for (int m = 0; m < 4; ++m)
+            store_bf16x8(sm.base + (zz ? M::X : M::S), tc::sw128_off(row, half * 64 + c32 * 32 + 8 * m, 16384),
+                         v + 8 * m);
+        }
       }
+      if (!kXfer) {
+        float o1[32], o2[32];
+        tc::tmem_ld32(tmem + lane_base + TM_O1 + half * 32, o1);
+        tc::tmem_ld32(tmem + lane_base + TM_O2 + half * 32, o2);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int t = half * 32 + i;
+          Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
+        }
+      }
+    }
+    if (kXfer) {
+      __syncthreads();
+      continue;
     }
     if (!__syncthreads_and(tc::mbar_wait(&mbar_z, chunk_parity, kWaitBudget))) { aborted = true; break; }
     z_pending = false;
@@ -680,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ss = fmaf(o4.w, o4.w, ss);
       ss = warp_sum(ss);
       const float rstd = rsqrtf(ss * (1.0f / kD) + p.rms_eps);
-      const uint2 zr = *reinterpret_cast<const uint2*>(sm.base + OFF_Z + t * 256 + lane * 8);
+      const uint2 zr = *reinterpret_cast<const uint2*>(sm.base + M::Z + t * 256 + lane * 8);
       const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
       float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
                     bf16_to_f32(zr.y >> 16)};
@@ -699,14 +811,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (raw_pending) tc::mbar_wait(&mbar_raw, chunk_parity, kWaitBudget);
     if (z_pending) tc::mbar_wait(&mbar_z, chunk_parity, kWaitBudget);
   } else {
-    // final state back to global memory
-    float4* dst = reinterpret_cast<float4*>(S_glob + (size_t)row * kD + half * 64);
+    // final state(s) back to global memory
 #pragma unroll
-    for (int c32 = 0; c32 < 2; ++c32) {
-      float v[32];
-      tc::tmem_ld32(tmem + lane_base + TM_Z + half * 64 + c32 * 32, v);
+    for (int zz = 0; zz < 2; ++zz) {
+      float* dst_base = kXfer ? xfer_ptr(p, sg.k0 + sg.sigma, h, zz == 0 ? 1 : 0) : (zz == 0 ? S_final : nullptr);
+      if (dst_base == nullptr) continue;
+      float4* dst = reinterpret_cast<float4*>(dst_base + (size_t)row * kD + half * 64);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) dst[c32 * 8 + q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int c32 = 0; c32 < 2; ++c32) {
+        float v[32];
+        tc::tmem_ld32(tmem + lane_base + (zz ? TM_ZX : TM_Z) + half * 64 + c32 * 32, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dst[c32 * 8 + q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
     }
   }
   tc::fence_before_sync();
@@ -714,10 +832,135 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, TM_COLS);
 }
 
+// The work list: every sequence split into segments of p.seg_tokens (the last
+// one ragged; a sequence of at most that many tokens is one segment), and the
+// list of sequences with more than one segment.  Validates cu_seqlens first:
+// on a violation both lists stay empty and the status word says why.
+__global__ void __launch_bounds__(256) seg_list_kernel(PrefillArgs p) {
+  __shared__ int s_cnt[256];
+  __shared__ int s_base, s_mbase;
+  if (!cu_seqlens_valid(p)) {
+    if (threadIdx.x == 0) {
+      record_status(p.status, GDN_ERR_DEVICE_BOUNDS);
+      p.seg_list[0] = 0;
+      p.multi_list[0] = 0;
+    }
+    return;
+  }
+  if (threadIdx.x == 0) { s_base = 0; s_mbase = 0; }
+  __syncthreads();
+  for (int n0 = 0; n0 < p.n_seqs; n0 += 256) {
+    const int n = n0 + threadIdx.x;
+    int nsig = 0, len = 0, st = 0;
+    if (n < p.n_seqs) {
+      st = p.cu_seqlens[n];
+      len = p.cu_seqlens[n + 1] - st;
+      nsig = len <= 0 ? 0 : (len + p.seg_tokens - 1) / p.seg_tokens;
+    }
+    // inclusive scan of segment counts over the tile (and of multi-segment flags)
+    // segment count in bits 0-21 (< 2^21 + 256), multi-segment count in bits 22-30 (<= 256)
+    s_cnt[threadIdx.x] = nsig | ((nsig > 1 ? 1 : 0) << 22);
+    __syncthreads();
+    for (int off = 1; off < 256; off <<= 1) {
+      const int v = threadIdx.x >= off ? s_cnt[threadIdx.x - off] : 0;
+      __syncthreads();
+      s_cnt[threadIdx.x] += v;
+      __syncthreads();
+    }
+    const int incl = s_cnt[threadIdx.x];
+    const int seg_off = s_base + (incl & 0x3FFFFF) - nsig;
+    const int m_off = s_mbase + (incl >> 22) - (nsig > 1 ? 1 : 0);
+    const int k0 = st / p.seg_tokens;
+    for (int sg = 0; sg < nsig; ++sg) {
+      int* e = p.seg_list + 4 + 8 * (seg_off + sg);
+      e[0] = n;
+      e[1] = sg * p.seg_tokens;
+      e[2] = min(p.seg_tokens, len - sg * p.seg_tokens);
+      e[3] = sg;
+      e[4] = nsig;
+      e[5] = k0;
+    }
+    if (nsig > 1) {
+      int* e = p.multi_list + 4 + 4 * m_off;
+      e[0] = n;
+      e[1] = k0;
+      e[2] = nsig;
+    }
+    __syncthreads();
+    if (threadIdx.x == 255) {
+      s_base += incl & 0x3FFFFF;
+      s_mbase += incl >> 22;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    p.seg_list[0] = s_base;
+    p.multi_list[0] = s_mbase;
+  }
+}
+
+// Combines the transfer maps of a multi-segment sequence, 16 state rows per
+// CTA (the rows of S evolve independently): S_{sigma+1} = S_sigma X_sigma +
+// S_sigma^0, in fp32, written over the slot's end state, after saving the
+// sequence's initial state (so the output pass never reads a state that the
+// last segment's CTA is writing).
+constexpr int kCombineRows = 16;
+constexpr uint32_t kCombineSmem = (kD * kD + kCombineRows * kD) * 4;
+
+__global__ void __launch_bounds__(256) combine_kernel(PrefillArgs p) {
+  extern __shared__ float csm[];
+  float* Xs = csm;                 // [128][128]
+  float* Sr = csm + kD * kD;       // [16][128]
+  const int per = p.h_v * (kD / kCombineRows);
+  const int u = blockIdx.x / per, rem = blockIdx.x % per;
+  const int h = rem / (kD / kCombineRows), rb = rem % (kD / kCombineRows);
+  if (u >= p.multi_list[0]) return;
+  const int* e = p.multi_list + 4 + 4 * u;
+  const int n = e[0], k0 = e[1], nsig = e[2];
+  const int r0 = rb * kCombineRows;
+  const int tid = threadIdx.x;
+  const float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
+  float* init = xfer_ptr(p, k0, h, 2);
+  for (int i = tid; i < kCombineRows * kD / 4; i += 256) {
+    const float4 v = reinterpret_cast<const float4*>(ssm + (size_t)r0 * kD)[i];
+    reinterpret_cast<float4*>(Sr)[i] = v;
+    reinterpret_cast<float4*>(init + (size_t)r0 * kD)[i] = v;
+  }
+  const int i = tid >> 4, c0 = (tid & 15) * 8;   // this thread: row i, columns c0 .. c0+7
+  for (int sg = 0; sg + 1 < nsig; ++sg) {
+    const float* Xg = xfer_ptr(p, k0 + sg, h, 0);
+    float* Sg = xfer_ptr(p, k0 + sg, h, 1);
+    __syncthreads();   // previous step's readers of Xs/Sr are done
+    for (int q = tid; q < kD * kD / 4; q += 256)
+      reinterpret_cast<float4*>(Xs)[q] = reinterpret_cast<const float4*>(Xg)[q];
+    __syncthreads();
+    float acc[8];
+    const float4 b0 = reinterpret_cast<const float4*>(Sg + (size_t)(r0 + i) * kD + c0)[0];
+    const float4 b1 = reinterpret_cast<const float4*>(Sg + (size_t)(r0 + i) * kD + c0)[1];
+    acc[0] = b0.x; acc[1] = b0.y; acc[2] = b0.z; acc[3] = b0.w;
+    acc[4] = b1.x; acc[5] = b1.y; acc[6] = b1.z; acc[7] = b1.w;
+#pragma unroll 4
+    for (int j = 0; j < kD; ++j) {
+      const float sv = Sr[i * kD + j];
+      const float4 x0 = reinterpret_cast<const float4*>(Xs + j * kD + c0)[0];
+      const float4 x1 = reinterpret_cast<const float4*>(Xs + j * kD + c0)[1];
+      acc[0] = fmaf(sv, x0.x, acc[0]); acc[1] = fmaf(sv, x0.y, acc[1]);
+      acc[2] = fmaf(sv, x0.z, acc[2]); acc[3] = fmaf(sv, x0.w, acc[3]);
+      acc[4] = fmaf(sv, x1.x, acc[4]); acc[5] = fmaf(sv, x1.y, acc[5]);
+      acc[6] = fmaf(sv, x1.z, acc[6]); acc[7] = fmaf(sv, x1.w, acc[7]);
+    }
+    __syncthreads();   // all reads of Sr done before it is overwritten
+#pragma unroll
+    for (int q = 0; q < 8; ++q) Sr[i * kD + c0 + q] = acc[q];
+    reinterpret_cast<float4*>(Sg + (size_t)(r0 + i) * kD + c0)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    reinterpret_cast<float4*>(Sg + (size_t)(r0 + i) * kD + c0)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  }
+}
+
 // The last conv_w - 1 raw inputs of each sequence become its conv state
 // (rows of the old state fill in when the sequence is shorter than that).
 __global__ void __launch_bounds__(256) conv_state_kernel(PrefillArgs p) {
-  if (!cu_seqlens_valid(p)) return;
+  if (*p.status == GDN_ERR_DEVICE_BOUNDS) return;   // cu_seqlens rejected by the list kernel
   const int Cc = 2 * p.h_k * kD + p.h_v * kD;
   const int n = blockIdx.y, c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= Cc) return;
@@ -735,7 +978,26 @@ __global__ void __launch_bounds__(256) conv_state_kernel(PrefillArgs p) {
 
 }  // namespace
 
-size_t prefill_scratch_bytes(int, int, int, long long) { return 0; }
+namespace {
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+struct ScratchLayout {
+  size_t seg_list, multi_list, xfer, total;
+};
+ScratchLayout scratch_layout(int n_seqs, int h_v, long long total_tokens) {
+  const long long slots = total_tokens / kSegTokens;
+  const long long units = slots + n_seqs;   // segments: sum of ceil(T_n / L) <= T / L + N
+  ScratchLayout l;
+  l.seg_list = 0;
+  l.multi_list = align256(16 + (size_t)units * 32);
+  l.xfer = l.multi_list + align256(16 + (size_t)slots * 16);
+  l.total = l.xfer + (size_t)slots * h_v * 3 * kD * kD * sizeof(float);
+  return l;
+}
+}  // namespace
+
+size_t prefill_scratch_bytes(int n_seqs, int, int h_v, long long total_tokens) {
+  return scratch_layout(n_seqs, h_v, total_tokens).total;
+}
 
 namespace {
 
@@ -768,20 +1030,49 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)SMEM_BYTES);
-  if (e != cudaSuccess) return e;
+cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream) {
+  PrefillArgs p = p_in;
+  const ScratchLayout l = scratch_layout(p.n_seqs, p.h_v, p.total_tokens);
+  char* scratch = static_cast<char*>(p.scratch);
+  p.seg_list = reinterpret_cast<int*>(scratch + l.seg_list);
+  p.multi_list = reinterpret_cast<int*>(scratch + l.multi_list);
+  p.xfer = reinterpret_cast<float*>(scratch + l.xfer);
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Map<false>::BYTES)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Map<true>::BYTES)) != cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kCombineSmem)) != cudaSuccess)
+    return e;
   const int Cc_ = 2 * p.h_k * kD + p.h_v * kD;
   CUtensorMap tm_qkv, tm_z;
   if (!make_map_2d(&tm_qkv, p.qkv, (uint64_t)Cc_, (uint64_t)p.total_tokens, kD, RAW_BOX_ROWS) ||
       !make_map_2d(&tm_z, p.z, (uint64_t)p.h_v * kD, (uint64_t)p.total_tokens, kD, C))
     return cudaErrorInvalidValue;
-  prefill_kernel<<<(unsigned)(p.n_seqs * p.h_v), kThreads, SMEM_BYTES, stream>>>(p, tm_qkv, tm_z);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int Cc = 2 * p.h_k * kD + p.h_v * kD;
-  conv_state_kernel<<<dim3((unsigned)((Cc + 255) / 256), (unsigned)p.n_seqs), 256, 0, stream>>>(p);
+  // Split long sequences into segments scanned in parallel only when one CTA
+  // per (sequence, value head) would leave the GPU short of work: the transfer
+  // pass that makes segments independent costs most of a second pass.
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const bool segment = (long long)p.n_seqs * p.h_v < 4LL * sms && p.total_tokens > kSegTokens;
+  p.seg_tokens = segment ? kSegTokens : 0x40000000;
+  const long long slots = segment ? p.total_tokens / kSegTokens : 0;
+  const unsigned units = (unsigned)(slots + p.n_seqs);
+  seg_list_kernel<<<1, 256, 0, stream>>>(p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (slots > 0) {   // some sequence may be longer than one segment
+    chunk_kernel<true><<<units * (unsigned)p.h_v, kThreads, Map<true>::BYTES, stream>>>(p, tm_qkv, tm_z);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    combine_kernel<<<(unsigned)slots * (unsigned)p.h_v * (kD / kCombineRows), 256, kCombineSmem, stream>>>(p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  chunk_kernel<false><<<units * (unsigned)p.h_v, kThreads, Map<false>::BYTES, stream>>>(p, tm_qkv, tm_z);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  conv_state_kernel<<<dim3((unsigned)((Cc_ + 255) / 256), (unsigned)p.n_seqs), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

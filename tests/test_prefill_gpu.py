@@ -67,6 +67,28 @@ def test_prefill_varlen_ragged_short_and_empty(slow):
     print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
 
 
+@pytest.mark.parametrize("slow", [False, True])
+def test_prefill_segment_boundaries(slow):
+    # sequences longer than one segment (1024 tokens) are scanned in parallel
+    # segments whose start states are composed from per-segment transfer maps;
+    # lengths straddle the segment size, and the slow-decay variant makes the
+    # state carry across every boundary
+    lengths = [1024, 1025, 2115, 5, 3000]
+    params, tok, st = _inputs(SH, lengths, 12, slow=slow, ssm_std=0.1 ** 0.5, conv_std=1.0,
+                              norm_w="uniform")
+    e = _check(SH, lengths, params, tok, st)
+    print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
+
+
+def test_prefill_many_sequences_unsegmented():
+    # 20 sequences x 32 value heads fill the GPU, so no sequence is split, even
+    # those longer than a segment; a mix of long, short and empty sequences
+    lengths = [1500, 30, 0, 1100, 64, 65, 3, 700, 1030, 128] * 2
+    params, tok, st = _inputs(SH, lengths, 13, slow=True, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    e = _check(SH, lengths, params, tok, st)
+    print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
+
+
 def test_prefill_single_sequence_4096():
     # T = 4096, zero initial state, seed 2
     params, tok, st = _inputs(SH, [4096], 2)
