@@ -79,6 +79,9 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode_step.restype = ctypes.c_int
             L.gdn_decode_step.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_int] + \
                 [_P] * 3 + [ctypes.c_int, _P, _P]
+            L.gdn_prefill_noalloc.restype = ctypes.c_int
+            L.gdn_prefill_noalloc.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
+                [_P] * 5
             L.gdn_read_device_status.restype = ctypes.c_int
             L.gdn_read_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
             _lib = L
@@ -145,6 +148,28 @@ def gdn_prefill(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, cu_seq
         _ptr(out, bf, "out", T * dims.h_v * dims.d_v), _ptr(workspace, workspace.dtype, "workspace"),
         ws_bytes, _stream(stream))
     _check(st, "gdn_prefill")
+
+
+def gdn_prefill_noalloc(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, cu_seqlens,
+                        conv_state, ssm_state, out, device_status=None, stream=None, n_seqs=None,
+                        total_tokens=None):
+    """gdn_prefill for callers that cannot allocate: no workspace argument; the
+    library's own fixed device array holds the scratch (see include/gdn.h)."""
+    bf, f32 = torch.bfloat16, torch.float32
+    N = int(n_seqs if n_seqs is not None else cu_seqlens.numel() - 1)
+    T = int(total_tokens if total_tokens is not None else qkv.shape[0])
+    Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
+    st = lib().gdn_prefill_noalloc(
+        ctypes.byref(dims), _ptr(qkv, bf, "qkv", T * Cc), _ptr(z, bf, "z", T * dims.h_v * dims.d_v),
+        _ptr(a, bf, "a", T * dims.h_v), _ptr(b, bf, "b", T * dims.h_v),
+        _ptr(A_log, f32, "A_log", dims.h_v), _ptr(dt_bias, f32, "dt_bias", dims.h_v),
+        _ptr(conv_w, bf, "conv_w", Cc * dims.conv_w), _ptr(norm_w, f32, "norm_w", dims.d_v),
+        _ptr(cu_seqlens, torch.int32, "cu_seqlens", N + 1), N, T,
+        _ptr(conv_state, f32, "conv_state", N * (dims.conv_w - 1) * Cc),
+        _ptr(ssm_state, f32, "ssm_state", N * dims.h_v * dims.d_v * dims.d_k),
+        _ptr(out, bf, "out", T * dims.h_v * dims.d_v),
+        _ptr(device_status, torch.int32, "device_status", 1), _stream(stream))
+    _check(st, "gdn_prefill_noalloc")
 
 
 def gdn_decode_step(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,

@@ -54,7 +54,10 @@ struct PrefillArgs {
 // Host launchers: enqueue on `stream`, return the launch error (or
 // cudaSuccess).  Dims are validated by the caller.
 cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream);
-cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream);
+// allow_split = false keeps every sequence in one segment (no transfer maps in
+// the scratch); the scratch then needs only prefill_scratch_bytes_unsplit().
+cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream, bool allow_split = true);
 size_t prefill_scratch_bytes(int n_seqs, int h_k, int h_v, long long total_tokens);
+size_t prefill_scratch_bytes_unsplit(int n_seqs);
 
 }  // namespace gdn

@@ -999,6 +999,8 @@ size_t prefill_scratch_bytes(int n_seqs, int, int h_v, long long total_tokens) {
   return scratch_layout(n_seqs, h_v, total_tokens).total;
 }
 
+size_t prefill_scratch_bytes_unsplit(int n_seqs) { return scratch_layout(n_seqs, 0, 0).total; }
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1030,7 +1032,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 
 }  // namespace
 
-cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream) {
+cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool allow_split) {
   PrefillArgs p = p_in;
   const ScratchLayout l = scratch_layout(p.n_seqs, p.h_v, p.total_tokens);
   char* scratch = static_cast<char*>(p.scratch);
@@ -1058,7 +1060,7 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream) {
   int dev = 0, sms = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const bool segment = (long long)p.n_seqs * p.h_v < 4LL * sms && p.total_tokens > kSegTokens;
+  const bool segment = allow_split && (long long)p.n_seqs * p.h_v < 4LL * sms && p.total_tokens > kSegTokens;
   p.seg_tokens = segment ? kSegTokens : 0x40000000;
   const long long slots = segment ? p.total_tokens / kSegTokens : 0;
   const unsigned units = (unsigned)(slots + p.n_seqs);

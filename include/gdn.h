@@ -163,6 +163,49 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
                            float* ssm_state, void* out, int out_dtype,
                            int32_t* device_status, void* stream);
 
+/*
+ * Prefill for callers that cannot allocate device memory.
+ *
+ * The source pages have no counterpart to this call: it exists for callers
+ * that cannot hand the library a device workspace at the point where they run
+ * the layer -- for instance a step recorded under a strict memory budget, an
+ * allocator that forbids new device allocations after start-up, or a host
+ * framework that gives the layer no allocation hook.  It computes the same
+ * prefill as gdn_prefill (same arguments, layouts and outputs) and allocates
+ * nothing: its scratch -- the device status word and the segment list --
+ * lives in one fixed device array of GDN_NOALLOC_SCRATCH_BYTES bytes inside
+ * the library, which every GPU that loads the library holds until the process
+ * exits.
+ *
+ * Limits and behaviour:
+ *   - n_seqs above GDN_NOALLOC_MAX_SEQS returns GDN_ERR_UNSUPPORTED without
+ *     launching (the fixed array holds no more).
+ *   - Sequences are never split into parallel segments (that needs transfer
+ *     maps far larger than the fixed array), so a batch of few long sequences
+ *     runs slower than through gdn_prefill; the results agree within the
+ *     prefill tolerance.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - All calls share the one array, which keeps the previous call's
+ *     contents; each call clears the status word itself.  Calls whose work
+ *     overlaps on the GPU (other streams, other host threads, concurrent
+ *     graph launches) race on the array and must be serialised by the caller.
+ *   - device_status: NULL, or a device int32 word that receives a copy of the
+ *     call's status word (GDN_OK or the first device-side error) in stream
+ *     order, for gdn_read_device_status.
+ */
+#define GDN_NOALLOC_MAX_SEQS 32768
+#define GDN_NOALLOC_SCRATCH_BYTES 1049344 /* status word + segment list for GDN_NOALLOC_MAX_SEQS */
+
+gdn_status gdn_prefill_noalloc(const gdn_dims* dims, const void* qkv, const void* z,
+                               const void* a, const void* b, const float* A_log,
+                               const float* dt_bias, const void* conv_w,
+                               const float* norm_w, const int32_t* cu_seqlens,
+                               int n_seqs, long long total_tokens, float* conv_state,
+                               float* ssm_state, void* out, int32_t* device_status,
+                               void* stream);
+
 /* Waits for the stream, then reads a device status word (the first 4 bytes
  * of a prefill workspace, or a decode device_status word) into *code:
  * GDN_OK or the first device-side error recorded.  Returns GDN_ERR_CUDA if

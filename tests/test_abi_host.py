@@ -140,6 +140,19 @@ def test_prefill_rejects_bad_arguments(L):
     assert _prefill(L, d, T=0) == OK
 
 
+def test_noalloc_prefill_rejects_more_sequences_than_its_fixed_scratch(L):
+    d = gdn.make_dims()
+    text = open(HEADER).read()
+    max_seqs = int(re.search(r"#define GDN_NOALLOC_MAX_SEQS (\d+)", text).group(1))
+    args = [FAKE] * 9
+    call = lambda n, T: L.gdn_prefill_noalloc(ctypes.byref(d), *args, n, T, FAKE, FAKE, FAKE, None, None)
+    assert call(max_seqs + 1, 1 << 20) == UNSUP
+    assert call(0, 100) == OK                        # nothing to launch
+    assert L.gdn_prefill_noalloc(None, *args, 1, 1, FAKE, FAKE, FAKE, None, None) == INVALID
+    assert L.gdn_prefill_noalloc(ctypes.byref(gdn.make_dims(d_k=64, d_v=64)), *args, 1, 1, FAKE,
+                                 FAKE, FAKE, None, None) == UNSUP
+
+
 def test_binding_checks_tensor_arguments(L):
     import torch
     d = gdn.make_dims()
