@@ -80,6 +80,38 @@ def test_prefill_segment_boundaries(slow):
     print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
 
 
+def test_prefill_segments_carry_state_with_near_unit_decay():
+    # with exp(g) in (0.999, 1) and small write gates the state a segment starts
+    # from still matters a thousand tokens later, so a wrong transfer map or a
+    # wrong composition of maps shows in the outputs and the final state
+    lengths = [3000, 1500, 10]
+    T = sum(lengths)
+    params = gi.make_params(SH, 14, norm_w="uniform")
+    tok = gi.make_tokens(SH, T, 14)
+    gc = gi.gate_controlled(SH, T, 14, decay=(0.999, 1.0), beta=(0.0, 0.05))
+    tok["a"], tok["b"] = gc["a"], gc["b"]
+    params["A_log"], params["dt_bias"] = gc["A_log"], gc["dt_bias"]
+    st = gi.make_states(SH, len(lengths), 14, ssm_std=1.0, conv_std=1.0)
+    e = _check(SH, lengths, params, tok, st)
+    print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
+
+
+def test_prefill_zero_write_no_decay_keeps_state_bitwise_across_segments():
+    # beta = 0 and exp(g) = 1: every chunk and every segment's transfer map is
+    # exactly the identity, so the state comes back bit for bit, whether or not
+    # the sequence was split
+    lengths = [2600, 40]
+    params, tok, st = _inputs(SH, lengths, 15, ssm_std=0.3, conv_std=1.0)
+    params["A_log"] = torch.full((SH.h_v,), -100.0)
+    tok["b"] = torch.full_like(tok["b"], -100.0)
+    out, conv, ssm, status = _run(SH, lengths, params, tok, st)
+    assert status == 0
+    assert torch.equal(ssm.cpu(), st["ssm_state"])
+    ref, _, _ = oracle_layer(SH, tok, params, gi.cu_seqlens(lengths),
+                             conv_state=st["conv_state"], ssm_state=st["ssm_state"])
+    assert rel_err(out, ref) <= PREFILL_TOL
+
+
 def test_prefill_many_sequences_unsegmented():
     # 20 sequences x 32 value heads fill the GPU, so no sequence is split, even
     # those longer than a segment; a mix of long, short and empty sequences
