@@ -899,18 +899,31 @@ __global__ void __launch_bounds__(256) seg_list_kernel(PrefillArgs p) {
   }
 }
 
-// Combines the transfer maps of a multi-segment sequence, 16 state rows per
+// Combines the transfer maps of a multi-segment sequence, 32 state rows per
 // CTA (the rows of S evolve independently): S_{sigma+1} = S_sigma X_sigma +
 // S_sigma^0, in fp32, written over the slot's end state, after saving the
 // sequence's initial state (so the output pass never reads a state that the
-// last segment's CTA is writing).
-constexpr int kCombineRows = 16;
-constexpr uint32_t kCombineSmem = (kD * kD + kCombineRows * kD) * 4;
+// last segment's CTA is writing).  The 64 KB maps stream through two shared
+// buffers by bulk TMA copies, the next one landing while the current step
+// computes.
+constexpr int kCombineRows = 32;
+constexpr uint32_t kMapBytes = kD * kD * 4;
+constexpr uint32_t kCombineSmem = 2 * kMapBytes + kCombineRows * kD * 4 + 16;
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* mbar) {
+  mbar_expect_tx(mbar, bytes);
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          tc::smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(tc::smem_u32(mbar))
+      : "memory");
+}
 
 __global__ void __launch_bounds__(256) combine_kernel(PrefillArgs p) {
-  extern __shared__ float csm[];
-  float* Xs = csm;                 // [128][128]
-  float* Sr = csm + kD * kD;       // [16][128]
+  extern __shared__ __align__(128) float csm[];
+  float* Xs = csm;                        // two [128][128] buffers
+  float* Sr = csm + 2 * kD * kD;          // [32][128]
+  __shared__ __align__(8) uint64_t mbar[2];
   const int per = p.h_v * (kD / kCombineRows);
   const int u = blockIdx.x / per, rem = blockIdx.x % per;
   const int h = rem / (kD / kCombineRows), rb = rem % (kD / kCombineRows);
@@ -919,6 +932,20 @@ __global__ void __launch_bounds__(256) combine_kernel(PrefillArgs p) {
   const int n = e[0], k0 = e[1], nsig = e[2];
   const int r0 = rb * kCombineRows;
   const int tid = threadIdx.x;
+  const int steps = nsig - 1;
+  if (tid == 0) {
+    tc::mbar_init(&mbar[0], 1);
+    tc::mbar_init(&mbar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  // copies issued / waited per buffer (the same on every thread: tid 0 issues
+  // under conditions every thread evaluates alike)
+  int issued[2] = {1, steps > 1 ? 1 : 0}, waited[2] = {0, 0};
+  if (tid == 0) {
+    bulk_load(Xs, xfer_ptr(p, k0, h, 0), kMapBytes, &mbar[0]);
+    if (steps > 1) bulk_load(Xs + kD * kD, xfer_ptr(p, k0 + 1, h, 0), kMapBytes, &mbar[1]);
+  }
   const float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
   float* init = xfer_ptr(p, k0, h, 2);
   for (int i = tid; i < kCombineRows * kD / 4; i += 256) {
@@ -926,34 +953,66 @@ __global__ void __launch_bounds__(256) combine_kernel(PrefillArgs p) {
     reinterpret_cast<float4*>(Sr)[i] = v;
     reinterpret_cast<float4*>(init + (size_t)r0 * kD)[i] = v;
   }
-  const int i = tid >> 4, c0 = (tid & 15) * 8;   // this thread: row i, columns c0 .. c0+7
-  for (int sg = 0; sg + 1 < nsig; ++sg) {
-    const float* Xg = xfer_ptr(p, k0 + sg, h, 0);
+  const int i = (tid >> 4) * 2, c0 = (tid & 15) * 8;   // this thread: rows i, i+1; columns c0 .. c0+7
+  float4 b[2][2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float* Bn = xfer_ptr(p, k0, h, 1) + (size_t)(r0 + i + r) * kD + c0;
+    b[r][0] = reinterpret_cast<const float4*>(Bn)[0];
+    b[r][1] = reinterpret_cast<const float4*>(Bn)[1];
+  }
+  bool ok = true;
+  for (int sg = 0; sg < steps; ++sg) {
     float* Sg = xfer_ptr(p, k0 + sg, h, 1);
-    __syncthreads();   // previous step's readers of Xs/Sr are done
-    for (int q = tid; q < kD * kD / 4; q += 256)
-      reinterpret_cast<float4*>(Xs)[q] = reinterpret_cast<const float4*>(Xg)[q];
-    __syncthreads();
-    float acc[8];
-    const float4 b0 = reinterpret_cast<const float4*>(Sg + (size_t)(r0 + i) * kD + c0)[0];
-    const float4 b1 = reinterpret_cast<const float4*>(Sg + (size_t)(r0 + i) * kD + c0)[1];
-    acc[0] = b0.x; acc[1] = b0.y; acc[2] = b0.z; acc[3] = b0.w;
-    acc[4] = b1.x; acc[5] = b1.y; acc[6] = b1.z; acc[7] = b1.w;
+    float acc[2][8];
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      acc[r][0] = b[r][0].x; acc[r][1] = b[r][0].y; acc[r][2] = b[r][0].z; acc[r][3] = b[r][0].w;
+      acc[r][4] = b[r][1].x; acc[r][5] = b[r][1].y; acc[r][6] = b[r][1].z; acc[r][7] = b[r][1].w;
+    }
+    if (sg + 1 < steps) {   // next step's end-state rows, into registers
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float* Bn = xfer_ptr(p, k0 + sg + 1, h, 1) + (size_t)(r0 + i + r) * kD + c0;
+        b[r][0] = reinterpret_cast<const float4*>(Bn)[0];
+        b[r][1] = reinterpret_cast<const float4*>(Bn)[1];
+      }
+    }
+    ok = tc::mbar_wait(&mbar[sg & 1], (uint32_t)((sg >> 1) & 1), kWaitBudget);
+    if (!__syncthreads_and(ok)) break;   // also: the initial rows of Sr are in place
+    ++waited[sg & 1];
+    const float* X = Xs + (sg & 1) * kD * kD;
 #pragma unroll 4
     for (int j = 0; j < kD; ++j) {
-      const float sv = Sr[i * kD + j];
-      const float4 x0 = reinterpret_cast<const float4*>(Xs + j * kD + c0)[0];
-      const float4 x1 = reinterpret_cast<const float4*>(Xs + j * kD + c0)[1];
-      acc[0] = fmaf(sv, x0.x, acc[0]); acc[1] = fmaf(sv, x0.y, acc[1]);
-      acc[2] = fmaf(sv, x0.z, acc[2]); acc[3] = fmaf(sv, x0.w, acc[3]);
-      acc[4] = fmaf(sv, x1.x, acc[4]); acc[5] = fmaf(sv, x1.y, acc[5]);
-      acc[6] = fmaf(sv, x1.z, acc[6]); acc[7] = fmaf(sv, x1.w, acc[7]);
-    }
-    __syncthreads();   // all reads of Sr done before it is overwritten
+      const float s0 = Sr[i * kD + j], s1 = Sr[(i + 1) * kD + j];
+      const float4 x0 = reinterpret_cast<const float4*>(X + j * kD + c0)[0];
+      const float4 x1 = reinterpret_cast<const float4*>(X + j * kD + c0)[1];
+      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-    for (int q = 0; q < 8; ++q) Sr[i * kD + c0 + q] = acc[q];
-    reinterpret_cast<float4*>(Sg + (size_t)(r0 + i) * kD + c0)[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    reinterpret_cast<float4*>(Sg + (size_t)(r0 + i) * kD + c0)[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      for (int q = 0; q < 8; ++q) {
+        acc[0][q] = fmaf(s0, xv[q], acc[0][q]);
+        acc[1][q] = fmaf(s1, xv[q], acc[1][q]);
+      }
+    }
+    __syncthreads();   // every read of Sr and of this buffer is done
+    if (sg + 2 < steps) {
+      if (tid == 0) bulk_load(Xs + (sg & 1) * kD * kD, xfer_ptr(p, k0 + sg + 2, h, 0), kMapBytes, &mbar[sg & 1]);
+      ++issued[sg & 1];
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) Sr[(i + r) * kD + c0 + q] = acc[r][q];
+      float4* dst = reinterpret_cast<float4*>(Sg + (size_t)(r0 + i + r) * kD + c0);
+      dst[0] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+      dst[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
+    }
+  }
+  if (!ok) {
+    if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+    // the map copies this CTA started must land (bounded) before its smem goes away
+    for (int q = 0; q < 2; ++q)
+      for (; waited[q] < issued[q]; ++waited[q]) tc::mbar_wait(&mbar[q], (uint32_t)(waited[q] & 1), kWaitBudget);
   }
 }
 
