@@ -47,7 +47,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
 constexpr int C = kChunk;
 constexpr int kSegTokens = 1024;   // segment length when long sequences are split (see launch_prefill)
 
@@ -319,12 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = tmem_base_s;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
   const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
-  const int half = warp >> 2;               // which half of the columns
+  const int part = warp >> 2;               // which quarter of a lane quarter's columns
 
   // initial state(s): fp32 into TMEM, bf16 into the operand tile(s)
-#pragma unroll
-  for (int c32 = 0; c32 < 2; ++c32) {
-    const int col0 = half * 64 + c32 * 32;
+  {
+    const int col0 = part * 32;
     float v[32];
     if (!kXfer) {
       const float4* src = reinterpret_cast<const float4*>(S_init + (size_t)row * kD + col0);
@@ -432,20 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!__syncthreads_and(tc::mbar_wait(&mbar_raw, chunk_parity, kWaitBudget))) { aborted = true; break; }
     raw_pending = false;
 
-    // ---- conv + SiLU + L2 norms -> K^, Q^, V tiles (all warps, a token per warp step,
-    //      two tokens in flight per warp); the transfer pass needs no q ----
+    // ---- conv + SiLU + L2 norms -> K^, Q^, V tiles (a token per warp step, the
+    //      16 warps interleaving); the transfer pass needs no q ----
     constexpr int kB0 = kXfer ? 1 : 0;
 #pragma unroll 1
-    for (int tb = warp; tb < C; tb += 2 * (kThreads / 32)) {
-      float y[2][3][4];
+    for (int t = warp; t < C; t += kThreads / 32) {
+      float y[3][4];
 #pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-        const int t = tb + uu * (kThreads / 32);
+      for (int blk = 0; blk < 3; ++blk)
 #pragma unroll
-        for (int blk = 0; blk < 3; ++blk)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) y[uu][blk][e] = 0.0f;
-        if (t >= L) continue;
+        for (int e = 0; e < 4; ++e) y[blk][e] = 0.0f;
+      if (t < L) {
 #pragma unroll
         for (int j = 0; j < kConvW; ++j) {
           const int tau = t0 + t - (kConvW - 1) + j;   // position in the sequence
@@ -464,50 +460,39 @@ __global__ void __launch_bounds__(kThreads, 1)
               x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
             }
             const float4 w4 = cwr[blk][j];
-            y[uu][blk][0] = fmaf(w4.x, x[0], y[uu][blk][0]);
-            y[uu][blk][1] = fmaf(w4.y, x[1], y[uu][blk][1]);
-            y[uu][blk][2] = fmaf(w4.z, x[2], y[uu][blk][2]);
-            y[uu][blk][3] = fmaf(w4.w, x[3], y[uu][blk][3]);
+            y[blk][0] = fmaf(w4.x, x[0], y[blk][0]);
+            y[blk][1] = fmaf(w4.y, x[1], y[blk][1]);
+            y[blk][2] = fmaf(w4.z, x[2], y[blk][2]);
+            y[blk][3] = fmaf(w4.w, x[3], y[blk][3]);
           }
         }
 #pragma unroll
-        for (int blk = kB0; blk < 3; ++blk) silu4(y[uu][blk]);
+        for (int blk = kB0; blk < 3; ++blk) silu4(y[blk]);
       }
-      float ss[2][2];
+      float sq = y[0][0] * y[0][0], sk = y[1][0] * y[1][0];
 #pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-        ss[uu][0] = y[uu][0][0] * y[uu][0][0];
-        ss[uu][1] = y[uu][1][0] * y[uu][1][0];
-#pragma unroll
-        for (int e = 1; e < 4; ++e) {
-          ss[uu][0] = fmaf(y[uu][0][e], y[uu][0][e], ss[uu][0]);
-          ss[uu][1] = fmaf(y[uu][1][e], y[uu][1][e], ss[uu][1]);
-        }
+      for (int e = 1; e < 4; ++e) {
+        sq = fmaf(y[0][e], y[0][e], sq);
+        sk = fmaf(y[1][e], y[1][e], sk);
       }
 #pragma unroll
-      for (int m = 16; m >= 1; m >>= 1)
+      for (int m = 16; m >= 1; m >>= 1) {
+        if (!kXfer) sq += __shfl_xor_sync(0xffffffffu, sq, m);
+        sk += __shfl_xor_sync(0xffffffffu, sk, m);
+      }
+      const float rq = rsqrtf(sq + p.l2_eps) * qscale, rk = rsqrtf(sk + p.l2_eps);
 #pragma unroll
-        for (int uu = 0; uu < 2; ++uu) {
-          if (!kXfer) ss[uu][0] += __shfl_xor_sync(0xffffffffu, ss[uu][0], m);
-          ss[uu][1] += __shfl_xor_sync(0xffffffffu, ss[uu][1], m);
-        }
-#pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-        const int t = tb + uu * (kThreads / 32);
-        const float rq = rsqrtf(ss[uu][0] + p.l2_eps) * qscale, rk = rsqrtf(ss[uu][1] + p.l2_eps);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          y[uu][0][e] *= rq;
-          y[uu][1][e] *= rk;
-        }
-        const uint32_t o16 = tc::sw128_off(t, 4 * lane, 16384), o8 = tc::sw128_off(t, 4 * lane, 8192);
-        store_bf16x4(sm.base + M::KQ, o16, y[uu][1][0], y[uu][1][1], y[uu][1][2], y[uu][1][3]);
-        store_bf16x4(sm.base + M::V, o8, y[uu][2][0], y[uu][2][1], y[uu][2][2], y[uu][2][3]);
-        store_f16x4(sm.base + M::KQ16, o16, y[uu][1][0], y[uu][1][1], y[uu][1][2], y[uu][1][3]);
-        if (!kXfer) {
-          store_bf16x4(sm.base + M::KQ + 8192, o16, y[uu][0][0], y[uu][0][1], y[uu][0][2], y[uu][0][3]);
-          store_f16x4(sm.base + M::KQ16 + 8192, o16, y[uu][0][0], y[uu][0][1], y[uu][0][2], y[uu][0][3]);
-        }
+      for (int e = 0; e < 4; ++e) {
+        y[0][e] *= rq;
+        y[1][e] *= rk;
+      }
+      const uint32_t o16 = tc::sw128_off(t, 4 * lane, 16384), o8 = tc::sw128_off(t, 4 * lane, 8192);
+      store_bf16x4(sm.base + M::KQ, o16, y[1][0], y[1][1], y[1][2], y[1][3]);
+      store_bf16x4(sm.base + M::V, o8, y[2][0], y[2][1], y[2][2], y[2][3]);
+      store_f16x4(sm.base + M::KQ16, o16, y[1][0], y[1][1], y[1][2], y[1][3]);
+      if (!kXfer) {
+        store_bf16x4(sm.base + M::KQ + 8192, o16, y[0][0], y[0][1], y[0][2], y[0][3]);
+        store_f16x4(sm.base + M::KQ16 + 8192, o16, y[0][0], y[0][1], y[0][2], y[0][3]);
       }
     }
     sync_for_mma();
@@ -535,10 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float dC = eg[C - 1];
 #pragma unroll
       for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
-#pragma unroll
-        for (int c32 = 0; c32 < 2; ++c32) {
+        {
           float v[32];
-          const uint32_t ta = tmem + lane_base + (zz ? TM_ZX : TM_Z) + half * 64 + c32 * 32;
+          const uint32_t ta = tmem + lane_base + (zz ? TM_ZX : TM_Z) + part * 32;
           tc::tmem_ld32(ta, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= dC;
@@ -551,26 +535,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- A (fp32, lanes 0-63) and P (bf16 tile, lanes 64-127) from the Gram rows;
     //      warps w and w+4 share a lane quarter and split its 64 columns ----
     if (!kXfer || (warp & 3) < 2) {
-      float v[32];
+      float v[16];
       const int t = row & 63;
       const float gt = gam[t];
-      const int c0 = half * 32;
-      tc::tmem_ld32(tmem + lane_base + TM_G + c0, v);
+      const int c0 = part * 16;
+      tc::tmem_ld16(tmem + lane_base + TM_G + c0, v);
       if ((warp & 3) < 2) {
         const float bt = bet[t];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
           const int s = c0 + i;
           Af[t * LDA + s] = s < t ? bt * __expf(gt - gam[s]) * v[i] : 0.0f;
         }
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < 16; ++i) {
           const int s = c0 + i;
           v[i] = s <= t ? v[i] * __expf(gt - gam[s]) : 0.0f;
         }
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
+        for (int m = 0; m < 2; ++m)
           store_bf16x8(sm.base + M::P, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
       }
     }
@@ -664,12 +648,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- -W tile [t][d_k] from W^T (lane = d_k index) ----
     {
-      float v[32];
-      tc::tmem_ld32(tmem + lane_base + TM_W + half * 32, v);
+      float v[16];
+      tc::tmem_ld16(tmem + lane_base + TM_W + part * 16, v);
       uint8_t* wn = sm.base + M::WN;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int t = half * 32 + i;
+      for (int i = 0; i < 16; ++i) {
+        const int t = part * 16 + i;
         *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(t, row, 8192)) = f32_to_bf16(-v[i]);
       }
     }
@@ -706,18 +690,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- Vn^T tiles (plain and decay-weighted), row = d_v index ----
     {
-      float v[32], vs[32];
-      tc::tmem_ld32(tmem + lane_base + TM_U + half * 32, v);
+      float v[16], vs[16];
+      tc::tmem_ld16(tmem + lane_base + TM_U + part * 16, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) vs[i] = v[i] * egc[half * 32 + i];
+      for (int i = 0; i < 16; ++i) vs[i] = v[i] * egc[part * 16 + i];
       if (kXfer) {
-        tc::tmem_ld32(tmem + lane_base + TM_VX + half * 32, v);
+        tc::tmem_ld16(tmem + lane_base + TM_VX + part * 16, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= egc[half * 32 + i];
+        for (int i = 0; i < 16; ++i) v[i] *= egc[part * 16 + i];
       }
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const uint32_t off = tc::sw128_off(row, half * 32 + 8 * m, 0);
+      for (int m = 0; m < 2; ++m) {
+        const uint32_t off = tc::sw128_off(row, part * 16 + 8 * m, 0);
         store_bf16x8(sm.base + M::VN, off, v + 8 * m);
         store_bf16x8(sm.base + M::VNS, off, vs + 8 * m);
       }
@@ -755,23 +739,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     {
 #pragma unroll
       for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
-#pragma unroll
-        for (int c32 = 0; c32 < 2; ++c32) {
+        {
           float v[32];
-          tc::tmem_ld32(tmem + lane_base + (zz ? TM_ZX : TM_Z) + half * 64 + c32 * 32, v);
+          tc::tmem_ld32(tmem + lane_base + (zz ? TM_ZX : TM_Z) + part * 32, v);
 #pragma unroll
           for (int m = 0; m < 4; ++m)
-            store_bf16x8(sm.base + (zz ? M::X : M::S), tc::sw128_off(row, half * 64 + c32 * 32 + 8 * m, 16384),
-                         v + 8 * m);
+            store_bf16x8(sm.base + (zz ? M::X : M::S), tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
         }
       }
       if (!kXfer) {
-        float o1[32], o2[32];
-        tc::tmem_ld32(tmem + lane_base + TM_O1 + half * 32, o1);
-        tc::tmem_ld32(tmem + lane_base + TM_O2 + half * 32, o2);
+        float o1[16], o2[16];
+        tc::tmem_ld16(tmem + lane_base + TM_O1 + part * 16, o1);
+        tc::tmem_ld16(tmem + lane_base + TM_O2 + part * 16, o2);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int t = half * 32 + i;
+        for (int i = 0; i < 16; ++i) {
+          const int t = part * 16 + i;
           Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
         }
       }
@@ -816,14 +798,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int zz = 0; zz < 2; ++zz) {
       float* dst_base = kXfer ? xfer_ptr(p, sg.k0 + sg.sigma, h, zz == 0 ? 1 : 0) : (zz == 0 ? S_final : nullptr);
       if (dst_base == nullptr) continue;
-      float4* dst = reinterpret_cast<float4*>(dst_base + (size_t)row * kD + half * 64);
-#pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
+      float4* dst = reinterpret_cast<float4*>(dst_base + (size_t)row * kD + part * 32);
+      {
         float v[32];
-        tc::tmem_ld32(tmem + lane_base + (zz ? TM_ZX : TM_Z) + half * 64 + c32 * 32, v);
+        tc::tmem_ld32(tmem + lane_base + (zz ? TM_ZX : TM_Z) + part * 32, v);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[c32 * 8 + q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       }
     }
   }
