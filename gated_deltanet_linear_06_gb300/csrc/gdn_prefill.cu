@@ -49,6 +49,7 @@ namespace {
 
 constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
 constexpr int C = kChunk;
+static_assert(kThreads / 32 * 4 == C, "the conv stage gives each warp a quad of a chunk's tokens");
 constexpr int kSegTokens = 1024;   // segment length when long sequences are split (see launch_prefill)
 
 // ---- shared memory maps (bytes from a 1024-aligned base), per pass ----
@@ -350,11 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  float4 cwr[3][kConvW];   // this lane's 4 channels of each block, per tap
-#pragma unroll
-  for (int blk = 0; blk < 3; ++blk)
-#pragma unroll
-    for (int j = 0; j < kConvW; ++j) cwr[blk][j] = reinterpret_cast<const float4*>(cw + (blk * 4 + j) * kD)[lane];
   const float A_exp = __expf(p.A_log[h]);
   const float dtb = p.dt_bias[h];
   const float qscale = rsqrtf((float)kD);
@@ -431,68 +427,90 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (!__syncthreads_and(tc::mbar_wait(&mbar_raw, chunk_parity, kWaitBudget))) { aborted = true; break; }
     raw_pending = false;
 
-    // ---- conv + SiLU + L2 norms -> K^, Q^, V tiles (a token per warp step, the
-    //      16 warps interleaving); the transfer pass needs no q ----
-    constexpr int kB0 = kXfer ? 1 : 0;
-#pragma unroll 1
-    for (int t = warp; t < C; t += kThreads / 32) {
-      float y[3][4];
+    // ---- conv + SiLU + L2 norms -> K^, Q^, V tiles.  Warp w takes tokens 4w .. 4w+3
+    //      of every block and a lane 4 channels of them, so each raw row is read once
+    //      for all the taps that use it and the four tokens are independent work;
+    //      the transfer pass needs no q ----
+    {
+      constexpr int kB0 = kXfer ? 1 : 0;
+      constexpr int kRows = 4 + kConvW - 1;   // raw rows under a token quad
+      const int tq = 4 * warp;
 #pragma unroll
-      for (int blk = 0; blk < 3; ++blk)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) y[blk][e] = 0.0f;
-      if (t < L) {
+      for (int blk = kB0; blk < 3; ++blk) {
+        float w[kConvW][4];
 #pragma unroll
         for (int j = 0; j < kConvW; ++j) {
-          const int tau = t0 + t - (kConvW - 1) + j;   // position in the sequence
+          const float4 w4 = reinterpret_cast<const float4*>(cw + (blk * 4 + j) * kD)[lane];
+          w[j][0] = w4.x; w[j][1] = w4.y; w[j][2] = w4.z; w[j][3] = w4.w;
+        }
+        float x[kRows][4];
 #pragma unroll
-          for (int blk = kB0; blk < 3; ++blk) {
-            float x[4];
-            if (tau >= 0) {
-              const uint2 r = *reinterpret_cast<const uint2*>(sm.base + M::RAW + blk * RAW_BLK +
-                                                              (t + j) * 256 + lane * 8);
-              x[0] = bf16_to_f32(r.x & 0xffffu); x[1] = bf16_to_f32(r.x >> 16);
-              x[2] = bf16_to_f32(r.y & 0xffffu); x[3] = bf16_to_f32(r.y >> 16);
-            } else {
-              const int ch = (blk == 0 ? kh * kD : blk == 1 ? Cq + kh * kD : 2 * Cq + h * kD) + 4 * lane;
-              const float4 r = *reinterpret_cast<const float4*>(
-                  p.conv_state + ((size_t)n * (kConvW - 1) + (kConvW - 1 + tau)) * Cc + ch);
-              x[0] = r.x; x[1] = r.y; x[2] = r.z; x[3] = r.w;
-            }
-            const float4 w4 = cwr[blk][j];
-            y[blk][0] = fmaf(w4.x, x[0], y[blk][0]);
-            y[blk][1] = fmaf(w4.y, x[1], y[blk][1]);
-            y[blk][2] = fmaf(w4.z, x[2], y[blk][2]);
-            y[blk][3] = fmaf(w4.w, x[3], y[blk][3]);
+        for (int r = 0; r < kRows; ++r) {
+          const int tau = t0 + tq - (kConvW - 1) + r;   // position in the sequence
+          if (tau >= 0) {
+            const uint2 v2 = *reinterpret_cast<const uint2*>(sm.base + M::RAW + blk * RAW_BLK + (tq + r) * 256 +
+                                                             lane * 8);
+            x[r][0] = bf16_to_f32(v2.x & 0xffffu); x[r][1] = bf16_to_f32(v2.x >> 16);
+            x[r][2] = bf16_to_f32(v2.y & 0xffffu); x[r][3] = bf16_to_f32(v2.y >> 16);
+          } else {   // before the sequence's first token of this call: the carried conv state
+            const int ch = (blk == 0 ? kh * kD : blk == 1 ? Cq + kh * kD : 2 * Cq + h * kD) + 4 * lane;
+            const float4 v4 = *reinterpret_cast<const float4*>(
+                p.conv_state + ((size_t)n * (kConvW - 1) + (kConvW - 1 + tau)) * Cc + ch);
+            x[r][0] = v4.x; x[r][1] = v4.y; x[r][2] = v4.z; x[r][3] = v4.w;
+          }
+        }
+        float y[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float acc = w[0][e] * x[i][e];
+#pragma unroll
+            for (int j = 1; j < kConvW; ++j) acc = fmaf(w[j][e], x[i + j][e], acc);
+            y[i][e] = tq + i < L ? acc : 0.0f;   // padding tokens of a partial chunk are zero
+          }
+          silu4(y[i]);
+        }
+        if (blk < 2) {
+          // the four tokens' sums of squares over the 128 channels: the first two
+          // butterfly steps each hand half of the sums to the partner lane, so a
+          // lane ends with the full sum of token 2 (lane bit 4) + (lane bit 3)
+          float ss[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            ss[i] = y[i][0] * y[i][0];
+#pragma unroll
+            for (int e = 1; e < 4; ++e) ss[i] = fmaf(y[i][e], y[i][e], ss[i]);
+          }
+          const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
+          float k0 = hi16 ? ss[2] : ss[0], k1 = hi16 ? ss[3] : ss[1];
+          const float s0 = hi16 ? ss[0] : ss[2], s1 = hi16 ? ss[1] : ss[3];
+          k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+          k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+          float tot = hi8 ? k1 : k0;
+          tot += __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
+          tot += __shfl_xor_sync(0xffffffffu, tot, 4);
+          tot += __shfl_xor_sync(0xffffffffu, tot, 2);
+          tot += __shfl_xor_sync(0xffffffffu, tot, 1);
+          const float rn = rsqrtf(tot + p.l2_eps) * (blk == 0 ? qscale : 1.0f);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float ri = __shfl_sync(0xffffffffu, rn, ((i >> 1) << 4) | ((i & 1) << 3));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) y[i][e] *= ri;
           }
         }
 #pragma unroll
-        for (int blk = kB0; blk < 3; ++blk) silu4(y[blk]);
-      }
-      float sq = y[0][0] * y[0][0], sk = y[1][0] * y[1][0];
-#pragma unroll
-      for (int e = 1; e < 4; ++e) {
-        sq = fmaf(y[0][e], y[0][e], sq);
-        sk = fmaf(y[1][e], y[1][e], sk);
-      }
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) {
-        if (!kXfer) sq += __shfl_xor_sync(0xffffffffu, sq, m);
-        sk += __shfl_xor_sync(0xffffffffu, sk, m);
-      }
-      const float rq = rsqrtf(sq + p.l2_eps) * qscale, rk = rsqrtf(sk + p.l2_eps);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        y[0][e] *= rq;
-        y[1][e] *= rk;
-      }
-      const uint32_t o16 = tc::sw128_off(t, 4 * lane, 16384), o8 = tc::sw128_off(t, 4 * lane, 8192);
-      store_bf16x4(sm.base + M::KQ, o16, y[1][0], y[1][1], y[1][2], y[1][3]);
-      store_bf16x4(sm.base + M::V, o8, y[2][0], y[2][1], y[2][2], y[2][3]);
-      store_f16x4(sm.base + M::KQ16, o16, y[1][0], y[1][1], y[1][2], y[1][3]);
-      if (!kXfer) {
-        store_bf16x4(sm.base + M::KQ + 8192, o16, y[0][0], y[0][1], y[0][2], y[0][3]);
-        store_f16x4(sm.base + M::KQ16 + 8192, o16, y[0][0], y[0][1], y[0][2], y[0][3]);
+        for (int i = 0; i < 4; ++i) {
+          const int t = tq + i;
+          if (blk == 2) {
+            store_bf16x4(sm.base + M::V, tc::sw128_off(t, 4 * lane, 8192), y[i][0], y[i][1], y[i][2], y[i][3]);
+          } else {
+            const uint32_t o16 = tc::sw128_off(t, 4 * lane, 16384) + (blk == 0 ? 8192u : 0u);
+            store_bf16x4(sm.base + M::KQ, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
+            store_f16x4(sm.base + M::KQ16, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
+          }
+        }
       }
     }
     sync_for_mma();
