@@ -341,12 +341,13 @@ def run_ours(args) -> dict | None:
     if rank != 0:
         return None
 
-    # kernels one gdn_prefill call launches: the work list, the output pass and the
-    # conv-state hand-off, plus the transfer and combine passes when the single
-    # sequence x 32 heads leaves the GPU short of CTAs and sequences are split
+    # kernels one gdn_prefill call launches: the work list, the prep pass, the
+    # output scan and the conv-state hand-off, plus the transfer scan and the
+    # combine pass when the single sequence x 32 heads leaves the GPU short of
+    # CTAs and sequences are split into segments
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     split = 1 * H_V < 4 * sms and PREFILL_T > 1024
-    prefill_kernels = 5 if split else 3
+    prefill_kernels = 6 if split else 4
     hbm = float(peaks["hbm_gbs"])
     tc_peak = float(peaks["bf16_tflops"])
     pre_bytes = PREFILL_T * PREFILL_BYTES_PER_TOKEN + 2 * STATE_BYTES

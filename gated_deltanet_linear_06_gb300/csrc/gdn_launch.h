@@ -46,6 +46,11 @@ struct PrefillArgs {
   int* seg_list;           // [count, pad x3][units][8]: the segments of every sequence
   int* multi_list;         // [count, pad x3][slots][4]: sequences longer than one segment
   float* xfer;             // per boundary slot and value head: transfer map, end state, initial state
+  int* chunk_off;          // [n_seqs + 1]: first chunk record of each sequence (split path; else null)
+  int2* chunk_list;        // [max_chunks]: (sequence, first token) of each chunk record, sequence -1 past the end
+  uint8_t* rec_kq;         // [max_chunks][h_k] per-chunk key/query tile records
+  uint8_t* rec_v;          // [max_chunks][h_v] per-chunk value-head records
+  int max_chunks;          // chunk records the workspace holds: total_tokens / 64 + n_seqs
   int n_seqs, h_k, h_v;
   long long total_tokens;
   float l2_eps, rms_eps;

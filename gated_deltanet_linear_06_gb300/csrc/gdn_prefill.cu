@@ -1,6 +1,14 @@
-// gdn_prefill.cu -- chunked prefill of the Gated DeltaNet layer (sm_103a).
+// gdn_prefill.cu -- chunked prefill of the Gated DeltaNet layer (sm_103a):
+// the launcher, the work list, the combine pass of segmented sequences, the
+// conv-state update, and the single-pass kernel.
 //
-// One CTA per (sequence, value head) walks that sequence in chunks of C = 64
+// gdn_prefill runs the split path (gdn_prefill_split.cu): a chunk-parallel
+// prep pass writes per-chunk records to the workspace, then state scans walk
+// the chunks.  The single-pass kernel below does everything in one CTA per
+// (sequence, value head) with no records, for callers without a workspace
+// (gdn_prefill_noalloc); the arithmetic is the same.
+//
+// The single pass walks a sequence in chunks of C = 64
 // tokens, keeping the head's state S (d_v x d_k = 128 x 128, fp32) in tensor
 // memory across chunks.  Per chunk, with q^, k^, v the conv+SiLU+normalised
 // inputs, gamma_t = sum_{s<=t} g_s the cumulative log-decay inside the chunk
@@ -43,26 +51,19 @@
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 #include "gdn_tc.cuh"
+#include "gdn_prefill.cuh"
 
 namespace gdn {
 namespace {
 
 constexpr int kThreads = 512;   // 16 warps: 4 per TMEM lane quarter
-constexpr int C = kChunk;
 static_assert(kThreads / 32 * 4 == C, "the conv stage gives each warp a quad of a chunk's tokens");
-constexpr int kSegTokens = 1024;   // segment length when long sequences are split (see launch_prefill)
 
-// ---- shared memory maps (bytes from a 1024-aligned base), per pass ----
-// Output pass: the layer over a token range, from a given state.
-// Transfer pass: the same chunk algebra run twice side by side with no
-// output -- S from 0 with the real inputs and X from the identity with v = 0 --
-// which yields the range's affine state map S_end = S_start X_end + S_end(0).
-template <bool kXfer> struct Lay;
-template <> struct Lay<false> {
+// ---- shared memory map (bytes from a 1024-aligned base) ----
+struct Lay {
   static constexpr uint32_t KQ = 0;        // [kb0: K^ | Q^][kb1: K^ | Q^], 8 KB each (64 rows x 128 B)
   static constexpr uint32_t V = 32768;     // V [t][d_v], 64-column blocks 8 KB apart
   static constexpr uint32_t S = 49152;     // S bf16 [d_v][d_k], K blocks 16 KB apart
-  static constexpr uint32_t X = 0;         // (unused)
   static constexpr uint32_t VN = 81920;    // Vn^T [d_v][t]
   static constexpr uint32_t VNS = 98304;   // Vn^T diag(e^{gamma_C - gamma}) [d_v][t]
   static constexpr uint32_t KQ16 = VN;     // fp16 copy of KQ for the Gram MMA (dead before Vn^T is written)
@@ -72,21 +73,6 @@ template <> struct Lay<false> {
   static constexpr uint32_t P = 147456;    // P [t][s]
   static constexpr uint32_t F32 = 155648;  // fp32: A [64][65] + T [64][65]
 };
-template <> struct Lay<true> {
-  static constexpr uint32_t KQ = 0;        // K^ as above (the Q^ halves are not written)
-  static constexpr uint32_t V = 32768;
-  static constexpr uint32_t S = 49152;
-  static constexpr uint32_t X = 81920;     // X bf16 [d_k][d_k]
-  static constexpr uint32_t VN = 114688;   // Vn_X^T diag(e^{gamma_C - gamma})
-  static constexpr uint32_t VNS = 131072;  // Vn_S^T diag(e^{gamma_C - gamma})
-  static constexpr uint32_t KQ16 = VN;
-  static constexpr uint32_t WN = 147456;
-  static constexpr uint32_t TB = 163840;
-  static constexpr uint32_t TW = 172032;
-  static constexpr uint32_t P = 0;         // (unused)
-  static constexpr uint32_t F32 = 180224;
-};
-constexpr int LDA = 65, LDO = 128;
 constexpr uint32_t F32_BYTES = 2 * 64 * LDA * 4;
 // Staging of a chunk's raw inputs, loaded by TMA (2-D tensor maps over qkv and z):
 // the raw q, k and v rows of tokens t0-3 .. t0+63 (bf16, one [67][128] box per
@@ -95,8 +81,8 @@ constexpr uint32_t F32_BYTES = 2 * 64 * LDA * 4;
 // the fp32 area's tail between the state-correction MMA and the epilogue.
 constexpr uint32_t RAW_BOX_ROWS = C + kConvW - 1;     // a chunk and its 3-token halo
 constexpr uint32_t RAW_BLK = RAW_BOX_ROWS * 256;       // one channel block: [67 rows][128 bf16]
-template <bool kXfer> struct Map : Lay<kXfer> {
-  using L_ = Lay<kXfer>;
+struct Map : Lay {
+  using L_ = Lay;
   static constexpr uint32_t CW = L_::F32 + F32_BYTES;   // conv weights fp32 [3][tap][128]
   static constexpr uint32_t NW = CW + 3 * 128 * 4 * 4;
   static constexpr uint32_t GATE = NW + 128 * 4;        // gam, beta, e^gam, e^{gamC-gam}
@@ -104,102 +90,27 @@ template <bool kXfer> struct Map : Lay<kXfer> {
   static constexpr uint32_t BYTES = USED + 1024;        // slack to align the base to 1024
   static constexpr uint32_t RAW = L_::WN;               // [q | k | v blocks]
   static constexpr uint32_t RAW_END = RAW + 3 * RAW_BLK;
-  static constexpr uint32_t OST = L_::VN;               // O staging fp32 [64][128] (output pass)
-  static constexpr uint32_t Z = RAW_END;                // z bf16 [64][128] (output pass)
+  static constexpr uint32_t OST = L_::VN;               // O staging fp32 [64][128]
+  static constexpr uint32_t Z = RAW_END;                // z bf16 [64][128]
   static_assert(RAW_END <= L_::F32 + F32_BYTES, "raw staging past the fp32 area");
   static_assert(RAW % 128 == 0 && RAW_BLK % 128 == 0 && RAW_END % 128 == 0, "TMA destinations need 128-B alignment");
-  static_assert(kXfer || Z + 64 * 128 * 2 <= CW, "z staging overlaps the conv weights");
-  static_assert(kXfer || OST + 64 * LDO * 4 <= L_::WN, "O staging overlaps -W");
+  static_assert(Z + 64 * 128 * 2 <= CW, "z staging overlaps the conv weights");
+  static_assert(OST + 64 * LDO * 4 <= L_::WN, "O staging overlaps -W");
   static_assert(BYTES <= 227 * 1024, "shared memory");
 };
 
 // ---- tensor memory columns ----
 constexpr uint32_t TM_G = 0, TM_W = 64, TM_U = 128, TM_O1 = 192, TM_O2 = 256, TM_Z = 384;
-constexpr uint32_t TM_VX = 192, TM_ZX = 256;          // transfer pass: X's Vn^T and X itself
 constexpr uint32_t TM_COLS = 512;
-
-constexpr uint64_t D_K = tc::sdesc_sw128(16, 1024);         // K-major tiles
-constexpr uint64_t D_MN_KQ = tc::sdesc_sw128(16384, 1024);  // K^ read MN-major
-constexpr uint64_t D_MN_V = tc::sdesc_sw128(8192, 1024);    // V read MN-major
-constexpr uint32_t ID_KK = tc::idesc_bf16(128, 64, 0, 0);
-constexpr uint32_t ID_GRAM = tc::idesc_f16(128, 64, 0, 0);
-constexpr uint32_t ID_MN_A = tc::idesc_bf16(128, 64, 1, 0);
-constexpr uint32_t ID_MN_B = tc::idesc_bf16(128, 128, 0, 1);
-
-constexpr long long kWaitBudget = 1LL << 31;  // clock cycles (~1 s) before a wait gives up
-
-struct Smem {
-  uint8_t* base;
-  uint32_t addr;  // shared-window address of base
-  __device__ float* f32(uint32_t off) const { return reinterpret_cast<float*>(base + off); }
-};
-
-__device__ __forceinline__ void store_bf16x4(uint8_t* tile, uint32_t off, float a, float b, float c,
-                                             float d) {
-  uint2 v;
-  v.x = pack_bf16x2(a, b);
-  v.y = pack_bf16x2(c, d);
-  *reinterpret_cast<uint2*>(tile + off) = v;
-}
-
-__device__ __forceinline__ void store_f16x4(uint8_t* tile, uint32_t off, float a, float b, float c,
-                                            float d) {
-  uint2 v;
-  v.x = pack_f16x2(a, b);
-  v.y = pack_f16x2(c, d);
-  *reinterpret_cast<uint2*>(tile + off) = v;
-}
-
-__device__ __forceinline__ void store_bf16x8(uint8_t* tile, uint32_t off, const float* x) {
-  uint4 v;
-  v.x = pack_bf16x2(x[0], x[1]);
-  v.y = pack_bf16x2(x[2], x[3]);
-  v.z = pack_bf16x2(x[4], x[5]);
-  v.w = pack_bf16x2(x[6], x[7]);
-  *reinterpret_cast<uint4*>(tile + off) = v;
-}
-
-// Four SiLUs with one reciprocal: with d_i = 1 + e^{-x_i}, 1/d_1 =
-// d_2 d_3 d_4 / (d_1 d_2 d_3 d_4), and so on.  Inputs are clamped at -20 so the
-// product stays below 2^126 (|silu(x)| < 4.2e-8 for x < -20, which the clamp
-// replaces by silu(-20)); this takes the special-function unit from two
-// operations per SiLU to 1.25.
-__device__ __forceinline__ void silu4(float (&x)[4]) {
-  float d[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = 1.0f + __expf(-fmaxf(x[i], -20.0f));
-  const float d01 = d[0] * d[1], d23 = d[2] * d[3];
-  const float r = __fdividef(1.0f, d01 * d23);   // approximate reciprocal (product < 2^126)
-  const float r01 = r * d23, r23 = r * d01;   // 1/(d0 d1), 1/(d2 d3)
-  x[0] *= r01 * d[1];
-  x[1] *= r01 * d[0];
-  x[2] *= r23 * d[3];
-  x[3] *= r23 * d[2];
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(mbar)), "r"(bytes)
-               : "memory");
-}
-
-// One 2-D TMA tile load: the box at column x, row y of the tensor map lands at
-// smem_dst and reports its bytes to mbar.  Rows outside the tensor read as zero.
-__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* tm, int x, int y, uint64_t* mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(tc::smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(tc::smem_u32(mbar))
-      : "memory");
-}
 
 // One thread: the raw q, k and v rows of tokens t0-3 .. t0+63 of a sequence
 // starting at packed row `start` (rows before the sequence are fetched too and
 // ignored: the conv reads the carried conv state for them).
 __device__ __forceinline__ void stage_raw(const CUtensorMap* tm_qkv, uint8_t* raw, uint64_t* mbar, int start,
-                                          int t0, int kh, int h, int Cq, bool with_q) {
-  mbar_expect_tx(mbar, (with_q ? 3 : 2) * RAW_BLK);
+                                          int t0, int kh, int h, int Cq) {
+  mbar_expect_tx(mbar, 3 * RAW_BLK);
   const int y = start + t0 - (kConvW - 1);
-  if (with_q) tma_load_2d(raw, tm_qkv, kh * kD, y, mbar);
+  tma_load_2d(raw, tm_qkv, kh * kD, y, mbar);
   tma_load_2d(raw + RAW_BLK, tm_qkv, Cq + kh * kD, y, mbar);
   tma_load_2d(raw + 2 * RAW_BLK, tm_qkv, 2 * Cq + h * kD, y, mbar);
 }
@@ -217,38 +128,12 @@ __device__ bool cu_seqlens_valid(const PrefillArgs& p) {
   return !__syncthreads_or(bad);
 }
 
-// Block-wide sync that also orders tensor-memory traffic and makes generic
-// smem writes visible to the tensor core.
-__device__ __forceinline__ void sync_for_mma() {
-  tc::fence_proxy_async();
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
-}
 
-// One segment of the work list (built on the device from cu_seqlens).
-struct Seg {
-  int n, begin, len, sigma, nsig, k0;   // sequence, token range within it, segment index/count,
-                                        // the sequence's first boundary slot
-};
 
-__device__ __forceinline__ Seg load_seg(const int* list, int u) {
-  const int* e = list + 4 + 8 * u;
-  return Seg{e[0], e[1], e[2], e[3], e[4], e[5]};
-}
-
-// Transfer matrices of boundary slot k, value head h: X (the map), S (end state
-// from zero, overwritten by the combine pass with the true start state of the
-// next segment), and the sequence's initial state (first slot only).
-__device__ __forceinline__ float* xfer_ptr(const PrefillArgs& p, int k, int h, int part) {
-  return p.xfer + (((size_t)k * p.h_v + h) * 3 + part) * (size_t)(kD * kD);
-}
-
-template <bool kXfer>
 __global__ void __launch_bounds__(kThreads, 1)
-    chunk_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv,
+    fused_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv,
                  const __grid_constant__ CUtensorMap tm_z) {
-  using M = Map<kXfer>;
+  using M = Map;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mbar;      // MMA completion
   __shared__ __align__(8) uint64_t mbar_raw;  // raw q|k|v rows of a chunk landed
@@ -259,34 +144,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int u = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
   if (u >= p.seg_list[0]) return;
   const Seg sg = load_seg(p.seg_list, u);
-  if (kXfer && sg.sigma == sg.nsig - 1) return;   // the last segment needs no transfer map
   const int n = sg.n;
   const int G = p.h_v / p.h_k, kh = h / G;
   const int start = p.cu_seqlens[n];
   const int seg_end = sg.begin + sg.len;          // token positions within the sequence
   const int Cq = p.h_k * kD, Cc = 2 * Cq + p.h_v * kD;
 
-  // where the state comes from and goes to
-  const float* S_init = nullptr;
-  float* S_final = nullptr;
+  // the state: read at the start, written back at the end (one segment per sequence)
   float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
-  if (!kXfer) {
-    if (sg.nsig == 1) {
-      S_init = ssm;
-      S_final = ssm;
-    } else {
-      S_init = sg.sigma == 0 ? xfer_ptr(p, sg.k0, h, 2) : xfer_ptr(p, sg.k0 + sg.sigma - 1, h, 1);
-      S_final = sg.sigma == sg.nsig - 1 ? ssm : nullptr;
-    }
-  }
 
-  Smem sm;
-  {
-    const uint32_t raw = tc::smem_u32(smem_raw);
-    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
-    sm.base = smem_raw + pad;
-    sm.addr = raw + pad;
-  }
+  const Smem sm = smem_aligned(smem_raw);
   float* cw = sm.f32(M::CW);      // [blk][tap][i]
   float* nw = sm.f32(M::NW);
   float* gam = sm.f32(M::GATE);
@@ -295,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* egc = gam + 192;
   float* Af = sm.f32(M::F32);
   float* Tf = Af + 64 * LDA;
-  float* Ost = sm.f32(M::OST);      // output pass: aliases the Vn tiles (used after them)
+  float* Ost = sm.f32(M::OST);      // aliases the Vn tiles (used after them)
 
   if (tid == 0) {
     tc::mbar_init(&mbar, 1);
@@ -322,33 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
   const int part = warp >> 2;               // which quarter of a lane quarter's columns
 
-  // initial state(s): fp32 into TMEM, bf16 into the operand tile(s)
+  // initial state: fp32 into TMEM, bf16 into the operand tile
   {
     const int col0 = part * 32;
     float v[32];
-    if (!kXfer) {
-      const float4* src = reinterpret_cast<const float4*>(S_init + (size_t)row * kD + col0);
+    const float4* src = reinterpret_cast<const float4*>(ssm + (size_t)row * kD + col0);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 x = src[q];
-        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    for (int q = 0; q < 8; ++q) {
+      const float4 x = src[q];
+      v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
     }
     tc::tmem_st32(tmem + lane_base + TM_Z + col0, v);
 #pragma unroll
     for (int m = 0; m < 4; ++m)
       store_bf16x8(sm.base + M::S, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
-    if (kXfer) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = (col0 + i == row) ? 1.0f : 0.0f;
-      tc::tmem_st32(tmem + lane_base + TM_ZX + col0, v);
-#pragma unroll
-      for (int m = 0; m < 4; ++m)
-        store_bf16x8(sm.base + M::X, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
-    }
   }
 
   const float A_exp = __expf(p.A_log[h]);
@@ -365,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     return all_ok;
   };
 
-  if (tid == 32) stage_raw(&tm_qkv, sm.base + M::RAW, &mbar_raw, start, sg.begin, kh, h, Cq, !kXfer);
+  if (tid == 32) stage_raw(&tm_qkv, sm.base + M::RAW, &mbar_raw, start, sg.begin, kh, h, Cq);
   // gate inputs of the next chunk, prefetched into warp 0's registers
   float a_nx[2] = {0.0f, 0.0f}, b_nx[2] = {0.0f, 0.0f};
   if (warp == 0) {
@@ -429,14 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ---- conv + SiLU + L2 norms -> K^, Q^, V tiles.  Warp w takes tokens 4w .. 4w+3
     //      of every block and a lane 4 channels of them, so each raw row is read once
-    //      for all the taps that use it and the four tokens are independent work;
-    //      the transfer pass needs no q ----
+    //      for all the taps that use it and the four tokens are independent work ----
     {
-      constexpr int kB0 = kXfer ? 1 : 0;
       constexpr int kRows = 4 + kConvW - 1;   // raw rows under a token quad
       const int tq = 4 * warp;
 #pragma unroll
-      for (int blk = kB0; blk < 3; ++blk) {
+      for (int blk = 0; blk < 3; ++blk) {
         float w[kConvW][4];
 #pragma unroll
         for (int j = 0; j < kConvW; ++j) {
@@ -472,33 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           silu4(y[i]);
         }
         if (blk < 2) {
-          // the four tokens' sums of squares over the 128 channels: the first two
-          // butterfly steps each hand half of the sums to the partner lane, so a
-          // lane ends with the full sum of token 2 (lane bit 4) + (lane bit 3)
-          float ss[4];
+          float rn[4];
+          l2_rnorm4(y, p.l2_eps, blk == 0 ? qscale : 1.0f, lane, rn);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            ss[i] = y[i][0] * y[i][0];
+          for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int e = 1; e < 4; ++e) ss[i] = fmaf(y[i][e], y[i][e], ss[i]);
-          }
-          const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
-          float k0 = hi16 ? ss[2] : ss[0], k1 = hi16 ? ss[3] : ss[1];
-          const float s0 = hi16 ? ss[0] : ss[2], s1 = hi16 ? ss[1] : ss[3];
-          k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-          k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-          float tot = hi8 ? k1 : k0;
-          tot += __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
-          tot += __shfl_xor_sync(0xffffffffu, tot, 4);
-          tot += __shfl_xor_sync(0xffffffffu, tot, 2);
-          tot += __shfl_xor_sync(0xffffffffu, tot, 1);
-          const float rn = rsqrtf(tot + p.l2_eps) * (blk == 0 ? qscale : 1.0f);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float ri = __shfl_sync(0xffffffffu, rn, ((i >> 1) << 4) | ((i & 1) << 3));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) y[i][e] *= ri;
-          }
+            for (int e = 0; e < 4; ++e) y[i][e] *= rn[i];
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -523,36 +354,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a = sm.addr + M::KQ16 + kb * 16384 + ks;
         tc::mma_bf16(tmem + TM_G, tc::sdesc_at(D_K, a), tc::sdesc_at(D_K, a), ID_GRAM, k > 0);
       }
-      if (!kXfer) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-          tc::mma_bf16(tmem + TM_O1, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
-                       tc::sdesc_at(D_K, sm.addr + M::KQ + kb * 16384 + 8192 + ks), ID_KK, k > 0);
-        }
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+        tc::mma_bf16(tmem + TM_O1, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                     tc::sdesc_at(D_K, sm.addr + M::KQ + kb * 16384 + 8192 + ks), ID_KK, k > 0);
       }
       tc::mma_commit(&mbar);
     }
-    // meanwhile: pre-scale the fp32 state(s) by the chunk's total decay
+    // meanwhile: pre-scale the fp32 state by the chunk's total decay
     {
       const float dC = eg[C - 1];
+      float v[32];
+      const uint32_t ta = tmem + lane_base + TM_Z + part * 32;
+      tc::tmem_ld32(ta, v);
 #pragma unroll
-      for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
-        {
-          float v[32];
-          const uint32_t ta = tmem + lane_base + (zz ? TM_ZX : TM_Z) + part * 32;
-          tc::tmem_ld32(ta, v);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= dC;
-          tc::tmem_st32(ta, v);
-        }
-      }
+      for (int i = 0; i < 32; ++i) v[i] *= dC;
+      tc::tmem_st32(ta, v);
     }
     if (!wait_mma()) { aborted = true; break; }
 
     // ---- A (fp32, lanes 0-63) and P (bf16 tile, lanes 64-127) from the Gram rows;
     //      warps w and w+4 share a lane quarter and split its 64 columns ----
-    if (!kXfer || (warp & 3) < 2) {
+    {
       float v[16];
       const int t = row & 63;
       const float gt = gam[t];
@@ -578,61 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    // ---- T = (I + A)^{-1}: 16 x 16 diagonal blocks, then block rows ----
-    if (tid < 64) {
-      const int b = tid >> 4, c = tid & 15;
-      float x[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = (r == c) ? 1.0f : 0.0f;
-#pragma unroll
-        for (int s = 0; s < r; ++s) acc = fmaf(-Af[(16 * b + r) * LDA + 16 * b + s], x[s], acc);
-        x[r] = acc;
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) Tf[(16 * b + r) * LDA + 16 * b + c] = x[r];
-    } else {
-      // zero the blocks above the diagonal
-      for (int e = tid - 64; e < 6 * 256; e += kThreads - 64) {
-        const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        Tf[(16 * bi + r) * LDA + 16 * bj + c] = 0.0f;
-      }
-    }
-    __syncthreads();
-#pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-      const int tasks = 64 * (4 - d);
-      if (tid < tasks) {
-        const int j = tid >> 6, i = j + d, c = (tid >> 2) & 15, qr = tid & 3;
-        // M[4qr + r][c] = sum_{k=j}^{i-1} A_ik T_kj
-        float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int kb = j; kb < i; ++kb) {
-#pragma unroll
-          for (int s2 = 0; s2 < 16; ++s2) {
-            const float tv = Tf[(16 * kb + s2) * LDA + 16 * j + c];
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-              m[r] = fmaf(Af[(16 * i + 4 * qr + r) * LDA + 16 * kb + s2], tv, m[r]);
-          }
-        }
-        float mf[16];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) mf[4 * q + r] = __shfl_sync(0xffffffffu, m[r], (lane & ~3) | q);
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int rr = 4 * qr + r;
-          float acc = 0.0f;
-#pragma unroll
-          for (int q = 0; q < 16; ++q) acc = fmaf(Tf[(16 * i + rr) * LDA + 16 * i + q], mf[q], acc);
-          Tf[(16 * i + rr) * LDA + 16 * j + c] = -acc;
-        }
-      }
-      __syncthreads();
-    }
+    // ---- T = (I + A)^{-1} ----
+    solve_unit_lower<kThreads>(Af, Tf, tid, lane);
     // T diag(beta) and T diag(beta e^gamma) as bf16 tiles [t][s]
     for (int e = tid; e < 64 * 8; e += kThreads) {
       const int t = e >> 3, c8 = (e & 7) * 8;
@@ -677,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     sync_for_mma();
 
-    // ---- Vn^T = U^T - S0 W^T  (transfer pass also: Vn_X^T = -X W^T) ----
+    // ---- Vn^T = U^T - S0 W^T ----
     if (tid == 0) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -685,26 +456,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::mma_bf16(tmem + TM_U, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
                      tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
       }
-      if (kXfer) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-          tc::mma_bf16(tmem + TM_VX, tc::sdesc_at(D_K, sm.addr + M::X + kb * 16384 + ks),
-                       tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, k > 0);
-        }
-      }
       tc::mma_commit(&mbar);
     }
     if (!wait_mma()) { aborted = true; break; }
 
-    if (!kXfer) {
-      // ---- z of the chunk -> smem (TMA; read by the epilogue) ----
-      if (tid == 32) {
-        mbar_expect_tx(&mbar_z, 64 * 256);
-        tma_load_2d(sm.base + M::Z, &tm_z, h * kD, start + t0, &mbar_z);
-      }
-      z_pending = true;
+    // ---- z of the chunk -> smem (TMA; read by the epilogue) ----
+    if (tid == 32) {
+      mbar_expect_tx(&mbar_z, 64 * 256);
+      tma_load_2d(sm.base + M::Z, &tm_z, h * kD, start + t0, &mbar_z);
     }
+    z_pending = true;
 
     // ---- Vn^T tiles (plain and decay-weighted), row = d_v index ----
     {
@@ -712,11 +473,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_ld16(tmem + lane_base + TM_U + part * 16, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) vs[i] = v[i] * egc[part * 16 + i];
-      if (kXfer) {
-        tc::tmem_ld16(tmem + lane_base + TM_VX + part * 16, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= egc[part * 16 + i];
-      }
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const uint32_t off = tc::sw128_off(row, part * 16 + 8 * m, 0);
@@ -726,20 +482,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     sync_for_mma();
 
-    // ---- O2 = Vn^T P^T and S += Vn^T diag(e^{gC-g}) K  (transfer: S and X updates) ----
+    // ---- O2 = Vn^T P^T and S += Vn^T diag(e^{gC-g}) K ----
     if (tid == 0) {
-      if (!kXfer) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          tc::mma_bf16(tmem + TM_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
-                       tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          tc::mma_bf16(tmem + TM_ZX, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
-                       tc::sdesc_at(D_MN_KQ, sm.addr + M::KQ + k * 2048), ID_MN_B, 1u);
-        }
+      for (int k = 0; k < 4; ++k) {
+        tc::mma_bf16(tmem + TM_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
+                     tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -750,35 +498,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!wait_mma()) { aborted = true; break; }
     // the next chunk's raw rows land while this chunk finishes
-    if (tid == 32 && t0 + C < seg_end) stage_raw(&tm_qkv, sm.base + M::RAW, &mbar_raw, start, t0 + C, kh, h, Cq, !kXfer);
+    if (tid == 32 && t0 + C < seg_end) stage_raw(&tm_qkv, sm.base + M::RAW, &mbar_raw, start, t0 + C, kh, h, Cq);
     raw_pending = t0 + C < seg_end;
 
-    // ---- new state(s) -> bf16 operand tiles; output pass: O = e^gamma O1 + O2 -> fp32 staging ----
+    // ---- new state -> bf16 operand tile; O = e^gamma O1 + O2 -> fp32 staging ----
     {
+      float v[32];
+      tc::tmem_ld32(tmem + lane_base + TM_Z + part * 32, v);
 #pragma unroll
-      for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
-        {
-          float v[32];
-          tc::tmem_ld32(tmem + lane_base + (zz ? TM_ZX : TM_Z) + part * 32, v);
+      for (int m = 0; m < 4; ++m)
+        store_bf16x8(sm.base + M::S, tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
+      float o1[16], o2[16];
+      tc::tmem_ld16(tmem + lane_base + TM_O1 + part * 16, o1);
+      tc::tmem_ld16(tmem + lane_base + TM_O2 + part * 16, o2);
 #pragma unroll
-          for (int m = 0; m < 4; ++m)
-            store_bf16x8(sm.base + (zz ? M::X : M::S), tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
-        }
+      for (int i = 0; i < 16; ++i) {
+        const int t = part * 16 + i;
+        Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
       }
-      if (!kXfer) {
-        float o1[16], o2[16];
-        tc::tmem_ld16(tmem + lane_base + TM_O1 + part * 16, o1);
-        tc::tmem_ld16(tmem + lane_base + TM_O2 + part * 16, o2);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = part * 16 + i;
-          Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
-        }
-      }
-    }
-    if (kXfer) {
-      __syncthreads();
-      continue;
     }
     if (!__syncthreads_and(tc::mbar_wait(&mbar_z, chunk_parity, kWaitBudget))) { aborted = true; break; }
     z_pending = false;
@@ -811,19 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (raw_pending) tc::mbar_wait(&mbar_raw, chunk_parity, kWaitBudget);
     if (z_pending) tc::mbar_wait(&mbar_z, chunk_parity, kWaitBudget);
   } else {
-    // final state(s) back to global memory
+    // final state back to global memory
+    float4* dst = reinterpret_cast<float4*>(ssm + (size_t)row * kD + part * 32);
+    float v[32];
+    tc::tmem_ld32(tmem + lane_base + TM_Z + part * 32, v);
 #pragma unroll
-    for (int zz = 0; zz < 2; ++zz) {
-      float* dst_base = kXfer ? xfer_ptr(p, sg.k0 + sg.sigma, h, zz == 0 ? 1 : 0) : (zz == 0 ? S_final : nullptr);
-      if (dst_base == nullptr) continue;
-      float4* dst = reinterpret_cast<float4*>(dst_base + (size_t)row * kD + part * 32);
-      {
-        float v[32];
-        tc::tmem_ld32(tmem + lane_base + (zz ? TM_ZX : TM_Z) + part * 32, v);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      }
-    }
+    for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -832,43 +562,54 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // The work list: every sequence split into segments of p.seg_tokens (the last
 // one ragged; a sequence of at most that many tokens is one segment), and the
-// list of sequences with more than one segment.  Validates cu_seqlens first:
-// on a violation both lists stay empty and the status word says why.
+// list of sequences with more than one segment.  On the split path it also
+// numbers the chunks of all sequences (a record slot per chunk): chunk_off[n]
+// is the first chunk of sequence n and chunk_list[c] the (sequence, first
+// token) of chunk c.  Validates cu_seqlens first: on a violation the lists
+// stay empty and the status word says why.
 __global__ void __launch_bounds__(256) seg_list_kernel(PrefillArgs p) {
-  __shared__ int s_cnt[256];
-  __shared__ int s_base, s_mbase;
+  __shared__ int s_cnt[256], s_ch[256];
+  __shared__ int s_base, s_mbase, s_cbase;
   if (!cu_seqlens_valid(p)) {
     if (threadIdx.x == 0) {
       record_status(p.status, GDN_ERR_DEVICE_BOUNDS);
       p.seg_list[0] = 0;
       p.multi_list[0] = 0;
     }
+    if (p.chunk_list)
+      for (int c = threadIdx.x; c < p.max_chunks; c += blockDim.x) p.chunk_list[c] = make_int2(-1, 0);
     return;
   }
-  if (threadIdx.x == 0) { s_base = 0; s_mbase = 0; }
+  if (threadIdx.x == 0) { s_base = 0; s_mbase = 0; s_cbase = 0; }
   __syncthreads();
   for (int n0 = 0; n0 < p.n_seqs; n0 += 256) {
     const int n = n0 + threadIdx.x;
-    int nsig = 0, len = 0, st = 0;
+    int nsig = 0, len = 0, st = 0, nch = 0;
     if (n < p.n_seqs) {
       st = p.cu_seqlens[n];
       len = p.cu_seqlens[n + 1] - st;
       nsig = len <= 0 ? 0 : (len + p.seg_tokens - 1) / p.seg_tokens;
+      nch = len <= 0 ? 0 : (len + C - 1) / C;
     }
-    // inclusive scan of segment counts over the tile (and of multi-segment flags)
-    // segment count in bits 0-21 (< 2^21 + 256), multi-segment count in bits 22-30 (<= 256)
+    // inclusive scans over the tile of segment counts (bits 0-21) with
+    // multi-segment flags (bits 22-30), and of chunk counts
     s_cnt[threadIdx.x] = nsig | ((nsig > 1 ? 1 : 0) << 22);
+    s_ch[threadIdx.x] = nch;
     __syncthreads();
     for (int off = 1; off < 256; off <<= 1) {
       const int v = threadIdx.x >= off ? s_cnt[threadIdx.x - off] : 0;
+      const int w = threadIdx.x >= off ? s_ch[threadIdx.x - off] : 0;
       __syncthreads();
       s_cnt[threadIdx.x] += v;
+      s_ch[threadIdx.x] += w;
       __syncthreads();
     }
-    const int incl = s_cnt[threadIdx.x];
+    const int incl = s_cnt[threadIdx.x], incl_ch = s_ch[threadIdx.x];
     const int seg_off = s_base + (incl & 0x3FFFFF) - nsig;
     const int m_off = s_mbase + (incl >> 22) - (nsig > 1 ? 1 : 0);
+    const int ch_off = s_cbase + incl_ch - nch;
     const int k0 = st / p.seg_tokens;
+    if (p.chunk_off && n < p.n_seqs) p.chunk_off[n] = ch_off;
     for (int sg = 0; sg < nsig; ++sg) {
       int* e = p.seg_list + 4 + 8 * (seg_off + sg);
       e[0] = n;
@@ -877,6 +618,7 @@ __global__ void __launch_bounds__(256) seg_list_kernel(PrefillArgs p) {
       e[3] = sg;
       e[4] = nsig;
       e[5] = k0;
+      e[6] = ch_off + sg * (p.seg_tokens / C);
     }
     if (nsig > 1) {
       int* e = p.multi_list + 4 + 4 * m_off;
@@ -888,12 +630,30 @@ __global__ void __launch_bounds__(256) seg_list_kernel(PrefillArgs p) {
     if (threadIdx.x == 255) {
       s_base += incl & 0x3FFFFF;
       s_mbase += incl >> 22;
+      s_cbase += incl_ch;
     }
     __syncthreads();
   }
   if (threadIdx.x == 0) {
     p.seg_list[0] = s_base;
     p.multi_list[0] = s_mbase;
+    if (p.chunk_off) p.chunk_off[p.n_seqs] = s_cbase;
+  }
+  if (!p.chunk_list) return;
+  __syncthreads();   // chunk_off is complete (and visible to the whole block)
+  const int n_chunks = s_cbase;
+  for (int c = threadIdx.x; c < p.max_chunks; c += blockDim.x) {
+    int2 e = make_int2(-1, 0);
+    if (c < n_chunks) {
+      // the last sequence whose first chunk is <= c (empty sequences share their successor's offset)
+      int lo = 0, hi = p.n_seqs - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.chunk_off[mid] <= c) lo = mid; else hi = mid - 1;
+      }
+      e = make_int2(lo, (c - p.chunk_off[lo]) * C);
+    }
+    p.chunk_list[c] = e;
   }
 }
 
@@ -908,14 +668,6 @@ constexpr int kCombineRows = 32;
 constexpr uint32_t kMapBytes = kD * kD * 4;
 constexpr uint32_t kCombineSmem = 2 * kMapBytes + kCombineRows * kD * 4 + 16;
 
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* mbar) {
-  mbar_expect_tx(mbar, bytes);
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          tc::smem_u32(smem_dst)),
-      "l"(gmem_src), "r"(bytes), "r"(tc::smem_u32(mbar))
-      : "memory");
-}
 
 __global__ void __launch_bounds__(256) combine_kernel(PrefillArgs p) {
   extern __shared__ __align__(128) float csm[];
@@ -1037,26 +789,39 @@ __global__ void __launch_bounds__(256) conv_state_kernel(PrefillArgs p) {
 
 namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t align1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
 struct ScratchLayout {
-  size_t seg_list, multi_list, xfer, total;
+  size_t seg_list, multi_list, xfer, chunk_off, chunk_list, rec_kq, rec_v, total;
+  long long max_chunks;
 };
-ScratchLayout scratch_layout(int n_seqs, int h_v, long long total_tokens) {
-  const long long slots = total_tokens / kSegTokens;
+// The scratch of one call.  The split path (records = true) has room for a
+// segment per 1024 tokens, their transfer maps, the chunk index and the
+// per-chunk records; the single-pass path needs only the unsplit work list,
+// whose size depends on n_seqs alone.
+ScratchLayout scratch_layout(int n_seqs, int h_k, int h_v, long long total_tokens, bool records) {
+  const long long slots = records ? total_tokens / kSegTokens : 0;   // the single pass never segments
   const long long units = slots + n_seqs;   // segments: sum of ceil(T_n / L) <= T / L + N
   ScratchLayout l;
   l.seg_list = 0;
   l.multi_list = align256(16 + (size_t)units * 32);
   l.xfer = l.multi_list + align256(16 + (size_t)slots * 16);
-  l.total = l.xfer + (size_t)slots * h_v * 3 * kD * kD * sizeof(float);
+  size_t end = l.xfer + (size_t)slots * h_v * 3 * kD * kD * sizeof(float);
+  l.max_chunks = records ? total_tokens / C + n_seqs : 0;
+  l.chunk_off = align256(end);
+  l.chunk_list = l.chunk_off + (records ? align256((size_t)(n_seqs + 1) * 4) : 0);
+  l.rec_kq = align1024(l.chunk_list + (size_t)l.max_chunks * 8);
+  l.rec_v = l.rec_kq + (size_t)l.max_chunks * h_k * kRecKQ;
+  end = l.rec_v + (size_t)l.max_chunks * h_v * kRecV;
+  l.total = records ? end : l.xfer + (size_t)slots * h_v * 3 * kD * kD * sizeof(float);
   return l;
 }
 }  // namespace
 
-size_t prefill_scratch_bytes(int n_seqs, int, int h_v, long long total_tokens) {
-  return scratch_layout(n_seqs, h_v, total_tokens).total;
+size_t prefill_scratch_bytes(int n_seqs, int h_k, int h_v, long long total_tokens) {
+  return scratch_layout(n_seqs, h_k, h_v, total_tokens, true).total;
 }
 
-size_t prefill_scratch_bytes_unsplit(int n_seqs) { return scratch_layout(n_seqs, 0, 0).total; }
+size_t prefill_scratch_bytes_unsplit(int n_seqs) { return scratch_layout(n_seqs, 0, 0, 0, false).total; }
 
 namespace {
 
@@ -1091,45 +856,55 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 
 cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool allow_split) {
   PrefillArgs p = p_in;
-  const ScratchLayout l = scratch_layout(p.n_seqs, p.h_v, p.total_tokens);
+  const ScratchLayout l = scratch_layout(p.n_seqs, p.h_k, p.h_v, p.total_tokens, allow_split);
   char* scratch = static_cast<char*>(p.scratch);
   p.seg_list = reinterpret_cast<int*>(scratch + l.seg_list);
   p.multi_list = reinterpret_cast<int*>(scratch + l.multi_list);
   p.xfer = reinterpret_cast<float*>(scratch + l.xfer);
+  p.chunk_off = allow_split ? reinterpret_cast<int*>(scratch + l.chunk_off) : nullptr;
+  p.chunk_list = allow_split ? reinterpret_cast<int2*>(scratch + l.chunk_list) : nullptr;
+  p.rec_kq = allow_split ? reinterpret_cast<uint8_t*>(scratch + l.rec_kq) : nullptr;
+  p.rec_v = allow_split ? reinterpret_cast<uint8_t*>(scratch + l.rec_v) : nullptr;
+  p.max_chunks = (int)l.max_chunks;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(chunk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Map<false>::BYTES)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(chunk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)Map<true>::BYTES)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kCombineSmem)) != cudaSuccess)
-    return e;
   const int Cc_ = 2 * p.h_k * kD + p.h_v * kD;
   CUtensorMap tm_qkv, tm_z;
   if (!make_map_2d(&tm_qkv, p.qkv, (uint64_t)Cc_, (uint64_t)p.total_tokens, kD, RAW_BOX_ROWS) ||
       !make_map_2d(&tm_z, p.z, (uint64_t)p.h_v * kD, (uint64_t)p.total_tokens, kD, C))
     return cudaErrorInvalidValue;
-  // Split long sequences into segments scanned in parallel only when one CTA
-  // per (sequence, value head) would leave the GPU short of work: the transfer
-  // pass that makes segments independent costs most of a second pass.
-  int dev = 0, sms = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-  const bool segment = allow_split && (long long)p.n_seqs * p.h_v < 4LL * sms && p.total_tokens > kSegTokens;
-  p.seg_tokens = segment ? kSegTokens : 0x40000000;
-  const long long slots = segment ? p.total_tokens / kSegTokens : 0;
-  const unsigned units = (unsigned)(slots + p.n_seqs);
-  seg_list_kernel<<<1, 256, 0, stream>>>(p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (slots > 0) {   // some sequence may be longer than one segment
-    chunk_kernel<true><<<units * (unsigned)p.h_v, kThreads, Map<true>::BYTES, stream>>>(p, tm_qkv, tm_z);
+  if (!allow_split) {
+    // one fused pass per (sequence, value head): no records, no segments
+    if ((e = cudaFuncSetAttribute(fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)Map::BYTES)) != cudaSuccess)
+      return e;
+    p.seg_tokens = 0x40000000;
+    seg_list_kernel<<<1, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    combine_kernel<<<(unsigned)slots * (unsigned)p.h_v * (kD / kCombineRows), 256, kCombineSmem, stream>>>(p);
+    fused_kernel<<<(unsigned)p.n_seqs * (unsigned)p.h_v, kThreads, Map::BYTES, stream>>>(p, tm_qkv, tm_z);
+  } else {
+    if ((e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kCombineSmem)) != cudaSuccess)
+      return e;
+    // Split long sequences into segments scanned in parallel only when one CTA
+    // per (sequence, value head) would leave the GPU short of work: the
+    // transfer pass that makes segments independent is a second scan.
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const bool segment = (long long)p.n_seqs * p.h_v < 4LL * sms && p.total_tokens > kSegTokens;
+    p.seg_tokens = segment ? kSegTokens : 0x40000000;
+    const long long slots = segment ? p.total_tokens / kSegTokens : 0;
+    const unsigned units = (unsigned)(slots + p.n_seqs);
+    seg_list_kernel<<<1, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_prefill_prep(p, (unsigned)l.max_chunks, stream)) != cudaSuccess) return e;
+    if (slots > 0) {   // some sequence may be longer than one segment
+      if ((e = launch_prefill_scan(p, true, units, tm_z, stream)) != cudaSuccess) return e;
+      combine_kernel<<<(unsigned)slots * (unsigned)p.h_v * (kD / kCombineRows), 256, kCombineSmem, stream>>>(p);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if ((e = launch_prefill_scan(p, false, units, tm_z, stream)) != cudaSuccess) return e;
   }
-  chunk_kernel<false><<<units * (unsigned)p.h_v, kThreads, Map<false>::BYTES, stream>>>(p, tm_qkv, tm_z);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   conv_state_kernel<<<dim3((unsigned)((Cc_ + 255) / 256), (unsigned)p.n_seqs), 256, 0, stream>>>(p);
   return cudaGetLastError();

@@ -1,0 +1,266 @@
+// gdn_prefill.cuh -- pieces shared by the prefill kernels: operand
+// descriptors, tile stores, bulk copies, the work list, the per-chunk records
+// and the unit-lower-triangular solve of the chunked WY/UT form.
+#pragma once
+#include <cuda.h>
+
+#include "gdn_common.cuh"
+#include "gdn_launch.h"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+
+constexpr int C = kChunk;
+constexpr int kSegTokens = 1024;   // segment length when long sequences are split
+constexpr int LDA = 65, LDO = 128;   // fp32 row strides: A and T [64][LDA], O staging [64][LDO]
+
+// ---- tcgen05 operand and instruction descriptors ----
+constexpr uint64_t D_K = tc::sdesc_sw128(16, 1024);         // K-major tiles
+constexpr uint64_t D_MN_KQ = tc::sdesc_sw128(16384, 1024);  // K^ of a [K^ | Q^] tile read MN-major
+constexpr uint64_t D_MN_V = tc::sdesc_sw128(8192, 1024);    // a [64][128] tile (blocks 8 KB apart) read MN-major
+constexpr uint32_t ID_KK = tc::idesc_bf16(128, 64, 0, 0);
+constexpr uint32_t ID_GRAM = tc::idesc_f16(128, 64, 0, 0);
+constexpr uint32_t ID_MN_A = tc::idesc_bf16(128, 64, 1, 0);
+constexpr uint32_t ID_MN_B = tc::idesc_bf16(128, 128, 0, 1);
+
+constexpr long long kWaitBudget = 1LL << 31;  // clock cycles (~1 s) before a wait gives up
+
+// ---- per-chunk records (prep pass -> scan passes), in the workspace ----
+// Tiles are stored byte for byte in their shared-memory layout (128-byte
+// swizzle, 1024-byte atoms), so a scan pass moves them with plain bulk copies.
+// Per (chunk, key head):   bf16 [K^ | Q^] tile, 64-column blocks 16 KB apart.
+constexpr uint32_t kRecKQ = 32768;
+// Per (chunk, value head):
+constexpr uint32_t kRecWN = 0;         // -W [t][d_k] bf16, blocks 8 KB apart
+constexpr uint32_t kRecVH = 16384;     // V^ [t][d_v] bf16 (conv + SiLU), blocks 8 KB apart
+constexpr uint32_t kRecTB = 32768;     // T diag(beta) [t][s] bf16
+constexpr uint32_t kRecP = 40960;      // P [t][s] bf16
+constexpr uint32_t kRecGate = 49152;   // fp32 e^gamma [64], e^{gamma_C - gamma} [64]
+constexpr uint32_t kRecGateBytes = 512;
+constexpr uint32_t kRecV = 50176;      // record size (multiple of 1024)
+static_assert(kRecGate + kRecGateBytes <= kRecV && kRecV % 1024 == 0, "value record layout");
+
+struct Smem {
+  uint8_t* base;
+  uint32_t addr;  // shared-window address of base
+  __device__ float* f32(uint32_t off) const { return reinterpret_cast<float*>(base + off); }
+};
+
+// The dynamic shared memory rounded up to a 1024-byte boundary (swizzle atoms).
+__device__ __forceinline__ Smem smem_aligned(uint8_t* raw_base) {
+  const uint32_t raw = tc::smem_u32(raw_base);
+  const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
+  return Smem{raw_base + pad, raw + pad};
+}
+
+__device__ __forceinline__ void store_bf16x4(uint8_t* tile, uint32_t off, float a, float b, float c,
+                                             float d) {
+  uint2 v;
+  v.x = pack_bf16x2(a, b);
+  v.y = pack_bf16x2(c, d);
+  *reinterpret_cast<uint2*>(tile + off) = v;
+}
+
+__device__ __forceinline__ void store_f16x4(uint8_t* tile, uint32_t off, float a, float b, float c,
+                                            float d) {
+  uint2 v;
+  v.x = pack_f16x2(a, b);
+  v.y = pack_f16x2(c, d);
+  *reinterpret_cast<uint2*>(tile + off) = v;
+}
+
+__device__ __forceinline__ void store_bf16x8(uint8_t* tile, uint32_t off, const float* x) {
+  uint4 v;
+  v.x = pack_bf16x2(x[0], x[1]);
+  v.y = pack_bf16x2(x[2], x[3]);
+  v.z = pack_bf16x2(x[4], x[5]);
+  v.w = pack_bf16x2(x[6], x[7]);
+  *reinterpret_cast<uint4*>(tile + off) = v;
+}
+
+// Four SiLUs with one reciprocal: with d_i = 1 + e^{-x_i}, 1/d_1 =
+// d_2 d_3 d_4 / (d_1 d_2 d_3 d_4), and so on.  Inputs are clamped at -20 so the
+// product stays below 2^126 (|silu(x)| < 4.2e-8 for x < -20, which the clamp
+// replaces by silu(-20)); this takes the special-function unit from two
+// operations per SiLU to 1.25.
+__device__ __forceinline__ void silu4(float (&x)[4]) {
+  float d[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = 1.0f + __expf(-fmaxf(x[i], -20.0f));
+  const float d01 = d[0] * d[1], d23 = d[2] * d[3];
+  const float r = __fdividef(1.0f, d01 * d23);   // approximate reciprocal (product < 2^126)
+  const float r01 = r * d23, r23 = r * d01;   // 1/(d0 d1), 1/(d2 d3)
+  x[0] *= r01 * d[1];
+  x[1] *= r01 * d[0];
+  x[2] *= r23 * d[3];
+  x[3] *= r23 * d[2];
+}
+
+// Sums of squares of four tokens' 128 channels (each lane holding 4 channels
+// of each token) -> 1/sqrt(sum + eps) * scale for token i, on every lane.  The
+// first two butterfly steps hand half of the sums to the partner lane, so a
+// lane ends with the full sum of token 2 (lane bit 4) + (lane bit 3).
+__device__ __forceinline__ void l2_rnorm4(const float (&y)[4][4], float eps, float scale, int lane,
+                                          float (&rn)[4]) {
+  float ss[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ss[i] = y[i][0] * y[i][0];
+#pragma unroll
+    for (int e = 1; e < 4; ++e) ss[i] = fmaf(y[i][e], y[i][e], ss[i]);
+  }
+  const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
+  float k0 = hi16 ? ss[2] : ss[0], k1 = hi16 ? ss[3] : ss[1];
+  const float s0 = hi16 ? ss[0] : ss[2], s1 = hi16 ? ss[1] : ss[3];
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  float tot = hi8 ? k1 : k0;
+  tot += __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
+  tot += __shfl_xor_sync(0xffffffffu, tot, 4);
+  tot += __shfl_xor_sync(0xffffffffu, tot, 2);
+  tot += __shfl_xor_sync(0xffffffffu, tot, 1);
+  const float r = rsqrtf(tot + eps) * scale;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) rn[i] = __shfl_sync(0xffffffffu, r, ((i >> 1) << 4) | ((i & 1) << 3));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(tc::smem_u32(mbar)), "r"(bytes)
+               : "memory");
+}
+
+// One 2-D TMA tile load: the box at column x, row y of the tensor map lands at
+// smem_dst and reports its bytes to mbar.  Rows outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* tm, int x, int y, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(tc::smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(tc::smem_u32(mbar))
+      : "memory");
+}
+
+// Bulk copy global -> shared that reports its bytes to mbar (the caller posts
+// the expected byte count); both addresses 16-byte aligned, bytes % 16 == 0.
+__device__ __forceinline__ void bulk_copy(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          tc::smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(tc::smem_u32(mbar))
+      : "memory");
+}
+
+// One bulk copy with its own expected-byte count.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* mbar) {
+  mbar_expect_tx(mbar, bytes);
+  bulk_copy(smem_dst, gmem_src, bytes, mbar);
+}
+
+// Bulk copy shared -> global in the issuing thread's current bulk group.
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+               "r"(tc::smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The issuing thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... and have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Block-wide sync that also orders tensor-memory traffic and makes generic
+// smem writes visible to the tensor core (and to bulk copies).
+__device__ __forceinline__ void sync_for_mma() {
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+}
+
+// One segment of the work list (built on the device from cu_seqlens).
+struct Seg {
+  int n, begin, len, sigma, nsig, k0, c0;   // sequence, token range within it, segment index/count,
+                                            // the sequence's first boundary slot, the segment's
+                                            // first chunk record
+};
+
+__device__ __forceinline__ Seg load_seg(const int* list, int u) {
+  const int* e = list + 4 + 8 * u;
+  return Seg{e[0], e[1], e[2], e[3], e[4], e[5], e[6]};
+}
+
+// Transfer matrices of boundary slot k, value head h: X (the map), S (end state
+// from zero, overwritten by the combine pass with the true start state of the
+// next segment), and the sequence's initial state (first slot only).
+__device__ __forceinline__ float* xfer_ptr(const PrefillArgs& p, int k, int h, int part) {
+  return p.xfer + (((size_t)k * p.h_v + h) * 3 + part) * (size_t)(kD * kD);
+}
+
+// T = (I + A)^{-1} for a strictly lower 64 x 64 matrix A (fp32, row stride
+// LDA): the 16 x 16 diagonal blocks by forward substitution, a column per
+// thread, then the blocks below them one block diagonal at a time,
+//   T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
+// Every thread of the CTA (NT of them) calls it; it ends with a CTA barrier.
+template <int NT>
+__device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, int tid, int lane) {
+  static_assert(NT >= 192 && NT % 32 == 0, "the block levels use up to 192 threads");
+  if (tid < 64) {
+    const int b = tid >> 4, c = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = (r == c) ? 1.0f : 0.0f;
+#pragma unroll
+      for (int s = 0; s < r; ++s) acc = fmaf(-Af[(16 * b + r) * LDA + 16 * b + s], x[s], acc);
+      x[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Tf[(16 * b + r) * LDA + 16 * b + c] = x[r];
+  } else {
+    // zero the blocks above the diagonal
+    for (int e = tid - 64; e < 6 * 256; e += NT - 64) {
+      const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+      const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+      const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+      Tf[(16 * bi + r) * LDA + 16 * bj + c] = 0.0f;
+    }
+  }
+  __syncthreads();
+#pragma unroll 1
+  for (int d = 1; d < 4; ++d) {
+    const int tasks = 64 * (4 - d);
+    if (tid < tasks) {
+      const int j = tid >> 6, i = j + d, c = (tid >> 2) & 15, qr = tid & 3;
+      // M[4qr + r][c] = sum_{k=j}^{i-1} A_ik T_kj
+      float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      for (int kb = j; kb < i; ++kb) {
+#pragma unroll
+        for (int s2 = 0; s2 < 16; ++s2) {
+          const float tv = Tf[(16 * kb + s2) * LDA + 16 * j + c];
+#pragma unroll
+          for (int r = 0; r < 4; ++r) m[r] = fmaf(Af[(16 * i + 4 * qr + r) * LDA + 16 * kb + s2], tv, m[r]);
+        }
+      }
+      float mf[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) mf[4 * q + r] = __shfl_sync(0xffffffffu, m[r], (lane & ~3) | q);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int rr = 4 * qr + r;
+        float acc = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc = fmaf(Tf[(16 * i + rr) * LDA + 16 * i + q], mf[q], acc);
+        Tf[(16 * i + rr) * LDA + 16 * j + c] = -acc;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Launchers of the split prefill (prep pass, then the scan passes).
+cudaError_t launch_prefill_prep(const PrefillArgs& p, unsigned max_chunks, cudaStream_t stream);
+cudaError_t launch_prefill_scan(const PrefillArgs& p, bool transfer, unsigned units, const CUtensorMap& tm_z,
+                                cudaStream_t stream);
+
+}  // namespace gdn

@@ -1,0 +1,775 @@
+// gdn_prefill_split.cu -- the chunked prefill as a chunk-parallel prep pass
+// followed by state scans (sm_103a).
+//
+// In the chunked WY/UT form of the gated delta rule, most of a 64-token
+// chunk's work does not depend on the state S0 entering it: the conv, SiLU
+// and L2 norms, the gates and their cumulative sums gamma, the Gram products
+// [K^; Q^] K^T, A and P, T = (I + A)^{-1}, and W = T diag(beta e^gamma) K^.
+// What does depend on S0 is short and all tensor-core work:
+//
+//   Vn^T = V^T (T diag beta)^T + S0 (-W)^T        U, then the correction
+//   O^T  = e^gamma (S0 Q^T) + Vn^T P^T            (output pass)
+//   S    = e^{gamma_C} S0 + (Vn^T diag(e^{gamma_C - gamma})) K^
+//
+// The prep pass therefore computes the state-free part of every chunk of
+// every sequence at once, one CTA per (chunk, key head) -- the q/k conv and
+// the Gram product are shared by the value heads that read that key head --
+// and stores it as per-chunk records (tiles in their shared-memory layout).
+// The scan passes walk the chunks of each (segment, value head) in order and
+// do only the products above, the record tiles of later chunks loading by
+// bulk copies while the current chunk computes; in the output pass the gated
+// RMSNorm epilogue of a chunk runs while the tensor core works on the next.
+//
+// The transfer pass (segments of a long sequence) runs the same scan from
+// S = 0 and, alongside, X from the identity with v = 0, which yields the
+// segment's affine map S_end = S_start X + S_end(0); the combine pass then
+// chains the maps into every segment's true start state.
+#include <cuda.h>
+
+#include "../../include/gdn.h"
+#include "gdn_common.cuh"
+#include "gdn_launch.h"
+#include "gdn_prefill.cuh"
+#include "gdn_tc.cuh"
+
+namespace gdn {
+namespace {
+
+// ============================== prep pass ==============================
+
+constexpr int kPrepThreads = 256;
+// Shared memory (bytes from a 1024-aligned base).  Sized for two CTAs per SM.
+struct PrepLay {
+  static constexpr uint32_t KQ = 0;             // bf16 [K^ | Q^], 64-column blocks 16 KB apart
+  static constexpr uint32_t KQ16 = 32768;       // fp16 copy of KQ (Gram operands) ...
+  static constexpr uint32_t AF = KQ16;          // ... then A and T fp32 [64][LDA] ...
+  static constexpr uint32_t TF = AF + 64 * LDA * 4;
+  static constexpr uint32_t WN = KQ16;          // ... then -W [t][d_k]
+  static constexpr uint32_t VH = 66560;         // V^ [t][d_v]
+  static constexpr uint32_t TB = VH + 16384;    // T diag(beta)
+  static constexpr uint32_t TW = TB + 8192;     // T diag(beta e^gamma)
+  static constexpr uint32_t P = TW + 8192;      // P
+  static constexpr uint32_t GATE = P + 8192;    // fp32 gamma, beta, e^gamma, e^{gamma_C - gamma} [64]
+  static constexpr uint32_t BYTES = GATE + 4 * 64 * 4 + 1024;   // + slack to align the base
+};
+static_assert(PrepLay::TF + 64 * LDA * 4 <= PrepLay::VH, "A and T overlap V^");
+static_assert(PrepLay::VH % 1024 == 0 && PrepLay::TB % 1024 == 0 && PrepLay::TW % 1024 == 0 &&
+                  PrepLay::P % 1024 == 0,
+              "operand tiles need 1024-byte alignment");
+static_assert(2 * (PrepLay::BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
+constexpr uint32_t TP_G = 0, TP_W = 64, TP_COLS = 128;   // TMEM: Gram [K^;Q^]K^T, W^T
+
+// Conv + SiLU of the 4 tokens tq .. tq+3 of a chunk over this lane's 4
+// channels ch .. ch+3, reading raw inputs from global memory: the carried conv
+// state before the sequence's first token, zeros past its end; padding tokens
+// of a partial chunk come out zero.
+__device__ __forceinline__ void conv_quad(const PrefillArgs& p, int n, int start, int len, int t0, int L, int tq,
+                                          int ch, int Cc, float (&y)[4][4]) {
+  float w[kConvW][4];
+  {
+    const uint4 u0 = *reinterpret_cast<const uint4*>(p.conv_w + (size_t)ch * kConvW);        // channels ch, ch+1
+    const uint4 u1 = *reinterpret_cast<const uint4*>(p.conv_w + (size_t)(ch + 2) * kConvW);  // ch+2, ch+3
+    const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+#pragma unroll
+      for (int j = 0; j < kConvW; ++j) {
+        const int k = e * kConvW + j;   // channel e, tap j
+        w[j][e] = bf16_to_f32((k & 1) ? (wv[k >> 1] >> 16) : (wv[k >> 1] & 0xffffu));
+      }
+  }
+  constexpr int kRows = 4 + kConvW - 1;
+  float x[kRows][4];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int tau = t0 + tq - (kConvW - 1) + r;   // position in the sequence
+    if (tau < 0) {
+      const float4 v4 = *reinterpret_cast<const float4*>(
+          p.conv_state + ((size_t)n * (kConvW - 1) + (kConvW - 1 + tau)) * Cc + ch);
+      x[r][0] = v4.x; x[r][1] = v4.y; x[r][2] = v4.z; x[r][3] = v4.w;
+    } else if (tau < len) {
+      const uint2 v2 = *reinterpret_cast<const uint2*>(p.qkv + (size_t)(start + tau) * Cc + ch);
+      x[r][0] = bf16_to_f32(v2.x & 0xffffu); x[r][1] = bf16_to_f32(v2.x >> 16);
+      x[r][2] = bf16_to_f32(v2.y & 0xffffu); x[r][3] = bf16_to_f32(v2.y >> 16);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[r][e] = 0.0f;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float acc = w[0][e] * x[i][e];
+#pragma unroll
+      for (int j = 1; j < kConvW; ++j) acc = fmaf(w[j][e], x[i + j][e], acc);
+      y[i][e] = tq + i < L ? acc : 0.0f;
+    }
+    silu4(y[i]);
+  }
+}
+
+// One CTA per (chunk, key head): the state-free part of the chunk for the G
+// value heads that read this key head, stored as records.
+__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs p) {
+  using L_ = PrepLay;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t mbar;   // MMA completion
+  __shared__ uint32_t tmem_base_s;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = blockIdx.x / p.h_k, kh = blockIdx.x % p.h_k;
+  if (*p.status == GDN_ERR_DEVICE_BOUNDS) return;   // cu_seqlens rejected by the list kernel
+  const int2 ce = p.chunk_list[c];
+  if (ce.x < 0 || ce.x >= p.n_seqs) return;          // past the last chunk
+  const int n = ce.x, t0 = ce.y;
+  const int start = p.cu_seqlens[n], len = p.cu_seqlens[n + 1] - start;
+  const int L = min(C, len - t0);
+  const int G = p.h_v / p.h_k;
+  const int Cq = p.h_k * kD, Cc = 2 * Cq + p.h_v * kD;
+
+  const Smem sm = smem_aligned(smem_raw);
+  float* Af = sm.f32(L_::AF);
+  float* Tf = sm.f32(L_::TF);
+  float* gam = sm.f32(L_::GATE);
+  float* bet = gam + 64;
+  float* eg = gam + 128;
+  float* egc = gam + 192;
+
+  if (tid == 0) {
+    tc::mbar_init(&mbar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base_s, TP_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base_s;
+  const int quarter = warp & 3, half = warp >> 2;   // TMEM lane quarter, 32-column half
+  const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+  const int row = 32 * quarter + lane;
+  uint32_t phase = 0;
+  auto wait_mma = [&]() -> bool {
+    const bool ok = tc::mbar_wait(&mbar, phase, kWaitBudget);
+    phase ^= 1u;
+    const bool all_ok = __syncthreads_and(ok);
+    tc::fence_after_sync();
+    return all_ok;
+  };
+
+  // ---- conv + SiLU + L2 norms of q and k -> [K^ | Q^] in bf16 and fp16 ----
+  {
+    const float qscale = rsqrtf((float)kD);
+#pragma unroll 1
+    for (int task = warp; task < 2 * (C / 4); task += kPrepThreads / 32) {
+      const int blk = task / (C / 4), tq = 4 * (task % (C / 4));   // blk 0: q, 1: k
+      float y[4][4];
+      conv_quad(p, n, start, len, t0, L, tq, (blk == 0 ? 0 : Cq) + kh * kD + 4 * lane, Cc, y);
+      float rn[4];
+      l2_rnorm4(y, p.l2_eps, blk == 0 ? qscale : 1.0f, lane, rn);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[i][e] *= rn[i];
+        const uint32_t o16 = tc::sw128_off(tq + i, 4 * lane, 16384) + (blk == 0 ? 8192u : 0u);
+        store_bf16x4(sm.base + L_::KQ, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
+        store_f16x4(sm.base + L_::KQ16, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
+      }
+    }
+  }
+  sync_for_mma();
+  if (tid == 0) {
+    // Gram [K^; Q^] K^T in fp16 (rows 0-63: K^K^T, 64-127: Q^K^T)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t a = sm.addr + L_::KQ16 + (k >> 2) * 16384 + (k & 3) * 32;
+      tc::mma_bf16(tmem + TP_G, tc::sdesc_at(D_K, a), tc::sdesc_at(D_K, a), ID_GRAM, k > 0);
+    }
+    tc::mma_commit(&mbar);
+    bulk_store(p.rec_kq + ((size_t)c * p.h_k + kh) * kRecKQ, sm.base + L_::KQ, kRecKQ);
+    bulk_commit();
+  }
+
+  bool ok = true;
+#pragma unroll 1
+  for (int g = 0; g < G; ++g) {
+    const int h = kh * G + g;
+    uint8_t* rv = p.rec_v + ((size_t)c * p.h_v + h) * kRecV;
+    if (g > 0) {   // the previous head's tiles must have left shared memory
+      if (tid == 0) bulk_wait_read();
+      __syncthreads();
+    }
+    // ---- gates and their cumulative sums (warp 0) ----
+    if (warp == 0) {
+      const float A_exp = __expf(p.A_log[h]);
+      const float dtb = p.dt_bias[h];
+      float g2[2], b2[2];
+#pragma unroll
+      for (int uu = 0; uu < 2; ++uu) {
+        const int t = lane + 32 * uu;
+        if (t < L) {
+          const size_t pidx = (size_t)(start + t0 + t) * p.h_v + h;
+          g2[uu] = -A_exp * softplus(bf16_to_f32(p.a[pidx]) + dtb);
+          b2[uu] = sigmoid(bf16_to_f32(p.b[pidx]));
+        } else {
+          g2[uu] = 0.0f;
+          b2[uu] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int uu = 0; uu < 2; ++uu) {
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, g2[uu], off);
+          if (lane >= off) g2[uu] += y;
+        }
+      }
+      g2[1] += __shfl_sync(0xffffffffu, g2[0], 31);
+      const float gC = __shfl_sync(0xffffffffu, g2[1], 31);
+      float* rg = reinterpret_cast<float*>(rv + kRecGate);
+#pragma unroll
+      for (int uu = 0; uu < 2; ++uu) {
+        const int t = lane + 32 * uu;
+        const float e1 = __expf(g2[uu]), e2 = __expf(gC - g2[uu]);
+        gam[t] = g2[uu];
+        bet[t] = b2[uu];
+        eg[t] = e1;
+        egc[t] = e2;
+        rg[t] = e1;
+        rg[64 + t] = e2;
+      }
+    }
+    // ---- conv + SiLU of this head's v -> V^ ----
+#pragma unroll 1
+    for (int task = warp; task < C / 4; task += kPrepThreads / 32) {
+      const int tq = 4 * task;
+      float y[4][4];
+      conv_quad(p, n, start, len, t0, L, tq, 2 * Cq + h * kD + 4 * lane, Cc, y);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        store_bf16x4(sm.base + L_::VH, tc::sw128_off(tq + i, 4 * lane, 8192), y[i][0], y[i][1], y[i][2], y[i][3]);
+    }
+    sync_for_mma();
+    if (tid == 0) {
+      bulk_store(rv + kRecVH, sm.base + L_::VH, 16384);
+      bulk_commit();
+    }
+    if (g == 0 && !wait_mma()) { ok = false; break; }   // the Gram product (and KQ16 is free)
+
+    // ---- A (fp32) and P (bf16 tile) from the Gram rows: lane quarters 0-1 hold
+    //      K^K^T rows, 2-3 Q^K^T rows; the two warps of a quarter split its columns ----
+    {
+      float v[32];
+      const int t = row & 63, c0 = 32 * half;
+      const float gt = gam[t];
+      tc::tmem_ld32(tmem + lane_base + TP_G + c0, v);
+      if (quarter < 2) {
+        const float bt = bet[t];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int s = c0 + i;
+          Af[t * LDA + s] = s < t ? bt * __expf(gt - gam[s]) * v[i] : 0.0f;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int s = c0 + i;
+          v[i] = s <= t ? v[i] * __expf(gt - gam[s]) : 0.0f;
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + L_::P, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
+      }
+    }
+    sync_for_mma();
+    if (tid == 0) {
+      bulk_store(rv + kRecP, sm.base + L_::P, 8192);
+      bulk_commit();
+    }
+
+    // ---- T = (I + A)^{-1}, then T diag(beta) and T diag(beta e^gamma) as bf16 tiles ----
+    solve_unit_lower<kPrepThreads>(Af, Tf, tid, lane);
+    for (int e = tid; e < 64 * 8; e += kPrepThreads) {
+      const int t = e >> 3, c8 = (e & 7) * 8;
+      float xb[8], xw[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float tv = Tf[t * LDA + c8 + q];
+        xb[q] = tv * bet[c8 + q];
+        xw[q] = xb[q] * eg[c8 + q];
+      }
+      store_bf16x8(sm.base + L_::TB, tc::sw128_off(t, c8, 0), xb);
+      store_bf16x8(sm.base + L_::TW, tc::sw128_off(t, c8, 0), xw);
+    }
+    sync_for_mma();
+    if (tid == 0) {
+      bulk_store(rv + kRecTB, sm.base + L_::TB, 8192);
+      bulk_commit();
+      // W^T = K^T (T diag(beta e^gamma))^T
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16(tmem + TP_W, tc::sdesc_at(D_MN_KQ, sm.addr + L_::KQ + k * 2048),
+                     tc::sdesc_at(D_K, sm.addr + L_::TW + k * 32), ID_MN_A, k > 0);
+      tc::mma_commit(&mbar);
+    }
+    if (!wait_mma()) { ok = false; break; }
+
+    // ---- -W tile [t][d_k] (over A and T, which are dead) ----
+    {
+      float v[32];
+      tc::tmem_ld32(tmem + lane_base + TP_W + 32 * half, v);
+      uint8_t* wn = sm.base + L_::WN;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(32 * half + i, row, 8192)) = f32_to_bf16(-v[i]);
+    }
+    sync_for_mma();
+    if (tid == 0) {
+      bulk_store(rv + kRecWN, sm.base + L_::WN, 16384);
+      bulk_commit();
+    }
+  }
+
+  if (tid == 0) {
+    if (!ok) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+    bulk_wait_all();   // the records are written before this CTA's shared memory goes away
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, TP_COLS);
+}
+
+// ============================== scan passes ==============================
+
+constexpr int kScanThreads = 512;   // 16 warps: 4 per TMEM lane quarter
+template <bool kXfer> struct ScanLay;
+template <> struct ScanLay<false> {    // output pass
+  static constexpr uint32_t S = 0;          // S bf16 [d_v][d_k], K blocks 16 KB apart
+  static constexpr uint32_t X = 0;          // (unused)
+  static constexpr uint32_t KQ = 32768;     // two [K^ | Q^] buffers
+  static constexpr uint32_t KQ_BUF = 32768;
+  static constexpr uint32_t WN = 98304;     // -W | V^ | T diag(beta): the record's first 40 KB, one copy
+  static constexpr uint32_t P = WN + 40960;
+  static constexpr uint32_t GT = P + 8192;  // two gate buffers: e^gamma [64], e^{gamma_C - gamma} [64]
+  static constexpr uint32_t Z = GT + 1024;  // z bf16 [64][128]
+  static constexpr uint32_t VN = Z + 16384;     // Vn^T [d_v][t]
+  static constexpr uint32_t VNS = VN + 16384;   // Vn^T diag(e^{gamma_C - gamma})
+  static constexpr uint32_t OST = VN;           // O fp32 [64][LDO], over VN and VNS once they are consumed
+  static constexpr uint32_t NW = VNS + 16384;   // RMSNorm weight
+  static constexpr uint32_t BYTES = NW + 512 + 1024;
+};
+template <> struct ScanLay<true> {     // transfer pass
+  static constexpr uint32_t S = 0;
+  static constexpr uint32_t X = 32768;      // X bf16 [d_k][d_k]
+  static constexpr uint32_t KQ = 65536;     // two K^ buffers [K^ kb0 | K^ kb1]
+  static constexpr uint32_t KQ_BUF = 16384;
+  static constexpr uint32_t WN = 98304;
+  static constexpr uint32_t P = 0;          // (unused)
+  static constexpr uint32_t GT = WN + 40960;
+  static constexpr uint32_t Z = 0;          // (unused)
+  static constexpr uint32_t VN = GT + 1024;     // X's Vn^T diag(e^{gamma_C - gamma})
+  static constexpr uint32_t VNS = VN + 16384;   // S's Vn^T diag(e^{gamma_C - gamma})
+  static constexpr uint32_t OST = 0;        // (unused)
+  static constexpr uint32_t NW = 0;         // (unused)
+  static constexpr uint32_t BYTES = VNS + 16384 + 1024;
+};
+template <bool kXfer> struct ScanMap : ScanLay<kXfer> {
+  using L_ = ScanLay<kXfer>;
+  static constexpr uint32_t VH = L_::WN + kRecVH;
+  static constexpr uint32_t TB = L_::WN + kRecTB;
+  static_assert(L_::WN % 1024 == 0 && VH % 1024 == 0 && TB % 1024 == 0 && L_::VN % 1024 == 0 &&
+                    L_::VNS % 1024 == 0 && L_::KQ % 1024 == 0 && (kXfer || L_::P % 1024 == 0),
+                "operand tiles need 1024-byte alignment");
+  static_assert(kXfer || L_::Z % 128 == 0, "TMA destination alignment");
+  static_assert(kXfer || L_::OST + 64 * LDO * 4 <= L_::NW, "O staging overlaps the norm weight");
+  static_assert(L_::BYTES <= 227 * 1024, "shared memory");
+};
+// TMEM columns
+constexpr uint32_t TS_S = 0, TS_O1 = 128, TS_U = 192, TS_O2 = 256;   // output pass
+constexpr uint32_t TS_X = 128, TS_UX = 256, TS_VX = 320;             // transfer pass (TS_UX: S's Vn)
+constexpr uint32_t TS_COLS = 512;
+
+// Block-wide sync for the tensor core that also ANDs a per-thread verdict.
+__device__ __forceinline__ bool sync_for_mma_and(bool ok) {
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  const bool all = __syncthreads_and(ok);
+  tc::fence_after_sync();
+  return all;
+}
+
+template <bool kXfer>
+__global__ void __launch_bounds__(kScanThreads, 1)
+    scan_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_z) {
+  using M = ScanMap<kXfer>;
+  constexpr uint32_t TU = kXfer ? TS_UX : TS_U;   // U, then S's Vn^T
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t mb_mma;     // MMA completion
+  __shared__ __align__(8) uint64_t mb_kq[2];   // [K^ | Q^] buffers
+  __shared__ __align__(8) uint64_t mb_a;       // -W | V^ | T diag(beta) and the gates
+  __shared__ __align__(8) uint64_t mb_p;       // P (output pass)
+  __shared__ __align__(8) uint64_t mb_z;       // z (output pass)
+  __shared__ uint32_t tmem_base_s;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int u = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
+  if (u >= p.seg_list[0]) return;
+  const Seg sg = load_seg(p.seg_list, u);
+  if (kXfer && sg.sigma == sg.nsig - 1) return;   // the last segment needs no transfer map
+  const int n = sg.n;
+  const int G = p.h_v / p.h_k, kh = h / G;
+  const int start = p.cu_seqlens[n];
+  const int seg_end = sg.begin + sg.len;
+  const int nch = (sg.len + C - 1) / C;
+
+  // where the state comes from and goes to
+  const float* S_init = nullptr;
+  float* S_final = nullptr;
+  float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
+  if (!kXfer) {
+    if (sg.nsig == 1) {
+      S_init = ssm;
+      S_final = ssm;
+    } else {
+      S_init = sg.sigma == 0 ? xfer_ptr(p, sg.k0, h, 2) : xfer_ptr(p, sg.k0 + sg.sigma - 1, h, 1);
+      S_final = sg.sigma == sg.nsig - 1 ? ssm : nullptr;
+    }
+  }
+
+  const Smem sm = smem_aligned(smem_raw);
+  float* Ost = sm.f32(M::OST);
+  float* nw = sm.f32(M::NW);
+  if (tid == 0) {
+    tc::mbar_init(&mb_mma, 1);
+    tc::mbar_init(&mb_kq[0], 1);
+    tc::mbar_init(&mb_kq[1], 1);
+    tc::mbar_init(&mb_a, 1);
+    tc::mbar_init(&mb_p, 1);
+    tc::mbar_init(&mb_z, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base_s, TS_COLS);
+  if (!kXfer && tid < kD) nw[tid] = p.norm_w[tid];
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base_s;
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+  const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
+  const int part = warp >> 2;               // which quarter of a lane quarter's columns
+
+  auto rec_kq = [&](int j) { return p.rec_kq + ((size_t)(sg.c0 + j) * p.h_k + kh) * kRecKQ; };
+  auto rec_v = [&](int j) { return p.rec_v + ((size_t)(sg.c0 + j) * p.h_v + h) * kRecV; };
+  // record loads, issued by one thread (tid 32); each barrier has at most one in flight
+  auto load_kq = [&](int j) {
+    uint8_t* dst = sm.base + M::KQ + (j & 1) * M::KQ_BUF;
+    if (!kXfer) {
+      bulk_load(dst, rec_kq(j), kRecKQ, &mb_kq[j & 1]);
+    } else {   // the K^ halves only
+      mbar_expect_tx(&mb_kq[j & 1], 16384);
+      bulk_copy(dst, rec_kq(j), 8192, &mb_kq[j & 1]);
+      bulk_copy(dst + 8192, rec_kq(j) + 16384, 8192, &mb_kq[j & 1]);
+    }
+  };
+  auto load_a = [&](int j) {
+    mbar_expect_tx(&mb_a, kRecP + kRecGateBytes);
+    bulk_copy(sm.base + M::WN, rec_v(j), kRecP, &mb_a);
+    bulk_copy(sm.base + M::GT + (j & 1) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_a);
+  };
+  auto load_p = [&](int j) { bulk_load(sm.base + M::P, rec_v(j) + kRecP, 8192, &mb_p); };
+  auto load_z = [&](int j) {
+    mbar_expect_tx(&mb_z, C * kD * 2);
+    tma_load_2d(sm.base + M::Z, &tm_z, h * kD, start + sg.begin + C * j, &mb_z);
+  };
+  // copies in flight per barrier, and waits completed (the k-th copy on a barrier
+  // completes its phase of parity k & 1); only the abort path needs these
+  bool pend_kq[2] = {true, nch > 1}, pend_a = true, pend_p = !kXfer, pend_z = !kXfer;
+  uint32_t w_kq[2] = {0, 0}, w_a = 0, w_p = 0, w_z = 0;
+  if (tid == 32) {
+    load_kq(0);
+    if (nch > 1) load_kq(1);
+    load_a(0);
+    if (!kXfer) {
+      load_p(0);
+      load_z(0);
+    }
+  }
+
+  // initial state(s): fp32 into TMEM, bf16 into the operand tile(s)
+  {
+    const int col0 = part * 32;
+    float v[32];
+    if (!kXfer) {
+      const float4* src = reinterpret_cast<const float4*>(S_init + (size_t)row * kD + col0);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 x = src[q];
+        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    }
+    tc::tmem_st32(tmem + lane_base + TS_S + col0, v);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::S, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
+    if (kXfer) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = (col0 + i == row) ? 1.0f : 0.0f;
+      tc::tmem_st32(tmem + lane_base + TS_X + col0, v);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::X, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
+    }
+  }
+  sync_for_mma();
+
+  uint32_t phase = 0;
+  auto wait_mma = [&]() -> bool {
+    const bool ok = tc::mbar_wait(&mb_mma, phase, kWaitBudget);
+    phase ^= 1u;
+    const bool all_ok = __syncthreads_and(ok);
+    tc::fence_after_sync();
+    return all_ok;
+  };
+  // output pass: the gated RMSNorm epilogue of chunk jj from the O staging, a
+  // warp per token and 4 channels per lane; then z of chunk jj + 1 may load
+  auto epilogue = [&](int jj) -> bool {
+    const int t0e = sg.begin + C * jj, Le = min(C, seg_end - t0e);
+    if (!__syncthreads_and(tc::mbar_wait(&mb_z, w_z & 1u, kWaitBudget))) return false;
+    pend_z = false;
+    ++w_z;
+    for (int t = warp; t < Le; t += kScanThreads / 32) {
+      const float4 o4 = reinterpret_cast<const float4*>(Ost + t * LDO)[lane];
+      float ss = o4.x * o4.x;
+      ss = fmaf(o4.y, o4.y, ss);
+      ss = fmaf(o4.z, o4.z, ss);
+      ss = fmaf(o4.w, o4.w, ss);
+      ss = warp_sum(ss);
+      const float rstd = rsqrtf(ss * (1.0f / kD) + p.rms_eps);
+      const uint2 zr = *reinterpret_cast<const uint2*>(sm.base + M::Z + t * 256 + lane * 8);
+      const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
+      float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
+                    bf16_to_f32(zr.y >> 16)};
+      silu4(g);
+      uint2 o;
+      o.x = pack_bf16x2(o4.x * rstd * w4.x * g[0], o4.y * rstd * w4.y * g[1]);
+      o.y = pack_bf16x2(o4.z * rstd * w4.z * g[2], o4.w * rstd * w4.w * g[3]);
+      *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0e + t) * p.h_v + h) * kD + 4 * lane) = o;
+    }
+    __syncthreads();   // the O staging and the z buffer are read
+    if (jj + 1 < nch) {
+      if (tid == 32) load_z(jj + 1);
+      pend_z = true;
+    }
+    return true;
+  };
+
+  bool aborted = false;
+  for (int j = 0; j < nch; ++j) {
+    const float* eg = sm.f32(M::GT + (j & 1) * 512);
+    const float* egc = eg + 64;
+    const uint32_t kq = sm.addr + M::KQ + (j & 1) * M::KQ_BUF;
+    {
+      bool ok = tc::mbar_wait(&mb_kq[j & 1], w_kq[j & 1] & 1u, kWaitBudget);
+      ok = tc::mbar_wait(&mb_a, w_a & 1u, kWaitBudget) && ok;
+      if (!__syncthreads_and(ok)) { aborted = true; break; }
+      pend_kq[j & 1] = false;
+      pend_a = false;
+      ++w_kq[j & 1];
+      ++w_a;
+    }
+
+    // ---- batch 1: [O1 = S0 Q^T,] U = V^T (T diag beta)^T, Vn^T = U + S0 (-W)^T
+    //      [, transfer: Vn_X^T = X0 (-W)^T] ----
+    if (tid == 0) {
+      if (!kXfer) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TS_O1, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                       tc::sdesc_at(D_K, kq + kb * 16384 + 8192 + ks), ID_KK, k > 0);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16(tmem + TU, tc::sdesc_at(D_MN_V, sm.addr + M::VH + k * 2048),
+                     tc::sdesc_at(D_K, sm.addr + M::TB + k * 32), ID_MN_A, k > 0);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+        tc::mma_bf16(tmem + TU, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                     tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
+      }
+      if (kXfer) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TS_VX, tc::sdesc_at(D_K, sm.addr + M::X + kb * 16384 + ks),
+                       tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, k > 0);
+        }
+      }
+      tc::mma_commit(&mb_mma);
+    }
+    // meanwhile: pre-scale the fp32 state(s) by the chunk's total decay ...
+    {
+      const float dC = eg[C - 1];
+#pragma unroll
+      for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
+        float v[32];
+        const uint32_t ta = tmem + lane_base + (zz ? TS_X : TS_S) + part * 32;
+        tc::tmem_ld32(ta, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= dC;
+        tc::tmem_st32(ta, v);
+      }
+    }
+    // ... and write out the previous chunk
+    if (!kXfer && j > 0 && !epilogue(j - 1)) { aborted = true; break; }
+    if (!wait_mma()) { aborted = true; break; }
+    // the next chunk's -W | V^ | T diag(beta) and gates go where batch 1 has finished
+    if (j + 1 < nch) {
+      if (tid == 32) load_a(j + 1);
+      pend_a = true;
+    }
+
+    // ---- Vn^T tiles, row = d_v index: output pass plain and decay-weighted,
+    //      transfer pass X's and S's, both decay-weighted ----
+    {
+      float v[16], vs[16];
+      tc::tmem_ld16(tmem + lane_base + TU + part * 16, v);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) vs[i] = v[i] * egc[part * 16 + i];
+      if (kXfer) {
+        tc::tmem_ld16(tmem + lane_base + TS_VX + part * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] *= egc[part * 16 + i];
+      }
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const uint32_t off = tc::sw128_off(row, part * 16 + 8 * m, 0);
+        store_bf16x8(sm.base + M::VN, off, v + 8 * m);
+        store_bf16x8(sm.base + M::VNS, off, vs + 8 * m);
+      }
+    }
+    {
+      const bool ok = kXfer || tc::mbar_wait(&mb_p, w_p & 1u, kWaitBudget);
+      if (!sync_for_mma_and(ok)) { aborted = true; break; }
+      if (!kXfer) {
+        pend_p = false;
+        ++w_p;
+      }
+    }
+
+    // ---- batch 2: [O2 = Vn^T P^T,] S += Vn^T diag(e^{gC-g}) K^ [, X likewise] ----
+    if (tid == 0) {
+      if (!kXfer) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
+                       tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
+                       tc::sdesc_at(D_MN_KQ, kq + k * 2048), ID_MN_B, 1u);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
+                       tc::sdesc_at(D_MN_V, kq + k * 2048), ID_MN_B, 1u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_X, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
+                       tc::sdesc_at(D_MN_V, kq + k * 2048), ID_MN_B, 1u);
+      }
+      tc::mma_commit(&mb_mma);
+    }
+    if (!wait_mma()) { aborted = true; break; }
+    // P of the next chunk and [K^ | Q^] of the one after go where batch 2 has finished
+    if (!kXfer && j + 1 < nch) {
+      if (tid == 32) load_p(j + 1);
+      pend_p = true;
+    }
+    if (j + 2 < nch) {
+      if (tid == 32) load_kq(j + 2);
+      pend_kq[j & 1] = true;
+    }
+
+    // ---- new state(s) -> bf16 operand tiles; output pass: O = e^gamma O1 + O2 -> fp32 staging ----
+    {
+#pragma unroll
+      for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
+        float v[32];
+        tc::tmem_ld32(tmem + lane_base + (zz ? TS_X : TS_S) + part * 32, v);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          store_bf16x8(sm.base + (zz ? M::X : M::S), tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
+      }
+      if (!kXfer) {
+        float o1[16], o2[16];
+        tc::tmem_ld16(tmem + lane_base + TS_O1 + part * 16, o1);
+        tc::tmem_ld16(tmem + lane_base + TS_O2 + part * 16, o2);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t = part * 16 + i;
+          Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
+        }
+      }
+    }
+    sync_for_mma();
+  }
+  if (!kXfer && !aborted && !epilogue(nch - 1)) aborted = true;
+
+  if (aborted) {
+    if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+    // let this CTA's own copies finish (bounded) before its shared memory goes
+    // away (a copy that already landed passes its wait at once)
+    if (pend_kq[0]) tc::mbar_wait(&mb_kq[0], w_kq[0] & 1u, kWaitBudget);
+    if (pend_kq[1]) tc::mbar_wait(&mb_kq[1], w_kq[1] & 1u, kWaitBudget);
+    if (pend_a) tc::mbar_wait(&mb_a, w_a & 1u, kWaitBudget);
+    if (pend_p) tc::mbar_wait(&mb_p, w_p & 1u, kWaitBudget);
+    if (pend_z) tc::mbar_wait(&mb_z, w_z & 1u, kWaitBudget);
+  } else {
+    // final state(s) back to global memory
+#pragma unroll
+    for (int zz = 0; zz < 2; ++zz) {
+      float* dst_base = kXfer ? xfer_ptr(p, sg.k0 + sg.sigma, h, zz == 0 ? 1 : 0) : (zz == 0 ? S_final : nullptr);
+      if (dst_base == nullptr) continue;
+      float4* dst = reinterpret_cast<float4*>(dst_base + (size_t)row * kD + part * 32);
+      float v[32];
+      tc::tmem_ld32(tmem + lane_base + (zz ? TS_X : TS_S) + part * 32, v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, TS_COLS);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_prep(const PrefillArgs& p, unsigned max_chunks, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)PrepLay::BYTES);
+  if (e != cudaSuccess) return e;
+  prep_kernel<<<max_chunks * (unsigned)p.h_k, kPrepThreads, PrepLay::BYTES, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_scan(const PrefillArgs& p, bool transfer, unsigned units, const CUtensorMap& tm_z,
+                                cudaStream_t stream) {
+  cudaError_t e;
+  if (transfer) {
+    if ((e = cudaFuncSetAttribute(scan_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)ScanLay<true>::BYTES)) != cudaSuccess)
+      return e;
+    scan_kernel<true><<<units * (unsigned)p.h_v, kScanThreads, ScanLay<true>::BYTES, stream>>>(p, tm_z);
+  } else {
+    if ((e = cudaFuncSetAttribute(scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)ScanLay<false>::BYTES)) != cudaSuccess)
+      return e;
+    scan_kernel<false><<<units * (unsigned)p.h_v, kScanThreads, ScanLay<false>::BYTES, stream>>>(p, tm_z);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace gdn
