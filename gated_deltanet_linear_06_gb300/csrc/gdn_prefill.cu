@@ -79,8 +79,6 @@ constexpr uint32_t F32_BYTES = 2 * 64 * LDA * 4;
 // block) land over -W, T, P and the fp32 area, which are dead from the last MMA of
 // the previous chunk to the end of this chunk's conv stage; z ([64][128]) lands in
 // the fp32 area's tail between the state-correction MMA and the epilogue.
-constexpr uint32_t RAW_BOX_ROWS = C + kConvW - 1;     // a chunk and its 3-token halo
-constexpr uint32_t RAW_BLK = RAW_BOX_ROWS * 256;       // one channel block: [67 rows][128 bf16]
 struct Map : Lay {
   using L_ = Lay;
   static constexpr uint32_t CW = L_::F32 + F32_BYTES;   // conv weights fp32 [3][tap][128]
@@ -285,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     //      of every block and a lane 4 channels of them, so each raw row is read once
     //      for all the taps that use it and the four tokens are independent work ----
     {
-      constexpr int kRows = 4 + kConvW - 1;   // raw rows under a token quad
       const int tq = 4 * warp;
 #pragma unroll
       for (int blk = 0; blk < 3; ++blk) {
@@ -295,34 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float4 w4 = reinterpret_cast<const float4*>(cw + (blk * 4 + j) * kD)[lane];
           w[j][0] = w4.x; w[j][1] = w4.y; w[j][2] = w4.z; w[j][3] = w4.w;
         }
-        float x[kRows][4];
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          const int tau = t0 + tq - (kConvW - 1) + r;   // position in the sequence
-          if (tau >= 0) {
-            const uint2 v2 = *reinterpret_cast<const uint2*>(sm.base + M::RAW + blk * RAW_BLK + (tq + r) * 256 +
-                                                             lane * 8);
-            x[r][0] = bf16_to_f32(v2.x & 0xffffu); x[r][1] = bf16_to_f32(v2.x >> 16);
-            x[r][2] = bf16_to_f32(v2.y & 0xffffu); x[r][3] = bf16_to_f32(v2.y >> 16);
-          } else {   // before the sequence's first token of this call: the carried conv state
-            const int ch = (blk == 0 ? kh * kD : blk == 1 ? Cq + kh * kD : 2 * Cq + h * kD) + 4 * lane;
-            const float4 v4 = *reinterpret_cast<const float4*>(
-                p.conv_state + ((size_t)n * (kConvW - 1) + (kConvW - 1 + tau)) * Cc + ch);
-            x[r][0] = v4.x; x[r][1] = v4.y; x[r][2] = v4.z; x[r][3] = v4.w;
-          }
-        }
         float y[4][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float acc = w[0][e] * x[i][e];
-#pragma unroll
-            for (int j = 1; j < kConvW; ++j) acc = fmaf(w[j][e], x[i + j][e], acc);
-            y[i][e] = tq + i < L ? acc : 0.0f;   // padding tokens of a partial chunk are zero
-          }
-          silu4(y[i]);
-        }
+        conv_quad_staged(sm.base + M::RAW + blk * RAW_BLK,
+                         p.conv_state + (size_t)n * (kConvW - 1) * Cc +
+                             (blk == 0 ? kh * kD : blk == 1 ? Cq + kh * kD : 2 * Cq + h * kD) + 4 * lane,
+                         Cc, t0, L, tq, lane, w, y);
         if (blk < 2) {
           float rn[4];
           l2_rnorm4(y, p.l2_eps, blk == 0 ? qscale : 1.0f, lane, rn);
@@ -657,115 +631,6 @@ __global__ void __launch_bounds__(256) seg_list_kernel(PrefillArgs p) {
   }
 }
 
-// Combines the transfer maps of a multi-segment sequence, 32 state rows per
-// CTA (the rows of S evolve independently): S_{sigma+1} = S_sigma X_sigma +
-// S_sigma^0, in fp32, written over the slot's end state, after saving the
-// sequence's initial state (so the output pass never reads a state that the
-// last segment's CTA is writing).  The 64 KB maps stream through two shared
-// buffers by bulk TMA copies, the next one landing while the current step
-// computes.
-constexpr int kCombineRows = 32;
-constexpr uint32_t kMapBytes = kD * kD * 4;
-constexpr uint32_t kCombineSmem = 2 * kMapBytes + kCombineRows * kD * 4 + 16;
-
-
-__global__ void __launch_bounds__(256) combine_kernel(PrefillArgs p) {
-  extern __shared__ __align__(128) float csm[];
-  float* Xs = csm;                        // two [128][128] buffers
-  float* Sr = csm + 2 * kD * kD;          // [32][128]
-  __shared__ __align__(8) uint64_t mbar[2];
-  const int per = p.h_v * (kD / kCombineRows);
-  const int u = blockIdx.x / per, rem = blockIdx.x % per;
-  const int h = rem / (kD / kCombineRows), rb = rem % (kD / kCombineRows);
-  if (u >= p.multi_list[0]) return;
-  const int* e = p.multi_list + 4 + 4 * u;
-  const int n = e[0], k0 = e[1], nsig = e[2];
-  const int r0 = rb * kCombineRows;
-  const int tid = threadIdx.x;
-  const int steps = nsig - 1;
-  if (tid == 0) {
-    tc::mbar_init(&mbar[0], 1);
-    tc::mbar_init(&mbar[1], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-  // copies issued / waited per buffer (the same on every thread: tid 0 issues
-  // under conditions every thread evaluates alike)
-  int issued[2] = {1, steps > 1 ? 1 : 0}, waited[2] = {0, 0};
-  if (tid == 0) {
-    bulk_load(Xs, xfer_ptr(p, k0, h, 0), kMapBytes, &mbar[0]);
-    if (steps > 1) bulk_load(Xs + kD * kD, xfer_ptr(p, k0 + 1, h, 0), kMapBytes, &mbar[1]);
-  }
-  const float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
-  float* init = xfer_ptr(p, k0, h, 2);
-  for (int i = tid; i < kCombineRows * kD / 4; i += 256) {
-    const float4 v = reinterpret_cast<const float4*>(ssm + (size_t)r0 * kD)[i];
-    reinterpret_cast<float4*>(Sr)[i] = v;
-    reinterpret_cast<float4*>(init + (size_t)r0 * kD)[i] = v;
-  }
-  const int i = (tid >> 4) * 2, c0 = (tid & 15) * 8;   // this thread: rows i, i+1; columns c0 .. c0+7
-  float4 b[2][2];
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    const float* Bn = xfer_ptr(p, k0, h, 1) + (size_t)(r0 + i + r) * kD + c0;
-    b[r][0] = reinterpret_cast<const float4*>(Bn)[0];
-    b[r][1] = reinterpret_cast<const float4*>(Bn)[1];
-  }
-  bool ok = true;
-  for (int sg = 0; sg < steps; ++sg) {
-    float* Sg = xfer_ptr(p, k0 + sg, h, 1);
-    float acc[2][8];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      acc[r][0] = b[r][0].x; acc[r][1] = b[r][0].y; acc[r][2] = b[r][0].z; acc[r][3] = b[r][0].w;
-      acc[r][4] = b[r][1].x; acc[r][5] = b[r][1].y; acc[r][6] = b[r][1].z; acc[r][7] = b[r][1].w;
-    }
-    if (sg + 1 < steps) {   // next step's end-state rows, into registers
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const float* Bn = xfer_ptr(p, k0 + sg + 1, h, 1) + (size_t)(r0 + i + r) * kD + c0;
-        b[r][0] = reinterpret_cast<const float4*>(Bn)[0];
-        b[r][1] = reinterpret_cast<const float4*>(Bn)[1];
-      }
-    }
-    ok = tc::mbar_wait(&mbar[sg & 1], (uint32_t)((sg >> 1) & 1), kWaitBudget);
-    if (!__syncthreads_and(ok)) break;   // also: the initial rows of Sr are in place
-    ++waited[sg & 1];
-    const float* X = Xs + (sg & 1) * kD * kD;
-#pragma unroll 4
-    for (int j = 0; j < kD; ++j) {
-      const float s0 = Sr[i * kD + j], s1 = Sr[(i + 1) * kD + j];
-      const float4 x0 = reinterpret_cast<const float4*>(X + j * kD + c0)[0];
-      const float4 x1 = reinterpret_cast<const float4*>(X + j * kD + c0)[1];
-      const float xv[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        acc[0][q] = fmaf(s0, xv[q], acc[0][q]);
-        acc[1][q] = fmaf(s1, xv[q], acc[1][q]);
-      }
-    }
-    __syncthreads();   // every read of Sr and of this buffer is done
-    if (sg + 2 < steps) {
-      if (tid == 0) bulk_load(Xs + (sg & 1) * kD * kD, xfer_ptr(p, k0 + sg + 2, h, 0), kMapBytes, &mbar[sg & 1]);
-      ++issued[sg & 1];
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) Sr[(i + r) * kD + c0 + q] = acc[r][q];
-      float4* dst = reinterpret_cast<float4*>(Sg + (size_t)(r0 + i + r) * kD + c0);
-      dst[0] = make_float4(acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
-      dst[1] = make_float4(acc[r][4], acc[r][5], acc[r][6], acc[r][7]);
-    }
-  }
-  if (!ok) {
-    if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
-    // the map copies this CTA started must land (bounded) before its smem goes away
-    for (int q = 0; q < 2; ++q)
-      for (; waited[q] < issued[q]; ++waited[q]) tc::mbar_wait(&mbar[q], (uint32_t)(waited[q] & 1), kWaitBudget);
-  }
-}
-
 // The last conv_w - 1 raw inputs of each sequence become its conv state
 // (rows of the old state fill in when the sequence is shorter than that).
 __global__ void __launch_bounds__(256) conv_state_kernel(PrefillArgs p) {
@@ -882,9 +747,6 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     fused_kernel<<<(unsigned)p.n_seqs * (unsigned)p.h_v, kThreads, Map::BYTES, stream>>>(p, tm_qkv, tm_z);
   } else {
-    if ((e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)kCombineSmem)) != cudaSuccess)
-      return e;
     // Split long sequences into segments scanned in parallel only when one CTA
     // per (sequence, value head) would leave the GPU short of work: the
     // transfer pass that makes segments independent is a second scan.
@@ -897,11 +759,10 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
     const unsigned units = (unsigned)(slots + p.n_seqs);
     seg_list_kernel<<<1, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_prefill_prep(p, (unsigned)l.max_chunks, stream)) != cudaSuccess) return e;
+    if ((e = launch_prefill_prep(p, (unsigned)l.max_chunks, tm_qkv, stream)) != cudaSuccess) return e;
     if (slots > 0) {   // some sequence may be longer than one segment
       if ((e = launch_prefill_scan(p, true, units, tm_z, stream)) != cudaSuccess) return e;
-      combine_kernel<<<(unsigned)slots * (unsigned)p.h_v * (kD / kCombineRows), 256, kCombineSmem, stream>>>(p);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = launch_prefill_combine(p, (unsigned)slots, stream)) != cudaSuccess) return e;
     }
     if ((e = launch_prefill_scan(p, false, units, tm_z, stream)) != cudaSuccess) return e;
   }

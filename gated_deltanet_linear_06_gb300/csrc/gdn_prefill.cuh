@@ -40,6 +40,12 @@ constexpr uint32_t kRecGateBytes = 512;
 constexpr uint32_t kRecV = 50176;      // record size (multiple of 1024)
 static_assert(kRecGate + kRecGateBytes <= kRecV && kRecV % 1024 == 0, "value record layout");
 
+// Raw inputs of a chunk staged in shared memory by a 2-D TMA load: the q, k or
+// v rows of tokens t0-3 .. t0+63 (a chunk and its conv halo), one
+// [67 rows][128 bf16] box per 128-channel block.
+constexpr uint32_t RAW_BOX_ROWS = C + kConvW - 1;
+constexpr uint32_t RAW_BLK = RAW_BOX_ROWS * 256;
+
 struct Smem {
   uint8_t* base;
   uint32_t addr;  // shared-window address of base
@@ -96,10 +102,63 @@ __device__ __forceinline__ void silu4(float (&x)[4]) {
   x[3] *= r23 * d[2];
 }
 
+// Conv + SiLU of the 4 tokens tq .. tq+3 of a chunk starting at position t0
+// of its sequence, over this lane's 4 channels, from a staged raw block (row r
+// = position t0 - 3 + r).  Positions before the sequence read the carried conv
+// state instead (cs: its 3 fp32 rows at this lane's channels, row stride
+// cs_stride floats); padding tokens (tq + i >= L) come out zero.  w[j][e] is
+// tap j of channel e (tap 3 multiplies the current token).
+__device__ __forceinline__ void conv_quad_staged(const uint8_t* raw_blk, const float* cs, size_t cs_stride, int t0,
+                                                 int L, int tq, int lane, const float (&w)[kConvW][4],
+                                                 float (&y)[4][4]) {
+  constexpr int kRows = 4 + kConvW - 1;
+  float x[kRows][4];
+#pragma unroll
+  for (int r = 0; r < kRows; ++r) {
+    const int tau = t0 + tq - (kConvW - 1) + r;   // position in the sequence
+    if (tau >= 0) {
+      const uint2 v2 = *reinterpret_cast<const uint2*>(raw_blk + (tq + r) * 256 + lane * 8);
+      x[r][0] = bf16_to_f32(v2.x & 0xffffu); x[r][1] = bf16_to_f32(v2.x >> 16);
+      x[r][2] = bf16_to_f32(v2.y & 0xffffu); x[r][3] = bf16_to_f32(v2.y >> 16);
+    } else {
+      const float4 v4 = *reinterpret_cast<const float4*>(cs + (size_t)(kConvW - 1 + tau) * cs_stride);
+      x[r][0] = v4.x; x[r][1] = v4.y; x[r][2] = v4.z; x[r][3] = v4.w;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float acc = w[0][e] * x[i][e];
+#pragma unroll
+      for (int j = 1; j < kConvW; ++j) acc = fmaf(w[j][e], x[i + j][e], acc);
+      y[i][e] = tq + i < L ? acc : 0.0f;   // padding tokens of a partial chunk are zero
+    }
+    silu4(y[i]);
+  }
+}
+
+// Sums over the warp of four per-token partial sums (one per lane and token):
+// the first two butterfly steps hand half of the sums to the partner lane, so
+// a lane ends with the full sum of token 2 (lane bit 4) + (lane bit 3), added
+// in the same tree as warp_sum.  token_lane(i) is a lane holding token i's sum.
+__device__ __forceinline__ float warp_sum4(const float (&s)[4], int lane) {
+  const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
+  float k0 = hi16 ? s[2] : s[0], k1 = hi16 ? s[3] : s[1];
+  const float s0 = hi16 ? s[0] : s[2], s1 = hi16 ? s[1] : s[3];
+  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+  float tot = hi8 ? k1 : k0;
+  tot += __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
+  tot += __shfl_xor_sync(0xffffffffu, tot, 4);
+  tot += __shfl_xor_sync(0xffffffffu, tot, 2);
+  tot += __shfl_xor_sync(0xffffffffu, tot, 1);
+  return tot;
+}
+__device__ __forceinline__ int token_lane(int i) { return ((i >> 1) << 4) | ((i & 1) << 3); }
+
 // Sums of squares of four tokens' 128 channels (each lane holding 4 channels
-// of each token) -> 1/sqrt(sum + eps) * scale for token i, on every lane.  The
-// first two butterfly steps hand half of the sums to the partner lane, so a
-// lane ends with the full sum of token 2 (lane bit 4) + (lane bit 3).
+// of each token) -> 1/sqrt(sum + eps) * scale for token i, on every lane.
 __device__ __forceinline__ void l2_rnorm4(const float (&y)[4][4], float eps, float scale, int lane,
                                           float (&rn)[4]) {
   float ss[4];
@@ -109,19 +168,9 @@ __device__ __forceinline__ void l2_rnorm4(const float (&y)[4][4], float eps, flo
 #pragma unroll
     for (int e = 1; e < 4; ++e) ss[i] = fmaf(y[i][e], y[i][e], ss[i]);
   }
-  const bool hi16 = (lane & 16) != 0, hi8 = (lane & 8) != 0;
-  float k0 = hi16 ? ss[2] : ss[0], k1 = hi16 ? ss[3] : ss[1];
-  const float s0 = hi16 ? ss[0] : ss[2], s1 = hi16 ? ss[1] : ss[3];
-  k0 += __shfl_xor_sync(0xffffffffu, s0, 16);
-  k1 += __shfl_xor_sync(0xffffffffu, s1, 16);
-  float tot = hi8 ? k1 : k0;
-  tot += __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
-  tot += __shfl_xor_sync(0xffffffffu, tot, 4);
-  tot += __shfl_xor_sync(0xffffffffu, tot, 2);
-  tot += __shfl_xor_sync(0xffffffffu, tot, 1);
-  const float r = rsqrtf(tot + eps) * scale;
+  const float r = rsqrtf(warp_sum4(ss, lane) + eps) * scale;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) rn[i] = __shfl_sync(0xffffffffu, r, ((i >> 1) << 4) | ((i & 1) << 3));
+  for (int i = 0; i < 4; ++i) rn[i] = __shfl_sync(0xffffffffu, r, token_lane(i));
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
@@ -188,11 +237,38 @@ __device__ __forceinline__ Seg load_seg(const int* list, int u) {
   return Seg{e[0], e[1], e[2], e[3], e[4], e[5], e[6]};
 }
 
-// Transfer matrices of boundary slot k, value head h: X (the map), S (end state
-// from zero, overwritten by the combine pass with the true start state of the
-// next segment), and the sequence's initial state (first slot only).
+// Transfer matrices of boundary slot k, value head h, 64 KB each: the map X
+// (as two bf16 tiles, X_hi = bf16(X) and X_lo = bf16(X - X_hi), rows = first
+// index, 64-column blocks 16 KB apart), S (fp32 end state from zero,
+// overwritten by the combine pass with the true start state of the next
+// segment), and the sequence's initial state (fp32, first slot only); the
+// fp32 states in tiled order (tiled_off).
 __device__ __forceinline__ float* xfer_ptr(const PrefillArgs& p, int k, int h, int part) {
   return p.xfer + (((size_t)k * p.h_v + h) * 3 + part) * (size_t)(kD * kD);
+}
+
+// fp32 128 x 128 states kept in the workspace (the transfer pass's end
+// states, the combine pass's start states, a saved initial state) are stored
+// in TMEM-native order: the 4-column group q of row r at float offset
+// (q * 128 + r) * 4, so a warp holding 32 consecutive rows (one TMEM lane
+// each) moves 512 contiguous bytes per 16-byte access.  The caller's
+// ssm_state is row-major.
+__device__ __forceinline__ size_t tiled_off(int r, int q) { return ((size_t)q * kD + r) * 4; }
+
+// This thread's row r, columns col0 .. col0+31 of a state, tiled or row-major.
+__device__ __forceinline__ void load_state_row(const float* base, bool tiled, int r, int col0, float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 x = *reinterpret_cast<const float4*>(
+        base + (tiled ? tiled_off(r, (col0 >> 2) + q) : (size_t)r * kD + col0 + 4 * q));
+    v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+  }
+}
+__device__ __forceinline__ void store_state_row(float* base, bool tiled, int r, int col0, const float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    *reinterpret_cast<float4*>(base + (tiled ? tiled_off(r, (col0 >> 2) + q) : (size_t)r * kD + col0 + 4 * q)) =
+        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
 // T = (I + A)^{-1} for a strictly lower 64 x 64 matrix A (fp32, row stride
@@ -259,7 +335,9 @@ __device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, int
 }
 
 // Launchers of the split prefill (prep pass, then the scan passes).
-cudaError_t launch_prefill_prep(const PrefillArgs& p, unsigned max_chunks, cudaStream_t stream);
+cudaError_t launch_prefill_prep(const PrefillArgs& p, unsigned max_chunks, const CUtensorMap& tm_qkv,
+                                cudaStream_t stream);
+cudaError_t launch_prefill_combine(const PrefillArgs& p, unsigned max_multi, cudaStream_t stream);
 cudaError_t launch_prefill_scan(const PrefillArgs& p, bool transfer, unsigned units, const CUtensorMap& tm_z,
                                 cudaStream_t stream);
 

@@ -38,83 +38,47 @@ namespace {
 // ============================== prep pass ==============================
 
 constexpr int kPrepThreads = 256;
+constexpr int kMaxG = 4;   // value heads per key head on the compiled path
 // Shared memory (bytes from a 1024-aligned base).  Sized for two CTAs per SM.
 struct PrepLay {
   static constexpr uint32_t KQ = 0;             // bf16 [K^ | Q^], 64-column blocks 16 KB apart
   static constexpr uint32_t KQ16 = 32768;       // fp16 copy of KQ (Gram operands) ...
   static constexpr uint32_t AF = KQ16;          // ... then A and T fp32 [64][LDA] ...
   static constexpr uint32_t TF = AF + 64 * LDA * 4;
-  static constexpr uint32_t WN = KQ16;          // ... then -W [t][d_k]
-  static constexpr uint32_t VH = 66560;         // V^ [t][d_v]
-  static constexpr uint32_t TB = VH + 16384;    // T diag(beta)
-  static constexpr uint32_t TW = TB + 8192;     // T diag(beta e^gamma)
-  static constexpr uint32_t P = TW + 8192;      // P
-  static constexpr uint32_t GATE = P + 8192;    // fp32 gamma, beta, e^gamma, e^{gamma_C - gamma} [64]
-  static constexpr uint32_t BYTES = GATE + 4 * 64 * 4 + 1024;   // + slack to align the base
+  static constexpr uint32_t TW = AF;            // ... then T diag(beta e^gamma) over A ...
+  static constexpr uint32_t WN = AF;            // ... then -W [t][d_k]
+  static constexpr uint32_t RAW = 66560;        // two staged raw blocks: q | k, then v of two heads ...
+  static constexpr uint32_t P = RAW;            // ... then a head's P tile
+  static constexpr uint32_t GATE = RAW + 2 * RAW_BLK;   // per head: fp32 gamma, beta, e^gamma [64]
+  static constexpr uint32_t BYTES = GATE + kMaxG * 3 * 64 * 4 + 1024;   // + slack to align the base
 };
-static_assert(PrepLay::TF + 64 * LDA * 4 <= PrepLay::VH, "A and T overlap V^");
-static_assert(PrepLay::VH % 1024 == 0 && PrepLay::TB % 1024 == 0 && PrepLay::TW % 1024 == 0 &&
-                  PrepLay::P % 1024 == 0,
-              "operand tiles need 1024-byte alignment");
+static_assert(PrepLay::TF + 64 * LDA * 4 <= PrepLay::RAW, "A and T overlap the raw staging");
+static_assert(PrepLay::RAW % 1024 == 0 && RAW_BLK % 128 == 0, "TMA destinations need 128-byte alignment");
 static_assert(2 * (PrepLay::BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
 constexpr uint32_t TP_G = 0, TP_W = 64, TP_COLS = 128;   // TMEM: Gram [K^;Q^]K^T, W^T
 
-// Conv + SiLU of the 4 tokens tq .. tq+3 of a chunk over this lane's 4
-// channels ch .. ch+3, reading raw inputs from global memory: the carried conv
-// state before the sequence's first token, zeros past its end; padding tokens
-// of a partial chunk come out zero.
-__device__ __forceinline__ void conv_quad(const PrefillArgs& p, int n, int start, int len, int t0, int L, int tq,
-                                          int ch, int Cc, float (&y)[4][4]) {
-  float w[kConvW][4];
-  {
-    const uint4 u0 = *reinterpret_cast<const uint4*>(p.conv_w + (size_t)ch * kConvW);        // channels ch, ch+1
-    const uint4 u1 = *reinterpret_cast<const uint4*>(p.conv_w + (size_t)(ch + 2) * kConvW);  // ch+2, ch+3
-    const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+// This lane's 4 channels ch .. ch+3 of the conv weight, w[tap][channel].
+__device__ __forceinline__ void conv_weights(const uint16_t* conv_w, int ch, float (&w)[kConvW][4]) {
+  const uint4 u0 = *reinterpret_cast<const uint4*>(conv_w + (size_t)ch * kConvW);        // channels ch, ch+1
+  const uint4 u1 = *reinterpret_cast<const uint4*>(conv_w + (size_t)(ch + 2) * kConvW);  // ch+2, ch+3
+  const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
+  for (int e = 0; e < 4; ++e)
 #pragma unroll
-      for (int j = 0; j < kConvW; ++j) {
-        const int k = e * kConvW + j;   // channel e, tap j
-        w[j][e] = bf16_to_f32((k & 1) ? (wv[k >> 1] >> 16) : (wv[k >> 1] & 0xffffu));
-      }
-  }
-  constexpr int kRows = 4 + kConvW - 1;
-  float x[kRows][4];
-#pragma unroll
-  for (int r = 0; r < kRows; ++r) {
-    const int tau = t0 + tq - (kConvW - 1) + r;   // position in the sequence
-    if (tau < 0) {
-      const float4 v4 = *reinterpret_cast<const float4*>(
-          p.conv_state + ((size_t)n * (kConvW - 1) + (kConvW - 1 + tau)) * Cc + ch);
-      x[r][0] = v4.x; x[r][1] = v4.y; x[r][2] = v4.z; x[r][3] = v4.w;
-    } else if (tau < len) {
-      const uint2 v2 = *reinterpret_cast<const uint2*>(p.qkv + (size_t)(start + tau) * Cc + ch);
-      x[r][0] = bf16_to_f32(v2.x & 0xffffu); x[r][1] = bf16_to_f32(v2.x >> 16);
-      x[r][2] = bf16_to_f32(v2.y & 0xffffu); x[r][3] = bf16_to_f32(v2.y >> 16);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[r][e] = 0.0f;
+    for (int j = 0; j < kConvW; ++j) {
+      const int k = e * kConvW + j;   // channel e, tap j
+      w[j][e] = bf16_to_f32((k & 1) ? (wv[k >> 1] >> 16) : (wv[k >> 1] & 0xffffu));
     }
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float acc = w[0][e] * x[i][e];
-#pragma unroll
-      for (int j = 1; j < kConvW; ++j) acc = fmaf(w[j][e], x[i + j][e], acc);
-      y[i][e] = tq + i < L ? acc : 0.0f;
-    }
-    silu4(y[i]);
-  }
 }
 
 // One CTA per (chunk, key head): the state-free part of the chunk for the G
 // value heads that read this key head, stored as records.
-__global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs p) {
+__global__ void __launch_bounds__(kPrepThreads, 2)
+    prep_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv) {
   using L_ = PrepLay;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t mbar;   // MMA completion
+  __shared__ __align__(8) uint64_t mbar;       // MMA completion
+  __shared__ __align__(8) uint64_t mbar_raw;   // staged raw rows landed
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -127,17 +91,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
   const int L = min(C, len - t0);
   const int G = p.h_v / p.h_k;
   const int Cq = p.h_k * kD, Cc = 2 * Cq + p.h_v * kD;
+  const float* cs_seq = p.conv_state + (size_t)n * (kConvW - 1) * Cc;   // this sequence's carried conv state
 
   const Smem sm = smem_aligned(smem_raw);
   float* Af = sm.f32(L_::AF);
   float* Tf = sm.f32(L_::TF);
-  float* gam = sm.f32(L_::GATE);
-  float* bet = gam + 64;
-  float* eg = gam + 128;
-  float* egc = gam + 192;
 
   if (tid == 0) {
     tc::mbar_init(&mbar, 1);
+    tc::mbar_init(&mbar_raw, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base_s, TP_COLS);
@@ -148,7 +110,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
   const int quarter = warp & 3, half = warp >> 2;   // TMEM lane quarter, 32-column half
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
   const int row = 32 * quarter + lane;
-  uint32_t phase = 0;
+  const int y_raw = start + t0 - (kConvW - 1);      // first staged row (a chunk and its halo)
+  if (tid == 32) {   // raw q and k rows
+    mbar_expect_tx(&mbar_raw, 2 * RAW_BLK);
+    tma_load_2d(sm.base + L_::RAW, &tm_qkv, kh * kD, y_raw, &mbar_raw);
+    tma_load_2d(sm.base + L_::RAW + RAW_BLK, &tm_qkv, Cq + kh * kD, y_raw, &mbar_raw);
+  }
+  uint32_t phase = 0, raw_phase = 0;
+  bool raw_pending = true;
   auto wait_mma = [&]() -> bool {
     const bool ok = tc::mbar_wait(&mbar, phase, kWaitBudget);
     phase ^= 1u;
@@ -156,15 +125,70 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
     tc::fence_after_sync();
     return all_ok;
   };
+  auto wait_raw = [&]() -> bool {   // on a time-out the copy stays pending for the exit path
+    const bool ok_all = __syncthreads_and(tc::mbar_wait(&mbar_raw, raw_phase, kWaitBudget));
+    if (ok_all) {
+      raw_phase ^= 1u;
+      raw_pending = false;
+    }
+    return ok_all;
+  };
+  bool ok = true;
+
+  // ---- gates and their cumulative sums, warp g for value head kh*G + g (meanwhile
+  //      the raw rows land); the scan passes get e^gamma and e^{gamma_C - gamma} ----
+  if (warp < G) {
+    const int h = kh * G + warp;
+    const float A_exp = __expf(p.A_log[h]);
+    const float dtb = p.dt_bias[h];
+    float g2[2], b2[2];
+#pragma unroll
+    for (int uu = 0; uu < 2; ++uu) {
+      const int t = lane + 32 * uu;
+      if (t < L) {
+        const size_t pidx = (size_t)(start + t0 + t) * p.h_v + h;
+        g2[uu] = -A_exp * softplus(bf16_to_f32(p.a[pidx]) + dtb);
+        b2[uu] = sigmoid(bf16_to_f32(p.b[pidx]));
+      } else {
+        g2[uu] = 0.0f;
+        b2[uu] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int uu = 0; uu < 2; ++uu) {
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, g2[uu], off);
+        if (lane >= off) g2[uu] += y;
+      }
+    }
+    g2[1] += __shfl_sync(0xffffffffu, g2[0], 31);
+    const float gC = __shfl_sync(0xffffffffu, g2[1], 31);
+    float* gam = sm.f32(L_::GATE + warp * 3 * 64 * 4);
+    float* rg = reinterpret_cast<float*>(p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecGate);
+#pragma unroll
+    for (int uu = 0; uu < 2; ++uu) {
+      const int t = lane + 32 * uu;
+      const float e1 = __expf(g2[uu]);
+      gam[t] = g2[uu];
+      gam[64 + t] = b2[uu];
+      gam[128 + t] = e1;
+      rg[t] = e1;
+      rg[64 + t] = __expf(gC - g2[uu]);
+    }
+  }
 
   // ---- conv + SiLU + L2 norms of q and k -> [K^ | Q^] in bf16 and fp16 ----
-  {
+  if (!wait_raw()) ok = false;
+  if (ok) {
     const float qscale = rsqrtf((float)kD);
 #pragma unroll 1
     for (int task = warp; task < 2 * (C / 4); task += kPrepThreads / 32) {
       const int blk = task / (C / 4), tq = 4 * (task % (C / 4));   // blk 0: q, 1: k
-      float y[4][4];
-      conv_quad(p, n, start, len, t0, L, tq, (blk == 0 ? 0 : Cq) + kh * kD + 4 * lane, Cc, y);
+      const int ch = (blk == 0 ? 0 : Cq) + kh * kD + 4 * lane;
+      float w[kConvW][4], y[4][4];
+      conv_weights(p.conv_w, ch, w);
+      conv_quad_staged(sm.base + L_::RAW + blk * RAW_BLK, cs_seq + ch, Cc, t0, L, tq, lane, w, y);
       float rn[4];
       l2_rnorm4(y, p.l2_eps, blk == 0 ? qscale : 1.0f, lane, rn);
 #pragma unroll
@@ -177,8 +201,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
       }
     }
   }
-  sync_for_mma();
-  if (tid == 0) {
+  sync_for_mma();   // also: the raw q | k rows are read
+  if (ok && tid == 0) {
     // Gram [K^; Q^] K^T in fp16 (rows 0-63: K^K^T, 64-127: Q^K^T)
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -190,74 +214,48 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
     bulk_commit();
   }
 
-  bool ok = true;
+  // ---- conv + SiLU of v, two value heads at a time, straight into their records ----
 #pragma unroll 1
-  for (int g = 0; g < G; ++g) {
+  for (int g0 = 0; g0 < G && ok; g0 += 2) {
+    const int nv = min(2, G - g0);
+    if (tid == 32) {
+      mbar_expect_tx(&mbar_raw, nv * RAW_BLK);
+      for (int i = 0; i < nv; ++i)
+        tma_load_2d(sm.base + L_::RAW + i * RAW_BLK, &tm_qkv, 2 * Cq + (kh * G + g0 + i) * kD, y_raw, &mbar_raw);
+    }
+    raw_pending = true;
+    if (!wait_raw()) { ok = false; break; }
+#pragma unroll 1
+    for (int task = warp; task < nv * (C / 4); task += kPrepThreads / 32) {
+      const int i = task / (C / 4), tq = 4 * (task % (C / 4));
+      const int h = kh * G + g0 + i;
+      const int ch = 2 * Cq + h * kD + 4 * lane;
+      float w[kConvW][4], y[4][4];
+      conv_weights(p.conv_w, ch, w);
+      conv_quad_staged(sm.base + L_::RAW + i * RAW_BLK, cs_seq + ch, Cc, t0, L, tq, lane, w, y);
+      uint8_t* vh = p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecVH;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
+    }
+    __syncthreads();   // the raw v rows are read
+  }
+  if (ok && !wait_mma()) ok = false;   // the Gram product (and KQ16 is free)
+
+#pragma unroll 1
+  for (int g = 0; g < G && ok; ++g) {
     const int h = kh * G + g;
     uint8_t* rv = p.rec_v + ((size_t)c * p.h_v + h) * kRecV;
-    if (g > 0) {   // the previous head's tiles must have left shared memory
+    const float* gam = sm.f32(L_::GATE + g * 3 * 64 * 4);
+    const float* bet = gam + 64;
+    const float* eg = gam + 128;
+    if (g > 0) {   // the previous head's -W and P tiles have left shared memory
       if (tid == 0) bulk_wait_read();
       __syncthreads();
     }
-    // ---- gates and their cumulative sums (warp 0) ----
-    if (warp == 0) {
-      const float A_exp = __expf(p.A_log[h]);
-      const float dtb = p.dt_bias[h];
-      float g2[2], b2[2];
-#pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-        const int t = lane + 32 * uu;
-        if (t < L) {
-          const size_t pidx = (size_t)(start + t0 + t) * p.h_v + h;
-          g2[uu] = -A_exp * softplus(bf16_to_f32(p.a[pidx]) + dtb);
-          b2[uu] = sigmoid(bf16_to_f32(p.b[pidx]));
-        } else {
-          g2[uu] = 0.0f;
-          b2[uu] = 0.0f;
-        }
-      }
-#pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, g2[uu], off);
-          if (lane >= off) g2[uu] += y;
-        }
-      }
-      g2[1] += __shfl_sync(0xffffffffu, g2[0], 31);
-      const float gC = __shfl_sync(0xffffffffu, g2[1], 31);
-      float* rg = reinterpret_cast<float*>(rv + kRecGate);
-#pragma unroll
-      for (int uu = 0; uu < 2; ++uu) {
-        const int t = lane + 32 * uu;
-        const float e1 = __expf(g2[uu]), e2 = __expf(gC - g2[uu]);
-        gam[t] = g2[uu];
-        bet[t] = b2[uu];
-        eg[t] = e1;
-        egc[t] = e2;
-        rg[t] = e1;
-        rg[64 + t] = e2;
-      }
-    }
-    // ---- conv + SiLU of this head's v -> V^ ----
-#pragma unroll 1
-    for (int task = warp; task < C / 4; task += kPrepThreads / 32) {
-      const int tq = 4 * task;
-      float y[4][4];
-      conv_quad(p, n, start, len, t0, L, tq, 2 * Cq + h * kD + 4 * lane, Cc, y);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        store_bf16x4(sm.base + L_::VH, tc::sw128_off(tq + i, 4 * lane, 8192), y[i][0], y[i][1], y[i][2], y[i][3]);
-    }
-    sync_for_mma();
-    if (tid == 0) {
-      bulk_store(rv + kRecVH, sm.base + L_::VH, 16384);
-      bulk_commit();
-    }
-    if (g == 0 && !wait_mma()) { ok = false; break; }   // the Gram product (and KQ16 is free)
-
-    // ---- A (fp32) and P (bf16 tile) from the Gram rows: lane quarters 0-1 hold
-    //      K^K^T rows, 2-3 Q^K^T rows; the two warps of a quarter split its columns ----
+    // ---- A (fp32) and P (bf16, staged over the raw rows) from the Gram rows: lane
+    //      quarters 0-1 hold K^K^T rows, 2-3 Q^K^T rows; the two warps of a quarter
+    //      split its columns ----
     {
       float v[32];
       const int t = row & 63, c0 = 32 * half;
@@ -286,24 +284,29 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
       bulk_commit();
     }
 
-    // ---- T = (I + A)^{-1}, then T diag(beta) and T diag(beta e^gamma) as bf16 tiles ----
+    // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) -> smem over A ----
     solve_unit_lower<kPrepThreads>(Af, Tf, tid, lane);
-    for (int e = tid; e < 64 * 8; e += kPrepThreads) {
-      const int t = e >> 3, c8 = (e & 7) * 8;
-      float xb[8], xw[8];
+    {
+      float xb[2][8], xw[2][8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float tv = Tf[t * LDA + c8 + q];
-        xb[q] = tv * bet[c8 + q];
-        xw[q] = xb[q] * eg[c8 + q];
+      for (int q2 = 0; q2 < 2; ++q2) {   // read all of T before TW overwrites A (T is separate)
+        const int e = tid + q2 * kPrepThreads, t = e >> 3, c8 = (e & 7) * 8;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float tv = Tf[t * LDA + c8 + q];
+          xb[q2][q] = tv * bet[c8 + q];
+          xw[q2][q] = xb[q2][q] * eg[c8 + q];
+        }
       }
-      store_bf16x8(sm.base + L_::TB, tc::sw128_off(t, c8, 0), xb);
-      store_bf16x8(sm.base + L_::TW, tc::sw128_off(t, c8, 0), xw);
+#pragma unroll
+      for (int q2 = 0; q2 < 2; ++q2) {
+        const int e = tid + q2 * kPrepThreads, t = e >> 3, c8 = (e & 7) * 8;
+        store_bf16x8(rv + kRecTB, tc::sw128_off(t, c8, 0), xb[q2]);
+        store_bf16x8(sm.base + L_::TW, tc::sw128_off(t, c8, 0), xw[q2]);
+      }
     }
     sync_for_mma();
     if (tid == 0) {
-      bulk_store(rv + kRecTB, sm.base + L_::TB, 8192);
-      bulk_commit();
       // W^T = K^T (T diag(beta e^gamma))^T
 #pragma unroll
       for (int k = 0; k < 4; ++k)
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
     }
     if (!wait_mma()) { ok = false; break; }
 
-    // ---- -W tile [t][d_k] (over A and T, which are dead) ----
+    // ---- -W tile [t][d_k] (over T diag(beta e^gamma), which the MMA has consumed) ----
     {
       float v[32];
       tc::tmem_ld32(tmem + lane_base + TP_W + 32 * half, v);
@@ -333,6 +336,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
     if (!ok) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
     bulk_wait_all();   // the records are written before this CTA's shared memory goes away
   }
+  // a raw copy still in flight after a time-out must land before the shared memory goes away
+  if (raw_pending) tc::mbar_wait(&mbar_raw, raw_phase, kWaitBudget);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TP_COLS);
@@ -341,6 +346,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) prep_kernel(const PrefillArgs
 // ============================== scan passes ==============================
 
 constexpr int kScanThreads = 512;   // 16 warps: 4 per TMEM lane quarter
+static_assert(kScanThreads / 32 * 4 == C, "the epilogue gives each warp 4 of a chunk's tokens");
 template <bool kXfer> struct ScanLay;
 template <> struct ScanLay<false> {    // output pass
   static constexpr uint32_t S = 0;          // S bf16 [d_v][d_k], K blocks 16 KB apart
@@ -405,7 +411,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mb_mma;     // MMA completion
   __shared__ __align__(8) uint64_t mb_kq[2];   // [K^ | Q^] buffers
-  __shared__ __align__(8) uint64_t mb_a;       // -W | V^ | T diag(beta) and the gates
+  __shared__ __align__(8) uint64_t mb_a;       // -W | V^ | T diag(beta)
+  __shared__ __align__(8) uint64_t mb_g;       // the gates (a chunk ahead)
   __shared__ __align__(8) uint64_t mb_p;       // P (output pass)
   __shared__ __align__(8) uint64_t mb_z;       // z (output pass)
   __shared__ uint32_t tmem_base_s;
@@ -422,9 +429,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int nch = (sg.len + C - 1) / C;
 
   // where the state comes from and goes to
+  // (the caller's state is row-major, the workspace slots tiled)
   const float* S_init = nullptr;
   float* S_final = nullptr;
   float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
+  const bool init_tiled = !kXfer && sg.nsig > 1;
   if (!kXfer) {
     if (sg.nsig == 1) {
       S_init = ssm;
@@ -443,6 +452,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     tc::mbar_init(&mb_kq[0], 1);
     tc::mbar_init(&mb_kq[1], 1);
     tc::mbar_init(&mb_a, 1);
+    tc::mbar_init(&mb_g, 1);
     tc::mbar_init(&mb_p, 1);
     tc::mbar_init(&mb_z, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -470,11 +480,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       bulk_copy(dst + 8192, rec_kq(j) + 16384, 8192, &mb_kq[j & 1]);
     }
   };
-  auto load_a = [&](int j) {
-    mbar_expect_tx(&mb_a, kRecP + kRecGateBytes);
-    bulk_copy(sm.base + M::WN, rec_v(j), kRecP, &mb_a);
-    bulk_copy(sm.base + M::GT + (j & 1) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_a);
-  };
+  auto load_a = [&](int j) { bulk_load(sm.base + M::WN, rec_v(j), kRecP, &mb_a); };
+  auto load_g = [&](int j) { bulk_load(sm.base + M::GT + (j & 1) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g); };
   auto load_p = [&](int j) { bulk_load(sm.base + M::P, rec_v(j) + kRecP, 8192, &mb_p); };
   auto load_z = [&](int j) {
     mbar_expect_tx(&mb_z, C * kD * 2);
@@ -482,9 +489,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   };
   // copies in flight per barrier, and waits completed (the k-th copy on a barrier
   // completes its phase of parity k & 1); only the abort path needs these
-  bool pend_kq[2] = {true, nch > 1}, pend_a = true, pend_p = !kXfer, pend_z = !kXfer;
-  uint32_t w_kq[2] = {0, 0}, w_a = 0, w_p = 0, w_z = 0;
+  bool pend_kq[2] = {true, nch > 1}, pend_a = true, pend_g = true, pend_p = !kXfer, pend_z = !kXfer;
+  uint32_t w_kq[2] = {0, 0}, w_a = 0, w_g = 0, w_p = 0, w_z = 0;
   if (tid == 32) {
+    load_g(0);
     load_kq(0);
     if (nch > 1) load_kq(1);
     load_a(0);
@@ -494,30 +502,37 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     }
   }
 
-  // initial state(s): fp32 into TMEM, bf16 into the operand tile(s)
+  // initial state(s): bf16 into the operand tile(s), and into TMEM in fp32
+  // already scaled by the first chunk's total decay (the state update adds to
+  // e^{gamma_C} S0; each chunk's end scales for the next one)
+  bool aborted = !__syncthreads_and(tc::mbar_wait(&mb_g, 0u, kWaitBudget));
+  if (!aborted) {
+    pend_g = false;
+    ++w_g;
+  }
   {
+    const float dC0 = sm.f32(M::GT)[C - 1];
     const int col0 = part * 32;
     float v[32];
     if (!kXfer) {
-      const float4* src = reinterpret_cast<const float4*>(S_init + (size_t)row * kD + col0);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 x = src[q];
-        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-      }
+      load_state_row(S_init, init_tiled, row, col0, v);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = 0.0f;
     }
-    tc::tmem_st32(tmem + lane_base + TS_S + col0, v);
 #pragma unroll
     for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::S, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= dC0;
+    tc::tmem_st32(tmem + lane_base + TS_S + col0, v);
     if (kXfer) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = (col0 + i == row) ? 1.0f : 0.0f;
-      tc::tmem_st32(tmem + lane_base + TS_X + col0, v);
 #pragma unroll
       for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::X, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= dC0;
+      tc::tmem_st32(tmem + lane_base + TS_X + col0, v);
     }
   }
   sync_for_mma();
@@ -531,29 +546,39 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     return all_ok;
   };
   // output pass: the gated RMSNorm epilogue of chunk jj from the O staging, a
-  // warp per token and 4 channels per lane; then z of chunk jj + 1 may load
+  // warp per 4 tokens and 4 channels per lane; then z of chunk jj + 1 may load
   auto epilogue = [&](int jj) -> bool {
     const int t0e = sg.begin + C * jj, Le = min(C, seg_end - t0e);
     if (!__syncthreads_and(tc::mbar_wait(&mb_z, w_z & 1u, kWaitBudget))) return false;
     pend_z = false;
     ++w_z;
-    for (int t = warp; t < Le; t += kScanThreads / 32) {
-      const float4 o4 = reinterpret_cast<const float4*>(Ost + t * LDO)[lane];
-      float ss = o4.x * o4.x;
-      ss = fmaf(o4.y, o4.y, ss);
-      ss = fmaf(o4.z, o4.z, ss);
-      ss = fmaf(o4.w, o4.w, ss);
-      ss = warp_sum(ss);
-      const float rstd = rsqrtf(ss * (1.0f / kD) + p.rms_eps);
-      const uint2 zr = *reinterpret_cast<const uint2*>(sm.base + M::Z + t * 256 + lane * 8);
+    {
+      const int tq = 4 * warp;
+      float o[4][4], ss[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 o4 = reinterpret_cast<const float4*>(Ost + (tq + i) * LDO)[lane];
+        o[i][0] = o4.x; o[i][1] = o4.y; o[i][2] = o4.z; o[i][3] = o4.w;
+        ss[i] = o4.x * o4.x;
+        ss[i] = fmaf(o4.y, o4.y, ss[i]);
+        ss[i] = fmaf(o4.z, o4.z, ss[i]);
+        ss[i] = fmaf(o4.w, o4.w, ss[i]);
+      }
+      const float r = rsqrtf(warp_sum4(ss, lane) * (1.0f / kD) + p.rms_eps);
       const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
-      float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
-                    bf16_to_f32(zr.y >> 16)};
-      silu4(g);
-      uint2 o;
-      o.x = pack_bf16x2(o4.x * rstd * w4.x * g[0], o4.y * rstd * w4.y * g[1]);
-      o.y = pack_bf16x2(o4.z * rstd * w4.z * g[2], o4.w * rstd * w4.w * g[3]);
-      *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0e + t) * p.h_v + h) * kD + 4 * lane) = o;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float rstd = __shfl_sync(0xffffffffu, r, token_lane(i));
+        const uint2 zr = *reinterpret_cast<const uint2*>(sm.base + M::Z + (tq + i) * 256 + lane * 8);
+        float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
+                      bf16_to_f32(zr.y >> 16)};
+        silu4(g);
+        uint2 ov;
+        ov.x = pack_bf16x2(o[i][0] * rstd * w4.x * g[0], o[i][1] * rstd * w4.y * g[1]);
+        ov.y = pack_bf16x2(o[i][2] * rstd * w4.z * g[2], o[i][3] * rstd * w4.w * g[3]);
+        if (tq + i < Le)
+          *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0e + tq + i) * p.h_v + h) * kD + 4 * lane) = ov;
+      }
     }
     __syncthreads();   // the O staging and the z buffer are read
     if (jj + 1 < nch) {
@@ -563,8 +588,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     return true;
   };
 
-  bool aborted = false;
-  for (int j = 0; j < nch; ++j) {
+  for (int j = 0; j < nch && !aborted; ++j) {
     const float* eg = sm.f32(M::GT + (j & 1) * 512);
     const float* egc = eg + 64;
     const uint32_t kq = sm.addr + M::KQ + (j & 1) * M::KQ_BUF;
@@ -576,6 +600,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       pend_a = false;
       ++w_kq[j & 1];
       ++w_a;
+    }
+    // the gates of the next chunk go where those of the chunk before this one were
+    if (j + 1 < nch) {
+      if (tid == 32) load_g(j + 1);
+      pend_g = true;
     }
 
     // ---- batch 1: [O1 = S0 Q^T,] U = V^T (T diag beta)^T, Vn^T = U + S0 (-W)^T
@@ -609,23 +638,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       }
       tc::mma_commit(&mb_mma);
     }
-    // meanwhile: pre-scale the fp32 state(s) by the chunk's total decay ...
-    {
-      const float dC = eg[C - 1];
-#pragma unroll
-      for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
-        float v[32];
-        const uint32_t ta = tmem + lane_base + (zz ? TS_X : TS_S) + part * 32;
-        tc::tmem_ld32(ta, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= dC;
-        tc::tmem_st32(ta, v);
-      }
-    }
-    // ... and write out the previous chunk
+    // meanwhile: write out the previous chunk
     if (!kXfer && j > 0 && !epilogue(j - 1)) { aborted = true; break; }
     if (!wait_mma()) { aborted = true; break; }
-    // the next chunk's -W | V^ | T diag(beta) and gates go where batch 1 has finished
+    // the next chunk's -W | V^ | T diag(beta) go where batch 1 has finished
     if (j + 1 < nch) {
       if (tid == 32) load_a(j + 1);
       pend_a = true;
@@ -693,15 +709,29 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       pend_kq[j & 1] = true;
     }
 
-    // ---- new state(s) -> bf16 operand tiles; output pass: O = e^gamma O1 + O2 -> fp32 staging ----
+    // ---- new state(s) -> bf16 operand tiles, and in TMEM scaled by the next
+    //      chunk's total decay; output pass: O = e^gamma O1 + O2 -> fp32 staging ----
     {
+      float dC = 1.0f;
+      if (j + 1 < nch) {
+        if (!__syncthreads_and(tc::mbar_wait(&mb_g, w_g & 1u, kWaitBudget))) { aborted = true; break; }
+        pend_g = false;
+        ++w_g;
+        dC = sm.f32(M::GT + ((j + 1) & 1) * 512)[C - 1];
+      }
 #pragma unroll
       for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
         float v[32];
-        tc::tmem_ld32(tmem + lane_base + (zz ? TS_X : TS_S) + part * 32, v);
+        const uint32_t ta = tmem + lane_base + (zz ? TS_X : TS_S) + part * 32;
+        tc::tmem_ld32(ta, v);
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           store_bf16x8(sm.base + (zz ? M::X : M::S), tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
+        if (j + 1 < nch) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= dC;
+          tc::tmem_st32(ta, v);
+        }
       }
       if (!kXfer) {
         float o1[16], o2[16];
@@ -725,19 +755,30 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     if (pend_kq[0]) tc::mbar_wait(&mb_kq[0], w_kq[0] & 1u, kWaitBudget);
     if (pend_kq[1]) tc::mbar_wait(&mb_kq[1], w_kq[1] & 1u, kWaitBudget);
     if (pend_a) tc::mbar_wait(&mb_a, w_a & 1u, kWaitBudget);
+    if (pend_g) tc::mbar_wait(&mb_g, w_g & 1u, kWaitBudget);
     if (pend_p) tc::mbar_wait(&mb_p, w_p & 1u, kWaitBudget);
     if (pend_z) tc::mbar_wait(&mb_z, w_z & 1u, kWaitBudget);
   } else {
-    // final state(s) back to global memory
-#pragma unroll
-    for (int zz = 0; zz < 2; ++zz) {
-      float* dst_base = kXfer ? xfer_ptr(p, sg.k0 + sg.sigma, h, zz == 0 ? 1 : 0) : (zz == 0 ? S_final : nullptr);
-      if (dst_base == nullptr) continue;
-      float4* dst = reinterpret_cast<float4*>(dst_base + (size_t)row * kD + part * 32);
+    // final state back to global memory (fp32); the transfer pass adds the map X
+    // as bf16 hi / lo tiles for the combine pass's tensor-core products
+    float* dst_base = kXfer ? xfer_ptr(p, sg.k0 + sg.sigma, h, 1) : S_final;
+    if (dst_base != nullptr) {
       float v[32];
-      tc::tmem_ld32(tmem + lane_base + (zz ? TS_X : TS_S) + part * 32, v);
+      tc::tmem_ld32(tmem + lane_base + TS_S + part * 32, v);
+      store_state_row(dst_base, kXfer, row, part * 32, v);
+    }
+    if (kXfer) {
+      uint8_t* xt = reinterpret_cast<uint8_t*>(xfer_ptr(p, sg.k0 + sg.sigma, h, 0));
+      float v[32], lo[32];
+      tc::tmem_ld32(tmem + lane_base + TS_X + part * 32, v);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) dst[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int i = 0; i < 32; ++i) lo[i] = v[i] - bf16_to_f32(f32_to_bf16(v[i]));   // exact in fp32
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t off = tc::sw128_off(row, part * 32 + 8 * m, 16384);
+        store_bf16x8(xt, off, v + 8 * m);
+        store_bf16x8(xt + 32768, off, lo + 8 * m);
+      }
     }
   }
   tc::fence_before_sync();
@@ -745,13 +786,156 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   if (warp == 0) tc::tmem_dealloc(tmem, TS_COLS);
 }
 
+// ============================== combine pass ==============================
+
+// Chains the transfer maps of a multi-segment sequence into every segment's
+// true start state, one CTA per (sequence, value head):
+//   S_{sigma+1} = S_sigma X_sigma + S_sigma^0,
+// written over slot sigma's end state after saving the initial state (so the
+// output pass never reads a state that the last segment's CTA is writing).
+//
+// The products run on the tensor core with fp32 accumulation.  S is split
+// into three bf16 parts (s1 = bf16(S), s2 = bf16(S - s1), s3 = bf16(S - s1 -
+// s2), which sum to S exactly) and X into two (X_hi, X_lo); TMEM starts at
+// S^0 and accumulates s1 X_hi + s2 X_hi + s3 X_hi + s1 X_lo.  The terms left
+// out are below 2^-16 of |S||X| per step.  A map that is exactly the identity
+// (no writes, no decay) gives back S bit for bit.
+constexpr int kCombThreads = 512;
+struct CombLay {
+  static constexpr uint32_t XB = 0;               // two map buffers: [X_hi 32 KB | X_lo 32 KB]
+  static constexpr uint32_t XB_BYTES = 65536;
+  static constexpr uint32_t S1 = 2 * XB_BYTES;    // s1, s2, s3: bf16 [row][k], K blocks 16 KB apart
+  static constexpr uint32_t S2 = S1 + 32768;
+  static constexpr uint32_t S3 = S2 + 32768;
+  static constexpr uint32_t BYTES = S3 + 32768 + 1024;
+};
+static_assert(CombLay::BYTES <= 227 * 1024, "shared memory");
+constexpr uint32_t TC_COLS = 128;
+
+__global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillArgs p) {
+  using L_ = CombLay;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t mb_x[2];   // map buffers landed
+  __shared__ __align__(8) uint64_t mb_mma;
+  __shared__ uint32_t tmem_base_s;
+  const int u = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
+  if (u >= p.multi_list[0]) return;
+  const int* e = p.multi_list + 4 + 4 * u;
+  const int n = e[0], k0 = e[1], nsig = e[2];
+  const int steps = nsig - 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = 32 * (warp & 3) + lane, col0 = 32 * (warp >> 2);   // TMEM lane = state row, 32 columns
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+  const Smem sm = smem_aligned(smem_raw);
+  if (tid == 0) {
+    tc::mbar_init(&mb_x[0], 1);
+    tc::mbar_init(&mb_x[1], 1);
+    tc::mbar_init(&mb_mma, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tc::tmem_alloc(&tmem_base_s, TC_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = tmem_base_s;
+  // copies issued / waited per buffer (the same on every thread: tid 32 issues
+  // under conditions every thread evaluates alike)
+  int issued[2] = {1, steps > 1 ? 1 : 0}, waited[2] = {0, 0};
+  if (tid == 32) {
+    bulk_load(sm.base + L_::XB, xfer_ptr(p, k0, h, 0), L_::XB_BYTES, &mb_x[0]);
+    if (steps > 1) bulk_load(sm.base + L_::XB + L_::XB_BYTES, xfer_ptr(p, k0 + 1, h, 0), L_::XB_BYTES, &mb_x[1]);
+  }
+  // S0 = the initial state: saved, and split into the operand tiles
+  auto split_store = [&](const float (&v)[32]) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float a[8], b[8], c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a[i] = bf16_to_f32(f32_to_bf16(v[8 * m + i]));
+        const float r1 = v[8 * m + i] - a[i];
+        b[i] = bf16_to_f32(f32_to_bf16(r1));
+        c[i] = r1 - b[i];
+      }
+      const uint32_t off = tc::sw128_off(row, col0 + 8 * m, 16384);
+      store_bf16x8(sm.base + L_::S1, off, a);
+      store_bf16x8(sm.base + L_::S2, off, b);
+      store_bf16x8(sm.base + L_::S3, off, c);
+    }
+  };
+  {
+    float v[32];
+    load_state_row(p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD, false, row, col0, v);
+    store_state_row(xfer_ptr(p, k0, h, 2), true, row, col0, v);
+    split_store(v);
+  }
+  float b[32];
+  load_state_row(xfer_ptr(p, k0, h, 1), true, row, col0, b);   // S^0 of the first segment
+  uint32_t phase = 0;
+  bool ok = true;
+#pragma unroll 1
+  for (int sg = 0; sg < steps; ++sg) {
+    tc::tmem_st32(tmem + lane_base + col0, b);   // the accumulator starts at S^0 of segment sg
+    if (sg + 1 < steps) load_state_row(xfer_ptr(p, k0 + sg + 1, h, 1), true, row, col0, b);
+    ok = tc::mbar_wait(&mb_x[sg & 1], (uint32_t)((sg >> 1) & 1), kWaitBudget);
+    if (!sync_for_mma_and(ok)) { ok = false; break; }   // also: the S parts are in place
+    ++waited[sg & 1];
+    if (tid == 0) {
+      const uint32_t xb = sm.addr + L_::XB + (sg & 1) * L_::XB_BYTES;
+      const uint32_t a_of[4] = {L_::S1, L_::S2, L_::S3, L_::S1};
+      const uint32_t b_of[4] = {0u, 0u, 0u, 32768u};
+#pragma unroll
+      for (int pass = 0; pass < 4; ++pass)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem, tc::sdesc_at(D_K, sm.addr + a_of[pass] + kb * 16384 + ks),
+                       tc::sdesc_at(D_MN_KQ, xb + b_of[pass] + k * 2048), ID_MN_B, 1u);
+        }
+      tc::mma_commit(&mb_mma);
+    }
+    ok = tc::mbar_wait(&mb_mma, phase, kWaitBudget);
+    phase ^= 1u;
+    if (!__syncthreads_and(ok)) { ok = false; break; }
+    tc::fence_after_sync();
+    // the map buffer and the S parts are free again
+    if (sg + 2 < steps) {
+      if (tid == 32) bulk_load(sm.base + L_::XB + (sg & 1) * L_::XB_BYTES, xfer_ptr(p, k0 + sg + 2, h, 0),
+                               L_::XB_BYTES, &mb_x[sg & 1]);
+      ++issued[sg & 1];
+    }
+    float v[32];
+    tc::tmem_ld32(tmem + lane_base + col0, v);
+    store_state_row(xfer_ptr(p, k0 + sg, h, 1), true, row, col0, v);
+    split_store(v);
+  }
+  if (!ok) {
+    if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+    // the map copies this CTA started must land (bounded) before its smem goes away
+    for (int q = 0; q < 2; ++q)
+      for (; waited[q] < issued[q]; ++waited[q]) tc::mbar_wait(&mb_x[q], (uint32_t)(waited[q] & 1), kWaitBudget);
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 0) tc::tmem_dealloc(tmem, TC_COLS);
+}
+
 }  // namespace
 
-cudaError_t launch_prefill_prep(const PrefillArgs& p, unsigned max_chunks, cudaStream_t stream) {
+cudaError_t launch_prefill_prep(const PrefillArgs& p, unsigned max_chunks, const CUtensorMap& tm_qkv,
+                                cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)PrepLay::BYTES);
   if (e != cudaSuccess) return e;
-  prep_kernel<<<max_chunks * (unsigned)p.h_k, kPrepThreads, PrepLay::BYTES, stream>>>(p);
+  prep_kernel<<<max_chunks * (unsigned)p.h_k, kPrepThreads, PrepLay::BYTES, stream>>>(p, tm_qkv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_combine(const PrefillArgs& p, unsigned max_multi, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)CombLay::BYTES);
+  if (e != cudaSuccess) return e;
+  combine_kernel<<<max_multi * (unsigned)p.h_v, kCombThreads, CombLay::BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
