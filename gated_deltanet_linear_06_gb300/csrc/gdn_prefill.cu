@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // ---- T = (I + A)^{-1} ----
-    solve_unit_lower<kThreads>(Af, Tf, tid, lane);
+    solve_unit_lower<kThreads>(Af, Tf, sm.f32(M::WN), tid, 0);   // scratch over -W (written later)
     // T diag(beta) and T diag(beta e^gamma) as bf16 tiles [t][s]
     for (int e = tid; e < 64 * 8; e += kThreads) {
       const int t = e >> 3, c8 = (e & 7) * 8;

@@ -271,14 +271,104 @@ __device__ __forceinline__ void store_state_row(float* base, bool tiled, int r, 
         make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
+// Barrier over the NT threads of a group: bar_id 0 is the whole CTA
+// (__syncthreads), others a named barrier that exactly those threads use.
+// (Ids 1 and 2 are the only named barriers used, as immediates.)
+template <int NT>
+__device__ __forceinline__ void group_sync(int bar_id) {
+  if (bar_id == 0)
+    __syncthreads();
+  else if (bar_id == 1)
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+  else
+    asm volatile("bar.sync 2, %0;" ::"n"(NT) : "memory");
+}
+
+// The same, returning whether every thread of the group passed ok.
+template <int NT>
+__device__ __forceinline__ bool group_sync_and(int bar_id, bool ok) {
+  if (bar_id == 0) return __syncthreads_and(ok);
+  uint32_t r;
+  if (bar_id == 1)
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "n"(NT)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 2, %2, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "n"(NT)
+        : "memory");
+  return r != 0;
+}
+
+// One block diagonal d = i - j of T (blocks (j + d, j), j = 0 .. 3 - d), over
+// NT threads, each with up to ceil(256 (4 - d) / NT) outputs in flight:
+//   M_ij = sum_{k=j}^{i-1} A_ik T_kj   (into the scratch Mf),
+//   T_ij = -T_ii M_ij.
+template <int NT, int D>
+__device__ __forceinline__ void solve_block_diagonal(const float* Af, float* Tf, float* Mf, int tid, int bar_id) {
+  constexpr int kOuts = 256 * (4 - D), kPer = (kOuts + NT - 1) / NT;
+  float m[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int o = tid + u * NT;
+    m[u] = 0.0f;
+    if (kPer * NT == kOuts || o < kOuts) {
+      const int j = o >> 8, i = j + D, r = (o >> 4) & 15, c = o & 15;
+#pragma unroll
+      for (int k2 = 0; k2 < D; ++k2) {
+        const int kb = j + k2;
+#pragma unroll
+        for (int s = 0; s < 16; ++s)
+          m[u] = fmaf(Af[(16 * i + r) * LDA + 16 * kb + s], Tf[(16 * kb + s) * LDA + 16 * j + c], m[u]);
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u)
+    if (kPer * NT == kOuts || tid + u * NT < kOuts) Mf[tid + u * NT] = m[u];
+  group_sync<NT>(bar_id);
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int o = tid + u * NT;
+    if (kPer * NT == kOuts || o < kOuts) {
+      const int j = o >> 8, i = j + D, r = (o >> 4) & 15, c = o & 15;
+      float acc = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 16; ++q) acc = fmaf(Tf[(16 * i + r) * LDA + 16 * i + q], Mf[(j << 8) + (q << 4) + c], acc);
+      m[u] = -acc;
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int o = tid + u * NT;
+    if (kPer * NT == kOuts || o < kOuts) {
+      const int j = o >> 8, i = j + D, r = (o >> 4) & 15, c = o & 15;
+      Tf[(16 * i + r) * LDA + 16 * j + c] = m[u];
+    }
+  }
+  group_sync<NT>(bar_id);
+}
+
 // T = (I + A)^{-1} for a strictly lower 64 x 64 matrix A (fp32, row stride
 // LDA): the 16 x 16 diagonal blocks by forward substitution, a column per
-// thread, then the blocks below them one block diagonal at a time,
-//   T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj.
-// Every thread of the CTA (NT of them) calls it; it ends with a CTA barrier.
+// thread, then the blocks below them one block diagonal at a time, each
+// product spread over the NT threads of a group (Mf: 3 x 16 x 16 fp32
+// scratch; tid: the thread's index in the group; bar_id: the group's barrier,
+// 0 for the whole CTA).  Every thread of the group calls it; it ends with a
+// group barrier.
 template <int NT>
-__device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, int tid, int lane) {
-  static_assert(NT >= 192 && NT % 32 == 0, "the block levels use up to 192 threads");
+__device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, float* Mf, int tid, int bar_id) {
+  static_assert(NT >= 64 && NT % 32 == 0, "the diagonal blocks use 64 threads");
   if (tid < 64) {
     const int b = tid >> 4, c = tid & 15;
     float x[16];
@@ -300,38 +390,10 @@ __device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, int
       Tf[(16 * bi + r) * LDA + 16 * bj + c] = 0.0f;
     }
   }
-  __syncthreads();
-#pragma unroll 1
-  for (int d = 1; d < 4; ++d) {
-    const int tasks = 64 * (4 - d);
-    if (tid < tasks) {
-      const int j = tid >> 6, i = j + d, c = (tid >> 2) & 15, qr = tid & 3;
-      // M[4qr + r][c] = sum_{k=j}^{i-1} A_ik T_kj
-      float m[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      for (int kb = j; kb < i; ++kb) {
-#pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2) {
-          const float tv = Tf[(16 * kb + s2) * LDA + 16 * j + c];
-#pragma unroll
-          for (int r = 0; r < 4; ++r) m[r] = fmaf(Af[(16 * i + 4 * qr + r) * LDA + 16 * kb + s2], tv, m[r]);
-        }
-      }
-      float mf[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) mf[4 * q + r] = __shfl_sync(0xffffffffu, m[r], (lane & ~3) | q);
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int rr = 4 * qr + r;
-        float acc = 0.0f;
-#pragma unroll
-        for (int q = 0; q < 16; ++q) acc = fmaf(Tf[(16 * i + rr) * LDA + 16 * i + q], mf[q], acc);
-        Tf[(16 * i + rr) * LDA + 16 * j + c] = -acc;
-      }
-    }
-    __syncthreads();
-  }
+  group_sync<NT>(bar_id);
+  solve_block_diagonal<NT, 1>(Af, Tf, Mf, tid, bar_id);
+  solve_block_diagonal<NT, 2>(Af, Tf, Mf, tid, bar_id);
+  solve_block_diagonal<NT, 3>(Af, Tf, Mf, tid, bar_id);
 }
 
 // Launchers of the split prefill (prep pass, then the scan passes).

@@ -42,20 +42,21 @@ constexpr int kMaxG = 4;   // value heads per key head on the compiled path
 // Shared memory (bytes from a 1024-aligned base).  Sized for two CTAs per SM.
 struct PrepLay {
   static constexpr uint32_t KQ = 0;             // bf16 [K^ | Q^], 64-column blocks 16 KB apart
-  static constexpr uint32_t KQ16 = 32768;       // fp16 copy of KQ (Gram operands) ...
-  static constexpr uint32_t AF = KQ16;          // ... then A and T fp32 [64][LDA] ...
-  static constexpr uint32_t TF = AF + 64 * LDA * 4;
-  static constexpr uint32_t TW = AF;            // ... then T diag(beta e^gamma) over A ...
-  static constexpr uint32_t WN = AF;            // ... then -W [t][d_k]
-  static constexpr uint32_t RAW = 66560;        // two staged raw blocks: q | k, then v of two heads ...
-  static constexpr uint32_t P = RAW;            // ... then a head's P tile
+  static constexpr uint32_t KQ16 = 32768;       // fp16 copy of KQ (Gram operands), then head group 0's area
+  static constexpr uint32_t RAW = 66560;        // two staged raw blocks: q | k, then v of two heads;
+                                                // then head group 1's area
   static constexpr uint32_t GATE = RAW + 2 * RAW_BLK;   // per head: fp32 gamma, beta, e^gamma [64]
-  static constexpr uint32_t BYTES = GATE + kMaxG * 3 * 64 * 4 + 1024;   // + slack to align the base
+  static constexpr uint32_t MF = GATE + kMaxG * 3 * 64 * 4;   // per head group: the solve's scratch
+  static constexpr uint32_t BYTES = MF + 2 * 3 * 256 * 4 + 1024;   // + slack to align the base
+  // A head group's area: A and T fp32 [64][LDA], then T diag(beta e^gamma)
+  // over A, then -W [t][d_k] over A
+  __host__ __device__ static constexpr uint32_t area(int grp) { return grp == 0 ? KQ16 : RAW; }
 };
-static_assert(PrepLay::TF + 64 * LDA * 4 <= PrepLay::RAW, "A and T overlap the raw staging");
+static_assert(PrepLay::KQ16 + 2 * 64 * LDA * 4 <= PrepLay::RAW, "head group 0's A and T overlap the raw staging");
+static_assert(2 * 64 * LDA * 4 <= 2 * RAW_BLK, "head group 1's A and T exceed the raw staging");
 static_assert(PrepLay::RAW % 1024 == 0 && RAW_BLK % 128 == 0, "TMA destinations need 128-byte alignment");
 static_assert(2 * (PrepLay::BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
-constexpr uint32_t TP_G = 0, TP_W = 64, TP_COLS = 128;   // TMEM: Gram [K^;Q^]K^T, W^T
+constexpr uint32_t TP_G = 0, TP_W = 64, TP_COLS = 256;   // TMEM: Gram [K^;Q^]K^T, W^T per head group
 
 // This lane's 4 channels ch .. ch+3 of the conv weight, w[tap][channel].
 __device__ __forceinline__ void conv_weights(const uint16_t* conv_w, int ch, float (&w)[kConvW][4]) {
@@ -79,6 +80,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mbar;       // MMA completion
   __shared__ __align__(8) uint64_t mbar_raw;   // staged raw rows landed
+  __shared__ __align__(8) uint64_t mb_w[2];    // a head group's W product done
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -94,12 +96,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   const float* cs_seq = p.conv_state + (size_t)n * (kConvW - 1) * Cc;   // this sequence's carried conv state
 
   const Smem sm = smem_aligned(smem_raw);
-  float* Af = sm.f32(L_::AF);
-  float* Tf = sm.f32(L_::TF);
 
   if (tid == 0) {
     tc::mbar_init(&mbar, 1);
     tc::mbar_init(&mbar_raw, 1);
+    tc::mbar_init(&mb_w[0], 1);
+    tc::mbar_init(&mb_w[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base_s, TP_COLS);
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base_s;
-  const int quarter = warp & 3, half = warp >> 2;   // TMEM lane quarter, 32-column half
+  const int quarter = warp & 3, half = warp >> 2;   // TMEM lane quarter; CTA half (= head group)
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
   const int row = 32 * quarter + lane;
   const int y_raw = start + t0 - (kConvW - 1);      // first staged row (a chunk and its halo)
@@ -242,99 +244,132 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   }
   if (ok && !wait_mma()) ok = false;   // the Gram product (and KQ16 is free)
 
+  // ---- per value head, the two halves of the CTA (128 threads, a warp per TMEM
+  //      lane quarter) each take a head, synchronising on their own barrier ----
+  {
+    const int grp = half, gtid = tid & 127, bar = 1 + grp;
+    float* Af = sm.f32(L_::area(grp));
+    float* Tf = Af + 64 * LDA;
+    float* Mf = sm.f32(L_::MF + grp * 3 * 256 * 4);
+    uint8_t* wn = sm.base + L_::area(grp);
+    const uint32_t tw = sm.addr + L_::area(grp);
+    const uint32_t tm_w = tmem + TP_W + 64 * grp;
+    uint32_t wphase = 0;
+    bool gok = ok;
 #pragma unroll 1
-  for (int g = 0; g < G && ok; ++g) {
-    const int h = kh * G + g;
-    uint8_t* rv = p.rec_v + ((size_t)c * p.h_v + h) * kRecV;
-    const float* gam = sm.f32(L_::GATE + g * 3 * 64 * 4);
-    const float* bet = gam + 64;
-    const float* eg = gam + 128;
-    if (g > 0) {   // the previous head's -W and P tiles have left shared memory
-      if (tid == 0) bulk_wait_read();
-      __syncthreads();
-    }
-    // ---- A (fp32) and P (bf16, staged over the raw rows) from the Gram rows: lane
-    //      quarters 0-1 hold K^K^T rows, 2-3 Q^K^T rows; the two warps of a quarter
-    //      split its columns ----
-    {
-      float v[32];
-      const int t = row & 63, c0 = 32 * half;
-      const float gt = gam[t];
-      tc::tmem_ld32(tmem + lane_base + TP_G + c0, v);
-      if (quarter < 2) {
+    for (int g = grp; g < G && gok; g += 2) {
+      const int h = kh * G + g;
+      uint8_t* rv = p.rec_v + ((size_t)c * p.h_v + h) * kRecV;
+      const float* gam = sm.f32(L_::GATE + g * 3 * 64 * 4);
+      const float* bet = gam + 64;
+      const float* eg = gam + 128;
+      if (g >= 2) {   // this group's previous -W tile has left shared memory
+        if (gtid == 0) bulk_wait_read();
+        group_sync<128>(bar);
+      }
+      // ---- A (fp32) and P (bf16, straight into the record) from the Gram rows:
+      //      lane quarters 0-1 hold K^K^T rows, 2-3 Q^K^T rows; rows 0-31 are zero
+      //      right of column 31 ----
+      {
+        const int t = row & 63;
+        const float gt = gam[t];
         const float bt = bet[t];
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const int c0 = 32 * hf;
+          if (t < 32 && hf == 1) {
+            if (quarter < 2) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int s = c0 + i;
-          Af[t * LDA + s] = s < t ? bt * __expf(gt - gam[s]) * v[i] : 0.0f;
+              for (int i = 0; i < 32; ++i) Af[t * LDA + c0 + i] = 0.0f;
+            } else {
+#pragma unroll
+              for (int m = 0; m < 4; ++m)
+                *reinterpret_cast<uint4*>(rv + kRecP + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
+            }
+            continue;
+          }
+          float v[32];
+          tc::tmem_ld32(tmem + lane_base + TP_G + c0, v);
+          if (quarter < 2) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int s = c0 + i;
+              Af[t * LDA + s] = s < t ? bt * __expf(gt - gam[s]) * v[i] : 0.0f;
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int s = c0 + i;
+              v[i] = s <= t ? v[i] * __expf(gt - gam[s]) : 0.0f;
+            }
+#pragma unroll
+            for (int m = 0; m < 4; ++m) store_bf16x8(rv + kRecP, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
+          }
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int s = c0 + i;
-          v[i] = s <= t ? v[i] * __expf(gt - gam[s]) : 0.0f;
-        }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + L_::P, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
       }
-    }
-    sync_for_mma();
-    if (tid == 0) {
-      bulk_store(rv + kRecP, sm.base + L_::P, 8192);
-      bulk_commit();
-    }
+      group_sync<128>(bar);
 
-    // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) -> smem over A ----
-    solve_unit_lower<kPrepThreads>(Af, Tf, tid, lane);
-    {
-      float xb[2][8], xw[2][8];
+      // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) over A ----
+      solve_unit_lower<128>(Af, Tf, Mf, gtid, bar);
+      {
+        float xb[4][8], xw[4][8];
 #pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {   // read all of T before TW overwrites A (T is separate)
-        const int e = tid + q2 * kPrepThreads, t = e >> 3, c8 = (e & 7) * 8;
+        for (int q4 = 0; q4 < 4; ++q4) {   // all of T is read before T diag(beta e^gamma) goes over A
+          const int e = gtid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const float tv = Tf[t * LDA + c8 + q];
-          xb[q2][q] = tv * bet[c8 + q];
-          xw[q2][q] = xb[q2][q] * eg[c8 + q];
+          for (int q = 0; q < 8; ++q) {
+            const float tv = Tf[t * LDA + c8 + q];
+            xb[q4][q] = tv * bet[c8 + q];
+            xw[q4][q] = xb[q4][q] * eg[c8 + q];
+          }
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int e = gtid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
+          store_bf16x8(rv + kRecTB, tc::sw128_off(t, c8, 0), xb[q4]);
+          store_bf16x8(wn, tc::sw128_off(t, c8, 0), xw[q4]);
         }
       }
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      group_sync<128>(bar);
+      tc::fence_after_sync();
+      if (gtid == 0) {
+        // W^T = K^T (T diag(beta e^gamma))^T
 #pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        const int e = tid + q2 * kPrepThreads, t = e >> 3, c8 = (e & 7) * 8;
-        store_bf16x8(rv + kRecTB, tc::sw128_off(t, c8, 0), xb[q2]);
-        store_bf16x8(sm.base + L_::TW, tc::sw128_off(t, c8, 0), xw[q2]);
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tm_w, tc::sdesc_at(D_MN_KQ, sm.addr + L_::KQ + k * 2048), tc::sdesc_at(D_K, tw + k * 32),
+                       ID_MN_A, k > 0);
+        tc::mma_commit(&mb_w[grp]);
+      }
+      gok = group_sync_and<128>(bar, tc::mbar_wait(&mb_w[grp], wphase, kWaitBudget));
+      wphase ^= 1u;
+      tc::fence_after_sync();
+      if (!gok) break;
+
+      // ---- -W tile [t][d_k] (over T diag(beta e^gamma), which the MMA has consumed) ----
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        float v[32];
+        tc::tmem_ld32(tm_w + lane_base + 32 * hf, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(32 * hf + i, row, 8192)) = f32_to_bf16(-v[i]);
+      }
+      tc::fence_proxy_async();
+      group_sync<128>(bar);
+      if (gtid == 0) {
+        bulk_store(rv + kRecWN, wn, 16384);
+        bulk_commit();
       }
     }
-    sync_for_mma();
-    if (tid == 0) {
-      // W^T = K^T (T diag(beta e^gamma))^T
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_bf16(tmem + TP_W, tc::sdesc_at(D_MN_KQ, sm.addr + L_::KQ + k * 2048),
-                     tc::sdesc_at(D_K, sm.addr + L_::TW + k * 32), ID_MN_A, k > 0);
-      tc::mma_commit(&mbar);
-    }
-    if (!wait_mma()) { ok = false; break; }
-
-    // ---- -W tile [t][d_k] (over T diag(beta e^gamma), which the MMA has consumed) ----
-    {
-      float v[32];
-      tc::tmem_ld32(tmem + lane_base + TP_W + 32 * half, v);
-      uint8_t* wn = sm.base + L_::WN;
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(32 * half + i, row, 8192)) = f32_to_bf16(-v[i]);
-    }
-    sync_for_mma();
-    if (tid == 0) {
-      bulk_store(rv + kRecWN, sm.base + L_::WN, 16384);
-      bulk_commit();
-    }
+    if (gtid == 0) bulk_wait_all();   // this group's records are written before its smem goes away
+    ok = __syncthreads_and(gok) && ok;
   }
 
   if (tid == 0) {
     if (!ok) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
-    bulk_wait_all();   // the records are written before this CTA's shared memory goes away
+    bulk_wait_all();   // the KQ record is written before this CTA's shared memory goes away
   }
   // a raw copy still in flight after a time-out must land before the shared memory goes away
   if (raw_pending) tc::mbar_wait(&mbar_raw, raw_phase, kWaitBudget);
@@ -356,8 +391,8 @@ template <> struct ScanLay<false> {    // output pass
   static constexpr uint32_t WN = 98304;     // -W | V^ | T diag(beta): the record's first 40 KB, one copy
   static constexpr uint32_t P = WN + 40960;
   static constexpr uint32_t GT = P + 8192;  // two gate buffers: e^gamma [64], e^{gamma_C - gamma} [64]
-  static constexpr uint32_t Z = GT + 1024;  // z bf16 [64][128]
-  static constexpr uint32_t VN = Z + 16384;     // Vn^T [d_v][t]
+  static constexpr uint32_t Z = GT + 1024;  // two z buffers, bf16 [64][128]
+  static constexpr uint32_t VN = Z + 32768;     // Vn^T [d_v][t]
   static constexpr uint32_t VNS = VN + 16384;   // Vn^T diag(e^{gamma_C - gamma})
   static constexpr uint32_t OST = VN;           // O fp32 [64][LDO], over VN and VNS once they are consumed
   static constexpr uint32_t NW = VNS + 16384;   // RMSNorm weight
@@ -414,7 +449,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   __shared__ __align__(8) uint64_t mb_a;       // -W | V^ | T diag(beta)
   __shared__ __align__(8) uint64_t mb_g;       // the gates (a chunk ahead)
   __shared__ __align__(8) uint64_t mb_p;       // P (output pass)
-  __shared__ __align__(8) uint64_t mb_z;       // z (output pass)
+  __shared__ __align__(8) uint64_t mb_z[2];    // z buffers (output pass)
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -454,7 +489,8 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     tc::mbar_init(&mb_a, 1);
     tc::mbar_init(&mb_g, 1);
     tc::mbar_init(&mb_p, 1);
-    tc::mbar_init(&mb_z, 1);
+    tc::mbar_init(&mb_z[0], 1);
+    tc::mbar_init(&mb_z[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base_s, TS_COLS);
@@ -469,47 +505,64 @@ __global__ void __launch_bounds__(kScanThreads, 1)
 
   auto rec_kq = [&](int j) { return p.rec_kq + ((size_t)(sg.c0 + j) * p.h_k + kh) * kRecKQ; };
   auto rec_v = [&](int j) { return p.rec_v + ((size_t)(sg.c0 + j) * p.h_v + h) * kRecV; };
-  // record loads, issued by one thread (tid 32); each barrier has at most one in flight
+  // Record loads, issued by one thread (tid 32) under conditions every thread
+  // evaluates alike, so every thread keeps the same counts.  The k-th copy on a
+  // barrier completes its phase of parity k & 1; each barrier has at most one
+  // copy in flight.
+  struct Pipe {
+    uint32_t issued, waited;
+  };
+  Pipe q_kq[2] = {{0, 0}, {0, 0}}, q_a = {0, 0}, q_g = {0, 0}, q_p = {0, 0}, q_z[2] = {{0, 0}, {0, 0}};
+  auto pwait = [&](uint64_t* mb, Pipe& q) -> bool {
+    const bool r = tc::mbar_wait(mb, q.waited & 1u, kWaitBudget);
+    if (r) ++q.waited;
+    return r;
+  };
   auto load_kq = [&](int j) {
     uint8_t* dst = sm.base + M::KQ + (j & 1) * M::KQ_BUF;
-    if (!kXfer) {
-      bulk_load(dst, rec_kq(j), kRecKQ, &mb_kq[j & 1]);
-    } else {   // the K^ halves only
-      mbar_expect_tx(&mb_kq[j & 1], 16384);
-      bulk_copy(dst, rec_kq(j), 8192, &mb_kq[j & 1]);
-      bulk_copy(dst + 8192, rec_kq(j) + 16384, 8192, &mb_kq[j & 1]);
+    if (tid == 32) {
+      if (!kXfer) {
+        bulk_load(dst, rec_kq(j), kRecKQ, &mb_kq[j & 1]);
+      } else {   // the K^ halves only
+        mbar_expect_tx(&mb_kq[j & 1], 16384);
+        bulk_copy(dst, rec_kq(j), 8192, &mb_kq[j & 1]);
+        bulk_copy(dst + 8192, rec_kq(j) + 16384, 8192, &mb_kq[j & 1]);
+      }
     }
+    ++q_kq[j & 1].issued;
   };
-  auto load_a = [&](int j) { bulk_load(sm.base + M::WN, rec_v(j), kRecP, &mb_a); };
-  auto load_g = [&](int j) { bulk_load(sm.base + M::GT + (j & 1) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g); };
-  auto load_p = [&](int j) { bulk_load(sm.base + M::P, rec_v(j) + kRecP, 8192, &mb_p); };
+  auto load_a = [&](int j) {
+    if (tid == 32) bulk_load(sm.base + M::WN, rec_v(j), kRecP, &mb_a);
+    ++q_a.issued;
+  };
+  auto load_g = [&](int j) {
+    if (tid == 32) bulk_load(sm.base + M::GT + (j & 1) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g);
+    ++q_g.issued;
+  };
+  auto load_p = [&](int j) {
+    if (tid == 32) bulk_load(sm.base + M::P, rec_v(j) + kRecP, 8192, &mb_p);
+    ++q_p.issued;
+  };
   auto load_z = [&](int j) {
-    mbar_expect_tx(&mb_z, C * kD * 2);
-    tma_load_2d(sm.base + M::Z, &tm_z, h * kD, start + sg.begin + C * j, &mb_z);
-  };
-  // copies in flight per barrier, and waits completed (the k-th copy on a barrier
-  // completes its phase of parity k & 1); only the abort path needs these
-  bool pend_kq[2] = {true, nch > 1}, pend_a = true, pend_g = true, pend_p = !kXfer, pend_z = !kXfer;
-  uint32_t w_kq[2] = {0, 0}, w_a = 0, w_g = 0, w_p = 0, w_z = 0;
-  if (tid == 32) {
-    load_g(0);
-    load_kq(0);
-    if (nch > 1) load_kq(1);
-    load_a(0);
-    if (!kXfer) {
-      load_p(0);
-      load_z(0);
+    if (tid == 32) {
+      mbar_expect_tx(&mb_z[j & 1], C * kD * 2);
+      tma_load_2d(sm.base + M::Z + (j & 1) * 16384, &tm_z, h * kD, start + sg.begin + C * j, &mb_z[j & 1]);
     }
+    ++q_z[j & 1].issued;
+  };
+  load_g(0);
+  load_kq(0);
+  if (nch > 1) load_kq(1);
+  load_a(0);
+  if (!kXfer) {
+    load_p(0);
+    load_z(0);
   }
 
   // initial state(s): bf16 into the operand tile(s), and into TMEM in fp32
   // already scaled by the first chunk's total decay (the state update adds to
   // e^{gamma_C} S0; each chunk's end scales for the next one)
-  bool aborted = !__syncthreads_and(tc::mbar_wait(&mb_g, 0u, kWaitBudget));
-  if (!aborted) {
-    pend_g = false;
-    ++w_g;
-  }
+  bool aborted = !__syncthreads_and(pwait(&mb_g, q_g));
   {
     const float dC0 = sm.f32(M::GT)[C - 1];
     const int col0 = part * 32;
@@ -535,77 +588,62 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       tc::tmem_st32(tmem + lane_base + TS_X + col0, v);
     }
   }
-  sync_for_mma();
+  // the first chunk's records (and the state tiles for the tensor core)
+  if (!aborted) {
+    const bool ok = pwait(&mb_kq[0], q_kq[0]) && pwait(&mb_a, q_a);
+    aborted = !sync_for_mma_and(ok);
+  }
 
   uint32_t phase = 0;
-  auto wait_mma = [&]() -> bool {
-    const bool ok = tc::mbar_wait(&mb_mma, phase, kWaitBudget);
+  auto wait_mma = [&](bool more) -> bool {   // ANDs in `more`, the thread's other waits
+    const bool ok = tc::mbar_wait(&mb_mma, phase, kWaitBudget) && more;
     phase ^= 1u;
     const bool all_ok = __syncthreads_and(ok);
     tc::fence_after_sync();
     return all_ok;
   };
-  // output pass: the gated RMSNorm epilogue of chunk jj from the O staging, a
-  // warp per 4 tokens and 4 channels per lane; then z of chunk jj + 1 may load
-  auto epilogue = [&](int jj) -> bool {
+  // output pass: the gated RMSNorm epilogue of chunk jj from the O staging (its z
+  // has landed), a warp per 4 tokens and 4 channels per lane
+  auto epilogue = [&](int jj) {
     const int t0e = sg.begin + C * jj, Le = min(C, seg_end - t0e);
-    if (!__syncthreads_and(tc::mbar_wait(&mb_z, w_z & 1u, kWaitBudget))) return false;
-    pend_z = false;
-    ++w_z;
-    {
-      const int tq = 4 * warp;
-      float o[4][4], ss[4];
+    const uint8_t* zb = sm.base + M::Z + (jj & 1) * 16384;
+    const int tq = 4 * warp;
+    float o[4][4], ss[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 o4 = reinterpret_cast<const float4*>(Ost + (tq + i) * LDO)[lane];
-        o[i][0] = o4.x; o[i][1] = o4.y; o[i][2] = o4.z; o[i][3] = o4.w;
-        ss[i] = o4.x * o4.x;
-        ss[i] = fmaf(o4.y, o4.y, ss[i]);
-        ss[i] = fmaf(o4.z, o4.z, ss[i]);
-        ss[i] = fmaf(o4.w, o4.w, ss[i]);
-      }
-      const float r = rsqrtf(warp_sum4(ss, lane) * (1.0f / kD) + p.rms_eps);
-      const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
+    for (int i = 0; i < 4; ++i) {
+      const float4 o4 = reinterpret_cast<const float4*>(Ost + (tq + i) * LDO)[lane];
+      o[i][0] = o4.x; o[i][1] = o4.y; o[i][2] = o4.z; o[i][3] = o4.w;
+      ss[i] = o4.x * o4.x;
+      ss[i] = fmaf(o4.y, o4.y, ss[i]);
+      ss[i] = fmaf(o4.z, o4.z, ss[i]);
+      ss[i] = fmaf(o4.w, o4.w, ss[i]);
+    }
+    const float r = rsqrtf(warp_sum4(ss, lane) * (1.0f / kD) + p.rms_eps);
+    const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float rstd = __shfl_sync(0xffffffffu, r, token_lane(i));
-        const uint2 zr = *reinterpret_cast<const uint2*>(sm.base + M::Z + (tq + i) * 256 + lane * 8);
-        float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
-                      bf16_to_f32(zr.y >> 16)};
-        silu4(g);
-        uint2 ov;
-        ov.x = pack_bf16x2(o[i][0] * rstd * w4.x * g[0], o[i][1] * rstd * w4.y * g[1]);
-        ov.y = pack_bf16x2(o[i][2] * rstd * w4.z * g[2], o[i][3] * rstd * w4.w * g[3]);
-        if (tq + i < Le)
-          *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0e + tq + i) * p.h_v + h) * kD + 4 * lane) = ov;
-      }
+    for (int i = 0; i < 4; ++i) {
+      const float rstd = __shfl_sync(0xffffffffu, r, token_lane(i));
+      const uint2 zr = *reinterpret_cast<const uint2*>(zb + (tq + i) * 256 + lane * 8);
+      float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
+                    bf16_to_f32(zr.y >> 16)};
+      silu4(g);
+      uint2 ov;
+      ov.x = pack_bf16x2(o[i][0] * rstd * w4.x * g[0], o[i][1] * rstd * w4.y * g[1]);
+      ov.y = pack_bf16x2(o[i][2] * rstd * w4.z * g[2], o[i][3] * rstd * w4.w * g[3]);
+      if (tq + i < Le)
+        *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0e + tq + i) * p.h_v + h) * kD + 4 * lane) = ov;
     }
-    __syncthreads();   // the O staging and the z buffer are read
-    if (jj + 1 < nch) {
-      if (tid == 32) load_z(jj + 1);
-      pend_z = true;
-    }
-    return true;
   };
 
+  // Four CTA barriers per chunk; every copy is waited for at the barrier before
+  // the phase that needs it, issued at the barrier after the phase that frees its
+  // buffer.
   for (int j = 0; j < nch && !aborted; ++j) {
     const float* eg = sm.f32(M::GT + (j & 1) * 512);
     const float* egc = eg + 64;
     const uint32_t kq = sm.addr + M::KQ + (j & 1) * M::KQ_BUF;
-    {
-      bool ok = tc::mbar_wait(&mb_kq[j & 1], w_kq[j & 1] & 1u, kWaitBudget);
-      ok = tc::mbar_wait(&mb_a, w_a & 1u, kWaitBudget) && ok;
-      if (!__syncthreads_and(ok)) { aborted = true; break; }
-      pend_kq[j & 1] = false;
-      pend_a = false;
-      ++w_kq[j & 1];
-      ++w_a;
-    }
     // the gates of the next chunk go where those of the chunk before this one were
-    if (j + 1 < nch) {
-      if (tid == 32) load_g(j + 1);
-      pend_g = true;
-    }
+    if (j + 1 < nch) load_g(j + 1);
 
     // ---- batch 1: [O1 = S0 Q^T,] U = V^T (T diag beta)^T, Vn^T = U + S0 (-W)^T
     //      [, transfer: Vn_X^T = X0 (-W)^T] ----
@@ -639,12 +677,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       tc::mma_commit(&mb_mma);
     }
     // meanwhile: write out the previous chunk
-    if (!kXfer && j > 0 && !epilogue(j - 1)) { aborted = true; break; }
-    if (!wait_mma()) { aborted = true; break; }
-    // the next chunk's -W | V^ | T diag(beta) go where batch 1 has finished
+    if (!kXfer && j > 0) epilogue(j - 1);
+    if (!wait_mma(true)) { aborted = true; break; }
+    // batch 1 has finished with -W | V^ | T diag(beta); the epilogue with the
+    // O staging and the previous z buffer
     if (j + 1 < nch) {
-      if (tid == 32) load_a(j + 1);
-      pend_a = true;
+      load_a(j + 1);
+      if (!kXfer) load_z(j + 1);
     }
 
     // ---- Vn^T tiles, row = d_v index: output pass plain and decay-weighted,
@@ -666,14 +705,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         store_bf16x8(sm.base + M::VNS, off, vs + 8 * m);
       }
     }
-    {
-      const bool ok = kXfer || tc::mbar_wait(&mb_p, w_p & 1u, kWaitBudget);
-      if (!sync_for_mma_and(ok)) { aborted = true; break; }
-      if (!kXfer) {
-        pend_p = false;
-        ++w_p;
-      }
-    }
+    if (!sync_for_mma_and(kXfer || pwait(&mb_p, q_p))) { aborted = true; break; }
 
     // ---- batch 2: [O2 = Vn^T P^T,] S += Vn^T diag(e^{gC-g}) K^ [, X likewise] ----
     if (tid == 0) {
@@ -698,27 +730,15 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       }
       tc::mma_commit(&mb_mma);
     }
-    if (!wait_mma()) { aborted = true; break; }
-    // P of the next chunk and [K^ | Q^] of the one after go where batch 2 has finished
-    if (!kXfer && j + 1 < nch) {
-      if (tid == 32) load_p(j + 1);
-      pend_p = true;
-    }
-    if (j + 2 < nch) {
-      if (tid == 32) load_kq(j + 2);
-      pend_kq[j & 1] = true;
-    }
+    if (!wait_mma(j + 1 >= nch || pwait(&mb_g, q_g))) { aborted = true; break; }
+    // batch 2 has finished with P and this [K^ | Q^] buffer
+    if (!kXfer && j + 1 < nch) load_p(j + 1);
+    if (j + 2 < nch) load_kq(j + 2);
 
     // ---- new state(s) -> bf16 operand tiles, and in TMEM scaled by the next
     //      chunk's total decay; output pass: O = e^gamma O1 + O2 -> fp32 staging ----
     {
-      float dC = 1.0f;
-      if (j + 1 < nch) {
-        if (!__syncthreads_and(tc::mbar_wait(&mb_g, w_g & 1u, kWaitBudget))) { aborted = true; break; }
-        pend_g = false;
-        ++w_g;
-        dC = sm.f32(M::GT + ((j + 1) & 1) * 512)[C - 1];
-      }
+      const float dC = j + 1 < nch ? sm.f32(M::GT + ((j + 1) & 1) * 512)[C - 1] : 1.0f;
 #pragma unroll
       for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
         float v[32];
@@ -744,20 +764,31 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         }
       }
     }
-    sync_for_mma();
+    // the next chunk's records and this chunk's z
+    {
+      bool ok = true;
+      if (j + 1 < nch) ok = pwait(&mb_kq[(j + 1) & 1], q_kq[(j + 1) & 1]) && pwait(&mb_a, q_a);
+      if (!kXfer) ok = pwait(&mb_z[j & 1], q_z[j & 1]) && ok;
+      if (!sync_for_mma_and(ok)) { aborted = true; break; }
+    }
   }
-  if (!kXfer && !aborted && !epilogue(nch - 1)) aborted = true;
+  if (!kXfer && !aborted) epilogue(nch - 1);
 
   if (aborted) {
     if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
     // let this CTA's own copies finish (bounded) before its shared memory goes
     // away (a copy that already landed passes its wait at once)
-    if (pend_kq[0]) tc::mbar_wait(&mb_kq[0], w_kq[0] & 1u, kWaitBudget);
-    if (pend_kq[1]) tc::mbar_wait(&mb_kq[1], w_kq[1] & 1u, kWaitBudget);
-    if (pend_a) tc::mbar_wait(&mb_a, w_a & 1u, kWaitBudget);
-    if (pend_g) tc::mbar_wait(&mb_g, w_g & 1u, kWaitBudget);
-    if (pend_p) tc::mbar_wait(&mb_p, w_p & 1u, kWaitBudget);
-    if (pend_z) tc::mbar_wait(&mb_z, w_z & 1u, kWaitBudget);
+    auto drain = [&](uint64_t* mb, Pipe& q) {
+      while (q.waited < q.issued && pwait(mb, q)) {
+      }
+    };
+    drain(&mb_kq[0], q_kq[0]);
+    drain(&mb_kq[1], q_kq[1]);
+    drain(&mb_a, q_a);
+    drain(&mb_g, q_g);
+    drain(&mb_p, q_p);
+    drain(&mb_z[0], q_z[0]);
+    drain(&mb_z[1], q_z[1]);
   } else {
     // final state back to global memory (fp32); the transfer pass adds the map X
     // as bf16 hi / lo tiles for the combine pass's tensor-core products
