@@ -62,12 +62,21 @@ def _peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def _src_hash(name: str) -> str:
-    with open(os.path.join(ROOT, "gated_deltanet_linear_06_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+# the sources each kernel family is built from: a change to any of them voids
+# the committed DRAM counters
+PREFILL_SRC = ("gdn_prefill.cu", "gdn_prefill_split.cu", "gdn_prefill.cuh", "gdn_tc.cuh", "gdn_common.cuh")
+DECODE_SRC = ("gdn_decode.cu",)
 
 
-def _traffic(kernel: str, src: str):
+def _src_hash(names) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_06_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel: str, src):
     """DRAM bytes per launch from the committed ncu summary, or None if the
     kernel source changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -372,7 +381,7 @@ def run_ours(args) -> dict | None:
                    "l2": "no flush: prefill inputs 0.77 GB and decode state 0.54 GB exceed the 129 MB L2",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": hbm, "unit": "GB/s",
-                     "frac": round(pre_gbs / hbm, 4), "traffic": _traffic("prefill", "gdn_prefill.cu"),
+                     "frac": round(pre_gbs / hbm, 4), "traffic": _traffic("prefill", PREFILL_SRC),
                      "kernel": "gdn_prefill (all its kernels: work list, transfer, combine, output, conv state)",
                      "algorithmic_bytes_per_launch": pre_bytes,
                      "peak_source": f"{peak_src} hbm_gbs",
@@ -384,7 +393,7 @@ def run_ours(args) -> dict | None:
                    "unit": "seq-steps/s", "ms_per_call": round(dec_ms / DECODE_CALLS, 4),
                    "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": hbm,
                                 "unit": "GB/s", "frac": round(dec_gbs / hbm, 4),
-                                "traffic": _traffic("decode", "gdn_decode.cu"),
+                                "traffic": _traffic("decode", DECODE_SRC),
                                 "algorithmic_bytes_per_launch": dec_bytes},
                    "e2e": {"value": round(world * DECODE_B * DECODE_CALLS / (e2e_dec_ms * 1e-3), 1),
                            "unit": "seq-steps/s", "h2d_bytes_per_step": h2d_dec,

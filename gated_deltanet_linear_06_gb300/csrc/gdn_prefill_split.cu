@@ -937,8 +937,8 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillA
     }
     float v[32];
     tc::tmem_ld32(tmem + lane_base + col0, v);
+    split_store(v);   // the next step's operands first; the global stores drain meanwhile
     store_state_row(xfer_ptr(p, k0 + sg, h, 1), true, row, col0, v);
-    split_store(v);
   }
   if (!ok) {
     if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
