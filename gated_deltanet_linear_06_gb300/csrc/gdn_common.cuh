@@ -20,14 +20,27 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// Two fp32 values -> bf16x2 (lo in bits 0-15), round to nearest even, in one
+// packed conversion: the same bits as converting each value alone, at several
+// times the throughput of two single conversions.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return static_cast<uint32_t>(f32_to_bf16(lo)) |
-         (static_cast<uint32_t>(f32_to_bf16(hi)) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
+// The same for fp16x2.
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(lo))) |
-         (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(hi))) << 16);
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// a and b rounded to bf16 (returned as fp32), with one packed conversion.
+__device__ __forceinline__ void round_bf16x2(float a, float b, float& ra, float& rb) {
+  const uint32_t r = pack_bf16x2(a, b);
+  ra = __uint_as_float(r << 16);
+  rb = __uint_as_float(r & 0xffff0000u);
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + __expf(-x)); }

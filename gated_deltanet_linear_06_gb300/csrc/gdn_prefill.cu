@@ -415,9 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::tmem_ld16(tmem + lane_base + TM_W + part * 16, v);
       uint8_t* wn = sm.base + M::WN;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < 16; i += 2) {   // two tokens per conversion
         const int t = part * 16 + i;
-        *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(t, row, 8192)) = f32_to_bf16(-v[i]);
+        const uint32_t w2 = pack_bf16x2(-v[i], -v[i + 1]);
+        *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(t, row, 8192)) = (uint16_t)(w2 & 0xffffu);
+        *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(t + 1, row, 8192)) = (uint16_t)(w2 >> 16);
       }
     }
     sync_for_mma();

@@ -353,8 +353,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         float v[32];
         tc::tmem_ld32(tm_w + lane_base + 32 * hf, v);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(32 * hf + i, row, 8192)) = f32_to_bf16(-v[i]);
+        for (int i = 0; i < 32; i += 2) {   // two tokens per conversion
+          const uint32_t w2 = pack_bf16x2(-v[i], -v[i + 1]);
+          *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(32 * hf + i, row, 8192)) = (uint16_t)(w2 & 0xffffu);
+          *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(32 * hf + i + 1, row, 8192)) = (uint16_t)(w2 >> 16);
+        }
       }
       tc::fence_proxy_async();
       group_sync<128>(bar);
@@ -803,7 +806,12 @@ __global__ void __launch_bounds__(kScanThreads, 1)
       float v[32], lo[32];
       tc::tmem_ld32(tmem + lane_base + TS_X + part * 32, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) lo[i] = v[i] - bf16_to_f32(f32_to_bf16(v[i]));   // exact in fp32
+      for (int i = 0; i < 32; i += 2) {   // X - bf16(X), exact in fp32
+        float r0, r1;
+        round_bf16x2(v[i], v[i + 1], r0, r1);
+        lo[i] = v[i] - r0;
+        lo[i + 1] = v[i + 1] - r1;
+      }
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const uint32_t off = tc::sw128_off(row, part * 32 + 8 * m, 16384);
@@ -882,11 +890,12 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillA
     for (int m = 0; m < 4; ++m) {
       float a[8], b[8], c[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        a[i] = bf16_to_f32(f32_to_bf16(v[8 * m + i]));
-        const float r1 = v[8 * m + i] - a[i];
-        b[i] = bf16_to_f32(f32_to_bf16(r1));
-        c[i] = r1 - b[i];
+      for (int i = 0; i < 8; i += 2) {
+        round_bf16x2(v[8 * m + i], v[8 * m + i + 1], a[i], a[i + 1]);
+        const float r0 = v[8 * m + i] - a[i], r1 = v[8 * m + i + 1] - a[i + 1];
+        round_bf16x2(r0, r1, b[i], b[i + 1]);
+        c[i] = r0 - b[i];
+        c[i + 1] = r1 - b[i + 1];
       }
       const uint32_t off = tc::sw128_off(row, col0 + 8 * m, 16384);
       store_bf16x8(sm.base + L_::S1, off, a);
