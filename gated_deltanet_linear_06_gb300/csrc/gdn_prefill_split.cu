@@ -20,10 +20,11 @@
 // bulk copies while the current chunk computes; in the output pass the gated
 // RMSNorm epilogue of a chunk runs while the tensor core works on the next.
 //
-// The transfer pass (segments of a long sequence) runs the same scan from
-// S = 0 and, alongside, X from the identity with v = 0, which yields the
-// segment's affine map S_end = S_start X + S_end(0); the combine pass then
-// chains the maps into every segment's true start state.
+// The transfer pass (segments of a long sequence) runs the same scan in two
+// independent tracks per segment: S from 0 with the real inputs, and X from
+// the identity with v = 0, which yields the segment's affine map S_end =
+// S_start X + S_end(0); the combine pass then chains the maps into every
+// segment's true start state.
 #include <cuda.h>
 
 #include "../../include/gdn.h"
@@ -381,17 +382,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   if (warp == 0) tc::tmem_dealloc(tmem, TP_COLS);
 }
 
-// ============================== scan passes ==============================
+// ============================== output pass ==============================
 
 constexpr int kScanThreads = 512;   // 16 warps: 4 per TMEM lane quarter
 static_assert(kScanThreads / 32 * 4 == C, "the epilogue gives each warp 4 of a chunk's tokens");
-template <bool kXfer> struct ScanLay;
-template <> struct ScanLay<false> {    // output pass
+struct ScanLay {                         // output pass
   static constexpr uint32_t S = 0;          // S bf16 [d_v][d_k], K blocks 16 KB apart
-  static constexpr uint32_t X = 0;          // (unused)
   static constexpr uint32_t KQ = 32768;     // two [K^ | Q^] buffers
   static constexpr uint32_t KQ_BUF = 32768;
   static constexpr uint32_t WN = 98304;     // -W | V^ | T diag(beta): the record's first 40 KB, one copy
+  static constexpr uint32_t VH = WN + kRecVH;
+  static constexpr uint32_t TB = WN + kRecTB;
   static constexpr uint32_t P = WN + 40960;
   static constexpr uint32_t GT = P + 8192;  // two gate buffers: e^gamma [64], e^{gamma_C - gamma} [64]
   static constexpr uint32_t Z = GT + 1024;  // two z buffers, bf16 [64][128]
@@ -401,36 +402,15 @@ template <> struct ScanLay<false> {    // output pass
   static constexpr uint32_t NW = VNS + 16384;   // RMSNorm weight
   static constexpr uint32_t BYTES = NW + 512 + 1024;
 };
-template <> struct ScanLay<true> {     // transfer pass
-  static constexpr uint32_t S = 0;
-  static constexpr uint32_t X = 32768;      // X bf16 [d_k][d_k]
-  static constexpr uint32_t KQ = 65536;     // two K^ buffers [K^ kb0 | K^ kb1]
-  static constexpr uint32_t KQ_BUF = 16384;
-  static constexpr uint32_t WN = 98304;
-  static constexpr uint32_t P = 0;          // (unused)
-  static constexpr uint32_t GT = WN + 40960;
-  static constexpr uint32_t Z = 0;          // (unused)
-  static constexpr uint32_t VN = GT + 1024;     // X's Vn^T diag(e^{gamma_C - gamma})
-  static constexpr uint32_t VNS = VN + 16384;   // S's Vn^T diag(e^{gamma_C - gamma})
-  static constexpr uint32_t OST = 0;        // (unused)
-  static constexpr uint32_t NW = 0;         // (unused)
-  static constexpr uint32_t BYTES = VNS + 16384 + 1024;
-};
-template <bool kXfer> struct ScanMap : ScanLay<kXfer> {
-  using L_ = ScanLay<kXfer>;
-  static constexpr uint32_t VH = L_::WN + kRecVH;
-  static constexpr uint32_t TB = L_::WN + kRecTB;
-  static_assert(L_::WN % 1024 == 0 && VH % 1024 == 0 && TB % 1024 == 0 && L_::VN % 1024 == 0 &&
-                    L_::VNS % 1024 == 0 && L_::KQ % 1024 == 0 && (kXfer || L_::P % 1024 == 0),
-                "operand tiles need 1024-byte alignment");
-  static_assert(kXfer || L_::Z % 128 == 0, "TMA destination alignment");
-  static_assert(kXfer || L_::OST + 64 * LDO * 4 <= L_::NW, "O staging overlaps the norm weight");
-  static_assert(L_::BYTES <= 227 * 1024, "shared memory");
-};
+static_assert(ScanLay::WN % 1024 == 0 && ScanLay::VH % 1024 == 0 && ScanLay::TB % 1024 == 0 &&
+                  ScanLay::VN % 1024 == 0 && ScanLay::VNS % 1024 == 0 && ScanLay::KQ % 1024 == 0 &&
+                  ScanLay::P % 1024 == 0,
+              "operand tiles need 1024-byte alignment");
+static_assert(ScanLay::Z % 128 == 0, "TMA destination alignment");
+static_assert(ScanLay::OST + 64 * LDO * 4 <= ScanLay::NW, "O staging overlaps the norm weight");
+static_assert(ScanLay::BYTES <= 227 * 1024, "shared memory");
 // TMEM columns
-constexpr uint32_t TS_S = 0, TS_O1 = 128, TS_U = 192, TS_O2 = 256;   // output pass
-constexpr uint32_t TS_X = 128, TS_UX = 256, TS_VX = 320;             // transfer pass (TS_UX: S's Vn)
-constexpr uint32_t TS_COLS = 512;
+constexpr uint32_t TS_S = 0, TS_O1 = 128, TS_U = 192, TS_O2 = 256, TS_COLS = 512;
 
 // Block-wide sync for the tensor core that also ANDs a per-thread verdict.
 __device__ __forceinline__ bool sync_for_mma_and(bool ok) {
@@ -441,11 +421,10 @@ __device__ __forceinline__ bool sync_for_mma_and(bool ok) {
   return all;
 }
 
-template <bool kXfer>
 __global__ void __launch_bounds__(kScanThreads, 1)
-    scan_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_z) {
-  using M = ScanMap<kXfer>;
-  constexpr uint32_t TU = kXfer ? TS_UX : TS_U;   // U, then S's Vn^T
+    output_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_z) {
+  using M = ScanLay;
+  constexpr uint32_t TU = TS_U;   // U, then Vn^T
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mb_mma;     // MMA completion
   __shared__ __align__(8) uint64_t mb_kq[2];   // [K^ | Q^] buffers
@@ -459,7 +438,6 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int u = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
   if (u >= p.seg_list[0]) return;
   const Seg sg = load_seg(p.seg_list, u);
-  if (kXfer && sg.sigma == sg.nsig - 1) return;   // the last segment needs no transfer map
   const int n = sg.n;
   const int G = p.h_v / p.h_k, kh = h / G;
   const int start = p.cu_seqlens[n];
@@ -471,15 +449,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const float* S_init = nullptr;
   float* S_final = nullptr;
   float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
-  const bool init_tiled = !kXfer && sg.nsig > 1;
-  if (!kXfer) {
-    if (sg.nsig == 1) {
-      S_init = ssm;
-      S_final = ssm;
-    } else {
-      S_init = sg.sigma == 0 ? xfer_ptr(p, sg.k0, h, 2) : xfer_ptr(p, sg.k0 + sg.sigma - 1, h, 1);
-      S_final = sg.sigma == sg.nsig - 1 ? ssm : nullptr;
-    }
+  const bool init_tiled = sg.nsig > 1;
+  if (sg.nsig == 1) {
+    S_init = ssm;
+    S_final = ssm;
+  } else {
+    S_init = sg.sigma == 0 ? xfer_ptr(p, sg.k0, h, 2) : xfer_ptr(p, sg.k0 + sg.sigma - 1, h, 1);
+    S_final = sg.sigma == sg.nsig - 1 ? ssm : nullptr;
   }
 
   const Smem sm = smem_aligned(smem_raw);
@@ -497,7 +473,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base_s, TS_COLS);
-  if (!kXfer && tid < kD) nw[tid] = p.norm_w[tid];
+  if (tid < kD) nw[tid] = p.norm_w[tid];
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -523,15 +499,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   };
   auto load_kq = [&](int j) {
     uint8_t* dst = sm.base + M::KQ + (j & 1) * M::KQ_BUF;
-    if (tid == 32) {
-      if (!kXfer) {
-        bulk_load(dst, rec_kq(j), kRecKQ, &mb_kq[j & 1]);
-      } else {   // the K^ halves only
-        mbar_expect_tx(&mb_kq[j & 1], 16384);
-        bulk_copy(dst, rec_kq(j), 8192, &mb_kq[j & 1]);
-        bulk_copy(dst + 8192, rec_kq(j) + 16384, 8192, &mb_kq[j & 1]);
-      }
-    }
+    if (tid == 32) bulk_load(dst, rec_kq(j), kRecKQ, &mb_kq[j & 1]);
     ++q_kq[j & 1].issued;
   };
   auto load_a = [&](int j) {
@@ -557,12 +525,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   load_kq(0);
   if (nch > 1) load_kq(1);
   load_a(0);
-  if (!kXfer) {
-    load_p(0);
-    load_z(0);
-  }
+  load_p(0);
+  load_z(0);
 
-  // initial state(s): bf16 into the operand tile(s), and into TMEM in fp32
+  // initial state: bf16 into the operand tile, and into TMEM in fp32
   // already scaled by the first chunk's total decay (the state update adds to
   // e^{gamma_C} S0; each chunk's end scales for the next one)
   bool aborted = !__syncthreads_and(pwait(&mb_g, q_g));
@@ -570,28 +536,14 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     const float dC0 = sm.f32(M::GT)[C - 1];
     const int col0 = part * 32;
     float v[32];
-    if (!kXfer) {
-      load_state_row(S_init, init_tiled, row, col0, v);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-    }
+    load_state_row(S_init, init_tiled, row, col0, v);
 #pragma unroll
     for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::S, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] *= dC0;
     tc::tmem_st32(tmem + lane_base + TS_S + col0, v);
-    if (kXfer) {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = (col0 + i == row) ? 1.0f : 0.0f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::X, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= dC0;
-      tc::tmem_st32(tmem + lane_base + TS_X + col0, v);
-    }
   }
-  // the first chunk's records (and the state tiles for the tensor core)
+  // the first chunk's records (and the state tile for the tensor core)
   if (!aborted) {
     const bool ok = pwait(&mb_kq[0], q_kq[0]) && pwait(&mb_a, q_a);
     aborted = !sync_for_mma_and(ok);
@@ -605,7 +557,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     tc::fence_after_sync();
     return all_ok;
   };
-  // output pass: the gated RMSNorm epilogue of chunk jj from the O staging (its z
+  // the gated RMSNorm epilogue of chunk jj from the O staging (its z
   // has landed), a warp per 4 tokens and 4 channels per lane
   auto epilogue = [&](int jj) {
     const int t0e = sg.begin + C * jj, Le = min(C, seg_end - t0e);
@@ -648,16 +600,13 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     // the gates of the next chunk go where those of the chunk before this one were
     if (j + 1 < nch) load_g(j + 1);
 
-    // ---- batch 1: [O1 = S0 Q^T,] U = V^T (T diag beta)^T, Vn^T = U + S0 (-W)^T
-    //      [, transfer: Vn_X^T = X0 (-W)^T] ----
+    // ---- batch 1: O1 = S0 Q^T, U = V^T (T diag beta)^T, Vn^T = U + S0 (-W)^T ----
     if (tid == 0) {
-      if (!kXfer) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-          tc::mma_bf16(tmem + TS_O1, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
-                       tc::sdesc_at(D_K, kq + kb * 16384 + 8192 + ks), ID_KK, k > 0);
-        }
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+        tc::mma_bf16(tmem + TS_O1, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                     tc::sdesc_at(D_K, kq + kb * 16384 + 8192 + ks), ID_KK, k > 0);
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k)
@@ -669,38 +618,24 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         tc::mma_bf16(tmem + TU, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
                      tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
       }
-      if (kXfer) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-          tc::mma_bf16(tmem + TS_VX, tc::sdesc_at(D_K, sm.addr + M::X + kb * 16384 + ks),
-                       tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, k > 0);
-        }
-      }
       tc::mma_commit(&mb_mma);
     }
     // meanwhile: write out the previous chunk
-    if (!kXfer && j > 0) epilogue(j - 1);
+    if (j > 0) epilogue(j - 1);
     if (!wait_mma(true)) { aborted = true; break; }
     // batch 1 has finished with -W | V^ | T diag(beta); the epilogue with the
     // O staging and the previous z buffer
     if (j + 1 < nch) {
       load_a(j + 1);
-      if (!kXfer) load_z(j + 1);
+      load_z(j + 1);
     }
 
-    // ---- Vn^T tiles, row = d_v index: output pass plain and decay-weighted,
-    //      transfer pass X's and S's, both decay-weighted ----
+    // ---- Vn^T tiles, plain and decay-weighted, row = d_v index ----
     {
       float v[16], vs[16];
       tc::tmem_ld16(tmem + lane_base + TU + part * 16, v);
 #pragma unroll
       for (int i = 0; i < 16; ++i) vs[i] = v[i] * egc[part * 16 + i];
-      if (kXfer) {
-        tc::tmem_ld16(tmem + lane_base + TS_VX + part * 16, v);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] *= egc[part * 16 + i];
-      }
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const uint32_t off = tc::sw128_off(row, part * 16 + 8 * m, 0);
@@ -708,74 +643,57 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         store_bf16x8(sm.base + M::VNS, off, vs + 8 * m);
       }
     }
-    if (!sync_for_mma_and(kXfer || pwait(&mb_p, q_p))) { aborted = true; break; }
+    if (!sync_for_mma_and(pwait(&mb_p, q_p))) { aborted = true; break; }
 
-    // ---- batch 2: [O2 = Vn^T P^T,] S += Vn^T diag(e^{gC-g}) K^ [, X likewise] ----
+    // ---- batch 2: O2 = Vn^T P^T, S += Vn^T diag(e^{gC-g}) K^ ----
     if (tid == 0) {
-      if (!kXfer) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + TS_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
-                       tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16(tmem + TS_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
+                     tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
-                       tc::sdesc_at(D_MN_KQ, kq + k * 2048), ID_MN_B, 1u);
-      } else {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
-                       tc::sdesc_at(D_MN_V, kq + k * 2048), ID_MN_B, 1u);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + TS_X, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
-                       tc::sdesc_at(D_MN_V, kq + k * 2048), ID_MN_B, 1u);
-      }
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
+                     tc::sdesc_at(D_MN_KQ, kq + k * 2048), ID_MN_B, 1u);
       tc::mma_commit(&mb_mma);
     }
     if (!wait_mma(j + 1 >= nch || pwait(&mb_g, q_g))) { aborted = true; break; }
     // batch 2 has finished with P and this [K^ | Q^] buffer
-    if (!kXfer && j + 1 < nch) load_p(j + 1);
+    if (j + 1 < nch) load_p(j + 1);
     if (j + 2 < nch) load_kq(j + 2);
 
-    // ---- new state(s) -> bf16 operand tiles, and in TMEM scaled by the next
-    //      chunk's total decay; output pass: O = e^gamma O1 + O2 -> fp32 staging ----
+    // ---- new state -> bf16 operand tile, and in TMEM scaled by the next
+    //      chunk's total decay; O = e^gamma O1 + O2 -> fp32 staging ----
     {
       const float dC = j + 1 < nch ? sm.f32(M::GT + ((j + 1) & 1) * 512)[C - 1] : 1.0f;
+      float v[32];
+      const uint32_t ta = tmem + lane_base + TS_S + part * 32;
+      tc::tmem_ld32(ta, v);
 #pragma unroll
-      for (int zz = 0; zz < (kXfer ? 2 : 1); ++zz) {
-        float v[32];
-        const uint32_t ta = tmem + lane_base + (zz ? TS_X : TS_S) + part * 32;
-        tc::tmem_ld32(ta, v);
+      for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::S, tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
+      if (j + 1 < nch) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m)
-          store_bf16x8(sm.base + (zz ? M::X : M::S), tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
-        if (j + 1 < nch) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= dC;
-          tc::tmem_st32(ta, v);
-        }
+        for (int i = 0; i < 32; ++i) v[i] *= dC;
+        tc::tmem_st32(ta, v);
       }
-      if (!kXfer) {
-        float o1[16], o2[16];
-        tc::tmem_ld16(tmem + lane_base + TS_O1 + part * 16, o1);
-        tc::tmem_ld16(tmem + lane_base + TS_O2 + part * 16, o2);
+      float o1[16], o2[16];
+      tc::tmem_ld16(tmem + lane_base + TS_O1 + part * 16, o1);
+      tc::tmem_ld16(tmem + lane_base + TS_O2 + part * 16, o2);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int t = part * 16 + i;
-          Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
-        }
+      for (int i = 0; i < 16; ++i) {
+        const int t = part * 16 + i;
+        Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
       }
     }
     // the next chunk's records and this chunk's z
     {
       bool ok = true;
       if (j + 1 < nch) ok = pwait(&mb_kq[(j + 1) & 1], q_kq[(j + 1) & 1]) && pwait(&mb_a, q_a);
-      if (!kXfer) ok = pwait(&mb_z[j & 1], q_z[j & 1]) && ok;
+      ok = pwait(&mb_z[j & 1], q_z[j & 1]) && ok;
       if (!sync_for_mma_and(ok)) { aborted = true; break; }
     }
   }
-  if (!kXfer && !aborted) epilogue(nch - 1);
+  if (!aborted) epilogue(nch - 1);
 
   if (aborted) {
     if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
@@ -793,31 +711,11 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     drain(&mb_z[0], q_z[0]);
     drain(&mb_z[1], q_z[1]);
   } else {
-    // final state back to global memory (fp32); the transfer pass adds the map X
-    // as bf16 hi / lo tiles for the combine pass's tensor-core products
-    float* dst_base = kXfer ? xfer_ptr(p, sg.k0 + sg.sigma, h, 1) : S_final;
-    if (dst_base != nullptr) {
+    // final state back to the caller (the last segment of a sequence)
+    if (S_final != nullptr) {
       float v[32];
       tc::tmem_ld32(tmem + lane_base + TS_S + part * 32, v);
-      store_state_row(dst_base, kXfer, row, part * 32, v);
-    }
-    if (kXfer) {
-      uint8_t* xt = reinterpret_cast<uint8_t*>(xfer_ptr(p, sg.k0 + sg.sigma, h, 0));
-      float v[32], lo[32];
-      tc::tmem_ld32(tmem + lane_base + TS_X + part * 32, v);
-#pragma unroll
-      for (int i = 0; i < 32; i += 2) {   // X - bf16(X), exact in fp32
-        float r0, r1;
-        round_bf16x2(v[i], v[i + 1], r0, r1);
-        lo[i] = v[i] - r0;
-        lo[i + 1] = v[i + 1] - r1;
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const uint32_t off = tc::sw128_off(row, part * 32 + 8 * m, 16384);
-        store_bf16x8(xt, off, v + 8 * m);
-        store_bf16x8(xt + 32768, off, lo + 8 * m);
-      }
+      store_state_row(S_final, false, row, part * 32, v);
     }
   }
   tc::fence_before_sync();
@@ -1219,10 +1117,10 @@ cudaError_t launch_prefill_scan(const PrefillArgs& p, bool transfer, unsigned un
       return e;
     xfer_kernel<<<2 * units * (unsigned)p.h_v, kXferThreads, XferLay::BYTES, stream>>>(p);
   } else {
-    if ((e = cudaFuncSetAttribute(scan_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)ScanLay<false>::BYTES)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)ScanLay::BYTES)) != cudaSuccess)
       return e;
-    scan_kernel<false><<<units * (unsigned)p.h_v, kScanThreads, ScanLay<false>::BYTES, stream>>>(p, tm_z);
+    output_kernel<<<units * (unsigned)p.h_v, kScanThreads, ScanLay::BYTES, stream>>>(p, tm_z);
   }
   return cudaGetLastError();
 }
