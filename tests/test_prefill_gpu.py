@@ -189,6 +189,18 @@ def test_prefill_other_head_groupings(h_k, h_v):
     _check(sh, lengths, params, tok, st)
 
 
+@pytest.mark.parametrize("h_k,h_v", [(32, 32), (8, 32)])
+def test_prefill_segmented_other_head_groupings(h_k, h_v):
+    # a sequence longer than one segment with 1 and 4 value heads per key head:
+    # the prep pass's head groups, both transfer tracks and the combine at
+    # groupings other than 2
+    sh = gi.Shape(h_k=h_k, h_v=h_v)
+    lengths = [2100, 30]
+    params, tok, st = _inputs(sh, lengths, 16, slow=True, ssm_std=0.3, conv_std=1.0, norm_w="uniform")
+    e = _check(sh, lengths, params, tok, st)
+    print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
+
+
 def test_prefill_extreme_decay_stays_finite():
     # a = 30 gives g ~ -30 exp(A_log) per token: the cumulative decay of a
     # chunk is far below fp32's range, and every exponential must stay finite

@@ -22,26 +22,26 @@ pytestmark = pytest.mark.gpu
 SH = gi.LAYER
 
 
-def _inputs(lengths, seed):
+def _inputs(lengths, seed, sh=SH):
     T = sum(lengths)
-    params = gi.make_params(SH, seed, norm_w="uniform")
-    tok = gi.make_tokens(SH, T, seed)
-    gc = gi.gate_controlled(SH, T, seed)
+    params = gi.make_params(sh, seed, norm_w="uniform")
+    tok = gi.make_tokens(sh, T, seed)
+    gc = gi.gate_controlled(sh, T, seed)
     tok["a"], tok["b"] = gc["a"], gc["b"]
     params["A_log"], params["dt_bias"] = gc["A_log"], gc["dt_bias"]
-    st = gi.make_states(SH, len(lengths), seed, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    st = gi.make_states(sh, len(lengths), seed, ssm_std=0.1 ** 0.5, conv_std=1.0)
     return to_dev(params), to_dev(tok), st
 
 
-def _both(lengths, seed, bitwise=False):
-    dims = dims_of(SH)
-    p, x, st = _inputs(lengths, seed)
+def _both(lengths, seed, bitwise=False, sh=SH):
+    dims = dims_of(sh)
+    p, x, st = _inputs(lengths, seed, sh)
     N, T = len(lengths), sum(lengths)
     cu = gi.cu_seqlens(lengths).to(DEV)
     res = {}
     for which in ("workspace", "noalloc"):
         conv, ssm = st["conv_state"].clone().to(DEV), st["ssm_state"].clone().to(DEV)
-        out = torch.full((T, SH.h_v, SH.d_v), float("nan"), dtype=torch.bfloat16, device=DEV)
+        out = torch.full((T, sh.h_v, sh.d_v), float("nan"), dtype=torch.bfloat16, device=DEV)
         if which == "workspace":
             ws = torch.empty(gdn.gdn_workspace_bytes(dims, N, T), dtype=torch.uint8, device=DEV)
             gdn.gdn_prefill(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
@@ -76,3 +76,10 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row():
     e2 = _both([64, 129, 0, 33], seed=22, bitwise=True)
     print(f"call 1 rel diff out {e1[0]:.2e} state {e1[1]:.2e}; "
           f"call 2 out {e2[0]:.2e} state {e2[1]:.2e}")
+
+
+@pytest.mark.parametrize("h_k,h_v", [(32, 32), (8, 32)])
+def test_noalloc_matches_prefill_bitwise_at_other_head_groupings(h_k, h_v):
+    # 1 and 4 value heads per key head, no sequence longer than one segment:
+    # the two entry points do the same arithmetic
+    _both([300, 64, 5], seed=23, bitwise=True, sh=gi.Shape(h_k=h_k, h_v=h_v))
