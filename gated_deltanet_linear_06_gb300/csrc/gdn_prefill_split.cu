@@ -384,9 +384,19 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
 // ============================== output pass ==============================
 
-constexpr int kScanThreads = 512;   // 16 warps: 4 per TMEM lane quarter
-static_assert(kScanThreads / 32 * 4 == C, "the epilogue gives each warp 4 of a chunk's tokens");
-struct ScanLay {                         // output pass
+// The output pass, warp-specialised.  One CTA per (segment, value head): 16
+// worker warps (4 per TMEM lane quarter) make the operand tiles from the
+// accumulators, stage O and run the gated RMSNorm epilogue; one more warp
+// issues every bulk copy and every tensor-core product.  The two sides meet on
+// mbarriers, so the per-chunk chain is only
+//   [U, Vn^T] -> Vn^T tiles -> [state update] -> state tile -> next [U, Vn^T]
+// while O1 = S0 Q^T, O2 = Vn^T P^T, the O staging and the epilogue run beside
+// it (O1 double-buffered in TMEM).  Every wait is bounded; the workers agree on
+// a time-out at their own barriers.
+constexpr int kOutWorkers = 512;              // 16 warps
+constexpr int kOutThreads = kOutWorkers + 32; // + the issuing warp
+static_assert(kOutWorkers / 32 * 4 == C, "the epilogue gives each worker warp 4 of a chunk's tokens");
+struct ScanLay {
   static constexpr uint32_t S = 0;          // S bf16 [d_v][d_k], K blocks 16 KB apart
   static constexpr uint32_t KQ = 32768;     // two [K^ | Q^] buffers
   static constexpr uint32_t KQ_BUF = 32768;
@@ -394,8 +404,8 @@ struct ScanLay {                         // output pass
   static constexpr uint32_t VH = WN + kRecVH;
   static constexpr uint32_t TB = WN + kRecTB;
   static constexpr uint32_t P = WN + 40960;
-  static constexpr uint32_t GT = P + 8192;  // two gate buffers: e^gamma [64], e^{gamma_C - gamma} [64]
-  static constexpr uint32_t Z = GT + 1024;  // two z buffers, bf16 [64][128]
+  static constexpr uint32_t GT = P + 8192;  // three gate buffers: e^gamma [64], e^{gamma_C - gamma} [64]
+  static constexpr uint32_t Z = GT + 2048;  // two z buffers, bf16 [64][128]
   static constexpr uint32_t VN = Z + 32768;     // Vn^T [d_v][t]
   static constexpr uint32_t VNS = VN + 16384;   // Vn^T diag(e^{gamma_C - gamma})
   static constexpr uint32_t OST = VN;           // O fp32 [64][LDO], over VN and VNS once they are consumed
@@ -409,8 +419,8 @@ static_assert(ScanLay::WN % 1024 == 0 && ScanLay::VH % 1024 == 0 && ScanLay::TB 
 static_assert(ScanLay::Z % 128 == 0, "TMA destination alignment");
 static_assert(ScanLay::OST + 64 * LDO * 4 <= ScanLay::NW, "O staging overlaps the norm weight");
 static_assert(ScanLay::BYTES <= 227 * 1024, "shared memory");
-// TMEM columns
-constexpr uint32_t TS_S = 0, TS_O1 = 128, TS_U = 192, TS_O2 = 256, TS_COLS = 512;
+// TMEM columns: S, U / Vn^T, O1 (two buffers), O2
+constexpr uint32_t TS_S = 0, TS_U = 128, TS_O1 = 192, TS_O2 = 320, TS_COLS = 512;
 
 // Block-wide sync for the tensor core that also ANDs a per-thread verdict.
 __device__ __forceinline__ bool sync_for_mma_and(bool ok) {
@@ -421,20 +431,33 @@ __device__ __forceinline__ bool sync_for_mma_and(bool ok) {
   return all;
 }
 
-__global__ void __launch_bounds__(kScanThreads, 1)
+__device__ __forceinline__ void mbar_arrive(uint64_t* mbar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(mbar)) : "memory");
+}
+
+// A worker warp's signal: its generic smem writes and tensor-memory traffic are
+// ordered before the arrival (one per warp).
+__device__ __forceinline__ void warp_signal(uint64_t* mbar, int lane) {
+  tc::fence_proxy_async();
+  tc::fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(mbar);
+}
+
+__global__ void __launch_bounds__(kOutThreads, 1)
     output_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_z) {
   using M = ScanLay;
-  constexpr uint32_t TU = TS_U;   // U, then Vn^T
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t mb_mma;     // MMA completion
-  __shared__ __align__(8) uint64_t mb_kq[2];   // [K^ | Q^] buffers
-  __shared__ __align__(8) uint64_t mb_a;       // -W | V^ | T diag(beta)
-  __shared__ __align__(8) uint64_t mb_g;       // the gates (a chunk ahead)
-  __shared__ __align__(8) uint64_t mb_p;       // P (output pass)
-  __shared__ __align__(8) uint64_t mb_z[2];    // z buffers (output pass)
+  // copies landed
+  __shared__ __align__(8) uint64_t mb_kq[2], mb_a, mb_g[3], mb_p, mb_z[2];
+  // products done: [U, Vn^T]; [state update] (and O1 before it); [O2] (and all before)
+  __shared__ __align__(8) uint64_t mb_b1, mb_b2, mb_o;
+  // worker warps done (16 arrivals): Vn^T tiles, state tile, O read, epilogue
+  __shared__ __align__(8) uint64_t mb_vn, mb_s, mb_or, mb_ep;
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool issuer = warp == kOutWorkers / 32;
   const int u = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
   if (u >= p.seg_list[0]) return;
   const Seg sg = load_seg(p.seg_list, u);
@@ -444,10 +467,10 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   const int seg_end = sg.begin + sg.len;
   const int nch = (sg.len + C - 1) / C;
 
-  // where the state comes from and goes to
-  // (the caller's state is row-major, the workspace slots tiled)
-  const float* S_init = nullptr;
-  float* S_final = nullptr;
+  // where the state comes from and goes to (the caller's state is row-major,
+  // the workspace slots tiled)
+  const float* S_init;
+  float* S_final;
   float* ssm = p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD;
   const bool init_tiled = sg.nsig > 1;
   if (sg.nsig == 1) {
@@ -462,14 +485,20 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   float* Ost = sm.f32(M::OST);
   float* nw = sm.f32(M::NW);
   if (tid == 0) {
-    tc::mbar_init(&mb_mma, 1);
-    tc::mbar_init(&mb_kq[0], 1);
-    tc::mbar_init(&mb_kq[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&mb_kq[i], 1);
+      tc::mbar_init(&mb_z[i], 1);
+    }
+    for (int i = 0; i < 3; ++i) tc::mbar_init(&mb_g[i], 1);
     tc::mbar_init(&mb_a, 1);
-    tc::mbar_init(&mb_g, 1);
     tc::mbar_init(&mb_p, 1);
-    tc::mbar_init(&mb_z[0], 1);
-    tc::mbar_init(&mb_z[1], 1);
+    tc::mbar_init(&mb_b1, 1);
+    tc::mbar_init(&mb_b2, 1);
+    tc::mbar_init(&mb_o, 1);
+    tc::mbar_init(&mb_vn, kOutWorkers / 32);
+    tc::mbar_init(&mb_s, kOutWorkers / 32);
+    tc::mbar_init(&mb_or, kOutWorkers / 32);
+    tc::mbar_init(&mb_ep, kOutWorkers / 32);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base_s, TS_COLS);
@@ -478,241 +507,237 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
-  const int part = warp >> 2;               // which quarter of a lane quarter's columns
+  auto wt = [&](uint64_t* mb, uint32_t k) -> bool {   // the k-th completion of mb (parity k & 1)
+    return tc::mbar_wait(mb, k & 1u, kWaitBudget);
+  };
+  bool ok = true;
 
-  auto rec_kq = [&](int j) { return p.rec_kq + ((size_t)(sg.c0 + j) * p.h_k + kh) * kRecKQ; };
-  auto rec_v = [&](int j) { return p.rec_v + ((size_t)(sg.c0 + j) * p.h_v + h) * kRecV; };
-  // Record loads, issued by one thread (tid 32) under conditions every thread
-  // evaluates alike, so every thread keeps the same counts.  The k-th copy on a
-  // barrier completes its phase of parity k & 1; each barrier has at most one
-  // copy in flight.
-  struct Pipe {
-    uint32_t issued, waited;
-  };
-  Pipe q_kq[2] = {{0, 0}, {0, 0}}, q_a = {0, 0}, q_g = {0, 0}, q_p = {0, 0}, q_z[2] = {{0, 0}, {0, 0}};
-  auto pwait = [&](uint64_t* mb, Pipe& q) -> bool {
-    const bool r = tc::mbar_wait(mb, q.waited & 1u, kWaitBudget);
-    if (r) ++q.waited;
-    return r;
-  };
-  auto load_kq = [&](int j) {
-    uint8_t* dst = sm.base + M::KQ + (j & 1) * M::KQ_BUF;
-    if (tid == 32) bulk_load(dst, rec_kq(j), kRecKQ, &mb_kq[j & 1]);
-    ++q_kq[j & 1].issued;
-  };
-  auto load_a = [&](int j) {
-    if (tid == 32) bulk_load(sm.base + M::WN, rec_v(j), kRecP, &mb_a);
-    ++q_a.issued;
-  };
-  auto load_g = [&](int j) {
-    if (tid == 32) bulk_load(sm.base + M::GT + (j & 1) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g);
-    ++q_g.issued;
-  };
-  auto load_p = [&](int j) {
-    if (tid == 32) bulk_load(sm.base + M::P, rec_v(j) + kRecP, 8192, &mb_p);
-    ++q_p.issued;
-  };
-  auto load_z = [&](int j) {
-    if (tid == 32) {
-      mbar_expect_tx(&mb_z[j & 1], C * kD * 2);
-      tma_load_2d(sm.base + M::Z + (j & 1) * 16384, &tm_z, h * kD, start + sg.begin + C * j, &mb_z[j & 1]);
-    }
-    ++q_z[j & 1].issued;
-  };
-  load_g(0);
-  load_kq(0);
-  if (nch > 1) load_kq(1);
-  load_a(0);
-  load_p(0);
-  load_z(0);
+  if (issuer) {
+    // ================= the issuing warp (one lane) =================
+    if (lane == 0) {
+      auto rec_kq = [&](int j) { return p.rec_kq + ((size_t)(sg.c0 + j) * p.h_k + kh) * kRecKQ; };
+      auto rec_v = [&](int j) { return p.rec_v + ((size_t)(sg.c0 + j) * p.h_v + h) * kRecV; };
+      uint32_t i_kq[2] = {0, 0}, i_a = 0, i_g[3] = {0, 0, 0}, i_p = 0, i_z[2] = {0, 0};   // copies issued
+      auto load_kq = [&](int j) {
+        bulk_load(sm.base + M::KQ + (j & 1) * M::KQ_BUF, rec_kq(j), kRecKQ, &mb_kq[j & 1]);
+        ++i_kq[j & 1];
+      };
+      auto load_a = [&](int j) {
+        bulk_load(sm.base + M::WN, rec_v(j), kRecP, &mb_a);
+        ++i_a;
+      };
+      auto load_g = [&](int j) {
+        bulk_load(sm.base + M::GT + (j % 3) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g[j % 3]);
+        ++i_g[j % 3];
+      };
+      auto load_p = [&](int j) {
+        bulk_load(sm.base + M::P, rec_v(j) + kRecP, 8192, &mb_p);
+        ++i_p;
+      };
+      auto load_z = [&](int j) {
+        mbar_expect_tx(&mb_z[j & 1], C * kD * 2);
+        tma_load_2d(sm.base + M::Z + (j & 1) * 16384, &tm_z, h * kD, start + sg.begin + C * j, &mb_z[j & 1]);
+        ++i_z[j & 1];
+      };
+      load_g(0);
+      if (nch > 1) load_g(1);
+      load_kq(0);
+      if (nch > 1) load_kq(1);
+      load_a(0);
+      load_p(0);
+      load_z(0);
+      if (nch > 1) load_z(1);
 
-  // initial state: bf16 into the operand tile, and into TMEM in fp32
-  // already scaled by the first chunk's total decay (the state update adds to
-  // e^{gamma_C} S0; each chunk's end scales for the next one)
-  bool aborted = !__syncthreads_and(pwait(&mb_g, q_g));
-  {
-    const float dC0 = sm.f32(M::GT)[C - 1];
-    const int col0 = part * 32;
-    float v[32];
-    load_state_row(S_init, init_tiled, row, col0, v);
+      for (int j = 0; j < nch; ++j) {
+        const uint32_t kq = sm.addr + M::KQ + (j & 1) * M::KQ_BUF;
+        // this chunk's records and the workers' state tile
+        if (!(wt(&mb_kq[j & 1], j >> 1) && wt(&mb_a, j) && wt(&mb_s, j))) { ok = false; break; }
+        tc::fence_after_sync();
+        // [U = V^T (T diag beta)^T, Vn^T = U + S0 (-W)^T]
 #pragma unroll
-    for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::S, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_U, tc::sdesc_at(D_MN_V, sm.addr + M::VH + k * 2048),
+                       tc::sdesc_at(D_K, sm.addr + M::TB + k * 32), ID_MN_A, k > 0);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= dC0;
-    tc::tmem_st32(tmem + lane_base + TS_S + col0, v);
-  }
-  // the first chunk's records (and the state tile for the tensor core)
-  if (!aborted) {
-    const bool ok = pwait(&mb_kq[0], q_kq[0]) && pwait(&mb_a, q_a);
-    aborted = !sync_for_mma_and(ok);
-  }
-
-  uint32_t phase = 0;
-  auto wait_mma = [&](bool more) -> bool {   // ANDs in `more`, the thread's other waits
-    const bool ok = tc::mbar_wait(&mb_mma, phase, kWaitBudget) && more;
-    phase ^= 1u;
-    const bool all_ok = __syncthreads_and(ok);
-    tc::fence_after_sync();
-    return all_ok;
-  };
-  // the gated RMSNorm epilogue of chunk jj from the O staging (its z
-  // has landed), a warp per 4 tokens and 4 channels per lane
-  auto epilogue = [&](int jj) {
-    const int t0e = sg.begin + C * jj, Le = min(C, seg_end - t0e);
-    const uint8_t* zb = sm.base + M::Z + (jj & 1) * 16384;
-    const int tq = 4 * warp;
-    float o[4][4], ss[4];
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TS_U, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                       tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
+        }
+        tc::mma_commit(&mb_b1);
+        // O1 = S0 Q^T into its buffer, which the workers read at chunk j - 2: the
+        // wait for that read was the O2 wait of chunk j - 1 (waiting for it again
+        // here could see the barrier two phases on, where its parity repeats)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 o4 = reinterpret_cast<const float4*>(Ost + (tq + i) * LDO)[lane];
-      o[i][0] = o4.x; o[i][1] = o4.y; o[i][2] = o4.z; o[i][3] = o4.w;
-      ss[i] = o4.x * o4.x;
-      ss[i] = fmaf(o4.y, o4.y, ss[i]);
-      ss[i] = fmaf(o4.z, o4.z, ss[i]);
-      ss[i] = fmaf(o4.w, o4.w, ss[i]);
-    }
-    const float r = rsqrtf(warp_sum4(ss, lane) * (1.0f / kD) + p.rms_eps);
-    const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TS_O1 + 64 * (j & 1), tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                       tc::sdesc_at(D_K, kq + kb * 16384 + 8192 + ks), ID_KK, k > 0);
+        }
+        // [U, Vn^T] has finished with -W | V^ | T diag(beta)
+        if (!wt(&mb_b1, j)) { ok = false; break; }
+        if (j + 1 < nch) load_a(j + 1);
+        // the workers' Vn^T tiles, and P
+        if (!(wt(&mb_vn, j) && wt(&mb_p, j))) { ok = false; break; }
+        tc::fence_after_sync();
+        // the workers ran the epilogue of chunk j - 1 before these tiles: its z buffer refills
+        if (j >= 1 && j + 1 < nch) {
+          if (!wt(&mb_ep, j - 1)) { ok = false; break; }
+          load_z(j + 1);
+        }
+        // [S += Vn^T diag(e^{gamma_C - gamma}) K^]
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float rstd = __shfl_sync(0xffffffffu, r, token_lane(i));
-      const uint2 zr = *reinterpret_cast<const uint2*>(zb + (tq + i) * 256 + lane * 8);
-      float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
-                    bf16_to_f32(zr.y >> 16)};
-      silu4(g);
-      uint2 ov;
-      ov.x = pack_bf16x2(o[i][0] * rstd * w4.x * g[0], o[i][1] * rstd * w4.y * g[1]);
-      ov.y = pack_bf16x2(o[i][2] * rstd * w4.z * g[2], o[i][3] * rstd * w4.w * g[3]);
-      if (tq + i < Le)
-        *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0e + tq + i) * p.h_v + h) * kD + 4 * lane) = ov;
-    }
-  };
-
-  // Four CTA barriers per chunk; every copy is waited for at the barrier before
-  // the phase that needs it, issued at the barrier after the phase that frees its
-  // buffer.
-  for (int j = 0; j < nch && !aborted; ++j) {
-    const float* eg = sm.f32(M::GT + (j & 1) * 512);
-    const float* egc = eg + 64;
-    const uint32_t kq = sm.addr + M::KQ + (j & 1) * M::KQ_BUF;
-    // the gates of the next chunk go where those of the chunk before this one were
-    if (j + 1 < nch) load_g(j + 1);
-
-    // ---- batch 1: O1 = S0 Q^T, U = V^T (T diag beta)^T, Vn^T = U + S0 (-W)^T ----
-    if (tid == 0) {
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
+                       tc::sdesc_at(D_MN_KQ, kq + k * 2048), ID_MN_B, 1u);
+        tc::mma_commit(&mb_b2);
+        // O2 = Vn^T P^T, once the workers have read O2 of chunk j - 1 (the gates of
+        // chunk j + 2 then go where those of chunk j - 1 were)
+        if (j >= 1 && !wt(&mb_or, j - 1)) { ok = false; break; }
+        tc::fence_after_sync();
+        if (j + 2 < nch) load_g(j + 2);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-        tc::mma_bf16(tmem + TS_O1, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
-                     tc::sdesc_at(D_K, kq + kb * 16384 + 8192 + ks), ID_KK, k > 0);
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
+                       tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
+        tc::mma_commit(&mb_o);
+        // the state update and O2 have finished with P and this [K^ | Q^] buffer
+        if (!wt(&mb_o, j)) { ok = false; break; }
+        if (j + 1 < nch) load_p(j + 1);
+        if (j + 2 < nch) load_kq(j + 2);
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_bf16(tmem + TU, tc::sdesc_at(D_MN_V, sm.addr + M::VH + k * 2048),
-                     tc::sdesc_at(D_K, sm.addr + M::TB + k * 32), ID_MN_A, k > 0);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-        tc::mma_bf16(tmem + TU, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
-                     tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
+      if (!ok) {
+        record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+        // the copies this CTA started land (bounded) before its shared memory goes away
+        auto drain = [&](uint64_t* mb, uint32_t issued) {
+          if (issued > 0) wt(mb, issued - 1);
+        };
+        drain(&mb_kq[0], i_kq[0]);
+        drain(&mb_kq[1], i_kq[1]);
+        drain(&mb_a, i_a);
+        for (int i = 0; i < 3; ++i) drain(&mb_g[i], i_g[i]);
+        drain(&mb_p, i_p);
+        drain(&mb_z[0], i_z[0]);
+        drain(&mb_z[1], i_z[1]);
       }
-      tc::mma_commit(&mb_mma);
     }
-    // meanwhile: write out the previous chunk
-    if (j > 0) epilogue(j - 1);
-    if (!wait_mma(true)) { aborted = true; break; }
-    // batch 1 has finished with -W | V^ | T diag(beta); the epilogue with the
-    // O staging and the previous z buffer
-    if (j + 1 < nch) {
-      load_a(j + 1);
-      load_z(j + 1);
-    }
-
-    // ---- Vn^T tiles, plain and decay-weighted, row = d_v index ----
+    __syncwarp();
+  } else {
+    // ================= the worker warps =================
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
+    const int part = warp >> 2;               // which quarter of a lane quarter's columns
+    // the initial state: bf16 into the operand tile, and into TMEM in fp32 already
+    // scaled by the first chunk's total decay (the state update adds to e^{gamma_C} S0;
+    // each chunk's end scales for the next one)
+    ok = wt(&mb_g[0], 0);
     {
-      float v[16], vs[16];
-      tc::tmem_ld16(tmem + lane_base + TU + part * 16, v);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) vs[i] = v[i] * egc[part * 16 + i];
-#pragma unroll
-      for (int m = 0; m < 2; ++m) {
-        const uint32_t off = tc::sw128_off(row, part * 16 + 8 * m, 0);
-        store_bf16x8(sm.base + M::VN, off, v + 8 * m);
-        store_bf16x8(sm.base + M::VNS, off, vs + 8 * m);
-      }
-    }
-    if (!sync_for_mma_and(pwait(&mb_p, q_p))) { aborted = true; break; }
-
-    // ---- batch 2: O2 = Vn^T P^T, S += Vn^T diag(e^{gC-g}) K^ ----
-    if (tid == 0) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_bf16(tmem + TS_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
-                     tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
-                     tc::sdesc_at(D_MN_KQ, kq + k * 2048), ID_MN_B, 1u);
-      tc::mma_commit(&mb_mma);
-    }
-    if (!wait_mma(j + 1 >= nch || pwait(&mb_g, q_g))) { aborted = true; break; }
-    // batch 2 has finished with P and this [K^ | Q^] buffer
-    if (j + 1 < nch) load_p(j + 1);
-    if (j + 2 < nch) load_kq(j + 2);
-
-    // ---- new state -> bf16 operand tile, and in TMEM scaled by the next
-    //      chunk's total decay; O = e^gamma O1 + O2 -> fp32 staging ----
-    {
-      const float dC = j + 1 < nch ? sm.f32(M::GT + ((j + 1) & 1) * 512)[C - 1] : 1.0f;
+      const float dC0 = sm.f32(M::GT)[C - 1];
+      const int col0 = part * 32;
       float v[32];
-      const uint32_t ta = tmem + lane_base + TS_S + part * 32;
-      tc::tmem_ld32(ta, v);
+      load_state_row(S_init, init_tiled, row, col0, v);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::S, tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
+      for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + M::S, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] *= dC0;
+      tc::tmem_st32(tmem + lane_base + TS_S + col0, v);
+    }
+    warp_signal(&mb_s, lane);
+
+    for (int j = 0; j < nch; ++j) {
+      const float* eg = sm.f32(M::GT + (j % 3) * 512);
+      const float* egc = eg + 64;
+      // ---- Vn^T tiles, plain and decay-weighted, row = d_v index ----
+      ok = wt(&mb_b1, j) && wt(&mb_g[j % 3], j / 3) && ok;
+      tc::fence_after_sync();
+      {
+        float v[16], vs[16];
+        tc::tmem_ld16(tmem + lane_base + TS_U + part * 16, v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) vs[i] = v[i] * egc[part * 16 + i];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint32_t off = tc::sw128_off(row, part * 16 + 8 * m, 0);
+          store_bf16x8(sm.base + M::VN, off, v + 8 * m);
+          store_bf16x8(sm.base + M::VNS, off, vs + 8 * m);
+        }
+      }
+      warp_signal(&mb_vn, lane);
+      // ---- the new state -> bf16 operand tile, and in TMEM scaled by the next
+      //      chunk's total decay ----
+      ok = wt(&mb_b2, j) && ok;
+      tc::fence_after_sync();
       if (j + 1 < nch) {
+        ok = wt(&mb_g[(j + 1) % 3], (j + 1) / 3) && ok;
+        const float dC = sm.f32(M::GT + ((j + 1) % 3) * 512)[C - 1];
+        float v[32];
+        const uint32_t ta = tmem + lane_base + TS_S + part * 32;
+        tc::tmem_ld32(ta, v);
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+          store_bf16x8(sm.base + M::S, tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] *= dC;
         tc::tmem_st32(ta, v);
+        warp_signal(&mb_s, lane);
       }
-      float o1[16], o2[16];
-      tc::tmem_ld16(tmem + lane_base + TS_O1 + part * 16, o1);
-      tc::tmem_ld16(tmem + lane_base + TS_O2 + part * 16, o2);
+      // ---- O = e^gamma O1 + O2 -> fp32 staging (over the Vn^T tiles, consumed) ----
+      ok = wt(&mb_o, j) && ok;
+      tc::fence_after_sync();
+      {
+        float o1[16], o2[16];
+        tc::tmem_ld16(tmem + lane_base + TS_O1 + 64 * (j & 1) + part * 16, o1);
+        tc::tmem_ld16(tmem + lane_base + TS_O2 + part * 16, o2);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int t = part * 16 + i;
-        Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
+        for (int i = 0; i < 16; ++i) {
+          const int t = part * 16 + i;
+          Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
+        }
       }
-    }
-    // the next chunk's records and this chunk's z
-    {
-      bool ok = true;
-      if (j + 1 < nch) ok = pwait(&mb_kq[(j + 1) & 1], q_kq[(j + 1) & 1]) && pwait(&mb_a, q_a);
-      ok = pwait(&mb_z[j & 1], q_z[j & 1]) && ok;
-      if (!sync_for_mma_and(ok)) { aborted = true; break; }
-    }
-  }
-  if (!aborted) epilogue(nch - 1);
-
-  if (aborted) {
-    if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
-    // let this CTA's own copies finish (bounded) before its shared memory goes
-    // away (a copy that already landed passes its wait at once)
-    auto drain = [&](uint64_t* mb, Pipe& q) {
-      while (q.waited < q.issued && pwait(mb, q)) {
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mb_or);
+      if (!group_sync_and<kOutWorkers>(1, ok)) { ok = false; break; }   // the O staging is complete
+      // ---- the gated RMSNorm epilogue, a warp per 4 tokens and 4 channels per lane ----
+      ok = wt(&mb_z[j & 1], j >> 1) && ok;
+      {
+        const int t0e = sg.begin + C * j, Le = min(C, seg_end - t0e);
+        const uint8_t* zb = sm.base + M::Z + (j & 1) * 16384;
+        const int tq = 4 * warp;
+        float o[4][4], ss[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float4 o4 = reinterpret_cast<const float4*>(Ost + (tq + i) * LDO)[lane];
+          o[i][0] = o4.x; o[i][1] = o4.y; o[i][2] = o4.z; o[i][3] = o4.w;
+          ss[i] = o4.x * o4.x;
+          ss[i] = fmaf(o4.y, o4.y, ss[i]);
+          ss[i] = fmaf(o4.z, o4.z, ss[i]);
+          ss[i] = fmaf(o4.w, o4.w, ss[i]);
+        }
+        const float r = rsqrtf(warp_sum4(ss, lane) * (1.0f / kD) + p.rms_eps);
+        const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float rstd = __shfl_sync(0xffffffffu, r, token_lane(i));
+          const uint2 zr = *reinterpret_cast<const uint2*>(zb + (tq + i) * 256 + lane * 8);
+          float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
+                        bf16_to_f32(zr.y >> 16)};
+          silu4(g);
+          uint2 ov;
+          ov.x = pack_bf16x2(o[i][0] * rstd * w4.x * g[0], o[i][1] * rstd * w4.y * g[1]);
+          ov.y = pack_bf16x2(o[i][2] * rstd * w4.z * g[2], o[i][3] * rstd * w4.w * g[3]);
+          if (tq + i < Le)
+            *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0e + tq + i) * p.h_v + h) * kD + 4 * lane) = ov;
+        }
       }
-    };
-    drain(&mb_kq[0], q_kq[0]);
-    drain(&mb_kq[1], q_kq[1]);
-    drain(&mb_a, q_a);
-    drain(&mb_g, q_g);
-    drain(&mb_p, q_p);
-    drain(&mb_z[0], q_z[0]);
-    drain(&mb_z[1], q_z[1]);
-  } else {
-    // final state back to the caller (the last segment of a sequence)
-    if (S_final != nullptr) {
+      if (!group_sync_and<kOutWorkers>(1, ok)) { ok = false; break; }   // the O staging and z are read
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mb_ep);
+    }
+    if (!ok) {
+      if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+    } else if (S_final != nullptr) {
+      // final state back to the caller (the last segment of a sequence)
       float v[32];
       tc::tmem_ld32(tmem + lane_base + TS_S + part * 32, v);
       store_state_row(S_final, false, row, part * 32, v);
@@ -1120,7 +1145,7 @@ cudaError_t launch_prefill_scan(const PrefillArgs& p, bool transfer, unsigned un
     if ((e = cudaFuncSetAttribute(output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)ScanLay::BYTES)) != cudaSuccess)
       return e;
-    output_kernel<<<units * (unsigned)p.h_v, kScanThreads, ScanLay::BYTES, stream>>>(p, tm_z);
+    output_kernel<<<units * (unsigned)p.h_v, kOutThreads, ScanLay::BYTES, stream>>>(p, tm_z);
   }
   return cudaGetLastError();
 }
