@@ -71,9 +71,9 @@ struct Lay {
   static constexpr uint32_t TB = 131072;   // T diag(beta) [t][s]
   static constexpr uint32_t TW = 139264;   // T diag(beta e^gamma) [t][s]
   static constexpr uint32_t P = 147456;    // P [t][s]
-  static constexpr uint32_t F32 = 155648;  // fp32: A [64][65] + T [64][65]
+  static constexpr uint32_t F32 = 155648;  // fp32: the solve's A and T, 16 KB each
 };
-constexpr uint32_t F32_BYTES = 2 * 64 * LDA * 4;
+constexpr uint32_t F32_BYTES = 2 * UT_BYTES;
 // Staging of a chunk's raw inputs, loaded by TMA (2-D tensor maps over qkv and z):
 // the raw q, k and v rows of tokens t0-3 .. t0+63 (bf16, one [67][128] box per
 // block) land over -W, T, P and the fp32 area, which are dead from the last MMA of
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* eg = gam + 128;
   float* egc = gam + 192;
   float* Af = sm.f32(M::F32);
-  float* Tf = Af + 64 * LDA;
+  float* Tf = Af + UT_BYTES / 4;
   float* Ost = sm.f32(M::OST);      // aliases the Vn tiles (used after them)
 
   if (tid == 0) {
@@ -348,8 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!wait_mma()) { aborted = true; break; }
 
-    // ---- A (fp32, lanes 0-63) and P (bf16 tile, lanes 64-127) from the Gram rows;
-    //      warps w and w+4 share a lane quarter and split its 64 columns ----
+    // ---- A (fp32, lanes 0-63, below its diagonal: the solve reads nothing
+    //      else) and P (bf16 tile, lanes 64-127) from the Gram rows; warps w and
+    //      w+4 share a lane quarter and split its 64 columns ----
     {
       float v[16];
       const int t = row & 63;
@@ -359,9 +360,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if ((warp & 3) < 2) {
         const float bt = bet[t];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int s = c0 + i;
-          Af[t * LDA + s] = s < t ? bt * __expf(gt - gam[s]) * v[i] : 0.0f;
+        for (int m = 0; m < 4; ++m) {
+          float a[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a[e] = bt * __expf(gt - gam[c0 + 4 * m + e]) * v[4 * m + e];
+          ut_st4(Af, t, c0 + 4 * m, a[0], a[1], a[2], a[3]);
         }
       } else {
 #pragma unroll
@@ -377,15 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // ---- T = (I + A)^{-1} ----
-    solve_unit_lower<kThreads>(Af, Tf, sm.f32(M::WN), tid, 0);   // scratch over -W (written later)
+    solve_unit_lower<kThreads>(Af, Tf, tid, 0);
     // T diag(beta) and T diag(beta e^gamma) as bf16 tiles [t][s]
     for (int e = tid; e < 64 * 8; e += kThreads) {
       const int t = e >> 3, c8 = (e & 7) * 8;
       float xb[8], xw[8];
+      const float4 lo = ut_ld4(Tf, t, c8), hi = ut_ld4(Tf, t, c8 + 4);
+      const float tv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float tv = Tf[t * LDA + c8 + q];
-        xb[q] = tv * bet[c8 + q];
+        xb[q] = (c8 + q <= t ? tv[q] : 0.0f) * bet[c8 + q];   // T is zero above its diagonal
         xw[q] = xb[q] * eg[c8 + q];
       }
       store_bf16x8(sm.base + M::TB, tc::sw128_off(t, c8, 0), xb);

@@ -12,7 +12,7 @@ namespace gdn {
 
 constexpr int C = kChunk;
 constexpr int kSegTokens = 1024;   // segment length when long sequences are split
-constexpr int LDA = 65, LDO = 128;   // fp32 row strides: A and T [64][LDA], O staging [64][LDO]
+constexpr int LDO = 128;   // fp32 row stride of the O staging [64][LDO]
 
 // ---- tcgen05 operand and instruction descriptors ----
 constexpr uint64_t D_K = tc::sdesc_sw128(16, 1024);         // K-major tiles
@@ -84,22 +84,22 @@ __device__ __forceinline__ void store_bf16x8(uint8_t* tile, uint32_t off, const 
   *reinterpret_cast<uint4*>(tile + off) = v;
 }
 
-// Four SiLUs with one reciprocal: with d_i = 1 + e^{-x_i}, 1/d_1 =
-// d_2 d_3 d_4 / (d_1 d_2 d_3 d_4), and so on.  Inputs are clamped at -20 so the
-// product stays below 2^126 (|silu(x)| < 4.2e-8 for x < -20, which the clamp
-// replaces by silu(-20)); this takes the special-function unit from two
-// operations per SiLU to 1.25.
+// SiLU of four values through the hyperbolic tangent: with h = x / 2,
+// sigma(x) = (1 + tanh h) / 2, so x sigma(x) = h + h tanh(h) -- one
+// special-function operation (tanh.approx, relative error about 2^-11) and two
+// more per value.  The error it adds, at most |h| 2^-11, stays below the bf16
+// rounding of the result wherever the result is not much smaller than x.
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void silu4(float (&x)[4]) {
-  float d[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = 1.0f + __expf(-fmaxf(x[i], -20.0f));
-  const float d01 = d[0] * d[1], d23 = d[2] * d[3];
-  const float r = __fdividef(1.0f, d01 * d23);   // approximate reciprocal (product < 2^126)
-  const float r01 = r * d23, r23 = r * d01;   // 1/(d0 d1), 1/(d2 d3)
-  x[0] *= r01 * d[1];
-  x[1] *= r01 * d[0];
-  x[2] *= r23 * d[3];
-  x[3] *= r23 * d[2];
+  for (int i = 0; i < 4; ++i) {
+    const float h = 0.5f * x[i];
+    x[i] = fmaf(h, tanh_approx(h), h);
+  }
 }
 
 // Conv + SiLU of the 4 tokens tq .. tq+3 of a chunk starting at position t0
@@ -310,90 +310,124 @@ __device__ __forceinline__ bool group_sync_and(int bar_id, bool ok) {
   return r != 0;
 }
 
-// One block diagonal d = i - j of T (blocks (j + d, j), j = 0 .. 3 - d), over
-// NT threads, each with up to ceil(256 (4 - d) / NT) outputs in flight:
-//   M_ij = sum_{k=j}^{i-1} A_ik T_kj   (into the scratch Mf),
-//   T_ij = -T_ii M_ij.
-template <int NT, int D>
-__device__ __forceinline__ void solve_block_diagonal(const float* Af, float* Tf, float* Mf, int tid, int bar_id) {
-  constexpr int kOuts = 256 * (4 - D), kPer = (kOuts + NT - 1) / NT;
-  float m[kPer];
+// ---- the UT solve's fp32 64 x 64 matrices (A, T) ----
+// Row-major, 64 floats a row, with the 16-byte column groups of row t
+// permuted by XOR with t mod 8: a warp reading or writing one column group of
+// 8 consecutive rows, or 8 column groups of one row, touches 32 distinct banks.
+constexpr uint32_t UT_BYTES = 64 * 64 * 4;
+__device__ __forceinline__ int ut_idx(int t, int s) { return t * 64 + ((((s >> 2) ^ (t & 7)) << 2) | (s & 3)); }
+// columns s4 .. s4+3 of row t (s4 a multiple of 4)
+__device__ __forceinline__ float4 ut_ld4(const float* M, int t, int s4) {
+  return *reinterpret_cast<const float4*>(M + ut_idx(t, s4));
+}
+__device__ __forceinline__ void ut_st4(float* M, int t, int s4, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(M + ut_idx(t, s4)) = make_float4(a, b, c, d);
+}
+
+// acc[r][e] += sum_{k < nk} X[xr[r]][xc + k] Y[yr + k][yc + e] for two rows
+// (R = 2) or one, the sum in increasing k; nk a multiple of 4.
+template <int R>
+__device__ __forceinline__ void ut_rowquad(const float* X, const int (&xr)[R], int xc, const float* Y, int yr,
+                                           int yc, int nk, float (&acc)[R][4]) {
+#pragma unroll 2
+  for (int k = 0; k < nk; k += 4) {
+    float xk[R][4];
 #pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int o = tid + u * NT;
-    m[u] = 0.0f;
-    if (kPer * NT == kOuts || o < kOuts) {
-      const int j = o >> 8, i = j + D, r = (o >> 4) & 15, c = o & 15;
+    for (int r = 0; r < R; ++r) {
+      const float4 x4 = ut_ld4(X, xr[r], xc + k);
+      xk[r][0] = x4.x; xk[r][1] = x4.y; xk[r][2] = x4.z; xk[r][3] = x4.w;
+    }
 #pragma unroll
-      for (int k2 = 0; k2 < D; ++k2) {
-        const int kb = j + k2;
+    for (int kk = 0; kk < 4; ++kk) {
+      const float4 y4 = ut_ld4(Y, yr + k + kk, yc);
 #pragma unroll
-        for (int s = 0; s < 16; ++s)
-          m[u] = fmaf(Af[(16 * i + r) * LDA + 16 * kb + s], Tf[(16 * kb + s) * LDA + 16 * j + c], m[u]);
+      for (int r = 0; r < R; ++r) {
+        acc[r][0] = fmaf(xk[r][kk], y4.x, acc[r][0]);
+        acc[r][1] = fmaf(xk[r][kk], y4.y, acc[r][1]);
+        acc[r][2] = fmaf(xk[r][kk], y4.z, acc[r][2]);
+        acc[r][3] = fmaf(xk[r][kk], y4.w, acc[r][3]);
       }
     }
   }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u)
-    if (kPer * NT == kOuts || tid + u * NT < kOuts) Mf[tid + u * NT] = m[u];
-  group_sync<NT>(bar_id);
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int o = tid + u * NT;
-    if (kPer * NT == kOuts || o < kOuts) {
-      const int j = o >> 8, i = j + D, r = (o >> 4) & 15, c = o & 15;
-      float acc = 0.0f;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) acc = fmaf(Tf[(16 * i + r) * LDA + 16 * i + q], Mf[(j << 8) + (q << 4) + c], acc);
-      m[u] = -acc;
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int o = tid + u * NT;
-    if (kPer * NT == kOuts || o < kOuts) {
-      const int j = o >> 8, i = j + D, r = (o >> 4) & 15, c = o & 15;
-      Tf[(16 * i + r) * LDA + 16 * j + c] = m[u];
-    }
-  }
-  group_sync<NT>(bar_id);
 }
 
-// T = (I + A)^{-1} for a strictly lower 64 x 64 matrix A (fp32, row stride
-// LDA): the 16 x 16 diagonal blocks by forward substitution, a column per
-// thread, then the blocks below them one block diagonal at a time, each
-// product spread over the NT threads of a group (Mf: 3 x 16 x 16 fp32
-// scratch; tid: the thread's index in the group; bar_id: the group's barrier,
-// 0 for the whole CTA).  Every thread of the group calls it; it ends with a
-// group barrier.
+// T = (I + A)^{-1} for a strictly lower 64 x 64 matrix A (both in the layout
+// above; A is read only below its diagonal).  With L = I + A partitioned into
+// blocks, [L11 0; L21 L22]^{-1} = [T11 0; -T22 L21 T11, T22], applied twice:
+//   1. the four 16 x 16 diagonal blocks by forward substitution (a column per
+//      thread, 64 threads);
+//   2. 16 -> 32: T10 = -T11 (A10 T00), T32 = -T33 (A32 T22);
+//   3. 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] (A[32:64][0:32] T[0:32][0:32]).
+// Each product's left factor is staged in a block of T above the diagonal,
+// where the inverse is zero: T holds the inverse on and below its diagonal
+// only, and whoever reads it takes T[t][s] = 0 for s > t.  The products run as
+// 128 units of one or two rows x 4 columns, so every output's sum has the same
+// order whatever the thread count NT (>= 128); the unit -> thread maps keep
+// each warp's loop bounds uniform.  tid: the thread's index in its group of NT;
+// bar_id: the group's named barrier (0 for the whole CTA).  Every thread of
+// the group calls it; it ends with a group barrier.
 template <int NT>
-__device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, float* Mf, int tid, int bar_id) {
-  static_assert(NT >= 64 && NT % 32 == 0, "the diagonal blocks use 64 threads");
+__device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, int tid, int bar_id) {
+  static_assert(NT >= 128 && NT % 32 == 0, "the products use 128 threads");
   if (tid < 64) {
     const int b = tid >> 4, c = tid & 15;
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
+      float a[16];
+#pragma unroll
+      for (int q = 0; 4 * q < r; ++q) {
+        const float4 a4 = ut_ld4(Af, 16 * b + r, 16 * b + 4 * q);
+        a[4 * q] = a4.x; a[4 * q + 1] = a4.y; a[4 * q + 2] = a4.z; a[4 * q + 3] = a4.w;
+      }
       float acc = (r == c) ? 1.0f : 0.0f;
 #pragma unroll
-      for (int s = 0; s < r; ++s) acc = fmaf(-Af[(16 * b + r) * LDA + 16 * b + s], x[s], acc);
+      for (int s = 0; s < r; ++s) acc = fmaf(-a[s], x[s], acc);
       x[r] = acc;
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Tf[(16 * b + r) * LDA + 16 * b + c] = x[r];
-  } else {
-    // zero the blocks above the diagonal
-    for (int e = tid - 64; e < 6 * 256; e += NT - 64) {
-      const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
-      const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-      const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-      Tf[(16 * bi + r) * LDA + 16 * bj + c] = 0.0f;
-    }
+    for (int r = 0; r < 16; ++r) Tf[ut_idx(16 * b + r, 16 * b + c)] = x[r];
   }
   group_sync<NT>(bar_id);
-  solve_block_diagonal<NT, 1>(Af, Tf, Mf, tid, bar_id);
-  solve_block_diagonal<NT, 2>(Af, Tf, Mf, tid, bar_id);
-  solve_block_diagonal<NT, 3>(Af, Tf, Mf, tid, bar_id);
+  // 16 -> 32; unit u: column group u & 3, row (u >> 2) & 15, pair u >> 6
+  const int u = tid;
+  const int s_cq = u & 3, s_r = (u >> 2) & 15, s_i = 2 * (u >> 6) + 1, s_j = s_i - 1;
+  if (u < 128) {   // A_ij T_jj -> the zero block (j, i)
+    float acc[1][4] = {{0.0f, 0.0f, 0.0f, 0.0f}};
+    const int xr[1] = {16 * s_i + s_r};
+    ut_rowquad<1>(Af, xr, 16 * s_j, Tf, 16 * s_j, 16 * s_j + 4 * s_cq, 16, acc);
+    ut_st4(Tf, 16 * s_j + s_r, 16 * s_i + 4 * s_cq, acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+  }
+  group_sync<NT>(bar_id);
+  if (u < 128) {   // T_ij = -T_ii (A_ij T_jj)
+    float acc[1][4] = {{0.0f, 0.0f, 0.0f, 0.0f}};
+    const int xr[1] = {16 * s_i + s_r};
+    ut_rowquad<1>(Tf, xr, 16 * s_i, Tf, 16 * s_j, 16 * s_i + 4 * s_cq, 16, acc);
+    ut_st4(Tf, 16 * s_i + s_r, 16 * s_j + 4 * s_cq, -acc[0][0], -acc[0][1], -acc[0][2], -acc[0][3]);
+  }
+  group_sync<NT>(bar_id);
+  // 32 -> 64; unit u: rows r0 = 16 rh + (u >> 2) & 7 and r0 + 8, column group
+  // 4 ch + (u & 3), with ch = (u >> 5) & 1 and rh = u >> 6
+  const int rh = (u >> 6) & 1, ch = (u >> 5) & 1;
+  const int r0 = 16 * rh + ((u >> 2) & 7), cq = 4 * ch + (u & 3);
+  if (u < 128) {   // A[32:64][0:32] T[0:32][0:32] -> T[0:32][32:64]; T[0:16][16:32] is staging, skipped
+    float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+    const int xr[2] = {32 + r0, 40 + r0};
+    const int k0 = 16 * ch;
+    ut_rowquad<2>(Af, xr, k0, Tf, k0, 4 * cq, 32 - k0, acc);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) ut_st4(Tf, r0 + 8 * r, 32 + 4 * cq, acc[r][0], acc[r][1], acc[r][2], acc[r][3]);
+  }
+  group_sync<NT>(bar_id);
+  if (u < 128) {   // -T[32:64][32:64] (...) -> T[32:64][0:32]; T[32:48][48:64] is staging, skipped
+    float acc[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
+    const int xr[2] = {32 + r0, 40 + r0};
+    ut_rowquad<2>(Tf, xr, 32, Tf, 0, 32 + 4 * cq, rh ? 32 : 16, acc);
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      ut_st4(Tf, 32 + r0 + 8 * r, 4 * cq, -acc[r][0], -acc[r][1], -acc[r][2], -acc[r][3]);
+  }
+  group_sync<NT>(bar_id);
 }
 
 // Launchers of the split prefill (prep pass, then the scan passes).

@@ -47,23 +47,29 @@ struct PrepLay {
   static constexpr uint32_t RAW = 66560;        // two staged raw blocks: q | k, then v of two heads;
                                                 // then head group 1's area
   static constexpr uint32_t GATE = RAW + 2 * RAW_BLK;   // per head: fp32 gamma, beta, e^gamma [64]
-  static constexpr uint32_t MF = GATE + kMaxG * 3 * 64 * 4;   // per head group: the solve's scratch
-  static constexpr uint32_t BYTES = MF + 2 * 3 * 256 * 4 + 1024;   // + slack to align the base
-  // A head group's area: A and T fp32 [64][LDA], then T diag(beta e^gamma)
-  // over A, then -W [t][d_k] over A
+  static constexpr uint32_t BYTES = GATE + kMaxG * 3 * 64 * 4 + 1024;   // + slack to align the base
+  // A head group's area: the solve's A and T (fp32, 16 KB each), then
+  // T diag(beta e^gamma) over A, then -W [t][d_k] over A
   __host__ __device__ static constexpr uint32_t area(int grp) { return grp == 0 ? KQ16 : RAW; }
 };
-static_assert(PrepLay::KQ16 + 2 * 64 * LDA * 4 <= PrepLay::RAW, "head group 0's A and T overlap the raw staging");
-static_assert(2 * 64 * LDA * 4 <= 2 * RAW_BLK, "head group 1's A and T exceed the raw staging");
+static_assert(PrepLay::KQ16 + 2 * UT_BYTES <= PrepLay::RAW, "head group 0's A and T overlap the raw staging");
+static_assert(2 * UT_BYTES <= 2 * RAW_BLK, "head group 1's A and T exceed the raw staging");
+static_assert(16384 <= UT_BYTES, "-W goes over A");
 static_assert(PrepLay::RAW % 1024 == 0 && RAW_BLK % 128 == 0, "TMA destinations need 128-byte alignment");
 static_assert(2 * (PrepLay::BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
 constexpr uint32_t TP_G = 0, TP_W = 64, TP_COLS = 256;   // TMEM: Gram [K^;Q^]K^T, W^T per head group
 
-// This lane's 4 channels ch .. ch+3 of the conv weight, w[tap][channel].
-__device__ __forceinline__ void conv_weights(const uint16_t* conv_w, int ch, float (&w)[kConvW][4]) {
-  const uint4 u0 = *reinterpret_cast<const uint4*>(conv_w + (size_t)ch * kConvW);        // channels ch, ch+1
-  const uint4 u1 = *reinterpret_cast<const uint4*>(conv_w + (size_t)(ch + 2) * kConvW);  // ch+2, ch+3
-  const uint32_t wv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+// This lane's 4 channels ch .. ch+3 of the conv weight as stored (bf16 [channel][tap]),
+// and unpacked to w[tap][channel].
+struct ConvW4 {
+  uint4 u0, u1;   // channels ch, ch+1 | ch+2, ch+3
+};
+__device__ __forceinline__ ConvW4 conv_weights_load(const uint16_t* conv_w, int ch) {
+  return {*reinterpret_cast<const uint4*>(conv_w + (size_t)ch * kConvW),
+          *reinterpret_cast<const uint4*>(conv_w + (size_t)(ch + 2) * kConvW)};
+}
+__device__ __forceinline__ void conv_weights(const ConvW4& cw, float (&w)[kConvW][4]) {
+  const uint32_t wv[8] = {cw.u0.x, cw.u0.y, cw.u0.z, cw.u0.w, cw.u1.x, cw.u1.y, cw.u1.z, cw.u1.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e)
 #pragma unroll
@@ -137,6 +143,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     return ok_all;
   };
   bool ok = true;
+  // this lane's q and k conv weights, in flight while the gates run
+  const ConvW4 cw_qk[2] = {conv_weights_load(p.conv_w, kh * kD + 4 * lane),
+                           conv_weights_load(p.conv_w, Cq + kh * kD + 4 * lane)};
 
   // ---- gates and their cumulative sums, warp g for value head kh*G + g (meanwhile
   //      the raw rows land); the scan passes get e^gamma and e^{gamma_C - gamma} ----
@@ -183,24 +192,29 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
   // ---- conv + SiLU + L2 norms of q and k -> [K^ | Q^] in bf16 and fp16 ----
   if (!wait_raw()) ok = false;
+  static_assert(C / 4 == 2 * (kPrepThreads / 32), "each warp takes two token quads of q and two of k");
   if (ok) {
     const float qscale = rsqrtf((float)kD);
-#pragma unroll 1
-    for (int task = warp; task < 2 * (C / 4); task += kPrepThreads / 32) {
-      const int blk = task / (C / 4), tq = 4 * (task % (C / 4));   // blk 0: q, 1: k
+#pragma unroll
+    for (int blk = 0; blk < 2; ++blk) {   // 0: q, 1: k
       const int ch = (blk == 0 ? 0 : Cq) + kh * kD + 4 * lane;
-      float w[kConvW][4], y[4][4];
-      conv_weights(p.conv_w, ch, w);
-      conv_quad_staged(sm.base + L_::RAW + blk * RAW_BLK, cs_seq + ch, Cc, t0, L, tq, lane, w, y);
-      float rn[4];
-      l2_rnorm4(y, p.l2_eps, blk == 0 ? qscale : 1.0f, lane, rn);
+      float w[kConvW][4];
+      conv_weights(cw_qk[blk], w);
+#pragma unroll 1
+      for (int qd = 0; qd < 2; ++qd) {
+        const int tq = 4 * (warp + 8 * qd);
+        float y[4][4];
+        conv_quad_staged(sm.base + L_::RAW + blk * RAW_BLK, cs_seq + ch, Cc, t0, L, tq, lane, w, y);
+        float rn[4];
+        l2_rnorm4(y, p.l2_eps, blk == 0 ? qscale : 1.0f, lane, rn);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+        for (int i = 0; i < 4; ++i) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) y[i][e] *= rn[i];
-        const uint32_t o16 = tc::sw128_off(tq + i, 4 * lane, 16384) + (blk == 0 ? 8192u : 0u);
-        store_bf16x4(sm.base + L_::KQ, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
-        store_f16x4(sm.base + L_::KQ16, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
+          for (int e = 0; e < 4; ++e) y[i][e] *= rn[i];
+          const uint32_t o16 = tc::sw128_off(tq + i, 4 * lane, 16384) + (blk == 0 ? 8192u : 0u);
+          store_bf16x4(sm.base + L_::KQ, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
+          store_f16x4(sm.base + L_::KQ16, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
+        }
       }
     }
   }
@@ -221,6 +235,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 #pragma unroll 1
   for (int g0 = 0; g0 < G && ok; g0 += 2) {
     const int nv = min(2, G - g0);
+    // this lane's conv weights of the two heads, in flight while their rows land
+    const ConvW4 cw_v[2] = {conv_weights_load(p.conv_w, 2 * Cq + (kh * G + g0) * kD + 4 * lane),
+                            conv_weights_load(p.conv_w, 2 * Cq + (kh * G + g0 + nv - 1) * kD + 4 * lane)};
     if (tid == 32) {
       mbar_expect_tx(&mbar_raw, nv * RAW_BLK);
       for (int i = 0; i < nv; ++i)
@@ -228,18 +245,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
     raw_pending = true;
     if (!wait_raw()) { ok = false; break; }
-#pragma unroll 1
-    for (int task = warp; task < nv * (C / 4); task += kPrepThreads / 32) {
-      const int i = task / (C / 4), tq = 4 * (task % (C / 4));
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      if (i >= nv) break;
       const int h = kh * G + g0 + i;
       const int ch = 2 * Cq + h * kD + 4 * lane;
-      float w[kConvW][4], y[4][4];
-      conv_weights(p.conv_w, ch, w);
-      conv_quad_staged(sm.base + L_::RAW + i * RAW_BLK, cs_seq + ch, Cc, t0, L, tq, lane, w, y);
+      float w[kConvW][4];
+      conv_weights(cw_v[i], w);
       uint8_t* vh = p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecVH;
+#pragma unroll 1
+      for (int qd = 0; qd < 2; ++qd) {
+        const int tq = 4 * (warp + 8 * qd);
+        float y[4][4];
+        conv_quad_staged(sm.base + L_::RAW + i * RAW_BLK, cs_seq + ch, Cc, t0, L, tq, lane, w, y);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
+        for (int q = 0; q < 4; ++q)
+          store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
+      }
     }
     __syncthreads();   // the raw v rows are read
   }
@@ -250,8 +272,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   {
     const int grp = half, gtid = tid & 127, bar = 1 + grp;
     float* Af = sm.f32(L_::area(grp));
-    float* Tf = Af + 64 * LDA;
-    float* Mf = sm.f32(L_::MF + grp * 3 * 256 * 4);
+    float* Tf = Af + UT_BYTES / 4;
     uint8_t* wn = sm.base + L_::area(grp);
     const uint32_t tw = sm.addr + L_::area(grp);
     const uint32_t tm_w = tmem + TP_W + 64 * grp;
@@ -268,9 +289,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         if (gtid == 0) bulk_wait_read();
         group_sync<128>(bar);
       }
-      // ---- A (fp32) and P (bf16, straight into the record) from the Gram rows:
-      //      lane quarters 0-1 hold K^K^T rows, 2-3 Q^K^T rows; rows 0-31 are zero
-      //      right of column 31 ----
+      // ---- A (fp32, below its diagonal: the solve reads nothing else) and P
+      //      (bf16, straight into the record) from the Gram rows: lane quarters
+      //      0-1 hold K^K^T rows, 2-3 Q^K^T rows; P's rows 0-31 are zero right
+      //      of column 31 ----
       {
         const int t = row & 63;
         const float gt = gam[t];
@@ -279,10 +301,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         for (int hf = 0; hf < 2; ++hf) {
           const int c0 = 32 * hf;
           if (t < 32 && hf == 1) {
-            if (quarter < 2) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) Af[t * LDA + c0 + i] = 0.0f;
-            } else {
+            if (quarter >= 2) {
 #pragma unroll
               for (int m = 0; m < 4; ++m)
                 *reinterpret_cast<uint4*>(rv + kRecP + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
@@ -293,9 +312,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
           tc::tmem_ld32(tmem + lane_base + TP_G + c0, v);
           if (quarter < 2) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int s = c0 + i;
-              Af[t * LDA + s] = s < t ? bt * __expf(gt - gam[s]) * v[i] : 0.0f;
+            for (int m = 0; m < 8; ++m) {
+              float a[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) a[e] = bt * __expf(gt - gam[c0 + 4 * m + e]) * v[4 * m + e];
+              ut_st4(Af, t, c0 + 4 * m, a[0], a[1], a[2], a[3]);
             }
           } else {
 #pragma unroll
@@ -311,16 +332,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       group_sync<128>(bar);
 
       // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) over A ----
-      solve_unit_lower<128>(Af, Tf, Mf, gtid, bar);
+      solve_unit_lower<128>(Af, Tf, gtid, bar);
       {
         float xb[4][8], xw[4][8];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {   // all of T is read before T diag(beta e^gamma) goes over A
+        for (int q4 = 0; q4 < 4; ++q4) {
           const int e = gtid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
+          const float4 lo = ut_ld4(Tf, t, c8), hi = ut_ld4(Tf, t, c8 + 4);
+          const float tv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            const float tv = Tf[t * LDA + c8 + q];
-            xb[q4][q] = tv * bet[c8 + q];
+            xb[q4][q] = (c8 + q <= t ? tv[q] : 0.0f) * bet[c8 + q];   // T is zero above its diagonal
             xw[q4][q] = xb[q4][q] * eg[c8 + q];
           }
         }
