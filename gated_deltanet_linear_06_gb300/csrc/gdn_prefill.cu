@@ -370,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int s = c0 + i;
-          v[i] = s <= t ? v[i] * __expf(gt - gam[s]) : 0.0f;
+          v[i] = keep_if_le(v[i] * __expf(gt - gam[s]), s, t);
         }
 #pragma unroll
         for (int m = 0; m < 2; ++m)
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float tv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        xb[q] = (c8 + q <= t ? tv[q] : 0.0f) * bet[c8 + q];   // T is zero above its diagonal
+        xb[q] = keep_if_le(tv[q], c8 + q, t) * bet[c8 + q];   // T is zero above its diagonal
         xw[q] = xb[q] * eg[c8 + q];
       }
       store_bf16x8(sm.base + M::TB, tc::sw128_off(t, c8, 0), xb);

@@ -48,7 +48,8 @@ struct PrepLay {
                                                 // then head group 1's area
   static constexpr uint32_t GATE = RAW + 2 * RAW_BLK;   // per head: fp32 gamma, beta, e^gamma [64]
   static constexpr uint32_t BYTES = GATE + kMaxG * 3 * 64 * 4 + 1024;   // + slack to align the base
-  // A head group's area: the solve's A and T (fp32, 16 KB each), then
+  // A head group's area: the solve's A and T (fp32, 16 KB each) -- with the
+  // bf16 P tile over T's first 8 KB until the solve writes T --, then
   // T diag(beta e^gamma) over A, then -W [t][d_k] over A
   __host__ __device__ static constexpr uint32_t area(int grp) { return grp == 0 ? KQ16 : RAW; }
 };
@@ -273,6 +274,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const int grp = half, gtid = tid & 127, bar = 1 + grp;
     float* Af = sm.f32(L_::area(grp));
     float* Tf = Af + UT_BYTES / 4;
+    uint8_t* ptile = sm.base + L_::area(grp) + UT_BYTES;
     uint8_t* wn = sm.base + L_::area(grp);
     const uint32_t tw = sm.addr + L_::area(grp);
     const uint32_t tm_w = tmem + TP_W + 64 * grp;
@@ -290,9 +292,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         group_sync<128>(bar);
       }
       // ---- A (fp32, below its diagonal: the solve reads nothing else) and P
-      //      (bf16, straight into the record) from the Gram rows: lane quarters
-      //      0-1 hold K^K^T rows, 2-3 Q^K^T rows; P's rows 0-31 are zero right
-      //      of column 31 ----
+      //      (bf16 tile, bulk-stored into the record) from the Gram rows: lane
+      //      quarters 0-1 hold K^K^T rows, 2-3 Q^K^T rows; P's rows 0-31 are
+      //      zero right of column 31 ----
       {
         const int t = row & 63;
         const float gt = gam[t];
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             if (quarter >= 2) {
 #pragma unroll
               for (int m = 0; m < 4; ++m)
-                *reinterpret_cast<uint4*>(rv + kRecP + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(ptile + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
             }
             continue;
           }
@@ -322,17 +324,25 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               const int s = c0 + i;
-              v[i] = s <= t ? v[i] * __expf(gt - gam[s]) : 0.0f;
+              v[i] = keep_if_le(v[i] * __expf(gt - gam[s]), s, t);
             }
 #pragma unroll
-            for (int m = 0; m < 4; ++m) store_bf16x8(rv + kRecP, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
+            for (int m = 0; m < 4; ++m) store_bf16x8(ptile, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
           }
         }
       }
+      tc::fence_proxy_async();
       group_sync<128>(bar);
+      if (gtid == 0) {
+        bulk_store(rv + kRecP, ptile, 8192);
+        bulk_commit();
+      }
 
       // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) over A ----
-      solve_unit_lower<128>(Af, Tf, gtid, bar);
+      solve_unit_lower<128>(Af, Tf, gtid, bar, [&] {   // the P tile has left T's rows
+        if (gtid == 0) bulk_wait_read();
+        group_sync<128>(bar);
+      });
       {
         float xb[4][8], xw[4][8];
 #pragma unroll
@@ -342,7 +352,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
           const float tv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
-            xb[q4][q] = (c8 + q <= t ? tv[q] : 0.0f) * bet[c8 + q];   // T is zero above its diagonal
+            xb[q4][q] = keep_if_le(tv[q], c8 + q, t) * bet[c8 + q];   // T is zero above its diagonal
             xw[q4][q] = xb[q4][q] * eg[c8 + q];
           }
         }
