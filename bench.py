@@ -350,13 +350,14 @@ def run_ours(args) -> dict | None:
     if rank != 0:
         return None
 
-    # kernels one gdn_prefill call launches: the work list, the prep pass, the
-    # output scan and the conv-state hand-off, plus the transfer scan and the
-    # combine pass when the single sequence x 32 heads leaves the GPU short of
-    # CTAs and sequences are split into segments
+    # kernels one gdn_prefill call launches: the work list and the conv-state
+    # hand-off, plus per head group the prep pass and the output scan; when the
+    # single sequence x 32 heads leaves the GPU short of CTAs, sequences are
+    # split into segments, which adds the transfer scan and the combine pass
+    # and runs the call as 4 head groups (16 key heads) on forked streams
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     split = 1 * H_V < 4 * sms and PREFILL_T > 1024
-    prefill_kernels = 6 if split else 4
+    prefill_kernels = 2 + 4 * 4 if split else 4
     hbm = float(peaks["hbm_gbs"])
     tc_peak = float(peaks["bf16_tflops"])
     pre_bytes = PREFILL_T * PREFILL_BYTES_PER_TOKEN + 2 * STATE_BYTES

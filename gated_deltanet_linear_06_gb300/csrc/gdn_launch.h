@@ -51,6 +51,10 @@ struct PrefillArgs {
   uint8_t* rec_kq;         // [max_chunks][h_k] per-chunk key/query tile records
   uint8_t* rec_v;          // [max_chunks][h_v] per-chunk value-head records
   int max_chunks;          // chunk records the workspace holds: total_tokens / 64 + n_seqs
+  // the heads one launch of the prep / scan / combine passes covers (a call may
+  // run as several head groups): key heads kh0 .. kh0+nkh-1, value heads
+  // h0 .. h0+nh-1
+  int kh0, nkh, h0, nh;
   int n_seqs, h_k, h_v;
   long long total_tokens;
   float l2_eps, rms_eps;

@@ -47,6 +47,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
@@ -723,10 +725,51 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A segmented call runs as kHeadGroups groups of key heads (with their value
+// heads), each on its own stream: every head's passes are independent of the
+// other heads', so one group's combine pass -- a chain of dependent steps on
+// one CTA per head -- and the passes' last partial waves overlap other groups'
+// work.  (Stream priorities, to run the first group ahead, measured slower: a
+// pending high-priority combine CTA needs a whole SM and holds back the rest.)
+// The first group runs on the caller's stream, the others on side streams, per
+// device, created on first use and kept for the life of the process; the
+// caller's stream forks to them through one event and joins back through one
+// event per side stream.  Enqueueing is serialised by a mutex, so concurrent
+// calls on one device also share (and are ordered on) the side streams.
+constexpr int kHeadGroups = 4;
+constexpr int kMaxDevices = 64;
+struct SideStreams {
+  bool ready = false;
+  cudaStream_t s[kHeadGroups - 1] = {};
+  cudaEvent_t fork = nullptr, join[kHeadGroups - 1] = {};
+};
+std::mutex g_side_mu;
+SideStreams g_side[kMaxDevices];
+
+cudaError_t side_streams_locked(int dev, SideStreams*& out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  SideStreams& ss = g_side[dev];
+  if (!ss.ready) {
+    cudaError_t e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+    for (int i = 0; i < kHeadGroups - 1 && e == cudaSuccess; ++i) {
+      e = cudaStreamCreateWithFlags(&ss.s[i], cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ss.join[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return e;   // a partial set is created again next time (the handles made so far leak)
+    ss.ready = true;
+  }
+  out = &ss;
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool allow_split) {
   PrefillArgs p = p_in;
+  p.kh0 = 0;
+  p.nkh = p.h_k;
+  p.h0 = 0;
+  p.nh = p.h_v;
   const ScratchLayout l = scratch_layout(p.n_seqs, p.h_k, p.h_v, p.total_tokens, allow_split);
   char* scratch = static_cast<char*>(p.scratch);
   p.seg_list = reinterpret_cast<int*>(scratch + l.seg_list);
@@ -765,12 +808,42 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
     const unsigned units = (unsigned)(slots + p.n_seqs);
     seg_list_kernel<<<1, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if ((e = launch_prefill_prep(p, (unsigned)l.max_chunks, tm_qkv, stream)) != cudaSuccess) return e;
-    if (slots > 0) {   // some sequence may be longer than one segment
-      if ((e = launch_prefill_scan(p, true, units, tm_z, stream)) != cudaSuccess) return e;
-      if ((e = launch_prefill_combine(p, (unsigned)slots, stream)) != cudaSuccess) return e;
+    // head groups on forked streams when there is a combine pass to hide
+    const int groups = (slots > 0 && p.h_k % kHeadGroups == 0) ? kHeadGroups : 1;
+    std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
+    SideStreams* ss = nullptr;
+    cudaStream_t st[kHeadGroups] = {stream};
+    if (groups > 1) {
+      lock.lock();
+      if ((e = side_streams_locked(dev, ss)) != cudaSuccess) return e;
+      if ((e = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return e;
+      for (int g = 1; g < groups; ++g) {
+        st[g] = ss->s[g - 1];
+        if ((e = cudaStreamWaitEvent(st[g], ss->fork, 0)) != cudaSuccess) return e;
+      }
     }
-    if ((e = launch_prefill_scan(p, false, units, tm_z, stream)) != cudaSuccess) return e;
+    PrefillArgs pg[kHeadGroups];
+    for (int g = 0; g < groups; ++g) {
+      pg[g] = p;
+      pg[g].nkh = p.h_k / groups;
+      pg[g].kh0 = g * pg[g].nkh;
+      pg[g].nh = pg[g].nkh * (p.h_v / p.h_k);
+      pg[g].h0 = pg[g].kh0 * (p.h_v / p.h_k);
+    }
+    for (int g = 0; g < groups; ++g)
+      if ((e = launch_prefill_prep(pg[g], (unsigned)l.max_chunks, tm_qkv, st[g])) != cudaSuccess) return e;
+    if (slots > 0) {   // some sequence may be longer than one segment
+      for (int g = 0; g < groups; ++g)
+        if ((e = launch_prefill_scan(pg[g], true, units, tm_z, st[g])) != cudaSuccess) return e;
+      for (int g = 0; g < groups; ++g)
+        if ((e = launch_prefill_combine(pg[g], (unsigned)slots, st[g])) != cudaSuccess) return e;
+    }
+    for (int g = 0; g < groups; ++g)
+      if ((e = launch_prefill_scan(pg[g], false, units, tm_z, st[g])) != cudaSuccess) return e;
+    for (int g = 1; g < groups; ++g) {
+      if ((e = cudaEventRecord(ss->join[g - 1], st[g])) != cudaSuccess) return e;
+      if ((e = cudaStreamWaitEvent(stream, ss->join[g - 1], 0)) != cudaSuccess) return e;
+    }
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   conv_state_kernel<<<dim3((unsigned)((Cc_ + 255) / 256), (unsigned)p.n_seqs), 256, 0, stream>>>(p);

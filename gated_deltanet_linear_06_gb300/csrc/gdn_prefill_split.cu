@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int c = blockIdx.x / p.h_k, kh = blockIdx.x % p.h_k;
+  const int c = blockIdx.x / p.nkh, kh = p.kh0 + blockIdx.x % p.nkh;
   if (*p.status == GDN_ERR_DEVICE_BOUNDS) return;   // cu_seqlens rejected by the list kernel
   const int2 ce = p.chunk_list[c];
   if (ce.x < 0 || ce.x >= p.n_seqs) return;          // past the last chunk
@@ -490,7 +490,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool issuer = warp == kOutWorkers / 32;
-  const int u = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
+  const int u = blockIdx.x / p.nh, h = p.h0 + blockIdx.x % p.nh;
   if (u >= p.seg_list[0]) return;
   const Seg sg = load_seg(p.seg_list, u);
   const int n = sg.n;
@@ -815,7 +815,7 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool track_x = (blockIdx.x & 1) != 0;
   const int cu = blockIdx.x >> 1;
-  const int u = cu / p.h_v, h = cu % p.h_v;
+  const int u = cu / p.nh, h = p.h0 + cu % p.nh;
   if (u >= p.seg_list[0]) return;
   const Seg sg = load_seg(p.seg_list, u);
   if (sg.sigma == sg.nsig - 1) return;   // the last segment needs no transfer map
@@ -1043,7 +1043,7 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillA
   __shared__ __align__(8) uint64_t mb_x[2];   // map buffers landed
   __shared__ __align__(8) uint64_t mb_mma;
   __shared__ uint32_t tmem_base_s;
-  const int u = blockIdx.x / p.h_v, h = blockIdx.x % p.h_v;
+  const int u = blockIdx.x / p.nh, h = p.h0 + blockIdx.x % p.nh;
   if (u >= p.multi_list[0]) return;
   const int* e = p.multi_list + 4 + 4 * u;
   const int n = e[0], k0 = e[1], nsig = e[2];
@@ -1153,7 +1153,7 @@ cudaError_t launch_prefill_prep(const PrefillArgs& p, unsigned max_chunks, const
   cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)PrepLay::BYTES);
   if (e != cudaSuccess) return e;
-  prep_kernel<<<max_chunks * (unsigned)p.h_k, kPrepThreads, PrepLay::BYTES, stream>>>(p, tm_qkv);
+  prep_kernel<<<max_chunks * (unsigned)p.nkh, kPrepThreads, PrepLay::BYTES, stream>>>(p, tm_qkv);
   return cudaGetLastError();
 }
 
@@ -1161,7 +1161,7 @@ cudaError_t launch_prefill_combine(const PrefillArgs& p, unsigned max_multi, cud
   cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)CombLay::BYTES);
   if (e != cudaSuccess) return e;
-  combine_kernel<<<max_multi * (unsigned)p.h_v, kCombThreads, CombLay::BYTES, stream>>>(p);
+  combine_kernel<<<max_multi * (unsigned)p.nh, kCombThreads, CombLay::BYTES, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -1172,12 +1172,12 @@ cudaError_t launch_prefill_scan(const PrefillArgs& p, bool transfer, unsigned un
     if ((e = cudaFuncSetAttribute(xfer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)XferLay::BYTES)) != cudaSuccess)
       return e;
-    xfer_kernel<<<2 * units * (unsigned)p.h_v, kXferThreads, XferLay::BYTES, stream>>>(p);
+    xfer_kernel<<<2 * units * (unsigned)p.nh, kXferThreads, XferLay::BYTES, stream>>>(p);
   } else {
     if ((e = cudaFuncSetAttribute(output_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)ScanLay::BYTES)) != cudaSuccess)
       return e;
-    output_kernel<<<units * (unsigned)p.h_v, kOutThreads, ScanLay::BYTES, stream>>>(p, tm_z);
+    output_kernel<<<units * (unsigned)p.nh, kOutThreads, ScanLay::BYTES, stream>>>(p, tm_z);
   }
   return cudaGetLastError();
 }

@@ -189,11 +189,12 @@ def test_prefill_other_head_groupings(h_k, h_v):
     _check(sh, lengths, params, tok, st)
 
 
-@pytest.mark.parametrize("h_k,h_v", [(32, 32), (8, 32)])
+@pytest.mark.parametrize("h_k,h_v", [(32, 32), (8, 32), (6, 12)])
 def test_prefill_segmented_other_head_groupings(h_k, h_v):
-    # a sequence longer than one segment with 1 and 4 value heads per key head:
-    # the prep pass's head groups, both transfer tracks and the combine at
-    # groupings other than 2
+    # a sequence longer than one segment with 1, 4 and 2 value heads per key
+    # head: the prep pass's head groups, both transfer tracks and the combine
+    # at groupings other than 2; 6 key heads do not split into the launcher's
+    # four stream groups, so that call runs as one group
     sh = gi.Shape(h_k=h_k, h_v=h_v)
     lengths = [2100, 30]
     params, tok, st = _inputs(sh, lengths, 16, slow=True, ssm_std=0.3, conv_std=1.0, norm_w="uniform")
