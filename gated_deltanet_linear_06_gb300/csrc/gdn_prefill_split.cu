@@ -419,14 +419,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // The output pass, warp-specialised.  One CTA per (segment, value head): 16
 // worker warps (4 per TMEM lane quarter) make the operand tiles from the
 // accumulators, stage O and run the gated RMSNorm epilogue; one more warp
-// issues every bulk copy and every tensor-core product.  The two sides meet on
-// mbarriers, so the per-chunk chain is only
+// issues the tensor-core products and another the bulk copies (issuing a copy
+// can stall, and the products are on the chain).  They meet on mbarriers, so
+// the per-chunk chain is only
 //   [U, Vn^T] -> Vn^T tiles -> [state update] -> state tile -> next [U, Vn^T]
 // while O1 = S0 Q^T, O2 = Vn^T P^T, the O staging and the epilogue run beside
 // it (O1 double-buffered in TMEM).  Every wait is bounded; the workers agree on
 // a time-out at their own barriers.
 constexpr int kOutWorkers = 512;              // 16 warps
-constexpr int kOutThreads = kOutWorkers + 32; // + the issuing warp
+constexpr int kOutThreads = kOutWorkers + 64; // + the MMA warp and the copy warp
 static_assert(kOutWorkers / 32 * 4 == C, "the epilogue gives each worker warp 4 of a chunk's tokens");
 struct ScanLay {
   static constexpr uint32_t S = 0;          // S bf16 [d_v][d_k], K blocks 16 KB apart
@@ -486,10 +487,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   __shared__ __align__(8) uint64_t mb_b1, mb_b2, mb_o;
   // worker warps done (16 arrivals): Vn^T tiles, state tile, O read, epilogue
   __shared__ __align__(8) uint64_t mb_vn, mb_s, mb_or, mb_ep;
+  __shared__ __align__(8) uint64_t mb_fin;   // after a time-out: every product issued has finished
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const bool issuer = warp == kOutWorkers / 32;
   const int u = blockIdx.x / p.nh, h = p.h0 + blockIdx.x % p.nh;
   if (u >= p.seg_list[0]) return;
   const Seg sg = load_seg(p.seg_list, u);
@@ -527,6 +528,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     tc::mbar_init(&mb_b1, 1);
     tc::mbar_init(&mb_b2, 1);
     tc::mbar_init(&mb_o, 1);
+    tc::mbar_init(&mb_fin, 1);
     tc::mbar_init(&mb_vn, kOutWorkers / 32);
     tc::mbar_init(&mb_s, kOutWorkers / 32);
     tc::mbar_init(&mb_or, kOutWorkers / 32);
@@ -544,12 +546,88 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   };
   bool ok = true;
 
-  if (issuer) {
-    // ================= the issuing warp (one lane) =================
+  if (warp == kOutWorkers / 32) {
+    // ================= the MMA warp (one lane) =================
+    // Each wait below is for a completion whose successor needs something this
+    // lane issues only afterwards, so the barrier is never two phases on.
+    if (lane == 0) {
+      uint32_t issued_mma = 0;
+      // U = V^T (T diag beta)^T needs only the records: each chunk's is issued
+      // ahead, before the state tile it waits for
+      auto issue_u = [&](int j) -> bool {
+        if (!wt(&mb_a, j)) return false;
+        tc::fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_U, tc::sdesc_at(D_MN_V, sm.addr + M::VH + k * 2048),
+                       tc::sdesc_at(D_K, sm.addr + M::TB + k * 32), ID_MN_A, k > 0);
+        ++issued_mma;
+        return true;
+      };
+      ok = issue_u(0);
+      for (int j = 0; j < nch && ok; ++j) {
+        const uint32_t kq = sm.addr + M::KQ + (j & 1) * M::KQ_BUF;
+        // this chunk's [K^ | Q^] and the workers' state tile
+        if (!(wt(&mb_kq[j & 1], j >> 1) && wt(&mb_s, j))) { ok = false; break; }
+        tc::fence_after_sync();
+        // [Vn^T = U + S0 (-W)^T]
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TS_U, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                       tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
+        }
+        tc::mma_commit(&mb_b1);
+        // O1 = S0 Q^T into its buffer, which the workers read at chunk j - 2 (the
+        // wait for that read was the O2 wait of chunk j - 1)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TS_O1 + 64 * (j & 1), tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
+                       tc::sdesc_at(D_K, kq + kb * 16384 + 8192 + ks), ID_KK, k > 0);
+        }
+        // the workers' Vn^T tiles, and P
+        if (!(wt(&mb_vn, j) && wt(&mb_p, j))) { ok = false; break; }
+        tc::fence_after_sync();
+        // [S += Vn^T diag(e^{gamma_C - gamma}) K^]
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
+                       tc::sdesc_at(D_MN_KQ, kq + k * 2048), ID_MN_B, 1u);
+        tc::mma_commit(&mb_b2);
+        // O2 = Vn^T P^T, once the workers have read O2 of chunk j - 1
+        if (j >= 1 && !wt(&mb_or, j - 1)) { ok = false; break; }
+        tc::fence_after_sync();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TS_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
+                       tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
+        tc::mma_commit(&mb_o);
+        // the next chunk's U (TS_U was read for the Vn^T tiles)
+        if (j + 1 < nch && !issue_u(j + 1)) { ok = false; break; }
+      }
+      if (!ok) {
+        record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+        // the products issued finish (bounded) before the tensor memory is freed
+        if (issued_mma > 0) {
+          tc::mma_commit(&mb_fin);
+          wt(&mb_fin, 0);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kOutWorkers / 32 + 1) {
+    // ================= the copy warp (one lane) =================
+    // Every buffer is refilled once a product barrier shows its last reader done:
+    // -W | V^ | T diag(beta) after [U, Vn^T] (b1); P and the [K^ | Q^] buffer after
+    // O2 (o), which follows the state update, O1 and -- through the MMA warp's own
+    // waits -- the workers' O read of the previous chunk (its gates) and their
+    // previous epilogue (its z).  The successor of each completion waited for needs
+    // a copy issued after the wait, so the barrier is never two phases on.
     if (lane == 0) {
       auto rec_kq = [&](int j) { return p.rec_kq + ((size_t)(sg.c0 + j) * p.h_k + kh) * kRecKQ; };
       auto rec_v = [&](int j) { return p.rec_v + ((size_t)(sg.c0 + j) * p.h_v + h) * kRecV; };
-      uint32_t i_kq[2] = {0, 0}, i_a = 0, i_g[3] = {0, 0, 0}, i_p = 0, i_z[2] = {0, 0};   // copies issued
+      uint32_t i_kq[2] = {0, 0}, i_a = 0, i_g0 = 0, i_g1 = 0, i_g2 = 0, i_p = 0, i_z[2] = {0, 0};   // copies issued
       auto load_kq = [&](int j) {
         bulk_load(sm.base + M::KQ + (j & 1) * M::KQ_BUF, rec_kq(j), kRecKQ, &mb_kq[j & 1]);
         ++i_kq[j & 1];
@@ -559,8 +637,9 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         ++i_a;
       };
       auto load_g = [&](int j) {
-        bulk_load(sm.base + M::GT + (j % 3) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g[j % 3]);
-        ++i_g[j % 3];
+        const int q = j % 3;
+        bulk_load(sm.base + M::GT + q * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g[q]);
+        if (q == 0) ++i_g0; else if (q == 1) ++i_g1; else ++i_g2;
       };
       auto load_p = [&](int j) {
         bulk_load(sm.base + M::P, rec_v(j) + kRecP, 8192, &mb_p);
@@ -571,72 +650,26 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         tma_load_2d(sm.base + M::Z + (j & 1) * 16384, &tm_z, h * kD, start + sg.begin + C * j, &mb_z[j & 1]);
         ++i_z[j & 1];
       };
-      load_g(0);
-      if (nch > 1) load_g(1);
-      load_kq(0);
-      if (nch > 1) load_kq(1);
       load_a(0);
+      load_kq(0);
+      load_g(0);
       load_p(0);
       load_z(0);
-      if (nch > 1) load_z(1);
-
-      for (int j = 0; j < nch; ++j) {
-        const uint32_t kq = sm.addr + M::KQ + (j & 1) * M::KQ_BUF;
-        // this chunk's records and the workers' state tile
-        if (!(wt(&mb_kq[j & 1], j >> 1) && wt(&mb_a, j) && wt(&mb_s, j))) { ok = false; break; }
-        tc::fence_after_sync();
-        // [U = V^T (T diag beta)^T, Vn^T = U + S0 (-W)^T]
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + TS_U, tc::sdesc_at(D_MN_V, sm.addr + M::VH + k * 2048),
-                       tc::sdesc_at(D_K, sm.addr + M::TB + k * 32), ID_MN_A, k > 0);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-          tc::mma_bf16(tmem + TS_U, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
-                       tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
-        }
-        tc::mma_commit(&mb_b1);
-        // O1 = S0 Q^T into its buffer, which the workers read at chunk j - 2: the
-        // wait for that read was the O2 wait of chunk j - 1 (waiting for it again
-        // here could see the barrier two phases on, where its parity repeats)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-          tc::mma_bf16(tmem + TS_O1 + 64 * (j & 1), tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
-                       tc::sdesc_at(D_K, kq + kb * 16384 + 8192 + ks), ID_KK, k > 0);
-        }
-        // [U, Vn^T] has finished with -W | V^ | T diag(beta)
+      if (nch > 1) {
+        load_kq(1);
+        load_g(1);
+        load_z(1);
+      }
+      for (int j = 0; j + 1 < nch; ++j) {
         if (!wt(&mb_b1, j)) { ok = false; break; }
-        if (j + 1 < nch) load_a(j + 1);
-        // the workers' Vn^T tiles, and P
-        if (!(wt(&mb_vn, j) && wt(&mb_p, j))) { ok = false; break; }
-        tc::fence_after_sync();
-        // the workers ran the epilogue of chunk j - 1 before these tiles: its z buffer refills
-        if (j >= 1 && j + 1 < nch) {
-          if (!wt(&mb_ep, j - 1)) { ok = false; break; }
-          load_z(j + 1);
-        }
-        // [S += Vn^T diag(e^{gamma_C - gamma}) K^]
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + TS_S, tc::sdesc_at(D_K, sm.addr + M::VNS + k * 32),
-                       tc::sdesc_at(D_MN_KQ, kq + k * 2048), ID_MN_B, 1u);
-        tc::mma_commit(&mb_b2);
-        // O2 = Vn^T P^T, once the workers have read O2 of chunk j - 1 (the gates of
-        // chunk j + 2 then go where those of chunk j - 1 were)
-        if (j >= 1 && !wt(&mb_or, j - 1)) { ok = false; break; }
-        tc::fence_after_sync();
-        if (j + 2 < nch) load_g(j + 2);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tmem + TS_O2, tc::sdesc_at(D_K, sm.addr + M::VN + k * 32),
-                       tc::sdesc_at(D_K, sm.addr + M::P + k * 32), ID_KK, k > 0);
-        tc::mma_commit(&mb_o);
-        // the state update and O2 have finished with P and this [K^ | Q^] buffer
+        load_a(j + 1);
         if (!wt(&mb_o, j)) { ok = false; break; }
-        if (j + 1 < nch) load_p(j + 1);
-        if (j + 2 < nch) load_kq(j + 2);
+        load_p(j + 1);
+        if (j >= 1) load_z(j + 1);
+        if (j + 2 < nch) {
+          load_kq(j + 2);
+          load_g(j + 2);
+        }
       }
       if (!ok) {
         record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
@@ -647,7 +680,9 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         drain(&mb_kq[0], i_kq[0]);
         drain(&mb_kq[1], i_kq[1]);
         drain(&mb_a, i_a);
-        for (int i = 0; i < 3; ++i) drain(&mb_g[i], i_g[i]);
+        drain(&mb_g[0], i_g0);
+        drain(&mb_g[1], i_g1);
+        drain(&mb_g[2], i_g2);
         drain(&mb_p, i_p);
         drain(&mb_z[0], i_z[0]);
         drain(&mb_z[1], i_z[1]);
@@ -1025,6 +1060,13 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
 // S^0 and accumulates s1 X_hi + s2 X_hi + s3 X_hi + s1 X_lo.  The terms left
 // out are below 2^-16 of |S||X| per step.  A map that is exactly the identity
 // (no writes, no decay) gives back S bit for bit.
+//
+// The accumulator is double-buffered in TMEM, so while the tensor core runs a
+// step's products the threads load the next step's S^0 into the other buffer
+// and store the previous step's result: per step the chain is only the
+// products, the read-back and the split into the next operands.  The warp that
+// issues the products does its share of that after its split instead, when the
+// other warps' stores have drained (behind them it would hold up the step).
 constexpr int kCombThreads = 512;
 struct CombLay {
   static constexpr uint32_t XB = 0;               // two map buffers: [X_hi 32 KB | X_lo 32 KB]
@@ -1035,7 +1077,7 @@ struct CombLay {
   static constexpr uint32_t BYTES = S3 + 32768 + 1024;
 };
 static_assert(CombLay::BYTES <= 227 * 1024, "shared memory");
-constexpr uint32_t TC_COLS = 128;
+constexpr uint32_t TC_COLS = 256;   // two accumulator buffers
 
 __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillArgs p) {
   using L_ = CombLay;
@@ -1095,16 +1137,19 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillA
     store_state_row(xfer_ptr(p, k0, h, 2), true, row, col0, v);
     split_store(v);
   }
+  // buffer 0 starts at S^0 of the first segment; b then holds the next one's
   float b[32];
-  load_state_row(xfer_ptr(p, k0, h, 1), true, row, col0, b);   // S^0 of the first segment
+  load_state_row(xfer_ptr(p, k0, h, 1), true, row, col0, b);
+  tc::tmem_st32(tmem + lane_base + col0, b);
+  if (steps > 1) load_state_row(xfer_ptr(p, k0 + 1, h, 1), true, row, col0, b);
+  float v[32];   // the last step's result, stored while the next step's products run
   uint32_t phase = 0;
   bool ok = true;
 #pragma unroll 1
   for (int sg = 0; sg < steps; ++sg) {
-    tc::tmem_st32(tmem + lane_base + col0, b);   // the accumulator starts at S^0 of segment sg
-    if (sg + 1 < steps) load_state_row(xfer_ptr(p, k0 + sg + 1, h, 1), true, row, col0, b);
+    const uint32_t acc = tmem + (uint32_t)(sg & 1) * 128;
     ok = tc::mbar_wait(&mb_x[sg & 1], (uint32_t)((sg >> 1) & 1), kWaitBudget);
-    if (!sync_for_mma_and(ok)) { ok = false; break; }   // also: the S parts are in place
+    if (!sync_for_mma_and(ok)) { ok = false; break; }   // also: the S parts and this accumulator are in place
     ++waited[sg & 1];
     if (tid == 0) {
       const uint32_t xb = sm.addr + L_::XB + (sg & 1) * L_::XB_BYTES;
@@ -1115,11 +1160,21 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillA
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-          tc::mma_bf16(tmem, tc::sdesc_at(D_K, sm.addr + a_of[pass] + kb * 16384 + ks),
+          tc::mma_bf16(acc, tc::sdesc_at(D_K, sm.addr + a_of[pass] + kb * 16384 + ks),
                        tc::sdesc_at(D_MN_KQ, xb + b_of[pass] + k * 2048), ID_MN_B, 1u);
         }
       tc::mma_commit(&mb_mma);
     }
+    // meanwhile: the last step's result out, the next step's S^0 into the other buffer
+    // (whose previous products were read back last step)
+    auto hand_off = [&](int done) {   // results of steps < done are out
+      if (done > 0) store_state_row(xfer_ptr(p, k0 + done - 1, h, 1), true, row, col0, v);
+      if (sg + 1 < steps) {
+        tc::tmem_st32(tmem + (uint32_t)((sg + 1) & 1) * 128 + lane_base + col0, b);
+        if (sg + 2 < steps) load_state_row(xfer_ptr(p, k0 + sg + 2, h, 1), true, row, col0, b);
+      }
+    };
+    if (warp != 0) hand_off(sg);
     ok = tc::mbar_wait(&mb_mma, phase, kWaitBudget);
     phase ^= 1u;
     if (!__syncthreads_and(ok)) { ok = false; break; }
@@ -1130,11 +1185,11 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillA
                                L_::XB_BYTES, &mb_x[sg & 1]);
       ++issued[sg & 1];
     }
-    float v[32];
-    tc::tmem_ld32(tmem + lane_base + col0, v);
-    split_store(v);   // the next step's operands first; the global stores drain meanwhile
-    store_state_row(xfer_ptr(p, k0 + sg, h, 1), true, row, col0, v);
+    tc::tmem_ld32(acc + lane_base + col0, v);
+    split_store(v);   // the next step's operands
+    if (warp == 0) hand_off(sg + 1);
   }
+  if (ok && steps > 0 && warp != 0) store_state_row(xfer_ptr(p, k0 + steps - 1, h, 1), true, row, col0, v);
   if (!ok) {
     if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
     // the map copies this CTA started must land (bounded) before its smem goes away
