@@ -69,7 +69,7 @@ struct Lay {
   static constexpr uint32_t VN = 81920;    // Vn^T [d_v][t]
   static constexpr uint32_t VNS = 98304;   // Vn^T diag(e^{gamma_C - gamma}) [d_v][t]
   static constexpr uint32_t KQ16 = VN;     // fp16 copy of KQ for the Gram MMA (dead before Vn^T is written)
-  static constexpr uint32_t WN = 114688;   // -W [t][d_k], K blocks 8 KB apart
+  static constexpr uint32_t WN = 114688;   // -W [d_k][t] (read MN-major)
   static constexpr uint32_t TB = 131072;   // T diag(beta) [t][s]
   static constexpr uint32_t TW = 139264;   // T diag(beta e^gamma) [t][s]
   static constexpr uint32_t P = 147456;    // P [t][s]
@@ -415,18 +415,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!wait_mma()) { aborted = true; break; }
 
-    // ---- -W tile [t][d_k] from W^T (lane = d_k index) ----
+    // ---- -W tile [d_k][t] from W^T (lane = d_k index: 32 contiguous bytes a thread) ----
     {
       float v[16];
       tc::tmem_ld16(tmem + lane_base + TM_W + part * 16, v);
-      uint8_t* wn = sm.base + M::WN;
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {   // two tokens per conversion
-        const int t = part * 16 + i;
-        const uint32_t w2 = pack_bf16x2(-v[i], -v[i + 1]);
-        *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(t, row, 8192)) = (uint16_t)(w2 & 0xffffu);
-        *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(t + 1, row, 8192)) = (uint16_t)(w2 >> 16);
-      }
+      for (int i = 0; i < 16; ++i) v[i] = -v[i];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) store_bf16x8(sm.base + M::WN, tc::sw128_off(row, part * 16 + 8 * m, 0), v + 8 * m);
     }
     sync_for_mma();
 
@@ -436,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 8; ++k) {
         const uint32_t kb = k >> 2, ks = (k & 3) * 32;
         tc::mma_bf16(tmem + TM_U, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
-                     tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
+                     tc::sdesc_at(D_MN_W, sm.addr + M::WN + k * 2048), ID_KMN, 1u);
       }
       tc::mma_commit(&mbar);
     }

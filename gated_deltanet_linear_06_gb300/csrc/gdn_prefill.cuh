@@ -18,10 +18,14 @@ constexpr int LDO = 128;   // fp32 row stride of the O staging [64][LDO]
 constexpr uint64_t D_K = tc::sdesc_sw128(16, 1024);         // K-major tiles
 constexpr uint64_t D_MN_KQ = tc::sdesc_sw128(16384, 1024);  // K^ of a [K^ | Q^] tile read MN-major
 constexpr uint64_t D_MN_V = tc::sdesc_sw128(8192, 1024);    // a [64][128] tile (blocks 8 KB apart) read MN-major
+// -W stored [d_k][t]: 128 rows of one 64-column atom, read MN-major as the B
+// operand (N = t); a K = 16 step advances 16 rows (2 KB)
+constexpr uint64_t D_MN_W = tc::sdesc_sw128(8192, 1024);
 constexpr uint32_t ID_KK = tc::idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_GRAM = tc::idesc_f16(128, 64, 0, 0);
 constexpr uint32_t ID_MN_A = tc::idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_MN_B = tc::idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t ID_KMN = tc::idesc_bf16(128, 64, 0, 1);   // A K-major, B MN-major, N = 64
 
 constexpr long long kWaitBudget = 1LL << 31;  // clock cycles (~1 s) before a wait gives up
 
@@ -31,7 +35,7 @@ constexpr long long kWaitBudget = 1LL << 31;  // clock cycles (~1 s) before a wa
 // Per (chunk, key head):   bf16 [K^ | Q^] tile, 64-column blocks 16 KB apart.
 constexpr uint32_t kRecKQ = 32768;
 // Per (chunk, value head):
-constexpr uint32_t kRecWN = 0;         // -W [t][d_k] bf16, blocks 8 KB apart
+constexpr uint32_t kRecWN = 0;         // -W [d_k][t] bf16 (one 64-column atom)
 constexpr uint32_t kRecVH = 16384;     // V^ [t][d_v] bf16 (conv + SiLU), blocks 8 KB apart
 constexpr uint32_t kRecTB = 32768;     // T diag(beta) [t][s] bf16
 constexpr uint32_t kRecP = 40960;      // P [t][s] bf16

@@ -50,7 +50,7 @@ struct PrepLay {
   static constexpr uint32_t BYTES = GATE + kMaxG * 3 * 64 * 4 + 1024;   // + slack to align the base
   // A head group's area: the solve's A and T (fp32, 16 KB each) -- with the
   // bf16 P tile over T's first 8 KB until the solve writes T --, then
-  // T diag(beta e^gamma) over A, then -W [t][d_k] over A
+  // T diag(beta e^gamma) over A, then -W [d_k][t] over A
   __host__ __device__ static constexpr uint32_t area(int grp) { return grp == 0 ? KQ16 : RAW; }
 };
 static_assert(PrepLay::KQ16 + 2 * UT_BYTES <= PrepLay::RAW, "head group 0's A and T overlap the raw staging");
@@ -87,8 +87,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   using L_ = PrepLay;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mbar;       // MMA completion
-  __shared__ __align__(8) uint64_t mbar_raw;   // staged raw rows landed
+  __shared__ __align__(8) uint64_t mbar_raw;   // staged raw q | k rows landed
+  __shared__ __align__(8) uint64_t mb_rv[2];   // a staging block's raw v rows landed
   __shared__ __align__(8) uint64_t mb_w[2];    // a head group's W product done
+  __shared__ int rv_read[2];                   // warps done reading a staging block (cumulative)
+  __shared__ int rv_issued[2];                 // v copies issued into a staging block
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -108,8 +111,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   if (tid == 0) {
     tc::mbar_init(&mbar, 1);
     tc::mbar_init(&mbar_raw, 1);
-    tc::mbar_init(&mb_w[0], 1);
-    tc::mbar_init(&mb_w[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&mb_rv[i], 1);
+      tc::mbar_init(&mb_w[i], 1);
+      rv_read[i] = 0;
+      rv_issued[i] = 0;
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base_s, TP_COLS);
@@ -142,6 +149,30 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       raw_pending = false;
     }
     return ok_all;
+  };
+  // The two staging blocks take raw v rows as soon as the rows before them are
+  // read: block b holds value head 2r + b in round r.  The last of the eight
+  // warps to finish reading a block (its release number `rel`, counted from 0)
+  // issues the refill with value head g, if the key head has one.
+  auto release_blk = [&](int blk, int g, int rel) {
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      if (atomicAdd(&rv_read[blk], 1) == (kPrepThreads / 32) * (rel + 1) - 1 && g < G) {
+        __threadfence_block();
+        tc::fence_proxy_async();
+        mbar_expect_tx(&mb_rv[blk], RAW_BLK);
+        tma_load_2d(sm.base + L_::RAW + blk * RAW_BLK, &tm_qkv, 2 * Cq + (kh * G + g) * kD, y_raw, &mb_rv[blk]);
+        ++rv_issued[blk];
+      }
+    }
+  };
+  uint32_t rv_waited0 = 0, rv_waited1 = 0;   // the same on every thread
+  auto wait_rv = [&](int blk) -> bool {
+    uint32_t& w = blk == 0 ? rv_waited0 : rv_waited1;
+    const bool all = __syncthreads_and(tc::mbar_wait(&mb_rv[blk], w & 1u, kWaitBudget));
+    if (all) ++w;
+    return all;
   };
   bool ok = true;
   // this lane's q and k conv weights, in flight while the gates run
@@ -217,6 +248,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
           store_f16x4(sm.base + L_::KQ16, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
         }
       }
+      release_blk(blk, blk, 0);   // q's block takes value head 0, k's value head 1
     }
   }
   sync_for_mma();   // also: the raw q | k rows are read
@@ -234,21 +266,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 
   // ---- conv + SiLU of v, two value heads at a time, straight into their records ----
 #pragma unroll 1
-  for (int g0 = 0; g0 < G && ok; g0 += 2) {
+  for (int g0 = 0, rel = 1; g0 < G && ok; g0 += 2, ++rel) {
     const int nv = min(2, G - g0);
-    // this lane's conv weights of the two heads, in flight while their rows land
+    // this lane's conv weights of the two heads
     const ConvW4 cw_v[2] = {conv_weights_load(p.conv_w, 2 * Cq + (kh * G + g0) * kD + 4 * lane),
                             conv_weights_load(p.conv_w, 2 * Cq + (kh * G + g0 + nv - 1) * kD + 4 * lane)};
-    if (tid == 32) {
-      mbar_expect_tx(&mbar_raw, nv * RAW_BLK);
-      for (int i = 0; i < nv; ++i)
-        tma_load_2d(sm.base + L_::RAW + i * RAW_BLK, &tm_qkv, 2 * Cq + (kh * G + g0 + i) * kD, y_raw, &mbar_raw);
-    }
-    raw_pending = true;
-    if (!wait_raw()) { ok = false; break; }
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       if (i >= nv) break;
+      if (!wait_rv(i)) { ok = false; break; }
       const int h = kh * G + g0 + i;
       const int ch = 2 * Cq + h * kD + 4 * lane;
       float w[kConvW][4];
@@ -263,8 +289,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         for (int q = 0; q < 4; ++q)
           store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
       }
+      release_blk(i, g0 + 2 + i, rel);
     }
-    __syncthreads();   // the raw v rows are read
   }
   if (ok && !wait_mma()) ok = false;   // the Gram product (and KQ16 is free)
 
@@ -380,17 +406,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       tc::fence_after_sync();
       if (!gok) break;
 
-      // ---- -W tile [t][d_k] (over T diag(beta e^gamma), which the MMA has consumed) ----
+      // ---- -W tile [d_k][t] (over T diag(beta e^gamma), which the MMA has consumed):
+      //      a thread's TMEM lane is its d_k row, so each writes 64 contiguous bytes ----
 #pragma unroll 1
       for (int hf = 0; hf < 2; ++hf) {
         float v[32];
         tc::tmem_ld32(tm_w + lane_base + 32 * hf, v);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {   // two tokens per conversion
-          const uint32_t w2 = pack_bf16x2(-v[i], -v[i + 1]);
-          *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(32 * hf + i, row, 8192)) = (uint16_t)(w2 & 0xffffu);
-          *reinterpret_cast<uint16_t*>(wn + tc::sw128_off(32 * hf + i + 1, row, 8192)) = (uint16_t)(w2 >> 16);
-        }
+        for (int i = 0; i < 32; ++i) v[i] = -v[i];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) store_bf16x8(wn, tc::sw128_off(row, 32 * hf + 8 * m, 0), v + 8 * m);
       }
       tc::fence_proxy_async();
       group_sync<128>(bar);
@@ -409,6 +434,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   }
   // a raw copy still in flight after a time-out must land before the shared memory goes away
   if (raw_pending) tc::mbar_wait(&mbar_raw, raw_phase, kWaitBudget);
+  if ((uint32_t)rv_issued[0] > rv_waited0) tc::mbar_wait(&mb_rv[0], rv_waited0 & 1u, kWaitBudget);
+  if ((uint32_t)rv_issued[1] > rv_waited1) tc::mbar_wait(&mb_rv[1], rv_waited1 & 1u, kWaitBudget);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TP_COLS);
@@ -575,7 +602,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         for (int k = 0; k < 8; ++k) {
           const uint32_t kb = k >> 2, ks = (k & 3) * 32;
           tc::mma_bf16(tmem + TS_U, tc::sdesc_at(D_K, sm.addr + M::S + kb * 16384 + ks),
-                       tc::sdesc_at(D_K, sm.addr + M::WN + kb * 8192 + ks), ID_KK, 1u);
+                       tc::sdesc_at(D_MN_W, sm.addr + M::WN + k * 2048), ID_KMN, 1u);
         }
         tc::mma_commit(&mb_b1);
         // O1 = S0 Q^T into its buffer, which the workers read at chunk j - 2 (the
@@ -949,7 +976,7 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
       for (int k = 0; k < 8; ++k) {
         const uint32_t kb = k >> 2, ks = (k & 3) * 32;
         tc::mma_bf16(tmem + TX_V, tc::sdesc_at(D_K, sm.addr + L_::ST + kb * 16384 + ks),
-                     tc::sdesc_at(D_K, sm.addr + L_::WN + kb * 8192 + ks), ID_KK, track_x ? (k > 0) : 1u);
+                     tc::sdesc_at(D_MN_W, sm.addr + L_::WN + k * 2048), ID_KMN, track_x ? (k > 0) : 1u);
       }
       tc::mma_commit(&mb_mma);
     }
