@@ -25,8 +25,10 @@
  * multiplies the current token and w[c][0] the oldest; there is no conv bias.
  *
  * Conventions for every call:
- *   - The caller owns all memory.  The library never allocates, frees or
- *     synchronises (gdn_read_device_status is the one call that waits).
+ *   - The caller owns all memory.  The library never allocates or frees
+ *     device memory and never synchronises (gdn_read_device_status is the one
+ *     call that waits).  The only resources it creates are, once per device,
+ *     the side streams and events of gdn_prefill's head groups (below).
  *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
  *     void*; NULL = the legacy default stream).  The returned status covers
  *     host-side validation and the launch only.  Device-side checks
@@ -124,6 +126,16 @@ size_t gdn_workspace_bytes(const gdn_dims* dims, int n_seqs, long long total_tok
  *              by the call itself.
  * Empty sequences are allowed and leave their states unchanged.  n_seqs = 0
  * or total_tokens = 0 launches nothing and returns GDN_OK.
+ *
+ * Streams: when some sequence is split into segments (few sequences, so one
+ * CTA per (sequence, value head) would leave the GPU short) and h_k is a
+ * multiple of 4, the call runs as 4 groups of key heads: the first on `stream`,
+ * the others on side streams of the library that wait for `stream` through an
+ * event and that `stream` waits for again before the call's last kernel.  Work
+ * enqueued on `stream` afterwards therefore sees the call complete, as with a
+ * single-stream call; it also works under stream capture.  Concurrent calls
+ * on one device from several host threads share the side streams (and are
+ * ordered on them).
  */
 gdn_status gdn_prefill(const gdn_dims* dims, const void* qkv, const void* z,
                        const void* a, const void* b, const float* A_log,

@@ -236,3 +236,42 @@ def test_prefill_writes_every_output_and_is_deterministic():
     assert not torch.isnan(a[0].float()).any()
     for x, y in zip(a[:3], b[:3]):
         assert torch.equal(x, y)
+
+
+def test_prefill_cuda_graph_replay_is_bitwise_eager():
+    # a segmented call -- its head groups fork from the caller's stream to the
+    # library's side streams and join back -- captured into a CUDA graph and
+    # replayed twice gives the eager call's output and states bit for bit
+    lengths = [2100, 30]
+    params, tok, st = _inputs(SH, lengths, 18, ssm_std=0.3, conv_std=1.0)
+    e_out, e_conv, e_ssm, status = _run(SH, lengths, params, tok, st)
+    assert status == 0
+    dims = dims_of(SH)
+    T = sum(lengths)
+    pd, td = to_dev(params), to_dev(tok)
+    cu = gi.cu_seqlens(lengths).to(DEV)
+    conv0, ssm0 = st["conv_state"].to(DEV), st["ssm_state"].to(DEV)
+    conv, ssm = conv0.clone(), ssm0.clone()
+    out = torch.empty(T, SH.h_v, SH.d_v, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(gdn.gdn_workspace_bytes(dims, len(lengths), T), dtype=torch.uint8, device=DEV)
+
+    def call():
+        gdn.gdn_prefill(dims, td["qkv"], td["z"], td["a"], td["b"], pd["A_log"], pd["dt_bias"],
+                        pd["conv_w"], pd["norm_w"], cu, conv, ssm, out, ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):   # warm-up off the default stream, as capture wants
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for _ in range(2):
+        conv.copy_(conv0)
+        ssm.copy_(ssm0)
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gdn.gdn_read_device_status(ws) == 0
+        assert torch.equal(out, e_out) and torch.equal(conv, e_conv) and torch.equal(ssm, e_ssm)
