@@ -11,7 +11,7 @@
 namespace gdn {
 
 constexpr int C = kChunk;
-constexpr int kSegTokens = 1024;   // segment length when long sequences are split
+constexpr int kSegTokens = 1024;   // shortest segment a long sequence is split into (sizes the workspace)
 constexpr int LDO = 128;   // fp32 row stride of the O staging [64][LDO]
 
 // ---- tcgen05 operand and instruction descriptors ----
