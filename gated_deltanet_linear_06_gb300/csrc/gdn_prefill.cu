@@ -726,8 +726,10 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 // heads), each on its own stream: every head's passes are independent of the
 // other heads', so one group's combine pass -- a chain of dependent steps on
 // one CTA per head -- and the passes' last partial waves overlap other groups'
-// work.  (Stream priorities, to run the first group ahead, measured slower: a
-// pending high-priority combine CTA needs a whole SM and holds back the rest.)
+// work.  (Measured slower: stream priorities to run the first group ahead -- a
+// pending high-priority combine CTA needs a whole SM and holds back the rest --
+// and chaining the groups' prep passes so each group's scans overlap the next
+// group's prep, 1.14 -> 1.28 ms at 32K tokens.)
 // The first group runs on the caller's stream, the others on side streams, per
 // device, created on first use and kept for the life of the process; the
 // caller's stream forks to them through one event and joins back through one

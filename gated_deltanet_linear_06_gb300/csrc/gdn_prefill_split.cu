@@ -424,13 +424,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         bulk_commit();
       }
     }
-    if (gtid == 0) bulk_wait_all();   // this group's records are written before its smem goes away
+    // this group's record copies have read their shared memory before it goes away
+    // (their global writes complete with the grid, before any later kernel reads them)
+    if (gtid == 0) bulk_wait_read();
     ok = __syncthreads_and(gok) && ok;
   }
 
   if (tid == 0) {
     if (!ok) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
-    bulk_wait_all();   // the KQ record is written before this CTA's shared memory goes away
+    bulk_wait_read();   // the KQ record copy has read this CTA's shared memory
   }
   // a raw copy still in flight after a time-out must land before the shared memory goes away
   if (raw_pending) tc::mbar_wait(&mbar_raw, raw_phase, kWaitBudget);
@@ -845,22 +847,29 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 // ============================== transfer pass ==============================
 
 // The transfer pass as two independent tracks per (non-last segment, value
-// head), one CTA each, so two fit on an SM and one's tensor-core batches
-// overlap the other's conversions:
+// head), one CTA each, so two fit on an SM:
 //   track S: S from 0 with the real inputs   -> the segment's end state S_end(0)
 //   track X: X from the identity with v = 0   -> the segment's map X
 // Per chunk, track S: U = V^T (T diag beta)^T, Vn^T = U + S (-W)^T, S <-
 // e^{gamma_C} S + (Vn^T diag(e^{gamma_C - gamma})) K^; track X the same with
-// v = 0 (no U).  K^ is read only by the second batch, so its single buffer
-// refills a chunk ahead.
-constexpr int kXferThreads = 256;   // 8 warps: 2 per TMEM lane quarter
+// v = 0 (no U).
+//
+// Warp-specialised like the output pass: 8 worker warps make the Vn^T and state
+// tiles from the accumulators, one warp issues the tensor-core products and one
+// the bulk copies; they meet on mbarriers.  The chain per chunk is [S (-W)^T] ->
+// Vn^T tile -> [state update] -> state tile; U of the next chunk, which needs
+// only its records, is issued while the state tile is made.  Each wait is for a
+// completion whose successor needs something issued only after the wait, so a
+// barrier is never two phases on.
+constexpr int kXferWorkers = 256;                 // 8 warps: 2 per TMEM lane quarter
+constexpr int kXferThreads = kXferWorkers + 64;   // + the MMA warp and the copy warp
 struct XferLay {
   static constexpr uint32_t ST = 0;          // the tracked state, bf16 [128][128], K blocks 16 KB apart
   static constexpr uint32_t KH = 32768;      // K^ [K^ kb0 | K^ kb1]
   static constexpr uint32_t WN = 49152;      // -W | V^ | T diag(beta) (track X: -W only)
   static constexpr uint32_t VH = WN + kRecVH;
   static constexpr uint32_t TB = WN + kRecTB;
-  static constexpr uint32_t GT = WN + kRecP; // two gate buffers of 512 B
+  static constexpr uint32_t GT = WN + kRecP; // two gate buffers of 512 B (chunk j in buffer j & 1)
   static constexpr uint32_t VN = GT + 1024;  // Vn^T diag(e^{gamma_C - gamma}) [d_v][t]
   static constexpr uint32_t BYTES = VN + 16384 + 1024;
 };
@@ -871,7 +880,9 @@ constexpr uint32_t TX_ST = 0, TX_V = 128, TX_COLS = 256;   // TMEM: the state, i
 __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs p) {
   using L_ = XferLay;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t mb_mma, mb_k, mb_a, mb_g;
+  __shared__ __align__(8) uint64_t mb_k, mb_a, mb_g[2];   // copies landed
+  __shared__ __align__(8) uint64_t mb_b1, mb_b2, mb_fin;  // products done (mb_fin: after a time-out)
+  __shared__ __align__(8) uint64_t mb_vn, mb_s;           // worker warps done (8 arrivals)
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -886,10 +897,15 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
 
   const Smem sm = smem_aligned(smem_raw);
   if (tid == 0) {
-    tc::mbar_init(&mb_mma, 1);
     tc::mbar_init(&mb_k, 1);
     tc::mbar_init(&mb_a, 1);
-    tc::mbar_init(&mb_g, 1);
+    tc::mbar_init(&mb_g[0], 1);
+    tc::mbar_init(&mb_g[1], 1);
+    tc::mbar_init(&mb_b1, 1);
+    tc::mbar_init(&mb_b2, 1);
+    tc::mbar_init(&mb_fin, 1);
+    tc::mbar_init(&mb_vn, kXferWorkers / 32);
+    tc::mbar_init(&mb_s, kXferWorkers / 32);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tc::tmem_alloc(&tmem_base_s, TX_COLS);
@@ -897,174 +913,199 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base_s;
-  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
-  const int hf = warp >> 2;                 // which half of the lane quarter's columns
-
+  auto wt = [&](uint64_t* mb, uint32_t k) -> bool {   // the k-th completion of mb (parity k & 1)
+    return tc::mbar_wait(mb, k & 1u, kWaitBudget);
+  };
   auto rec_kq = [&](int j) { return p.rec_kq + ((size_t)(sg.c0 + j) * p.h_k + kh) * kRecKQ; };
   auto rec_v = [&](int j) { return p.rec_v + ((size_t)(sg.c0 + j) * p.h_v + h) * kRecV; };
-  // record loads, issued by tid 32 under conditions every thread evaluates alike
-  struct Pipe {
-    uint32_t issued, waited;
-  };
-  Pipe q_k = {0, 0}, q_a = {0, 0}, q_g = {0, 0};
-  auto pwait = [&](uint64_t* mb, Pipe& q) -> bool {
-    const bool r = tc::mbar_wait(mb, q.waited & 1u, kWaitBudget);
-    if (r) ++q.waited;
-    return r;
-  };
-  auto load_k = [&](int j) {   // the K^ halves of the [K^ | Q^] record
-    if (tid == 32) {
-      mbar_expect_tx(&mb_k, 16384);
-      bulk_copy(sm.base + L_::KH, rec_kq(j), 8192, &mb_k);
-      bulk_copy(sm.base + L_::KH + 8192, rec_kq(j) + 16384, 8192, &mb_k);
-    }
-    ++q_k.issued;
-  };
-  auto load_a = [&](int j) {   // track S: -W | V^ | T diag(beta); track X: -W
-    if (tid == 32) bulk_load(sm.base + L_::WN, rec_v(j), track_x ? 16384u : kRecP, &mb_a);
-    ++q_a.issued;
-  };
-  auto load_g = [&](int j) {
-    if (tid == 32) bulk_load(sm.base + L_::GT + (j & 1) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g);
-    ++q_g.issued;
-  };
-  load_g(0);
-  load_k(0);
-  load_a(0);
+  bool ok = true;
 
-  // the initial state -- S = 0 or X = I -- as the bf16 operand tile, and in TMEM
-  // scaled by the first chunk's total decay
-  bool aborted = !__syncthreads_and(pwait(&mb_g, q_g));
-  {
-    const float dC0 = sm.f32(L_::GT)[C - 1];
-#pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int col0 = 64 * hf + 32 * c2;
-      float v[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = (track_x && col0 + i == row) ? 1.0f : 0.0f;
-#pragma unroll
-      for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + L_::ST, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= dC0;
-      tc::tmem_st32(tmem + lane_base + TX_ST + col0, v);
-    }
-  }
-  if (!aborted) aborted = !sync_for_mma_and(pwait(&mb_a, q_a));   // (and the state tile is in place)
-
-  uint32_t phase = 0;
-  auto wait_mma = [&](bool more) -> bool {   // ANDs in `more`, the thread's other waits
-    const bool ok = tc::mbar_wait(&mb_mma, phase, kWaitBudget) && more;
-    phase ^= 1u;
-    const bool all_ok = __syncthreads_and(ok);
-    tc::fence_after_sync();
-    return all_ok;
-  };
-  for (int j = 0; j < nch && !aborted; ++j) {
-    const float* egc = sm.f32(L_::GT + (j & 1) * 512) + 64;
-    if (j + 1 < nch) load_g(j + 1);
-    // ---- batch 1: [U = V^T (T diag beta)^T,] Vn^T = U + S (-W)^T   (track X: X (-W)^T) ----
-    if (tid == 0) {
-      if (!track_x) {
+  if (warp == kXferWorkers / 32) {
+    // ================= the MMA warp (one lane) =================
+    if (lane == 0) {
+      bool issued = false;
+      auto issue_u = [&](int j) -> bool {   // track S: U = V^T (T diag beta)^T into TX_V
+        if (!wt(&mb_a, j)) return false;
+        tc::fence_after_sync();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           tc::mma_bf16(tmem + TX_V, tc::sdesc_at(D_MN_V, sm.addr + L_::VH + k * 2048),
                        tc::sdesc_at(D_K, sm.addr + L_::TB + k * 32), ID_MN_A, k > 0);
+        issued = true;
+        return true;
+      };
+      if (!track_x) ok = issue_u(0);
+      for (int j = 0; j < nch && ok; ++j) {
+        // the workers' state tile (track X: and this chunk's -W)
+        if (!(wt(&mb_s, j) && (!track_x || wt(&mb_a, j)))) { ok = false; break; }
+        tc::fence_after_sync();
+        // [Vn^T = U + S (-W)^T]   (track X: X (-W)^T)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t kb = k >> 2, ks = (k & 3) * 32;
+          tc::mma_bf16(tmem + TX_V, tc::sdesc_at(D_K, sm.addr + L_::ST + kb * 16384 + ks),
+                       tc::sdesc_at(D_MN_W, sm.addr + L_::WN + k * 2048), ID_KMN, track_x ? (k > 0) : 1u);
+        }
+        issued = true;
+        tc::mma_commit(&mb_b1);
+        // the workers' Vn^T tile, and K^
+        if (!(wt(&mb_vn, j) && wt(&mb_k, j))) { ok = false; break; }
+        tc::fence_after_sync();
+        // [state += Vn^T diag(e^{gamma_C - gamma}) K^]
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc::mma_bf16(tmem + TX_ST, tc::sdesc_at(D_K, sm.addr + L_::VN + k * 32),
+                       tc::sdesc_at(D_MN_V, sm.addr + L_::KH + k * 2048), ID_MN_B, 1u);
+        tc::mma_commit(&mb_b2);
+        // the next chunk's U (TX_V was read for the Vn^T tile)
+        if (!track_x && j + 1 < nch && !issue_u(j + 1)) { ok = false; break; }
       }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t kb = k >> 2, ks = (k & 3) * 32;
-        tc::mma_bf16(tmem + TX_V, tc::sdesc_at(D_K, sm.addr + L_::ST + kb * 16384 + ks),
-                     tc::sdesc_at(D_MN_W, sm.addr + L_::WN + k * 2048), ID_KMN, track_x ? (k > 0) : 1u);
+      if (!ok) {
+        record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+        if (issued) {   // the products issued finish (bounded) before the tensor memory is freed
+          tc::mma_commit(&mb_fin);
+          wt(&mb_fin, 0);
+        }
       }
-      tc::mma_commit(&mb_mma);
     }
-    if (!wait_mma(true)) { aborted = true; break; }
-    if (j + 1 < nch) load_a(j + 1);   // batch 1 has finished with -W | V^ | T diag(beta)
-
-    // ---- Vn^T diag(e^{gamma_C - gamma}) tile, row = d_v index ----
-    {
-      float v[32];
-      tc::tmem_ld32(tmem + lane_base + TX_V + 32 * hf, v);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] *= egc[32 * hf + i];
-#pragma unroll
-      for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + L_::VN, tc::sw128_off(row, 32 * hf + 8 * m, 0), v + 8 * m);
+    __syncwarp();
+  } else if (warp == kXferWorkers / 32 + 1) {
+    // ================= the copy warp (one lane) =================
+    // -W | V^ | T diag(beta) refills after [S (-W)^T] (b1), K^ after the state
+    // update (b2), which also follows the Vn^T tile that last read the gates two
+    // chunks back.
+    if (lane == 0) {
+      uint32_t i_k = 0, i_a = 0, i_g0 = 0, i_g1 = 0;   // copies issued
+      auto load_k = [&](int j) {   // the K^ halves of the [K^ | Q^] record
+        mbar_expect_tx(&mb_k, 16384);
+        bulk_copy(sm.base + L_::KH, rec_kq(j), 8192, &mb_k);
+        bulk_copy(sm.base + L_::KH + 8192, rec_kq(j) + 16384, 8192, &mb_k);
+        ++i_k;
+      };
+      auto load_a = [&](int j) {   // track S: -W | V^ | T diag(beta); track X: -W
+        bulk_load(sm.base + L_::WN, rec_v(j), track_x ? 16384u : kRecP, &mb_a);
+        ++i_a;
+      };
+      auto load_g = [&](int j) {
+        bulk_load(sm.base + L_::GT + (j & 1) * 512, rec_v(j) + kRecGate, kRecGateBytes, &mb_g[j & 1]);
+        if (j & 1) ++i_g1; else ++i_g0;
+      };
+      load_g(0);
+      if (nch > 1) load_g(1);
+      load_k(0);
+      load_a(0);
+      for (int j = 0; j + 1 < nch; ++j) {
+        if (!wt(&mb_b1, j)) { ok = false; break; }
+        load_a(j + 1);
+        if (!wt(&mb_b2, j)) { ok = false; break; }
+        load_k(j + 1);
+        if (j + 2 < nch) load_g(j + 2);
+      }
+      if (!ok) {
+        record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+        // the copies this CTA started land (bounded) before its shared memory goes away
+        auto drain = [&](uint64_t* mb, uint32_t n_issued) {
+          if (n_issued > 0) wt(mb, n_issued - 1);
+        };
+        drain(&mb_k, i_k);
+        drain(&mb_a, i_a);
+        drain(&mb_g[0], i_g0);
+        drain(&mb_g[1], i_g1);
+      }
     }
-    if (!sync_for_mma_and(pwait(&mb_k, q_k))) { aborted = true; break; }
-
-    // ---- batch 2: state += Vn^T diag(e^{gamma_C - gamma}) K^ ----
-    if (tid == 0) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        tc::mma_bf16(tmem + TX_ST, tc::sdesc_at(D_K, sm.addr + L_::VN + k * 32),
-                     tc::sdesc_at(D_MN_V, sm.addr + L_::KH + k * 2048), ID_MN_B, 1u);
-      tc::mma_commit(&mb_mma);
-    }
-    if (!wait_mma(j + 1 >= nch || pwait(&mb_g, q_g))) { aborted = true; break; }
-    if (j + 1 < nch) load_k(j + 1);   // batch 2 has finished with K^
-
-    // ---- the new state -> bf16 operand tile, and in TMEM scaled by the next chunk's decay ----
-    {
-      const float dC = j + 1 < nch ? sm.f32(L_::GT + ((j + 1) & 1) * 512)[C - 1] : 1.0f;
+    __syncwarp();
+  } else {
+    // ================= the worker warps =================
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    const int row = 32 * (warp & 3) + lane;   // TMEM lane this thread reads
+    const int hf = warp >> 2;                 // which half of the lane quarter's columns
+    // the initial state -- S = 0 or X = I -- as the bf16 operand tile, and in TMEM
+    // scaled by the first chunk's total decay
+    ok = wt(&mb_g[0], 0);
+    if (ok) {
+      const float dC0 = sm.f32(L_::GT)[C - 1];
 #pragma unroll
       for (int c2 = 0; c2 < 2; ++c2) {
         const int col0 = 64 * hf + 32 * c2;
         float v[32];
-        const uint32_t ta = tmem + lane_base + TX_ST + col0;
-        tc::tmem_ld32(ta, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = (track_x && col0 + i == row) ? 1.0f : 0.0f;
 #pragma unroll
         for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + L_::ST, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
-        if (j + 1 < nch) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= dC0;
+        tc::tmem_st32(tmem + lane_base + TX_ST + col0, v);
+      }
+      warp_signal(&mb_s, lane);
+    }
+    for (int j = 0; j < nch && ok; ++j) {
+      const float* egc = sm.f32(L_::GT + (j & 1) * 512) + 64;
+      // ---- Vn^T diag(e^{gamma_C - gamma}) tile, row = d_v index ----
+      if (!(wt(&mb_b1, j) && wt(&mb_g[j & 1], j >> 1))) { ok = false; break; }
+      tc::fence_after_sync();
+      {
+        float v[32];
+        tc::tmem_ld32(tmem + lane_base + TX_V + 32 * hf, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= egc[32 * hf + i];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + L_::VN, tc::sw128_off(row, 32 * hf + 8 * m, 0), v + 8 * m);
+      }
+      warp_signal(&mb_vn, lane);
+      // ---- the new state -> bf16 operand tile, and in TMEM scaled by the next chunk's
+      //      decay (after the last chunk the accumulator is read out below) ----
+      if (!wt(&mb_b2, j)) { ok = false; break; }
+      tc::fence_after_sync();
+      if (j + 1 < nch) {
+        if (!wt(&mb_g[(j + 1) & 1], (j + 1) >> 1)) { ok = false; break; }
+        const float dC = sm.f32(L_::GT + ((j + 1) & 1) * 512)[C - 1];
+#pragma unroll 1
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int col0 = 64 * hf + 32 * c2;
+          float v[32];
+          const uint32_t ta = tmem + lane_base + TX_ST + col0;
+          tc::tmem_ld32(ta, v);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) store_bf16x8(sm.base + L_::ST, tc::sw128_off(row, col0 + 8 * m, 16384), v + 8 * m);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= dC;
           tc::tmem_st32(ta, v);
         }
+        warp_signal(&mb_s, lane);
       }
     }
-    if (!sync_for_mma_and(j + 1 >= nch || pwait(&mb_a, q_a))) { aborted = true; break; }
-  }
-
-  if (aborted) {
-    if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
-    // this CTA's own copies land (bounded) before its shared memory goes away
-    auto drain = [&](uint64_t* mb, Pipe& q) {
-      while (q.waited < q.issued && pwait(mb, q)) {
+    if (!ok) {
+      if (lane == 0) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
+    } else if (!track_x) {
+      // S_end(0), fp32 in tiled order
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int col0 = 64 * hf + 32 * c2;
+        float v[32];
+        tc::tmem_ld32(tmem + lane_base + TX_ST + col0, v);
+        store_state_row(xfer_ptr(p, sg.k0 + sg.sigma, h, 1), true, row, col0, v);
       }
-    };
-    drain(&mb_k, q_k);
-    drain(&mb_a, q_a);
-    drain(&mb_g, q_g);
-  } else if (!track_x) {
-    // S_end(0), fp32 in tiled order
+    } else {
+      // X as bf16 hi / lo tiles for the combine pass's tensor-core products
+      uint8_t* xt = reinterpret_cast<uint8_t*>(xfer_ptr(p, sg.k0 + sg.sigma, h, 0));
 #pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int col0 = 64 * hf + 32 * c2;
-      float v[32];
-      tc::tmem_ld32(tmem + lane_base + TX_ST + col0, v);
-      store_state_row(xfer_ptr(p, sg.k0 + sg.sigma, h, 1), true, row, col0, v);
-    }
-  } else {
-    // X as bf16 hi / lo tiles for the combine pass's tensor-core products
-    uint8_t* xt = reinterpret_cast<uint8_t*>(xfer_ptr(p, sg.k0 + sg.sigma, h, 0));
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int col0 = 64 * hf + 32 * c2;
+        float v[32], lo[32];
+        tc::tmem_ld32(tmem + lane_base + TX_ST + col0, v);
 #pragma unroll
-    for (int c2 = 0; c2 < 2; ++c2) {
-      const int col0 = 64 * hf + 32 * c2;
-      float v[32], lo[32];
-      tc::tmem_ld32(tmem + lane_base + TX_ST + col0, v);
+        for (int i = 0; i < 32; i += 2) {   // X - bf16(X), exact in fp32
+          float r0, r1;
+          round_bf16x2(v[i], v[i + 1], r0, r1);
+          lo[i] = v[i] - r0;
+          lo[i + 1] = v[i + 1] - r1;
+        }
 #pragma unroll
-      for (int i = 0; i < 32; i += 2) {   // X - bf16(X), exact in fp32
-        float r0, r1;
-        round_bf16x2(v[i], v[i + 1], r0, r1);
-        lo[i] = v[i] - r0;
-        lo[i + 1] = v[i + 1] - r1;
-      }
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const uint32_t off = tc::sw128_off(row, col0 + 8 * m, 16384);
-        store_bf16x8(xt, off, v + 8 * m);
-        store_bf16x8(xt + 32768, off, lo + 8 * m);
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t off = tc::sw128_off(row, col0 + 8 * m, 16384);
+          store_bf16x8(xt, off, v + 8 * m);
+          store_bf16x8(xt + 32768, off, lo + 8 * m);
+        }
       }
     }
   }
