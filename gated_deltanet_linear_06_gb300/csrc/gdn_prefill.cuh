@@ -88,6 +88,18 @@ __device__ __forceinline__ void store_bf16x8(uint8_t* tile, uint32_t off, const 
   *reinterpret_cast<uint4*>(tile + off) = v;
 }
 
+// The prefill's gates with the fast exp, log and divide.  softplus(x) =
+// max(x, 0) + log(1 + e^{-|x|}): __logf of 1 + e^{-|x|} is off by well under
+// 1e-6 absolute, where g = -e^{A_log} softplus(.) needs about 1e-3 relative.
+// sigmoid clamps the exponent at 80 so that the denominator stays below 2^126,
+// where the fast divide is exact to a few ulp (sigma(-80) < 2e-35 either way).
+__device__ __forceinline__ float softplus_gate(float x) {
+  return fmaxf(x, 0.0f) + __logf(1.0f + __expf(-fabsf(x)));
+}
+__device__ __forceinline__ float sigmoid_gate(float x) {
+  return __fdividef(1.0f, 1.0f + __expf(fminf(-x, 80.0f)));
+}
+
 // x where s <= t, else +0, by masking the bits: no compare-and-select, which
 // next to the exp of the decay factor measured about three times slower.
 __device__ __forceinline__ float keep_if_le(float x, int s, int t) {
@@ -196,6 +208,19 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
           "r"(tc::smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(tc::smem_u32(mbar))
       : "memory");
+}
+
+// Prefetch the box at column x, row y of a 2-D tensor map into L2 (no shared
+// memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
+// Prefetch bytes of global memory into L2 (address and size multiples of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Bulk copy global -> shared that reports its bytes to mbar (the caller posts
