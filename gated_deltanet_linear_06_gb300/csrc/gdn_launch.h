@@ -55,7 +55,6 @@ struct PrefillArgs {
   // run as several head groups): key heads kh0 .. kh0+nkh-1, value heads
   // h0 .. h0+nh-1
   int kh0, nkh, h0, nh;
-  int prep_ahead;          // prep: also prefetch into L2 the inputs of CTA blockIdx + prep_ahead
   int n_seqs, h_k, h_v;
   long long total_tokens;
   float l2_eps, rms_eps;

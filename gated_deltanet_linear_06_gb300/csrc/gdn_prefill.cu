@@ -769,7 +769,6 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
   p.nkh = p.h_k;
   p.h0 = 0;
   p.nh = p.h_v;
-  p.prep_ahead = 0;
   const ScratchLayout l = scratch_layout(p.n_seqs, p.h_k, p.h_v, p.total_tokens, allow_split);
   char* scratch = static_cast<char*>(p.scratch);
   p.seg_list = reinterpret_cast<int*>(scratch + l.seg_list);
@@ -806,7 +805,6 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
     // workspace), chosen so that the (segment, value head) units number about 1.7
     // per SM.  Measured at 32K tokens, 32 value heads, 152 SMs: 4096-token segments
     // (256 units) 1.14 ms a call; 2048: 1.19; 1024: 1.27; 8192 (128 units): 1.22.
-    p.prep_ahead = 2 * sms;   // two prep CTAs are resident per SM
     const long long per_head = std::max(1LL, (17LL * sms / 10 + p.h_v / 2) / p.h_v);
     long long seg_len = (p.total_tokens + per_head - 1) / per_head;
     seg_len = std::max<long long>((seg_len + C - 1) / C * C, kSegTokens);

@@ -210,19 +210,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
       : "memory");
 }
 
-// Prefetch the box at column x, row y of a 2-D tensor map into L2 (no shared
-// memory, no completion to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* tm, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(tm)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
-// Prefetch bytes of global memory into L2 (address and size multiples of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Bulk copy global -> shared that reports its bytes to mbar (the caller posts
 // the expected byte count); both addresses 16-byte aligned, bytes % 16 == 0.
 __device__ __forceinline__ void bulk_copy(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* mbar) {

@@ -128,29 +128,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
   const int row = 32 * quarter + lane;
   const int y_raw = start + t0 - (kConvW - 1);      // first staged row (a chunk and its halo)
-  if (tid == kPrepThreads - 32 && blockIdx.x + p.prep_ahead < gridDim.x) {
-    // the inputs of the CTA that will most likely take this slot next (a full wave
-    // on), into L2 now, so that its loads hit: its raw q | k | v boxes (only boxes
-    // wholly inside the tensor) and its a, b rows (rounded inwards to 16 bytes)
-    const int nb = blockIdx.x + p.prep_ahead;
-    const int2 ce2 = p.chunk_list[nb / p.nkh];
-    const int kh2 = p.kh0 + nb % p.nkh;
-    if (ce2.x >= 0 && ce2.x < p.n_seqs) {
-      const int s2 = p.cu_seqlens[ce2.x], L2 = min(C, p.cu_seqlens[ce2.x + 1] - s2 - ce2.y);
-      const int y2 = s2 + ce2.y - (kConvW - 1);
-      if (y2 >= 0 && y2 + RAW_BOX_ROWS <= p.total_tokens) {
-        tma_prefetch_2d(&tm_qkv, kh2 * kD, y2);
-        tma_prefetch_2d(&tm_qkv, Cq + kh2 * kD, y2);
-        for (int g = 0; g < G; ++g) tma_prefetch_2d(&tm_qkv, 2 * Cq + (kh2 * G + g) * kD, y2);
-      }
-      const size_t b0 = ((size_t)(s2 + ce2.y) * p.h_v * 2 + 15) & ~(size_t)15;
-      const size_t b1 = ((size_t)(s2 + ce2.y + L2) * p.h_v * 2) & ~(size_t)15;
-      if (b1 > b0) {
-        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.a) + b0, (uint32_t)(b1 - b0));
-        bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.b) + b0, (uint32_t)(b1 - b0));
-      }
-    }
-  }
   if (tid == 32) {   // raw q and k rows
     mbar_expect_tx(&mbar_raw, 2 * RAW_BLK);
     tma_load_2d(sm.base + L_::RAW, &tm_qkv, kh * kD, y_raw, &mbar_raw);
