@@ -726,10 +726,16 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 // heads), each on its own stream: every head's passes are independent of the
 // other heads', so one group's combine pass -- a chain of dependent steps on
 // one CTA per head -- and the passes' last partial waves overlap other groups'
-// work.  (Measured slower: stream priorities to run the first group ahead -- a
-// pending high-priority combine CTA needs a whole SM and holds back the rest --
-// and chaining the groups' prep passes so each group's scans overlap the next
-// group's prep, 1.14 -> 1.28 ms at 32K tokens.)
+// work.  A kernel timeline shows the groups' prep passes running one after
+// another and the scans after them: the dispatcher hands out pending CTAs in the
+// order their grids became eligible.  Measured slower, each time because the SMs
+// are busy in both phases and reordering only moves work around:
+//   - stream priorities to run the first group ahead (a pending high-priority
+//     combine CTA needs a whole SM and holds back the rest);
+//   - chaining the groups' prep passes, 1.14 -> 1.28 ms at 32K tokens;
+//   - the transfer scans on high-priority streams, beside the later prep passes
+//     (those slowed by about as much as they absorbed, and the last group's
+//     chain then queued behind the other groups' output scans), 1.14 -> 1.29 ms.
 // The first group runs on the caller's stream, the others on side streams, per
 // device, created on first use and kept for the life of the process; the
 // caller's stream forks to them through one event and joins back through one
