@@ -807,13 +807,28 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    // Segment length: a whole number of chunks, at least kSegTokens (which sizes the
-    // workspace), chosen so that the (segment, value head) units number about 1.7
-    // per SM.  Measured at 32K tokens, 32 value heads, 152 SMs: 4096-token segments
-    // (256 units) 1.14 ms a call; 2048: 1.19; 1024: 1.27; 8192 (128 units): 1.22.
-    const long long per_head = std::max(1LL, (17LL * sms / 10 + p.h_v / 2) / p.h_v);
-    long long seg_len = (p.total_tokens + per_head - 1) / per_head;
-    seg_len = std::max<long long>((seg_len + C - 1) / C * C, kSegTokens);
+    // Segment length L: whole chunks, at least kSegTokens (which sizes the
+    // workspace), at least two segments.  Chosen by a cost model of the scans, as
+    // if all tokens were one sequence: with s = ceil(T / L) segments of L / C
+    // chunks, the output scan runs ceil(s h_v / SMs) waves of CTAs each walking
+    // L / C chunks, the transfer scan ceil((s - 1) h_v / SMs) such waves (two
+    // tracks, two CTAs per SM), and the combine s - 1 dependent steps of about
+    // 1.5 chunk-times.  Measured at 32K tokens, 32 value heads, 152 SMs: the
+    // model's choice, 3648 tokens (9 segments), 1.10 ms a call; 4096: 1.14; 2368:
+    // 1.14; 2048: 1.19; 1024: 1.27; 8192: 1.22.
+    long long seg_len = kSegTokens;
+    double best = 1e300;
+    for (long long s = 2; s <= 64; ++s) {
+      long long L = (p.total_tokens + s - 1) / s;
+      L = std::max<long long>((L + C - 1) / C * C, kSegTokens);
+      const long long segs = (p.total_tokens + L - 1) / L;
+      const long long waves = (segs * p.h_v + sms - 1) / sms + ((segs - 1) * p.h_v + sms - 1) / sms;
+      const double cost = (double)waves * (double)(L / C) + 1.5 * (double)(segs - 1);
+      if (cost < best - 1e-9 || (cost < best + 1e-9 && L > seg_len)) {
+        best = cost;
+        seg_len = L;
+      }
+    }
     const bool segment = (long long)p.n_seqs * p.h_v < 4LL * sms && p.total_tokens > seg_len;
     p.seg_tokens = segment ? (int)seg_len : 0x40000000;
     const long long slots = segment ? p.total_tokens / seg_len : 0;   // >= the segment boundaries
