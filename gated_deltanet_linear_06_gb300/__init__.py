@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_state_bytes.argtypes = [DP]
             L.gdn_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_workspace_bytes.argtypes = [DP, ctypes.c_int, ctypes.c_longlong]
+            L.gdn_prefill_segment_tokens.restype = ctypes.c_longlong
+            L.gdn_prefill_segment_tokens.argtypes = [DP, ctypes.c_int, ctypes.c_longlong]
             L.gdn_prefill.restype = ctypes.c_int
             L.gdn_prefill.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
                 [_P] * 4 + [ctypes.c_size_t, _P]
@@ -102,6 +104,10 @@ def gdn_state_bytes(dims: Dims) -> int:
 
 def gdn_workspace_bytes(dims: Dims, n_seqs: int, total_tokens: int) -> int:
     return lib().gdn_workspace_bytes(ctypes.byref(dims), int(n_seqs), int(total_tokens))
+
+
+def gdn_prefill_segment_tokens(dims: Dims, n_seqs: int, total_tokens: int) -> int:
+    return lib().gdn_prefill_segment_tokens(ctypes.byref(dims), int(n_seqs), int(total_tokens))
 
 
 def _stream(stream) -> int | None:

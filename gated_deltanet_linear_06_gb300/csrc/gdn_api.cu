@@ -73,6 +73,15 @@ size_t gdn_workspace_bytes(const gdn_dims* d, int n_seqs, long long total_tokens
   return 256 + gdn::prefill_scratch_bytes(n_seqs, d->h_k, d->h_v, total_tokens);
 }
 
+long long gdn_prefill_segment_tokens(const gdn_dims* d, int n_seqs, long long total_tokens) {
+  if (check_dims(d) != GDN_OK || n_seqs < 0 || total_tokens < 0) return -1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return -1;
+  return gdn::prefill_segment_tokens(n_seqs, d->h_v, total_tokens, sms);
+}
+
 gdn_status gdn_prefill(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
                        const void* b, const float* A_log, const float* dt_bias,
                        const void* conv_w, const float* norm_w, const int32_t* cu_seqlens,

@@ -68,5 +68,8 @@ cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream
 cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream, bool allow_split = true);
 size_t prefill_scratch_bytes(int n_seqs, int h_k, int h_v, long long total_tokens);
 size_t prefill_scratch_bytes_unsplit(int n_seqs);
+// The segment length gdn_prefill splits long sequences into on a GPU with `sms`
+// SMs, or 0 when it does not split (a whole number of chunks, >= 1024 tokens).
+long long prefill_segment_tokens(int n_seqs, int h_v, long long total_tokens, int sms);
 
 }  // namespace gdn

@@ -693,6 +693,36 @@ size_t prefill_scratch_bytes(int n_seqs, int h_k, int h_v, long long total_token
 
 size_t prefill_scratch_bytes_unsplit(int n_seqs) { return scratch_layout(n_seqs, 0, 0, 0, false).total; }
 
+// Segment length L: whole chunks, at least kSegTokens (which sizes the
+// workspace), at least two segments, and only when one CTA per (sequence,
+// value head) would leave the GPU short (sequences x h_v < 4 x SMs) and some
+// sequence could be longer than L.  L minimises a cost model of the scans, as
+// if all tokens were one sequence: with s = ceil(T / L) segments of L / C
+// chunks, the output scan runs ceil(s h_v / SMs) waves of CTAs each walking
+// L / C chunks, the transfer scan ceil((s - 1) h_v / SMs) such waves (two
+// tracks, two CTAs per SM), and the combine s - 1 dependent steps of about 1.5
+// chunk-times.  Measured at 32K tokens, 32 value heads, 152 SMs: the model's
+// choice, 3648 tokens (9 segments), 1.10 ms a call; 4096: 1.14; 2368: 1.14;
+// 2048: 1.19; 1024: 1.27; 8192: 1.22.
+long long prefill_segment_tokens(int n_seqs, int h_v, long long total_tokens, int sms) {
+  if (n_seqs <= 0 || h_v <= 0 || sms <= 0 || (long long)n_seqs * h_v >= 4LL * sms || total_tokens <= kSegTokens)
+    return 0;
+  long long seg_len = kSegTokens;
+  double best = 1e300;
+  for (long long s = 2; s <= 64; ++s) {
+    long long L = (total_tokens + s - 1) / s;
+    L = std::max<long long>((L + C - 1) / C * C, kSegTokens);
+    const long long segs = (total_tokens + L - 1) / L;
+    const long long waves = (segs * h_v + sms - 1) / sms + ((segs - 1) * h_v + sms - 1) / sms;
+    const double cost = (double)waves * (double)(L / C) + 1.5 * (double)(segs - 1);
+    if (cost < best - 1e-9 || (cost < best + 1e-9 && L > seg_len)) {
+      best = cost;
+      seg_len = L;
+    }
+  }
+  return total_tokens > seg_len ? seg_len : 0;
+}
+
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -807,29 +837,8 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
     int dev = 0, sms = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    // Segment length L: whole chunks, at least kSegTokens (which sizes the
-    // workspace), at least two segments.  Chosen by a cost model of the scans, as
-    // if all tokens were one sequence: with s = ceil(T / L) segments of L / C
-    // chunks, the output scan runs ceil(s h_v / SMs) waves of CTAs each walking
-    // L / C chunks, the transfer scan ceil((s - 1) h_v / SMs) such waves (two
-    // tracks, two CTAs per SM), and the combine s - 1 dependent steps of about
-    // 1.5 chunk-times.  Measured at 32K tokens, 32 value heads, 152 SMs: the
-    // model's choice, 3648 tokens (9 segments), 1.10 ms a call; 4096: 1.14; 2368:
-    // 1.14; 2048: 1.19; 1024: 1.27; 8192: 1.22.
-    long long seg_len = kSegTokens;
-    double best = 1e300;
-    for (long long s = 2; s <= 64; ++s) {
-      long long L = (p.total_tokens + s - 1) / s;
-      L = std::max<long long>((L + C - 1) / C * C, kSegTokens);
-      const long long segs = (p.total_tokens + L - 1) / L;
-      const long long waves = (segs * p.h_v + sms - 1) / sms + ((segs - 1) * p.h_v + sms - 1) / sms;
-      const double cost = (double)waves * (double)(L / C) + 1.5 * (double)(segs - 1);
-      if (cost < best - 1e-9 || (cost < best + 1e-9 && L > seg_len)) {
-        best = cost;
-        seg_len = L;
-      }
-    }
-    const bool segment = (long long)p.n_seqs * p.h_v < 4LL * sms && p.total_tokens > seg_len;
+    const long long seg_len = prefill_segment_tokens(p.n_seqs, p.h_v, p.total_tokens, sms);
+    const bool segment = seg_len > 0;
     p.seg_tokens = segment ? (int)seg_len : 0x40000000;
     const long long slots = segment ? p.total_tokens / seg_len : 0;   // >= the segment boundaries
     const unsigned units = (unsigned)(slots + p.n_seqs);

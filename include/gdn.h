@@ -98,6 +98,15 @@ size_t gdn_state_bytes(const gdn_dims* dims);
  * the device status word at offset 0).  Returns 0 for invalid arguments. */
 size_t gdn_workspace_bytes(const gdn_dims* dims, int n_seqs, long long total_tokens);
 
+/* The segment length, in tokens, that gdn_prefill on the current device splits
+ * the sequences of this problem into: a multiple of the chunk (64), at least
+ * 1024, chosen from the token count, the value heads and the SM count; 0 when
+ * the call splits nothing (enough sequences to fill the GPU, or too few
+ * tokens); -1 for invalid arguments or when no device can be queried.  A
+ * chunked-prefill scheduler can use it to align its own boundaries; segments
+ * never change results beyond rounding. */
+long long gdn_prefill_segment_tokens(const gdn_dims* dims, int n_seqs, long long total_tokens);
+
 /*
  * Chunked prefill over cu_seqlens-packed variable-length sequences.
  *

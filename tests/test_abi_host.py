@@ -65,6 +65,13 @@ def test_state_bytes_matches_the_pages_state_size(L):
     assert gdn.gdn_state_bytes(gdn.make_dims(h_k=0)) == 0
 
 
+def test_prefill_segment_tokens_rejects_bad_arguments(L):
+    # argument checks come before any device query, so they hold without a GPU
+    assert gdn.gdn_prefill_segment_tokens(gdn.make_dims(d_k=64), 1, 4096) == -1
+    assert gdn.gdn_prefill_segment_tokens(gdn.make_dims(), -1, 4096) == -1
+    assert gdn.gdn_prefill_segment_tokens(gdn.make_dims(), 1, -5) == -1
+
+
 def test_workspace_bytes(L):
     d = gdn.make_dims()
     assert gdn.gdn_workspace_bytes(d, 1, 4096) >= 256

@@ -69,11 +69,17 @@ def test_prefill_varlen_ragged_short_and_empty(slow):
 
 @pytest.mark.parametrize("slow", [False, True])
 def test_prefill_segment_boundaries(slow):
-    # sequences longer than one segment (1024 tokens) are scanned in parallel
-    # segments whose start states are composed from per-segment transfer maps;
-    # lengths straddle the segment size, and the slow-decay variant makes the
-    # state carry across every boundary
-    lengths = [1024, 1025, 2115, 5, 3000]
+    # sequences longer than one segment are scanned in parallel segments whose
+    # start states are composed from per-segment transfer maps.  The lengths
+    # straddle the segment length this call uses (exactly one segment, one and a
+    # token, two and a ragged tail); the slow-decay variant makes the state carry
+    # across every boundary
+    T, n = 16384, 5
+    L = gdn.gdn_prefill_segment_tokens(dims_of(SH), n, T)
+    assert L >= 1024 and L % 64 == 0
+    lengths = [L, L + 1, 2 * L + 67, 5]
+    lengths.append(T - sum(lengths))
+    assert lengths[-1] > 0
     params, tok, st = _inputs(SH, lengths, 12, slow=slow, ssm_std=0.1 ** 0.5, conv_std=1.0,
                               norm_w="uniform")
     e = _check(SH, lengths, params, tok, st)
@@ -116,6 +122,7 @@ def test_prefill_many_sequences_unsegmented():
     # 20 sequences x 32 value heads fill the GPU, so no sequence is split, even
     # those longer than a segment; a mix of long, short and empty sequences
     lengths = [1500, 30, 0, 1100, 64, 65, 3, 700, 1030, 128] * 2
+    assert gdn.gdn_prefill_segment_tokens(dims_of(SH), len(lengths), sum(lengths)) == 0
     params, tok, st = _inputs(SH, lengths, 13, slow=True, ssm_std=0.1 ** 0.5, conv_std=1.0)
     e = _check(SH, lengths, params, tok, st)
     print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
