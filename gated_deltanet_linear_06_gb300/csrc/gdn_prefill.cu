@@ -849,13 +849,15 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
     std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
     SideStreams* ss = nullptr;
     cudaStream_t st[kHeadGroups] = {stream};
+    int forked = 1;   // streams that the caller's stream must join again
     if (groups > 1) {
       lock.lock();
       if ((e = side_streams_locked(dev, ss)) != cudaSuccess) return e;
       if ((e = cudaEventRecord(ss->fork, stream)) != cudaSuccess) return e;
       for (int g = 1; g < groups; ++g) {
         st[g] = ss->s[g - 1];
-        if ((e = cudaStreamWaitEvent(st[g], ss->fork, 0)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(st[g], ss->fork, 0)) != cudaSuccess) break;
+        forked = g + 1;
       }
     }
     PrefillArgs pg[kHeadGroups];
@@ -866,20 +868,21 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
       pg[g].nh = pg[g].nkh * (p.h_v / p.h_k);
       pg[g].h0 = pg[g].kh0 * (p.h_v / p.h_k);
     }
-    for (int g = 0; g < groups; ++g)
-      if ((e = launch_prefill_prep(pg[g], (unsigned)l.max_chunks, tm_qkv, st[g])) != cudaSuccess) return e;
+    // On an error part-way, the streams already forked still join the caller's
+    // stream, so that nothing enqueued on it afterwards overtakes their work.
+    for (int g = 0; g < groups && e == cudaSuccess; ++g)
+      e = launch_prefill_prep(pg[g], (unsigned)l.max_chunks, tm_qkv, st[g]);
     if (slots > 0) {   // some sequence may be longer than one segment
-      for (int g = 0; g < groups; ++g)
-        if ((e = launch_prefill_scan(pg[g], true, units, tm_z, st[g])) != cudaSuccess) return e;
-      for (int g = 0; g < groups; ++g)
-        if ((e = launch_prefill_combine(pg[g], (unsigned)slots, st[g])) != cudaSuccess) return e;
+      for (int g = 0; g < groups && e == cudaSuccess; ++g) e = launch_prefill_scan(pg[g], true, units, tm_z, st[g]);
+      for (int g = 0; g < groups && e == cudaSuccess; ++g) e = launch_prefill_combine(pg[g], (unsigned)slots, st[g]);
     }
-    for (int g = 0; g < groups; ++g)
-      if ((e = launch_prefill_scan(pg[g], false, units, tm_z, st[g])) != cudaSuccess) return e;
-    for (int g = 1; g < groups; ++g) {
-      if ((e = cudaEventRecord(ss->join[g - 1], st[g])) != cudaSuccess) return e;
-      if ((e = cudaStreamWaitEvent(stream, ss->join[g - 1], 0)) != cudaSuccess) return e;
+    for (int g = 0; g < groups && e == cudaSuccess; ++g) e = launch_prefill_scan(pg[g], false, units, tm_z, st[g]);
+    for (int g = 1; g < forked; ++g) {
+      cudaError_t j = cudaEventRecord(ss->join[g - 1], st[g]);
+      if (j == cudaSuccess) j = cudaStreamWaitEvent(stream, ss->join[g - 1], 0);
+      if (e == cudaSuccess) e = j;
     }
+    if (e != cudaSuccess) return e;
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   conv_state_kernel<<<dim3((unsigned)((Cc_ + 255) / 256), (unsigned)p.n_seqs), 256, 0, stream>>>(p);
