@@ -26,6 +26,7 @@ LIB_PATH = os.path.join(_HERE, "libgdn.so")
 GDN_OK = 0
 GDN_DTYPE_BF16 = 0
 GDN_DTYPE_F32 = 1
+GDN_DECODE_MAX_STEPS = 8   # most tokens one gdn_decode_multi call takes per sequence
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED",
                 3: "GDN_ERR_WORKSPACE", 4: "GDN_ERR_CUDA", 5: "GDN_ERR_DEVICE_TIMEOUT",
                 6: "GDN_ERR_DEVICE_BOUNDS"}
@@ -81,6 +82,9 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode_step.restype = ctypes.c_int
             L.gdn_decode_step.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_int] + \
                 [_P] * 3 + [ctypes.c_int, _P, _P]
+            L.gdn_decode_multi.restype = ctypes.c_int
+            L.gdn_decode_multi.argtypes = [DP] + [_P] * 9 + [ctypes.c_int] * 3 + [_P] * 3 + \
+                [ctypes.c_int] + [_P] * 4
             L.gdn_prefill_noalloc.restype = ctypes.c_int
             L.gdn_prefill_noalloc.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
                 [_P] * 5
@@ -196,6 +200,31 @@ def gdn_decode_step(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, sl
         _ptr(out, out.dtype, "out", B * dims.h_v * dims.d_v), out_dtype,
         _ptr(device_status, torch.int32, "device_status", 1), _stream(stream))
     _check(st, "gdn_decode_step")
+
+
+def gdn_decode_multi(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,
+                     conv_state, ssm_state, out, steps, ssm_trace=None, conv_trace=None,
+                     device_status=None, stream=None, batch=None):
+    """``steps`` decode steps per sequence for ``batch`` sequences in one call
+    (token-major activations [batch][steps][...]; states updated in place)."""
+    bf, f32 = torch.bfloat16, torch.float32
+    K = int(steps)
+    B = int(batch if batch is not None else out.shape[0])
+    Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
+    out_dtype = GDN_DTYPE_F32 if out.dtype == f32 else GDN_DTYPE_BF16
+    st = lib().gdn_decode_multi(
+        ctypes.byref(dims), _ptr(qkv, bf, "qkv", B * K * Cc), _ptr(z, bf, "z", B * K * dims.h_v * dims.d_v),
+        _ptr(a, bf, "a", B * K * dims.h_v), _ptr(b, bf, "b", B * K * dims.h_v),
+        _ptr(A_log, f32, "A_log", dims.h_v), _ptr(dt_bias, f32, "dt_bias", dims.h_v),
+        _ptr(conv_w, bf, "conv_w", Cc * dims.conv_w), _ptr(norm_w, f32, "norm_w", dims.d_v),
+        _ptr(slot, torch.int32, "slot", B), int(n_slots), B, K,
+        _ptr(conv_state, f32, "conv_state", int(n_slots) * (dims.conv_w - 1) * Cc),
+        _ptr(ssm_state, f32, "ssm_state", int(n_slots) * dims.h_v * dims.d_v * dims.d_k),
+        _ptr(out, out.dtype, "out", B * K * dims.h_v * dims.d_v), out_dtype,
+        _ptr(ssm_trace, f32, "ssm_trace", B * K * dims.h_v * dims.d_v * dims.d_k),
+        _ptr(conv_trace, f32, "conv_trace", B * K * (dims.conv_w - 1) * Cc),
+        _ptr(device_status, torch.int32, "device_status", 1), _stream(stream))
+    _check(st, "gdn_decode_multi")
 
 
 def gdn_read_device_status(status_word, stream=None) -> int:

@@ -169,7 +169,66 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
   p.h_v = dims->h_v;
   p.l2_eps = dims->l2_eps;
   p.rms_eps = dims->rms_eps;
+  p.steps = 1;
+  p.ssm_trace = nullptr;
+  p.conv_trace = nullptr;
   return gdn::launch_decode(p, out_dtype == GDN_DTYPE_F32, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
+static_assert(GDN_DECODE_MAX_STEPS == gdn::kDecodeMaxSteps, "the header's token limit is the kernel's");
+
+gdn_status gdn_decode_multi(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
+                            const void* b, const float* A_log, const float* dt_bias,
+                            const void* conv_w, const float* norm_w, const int32_t* slot,
+                            int n_slots, int batch, int steps, float* conv_state, float* ssm_state,
+                            void* out, int out_dtype, float* ssm_trace, float* conv_trace,
+                            int32_t* device_status, void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (batch < 0 || n_slots < 0 || steps < 1 || steps > GDN_DECODE_MAX_STEPS ||
+      (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32))
+    return GDN_ERR_INVALID_ARG;
+  if (batch == 0) return GDN_OK;
+  if ((long long)batch * dims->h_k > 0x7fffffffLL || (long long)batch * steps > 0x7fffffffLL)
+    return GDN_ERR_INVALID_ARG;
+  if (n_slots < 1 || (!slot && n_slots < batch)) return GDN_ERR_INVALID_ARG;
+  if (!ptr_ok(qkv) || !ptr_ok(z) || !ptr_ok(a) || !ptr_ok(b) || !ptr_ok(A_log) ||
+      !ptr_ok(dt_bias) || !ptr_ok(conv_w) || !ptr_ok(norm_w) || !ptr_ok(conv_state) ||
+      !ptr_ok(ssm_state) || !ptr_ok(out))
+    return GDN_ERR_INVALID_ARG;
+  if ((slot && !aligned16(slot)) || (ssm_trace && !aligned16(ssm_trace)) ||
+      (conv_trace && !aligned16(conv_trace)))
+    return GDN_ERR_INVALID_ARG;
+  if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
+    return GDN_ERR_INVALID_ARG;
+
+  gdn::DecodeArgs p;
+  p.qkv = static_cast<const uint16_t*>(qkv);
+  p.z = static_cast<const uint16_t*>(z);
+  p.a = static_cast<const uint16_t*>(a);
+  p.b = static_cast<const uint16_t*>(b);
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.conv_w = static_cast<const uint16_t*>(conv_w);
+  p.norm_w = norm_w;
+  p.slot = slot;
+  p.conv_state = conv_state;
+  p.ssm_state = ssm_state;
+  p.out = out;
+  p.status = device_status;
+  p.n_slots = n_slots;
+  p.batch = batch;
+  p.h_k = dims->h_k;
+  p.h_v = dims->h_v;
+  p.l2_eps = dims->l2_eps;
+  p.rms_eps = dims->rms_eps;
+  p.steps = steps;
+  p.ssm_trace = ssm_trace;
+  p.conv_trace = conv_trace;
+  return gdn::launch_decode_multi(p, out_dtype == GDN_DTYPE_F32, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? GDN_OK
              : GDN_ERR_CUDA;

@@ -203,6 +203,208 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs p) {
   }
 }
 
+// p.steps decode steps per sequence in one launch: the state rows are read
+// once, taken through every token in registers and written once (plus, when
+// p.ssm_trace is set, once per token into the trace), so the HBM traffic per
+// token falls by the number of tokens.  Every step repeats the single-step
+// kernel's arithmetic in its order -- the conv window shift, the norms' lane
+// split and butterflies, the gates, each row's decay, dot products, update and
+// output dot, the gated RMSNorm -- so k tokens here give, bit for bit, what k
+// successive single steps give.
+template <int G, bool OUT_F32>
+__global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p) {
+  constexpr int kBatches = G * kBatchesPerHead;
+  const int bidx = blockIdx.x / p.h_k;
+  const int kh = blockIdx.x - bidx * p.h_k;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Cq = p.h_k * kD;
+  const int Cc = 2 * Cq + p.h_v * kD;
+  const int K = p.steps;
+
+  int s = bidx;
+  if (p.slot) {
+    s = p.slot[bidx];
+    if (s < 0 || s >= p.n_slots) {
+      if (tid == 0) record_status(p.status, GDN_ERR_DEVICE_BOUNDS);
+      return;
+    }
+  }
+
+  __shared__ float sq[kDecodeMaxSteps][kD], sk[kDecodeMaxSteps][kD];
+  __shared__ float sv[kDecodeMaxSteps][G][kD], so[kDecodeMaxSteps][G][kD];
+  __shared__ float s_decay[kDecodeMaxSteps][G], s_beta[kDecodeMaxSteps][G], s_rstd[kDecodeMaxSteps][G];
+  __shared__ float s_rq[kDecodeMaxSteps], s_rk[kDecodeMaxSteps];
+
+  // state rows of value head kh*G + vh, row r: base + (vh*kD + r)*kD
+  float* const S_base = p.ssm_state + ((size_t)s * p.h_v + (size_t)kh * G) * kD * kD;
+  auto row_of = [&](int nb, int j) {
+    return warp * (kBatchesPerHead * kRowsPerBatch) + (nb % kBatchesPerHead) * kRowsPerBatch + j;
+  };
+  auto row_ptr = [&](int nb, int j) -> float4* {
+    const int vh = nb / kBatchesPerHead;
+    return reinterpret_cast<float4*>(S_base + ((size_t)vh * kD + row_of(nb, j)) * kD) + lane;
+  };
+  auto trace_ptr = [&](int t, int nb, int j) -> float4* {
+    const int vh = nb / kBatchesPerHead;
+    float* base = p.ssm_trace + (((size_t)bidx * K + t) * p.h_v + (size_t)kh * G + vh) * kD * kD;
+    return reinterpret_cast<float4*>(base + (size_t)row_of(nb, j) * kD) + lane;
+  };
+
+  float4 cur[kRowsPerBatch];
+#pragma unroll
+  for (int j = 0; j < kRowsPerBatch; ++j) cur[j] = __ldcs(row_ptr(0, j));
+
+  // ---- conv + SiLU over this CTA's channels for every token, the window shifting
+  //      one token at a time ----
+  {
+    float* cs = p.conv_state + (size_t)s * (kConvW - 1) * Cc;
+    for (int ci = tid; ci < (2 + G) * kD; ci += kThreads) {
+      int c;
+      if (ci < kD) c = kh * kD + ci;
+      else if (ci < 2 * kD) c = Cq + kh * kD + (ci - kD);
+      else c = 2 * Cq + kh * G * kD + (ci - 2 * kD);
+      float s0 = cs[c], s1 = cs[Cc + c], s2 = cs[2 * Cc + c];
+      const uint2 wr = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)c * kConvW);
+      const float w0 = bf16_to_f32(wr.x & 0xffffu), w1 = bf16_to_f32(wr.x >> 16);
+      const float w2 = bf16_to_f32(wr.y & 0xffffu), w3 = bf16_to_f32(wr.y >> 16);
+      for (int t = 0; t < K; ++t) {
+        const float xt = bf16_to_f32(p.qkv[((size_t)bidx * K + t) * Cc + c]);
+        float y = w0 * s0;
+        y = fmaf(w1, s1, y);
+        y = fmaf(w2, s2, y);
+        y = fmaf(w3, xt, y);
+        y = silu(y);
+        s0 = s1;
+        s1 = s2;
+        s2 = xt;
+        if (p.conv_trace) {
+          float* ct = p.conv_trace + ((size_t)bidx * K + t) * (kConvW - 1) * Cc;
+          ct[c] = s0;
+          ct[Cc + c] = s1;
+          ct[2 * Cc + c] = s2;
+        }
+        if (ci < kD) sq[t][ci] = y;
+        else if (ci < 2 * kD) sk[t][ci - kD] = y;
+        else sv[t][(ci - 2 * kD) / kD][(ci - 2 * kD) % kD] = y;
+      }
+      cs[c] = s0;
+      cs[Cc + c] = s1;
+      cs[2 * Cc + c] = s2;
+    }
+  }
+  __syncthreads();
+
+  // ---- L2 norms of q and k (a warp per token and vector), gates ----
+  for (int pr = warp; pr < 2 * K; pr += kWarps) {
+    const int t = pr >> 1;
+    const float* v = (pr & 1) ? sk[t] : sq[t];
+    const float4 x4 = reinterpret_cast<const float4*>(v)[lane];
+    float ss = x4.x * x4.x;
+    ss = fmaf(x4.y, x4.y, ss);
+    ss = fmaf(x4.z, x4.z, ss);
+    ss = fmaf(x4.w, x4.w, ss);
+    ss = warp_sum(ss);
+    if (lane == 0) {
+      const float r = rsqrtf(ss + p.l2_eps);
+      if (pr & 1) s_rk[t] = r;
+      else s_rq[t] = r * rsqrtf((float)kD);
+    }
+  }
+  for (int i = tid; i < K * G; i += kThreads) {
+    const int t = i / G, g = i - t * G;
+    const int h = kh * G + g;
+    const size_t ab = ((size_t)bidx * K + t) * p.h_v + h;
+    const float gg = -__expf(p.A_log[h]) * softplus(bf16_to_f32(p.a[ab]) + p.dt_bias[h]);
+    s_decay[t][g] = __expf(gg);
+    s_beta[t][g] = sigmoid(bf16_to_f32(p.b[ab]));
+  }
+  __syncthreads();
+
+  // ---- the state stream: each batch of rows through every token ----
+#pragma unroll
+  for (int nb = 0; nb < kBatches; ++nb) {
+    float4 nxt[kRowsPerBatch];
+    if (nb + 1 < kBatches) {
+#pragma unroll
+      for (int j = 0; j < kRowsPerBatch; ++j) nxt[j] = __ldcs(row_ptr(nb + 1, j));
+    }
+    const int vh = nb / kBatchesPerHead;
+    const int r0 = row_of(nb, 0);
+#pragma unroll 1
+    for (int t = 0; t < K; ++t) {
+      float qh[4], kk[4];
+      const float rq = s_rq[t], rk = s_rk[t];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        qh[i] = sq[t][4 * lane + i] * rq;
+        kk[i] = sk[t][4 * lane + i] * rk;
+      }
+      const float decay = s_decay[t][vh], beta = s_beta[t][vh];
+      float red[kRowsPerBatch];
+#pragma unroll
+      for (int j = 0; j < kRowsPerBatch; ++j) {
+        cur[j].x *= decay; cur[j].y *= decay; cur[j].z *= decay; cur[j].w *= decay;
+        red[j] = dot4(cur[j], kk);
+      }
+#pragma unroll
+      for (int j = 0; j < kRowsPerBatch; ++j) red[j] = warp_sum(red[j]);
+#pragma unroll
+      for (int j = 0; j < kRowsPerBatch; ++j) {
+        const float u = beta * (sv[t][vh][r0 + j] - red[j]);
+        cur[j].x = fmaf(u, kk[0], cur[j].x);
+        cur[j].y = fmaf(u, kk[1], cur[j].y);
+        cur[j].z = fmaf(u, kk[2], cur[j].z);
+        cur[j].w = fmaf(u, kk[3], cur[j].w);
+        if (p.ssm_trace) __stcs(trace_ptr(t, nb, j), cur[j]);
+        red[j] = dot4(cur[j], qh);
+      }
+#pragma unroll
+      for (int j = 0; j < kRowsPerBatch; ++j) red[j] = warp_sum(red[j]);
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < kRowsPerBatch; ++j) so[t][vh][r0 + j] = red[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kRowsPerBatch; ++j) __stcs(row_ptr(nb, j), cur[j]);
+    if (nb + 1 < kBatches) {
+#pragma unroll
+      for (int j = 0; j < kRowsPerBatch; ++j) cur[j] = nxt[j];
+    }
+  }
+  __syncthreads();
+
+  // ---- gated RMSNorm over d_v of each (token, value head) ----
+  for (int pr = warp; pr < K * G; pr += kWarps) {
+    const int t = pr / G, vh = pr - t * G;
+    const float4 o4 = reinterpret_cast<const float4*>(so[t][vh])[lane];
+    float ss = o4.x * o4.x;
+    ss = fmaf(o4.y, o4.y, ss);
+    ss = fmaf(o4.z, o4.z, ss);
+    ss = fmaf(o4.w, o4.w, ss);
+    ss = warp_sum(ss);
+    if (lane == 0) s_rstd[t][vh] = rsqrtf(ss * (1.0f / kD) + p.rms_eps);
+  }
+  __syncthreads();
+  for (int i = tid; i < K * G * kD; i += kThreads) {
+    const int t = i / (G * kD), rem = i - t * (G * kD);
+    const int vh = rem / kD, r = rem - vh * kD;
+    const size_t o_idx = (((size_t)bidx * K + t) * p.h_v + (size_t)kh * G + vh) * kD + r;
+    const float zz = bf16_to_f32(p.z[o_idx]);
+    const float val = so[t][vh][r] * s_rstd[t][vh] * p.norm_w[r] * silu(zz);
+    if (OUT_F32) reinterpret_cast<float*>(p.out)[o_idx] = val;
+    else reinterpret_cast<uint16_t*>(p.out)[o_idx] = f32_to_bf16(val);
+  }
+}
+
+template <int G>
+cudaError_t launch_multi_g(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {
+  const dim3 grid((unsigned)(p.batch * p.h_k)), block(kThreads);
+  if (out_f32) decode_multi_kernel<G, true><<<grid, block, 0, stream>>>(p);
+  else decode_multi_kernel<G, false><<<grid, block, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int G>
 cudaError_t launch_g(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {
   const dim3 grid((unsigned)(p.batch * p.h_k)), block(kThreads);
@@ -212,6 +414,16 @@ cudaError_t launch_g(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {
 }
 
 }  // namespace
+
+cudaError_t launch_decode_multi(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {
+  if (p.steps < 1 || p.steps > kDecodeMaxSteps) return cudaErrorInvalidValue;
+  switch (p.h_v / p.h_k) {
+    case 1: return launch_multi_g<1>(p, out_f32, stream);
+    case 2: return launch_multi_g<2>(p, out_f32, stream);
+    case 4: return launch_multi_g<4>(p, out_f32, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 
 cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {
   switch (p.h_v / p.h_k) {

@@ -23,6 +23,12 @@ struct DecodeArgs {
   int32_t* status;         // nullable device word
   int n_slots, batch, h_k, h_v;
   float l2_eps, rms_eps;
+  // multi-token decode (launch_decode_multi): tokens per sequence, the token-major
+  // activations above then being [batch][steps][...], and the nullable traces of
+  // the states after every token
+  int steps;
+  float* ssm_trace;        // [batch][steps][h_v][128][128]
+  float* conv_trace;       // [batch][steps][3][Cc]
 };
 
 struct PrefillArgs {
@@ -63,6 +69,9 @@ struct PrefillArgs {
 // Host launchers: enqueue on `stream`, return the launch error (or
 // cudaSuccess).  Dims are validated by the caller.
 cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream);
+// p.steps tokens per sequence in one launch (1 <= steps <= kDecodeMaxSteps).
+constexpr int kDecodeMaxSteps = 8;
+cudaError_t launch_decode_multi(const DecodeArgs& p, bool out_f32, cudaStream_t stream);
 // allow_split = false keeps every sequence in one segment (no transfer maps in
 // the scratch); the scratch then needs only prefill_scratch_bytes_unsplit().
 cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream, bool allow_split = true);

@@ -2,6 +2,7 @@
 
   python -m gated_deltanet_linear_06_gb300.profile_case --kernel prefill --tokens 8192
   python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode --batch 128
+  python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode_multi --batch 256 --steps 4
 
 Builds seeded synthetic inputs (the same distributions as the benchmark),
 runs the kernel ``--warmup`` times, then ``--iters`` times, and prints the
@@ -27,10 +28,12 @@ def main():
     import gdn_inputs as gi
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["prefill", "decode"], required=True)
+    ap.add_argument("--kernel", choices=["prefill", "decode", "decode_multi"], required=True)
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: tokens of one sequence")
     ap.add_argument("--seqs", type=int, default=1, help="prefill: equal-length sequences")
     ap.add_argument("--batch", type=int, default=128, help="decode: sequences")
+    ap.add_argument("--steps", type=int, default=4, help="decode_multi: tokens per sequence")
+    ap.add_argument("--trace", action="store_true", help="decode_multi: also write the SSM trace")
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
@@ -53,7 +56,7 @@ def main():
             gdn.gdn_prefill(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
                             p["conv_w"], p["norm_w"], cu, conv, ssm, out, ws, stream=stream)
         unit, per_call = "tokens", T
-    else:
+    elif args.kernel == "decode":
         B = args.batch
         p = {k: v.to(dev) for k, v in gi.make_params(sh, 4).items()}
         st = gi.make_states(sh, B, 4, ssm_std=0.1 ** 0.5, conv_std=1.0)
@@ -65,6 +68,20 @@ def main():
             gdn.gdn_decode_step(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
                                 p["conv_w"], p["norm_w"], None, B, conv, ssm, out, stream=stream)
         unit, per_call = "seq-steps", B
+    else:
+        B, K = args.batch, args.steps
+        p = {k: v.to(dev) for k, v in gi.make_params(sh, 4).items()}
+        st = gi.make_states(sh, B, 4, ssm_std=0.1 ** 0.5, conv_std=1.0)
+        conv, ssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
+        x = {k: v.to(dev) for k, v in gi.make_tokens(sh, B * K, 4).items()}
+        out = torch.empty(B, K, sh.h_v, 128, dtype=torch.bfloat16, device=dev)
+        trace = torch.empty(B, K, sh.h_v, 128, 128, device=dev) if args.trace else None
+
+        def call():
+            gdn.gdn_decode_multi(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
+                                 p["conv_w"], p["norm_w"], None, B, conv, ssm, out, K,
+                                 ssm_trace=trace, stream=stream)
+        unit, per_call = "seq-steps", B * K
 
     for _ in range(args.warmup):
         call()

@@ -184,6 +184,38 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
                            float* ssm_state, void* out, int out_dtype,
                            int32_t* device_status, void* stream);
 
+/* Most tokens per sequence one gdn_decode_multi call takes. */
+#define GDN_DECODE_MAX_STEPS 8
+
+/*
+ * `steps` decode steps per sequence in one call: multi-token decode, or the
+ * verification pass of speculative decoding (the draft tokens of every
+ * sequence at once).  The result is bit-identical to `steps` successive
+ * gdn_decode_step calls on the same tokens -- every step repeats that call's
+ * arithmetic in its order -- while each state is read and written once per
+ * call instead of once per token.
+ *
+ *   qkv  bf16 [batch][steps][Cc];  z bf16 [batch][steps][h_v][d_v];
+ *   a, b bf16 [batch][steps][h_v]  (token t of sequence i at [i][t])
+ *   A_log, dt_bias, conv_w, norm_w, slot, n_slots, conv_state, ssm_state,
+ *   device_status   as for gdn_decode_step; the states end after the last token
+ *   steps      1 .. GDN_DECODE_MAX_STEPS
+ *   out        [batch][steps][h_v][d_v], bf16 or fp32 per out_dtype (output)
+ *   ssm_trace  NULL, or fp32 [batch][steps][h_v][d_v][d_k]: the SSM state after
+ *              each token (for rolling back to the last accepted draft token);
+ *              it costs one more state write per token
+ *   conv_trace NULL, or fp32 [batch][steps][conv_w - 1][Cc]: the conv state
+ *              after each token
+ * batch = 0 launches nothing and returns GDN_OK.
+ */
+gdn_status gdn_decode_multi(const gdn_dims* dims, const void* qkv, const void* z,
+                            const void* a, const void* b, const float* A_log,
+                            const float* dt_bias, const void* conv_w, const float* norm_w,
+                            const int32_t* slot, int n_slots, int batch, int steps,
+                            float* conv_state, float* ssm_state, void* out, int out_dtype,
+                            float* ssm_trace, float* conv_trace, int32_t* device_status,
+                            void* stream);
+
 /*
  * Prefill for callers that cannot allocate device memory.
  *

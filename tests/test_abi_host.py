@@ -34,7 +34,8 @@ def _declared_functions():
 def test_header_declares_the_entry_points():
     names = _declared_functions()
     for want in ("gdn_prefill", "gdn_decode_step", "gdn_workspace_bytes", "gdn_state_bytes",
-                 "gdn_read_device_status", "gdn_status_string", "gdn_version"):
+                 "gdn_read_device_status", "gdn_status_string", "gdn_version",
+                 "gdn_decode_multi", "gdn_prefill_noalloc", "gdn_prefill_segment_tokens"):
         assert want in names
 
 
@@ -129,6 +130,44 @@ def test_decode_rejects_bad_pointers_and_sizes(L):
     assert _decode(L, d, n_slots=3) == INVALID                         # fewer states than batch
     assert _decode(L, d, out_dtype=7) == INVALID
     assert _decode(L, d, batch=0) == OK                                # nothing to launch
+
+
+def _decode_multi(L, dims, **kw):
+    args = dict(qkv=FAKE, z=FAKE, a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE, conv_w=FAKE,
+                norm_w=FAKE, slot=None, n_slots=4, batch=4, steps=4, conv_state=FAKE,
+                ssm_state=FAKE, out=FAKE, out_dtype=0, ssm_trace=None, conv_trace=None,
+                status=None, stream=None)
+    args.update(kw)
+    return L.gdn_decode_multi(ctypes.byref(dims) if dims is not None else None, args["qkv"],
+                              args["z"], args["a"], args["b"], args["A_log"], args["dt_bias"],
+                              args["conv_w"], args["norm_w"], args["slot"], args["n_slots"],
+                              args["batch"], args["steps"], args["conv_state"],
+                              args["ssm_state"], args["out"], args["out_dtype"],
+                              args["ssm_trace"], args["conv_trace"], args["status"],
+                              args["stream"])
+
+
+def test_decode_multi_rejects_bad_arguments(L):
+    d = gdn.make_dims()
+    assert gdn.GDN_DECODE_MAX_STEPS == 8
+    assert _decode_multi(L, None) == INVALID
+    assert _decode_multi(L, gdn.make_dims(h_k=3, h_v=32)) == INVALID
+    assert _decode_multi(L, gdn.make_dims(d_k=64, d_v=64)) == UNSUP
+    assert _decode_multi(L, gdn.make_dims(h_k=4, h_v=32)) == UNSUP     # G = 8
+    assert _decode_multi(L, d, steps=0) == INVALID
+    assert _decode_multi(L, d, steps=9) == INVALID                     # above the limit
+    assert _decode_multi(L, d, steps=-3) == INVALID
+    assert _decode_multi(L, d, qkv=None) == INVALID
+    assert _decode_multi(L, d, ssm_state=FAKE + 4) == INVALID
+    assert _decode_multi(L, d, ssm_trace=FAKE + 8) == INVALID          # misaligned trace
+    assert _decode_multi(L, d, conv_trace=FAKE + 4) == INVALID
+    assert _decode_multi(L, d, slot=FAKE + 4) == INVALID
+    assert _decode_multi(L, d, status=FAKE + 2) == INVALID
+    assert _decode_multi(L, d, batch=-1) == INVALID
+    assert _decode_multi(L, d, n_slots=3) == INVALID
+    assert _decode_multi(L, d, out_dtype=5) == INVALID
+    assert _decode_multi(L, d, batch=0) == OK
+    assert _decode_multi(L, d, batch=0, steps=8) == OK
 
 
 def test_prefill_rejects_bad_arguments(L):
