@@ -7,10 +7,14 @@
 //   - one CTA per (sequence, key head) owns the q/k conv channels of that key
 //     head and the v channels of its G value heads, so the conv state it
 //     reads and rewrites belongs to no other CTA;
-//   - a warp updates one state row at a time, each lane holding 4 consecutive
-//     fp32 columns (one 128-bit load and one 128-bit store per lane per row,
-//     512 contiguous bytes per warp), with batches of 8 rows in flight and
-//     the next batch prefetched while the current one is updated;
+//   - a warp updates 8 state rows at a time, 8 lanes per row: lane 8*rr + q
+//     holds, for each of two groups of 4 rows, row 4*gi + rr at the columns of
+//     the float4 chunks q, q + 8, q + 16, q + 24, so each 128-bit warp load or
+//     store covers 4 whole 128-byte row segments; the next batch of rows is
+//     prefetched while the current one is updated;
+//   - the d_k reductions are an in-lane sum of 16 products in packed fp32x2
+//     arithmetic and a 3-level butterfly over the row's 8 lanes, which serves
+//     4 rows with each shuffle;
 //   - loads and stores use the streaming cache hint, since the state is
 //     touched once per step;
 //   - the conv, the norms and the gates run before the first row is needed,
@@ -35,12 +39,113 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerBatch = 8;
 constexpr int kBatchesPerHead = kD / (kWarps * kRowsPerBatch);  // 2
 
-__device__ __forceinline__ float dot4(const float4& s, const float (&v)[4]) {
-  float acc = s.x * v[0];
-  acc = fmaf(s.y, v[1], acc);
-  acc = fmaf(s.z, v[2], acc);
-  acc = fmaf(s.w, v[3], acc);
-  return acc;
+// A warp's batch of 8 state rows: v[gi][i] is row 4*gi + rr, float4 chunk q + 8*i
+// (lane = 8*rr + q).  The 8 chunk indices of a row are the row's 8 lanes.
+struct RowBatch {
+  float4 v[2][4];
+};
+
+// Columns of a lane: float4 chunks q + 8*i, i < 4, as 8 float2 pairs.
+struct LaneCols {
+  float2 c[8];
+};
+
+__device__ __forceinline__ void load_lane_cols(LaneCols& x, const float* vec, int q) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = reinterpret_cast<const float4*>(vec)[q + 8 * i];
+    x.c[2 * i] = make_float2(f.x, f.y);
+    x.c[2 * i + 1] = make_float2(f.z, f.w);
+  }
+}
+
+// rows: the batch's first row; row stride kD floats
+__device__ __forceinline__ void load_rows(RowBatch& R, const float* rows, int rr, int q) {
+#pragma unroll
+  for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      R.v[gi][i] = __ldcs(reinterpret_cast<const float4*>(rows + (size_t)(4 * gi + rr) * kD) + q + 8 * i);
+}
+
+__device__ __forceinline__ void store_rows(float* rows, const RowBatch& R, int rr, int q) {
+#pragma unroll
+  for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      __stcs(reinterpret_cast<float4*>(rows + (size_t)(4 * gi + rr) * kD) + q + 8 * i, R.v[gi][i]);
+}
+
+__device__ __forceinline__ float2 lo2(const float4& f) { return make_float2(f.x, f.y); }
+__device__ __forceinline__ float2 hi2(const float4& f) { return make_float2(f.z, f.w); }
+
+// The lane's 16 products of a row with x, summed in a fixed order.
+__device__ __forceinline__ float lane_dot(const float4 (&r)[4], const LaneCols& x) {
+  float2 acc = __fmul2_rn(lo2(r[0]), x.c[0]);
+  acc = __ffma2_rn(hi2(r[0]), x.c[1], acc);
+#pragma unroll
+  for (int i = 1; i < 4; ++i) {
+    acc = __ffma2_rn(lo2(r[i]), x.c[2 * i], acc);
+    acc = __ffma2_rn(hi2(r[i]), x.c[2 * i + 1], acc);
+  }
+  return acc.x + acc.y;
+}
+
+// One token on a batch of rows.  With d_k = S_i . k^ and d_q = S_i . q^ taken
+// from the state before the token:
+//   u = beta (v_i - e^g d_k);   S_i <- e^g S_i + u k^;   o_i = e^g d_q + u (k^ . q^)
+// which is S <- e^g S (I - beta k^ k^T) + beta v k^T followed by o = S q^, with the
+// output dot moved before the update so that both dots share one butterfly (a
+// 3-level xor butterfly over the row's 8 lanes: every lane of the row ends with the
+// same bits).  v[gi] is v at the lane's row of group gi; kq = k^ . q^.
+__device__ __forceinline__ void rows_token(RowBatch& R, const LaneCols& kk, const LaneCols& qh,
+                                           float decay, float beta, float kq, const float (&v)[2],
+                                           float (&o)[2]) {
+  float dk[2], dq[2];
+#pragma unroll
+  for (int gi = 0; gi < 2; ++gi) {
+    dk[gi] = lane_dot(R.v[gi], kk);
+    dq[gi] = lane_dot(R.v[gi], qh);
+  }
+#pragma unroll
+  for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+      dk[gi] += __shfl_xor_sync(0xffffffffu, dk[gi], m);
+      dq[gi] += __shfl_xor_sync(0xffffffffu, dq[gi], m);
+    }
+  const float2 d2 = make_float2(decay, decay);
+#pragma unroll
+  for (int gi = 0; gi < 2; ++gi) {
+    const float u = beta * fmaf(-decay, dk[gi], v[gi]);
+    o[gi] = fmaf(u, kq, decay * dq[gi]);
+    const float2 u2 = make_float2(u, u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = __ffma2_rn(lo2(R.v[gi][i]), d2, __fmul2_rn(u2, kk.c[2 * i]));
+      const float2 b = __ffma2_rn(hi2(R.v[gi][i]), d2, __fmul2_rn(u2, kk.c[2 * i + 1]));
+      R.v[gi][i] = make_float4(a.x, a.y, b.x, b.y);
+    }
+  }
+}
+
+// Norms of one token's q and k and their dot (a warp; lane holds 4 consecutive
+// elements): rq = 1/sqrt(sum q^2 + eps) / sqrt(d_k), rk = 1/sqrt(sum k^2 + eps),
+// kq = (q . k) rq rk = k^ . q^.
+__device__ __forceinline__ void token_norms(const float* qv, const float* kv, int lane, float eps,
+                                            float& rq, float& rk, float& kq) {
+  const float4 a = reinterpret_cast<const float4*>(qv)[lane];
+  const float4 b = reinterpret_cast<const float4*>(kv)[lane];
+  float sq = a.x * a.x, sk = b.x * b.x, qk = a.x * b.x;
+  sq = fmaf(a.y, a.y, sq); sk = fmaf(b.y, b.y, sk); qk = fmaf(a.y, b.y, qk);
+  sq = fmaf(a.z, a.z, sq); sk = fmaf(b.z, b.z, sk); qk = fmaf(a.z, b.z, qk);
+  sq = fmaf(a.w, a.w, sq); sk = fmaf(b.w, b.w, sk); qk = fmaf(a.w, b.w, qk);
+  sq = warp_sum(sq);
+  sk = warp_sum(sk);
+  qk = warp_sum(qk);
+  rq = rsqrtf(sq + eps) * rsqrtf((float)kD);
+  rk = rsqrtf(sk + eps);
+  kq = qk * rq * rk;
 }
 
 template <int G, bool OUT_F32>
@@ -61,21 +166,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs p) {
     }
   }
 
-  __shared__ float sq[kD], sk[kD], sv[G][kD], so[G][kD];
+  __shared__ __align__(16) float sq[kD], sk[kD], sv[G][kD], so[G][kD];
   __shared__ float s_decay[G], s_beta[G], s_rstd[G];
-  __shared__ float s_rq, s_rk;
+  __shared__ float s_rq, s_rk, s_kq;
 
-  // state rows of value head kh*G + vh, row r: base + (vh*kD + r)*kD
+  // state rows of value head kh*G + vh, row r: base + (vh*kD + r)*kD; batch nb
+  // of a warp covers rows batch_row0(nb) .. + 7 of value head nb / kBatchesPerHead
   float* const S_base = p.ssm_state + ((size_t)s * p.h_v + (size_t)kh * G) * kD * kD;
-  auto row_ptr = [&](int nb, int j) -> float4* {
-    const int vh = nb / kBatchesPerHead;
-    const int r = warp * (kBatchesPerHead * kRowsPerBatch) + (nb % kBatchesPerHead) * kRowsPerBatch + j;
-    return reinterpret_cast<float4*>(S_base + ((size_t)vh * kD + r) * kD) + lane;
+  const int rr = lane >> 3, q = lane & 7;
+  auto batch_row0 = [&](int nb) {
+    return warp * (kBatchesPerHead * kRowsPerBatch) + (nb % kBatchesPerHead) * kRowsPerBatch;
+  };
+  auto batch_rows = [&](int nb) -> float* {
+    return S_base + ((size_t)(nb / kBatchesPerHead) * kD + batch_row0(nb)) * kD;
   };
 
-  float4 cur[kRowsPerBatch];
-#pragma unroll
-  for (int j = 0; j < kRowsPerBatch; ++j) cur[j] = __ldcs(row_ptr(0, j));
+  RowBatch cur;
+  load_rows(cur, batch_rows(0), rr, q);
 
   // ---- conv + SiLU over this CTA's channels, conv-state shift ----
   {
@@ -106,19 +213,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs p) {
   }
   __syncthreads();
 
-  // ---- L2 norms of q and k, gates ----
-  if (warp == 0 || warp == 1) {
-    const float* v = warp == 0 ? sq : sk;
-    const float4 x4 = reinterpret_cast<const float4*>(v)[lane];
-    float ss = x4.x * x4.x;
-    ss = fmaf(x4.y, x4.y, ss);
-    ss = fmaf(x4.z, x4.z, ss);
-    ss = fmaf(x4.w, x4.w, ss);
-    ss = warp_sum(ss);
+  // ---- L2 norms of q and k and k^ . q^, gates ----
+  if (warp == 0) {
+    float rq, rk, kq;
+    token_norms(sq, sk, lane, p.l2_eps, rq, rk, kq);
     if (lane == 0) {
-      const float r = rsqrtf(ss + p.l2_eps);
-      if (warp == 0) s_rq = r * rsqrtf((float)kD);
-      else s_rk = r;
+      s_rq = rq;
+      s_rk = rk;
+      s_kq = kq;
     }
   } else if (warp == 2 && lane < G) {
     const int h = kh * G + lane;
@@ -129,56 +231,33 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs p) {
     s_beta[lane] = sigmoid(bv);
   }
   __syncthreads();
-
-  float qh[4], kk[4];
-  {
-    const float rq = s_rq, rk = s_rk;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      qh[i] = sq[4 * lane + i] * rq;
-      kk[i] = sk[4 * lane + i] * rk;
-    }
+  if (tid < kD) {
+    sq[tid] *= s_rq;
+    sk[tid] *= s_rk;
   }
+  __syncthreads();
+
+  LaneCols qh, kk;
+  load_lane_cols(qh, sq, q);
+  load_lane_cols(kk, sk, q);
+  const float kq = s_kq;
 
   // ---- the state stream ----
-#pragma unroll
+#pragma unroll 1
   for (int nb = 0; nb < kBatches; ++nb) {
-    float4 nxt[kRowsPerBatch];
-    if (nb + 1 < kBatches) {
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) nxt[j] = __ldcs(row_ptr(nb + 1, j));
-    }
+    RowBatch nxt;
+    if (nb + 1 < kBatches) load_rows(nxt, batch_rows(nb + 1), rr, q);
     const int vh = nb / kBatchesPerHead;
-    const int r0 = warp * (kBatchesPerHead * kRowsPerBatch) + (nb % kBatchesPerHead) * kRowsPerBatch;
-    const float decay = s_decay[vh], beta = s_beta[vh];
-    float red[kRowsPerBatch];
-#pragma unroll
-    for (int j = 0; j < kRowsPerBatch; ++j) {
-      cur[j].x *= decay; cur[j].y *= decay; cur[j].z *= decay; cur[j].w *= decay;
-      red[j] = dot4(cur[j], kk);
+    const int r0 = batch_row0(nb);
+    const float v[2] = {sv[vh][r0 + rr], sv[vh][r0 + 4 + rr]};
+    float o[2];
+    rows_token(cur, kk, qh, s_decay[vh], s_beta[vh], kq, v, o);
+    store_rows(batch_rows(nb), cur, rr, q);
+    if (q == 0) {
+      so[vh][r0 + rr] = o[0];
+      so[vh][r0 + 4 + rr] = o[1];
     }
-#pragma unroll
-    for (int j = 0; j < kRowsPerBatch; ++j) red[j] = warp_sum(red[j]);
-#pragma unroll
-    for (int j = 0; j < kRowsPerBatch; ++j) {
-      const float u = beta * (sv[vh][r0 + j] - red[j]);
-      cur[j].x = fmaf(u, kk[0], cur[j].x);
-      cur[j].y = fmaf(u, kk[1], cur[j].y);
-      cur[j].z = fmaf(u, kk[2], cur[j].z);
-      cur[j].w = fmaf(u, kk[3], cur[j].w);
-      __stcs(row_ptr(nb, j), cur[j]);
-      red[j] = dot4(cur[j], qh);
-    }
-#pragma unroll
-    for (int j = 0; j < kRowsPerBatch; ++j) red[j] = warp_sum(red[j]);
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) so[vh][r0 + j] = red[j];
-    }
-    if (nb + 1 < kBatches) {
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) cur[j] = nxt[j];
-    }
+    if (nb + 1 < kBatches) cur = nxt;
   }
   __syncthreads();
 
@@ -230,29 +309,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
     }
   }
 
-  __shared__ float sq[kDecodeMaxSteps][kD], sk[kDecodeMaxSteps][kD];
-  __shared__ float sv[kDecodeMaxSteps][G][kD], so[kDecodeMaxSteps][G][kD];
+  __shared__ __align__(16) float sq[kDecodeMaxSteps][kD], sk[kDecodeMaxSteps][kD];
+  __shared__ __align__(16) float sv[kDecodeMaxSteps][G][kD], so[kDecodeMaxSteps][G][kD];
   __shared__ float s_decay[kDecodeMaxSteps][G], s_beta[kDecodeMaxSteps][G], s_rstd[kDecodeMaxSteps][G];
-  __shared__ float s_rq[kDecodeMaxSteps], s_rk[kDecodeMaxSteps];
+  __shared__ float s_rq[kDecodeMaxSteps], s_rk[kDecodeMaxSteps], s_kq[kDecodeMaxSteps];
 
-  // state rows of value head kh*G + vh, row r: base + (vh*kD + r)*kD
+  // state rows of value head kh*G + vh, row r: base + (vh*kD + r)*kD (the same
+  // batches of rows as the single step)
   float* const S_base = p.ssm_state + ((size_t)s * p.h_v + (size_t)kh * G) * kD * kD;
-  auto row_of = [&](int nb, int j) {
-    return warp * (kBatchesPerHead * kRowsPerBatch) + (nb % kBatchesPerHead) * kRowsPerBatch + j;
+  const int rr = lane >> 3, q = lane & 7;
+  auto batch_row0 = [&](int nb) {
+    return warp * (kBatchesPerHead * kRowsPerBatch) + (nb % kBatchesPerHead) * kRowsPerBatch;
   };
-  auto row_ptr = [&](int nb, int j) -> float4* {
-    const int vh = nb / kBatchesPerHead;
-    return reinterpret_cast<float4*>(S_base + ((size_t)vh * kD + row_of(nb, j)) * kD) + lane;
+  auto batch_rows = [&](int nb) -> float* {
+    return S_base + ((size_t)(nb / kBatchesPerHead) * kD + batch_row0(nb)) * kD;
   };
-  auto trace_ptr = [&](int t, int nb, int j) -> float4* {
+  auto trace_rows = [&](int t, int nb) -> float* {
     const int vh = nb / kBatchesPerHead;
     float* base = p.ssm_trace + (((size_t)bidx * K + t) * p.h_v + (size_t)kh * G + vh) * kD * kD;
-    return reinterpret_cast<float4*>(base + (size_t)row_of(nb, j) * kD) + lane;
+    return base + (size_t)batch_row0(nb) * kD;
   };
 
-  float4 cur[kRowsPerBatch];
-#pragma unroll
-  for (int j = 0; j < kRowsPerBatch; ++j) cur[j] = __ldcs(row_ptr(0, j));
+  RowBatch cur;
+  load_rows(cur, batch_rows(0), rr, q);
 
   // ---- conv + SiLU over this CTA's channels for every token, the window shifting
   //      one token at a time ----
@@ -267,8 +346,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
       const uint2 wr = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)c * kConvW);
       const float w0 = bf16_to_f32(wr.x & 0xffffu), w1 = bf16_to_f32(wr.x >> 16);
       const float w2 = bf16_to_f32(wr.y & 0xffffu), w3 = bf16_to_f32(wr.y >> 16);
-      for (int t = 0; t < K; ++t) {
-        const float xt = bf16_to_f32(p.qkv[((size_t)bidx * K + t) * Cc + c]);
+      float xs[kDecodeMaxSteps];  // every token's input issued before the first is used
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxSteps; ++t)
+        if (t < K) xs[t] = bf16_to_f32(p.qkv[((size_t)bidx * K + t) * Cc + c]);
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxSteps; ++t) {
+        if (t >= K) break;
+        const float xt = xs[t];
         float y = w0 * s0;
         y = fmaf(w1, s1, y);
         y = fmaf(w2, s2, y);
@@ -294,20 +379,15 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
   }
   __syncthreads();
 
-  // ---- L2 norms of q and k (a warp per token and vector), gates ----
-  for (int pr = warp; pr < 2 * K; pr += kWarps) {
-    const int t = pr >> 1;
-    const float* v = (pr & 1) ? sk[t] : sq[t];
-    const float4 x4 = reinterpret_cast<const float4*>(v)[lane];
-    float ss = x4.x * x4.x;
-    ss = fmaf(x4.y, x4.y, ss);
-    ss = fmaf(x4.z, x4.z, ss);
-    ss = fmaf(x4.w, x4.w, ss);
-    ss = warp_sum(ss);
+  // ---- L2 norms of q and k and k^ . q^ (a warp per token), gates ----
+  static_assert(kDecodeMaxSteps <= kWarps, "a warp per token");
+  if (warp < K) {
+    float rq, rk, kq;
+    token_norms(sq[warp], sk[warp], lane, p.l2_eps, rq, rk, kq);
     if (lane == 0) {
-      const float r = rsqrtf(ss + p.l2_eps);
-      if (pr & 1) s_rk[t] = r;
-      else s_rq[t] = r * rsqrtf((float)kD);
+      s_rq[warp] = rq;
+      s_rk[warp] = rk;
+      s_kq[warp] = kq;
     }
   }
   for (int i = tid; i < K * G; i += kThreads) {
@@ -319,58 +399,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
     s_beta[t][g] = sigmoid(bf16_to_f32(p.b[ab]));
   }
   __syncthreads();
+  for (int i = tid; i < K * kD; i += kThreads) {
+    const int t = i / kD, c = i - t * kD;
+    sq[t][c] *= s_rq[t];
+    sk[t][c] *= s_rk[t];
+  }
+  __syncthreads();
 
   // ---- the state stream: each batch of rows through every token ----
 #pragma unroll
   for (int nb = 0; nb < kBatches; ++nb) {
-    float4 nxt[kRowsPerBatch];
-    if (nb + 1 < kBatches) {
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) nxt[j] = __ldcs(row_ptr(nb + 1, j));
-    }
+    RowBatch nxt;
+    if (nb + 1 < kBatches) load_rows(nxt, batch_rows(nb + 1), rr, q);
     const int vh = nb / kBatchesPerHead;
-    const int r0 = row_of(nb, 0);
+    const int r0 = batch_row0(nb);
 #pragma unroll 1
     for (int t = 0; t < K; ++t) {
-      float qh[4], kk[4];
-      const float rq = s_rq[t], rk = s_rk[t];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        qh[i] = sq[t][4 * lane + i] * rq;
-        kk[i] = sk[t][4 * lane + i] * rk;
-      }
-      const float decay = s_decay[t][vh], beta = s_beta[t][vh];
-      float red[kRowsPerBatch];
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) {
-        cur[j].x *= decay; cur[j].y *= decay; cur[j].z *= decay; cur[j].w *= decay;
-        red[j] = dot4(cur[j], kk);
-      }
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) red[j] = warp_sum(red[j]);
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) {
-        const float u = beta * (sv[t][vh][r0 + j] - red[j]);
-        cur[j].x = fmaf(u, kk[0], cur[j].x);
-        cur[j].y = fmaf(u, kk[1], cur[j].y);
-        cur[j].z = fmaf(u, kk[2], cur[j].z);
-        cur[j].w = fmaf(u, kk[3], cur[j].w);
-        if (p.ssm_trace) __stcs(trace_ptr(t, nb, j), cur[j]);
-        red[j] = dot4(cur[j], qh);
-      }
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) red[j] = warp_sum(red[j]);
-      if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < kRowsPerBatch; ++j) so[t][vh][r0 + j] = red[j];
+      LaneCols qh, kk;
+      load_lane_cols(qh, sq[t], q);
+      load_lane_cols(kk, sk[t], q);
+      const float v[2] = {sv[t][vh][r0 + rr], sv[t][vh][r0 + 4 + rr]};
+      float o[2];
+      rows_token(cur, kk, qh, s_decay[t][vh], s_beta[t][vh], s_kq[t], v, o);
+      if (p.ssm_trace) store_rows(trace_rows(t, nb), cur, rr, q);
+      if (q == 0) {
+        so[t][vh][r0 + rr] = o[0];
+        so[t][vh][r0 + 4 + rr] = o[1];
       }
     }
-#pragma unroll
-    for (int j = 0; j < kRowsPerBatch; ++j) __stcs(row_ptr(nb, j), cur[j]);
-    if (nb + 1 < kBatches) {
-#pragma unroll
-      for (int j = 0; j < kRowsPerBatch; ++j) cur[j] = nxt[j];
-    }
+    store_rows(batch_rows(nb), cur, rr, q);
+    if (nb + 1 < kBatches) cur = nxt;
   }
   __syncthreads();
 
@@ -417,6 +475,8 @@ cudaError_t launch_g(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {
 
 cudaError_t launch_decode_multi(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {
   if (p.steps < 1 || p.steps > kDecodeMaxSteps) return cudaErrorInvalidValue;
+  // one token and no trace: the single-step kernel (same layouts, same arithmetic)
+  if (p.steps == 1 && !p.ssm_trace && !p.conv_trace) return launch_decode(p, out_f32, stream);
   switch (p.h_v / p.h_k) {
     case 1: return launch_multi_g<1>(p, out_f32, stream);
     case 2: return launch_multi_g<2>(p, out_f32, stream);
