@@ -85,6 +85,19 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode_multi.restype = ctypes.c_int
             L.gdn_decode_multi.argtypes = [DP] + [_P] * 9 + [ctypes.c_int] * 3 + [_P] * 3 + \
                 [ctypes.c_int] + [_P] * 4
+            L.gdn_state_copy.restype = ctypes.c_int
+            L.gdn_state_copy.argtypes = [DP, _P, _P, ctypes.c_int, _P, _P, _P, ctypes.c_int, _P,
+                                         ctypes.c_int, _P, _P]
+            L.gdn_state_reset.restype = ctypes.c_int
+            L.gdn_state_reset.argtypes = [DP, _P, _P, ctypes.c_int, _P, ctypes.c_int, _P, _P]
+            L.gdn_decode_graph_create.restype = ctypes.c_int
+            L.gdn_decode_graph_create.argtypes = [DP, ctypes.c_int] + [_P] * 9 + \
+                [ctypes.c_int, ctypes.c_int] + [_P] * 3 + [ctypes.c_int, _P,
+                                                           ctypes.POINTER(ctypes.c_void_p)]
+            L.gdn_decode_graph_launch.restype = ctypes.c_int
+            L.gdn_decode_graph_launch.argtypes = [ctypes.c_void_p, _P]
+            L.gdn_decode_graph_destroy.restype = None
+            L.gdn_decode_graph_destroy.argtypes = [ctypes.c_void_p]
             L.gdn_prefill_noalloc.restype = ctypes.c_int
             L.gdn_prefill_noalloc.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
                 [_P] * 5
@@ -225,6 +238,92 @@ def gdn_decode_multi(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, s
         _ptr(conv_trace, f32, "conv_trace", B * K * (dims.conv_w - 1) * Cc),
         _ptr(device_status, torch.int32, "device_status", 1), _stream(stream))
     _check(st, "gdn_decode_multi")
+
+
+class DecodeGraph:
+    """A CUDA graph of ``steps`` successive decode steps over bound buffers
+    (gdn_decode_graph_create); ``launch()`` runs them all, ``close()`` frees it."""
+
+    def __init__(self, handle, keep):
+        self._h = handle
+        self._keep = keep              # the bound tensors stay alive with the graph
+
+    def launch(self, stream=None):
+        if not self._h:
+            raise ValueError("gdn_decode_graph: closed")
+        _check(lib().gdn_decode_graph_launch(self._h, _stream(stream)), "gdn_decode_graph_launch")
+
+    def close(self):
+        if self._h:
+            lib().gdn_decode_graph_destroy(self._h)
+            self._h = None
+            self._keep = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def gdn_decode_graph_create(dims: Dims, steps, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w,
+                            slot, n_slots, conv_state, ssm_state, out, device_status=None):
+    """Capture ``steps`` decode steps over step-major buffers ([steps][batch][...])."""
+    bf, f32 = torch.bfloat16, torch.float32
+    S, B = int(steps), int(out.shape[1])
+    Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
+    out_dtype = GDN_DTYPE_F32 if out.dtype == f32 else GDN_DTYPE_BF16
+    h = ctypes.c_void_p()
+    st = lib().gdn_decode_graph_create(
+        ctypes.byref(dims), S, _ptr(qkv, bf, "qkv", S * B * Cc),
+        _ptr(z, bf, "z", S * B * dims.h_v * dims.d_v), _ptr(a, bf, "a", S * B * dims.h_v),
+        _ptr(b, bf, "b", S * B * dims.h_v), _ptr(A_log, f32, "A_log", dims.h_v),
+        _ptr(dt_bias, f32, "dt_bias", dims.h_v), _ptr(conv_w, bf, "conv_w", Cc * dims.conv_w),
+        _ptr(norm_w, f32, "norm_w", dims.d_v), _ptr(slot, torch.int32, "slot", B), int(n_slots), B,
+        _ptr(conv_state, f32, "conv_state", int(n_slots) * (dims.conv_w - 1) * Cc),
+        _ptr(ssm_state, f32, "ssm_state", int(n_slots) * dims.h_v * dims.d_v * dims.d_k),
+        _ptr(out, out.dtype, "out", S * B * dims.h_v * dims.d_v), out_dtype,
+        _ptr(device_status, torch.int32, "device_status", 1), ctypes.byref(h))
+    _check(st, "gdn_decode_graph_create")
+    keep = (qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, conv_state, ssm_state, out,
+            device_status)
+    return DecodeGraph(h.value, keep)
+
+
+def _pool(dims: Dims, conv_state, ssm_state, name):
+    """Slot count of a state pool ([slots][W-1][Cc] and [slots][h_v][d_v][d_k] fp32)."""
+    n = int(ssm_state.shape[0])
+    Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
+    f32 = torch.float32
+    return n, (_ptr(conv_state, f32, name + " conv_state", n * (dims.conv_w - 1) * Cc),
+               _ptr(ssm_state, f32, name + " ssm_state", n * dims.h_v * dims.d_v * dims.d_k))
+
+
+def gdn_state_copy(dims: Dims, src_conv_state, src_ssm_state, dst_conv_state, dst_ssm_state,
+                   src_slot=None, dst_slot=None, n=None, device_status=None, stream=None):
+    """Copy n whole states from one state pool's slots into another's (snapshot / restore)."""
+    ns, (sc, ss) = _pool(dims, src_conv_state, src_ssm_state, "source")
+    nd, (dc, ds) = _pool(dims, dst_conv_state, dst_ssm_state, "destination")
+    if n is None:
+        n = int(src_slot.numel()) if src_slot is not None else (
+            int(dst_slot.numel()) if dst_slot is not None else min(ns, nd))
+    st = lib().gdn_state_copy(
+        ctypes.byref(dims), sc, ss, ns, _ptr(src_slot, torch.int32, "src_slot", n), dc, ds, nd,
+        _ptr(dst_slot, torch.int32, "dst_slot", n), int(n),
+        _ptr(device_status, torch.int32, "device_status", 1), _stream(stream))
+    _check(st, "gdn_state_copy")
+
+
+def gdn_state_reset(dims: Dims, conv_state, ssm_state, slot=None, n=None, device_status=None,
+                    stream=None):
+    """Zero the states of n slots of a state pool."""
+    ns, (c, s) = _pool(dims, conv_state, ssm_state, "pool")
+    if n is None:
+        n = int(slot.numel()) if slot is not None else ns
+    st = lib().gdn_state_reset(ctypes.byref(dims), c, s, ns, _ptr(slot, torch.int32, "slot", n),
+                               int(n), _ptr(device_status, torch.int32, "device_status", 1),
+                               _stream(stream))
+    _check(st, "gdn_state_reset")
 
 
 def gdn_read_device_status(status_word, stream=None) -> int:

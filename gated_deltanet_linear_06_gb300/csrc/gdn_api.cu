@@ -8,6 +8,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <new>
+
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
@@ -128,84 +130,35 @@ gdn_status gdn_prefill(const gdn_dims* dims, const void* qkv, const void* z, con
   return gdn::launch_prefill(p, s) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
-                           const void* a, const void* b, const float* A_log,
-                           const float* dt_bias, const void* conv_w, const float* norm_w,
-                           const int32_t* slot, int n_slots, int batch, float* conv_state,
-                           float* ssm_state, void* out, int out_dtype,
-                           int32_t* device_status, void* stream) {
-  gdn_status st = check_dims(dims);
-  if (st != GDN_OK) return st;
-  if (batch < 0 || n_slots < 0 || (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32))
-    return GDN_ERR_INVALID_ARG;
-  if (batch == 0) return GDN_OK;
-  if ((long long)batch * dims->h_k > 0x7fffffffLL) return GDN_ERR_INVALID_ARG;
-  if (n_slots < 1 || (!slot && n_slots < batch)) return GDN_ERR_INVALID_ARG;
-  if (!ptr_ok(qkv) || !ptr_ok(z) || !ptr_ok(a) || !ptr_ok(b) || !ptr_ok(A_log) ||
-      !ptr_ok(dt_bias) || !ptr_ok(conv_w) || !ptr_ok(norm_w) || !ptr_ok(conv_state) ||
-      !ptr_ok(ssm_state) || !ptr_ok(out))
-    return GDN_ERR_INVALID_ARG;
-  if (slot && !aligned16(slot)) return GDN_ERR_INVALID_ARG;
-  if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
-    return GDN_ERR_INVALID_ARG;
+}  // extern "C"
 
-  gdn::DecodeArgs p;
-  p.qkv = static_cast<const uint16_t*>(qkv);
-  p.z = static_cast<const uint16_t*>(z);
-  p.a = static_cast<const uint16_t*>(a);
-  p.b = static_cast<const uint16_t*>(b);
-  p.A_log = A_log;
-  p.dt_bias = dt_bias;
-  p.conv_w = static_cast<const uint16_t*>(conv_w);
-  p.norm_w = norm_w;
-  p.slot = slot;
-  p.conv_state = conv_state;
-  p.ssm_state = ssm_state;
-  p.out = out;
-  p.status = device_status;
-  p.n_slots = n_slots;
-  p.batch = batch;
-  p.h_k = dims->h_k;
-  p.h_v = dims->h_v;
-  p.l2_eps = dims->l2_eps;
-  p.rms_eps = dims->rms_eps;
-  p.steps = 1;
-  p.ssm_trace = nullptr;
-  p.conv_trace = nullptr;
-  return gdn::launch_decode(p, out_dtype == GDN_DTYPE_F32, static_cast<cudaStream_t>(stream)) ==
-                 cudaSuccess
-             ? GDN_OK
-             : GDN_ERR_CUDA;
-}
+namespace {
 
-static_assert(GDN_DECODE_MAX_STEPS == gdn::kDecodeMaxSteps, "the header's token limit is the kernel's");
-
-gdn_status gdn_decode_multi(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
-                            const void* b, const float* A_log, const float* dt_bias,
-                            const void* conv_w, const float* norm_w, const int32_t* slot,
-                            int n_slots, int batch, int steps, float* conv_state, float* ssm_state,
-                            void* out, int out_dtype, float* ssm_trace, float* conv_trace,
-                            int32_t* device_status, void* stream) {
+// Host checks shared by the decode entry points; fills p on success.  `steps`
+// tokens per sequence per launch (1 for the single step).
+gdn_status decode_args(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
+                       const void* b, const float* A_log, const float* dt_bias,
+                       const void* conv_w, const float* norm_w, const int32_t* slot, int n_slots,
+                       int batch, int steps, float* conv_state, float* ssm_state, void* out,
+                       int out_dtype, float* ssm_trace, float* conv_trace,
+                       int32_t* device_status, gdn::DecodeArgs& p) {
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
   if (batch < 0 || n_slots < 0 || steps < 1 || steps > GDN_DECODE_MAX_STEPS ||
       (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32))
     return GDN_ERR_INVALID_ARG;
-  if (batch == 0) return GDN_OK;
   if ((long long)batch * dims->h_k > 0x7fffffffLL || (long long)batch * steps > 0x7fffffffLL)
     return GDN_ERR_INVALID_ARG;
-  if (n_slots < 1 || (!slot && n_slots < batch)) return GDN_ERR_INVALID_ARG;
-  if (!ptr_ok(qkv) || !ptr_ok(z) || !ptr_ok(a) || !ptr_ok(b) || !ptr_ok(A_log) ||
-      !ptr_ok(dt_bias) || !ptr_ok(conv_w) || !ptr_ok(norm_w) || !ptr_ok(conv_state) ||
-      !ptr_ok(ssm_state) || !ptr_ok(out))
+  if (batch > 0 && (n_slots < 1 || (!slot && n_slots < batch))) return GDN_ERR_INVALID_ARG;
+  if (batch > 0 && (!ptr_ok(qkv) || !ptr_ok(z) || !ptr_ok(a) || !ptr_ok(b) || !ptr_ok(A_log) ||
+                    !ptr_ok(dt_bias) || !ptr_ok(conv_w) || !ptr_ok(norm_w) ||
+                    !ptr_ok(conv_state) || !ptr_ok(ssm_state) || !ptr_ok(out)))
     return GDN_ERR_INVALID_ARG;
   if ((slot && !aligned16(slot)) || (ssm_trace && !aligned16(ssm_trace)) ||
       (conv_trace && !aligned16(conv_trace)))
     return GDN_ERR_INVALID_ARG;
   if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
     return GDN_ERR_INVALID_ARG;
-
-  gdn::DecodeArgs p;
   p.qkv = static_cast<const uint16_t*>(qkv);
   p.z = static_cast<const uint16_t*>(z);
   p.a = static_cast<const uint16_t*>(a);
@@ -228,10 +181,191 @@ gdn_status gdn_decode_multi(const gdn_dims* dims, const void* qkv, const void* z
   p.steps = steps;
   p.ssm_trace = ssm_trace;
   p.conv_trace = conv_trace;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
+                           const void* a, const void* b, const float* A_log,
+                           const float* dt_bias, const void* conv_w, const float* norm_w,
+                           const int32_t* slot, int n_slots, int batch, float* conv_state,
+                           float* ssm_state, void* out, int out_dtype,
+                           int32_t* device_status, void* stream) {
+  gdn::DecodeArgs p;
+  const gdn_status st = decode_args(dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot,
+                                    n_slots, batch, 1, conv_state, ssm_state, out, out_dtype,
+                                    nullptr, nullptr, device_status, p);
+  if (st != GDN_OK || batch == 0) return st;
+  return gdn::launch_decode(p, out_dtype == GDN_DTYPE_F32, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
+static_assert(GDN_DECODE_MAX_STEPS == gdn::kDecodeMaxSteps, "the header's token limit is the kernel's");
+
+gdn_status gdn_decode_multi(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
+                            const void* b, const float* A_log, const float* dt_bias,
+                            const void* conv_w, const float* norm_w, const int32_t* slot,
+                            int n_slots, int batch, int steps, float* conv_state, float* ssm_state,
+                            void* out, int out_dtype, float* ssm_trace, float* conv_trace,
+                            int32_t* device_status, void* stream) {
+  gdn::DecodeArgs p;
+  const gdn_status st = decode_args(dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot,
+                                    n_slots, batch, steps, conv_state, ssm_state, out, out_dtype,
+                                    ssm_trace, conv_trace, device_status, p);
+  if (st != GDN_OK || batch == 0) return st;
   return gdn::launch_decode_multi(p, out_dtype == GDN_DTYPE_F32, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
              ? GDN_OK
              : GDN_ERR_CUDA;
+}
+
+}  // extern "C"
+
+// A captured chain of single decode steps: the graph and its executable form.
+struct gdn_decode_graph {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+extern "C" {
+
+gdn_status gdn_decode_graph_create(const gdn_dims* dims, int steps, const void* qkv, const void* z,
+                                   const void* a, const void* b, const float* A_log,
+                                   const float* dt_bias, const void* conv_w, const float* norm_w,
+                                   const int32_t* slot, int n_slots, int batch, float* conv_state,
+                                   float* ssm_state, void* out, int out_dtype,
+                                   int32_t* device_status, gdn_decode_graph** graph) {
+  if (!graph) return GDN_ERR_INVALID_ARG;
+  *graph = nullptr;
+  if (steps < 1 || steps > (1 << 20) || batch < 1) return GDN_ERR_INVALID_ARG;
+  gdn::DecodeArgs p;
+  gdn_status st = decode_args(dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,
+                              batch, 1, conv_state, ssm_state, out, out_dtype, nullptr, nullptr,
+                              device_status, p);
+  if (st != GDN_OK) return st;
+  const bool f32 = out_dtype == GDN_DTYPE_F32;
+  // per-step strides of the step-major buffers, in elements
+  const size_t cc = (size_t)channels(dims), hv = (size_t)dims->h_v, dv = (size_t)dims->d_v;
+  const size_t qkv_step = (size_t)batch * cc, z_step = (size_t)batch * hv * dv;
+  const size_t ab_step = (size_t)batch * hv, out_step_bytes = z_step * (f32 ? 4 : 2);
+
+  cudaStream_t s = nullptr;
+  if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return GDN_ERR_CUDA;
+  cudaError_t err = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+  if (err != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return GDN_ERR_CUDA;
+  }
+  for (int t = 0; t < steps && err == cudaSuccess; ++t) {
+    gdn::DecodeArgs q = p;
+    q.qkv = p.qkv + t * qkv_step;
+    q.z = p.z + t * z_step;
+    q.a = p.a + t * ab_step;
+    q.b = p.b + t * ab_step;
+    q.out = static_cast<char*>(p.out) + t * out_step_bytes;
+    err = gdn::launch_decode(q, f32, s);
+  }
+  cudaGraph_t g = nullptr;
+  const cudaError_t end = cudaStreamEndCapture(s, &g);
+  cudaStreamDestroy(s);
+  if (err != cudaSuccess || end != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return GDN_ERR_CUDA;
+  }
+  cudaGraphExec_t x = nullptr;
+  if (cudaGraphInstantiate(&x, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return GDN_ERR_CUDA;
+  }
+  gdn_decode_graph* h = new (std::nothrow) gdn_decode_graph{g, x};
+  if (!h) {
+    cudaGraphExecDestroy(x);
+    cudaGraphDestroy(g);
+    return GDN_ERR_CUDA;
+  }
+  *graph = h;
+  return GDN_OK;
+}
+
+gdn_status gdn_decode_graph_launch(gdn_decode_graph* graph, void* stream) {
+  if (!graph) return GDN_ERR_INVALID_ARG;
+  return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
+void gdn_decode_graph_destroy(gdn_decode_graph* graph) {
+  if (!graph) return;
+  cudaGraphExecDestroy(graph->exec);
+  cudaGraphDestroy(graph->graph);
+  delete graph;
+}
+
+}  // extern "C"
+
+namespace {
+
+gdn_status state_copy(const gdn_dims* dims, const float* src_conv, const float* src_ssm,
+                      int src_slots, const int32_t* src_slot, float* dst_conv, float* dst_ssm,
+                      int dst_slots, const int32_t* dst_slot, int n, int32_t* device_status,
+                      void* stream) {
+  gdn_status st = check_dims(dims);
+  if (st != GDN_OK) return st;
+  if (n < 0 || n > 65535) return GDN_ERR_INVALID_ARG;
+  if (n == 0) return GDN_OK;
+  const bool zero = src_ssm == nullptr;
+  if (dst_slots < 1 || (!dst_slot && dst_slots < n)) return GDN_ERR_INVALID_ARG;
+  if (!ptr_ok(dst_conv) || !ptr_ok(dst_ssm) || (dst_slot && !aligned16(dst_slot)))
+    return GDN_ERR_INVALID_ARG;
+  if (!zero) {
+    if (src_slots < 1 || (!src_slot && src_slots < n)) return GDN_ERR_INVALID_ARG;
+    if (!ptr_ok(src_conv) || !ptr_ok(src_ssm) || (src_slot && !aligned16(src_slot)))
+      return GDN_ERR_INVALID_ARG;
+  }
+  if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u))
+    return GDN_ERR_INVALID_ARG;
+  gdn::StateCopyArgs p;
+  p.src_conv = zero ? nullptr : src_conv;
+  p.src_ssm = zero ? nullptr : src_ssm;
+  p.src_idx = zero ? nullptr : src_slot;
+  p.dst_conv = dst_conv;
+  p.dst_ssm = dst_ssm;
+  p.dst_idx = dst_slot;
+  p.status = device_status;
+  p.conv_floats = (long long)(dims->conv_w - 1) * channels(dims);
+  p.ssm_floats = (long long)dims->h_v * dims->d_v * dims->d_k;
+  p.src_slots = zero ? 0 : src_slots;
+  p.dst_slots = dst_slots;
+  p.n = n;
+  return gdn::launch_state_copy(p, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_state_copy(const gdn_dims* dims, const float* src_conv_state,
+                          const float* src_ssm_state, int src_slots, const int32_t* src_slot,
+                          float* dst_conv_state, float* dst_ssm_state, int dst_slots,
+                          const int32_t* dst_slot, int n, int32_t* device_status, void* stream) {
+  if (!src_conv_state || !src_ssm_state) return GDN_ERR_INVALID_ARG;
+  return state_copy(dims, src_conv_state, src_ssm_state, src_slots, src_slot, dst_conv_state,
+                    dst_ssm_state, dst_slots, dst_slot, n, device_status, stream);
+}
+
+gdn_status gdn_state_reset(const gdn_dims* dims, float* conv_state, float* ssm_state, int n_slots,
+                           const int32_t* slot, int n, int32_t* device_status, void* stream) {
+  return state_copy(dims, nullptr, nullptr, 0, nullptr, conv_state, ssm_state, n_slots, slot, n,
+                    device_status, stream);
 }
 
 gdn_status gdn_read_device_status(const void* status_word, void* stream, int32_t* code) {

@@ -66,12 +66,31 @@ struct PrefillArgs {
   float l2_eps, rms_eps;
 };
 
+// Slot-to-slot copies of whole states (conv state then SSM state of a slot).
+// Pair i copies source slot src_idx[i] (i when src_idx is null) to destination
+// slot dst_idx[i] (i when null); with src_conv = src_ssm = null it zeroes the
+// destination slot instead.  Slot indices are checked on the device.
+struct StateCopyArgs {
+  const float* src_conv;
+  const float* src_ssm;
+  const int32_t* src_idx;
+  float* dst_conv;
+  float* dst_ssm;
+  const int32_t* dst_idx;
+  int32_t* status;
+  long long conv_floats;  // per slot: (W-1) * Cc
+  long long ssm_floats;   // per slot: h_v * d_v * d_k
+  int src_slots, dst_slots, n;
+};
+
 // Host launchers: enqueue on `stream`, return the launch error (or
 // cudaSuccess).  Dims are validated by the caller.
 cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream);
 // p.steps tokens per sequence in one launch (1 <= steps <= kDecodeMaxSteps).
 constexpr int kDecodeMaxSteps = 8;
 cudaError_t launch_decode_multi(const DecodeArgs& p, bool out_f32, cudaStream_t stream);
+// n <= 65535 pairs per launch.
+cudaError_t launch_state_copy(const StateCopyArgs& p, cudaStream_t stream);
 // allow_split = false keeps every sequence in one segment (no transfer maps in
 // the scratch); the scratch then needs only prefill_scratch_bytes_unsplit().
 cudaError_t launch_prefill(const PrefillArgs& p, cudaStream_t stream, bool allow_split = true);

@@ -3,6 +3,8 @@
   python -m gated_deltanet_linear_06_gb300.profile_case --kernel prefill --tokens 8192
   python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode --batch 128
   python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode_multi --batch 256 --steps 4
+  python -m gated_deltanet_linear_06_gb300.profile_case --kernel state_copy --batch 256
+  python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode_graph --batch 3 --steps 64
 
 Builds seeded synthetic inputs (the same distributions as the benchmark),
 runs the kernel ``--warmup`` times, then ``--iters`` times, and prints the
@@ -28,7 +30,7 @@ def main():
     import gdn_inputs as gi
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["prefill", "decode", "decode_multi"], required=True)
+    ap.add_argument("--kernel", choices=["prefill", "decode", "decode_multi", "state_copy", "decode_graph"], required=True)
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: tokens of one sequence")
     ap.add_argument("--seqs", type=int, default=1, help="prefill: equal-length sequences")
     ap.add_argument("--batch", type=int, default=128, help="decode: sequences")
@@ -68,6 +70,29 @@ def main():
             gdn.gdn_decode_step(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
                                 p["conv_w"], p["norm_w"], None, B, conv, ssm, out, stream=stream)
         unit, per_call = "seq-steps", B
+    elif args.kernel == "decode_graph":
+        B, S = args.batch, args.steps
+        p = {k: v.to(dev) for k, v in gi.make_params(sh, 1).items()}
+        st = gi.make_states(sh, B, 1, ssm_std=0.1 ** 0.5, conv_std=1.0)
+        conv, ssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
+        x = {k: v.to(dev) for k, v in gi.make_tokens(sh, S * B, 1).items()}
+        out = torch.empty(S, B, sh.h_v, 128, dtype=torch.bfloat16, device=dev)
+        graph = gdn.gdn_decode_graph_create(dims, S, x["qkv"], x["z"], x["a"], x["b"], p["A_log"],
+                                            p["dt_bias"], p["conv_w"], p["norm_w"], None, B, conv,
+                                            ssm, out)
+
+        def call():
+            graph.launch(stream=stream)
+        unit, per_call = "seq-steps", B * S
+    elif args.kernel == "state_copy":
+        B = args.batch
+        st = gi.make_states(sh, B, 5, ssm_std=0.1 ** 0.5, conv_std=1.0)
+        conv, ssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
+        bconv, bssm = torch.empty_like(conv), torch.empty_like(ssm)
+
+        def call():
+            gdn.gdn_state_copy(dims, conv, ssm, bconv, bssm, stream=stream)
+        unit, per_call = "GB", 2e-9 * gdn.gdn_state_bytes(dims) * B
     else:
         B, K = args.batch, args.steps
         p = {k: v.to(dev) for k, v in gi.make_params(sh, 4).items()}

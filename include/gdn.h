@@ -184,6 +184,67 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
                            float* ssm_state, void* out, int out_dtype,
                            int32_t* device_status, void* stream);
 
+/*
+ * Copy whole sequence states between slots of caller-owned state pools:
+ * snapshot a prefix's state into a bank and restore it later, or fork one
+ * sequence's state into several ("xwen" README, batch mode: the shared prefix
+ * is prefilled once and restored for every item; "Our own inference runtime",
+ * section "What it is": state "snapshot banks").  The copy is exact, so
+ * decoding or prefilling from a restored state gives, bit for bit, what the
+ * uninterrupted run gives.
+ *
+ *   src_conv_state, src_ssm_state  fp32 [src_slots][W-1][Cc], [src_slots][h_v][d_v][d_k]
+ *   dst_conv_state, dst_ssm_state  fp32 [dst_slots][...] the same per-slot layout (output)
+ *   src_slot, dst_slot  NULL (pair i uses slot i; the pool then needs >= n slots)
+ *              or int32 [n] DEVICE arrays of slot indices.  A pair whose index is
+ *              out of range is skipped on the device and GDN_ERR_DEVICE_BOUNDS is
+ *              written to *device_status if given.
+ *   n          pairs, 0 .. 65535 (0 launches nothing)
+ * The source and destination slots of one call must not overlap, and no
+ * destination slot may appear twice (the copies run concurrently).  Any dims
+ * gdn_decode_step accepts; other dims return the same status it does.
+ */
+gdn_status gdn_state_copy(const gdn_dims* dims, const float* src_conv_state,
+                          const float* src_ssm_state, int src_slots, const int32_t* src_slot,
+                          float* dst_conv_state, float* dst_ssm_state, int dst_slots,
+                          const int32_t* dst_slot, int n, int32_t* device_status, void* stream);
+
+/*
+ * Zero the conv and SSM states of n slots of a state pool: the start of a new
+ * sequence in a reused slot.  Arguments as for gdn_state_copy's destination.
+ */
+gdn_status gdn_state_reset(const gdn_dims* dims, float* conv_state, float* ssm_state, int n_slots,
+                           const int32_t* slot, int n, int32_t* device_status, void* stream);
+
+/*
+ * A CUDA graph of `steps` successive gdn_decode_step calls, for small batches
+ * whose steps are launch-bound (three sequences decode a step in a few
+ * microseconds of HBM time).  The buffers are bound when the graph is
+ * created; the caller refills them between launches.
+ *
+ *   qkv  bf16 [steps][batch][Cc];  z bf16 [steps][batch][h_v][d_v];
+ *   a, b bf16 [steps][batch][h_v]     step t's tokens at [t]
+ *   out        [steps][batch][h_v][d_v], bf16 or fp32 per out_dtype
+ *   the rest   as for gdn_decode_step (the states advance by `steps` tokens
+ *              per launch)
+ *   steps 1 .. 2^20, batch >= 1
+ *   *graph     receives the handle (NULL on failure)
+ * gdn_decode_graph_launch enqueues one run of all the steps on `stream`;
+ * results are bit-identical to the same gdn_decode_step calls made one by
+ * one.  gdn_decode_graph_destroy frees the handle (NULL is a no-op); the
+ * caller must not destroy a graph with a launch still in flight.
+ */
+typedef struct gdn_decode_graph gdn_decode_graph;
+
+gdn_status gdn_decode_graph_create(const gdn_dims* dims, int steps, const void* qkv, const void* z,
+                                   const void* a, const void* b, const float* A_log,
+                                   const float* dt_bias, const void* conv_w, const float* norm_w,
+                                   const int32_t* slot, int n_slots, int batch, float* conv_state,
+                                   float* ssm_state, void* out, int out_dtype,
+                                   int32_t* device_status, gdn_decode_graph** graph);
+gdn_status gdn_decode_graph_launch(gdn_decode_graph* graph, void* stream);
+void gdn_decode_graph_destroy(gdn_decode_graph* graph);
+
 /* Most tokens per sequence one gdn_decode_multi call takes. */
 #define GDN_DECODE_MAX_STEPS 8
 

@@ -35,7 +35,9 @@ def test_header_declares_the_entry_points():
     names = _declared_functions()
     for want in ("gdn_prefill", "gdn_decode_step", "gdn_workspace_bytes", "gdn_state_bytes",
                  "gdn_read_device_status", "gdn_status_string", "gdn_version",
-                 "gdn_decode_multi", "gdn_prefill_noalloc", "gdn_prefill_segment_tokens"):
+                 "gdn_decode_multi", "gdn_prefill_noalloc", "gdn_prefill_segment_tokens",
+                 "gdn_state_copy", "gdn_state_reset", "gdn_decode_graph_create",
+                 "gdn_decode_graph_launch", "gdn_decode_graph_destroy"):
         assert want in names
 
 
@@ -168,6 +170,64 @@ def test_decode_multi_rejects_bad_arguments(L):
     assert _decode_multi(L, d, out_dtype=5) == INVALID
     assert _decode_multi(L, d, batch=0) == OK
     assert _decode_multi(L, d, batch=0, steps=8) == OK
+
+
+def _copy(L, dims, **kw):
+    args = dict(sc=FAKE, ss=FAKE, ns=4, si=None, dc=FAKE, ds=FAKE, nd=4, di=None, n=4,
+                status=None, stream=None)
+    args.update(kw)
+    return L.gdn_state_copy(ctypes.byref(dims) if dims is not None else None, args["sc"],
+                            args["ss"], args["ns"], args["si"], args["dc"], args["ds"],
+                            args["nd"], args["di"], args["n"], args["status"], args["stream"])
+
+
+def test_state_copy_and_reset_reject_bad_arguments(L):
+    d = gdn.make_dims()
+    assert _copy(L, None) == INVALID
+    assert _copy(L, gdn.make_dims(d_k=64, d_v=64)) == UNSUP
+    assert _copy(L, d, sc=None) == INVALID                  # a copy needs a source
+    assert _copy(L, d, ss=None) == INVALID
+    assert _copy(L, d, dc=None) == INVALID
+    assert _copy(L, d, ds=FAKE + 4) == INVALID              # misaligned
+    assert _copy(L, d, si=FAKE + 4) == INVALID
+    assert _copy(L, d, di=FAKE + 8) == INVALID
+    assert _copy(L, d, status=FAKE + 2) == INVALID
+    assert _copy(L, d, ns=3) == INVALID                     # fewer source slots than pairs
+    assert _copy(L, d, nd=3) == INVALID
+    assert _copy(L, d, ns=0, si=FAKE) == INVALID            # an index array into no slots
+    assert _copy(L, d, n=-1) == INVALID
+    assert _copy(L, d, n=65536, ns=1 << 20, nd=1 << 20) == INVALID
+    assert _copy(L, d, n=0) == OK                           # nothing to launch
+    rst = lambda **kw: L.gdn_state_reset(ctypes.byref(d), kw.get("c", FAKE), kw.get("s", FAKE),
+                                         kw.get("ns", 4), kw.get("slot"), kw.get("n", 4),
+                                         None, None)
+    assert rst(c=None) == INVALID
+    assert rst(s=FAKE + 4) == INVALID
+    assert rst(ns=2) == INVALID
+    assert rst(slot=FAKE + 4) == INVALID
+    assert rst(n=0) == OK
+
+
+def test_decode_graph_create_rejects_bad_arguments_without_a_device(L):
+    d = gdn.make_dims()
+
+    def create(dims=d, steps=4, batch=3, n_slots=3, out=FAKE, graph=True, **kw):
+        h = ctypes.c_void_p(12345)
+        st = L.gdn_decode_graph_create(ctypes.byref(dims) if dims is not None else None, steps,
+                                       FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                       kw.get("slot"), n_slots, batch, FAKE, FAKE, out, 0, None,
+                                       ctypes.byref(h) if graph else None)
+        return st, h.value
+    assert create(graph=False)[0] == INVALID
+    assert create(dims=None) == (INVALID, None)         # the handle is cleared on failure
+    assert create(steps=0)[0] == INVALID
+    assert create(batch=0)[0] == INVALID
+    assert create(n_slots=2)[0] == INVALID
+    assert create(out=FAKE + 4)[0] == INVALID
+    assert create(slot=FAKE + 4)[0] == INVALID
+    assert create(dims=gdn.make_dims(h_k=4, h_v=32))[0] == UNSUP
+    assert L.gdn_decode_graph_launch(None, None) == INVALID
+    L.gdn_decode_graph_destroy(None)                    # a no-op
 
 
 def test_prefill_rejects_bad_arguments(L):

@@ -147,3 +147,28 @@ def test_decode_multi_flags_bad_slots_and_leaves_other_states():
     keep = [0, 1, 2, 3, 4, 5, 6]
     assert torch.equal(ssm_p[keep].cpu(), st["ssm_state"][keep])
     assert torch.equal(conv_p[keep].cpu(), st["conv_state"][keep])
+
+
+def test_decode_multi_one_token_without_traces_equals_single_step():
+    # one token and no trace runs the single-step kernel; with a trace, the
+    # multi-token kernel: both must give the single step's bits
+    B = 11
+    params = to_dev(gi.make_params(SH, 65))
+    st = gi.make_states(SH, B, 65, ssm_std=0.3, conv_std=1.0)
+    toks = _tokens(SH, 1, B, 65)
+    dims = dims_of(SH)
+    res = []
+    for mode in ("single", "multi", "multi_traced"):
+        conv, ssm = st["conv_state"].to(DEV), st["ssm_state"].to(DEV)
+        if mode == "single":
+            out = torch.empty(B, SH.h_v, SH.d_v, device=DEV)
+            _single(dims, to_dev({k: v[0] for k, v in toks.items()}), params, conv, ssm, out)
+        else:
+            out = torch.empty(B, 1, SH.h_v, SH.d_v, device=DEV)
+            tr = torch.empty(B, 1, SH.h_v, SH.d_v, SH.d_k, device=DEV) if mode == "multi_traced" else None
+            _multi(dims, to_dev(_seq_major(toks)), params, conv, ssm, out, 1, ssm_trace=tr)
+            out = out[:, 0]
+        res.append((out, ssm, conv))
+    for other in res[1:]:
+        for x, y in zip(res[0], other):
+            assert torch.equal(x, y)
