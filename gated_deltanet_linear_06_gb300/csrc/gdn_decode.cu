@@ -27,6 +27,8 @@
 // Bit-identity: every value a sequence produces depends only on its own
 // inputs, through reductions in a fixed order (butterfly shuffles over fixed
 // lanes); batch size and batch neighbours change only which CTA runs it.
+#include <atomic>
+
 #include "gdn_common.cuh"
 #include "gdn_launch.h"
 #include "../../include/gdn.h"
@@ -75,6 +77,14 @@ __device__ __forceinline__ void store_rows(float* rows, const RowBatch& R, int r
     for (int i = 0; i < 4; ++i)
       __stcs(reinterpret_cast<float4*>(rows + (size_t)(4 * gi + rr) * kD) + q + 8 * i, R.v[gi][i]);
 }
+
+// 16-byte asynchronous copy global -> shared (L2 only), its commit and wait.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ float2 lo2(const float4& f) { return make_float2(f.x, f.y); }
 __device__ __forceinline__ float2 hi2(const float4& f) { return make_float2(f.z, f.w); }
@@ -290,8 +300,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(DecodeArgs p) {
 // split and butterflies, the gates, each row's decay, dot products, update and
 // output dot, the gated RMSNorm -- so k tokens here give, bit for bit, what k
 // successive single steps give.
+// Bytes of dynamic shared memory of decode_multi_kernel: each warp's staging
+// area for its next batch of rows, [8 chunks of the lane][32 lanes] float4.
+constexpr int kMultiStageBytes = kWarps * 8 * 32 * 16;
+
 template <int G, bool OUT_F32>
-__global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p) {
+__global__ void __launch_bounds__(kThreads, 3) decode_multi_kernel(DecodeArgs p) {
   constexpr int kBatches = G * kBatchesPerHead;
   const int bidx = blockIdx.x / p.h_k;
   const int kh = blockIdx.x - bidx * p.h_k;
@@ -329,9 +343,30 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
     float* base = p.ssm_trace + (((size_t)bidx * K + t) * p.h_v + (size_t)kh * G + vh) * kD * kD;
     return base + (size_t)batch_row0(nb) * kD;
   };
+  // The next batch of rows waits in shared memory, not in registers: each lane
+  // copies its own 8 chunks asynchronously and later reads back only what it
+  // copied, so the registers go to a third CTA per SM instead.
+  extern __shared__ float4 stage_all[];
+  float4* const stage = stage_all + warp * (8 * 32) + lane;
+  auto stage_batch = [&](int nb) {
+    const float* rows = batch_rows(nb);
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        cp_async16(stage + (4 * gi + i) * 32,
+                   reinterpret_cast<const float4*>(rows + (size_t)(4 * gi + rr) * kD) + q + 8 * i);
+    cp_async_commit();
+  };
+  auto take_batch = [&](RowBatch& R) {
+    cp_async_wait_all();
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) R.v[gi][i] = stage[(4 * gi + i) * 32];
+  };
 
-  RowBatch cur;
-  load_rows(cur, batch_rows(0), rr, q);
+  stage_batch(0);
 
   // ---- conv + SiLU over this CTA's channels for every token, the window shifting
   //      one token at a time ----
@@ -407,10 +442,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
   __syncthreads();
 
   // ---- the state stream: each batch of rows through every token ----
-#pragma unroll
+#pragma unroll 1
   for (int nb = 0; nb < kBatches; ++nb) {
-    RowBatch nxt;
-    if (nb + 1 < kBatches) load_rows(nxt, batch_rows(nb + 1), rr, q);
+    RowBatch cur;
+    take_batch(cur);
     const int vh = nb / kBatchesPerHead;
     const int r0 = batch_row0(nb);
 #pragma unroll 1
@@ -421,6 +456,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
       const float v[2] = {sv[t][vh][r0 + rr], sv[t][vh][r0 + 4 + rr]};
       float o[2];
       rows_token(cur, kk, qh, s_decay[t][vh], s_beta[t][vh], s_kq[t], v, o);
+      // the staging area is free again once the first token has consumed the
+      // values read from it: refill it with the next batch
+      if (t == 0 && nb + 1 < kBatches) stage_batch(nb + 1);
       if (p.ssm_trace) store_rows(trace_rows(t, nb), cur, rr, q);
       if (q == 0) {
         so[t][vh][r0 + rr] = o[0];
@@ -428,7 +466,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
       }
     }
     store_rows(batch_rows(nb), cur, rr, q);
-    if (nb + 1 < kBatches) cur = nxt;
   }
   __syncthreads();
 
@@ -455,12 +492,29 @@ __global__ void __launch_bounds__(kThreads, 2) decode_multi_kernel(DecodeArgs p)
   }
 }
 
+template <int G, bool OUT_F32>
+cudaError_t launch_multi_go(const DecodeArgs& p, cudaStream_t stream) {
+  // the staging area takes the block's shared memory past the default 48 KiB;
+  // the attribute is set once per device and instantiation
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (!bit || !(done.load(std::memory_order_acquire) & bit)) {
+    err = cudaFuncSetAttribute(decode_multi_kernel<G, OUT_F32>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMultiStageBytes);
+    if (err != cudaSuccess) return err;
+    done.fetch_or(bit, std::memory_order_release);
+  }
+  decode_multi_kernel<G, OUT_F32>
+      <<<dim3((unsigned)(p.batch * p.h_k)), dim3(kThreads), kMultiStageBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
 template <int G>
 cudaError_t launch_multi_g(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {
-  const dim3 grid((unsigned)(p.batch * p.h_k)), block(kThreads);
-  if (out_f32) decode_multi_kernel<G, true><<<grid, block, 0, stream>>>(p);
-  else decode_multi_kernel<G, false><<<grid, block, 0, stream>>>(p);
-  return cudaGetLastError();
+  return out_f32 ? launch_multi_go<G, true>(p, stream) : launch_multi_go<G, false>(p, stream);
 }
 
 template <int G>
