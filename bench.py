@@ -49,7 +49,8 @@ FLOP_PER_TOKEN = (2 * 64 * (3 * D + 2 * D) + 6 * D * D) * H_V
 PREFILL_BYTES_PER_TOKEN = CC * 2 + H_V * D * 2 + 2 * H_V * 2 + H_V * D * 2
 STATE_BYTES = H_V * D * D * 4 + 3 * CC * 4          # per sequence (ssm + conv)
 # per decode seq-step: state read + write, activations, output
-DECODE_BYTES_PER_SEQSTEP = 2 * STATE_BYTES + CC * 2 + H_V * D * 2 + 2 * H_V * 2 + H_V * D * 2
+DECODE_TOKEN_BYTES = CC * 2 + H_V * D * 2 + 2 * H_V * 2 + H_V * D * 2   # qkv, z, a, b, out
+DECODE_BYTES_PER_SEQSTEP = 2 * STATE_BYTES + DECODE_TOKEN_BYTES
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -225,6 +226,76 @@ def cpu_baseline() -> dict:
 
 # ---- our arm --------------------------------------------------------------------
 
+def _timed(call, iters: int, stream) -> float:
+    """Mean ms of `call` over `iters` calls after 3 warm-up calls (CUDA events on `stream`)."""
+    import torch
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def next_rows(gdn, gi, dims, sh, dev, stream, hbm: float) -> dict:
+    """The paths beyond the headline step, each timed on its own (not part of `value`):
+    4-token decode calls at B = 256, a 256-state snapshot copy, and a 64-step
+    decode graph at B = 3 against the same steps launched one by one."""
+    import torch
+    res = {}
+    B, K = 256, 4
+    p = {k: v.to(dev) for k, v in gi.make_params(sh, DECODE_SEED).items()}
+    st = gi.make_states(sh, B, DECODE_SEED, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    conv, ssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
+    x = {k: v.to(dev) for k, v in gi.make_tokens(sh, B * K, DECODE_SEED).items()}
+    out = torch.empty(B, K, sh.h_v, D, dtype=torch.bfloat16, device=dev)
+    ms = _timed(lambda: gdn.gdn_decode_multi(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"],
+                                             p["dt_bias"], p["conv_w"], p["norm_w"], None, B, conv,
+                                             ssm, out, K, stream=stream), 20, stream)
+    byts = B * (2 * STATE_BYTES + K * DECODE_TOKEN_BYTES)
+    res["decode_multi"] = {"workload": f"{B} sequences x {K} tokens per call",
+                           "value": round(B * K / (ms * 1e-3), 1), "unit": "seq-steps/s",
+                           "ms_per_call": round(ms, 4),
+                           "hbm_frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+    bconv, bssm = torch.empty_like(conv), torch.empty_like(ssm)
+    ms = _timed(lambda: gdn.gdn_state_copy(dims, conv, ssm, bconv, bssm, stream=stream), 20, stream)
+    byts = 2 * B * STATE_BYTES
+    res["state_copy"] = {"workload": f"{B} states, pool to bank",
+                         "value": round(byts / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                         "ms_per_call": round(ms, 4),
+                         "hbm_frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+    del bconv, bssm, conv, ssm, x, out
+    B3, S = 3, 64
+    st = gi.make_states(sh, B3, 1, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    conv, ssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
+    x = {k: v.to(dev).reshape(S, B3, *v.shape[1:])
+         for k, v in gi.make_tokens(sh, S * B3, 1).items()}
+    out = torch.empty(S, B3, sh.h_v, D, dtype=torch.bfloat16, device=dev)
+    graph = gdn.gdn_decode_graph_create(dims, S, x["qkv"], x["z"], x["a"], x["b"], p["A_log"],
+                                        p["dt_bias"], p["conv_w"], p["norm_w"], None, B3, conv,
+                                        ssm, out)
+    try:
+        ms_g = _timed(lambda: graph.launch(stream=stream), 10, stream)
+    finally:
+        graph.close()
+
+    def eager():
+        for t in range(S):
+            gdn.gdn_decode_step(dims, x["qkv"][t], x["z"][t], x["a"][t], x["b"][t], p["A_log"],
+                                p["dt_bias"], p["conv_w"], p["norm_w"], None, B3, conv, ssm,
+                                out[t], stream=stream)
+    ms_e = _timed(eager, 5, stream)
+    res["decode_graph"] = {"workload": f"{B3} sequences, {S} steps per launch",
+                           "value": round(B3 * S / (ms_g * 1e-3), 1), "unit": "seq-steps/s",
+                           "us_per_step": round(ms_g * 1e3 / S, 2),
+                           "eager_us_per_step": round(ms_e * 1e3 / S, 2)}
+    return res
+
+
 def run_ours(args) -> dict | None:
     import torch
 
@@ -349,6 +420,7 @@ def run_ours(args) -> dict | None:
     e2e_dec_ms = aggregate_max(sum(e[2].elapsed_time(e[3]) for e in e2e_ev) / K, world)
     if rank != 0:
         return None
+    extra = next_rows(gdn, gi, dims, sh, dev, stream, float(peaks["hbm_gbs"]))
 
     # kernels one gdn_prefill call launches: the work list and the conv-state
     # hand-off, plus per head group the prep pass and the output scan; when the
@@ -402,6 +474,7 @@ def run_ours(args) -> dict | None:
         "e2e": {"value": round(world * PREFILL_T / (e2e_pre_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre},
         "gpu_launches": K * (prefill_kernels + DECODE_CALLS),
+        "next_rows": extra,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
     }
