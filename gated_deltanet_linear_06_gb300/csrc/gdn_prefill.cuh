@@ -116,11 +116,15 @@ __device__ __forceinline__ float tanh_approx(float x) {
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// SiLU(x) = h + h tanh(h) with h = x / 2, two elements per packed fp32x2 op
+// (each element rounds as the scalar fmul and fma would).
 __device__ __forceinline__ void silu4(float (&x)[4]) {
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float h = 0.5f * x[i];
-    x[i] = fmaf(h, tanh_approx(h), h);
+  for (int pp = 0; pp < 2; ++pp) {
+    const float2 h = __fmul2_rn(make_float2(x[2 * pp], x[2 * pp + 1]), make_float2(0.5f, 0.5f));
+    const float2 r = __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+    x[2 * pp] = r.x;
+    x[2 * pp + 1] = r.y;
   }
 }
 
@@ -134,27 +138,33 @@ __device__ __forceinline__ void conv_quad_staged(const uint8_t* raw_blk, const f
                                                  int L, int tq, int lane, const float (&w)[kConvW][4],
                                                  float (&y)[4][4]) {
   constexpr int kRows = 4 + kConvW - 1;
-  float x[kRows][4];
+  float2 x[kRows][2];   // channel pairs (0, 1) and (2, 3)
 #pragma unroll
   for (int r = 0; r < kRows; ++r) {
     const int tau = t0 + tq - (kConvW - 1) + r;   // position in the sequence
     if (tau >= 0) {
       const uint2 v2 = *reinterpret_cast<const uint2*>(raw_blk + (tq + r) * 256 + lane * 8);
-      x[r][0] = bf16_to_f32(v2.x & 0xffffu); x[r][1] = bf16_to_f32(v2.x >> 16);
-      x[r][2] = bf16_to_f32(v2.y & 0xffffu); x[r][3] = bf16_to_f32(v2.y >> 16);
+      x[r][0] = make_float2(bf16_to_f32(v2.x & 0xffffu), bf16_to_f32(v2.x >> 16));
+      x[r][1] = make_float2(bf16_to_f32(v2.y & 0xffffu), bf16_to_f32(v2.y >> 16));
     } else {
       const float4 v4 = *reinterpret_cast<const float4*>(cs + (size_t)(kConvW - 1 + tau) * cs_stride);
-      x[r][0] = v4.x; x[r][1] = v4.y; x[r][2] = v4.z; x[r][3] = v4.w;
+      x[r][0] = make_float2(v4.x, v4.y);
+      x[r][1] = make_float2(v4.z, v4.w);
     }
   }
+  // taps in order, two channels per packed fp32x2 multiply-add (each channel
+  // rounds as the scalar chain w0 x0, fma(w1, x1, .), ... would)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
+    const bool live = tq + i < L;   // padding tokens of a partial chunk are zero
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float acc = w[0][e] * x[i][e];
+    for (int pp = 0; pp < 2; ++pp) {
+      float2 acc = __fmul2_rn(make_float2(w[0][2 * pp], w[0][2 * pp + 1]), x[i][pp]);
 #pragma unroll
-      for (int j = 1; j < kConvW; ++j) acc = fmaf(w[j][e], x[i + j][e], acc);
-      y[i][e] = tq + i < L ? acc : 0.0f;   // padding tokens of a partial chunk are zero
+      for (int j = 1; j < kConvW; ++j)
+        acc = __ffma2_rn(make_float2(w[j][2 * pp], w[j][2 * pp + 1]), x[i + j][pp], acc);
+      y[i][2 * pp] = live ? acc.x : 0.0f;
+      y[i][2 * pp + 1] = live ? acc.y : 0.0f;
     }
     silu4(y[i]);
   }

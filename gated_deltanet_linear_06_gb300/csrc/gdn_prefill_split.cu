@@ -241,8 +241,10 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         l2_rnorm4(y, p.l2_eps, blk == 0 ? qscale : 1.0f, lane, rn);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) y[i][e] *= rn[i];
+          const float2 r2 = make_float2(rn[i], rn[i]);
+          const float2 a = __fmul2_rn(make_float2(y[i][0], y[i][1]), r2);
+          const float2 b = __fmul2_rn(make_float2(y[i][2], y[i][3]), r2);
+          y[i][0] = a.x; y[i][1] = a.y; y[i][2] = b.x; y[i][3] = b.y;
           const uint32_t o16 = tc::sw128_off(tq + i, 4 * lane, 16384) + (blk == 0 ? 8192u : 0u);
           store_bf16x4(sm.base + L_::KQ, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
           store_f16x4(sm.base + L_::KQ16, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
