@@ -98,6 +98,12 @@ def lib() -> ctypes.CDLL:
             L.gdn_decode_graph_launch.argtypes = [ctypes.c_void_p, _P]
             L.gdn_decode_graph_destroy.restype = None
             L.gdn_decode_graph_destroy.argtypes = [ctypes.c_void_p]
+            L.gdn_prefill_host_workspace_bytes.restype = ctypes.c_size_t
+            L.gdn_prefill_host_workspace_bytes.argtypes = [DP, ctypes.c_int, ctypes.c_longlong,
+                                                           ctypes.c_int]
+            L.gdn_prefill_host.restype = ctypes.c_int
+            L.gdn_prefill_host.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
+                [_P] * 3 + [ctypes.c_int, _P, ctypes.c_size_t, _P]
             L.gdn_prefill_noalloc.restype = ctypes.c_int
             L.gdn_prefill_noalloc.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
                 [_P] * 5
@@ -141,6 +147,15 @@ def _ptr(t, dtype, name, numel=None):
     if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
         raise ValueError(f"{name}: want a contiguous CUDA {dtype} tensor, "
                          f"got {t.dtype} on {t.device} (contiguous={t.is_contiguous()})")
+    if numel is not None and t.numel() != numel:
+        raise ValueError(f"{name}: want {numel} elements, got {t.numel()}")
+    return t.data_ptr()
+
+
+def _hptr(t, dtype, name, numel=None):
+    """Address of a contiguous HOST tensor (pinned memory lets copies overlap)."""
+    if not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: want a contiguous host {dtype} tensor")
     if numel is not None and t.numel() != numel:
         raise ValueError(f"{name}: want {numel} elements, got {t.numel()}")
     return t.data_ptr()
@@ -238,6 +253,33 @@ def gdn_decode_multi(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, s
         _ptr(conv_trace, f32, "conv_trace", B * K * (dims.conv_w - 1) * Cc),
         _ptr(device_status, torch.int32, "device_status", 1), _stream(stream))
     _check(st, "gdn_decode_multi")
+
+
+def gdn_prefill_host_workspace_bytes(dims: Dims, n_seqs: int, total_tokens: int,
+                                     seg_tokens: int = 0) -> int:
+    return lib().gdn_prefill_host_workspace_bytes(ctypes.byref(dims), int(n_seqs),
+                                                  int(total_tokens), int(seg_tokens))
+
+
+def gdn_prefill_host(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, cu_seqlens,
+                     conv_state, ssm_state, out, workspace, seg_tokens=0, stream=None):
+    """gdn_prefill from host activations (qkv, z, a, b, cu_seqlens, out on the host;
+    parameters, states and workspace on the device), copies overlapped with compute."""
+    bf, f32 = torch.bfloat16, torch.float32
+    N = int(cu_seqlens.numel()) - 1
+    T = int(qkv.shape[0])
+    Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
+    st = lib().gdn_prefill_host(
+        ctypes.byref(dims), _hptr(qkv, bf, "qkv", T * Cc), _hptr(z, bf, "z", T * dims.h_v * dims.d_v),
+        _hptr(a, bf, "a", T * dims.h_v), _hptr(b, bf, "b", T * dims.h_v),
+        _ptr(A_log, f32, "A_log", dims.h_v), _ptr(dt_bias, f32, "dt_bias", dims.h_v),
+        _ptr(conv_w, bf, "conv_w", Cc * dims.conv_w), _ptr(norm_w, f32, "norm_w", dims.d_v),
+        _hptr(cu_seqlens, torch.int32, "cu_seqlens", N + 1), N, T,
+        _ptr(conv_state, f32, "conv_state", N * (dims.conv_w - 1) * Cc),
+        _ptr(ssm_state, f32, "ssm_state", N * dims.h_v * dims.d_v * dims.d_k),
+        _hptr(out, bf, "out", T * dims.h_v * dims.d_v), int(seg_tokens),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream))
+    _check(st, "gdn_prefill_host")
 
 
 class DecodeGraph:

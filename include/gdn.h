@@ -185,6 +185,42 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
                            int32_t* device_status, void* stream);
 
 /*
+ * gdn_prefill with the activations in HOST memory: the call copies the inputs
+ * in and the output out itself, overlapping the host link with the compute.
+ *
+ * The packed tokens are cut into segments of seg_tokens (0: 4096) tokens, fed
+ * as a chunked-prefill scheduler would (llmxabe README, worker diagram): each
+ * segment is one gdn_prefill call whose sequences continue from the states the
+ * previous segment left.  Two library copy streams move segment i+1's inputs
+ * host->device and segment i-1's output device->host while segment i computes.
+ * The result equals those gdn_prefill calls made one after another (a segment
+ * boundary inside a sequence changes rounding only, as any chunked prefill).
+ *
+ *   qkv, z, a, b   HOST bf16, layouts as for gdn_prefill; pinned (page-locked)
+ *                  memory lets the copies overlap, pageable memory still works
+ *   A_log, dt_bias, conv_w, norm_w   DEVICE, as for gdn_prefill
+ *   cu_seqlens     HOST int32 [n_seqs + 1], read during the call (checked on
+ *                  the host: 0 first, non-decreasing, total_tokens last)
+ *   conv_state, ssm_state            DEVICE, in/out, as for gdn_prefill
+ *   out            HOST bf16 [total_tokens][h_v][d_v] (output)
+ *   seg_tokens     0 or >= 64
+ *   workspace      DEVICE, 256-byte aligned, >= gdn_prefill_host_workspace_bytes();
+ *                  the int32 at offset 0 holds the first nonzero device status of
+ *                  any segment (read it with gdn_read_device_status)
+ * Everything is ordered after the caller's earlier work on `stream`, and work
+ * enqueued on `stream` afterwards sees the output in host memory.  Not for
+ * stream capture.  Concurrent calls on one device share the copy streams.
+ */
+size_t gdn_prefill_host_workspace_bytes(const gdn_dims* dims, int n_seqs, long long total_tokens,
+                                        int seg_tokens);
+gdn_status gdn_prefill_host(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
+                            const void* b, const float* A_log, const float* dt_bias,
+                            const void* conv_w, const float* norm_w, const int32_t* cu_seqlens,
+                            int n_seqs, long long total_tokens, float* conv_state,
+                            float* ssm_state, void* out, int seg_tokens, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+/*
  * Copy whole sequence states between slots of caller-owned state pools:
  * snapshot a prefix's state into a bank and restore it later, or fork one
  * sequence's state into several ("xwen" README, batch mode: the shared prefix

@@ -37,7 +37,8 @@ def test_header_declares_the_entry_points():
                  "gdn_read_device_status", "gdn_status_string", "gdn_version",
                  "gdn_decode_multi", "gdn_prefill_noalloc", "gdn_prefill_segment_tokens",
                  "gdn_state_copy", "gdn_state_reset", "gdn_decode_graph_create",
-                 "gdn_decode_graph_launch", "gdn_decode_graph_destroy"):
+                 "gdn_decode_graph_launch", "gdn_decode_graph_destroy", "gdn_prefill_host",
+                 "gdn_prefill_host_workspace_bytes"):
         assert want in names
 
 
@@ -228,6 +229,31 @@ def test_decode_graph_create_rejects_bad_arguments_without_a_device(L):
     assert create(dims=gdn.make_dims(h_k=4, h_v=32))[0] == UNSUP
     assert L.gdn_decode_graph_launch(None, None) == INVALID
     L.gdn_decode_graph_destroy(None)                    # a no-op
+
+
+def test_prefill_host_rejects_bad_arguments_before_any_device_call(L):
+    d = gdn.make_dims()
+    cu_ok = (ctypes.c_int32 * 3)(0, 100, 250)
+    need = L.gdn_prefill_host_workspace_bytes(ctypes.byref(d), 2, 250, 64)
+    assert need > 0
+    assert L.gdn_prefill_host_workspace_bytes(ctypes.byref(d), 2, 250, 32) == 0   # seg < 64
+    assert L.gdn_prefill_host_workspace_bytes(None, 2, 250, 0) == 0
+
+    def call(dims=d, cu=cu_ok, n=2, T=250, seg=64, ws=0x100000, ws_bytes=None):
+        return L.gdn_prefill_host(ctypes.byref(dims) if dims is not None else None, FAKE, FAKE,
+                                  FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, cu, n, T, FAKE, FAKE, FAKE,
+                                  seg, ws, need if ws_bytes is None else ws_bytes, None)
+    assert call(dims=None) == INVALID
+    assert call(dims=gdn.make_dims(d_k=64, d_v=64)) == UNSUP
+    assert call(cu=None) == INVALID
+    assert call(cu=(ctypes.c_int32 * 3)(0, 100, 249)) == INVALID        # last != total
+    assert call(cu=(ctypes.c_int32 * 3)(1, 100, 250)) == INVALID        # first != 0
+    assert call(cu=(ctypes.c_int32 * 3)(0, 200, 150), T=150) == INVALID  # decreasing
+    assert call(seg=10) == INVALID
+    assert call(seg=-1) == INVALID
+    assert call(ws_bytes=need - 1) == WS
+    assert call(ws=0x100010) == WS                                      # not 256-aligned
+    assert call(cu=(ctypes.c_int32 * 1)(0), n=0, T=0) == OK             # nothing to do
 
 
 def test_prefill_rejects_bad_arguments(L):
