@@ -27,15 +27,20 @@
  * Conventions for every call:
  *   - The caller owns all memory.  The library never allocates or frees
  *     device memory and never synchronises (gdn_read_device_status is the one
- *     call that waits).  The only resources it creates are, once per device,
- *     the side streams and events of gdn_prefill's head groups (below).
+ *     call that waits; gdn_prefill_host from pageable host memory may wait in
+ *     the runtime's copies).  The only resources it creates are, once per
+ *     device, the side streams and events of gdn_prefill's head groups and of
+ *     gdn_prefill_host's copies, and the CUDA graph a gdn_decode_graph handle
+ *     owns until it is destroyed.
  *   - Calls are asynchronous on the given stream (a cudaStream_t passed as
  *     void*; NULL = the legacy default stream).  The returned status covers
  *     host-side validation and the launch only.  Device-side checks
  *     (cu_seqlens contents, slot indices, bounded waits) write a code into a
  *     device status word instead of faulting; read it with
  *     gdn_read_device_status.
- *   - On any non-OK status nothing was launched and no buffer was touched.
+ *   - On GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED or GDN_ERR_WORKSPACE nothing
+ *     was launched and no buffer was touched.  GDN_ERR_CUDA can follow part of
+ *     a call's launches; the outputs and states are then undefined.
  *   - All device pointers must be 16-byte aligned.  Tensors are dense and
  *     row-major in the shapes given below.
  *   - Activations (qkv, z, a, b), conv weights and the prefill output are

@@ -52,7 +52,7 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_version_and_status_strings(L):
-    assert gdn.gdn_version() >= 100
+    assert gdn.gdn_version() >= 200
     for code in range(7):
         s = gdn.gdn_status_string(code)
         assert s.startswith(gdn.STATUS_NAMES[code])
