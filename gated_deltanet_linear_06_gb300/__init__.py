@@ -101,6 +101,9 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_host_workspace_bytes.restype = ctypes.c_size_t
             L.gdn_prefill_host_workspace_bytes.argtypes = [DP, ctypes.c_int, ctypes.c_longlong,
                                                            ctypes.c_int]
+            L.gdn_prefill_host_segments.restype = ctypes.c_longlong
+            L.gdn_prefill_host_segments.argtypes = [_P, ctypes.c_int, ctypes.c_longlong,
+                                                    ctypes.c_int, _P, ctypes.c_longlong]
             L.gdn_prefill_host.restype = ctypes.c_int
             L.gdn_prefill_host.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
                 [_P] * 3 + [ctypes.c_int, _P, ctypes.c_size_t, _P]
@@ -259,6 +262,20 @@ def gdn_prefill_host_workspace_bytes(dims: Dims, n_seqs: int, total_tokens: int,
                                      seg_tokens: int = 0) -> int:
     return lib().gdn_prefill_host_workspace_bytes(ctypes.byref(dims), int(n_seqs),
                                                   int(total_tokens), int(seg_tokens))
+
+
+def gdn_prefill_host_segments(cu_seqlens, seg_tokens: int = 0) -> list[tuple[int, int, int, int]]:
+    """gdn_prefill_host's segments for a host int32 cu_seqlens: a list of
+    (first token, end token, first sequence, sequence count)."""
+    N = int(cu_seqlens.numel()) - 1
+    cu = _hptr(cu_seqlens, torch.int32, "cu_seqlens", N + 1)
+    T = int(cu_seqlens[-1])
+    n = lib().gdn_prefill_host_segments(cu, N, T, int(seg_tokens), None, 0)
+    if n < 0:
+        raise GdnError(1, "gdn_prefill_host_segments")
+    info = (ctypes.c_longlong * (4 * max(n, 1)))()
+    lib().gdn_prefill_host_segments(cu, N, T, int(seg_tokens), info, n)
+    return [tuple(info[4 * i: 4 * i + 4]) for i in range(n)]
 
 
 def gdn_prefill_host(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, cu_seqlens,

@@ -73,6 +73,46 @@ __global__ void put_ints_kernel(int32_t* dst, int n, const IntBlock blk) {
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The segment length a call uses: seg_tokens, 0 meaning the default, never
+// more than the tokens there are.
+long long effective_seg(int seg_tokens, long long T) {
+  long long seg = seg_tokens > 0 ? seg_tokens : kDefaultSegTokens;
+  return (T > 0 && seg > T) ? T : seg;
+}
+
+// cu_seqlens as the prefill needs it: 0 first, non-decreasing, T last.
+bool cu_valid(const int32_t* cu, int n_seqs, long long T) {
+  if (!cu || n_seqs < 0 || cu[0] != 0 || cu[n_seqs] != T) return false;
+  for (int j = 0; j < n_seqs; ++j)
+    if (cu[j + 1] < cu[j]) return false;
+  return true;
+}
+
+// Segment i: tokens [s0, s1) and the sequences ja .. ja + nj - 1 holding them
+// (from the one holding token s0 to the one holding token s1 - 1; empty
+// sequences between them come along with no tokens, empty ones at a boundary
+// are skipped, which leaves their states as they are, as a call over them would).
+struct SegPlan {
+  long long s0, s1;
+  int ja, nj;
+};
+
+void plan_segments(const int32_t* cu, long long T, long long seg, std::vector<SegPlan>& out) {
+  out.clear();
+  int j = 0;
+  for (long long s0 = 0; s0 < T; s0 += seg) {
+    SegPlan g;
+    g.s0 = s0;
+    g.s1 = s0 + seg < T ? s0 + seg : T;
+    while (cu[j + 1] <= g.s0) ++j;   // the sequence holding token s0
+    int jb = j;
+    while (cu[jb + 1] < g.s1) ++jb;  // the sequence holding token s1 - 1
+    g.ja = j;
+    g.nj = jb - j + 1;
+    out.push_back(g);
+  }
+}
+
 struct HostLayout {
   long long seg;             // tokens per segment
   int nseg;
@@ -81,8 +121,7 @@ struct HostLayout {
 
 bool host_layout(const gdn_dims* d, int n_seqs, long long T, int seg_tokens, HostLayout& l) {
   if (!d || n_seqs < 0 || T < 0 || seg_tokens < 0 || (seg_tokens > 0 && seg_tokens < 64)) return false;
-  l.seg = seg_tokens > 0 ? seg_tokens : kDefaultSegTokens;
-  if (T > 0 && l.seg > T) l.seg = T;
+  l.seg = effective_seg(seg_tokens, T);
   const long long nseg = T > 0 ? (T + l.seg - 1) / l.seg : 0;
   if (nseg > (1 << 24)) return false;
   l.nseg = (int)nseg;
@@ -110,6 +149,22 @@ bool host_layout(const gdn_dims* d, int n_seqs, long long T, int seg_tokens, Hos
 
 extern "C" {
 
+long long gdn_prefill_host_segments(const int32_t* cu_seqlens, int n_seqs, long long total_tokens,
+                                    int seg_tokens, long long* seg_info, long long max_segs) {
+  if (total_tokens < 0 || seg_tokens < 0 || (seg_tokens > 0 && seg_tokens < 64) || max_segs < 0 ||
+      (max_segs > 0 && !seg_info) || !cu_valid(cu_seqlens, n_seqs, total_tokens))
+    return -1;
+  std::vector<SegPlan> segs;
+  plan_segments(cu_seqlens, total_tokens, effective_seg(seg_tokens, total_tokens), segs);
+  for (size_t i = 0; i < segs.size() && (long long)i < max_segs; ++i) {
+    seg_info[4 * i + 0] = segs[i].s0;
+    seg_info[4 * i + 1] = segs[i].s1;
+    seg_info[4 * i + 2] = segs[i].ja;
+    seg_info[4 * i + 3] = segs[i].nj;
+  }
+  return (long long)segs.size();
+}
+
 size_t gdn_prefill_host_workspace_bytes(const gdn_dims* dims, int n_seqs, long long total_tokens,
                                         int seg_tokens) {
   HostLayout l;
@@ -130,10 +185,7 @@ gdn_status gdn_prefill_host(const gdn_dims* dims, const void* qkv, const void* z
   if (dst != GDN_OK) return dst;
   HostLayout l;
   if (!host_layout(dims, n_seqs, total_tokens, seg_tokens, l)) return GDN_ERR_INVALID_ARG;
-  if (!cu_seqlens || n_seqs < 0) return GDN_ERR_INVALID_ARG;
-  if (cu_seqlens[0] != 0 || cu_seqlens[n_seqs] != total_tokens) return GDN_ERR_INVALID_ARG;
-  for (int j = 0; j < n_seqs; ++j)
-    if (cu_seqlens[j + 1] < cu_seqlens[j]) return GDN_ERR_INVALID_ARG;
+  if (!cu_valid(cu_seqlens, n_seqs, total_tokens)) return GDN_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < l.total)
     return GDN_ERR_WORKSPACE;
   if (n_seqs == 0 || total_tokens == 0) return GDN_OK;
@@ -147,28 +199,18 @@ gdn_status gdn_prefill_host(const gdn_dims* dims, const void* qkv, const void* z
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   // per-segment sequence ranges and local cu_seqlens, planned on the host
-  struct Seg {
-    long long s0, s1;
-    int ja, nj;
-    size_t cu_off;   // int32 index into the device cu area
-  };
-  std::vector<Seg> segs((size_t)l.nseg);
+  std::vector<SegPlan> segs;
+  plan_segments(cu_seqlens, total_tokens, l.seg, segs);
+  if ((int)segs.size() != l.nseg) return GDN_ERR_INVALID_ARG;
+  std::vector<size_t> cu_off(segs.size());   // int32 index of each segment's cu_seqlens
   std::vector<int32_t> cu_all;
   cu_all.reserve((size_t)n_seqs + 6 * (size_t)l.nseg + 8);
-  int j = 0;
-  for (int i = 0; i < l.nseg; ++i) {
-    Seg& g = segs[(size_t)i];
-    g.s0 = (long long)i * l.seg;
-    g.s1 = g.s0 + l.seg < total_tokens ? g.s0 + l.seg : total_tokens;
-    while (cu_seqlens[j + 1] <= g.s0) ++j;   // the sequence holding token s0
-    int jb = j;
-    while (cu_seqlens[jb + 1] < g.s1) ++jb;  // the sequence holding token s1 - 1
-    g.ja = j;
-    g.nj = jb - j + 1;
+  for (size_t i = 0; i < segs.size(); ++i) {
+    const SegPlan& g = segs[i];
     while (cu_all.size() % 4) cu_all.push_back(0);   // gdn_prefill wants 16-byte-aligned cu_seqlens
-    g.cu_off = cu_all.size();
+    cu_off[i] = cu_all.size();
     cu_all.push_back(0);
-    for (int q = j; q <= jb; ++q) {
+    for (int q = g.ja; q < g.ja + g.nj; ++q) {
       const long long e = cu_seqlens[q + 1] < g.s1 ? cu_seqlens[q + 1] : g.s1;
       cu_all.push_back((int32_t)(e - g.s0));
     }
@@ -210,7 +252,7 @@ gdn_status gdn_prefill_host(const gdn_dims* dims, const void* qkv, const void* z
   const char* hb = static_cast<const char*>(b);
   char* ho = static_cast<char*>(out);
   for (int i = 0; i < l.nseg && st == GDN_OK; ++i) {
-    const Seg& g = segs[(size_t)i];
+    const SegPlan& g = segs[(size_t)i];
     const int k = i & 1;
     const size_t n = (size_t)(g.s1 - g.s0);
     const size_t t0 = (size_t)g.s0;
@@ -226,7 +268,7 @@ gdn_status gdn_prefill_host(const gdn_dims* dims, const void* qkv, const void* z
     if (!cuda_ok(cudaStreamWaitEvent(s, cs->in_done[k], 0))) break;
     if (i >= 2 && !cuda_ok(cudaStreamWaitEvent(s, cs->out_done[k], 0))) break;
     st = gdn_prefill(dims, ws + l.in_qkv[k], ws + l.in_z[k], ws + l.in_a[k], ws + l.in_b[k], A_log,
-                     dt_bias, conv_w, norm_w, cu_dev + g.cu_off, g.nj, (long long)n,
+                     dt_bias, conv_w, norm_w, cu_dev + cu_off[(size_t)i], g.nj, (long long)n,
                      conv_state + (size_t)g.ja * conv_per_seq, ssm_state + (size_t)g.ja * ssm_per_seq,
                      ws + l.out[k], ws + l.pws, l.pws_bytes, stream);
     if (st != GDN_OK) break;

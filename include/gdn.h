@@ -218,6 +218,18 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
  */
 size_t gdn_prefill_host_workspace_bytes(const gdn_dims* dims, int n_seqs, long long total_tokens,
                                         int seg_tokens);
+/*
+ * The segments gdn_prefill_host cuts a batch into (host only, no device use):
+ * returns their count, or -1 for invalid arguments (cu_seqlens as for
+ * gdn_prefill_host, seg_tokens 0 or >= 64), and writes the first max_segs of
+ * them to seg_info as {first token, end token, first sequence, sequence
+ * count}.  Segment i covers tokens [i * seg, min((i + 1) * seg, total)) and the
+ * sequences from the one holding its first token to the one holding its last;
+ * an empty sequence at a segment boundary belongs to no segment (its states
+ * stay as they are).
+ */
+long long gdn_prefill_host_segments(const int32_t* cu_seqlens, int n_seqs, long long total_tokens,
+                                    int seg_tokens, long long* seg_info, long long max_segs);
 gdn_status gdn_prefill_host(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
                             const void* b, const float* A_log, const float* dt_bias,
                             const void* conv_w, const float* norm_w, const int32_t* cu_seqlens,

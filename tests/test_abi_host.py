@@ -9,7 +9,9 @@ import os
 import re
 import subprocess
 
+import numpy as np
 import pytest
+import torch
 
 import gated_deltanet_linear_06_gb300 as gdn
 from gated_deltanet_linear_06_gb300 import build as gbuild
@@ -38,7 +40,7 @@ def test_header_declares_the_entry_points():
                  "gdn_decode_multi", "gdn_prefill_noalloc", "gdn_prefill_segment_tokens",
                  "gdn_state_copy", "gdn_state_reset", "gdn_decode_graph_create",
                  "gdn_decode_graph_launch", "gdn_decode_graph_destroy", "gdn_prefill_host",
-                 "gdn_prefill_host_workspace_bytes"):
+                 "gdn_prefill_host_workspace_bytes", "gdn_prefill_host_segments"):
         assert want in names
 
 
@@ -254,6 +256,48 @@ def test_prefill_host_rejects_bad_arguments_before_any_device_call(L):
     assert call(ws_bytes=need - 1) == WS
     assert call(ws=0x100010) == WS                                      # not 256-aligned
     assert call(cu=(ctypes.c_int32 * 1)(0), n=0, T=0) == OK             # nothing to do
+
+
+def _segments_model(cu, T, seg):
+    """Plain restatement of the segmentation: tokens [s0, s1) and the
+    sequences from the one holding s0 to the one holding s1 - 1."""
+    holder = lambda t: max(q for q in range(len(cu) - 1) if cu[q] <= t < cu[q + 1])
+    out = []
+    for s0 in range(0, T, seg):
+        s1 = min(T, s0 + seg)
+        ja, jb = holder(s0), holder(s1 - 1)
+        out.append((s0, s1, ja, jb - ja + 1))
+    return out
+
+
+def test_prefill_host_segments_match_the_plain_model_and_tile_the_batch(L):
+    # 300 random packed batches (seed 5): 1-12 sequences of 0-3000 tokens,
+    # with empty sequences and lengths at and around segment boundaries
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        n = int(rng.integers(1, 13))
+        pick = rng.integers(0, 4, size=n)
+        lens = np.where(pick == 0, 0, np.where(pick == 1, rng.integers(1, 70, size=n),
+                                               rng.integers(1, 3000, size=n)))
+        if lens.sum() == 0:
+            lens[0] = 1
+        seg = int(rng.choice([0, 64, 100, 1024, 4096]))
+        cu = [0] + list(np.cumsum(lens).astype(int))
+        T = cu[-1]
+        got = gdn.gdn_prefill_host_segments(torch.tensor(cu, dtype=torch.int32), seg)
+        eff = min(seg if seg else 4096, T)
+        assert got == _segments_model(cu, T, eff), (trial, cu, seg)
+        # the segments tile [0, T) and each holds every token of its sequences' overlap
+        assert got[0][0] == 0 and got[-1][1] == T
+        assert all(a[1] == b[0] for a, b in zip(got, got[1:]))
+        for s0, s1, ja, nj in got:
+            held = [q for q in range(n) if cu[q] < s1 and cu[q + 1] > s0]
+            assert held and held[0] == ja and held[-1] == ja + nj - 1
+    bad = torch.tensor([0, 5, 3], dtype=torch.int32)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_host_segments(bad)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_prefill_host_segments(torch.tensor([0, 100], dtype=torch.int32), 32)
 
 
 def test_prefill_rejects_bad_arguments(L):
