@@ -209,6 +209,25 @@ def test_hand_expanded_two_steps():
         np.testing.assert_allclose(S, [[3.0, 0.5], [5.0, 0.75], [7.0, 1.0]], atol=1e-15)
 
 
+@pytest.mark.parametrize("slow", [False, True])
+def test_output_from_the_state_before_the_token_equals_the_oracle(slow):
+    # The decode kernels take o_t from the state before token t:
+    #   u = beta (v - e^g S k),  o = e^g (S q) + u (k . q)
+    # which is S' q with S' = e^g S + u k^T, the oracle's order.  Checked on 8
+    # tokens, d_k = 6, d_v = 5, against the oracle's outputs and states.
+    T = 8
+    q, k, v, g, beta, S0 = _case(17, T, 6, 5, slow=slow)
+    o_ref, _ = oracle.recurrence_seq(q, k, v, g, beta, S0)
+    S = S0.copy()
+    for t in range(T):
+        d = math.exp(g[t])
+        u = beta[t] * (v[t] - d * (S @ k[t]))
+        o = d * (S @ q[t]) + u * float(k[t] @ q[t])
+        np.testing.assert_allclose(o, o_ref[t], rtol=0, atol=1e-12)
+        _, S = oracle.recurrence_seq(q[: t + 1], k[: t + 1], v[: t + 1], g[: t + 1],
+                                     beta[: t + 1], S0)
+
+
 def test_beta0_g0_leaves_state_bitwise():
     q, k, v, _, _, S0 = _case(11, 10, 8, 6)
     o, S = oracle.recurrence_seq(q, k, v, np.zeros(10), np.zeros(10), S0)
