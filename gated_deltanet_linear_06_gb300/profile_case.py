@@ -5,6 +5,7 @@
   python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode_multi --batch 256 --steps 4
   python -m gated_deltanet_linear_06_gb300.profile_case --kernel state_copy --batch 256
   python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode_graph --batch 3 --steps 64
+  python -m gated_deltanet_linear_06_gb300.profile_case --kernel prefill_host --tokens 32768 --seg 4096
 
 Builds seeded synthetic inputs (the same distributions as the benchmark),
 runs the kernel ``--warmup`` times, then ``--iters`` times, and prints the
@@ -30,12 +31,13 @@ def main():
     import gdn_inputs as gi
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["prefill", "decode", "decode_multi", "state_copy", "decode_graph"], required=True)
+    ap.add_argument("--kernel", choices=["prefill", "decode", "decode_multi", "state_copy", "decode_graph", "prefill_host"], required=True)
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: tokens of one sequence")
     ap.add_argument("--seqs", type=int, default=1, help="prefill: equal-length sequences")
     ap.add_argument("--batch", type=int, default=128, help="decode: sequences")
     ap.add_argument("--steps", type=int, default=4, help="decode_multi: tokens per sequence")
     ap.add_argument("--trace", action="store_true", help="decode_multi: also write the SSM trace")
+    ap.add_argument("--seg", type=int, default=0, help="prefill_host: tokens per segment (0: default)")
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
@@ -70,6 +72,24 @@ def main():
             gdn.gdn_decode_step(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
                                 p["conv_w"], p["norm_w"], None, B, conv, ssm, out, stream=stream)
         unit, per_call = "seq-steps", B
+    elif args.kernel == "prefill_host":
+        # activations in pinned host memory, output back to it: the copies are
+        # part of each call
+        N, T = args.seqs, args.seqs * args.tokens
+        p = {k: v.to(dev) for k, v in gi.make_params(sh, 3).items()}
+        x = {k: v.pin_memory() for k, v in gi.make_tokens(sh, T, 3).items()}
+        cu = gi.cu_seqlens([args.tokens] * N)
+        conv = torch.zeros(N, 3, sh.cc, device=dev)
+        ssm = torch.zeros(N, sh.h_v, 128, 128, device=dev)
+        out = torch.empty(T, sh.h_v, 128, dtype=torch.bfloat16).pin_memory()
+        ws = torch.empty(gdn.gdn_prefill_host_workspace_bytes(dims, N, T, args.seg),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            gdn.gdn_prefill_host(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
+                                 p["conv_w"], p["norm_w"], cu, conv, ssm, out, ws,
+                                 seg_tokens=args.seg, stream=stream)
+        unit, per_call = "tokens", T
     elif args.kernel == "decode_graph":
         B, S = args.batch, args.steps
         p = {k: v.to(dev) for k, v in gi.make_params(sh, 1).items()}
