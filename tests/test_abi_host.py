@@ -336,3 +336,41 @@ def test_binding_checks_tensor_arguments(L):
     with pytest.raises(ValueError):
         gdn.gdn_decode_step(d, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, None, 4, cpu, cpu,
                             torch.zeros(4, 32, 128), stream=0)
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include "gdn.h"
+int main(void) {
+  gdn_dims d = {16, 32, 128, 128, 4, 64, 1e-6f, 1e-6f};
+  int32_t cu[4] = {0, 5000, 5000, 9000};
+  long long info[16];
+  long long n = gdn_prefill_host_segments(cu, 3, 9000, 4096, info, 4);
+  gdn_decode_graph* g = NULL;
+  gdn_status bad = gdn_decode_graph_create(&d, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 1, 1, 0, 0, 0, 0, 0, &g);
+  printf("%d %zu %lld %lld %lld %lld %lld %d\n", gdn_version(), gdn_state_bytes(&d), n,
+         info[4], info[5], info[6], info[7], (int)bad);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_a_c_program_links_the_library(L, tmp_path):
+    # the ABI is for C callers: the header must compile as strict C99, and a C
+    # program must link libgdn.so and get the host-only answers without a GPU
+    inc = os.path.dirname(HEADER)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-x", "c",
+                    "-fsyntax-only", HEADER], check=True)
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    libdir = os.path.dirname(gdn.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", inc, str(src), "-L", libdir,
+                    "-lgdn", f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()
+    version, state, nseg, s0, s1, ja, nj, bad = map(int, out)
+    assert version == gdn.gdn_version() and state == gdn.gdn_state_bytes(gdn.make_dims())
+    # 9000 tokens in 4096-token segments: the second covers tokens 4096-8191, from
+    # sequence 0 (tokens 0-4999) through sequence 2 (5000-8999), the empty one between
+    assert (nseg, s0, s1, ja, nj) == (3, 4096, 8192, 0, 3)
+    assert bad == INVALID     # steps = 0
