@@ -58,7 +58,10 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             if log:
                 print(log)
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-Xcompiler", "-fPIC"]
+    # -ldl: the NVTX ranges look up a profiler's library with dlopen (in libc
+    # from glibc 2.34, in libdl before)
+    cmd = [nvcc, "-shared", "-o", tmp] + [o for o, _ in results] + ARCH + ["-Xcompiler", "-fPIC",
+                                                                           "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")

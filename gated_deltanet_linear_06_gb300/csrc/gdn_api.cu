@@ -90,6 +90,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, const void* qkv, const void* z, con
                        int n_seqs, long long total_tokens, float* conv_state,
                        float* ssm_state, void* out, void* workspace, size_t workspace_bytes,
                        void* stream) {
+  gdn::TraceRange trace_range("gdn_prefill");
   gdn_status st = check_dims(dims);
   if (st != GDN_OK) return st;
   if (n_seqs < 0 || total_tokens < 0 || total_tokens > (1LL << 31) - 1)
@@ -194,6 +195,7 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
                            const int32_t* slot, int n_slots, int batch, float* conv_state,
                            float* ssm_state, void* out, int out_dtype,
                            int32_t* device_status, void* stream) {
+  gdn::TraceRange trace_range("gdn_decode_step");
   gdn::DecodeArgs p;
   const gdn_status st = decode_args(dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot,
                                     n_slots, batch, 1, conv_state, ssm_state, out, out_dtype,
@@ -213,6 +215,7 @@ gdn_status gdn_decode_multi(const gdn_dims* dims, const void* qkv, const void* z
                             int n_slots, int batch, int steps, float* conv_state, float* ssm_state,
                             void* out, int out_dtype, float* ssm_trace, float* conv_trace,
                             int32_t* device_status, void* stream) {
+  gdn::TraceRange trace_range("gdn_decode_multi");
   gdn::DecodeArgs p;
   const gdn_status st = decode_args(dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot,
                                     n_slots, batch, steps, conv_state, ssm_state, out, out_dtype,
@@ -240,6 +243,7 @@ gdn_status gdn_decode_graph_create(const gdn_dims* dims, int steps, const void* 
                                    const int32_t* slot, int n_slots, int batch, float* conv_state,
                                    float* ssm_state, void* out, int out_dtype,
                                    int32_t* device_status, gdn_decode_graph** graph) {
+  gdn::TraceRange trace_range("gdn_decode_graph_create");
   if (!graph) return GDN_ERR_INVALID_ARG;
   *graph = nullptr;
   if (steps < 1 || steps > (1 << 20) || batch < 1) return GDN_ERR_INVALID_ARG;
@@ -295,6 +299,7 @@ gdn_status gdn_decode_graph_create(const gdn_dims* dims, int steps, const void* 
 }
 
 gdn_status gdn_decode_graph_launch(gdn_decode_graph* graph, void* stream) {
+  gdn::TraceRange trace_range("gdn_decode_graph_launch");
   if (!graph) return GDN_ERR_INVALID_ARG;
   return cudaGraphLaunch(graph->exec, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? GDN_OK
@@ -357,6 +362,7 @@ gdn_status gdn_state_copy(const gdn_dims* dims, const float* src_conv_state,
                           const float* src_ssm_state, int src_slots, const int32_t* src_slot,
                           float* dst_conv_state, float* dst_ssm_state, int dst_slots,
                           const int32_t* dst_slot, int n, int32_t* device_status, void* stream) {
+  gdn::TraceRange trace_range("gdn_state_copy");
   if (!src_conv_state || !src_ssm_state) return GDN_ERR_INVALID_ARG;
   return state_copy(dims, src_conv_state, src_ssm_state, src_slots, src_slot, dst_conv_state,
                     dst_ssm_state, dst_slots, dst_slot, n, device_status, stream);
@@ -364,11 +370,13 @@ gdn_status gdn_state_copy(const gdn_dims* dims, const float* src_conv_state,
 
 gdn_status gdn_state_reset(const gdn_dims* dims, float* conv_state, float* ssm_state, int n_slots,
                            const int32_t* slot, int n, int32_t* device_status, void* stream) {
+  gdn::TraceRange trace_range("gdn_state_reset");
   return state_copy(dims, nullptr, nullptr, 0, nullptr, conv_state, ssm_state, n_slots, slot, n,
                     device_status, stream);
 }
 
 gdn_status gdn_read_device_status(const void* status_word, void* stream, int32_t* code) {
+  gdn::TraceRange trace_range("gdn_read_device_status");
   if (!status_word || !code || (reinterpret_cast<uintptr_t>(status_word) & 3u))
     return GDN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

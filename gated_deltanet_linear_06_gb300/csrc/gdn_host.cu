@@ -22,6 +22,7 @@
 #include <vector>
 
 #include "../../include/gdn.h"
+#include "gdn_common.cuh"
 
 namespace {
 
@@ -178,6 +179,7 @@ gdn_status gdn_prefill_host(const gdn_dims* dims, const void* qkv, const void* z
                             int n_seqs, long long total_tokens, float* conv_state,
                             float* ssm_state, void* out, int seg_tokens, void* workspace,
                             size_t workspace_bytes, void* stream) {
+  gdn::TraceRange trace_range("gdn_prefill_host");
   // dims as gdn_prefill checks them (an empty problem launches nothing)
   const gdn_status dst = gdn_prefill(dims, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                                      nullptr, nullptr, nullptr, 0, 0, nullptr, nullptr, nullptr,

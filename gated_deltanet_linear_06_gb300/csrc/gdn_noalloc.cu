@@ -66,6 +66,7 @@ extern "C" gdn_status gdn_prefill_noalloc(const gdn_dims* d, const void* qkv, co
                                           int n_seqs, long long total_tokens, float* conv_state,
                                           float* ssm_state, void* out, int32_t* device_status,
                                           void* stream) {
+  gdn::TraceRange trace_range("gdn_prefill_noalloc");
   if (!d) return GDN_ERR_INVALID_ARG;
   if (d->h_k <= 0 || d->h_v <= 0 || d->h_v % d->h_k != 0 || d->d_k <= 0 || d->d_v <= 0 ||
       d->conv_w <= 0 || d->chunk <= 0 || !(d->l2_eps >= 0.0f) || !(d->rms_eps >= 0.0f) ||
