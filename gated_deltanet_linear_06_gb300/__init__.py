@@ -76,6 +76,9 @@ def lib() -> ctypes.CDLL:
             L.gdn_workspace_bytes.argtypes = [DP, ctypes.c_int, ctypes.c_longlong]
             L.gdn_prefill_segment_tokens.restype = ctypes.c_longlong
             L.gdn_prefill_segment_tokens.argtypes = [DP, ctypes.c_int, ctypes.c_longlong]
+            L.gdn_prefill_segment_tokens_for.restype = ctypes.c_longlong
+            L.gdn_prefill_segment_tokens_for.argtypes = [DP, ctypes.c_int, ctypes.c_longlong,
+                                                         ctypes.c_int]
             L.gdn_prefill.restype = ctypes.c_int
             L.gdn_prefill.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
                 [_P] * 4 + [ctypes.c_size_t, _P]
@@ -134,6 +137,12 @@ def gdn_workspace_bytes(dims: Dims, n_seqs: int, total_tokens: int) -> int:
 
 def gdn_prefill_segment_tokens(dims: Dims, n_seqs: int, total_tokens: int) -> int:
     return lib().gdn_prefill_segment_tokens(ctypes.byref(dims), int(n_seqs), int(total_tokens))
+
+
+def gdn_prefill_segment_tokens_for(dims: Dims, n_seqs: int, total_tokens: int, sms: int) -> int:
+    """gdn_prefill's segment length on a GPU with `sms` SMs (no device needed)."""
+    return lib().gdn_prefill_segment_tokens_for(ctypes.byref(dims), int(n_seqs),
+                                                int(total_tokens), int(sms))
 
 
 def _stream(stream) -> int | None:

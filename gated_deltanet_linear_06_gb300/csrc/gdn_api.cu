@@ -84,6 +84,12 @@ long long gdn_prefill_segment_tokens(const gdn_dims* d, int n_seqs, long long to
   return gdn::prefill_segment_tokens(n_seqs, d->h_v, total_tokens, sms);
 }
 
+long long gdn_prefill_segment_tokens_for(const gdn_dims* d, int n_seqs, long long total_tokens,
+                                         int sms) {
+  if (check_dims(d) != GDN_OK || n_seqs < 0 || total_tokens < 0 || sms <= 0) return -1;
+  return gdn::prefill_segment_tokens(n_seqs, d->h_v, total_tokens, sms);
+}
+
 gdn_status gdn_prefill(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
                        const void* b, const float* A_log, const float* dt_bias,
                        const void* conv_w, const float* norm_w, const int32_t* cu_seqlens,

@@ -111,6 +111,10 @@ size_t gdn_workspace_bytes(const gdn_dims* dims, int n_seqs, long long total_tok
  * chunked-prefill scheduler can use it to align its own boundaries; segments
  * never change results beyond rounding. */
 long long gdn_prefill_segment_tokens(const gdn_dims* dims, int n_seqs, long long total_tokens);
+/* The same choice for a GPU with `sms` SMs, without touching a device (for
+ * schedulers that plan ahead, and for tests); -1 for invalid arguments. */
+long long gdn_prefill_segment_tokens_for(const gdn_dims* dims, int n_seqs, long long total_tokens,
+                                         int sms);
 
 /*
  * Chunked prefill over cu_seqlens-packed variable-length sequences.

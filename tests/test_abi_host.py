@@ -40,7 +40,8 @@ def test_header_declares_the_entry_points():
                  "gdn_decode_multi", "gdn_prefill_noalloc", "gdn_prefill_segment_tokens",
                  "gdn_state_copy", "gdn_state_reset", "gdn_decode_graph_create",
                  "gdn_decode_graph_launch", "gdn_decode_graph_destroy", "gdn_prefill_host",
-                 "gdn_prefill_host_workspace_bytes", "gdn_prefill_host_segments"):
+                 "gdn_prefill_host_workspace_bytes", "gdn_prefill_host_segments",
+                 "gdn_prefill_segment_tokens_for"):
         assert want in names
 
 
@@ -298,6 +299,22 @@ def test_prefill_host_segments_match_the_plain_model_and_tile_the_batch(L):
         gdn.gdn_prefill_host_segments(bad)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_prefill_host_segments(torch.tensor([0, 100], dtype=torch.int32), 32)
+
+
+def test_prefill_segment_length_cost_model(L):
+    # the choices measured on a 152-SM GB300 (32 value heads): 3648 tokens at
+    # 32K (9 segments, the fastest of the lengths timed), 3456 at 64K, 2048 at 8K
+    d = gdn.make_dims()
+    seg = lambda n, T, sms=152: gdn.gdn_prefill_segment_tokens_for(d, n, T, sms)
+    assert seg(1, 32768) == 3648 and seg(1, 65536) == 3456 and seg(1, 8192) == 2048
+    assert seg(1, 1024) == 0                  # no longer than the shortest segment
+    assert seg(19, 100000) == 0               # 19 x 32 heads >= 4 x 152: the GPU is full
+    for n in (1, 2, 5, 18):
+        for T in (1025, 5000, 32768, 131072, 262144):
+            L_ = seg(n, T)
+            assert L_ % 64 == 0 and 1024 <= L_ < T, (n, T, L_)
+    assert seg(1, 32768, sms=0) == -1
+    assert gdn.gdn_prefill_segment_tokens_for(gdn.make_dims(d_k=64, d_v=64), 1, 32768, 152) == -1
 
 
 def test_prefill_rejects_bad_arguments(L):
