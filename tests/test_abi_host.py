@@ -301,6 +301,24 @@ def test_prefill_host_segments_match_the_plain_model_and_tile_the_batch(L):
         gdn.gdn_prefill_host_segments(torch.tensor([0, 100], dtype=torch.int32), 32)
 
 
+def test_workspace_grows_with_sequences_and_tokens(L):
+    # gdn_prefill_host sizes one gdn_prefill workspace for (all sequences, one
+    # segment of tokens) and reuses it for every segment's call, whose counts
+    # are no larger: that needs gdn_workspace_bytes non-decreasing in both
+    d = gdn.make_dims()
+    ns = [1, 2, 3, 5, 8, 19, 64, 300]
+    Ts = [1, 63, 64, 1024, 1025, 4096, 4100, 32768, 100000]
+    for n in ns:
+        row = [gdn.gdn_workspace_bytes(d, n, T) for T in Ts]
+        assert all(x > 0 for x in row) and row == sorted(row), (n, row)
+    for T in Ts:
+        col = [gdn.gdn_workspace_bytes(d, n, T) for n in ns]
+        assert col == sorted(col), (T, col)
+    # and the host-fed call's own workspace holds at least that much
+    assert (gdn.gdn_prefill_host_workspace_bytes(d, 5, 100000, 4096)
+            > gdn.gdn_workspace_bytes(d, 5, 4096))
+
+
 def test_prefill_segment_length_cost_model(L):
     # the choices measured on a 152-SM GB300 (32 value heads): 3648 tokens at
     # 32K (9 segments, the fastest of the lengths timed), 3456 at 64K, 2048 at 8K
