@@ -113,6 +113,8 @@ def lib() -> ctypes.CDLL:
             L.gdn_prefill_noalloc.restype = ctypes.c_int
             L.gdn_prefill_noalloc.argtypes = [DP] + [_P] * 9 + [ctypes.c_int, ctypes.c_longlong] + \
                 [_P] * 5
+            L.gdn_selftest_wait_timeout.restype = ctypes.c_int
+            L.gdn_selftest_wait_timeout.argtypes = [_P, ctypes.c_longlong, _P]
             L.gdn_read_device_status.restype = ctypes.c_int
             L.gdn_read_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
             _lib = L
@@ -392,6 +394,14 @@ def gdn_state_reset(dims: Dims, conv_state, ssm_state, slot=None, n=None, device
                                int(n), _ptr(device_status, torch.int32, "device_status", 1),
                                _stream(stream))
     _check(st, "gdn_state_reset")
+
+
+def gdn_selftest_wait_timeout(device_status, budget_cycles: int = 1 << 22, stream=None):
+    """Run the bounded-wait self-test (the kernel times out on purpose and
+    writes GDN_ERR_DEVICE_TIMEOUT into ``device_status``)."""
+    st = lib().gdn_selftest_wait_timeout(_ptr(device_status, torch.int32, "device_status", 1),
+                                         int(budget_cycles), _stream(stream))
+    _check(st, "gdn_selftest_wait_timeout")
 
 
 def gdn_read_device_status(status_word, stream=None) -> int:

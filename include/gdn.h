@@ -302,6 +302,17 @@ gdn_status gdn_decode_graph_create(const gdn_dims* dims, int steps, const void* 
 gdn_status gdn_decode_graph_launch(gdn_decode_graph* graph, void* stream);
 void gdn_decode_graph_destroy(gdn_decode_graph* graph);
 
+/*
+ * Self-test of the device-side failure path.  Launches one CTA whose threads
+ * wait, with the kernels' bounded wait and a budget of budget_cycles clock
+ * cycles (1 .. 2^31; about 2 GHz), on a shared-memory barrier that nothing
+ * completes.  The wait gives up, GDN_ERR_DEVICE_TIMEOUT is written to
+ * *device_status (a device int32, left alone if it already holds a code) and
+ * the kernel exits; the context stays usable.  The status returned covers the
+ * launch only.
+ */
+gdn_status gdn_selftest_wait_timeout(int32_t* device_status, long long budget_cycles, void* stream);
+
 /* Most tokens per sequence one gdn_decode_multi call takes. */
 #define GDN_DECODE_MAX_STEPS 8
 

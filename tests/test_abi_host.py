@@ -41,7 +41,7 @@ def test_header_declares_the_entry_points():
                  "gdn_state_copy", "gdn_state_reset", "gdn_decode_graph_create",
                  "gdn_decode_graph_launch", "gdn_decode_graph_destroy", "gdn_prefill_host",
                  "gdn_prefill_host_workspace_bytes", "gdn_prefill_host_segments",
-                 "gdn_prefill_segment_tokens_for"):
+                 "gdn_prefill_segment_tokens_for", "gdn_selftest_wait_timeout"):
         assert want in names
 
 
@@ -299,6 +299,13 @@ def test_prefill_host_segments_match_the_plain_model_and_tile_the_batch(L):
         gdn.gdn_prefill_host_segments(bad)
     with pytest.raises(gdn.GdnError):
         gdn.gdn_prefill_host_segments(torch.tensor([0, 100], dtype=torch.int32), 32)
+
+
+def test_selftest_wait_timeout_rejects_bad_arguments(L):
+    assert L.gdn_selftest_wait_timeout(None, 1 << 20, None) == INVALID
+    assert L.gdn_selftest_wait_timeout(FAKE + 2, 1 << 20, None) == INVALID     # misaligned
+    assert L.gdn_selftest_wait_timeout(FAKE, 0, None) == INVALID
+    assert L.gdn_selftest_wait_timeout(FAKE, (1 << 31) + 1, None) == INVALID    # over ~1 s
 
 
 def test_workspace_grows_with_sequences_and_tokens(L):
