@@ -378,6 +378,23 @@ def test_binding_checks_tensor_arguments(L):
     with pytest.raises(ValueError):
         gdn.gdn_decode_step(d, cpu, cpu, cpu, cpu, cpu, cpu, cpu, cpu, None, 4, cpu, cpu,
                             torch.zeros(4, 32, 128), stream=0)
+    # the host-fed prefill wants host activations of the right dtype and size,
+    # before anything reaches the library
+    T = 64
+    qkv = torch.zeros(T, 8192, dtype=torch.bfloat16)
+    z = torch.zeros(T, 32, 128, dtype=torch.bfloat16)
+    ab = torch.zeros(T, 32, dtype=torch.bfloat16)
+    out = torch.zeros(T, 32, 128, dtype=torch.bfloat16)
+    cu = torch.tensor([0, T], dtype=torch.int32)
+    for bad in (dict(qkv=qkv.float()), dict(z=z[:, :16]), dict(out=out[: T - 1]),
+                dict(cu=cu.long()), dict(qkv=qkv.t())):
+        a = dict(qkv=qkv, z=z, out=out, cu=cu)
+        a.update(bad)
+        with pytest.raises(ValueError):
+            gdn.gdn_prefill_host(d, a["qkv"], a["z"], ab, ab, None, None, None, None, a["cu"],
+                                 None, None, a["out"], None)
+    with pytest.raises(ValueError):
+        gdn.gdn_prefill_host_segments(cu.long())
 
 
 C_CONSUMER = r"""
