@@ -191,7 +191,12 @@ gdn_status gdn_prefill_host(const gdn_dims* dims, const void* qkv, const void* z
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < l.total)
     return GDN_ERR_WORKSPACE;
   if (n_seqs == 0 || total_tokens == 0) return GDN_OK;
-  if (!qkv || !z || !a || !b || !out || !conv_state || !ssm_state) return GDN_ERR_INVALID_ARG;
+  // every check a segment's gdn_prefill makes on these, made before anything is
+  // enqueued, so that an invalid argument launches nothing
+  auto dev_ok = [](const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!qkv || !z || !a || !b || !out || !dev_ok(A_log) || !dev_ok(dt_bias) || !dev_ok(conv_w) ||
+      !dev_ok(norm_w) || !dev_ok(conv_state) || !dev_ok(ssm_state))
+    return GDN_ERR_INVALID_ARG;
 
   const size_t cc = 2ull * dims->h_k * dims->d_k + (size_t)dims->h_v * dims->d_v;
   const size_t zv = (size_t)dims->h_v * dims->d_v, hv = (size_t)dims->h_v;

@@ -256,6 +256,16 @@ def test_prefill_host_rejects_bad_arguments_before_any_device_call(L):
     assert call(seg=-1) == INVALID
     assert call(ws_bytes=need - 1) == WS
     assert call(ws=0x100010) == WS                                      # not 256-aligned
+
+    def call_dev(**bad):                        # device pointers, checked before any copy
+        p = dict(A_log=FAKE, dt_bias=FAKE, conv_w=FAKE, norm_w=FAKE, conv=FAKE, ssm=FAKE)
+        p.update(bad)
+        return L.gdn_prefill_host(ctypes.byref(d), FAKE, FAKE, FAKE, FAKE, p["A_log"],
+                                  p["dt_bias"], p["conv_w"], p["norm_w"], cu_ok, 2, 250, p["conv"],
+                                  p["ssm"], FAKE, 64, 0x100000, need, None)
+    for name in ("A_log", "dt_bias", "conv_w", "norm_w", "conv", "ssm"):
+        assert call_dev(**{name: None}) == INVALID, name
+        assert call_dev(**{name: FAKE + 4}) == INVALID, name
     assert call(cu=(ctypes.c_int32 * 1)(0), n=0, T=0) == OK             # nothing to do
 
 
