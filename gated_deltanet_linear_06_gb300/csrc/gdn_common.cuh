@@ -3,20 +3,9 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
-#include <nvtx3/nvToolsExt.h>
 #include <stdint.h>
 
 namespace gdn {
-
-// An NVTX range over the host side of one C-ABI call (a profiler attached to
-// the process shows each call as a named range; without one, push and pop do
-// nothing).
-struct TraceRange {
-  explicit TraceRange(const char* name) { nvtxRangePushA(name); }
-  ~TraceRange() { nvtxRangePop(); }
-  TraceRange(const TraceRange&) = delete;
-  TraceRange& operator=(const TraceRange&) = delete;
-};
 
 constexpr int kD = 128;       // d_k = d_v of the compiled fast path
 constexpr int kConvW = 4;     // conv width

@@ -23,6 +23,7 @@
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include "gdn_trace.h"
 
 namespace {
 

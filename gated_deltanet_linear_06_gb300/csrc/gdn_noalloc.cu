@@ -21,6 +21,7 @@
 
 #include "../../include/gdn.h"
 #include "gdn_common.cuh"
+#include "gdn_trace.h"
 #include "gdn_launch.h"
 
 namespace {
