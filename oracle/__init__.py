@@ -77,6 +77,10 @@ def _configure(L):
         _I64, ctypes.c_int, _D, _D, _D, _I32, ctypes.c_int, ctypes.c_int]
     L.or_max_threads.restype = ctypes.c_int
     L.or_max_threads.argtypes = []
+    L.or_linear.restype = None
+    L.or_linear.argtypes = [ctypes.c_long] * 3 + [_D] * 3
+    L.or_round_bf16.restype = None
+    L.or_round_bf16.argtypes = [ctypes.c_long, _D, _D]
     return L
 
 
@@ -261,3 +265,51 @@ def layer(*, h_k, h_v, d_k, d_v, conv_w_width=4, l2_eps=1e-6, rms_eps=1e-6,
     if rc != 0:
         raise ValueError("oracle: inconsistent arguments")
     return out, cs, ss
+
+
+# ---- the dense projections around the layer -----------------------------------
+
+def linear(x, w):
+    """y = x w^T in fp64 (x [M, K], w [N, K] output features by input features)."""
+    x, w = _f64(x), _f64(w)
+    M, K = x.shape
+    N = w.shape[0]
+    assert w.shape[1] == K
+    y = np.empty((M, N))
+    lib().or_linear(M, N, K, _p(x), _p(w), _p(y))
+    return y
+
+
+def round_bf16(x):
+    """Each value rounded to bf16 (nearest, ties to even), as fp64."""
+    x = _f64(x)
+    y = np.empty_like(x)
+    lib().or_round_bf16(x.size, _p(x), _p(y))
+    return y
+
+
+def in_proj(x, w_in, *, h_k, h_v, d_k, d_v):
+    """The input projection, stored as the layer's bf16 inputs.
+
+    x [T, hidden]; w_in [Cc + h_v d_v + 2 h_v, hidden], its rows (output
+    features) in the order: the Cc mixed q|k|v conv channels, z (value head
+    major), a, b.  Returns (qkv [T, Cc], z [T, h_v, d_v], a [T, h_v],
+    b [T, h_v]), each the fp64 product rounded to bf16.
+    """
+    Cc = 2 * h_k * d_k + h_v * d_v
+    y = round_bf16(linear(x, w_in))
+    assert y.shape[1] == Cc + h_v * d_v + 2 * h_v
+    T = y.shape[0]
+    qkv = y[:, :Cc]
+    z = y[:, Cc:Cc + h_v * d_v].reshape(T, h_v, d_v)
+    a = y[:, Cc + h_v * d_v:Cc + h_v * d_v + h_v]
+    b = y[:, Cc + h_v * d_v + h_v:]
+    return (np.ascontiguousarray(qkv), np.ascontiguousarray(z), np.ascontiguousarray(a),
+            np.ascontiguousarray(b))
+
+
+def out_proj(o, w_out):
+    """The output projection of the layer's output o [T, h_v, d_v] (or [T, h_v d_v]),
+    w_out [hidden, h_v d_v]: fp64 [T, hidden]."""
+    o = _f64(o)
+    return linear(o.reshape(o.shape[0], -1), w_out)

@@ -415,6 +415,48 @@ int or_layer(const or_dims* dm, const double* qkv, const double* z,
   return 0;
 }
 
+/* ---- the dense projections around the layer ---------------------------
+ *
+ * In the hybrid models the pages run, every Gated DeltaNet layer sits between
+ * two dense projections ("Serving large language models on our own stack",
+ * section "Qwen3.5-35B-A3B from a real GGUF"; llmxabe README, architecture
+ * paragraph): an input projection from the hidden state to the layer's
+ * inputs q|k|v, z, a, b, and an output projection from the gated-norm output
+ * back to the hidden size.  Both are y = x w^T with w stored output features
+ * by input features.
+ *
+ * x: [M][K];  w: [N][K];  y: [M][N];  y[m][n] = sum_{k} x[m][k] w[n][k],
+ * summed in increasing k in fp64.
+ */
+void or_linear(long M, long N, long K, const double* x, const double* w, double* y) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+  for (long m = 0; m < M; ++m)
+    for (long n = 0; n < N; ++n) {
+      double acc = 0.0;
+      for (long k = 0; k < K; ++k) acc += x[m * K + k] * w[n * K + k];
+      y[m * N + n] = acc;
+    }
+}
+
+/* Storage of a value as bf16 (8 significant bits, round to nearest, ties to
+ * even): the layer's activations, the projections' outputs, are bf16.  With
+ * x = m 2^e, 1/2 <= |m| < 1, the bf16 value is round(m 2^8) 2^(e-8), the
+ * rounding in the default nearest-even mode.  Zero, infinities and NaN pass
+ * through; values below the bf16 normal range (2^-126) are not handled. */
+void or_round_bf16(long n, const double* x, double* y) {
+  for (long i = 0; i < n; ++i) {
+    if (x[i] == 0.0 || !isfinite(x[i])) {
+      y[i] = x[i];
+      continue;
+    }
+    int e;
+    const double m = frexp(x[i], &e);
+    y[i] = ldexp(nearbyint(ldexp(m, 8)), e - 8);
+  }
+}
+
 /* Threads the OpenMP runtime would use (reported beside the CPU timing). */
 int or_max_threads(void) {
 #ifdef _OPENMP

@@ -14,6 +14,7 @@ import pytest
 import oracle
 import test_oracle_layer as L
 import test_oracle_pins as P
+import test_oracle_proj as J
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "gdn_oracle.c")
 
@@ -58,6 +59,18 @@ MUTANTS = {
     "conv handoff from wrong rows": (
         "conv_input(qkv + t0 * Cc, Cc, st, Cc, W, T - (W - 1) + r, c);",
         "conv_input(qkv + t0 * Cc, Cc, st, Cc, W, (T - (W - 1) + r) < 0 ? (T - (W - 1) + r) : 0, c);"),
+    "projection reads w reversed": ("acc += x[m * K + k] * w[n * K + k];",
+                                    "acc += x[m * K + k] * w[n * K + (K - 1 - k)];"),
+    "projection drops the last term": ("for (long k = 0; k < K; ++k) acc +=",
+                                       "for (long k = 0; k + 1 < K; ++k) acc +="),
+    "projection reads x row of n": ("acc += x[m * K + k] * w[n * K + k];",
+                                    "acc += x[(n % M) * K + k] * w[n * K + k];"),
+    "bf16 rounding truncates": ("y[i] = ldexp(nearbyint(ldexp(m, 8)), e - 8);",
+                                "y[i] = ldexp(trunc(ldexp(m, 8)), e - 8);"),
+    "bf16 ties away from zero": ("y[i] = ldexp(nearbyint(ldexp(m, 8)), e - 8);",
+                                 "y[i] = ldexp(round(ldexp(m, 8)), e - 8);"),
+    "bf16 keeps 9 bits": ("y[i] = ldexp(nearbyint(ldexp(m, 8)), e - 8);",
+                          "y[i] = ldexp(nearbyint(ldexp(m, 9)), e - 9);"),
 }
 
 BATTERY = [
@@ -75,6 +88,9 @@ BATTERY = [
     L.test_write_gate_one_overwrites_key_direction,
     L.test_prefill_then_decode_equals_longer_prefill,
     lambda: L.test_tiny_fp32_sequential_equals_chunked16(True),
+    J.test_linear_identity_weight_returns_input, J.test_linear_one_hot_rows_pick_input_columns,
+    J.test_linear_hand_computed_2x3, J.test_round_bf16_nearest_even_on_constructed_ties,
+    J.test_in_proj_splits_columns_in_the_documented_order, J.test_out_proj_reads_heads_in_row_major_order,
 ]
 
 
