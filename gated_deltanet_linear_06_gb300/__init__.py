@@ -24,6 +24,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libgdn.so")
 
 GDN_OK = 0
+GDN_ERR_DEVICE_TIMEOUT = 5
+GDN_ERR_DEVICE_BOUNDS = 6
 GDN_DTYPE_BF16 = 0
 GDN_DTYPE_F32 = 1
 GDN_DECODE_MAX_STEPS = 8   # most tokens one gdn_decode_multi call takes per sequence
@@ -115,6 +117,10 @@ def lib() -> ctypes.CDLL:
                 [_P] * 5
             L.gdn_selftest_wait_timeout.restype = ctypes.c_int
             L.gdn_selftest_wait_timeout.argtypes = [_P, ctypes.c_longlong, _P]
+            L.gdn_in_proj.restype = ctypes.c_int
+            L.gdn_in_proj.argtypes = [DP, ctypes.c_int, ctypes.c_longlong] + [_P] * 8
+            L.gdn_out_proj.restype = ctypes.c_int
+            L.gdn_out_proj.argtypes = [DP, ctypes.c_int, ctypes.c_longlong] + [_P] * 5
             L.gdn_read_device_status.restype = ctypes.c_int
             L.gdn_read_device_status.argtypes = [_P, _P, ctypes.POINTER(ctypes.c_int32)]
             _lib = L
@@ -402,6 +408,41 @@ def gdn_selftest_wait_timeout(device_status, budget_cycles: int = 1 << 22, strea
     st = lib().gdn_selftest_wait_timeout(_ptr(device_status, torch.int32, "device_status", 1),
                                          int(budget_cycles), _stream(stream))
     _check(st, "gdn_selftest_wait_timeout")
+
+
+def in_proj_features(dims: Dims) -> int:
+    """Rows of gdn_in_proj's weight: Cc conv channels, z, a, b."""
+    return 2 * dims.h_k * dims.d_k + 2 * dims.h_v * dims.d_v + 2 * dims.h_v
+
+
+def gdn_in_proj(dims: Dims, hidden: int, x, w_in, qkv, z, a, b, device_status=None, stream=None,
+                tokens=None):
+    """Input projection x [T, hidden] -> the layer's qkv, z, a, b (bf16, written in place)."""
+    bf = torch.bfloat16
+    T = int(tokens if tokens is not None else x.shape[0])
+    H = int(hidden)
+    Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
+    st = lib().gdn_in_proj(
+        ctypes.byref(dims), H, T, _ptr(x, bf, "x", T * H),
+        _ptr(w_in, bf, "w_in", in_proj_features(dims) * H), _ptr(qkv, bf, "qkv", T * Cc),
+        _ptr(z, bf, "z", T * dims.h_v * dims.d_v), _ptr(a, bf, "a", T * dims.h_v),
+        _ptr(b, bf, "b", T * dims.h_v), _ptr(device_status, torch.int32, "device_status", 1),
+        _stream(stream))
+    _check(st, "gdn_in_proj")
+
+
+def gdn_out_proj(dims: Dims, hidden: int, o, w_out, y, device_status=None, stream=None,
+                 tokens=None):
+    """Output projection o [T, h_v, d_v] -> y [T, hidden] (bf16)."""
+    bf = torch.bfloat16
+    T = int(tokens if tokens is not None else o.shape[0])
+    H = int(hidden)
+    Cv = dims.h_v * dims.d_v
+    st = lib().gdn_out_proj(
+        ctypes.byref(dims), H, T, _ptr(o, bf, "o", T * Cv), _ptr(w_out, bf, "w_out", H * Cv),
+        _ptr(y, bf, "y", T * H), _ptr(device_status, torch.int32, "device_status", 1),
+        _stream(stream))
+    _check(st, "gdn_out_proj")
 
 
 def gdn_read_device_status(status_word, stream=None) -> int:

@@ -17,7 +17,7 @@
 
 namespace {
 
-constexpr int kVersion = 200;  // 0.2.0: multi-token decode, decode graph, state pool, host-fed prefill
+constexpr int kVersion = 300;  // 0.3.0: the input and output projections around the layer
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -393,6 +393,71 @@ gdn_status gdn_read_device_status(const void* status_word, void* stream, int32_t
   if (cudaStreamSynchronize(s) != cudaSuccess) return GDN_ERR_CUDA;
   *code = v;
   return GDN_OK;
+}
+
+}  // extern "C"
+
+// ---- the dense projections around the layer ----
+namespace {
+
+// The checks both projections share: dims as every call, a hidden size the
+// GEMM's K-blocks and stores handle, h_v a multiple of 8 (the a and b column
+// runs of the input projection are 16-byte stores), and an int-sized problem.
+gdn_status check_proj(const gdn_dims* d, int hidden, long long tokens, int32_t* device_status) {
+  gdn_status st = check_dims(d);
+  if (st != GDN_OK) return st;
+  if (hidden <= 0 || tokens < 0 || tokens > (1LL << 31) - 1) return GDN_ERR_INVALID_ARG;
+  if (hidden % 64 != 0 || hidden > 65536 || d->h_v % 8 != 0) return GDN_ERR_UNSUPPORTED;
+  if (device_status && (reinterpret_cast<uintptr_t>(device_status) & 3u)) return GDN_ERR_INVALID_ARG;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdn_status gdn_in_proj(const gdn_dims* dims, int hidden, long long tokens, const void* x,
+                       const void* w_in, void* qkv, void* z, void* a, void* b,
+                       int32_t* device_status, void* stream) {
+  gdn::TraceRange trace_range("gdn_in_proj");
+  gdn_status st = check_proj(dims, hidden, tokens, device_status);
+  if (st != GDN_OK) return st;
+  if (tokens == 0) return GDN_OK;
+  if (!ptr_ok(x) || !ptr_ok(w_in) || !ptr_ok(qkv) || !ptr_ok(z) || !ptr_ok(a) || !ptr_ok(b))
+    return GDN_ERR_INVALID_ARG;
+  const int Cc = (int)channels(dims), Cv = dims->h_v * dims->d_v;
+  gdn::GemmArgs g;
+  g.A = static_cast<const uint16_t*>(x);
+  g.B = static_cast<const uint16_t*>(w_in);
+  g.M = (int)tokens;
+  g.N = Cc + Cv + 2 * dims->h_v;
+  g.K = hidden;
+  g.nseg = 4;
+  g.seg[0] = gdn::GemmOut{static_cast<uint16_t*>(qkv), Cc, 0, Cc};
+  g.seg[1] = gdn::GemmOut{static_cast<uint16_t*>(z), Cv, Cc, Cv};
+  g.seg[2] = gdn::GemmOut{static_cast<uint16_t*>(a), dims->h_v, Cc + Cv, dims->h_v};
+  g.seg[3] = gdn::GemmOut{static_cast<uint16_t*>(b), dims->h_v, Cc + Cv + dims->h_v, dims->h_v};
+  g.status = device_status;
+  return gdn::launch_gemm(g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_out_proj(const gdn_dims* dims, int hidden, long long tokens, const void* o,
+                        const void* w_out, void* y, int32_t* device_status, void* stream) {
+  gdn::TraceRange trace_range("gdn_out_proj");
+  gdn_status st = check_proj(dims, hidden, tokens, device_status);
+  if (st != GDN_OK) return st;
+  if (tokens == 0) return GDN_OK;
+  if (!ptr_ok(o) || !ptr_ok(w_out) || !ptr_ok(y)) return GDN_ERR_INVALID_ARG;
+  gdn::GemmArgs g;
+  g.A = static_cast<const uint16_t*>(o);
+  g.B = static_cast<const uint16_t*>(w_out);
+  g.M = (int)tokens;
+  g.N = hidden;
+  g.K = dims->h_v * dims->d_v;
+  g.nseg = 1;
+  g.seg[0] = gdn::GemmOut{static_cast<uint16_t*>(y), hidden, 0, hidden};
+  g.status = device_status;
+  return gdn::launch_gemm(g, static_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // extern "C"

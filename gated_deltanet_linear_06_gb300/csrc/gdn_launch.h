@@ -83,6 +83,27 @@ struct StateCopyArgs {
   int src_slots, dst_slots, n;
 };
 
+// Dense projection D = A B^T (bf16 operands, fp32 accumulation, bf16 out):
+// A [M][K] and B [N][K] row-major (K contiguous, K % 8 == 0, 16-byte aligned
+// bases).  The N output columns are split into runs: columns col0 ..
+// col0+ncols-1 go to ptr[row * ld + (col - col0)] (col0, ncols, ld multiples
+// of 8, ptr 16-byte aligned).
+constexpr int kGemmMaxSegs = 4;
+struct GemmOut {
+  uint16_t* ptr;
+  long long ld;
+  int col0, ncols;
+};
+struct GemmArgs {
+  const uint16_t* A;
+  const uint16_t* B;
+  int M, N, K;
+  int nseg;
+  GemmOut seg[kGemmMaxSegs];
+  int32_t* status;         // nullable device word (bounded waits that give up)
+};
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream);
+
 // Host launchers: enqueue on `stream`, return the launch error (or
 // cudaSuccess).  Dims are validated by the caller.
 cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream);

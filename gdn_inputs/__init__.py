@@ -12,6 +12,9 @@ Default distributions (the small fp32 case and the bf16 layer cases):
   SSM state ~ N(0, variance 0.1) or 0;  conv state ~ N(0, 1) or 0.
 The second parameter of N(.,.) is read as the variance.
 
+Projection inputs: the hidden state x ~ N(0, 1); projection weights
+~ N(0, variance 1 / fan-in), so each projected value is about N(0, 1).
+
 Controlled-gate variants pick the decay and write gates directly:
 ``gate_controlled`` draws u ~ U(lo, hi) and beta ~ U(blo, bhi), then sets
 A_log = 0, dt_bias = 0, a = ln(1/u - 1) and b = ln(beta / (1 - beta)).
@@ -51,7 +54,8 @@ class Shape:
 LAYER = Shape()                      # 16 key heads, 32 value heads, d = 128
 TINY = Shape(h_k=2, h_v=2, d_k=32, d_v=32)
 
-_STREAMS = {"params": 1, "tokens": 2, "states": 3, "gates": 4, "norm_w": 5}
+_STREAMS = {"params": 1, "tokens": 2, "states": 3, "gates": 4, "norm_w": 5, "hidden": 6,
+            "proj": 7}
 _BLOCK = 2048                        # rows drawn per block (bounds fp32 temps)
 
 
@@ -152,3 +156,18 @@ def cu_seqlens(lengths) -> torch.Tensor:
     for n in lengths:
         c.append(c[-1] + int(n))
     return torch.tensor(c, dtype=torch.int32)
+
+
+def make_hidden(T: int, hidden: int, seed: int, dtype=torch.bfloat16, offset: int = 0) -> torch.Tensor:
+    """Hidden states x [T, hidden] ~ N(0, 1) (rows ``offset`` .. ``offset+T``)."""
+    return _randn_rows(T, hidden, seed, "hidden", 1.0, dtype, offset)
+
+
+def make_proj_weights(shape: Shape, hidden: int, seed: int, dtype=torch.bfloat16) -> dict:
+    """The projections' weights, output features by input features:
+    w_in [cc + cv + 2 h_v, hidden] ~ N(0, 1/hidden) (rows: q|k|v channels, z,
+    a, b) and w_out [hidden, cv] ~ N(0, 1/cv)."""
+    n_in = shape.cc + shape.cv + 2 * shape.h_v
+    w_in = _randn_rows(n_in, hidden, seed, "proj", hidden ** -0.5, dtype)
+    w_out = _randn_rows(hidden, shape.cv, seed + 31_337, "proj", shape.cv ** -0.5, dtype)
+    return {"w_in": w_in, "w_out": w_out}

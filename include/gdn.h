@@ -366,16 +366,21 @@ gdn_status gdn_decode_multi(const gdn_dims* dims, const void* qkv, const void* z
  *     maps far larger than the fixed array), so a batch of few long sequences
  *     runs slower than through gdn_prefill; the results agree within the
  *     prefill tolerance.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.
+ *   - The first call in a CUDA context looks up the array's device address
+ *     (once per context, with that context's device current) and caches it
+ *     under the context's id, so a context rebuilt after cudaDeviceReset looks
+ *     it up again; make that first call before any stream capture.
  *   - All calls share the one array, which keeps the previous call's
  *     contents; each call clears the status word itself.  Calls whose work
  *     overlaps on the GPU (other streams, other host threads, concurrent
  *     graph launches) race on the array and must be serialised by the caller.
  *   - device_status: NULL, or a device int32 word that receives a copy of the
  *     call's status word (GDN_OK or the first device-side error) in stream
- *     order, for gdn_read_device_status.
+ *     order, for gdn_read_device_status.  With NULL the device-side errors of
+ *     the call are lost: a rejected cu_seqlens (GDN_ERR_DEVICE_BOUNDS, nothing
+ *     written, so out and the states keep their old contents) or a bounded
+ *     wait that gave up (GDN_ERR_DEVICE_TIMEOUT) goes only to the library's
+ *     internal word, which the next call clears.
  */
 #define GDN_NOALLOC_MAX_SEQS 32768
 #define GDN_NOALLOC_SCRATCH_BYTES 1049344 /* status word + segment list for GDN_NOALLOC_MAX_SEQS */
@@ -387,6 +392,42 @@ gdn_status gdn_prefill_noalloc(const gdn_dims* dims, const void* qkv, const void
                                int n_seqs, long long total_tokens, float* conv_state,
                                float* ssm_state, void* out, int32_t* device_status,
                                void* stream);
+
+/*
+ * The dense projections around the layer.  In the hybrid models the pages
+ * run, every Gated DeltaNet layer sits between an input projection of the
+ * hidden state and an output projection back to it ("Serving large language
+ * models on our own stack", section "Qwen3.5-35B-A3B from a real GGUF";
+ * llmxabe README, architecture paragraph: three Gated DeltaNet layers per
+ * gated-attention layer).  Both are y = x w^T on the tensor cores, with bf16
+ * operands, fp32 accumulation and the result rounded to bf16 (nearest even).
+ * Weights are in the output-features-by-input-features layout.
+ *
+ * gdn_in_proj writes its output columns straight into the layer's input
+ * buffers, in the layouts gdn_prefill and gdn_decode_step read, so nothing is
+ * copied between the projection and the layer:
+ *   x      bf16 [tokens][hidden]                    (input)
+ *   w_in   bf16 [Cc + h_v d_v + 2 h_v][hidden]      rows in the order: the Cc
+ *          mixed q|k|v conv channels, z (value head major), a (h_v), b (h_v)
+ *   qkv    bf16 [tokens][Cc];  z bf16 [tokens][h_v][d_v];
+ *   a, b   bf16 [tokens][h_v]                       (outputs)
+ *
+ * gdn_out_proj maps the layer's output to the hidden size:
+ *   o      bf16 [tokens][h_v][d_v]                  (the gdn_prefill / bf16 decode output)
+ *   w_out  bf16 [hidden][h_v d_v]
+ *   y      bf16 [tokens][hidden]                    (output)
+ *
+ * hidden: a multiple of 64, at most 65536 (else GDN_ERR_UNSUPPORTED); h_v a
+ * multiple of 8; tokens 0 .. 2^31 - 1 (0 launches nothing); dims as for
+ * gdn_prefill.  device_status: NULL or a device int32 word that a bounded
+ * wait that gave up writes GDN_ERR_DEVICE_TIMEOUT into.  The kernel keeps one
+ * CTA per SM resident for the call and uses all of its tensor memory.
+ */
+gdn_status gdn_in_proj(const gdn_dims* dims, int hidden, long long tokens, const void* x,
+                       const void* w_in, void* qkv, void* z, void* a, void* b,
+                       int32_t* device_status, void* stream);
+gdn_status gdn_out_proj(const gdn_dims* dims, int hidden, long long tokens, const void* o,
+                        const void* w_out, void* y, int32_t* device_status, void* stream);
 
 /* Waits for the stream, then reads a device status word (the first 4 bytes
  * of a prefill workspace, or a decode device_status word) into *code:

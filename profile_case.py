@@ -1,11 +1,13 @@
 """A small, self-contained case of one kernel, for profilers.
 
-  python -m gated_deltanet_linear_06_gb300.profile_case --kernel prefill --tokens 8192
-  python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode --batch 128
-  python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode_multi --batch 256 --steps 4
-  python -m gated_deltanet_linear_06_gb300.profile_case --kernel state_copy --batch 256
-  python -m gated_deltanet_linear_06_gb300.profile_case --kernel decode_graph --batch 3 --steps 64
-  python -m gated_deltanet_linear_06_gb300.profile_case --kernel prefill_host --tokens 32768 --seg 4096
+  python profile_case.py --kernel prefill --tokens 8192
+  python profile_case.py --kernel decode --batch 128
+  python profile_case.py --kernel decode_multi --batch 256 --steps 4
+  python profile_case.py --kernel state_copy --batch 256
+  python profile_case.py --kernel decode_graph --batch 3 --steps 64
+  python profile_case.py --kernel prefill_host --tokens 32768 --seg 4096
+  python profile_case.py --kernel in_proj --tokens 32768 --hidden 2048
+  python profile_case.py --kernel out_proj --tokens 32768 --hidden 2048
 
 Builds seeded synthetic inputs (the same distributions as the benchmark),
 runs the kernel ``--warmup`` times, then ``--iters`` times, and prints the
@@ -19,7 +21,7 @@ import argparse
 import os
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -31,13 +33,15 @@ def main():
     import gdn_inputs as gi
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("--kernel", choices=["prefill", "decode", "decode_multi", "state_copy", "decode_graph", "prefill_host"], required=True)
+    ap.add_argument("--kernel", choices=["prefill", "decode", "decode_multi", "state_copy", "decode_graph", "prefill_host",
+                             "in_proj", "out_proj"], required=True)
     ap.add_argument("--tokens", type=int, default=8192, help="prefill: tokens of one sequence")
     ap.add_argument("--seqs", type=int, default=1, help="prefill: equal-length sequences")
     ap.add_argument("--batch", type=int, default=128, help="decode: sequences")
     ap.add_argument("--steps", type=int, default=4, help="decode_multi: tokens per sequence")
     ap.add_argument("--trace", action="store_true", help="decode_multi: also write the SSM trace")
     ap.add_argument("--seg", type=int, default=0, help="prefill_host: tokens per segment (0: default)")
+    ap.add_argument("--hidden", type=int, default=2048, help="in_proj / out_proj: hidden size")
     ap.add_argument("--warmup", type=int, default=2)
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args()
@@ -72,6 +76,28 @@ def main():
             gdn.gdn_decode_step(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"], p["dt_bias"],
                                 p["conv_w"], p["norm_w"], None, B, conv, ssm, out, stream=stream)
         unit, per_call = "seq-steps", B
+    elif args.kernel in ("in_proj", "out_proj"):
+        T, H = args.tokens, args.hidden
+        w = {k: v.to(dev) for k, v in gi.make_proj_weights(sh, H, 6).items()}
+        if args.kernel == "in_proj":
+            xh = gi.make_hidden(T, H, 6).to(dev)
+            qkv = torch.empty(T, sh.cc, dtype=torch.bfloat16, device=dev)
+            z = torch.empty(T, sh.h_v, 128, dtype=torch.bfloat16, device=dev)
+            a = torch.empty(T, sh.h_v, dtype=torch.bfloat16, device=dev)
+            b = torch.empty(T, sh.h_v, dtype=torch.bfloat16, device=dev)
+            n_out = gdn.in_proj_features(dims)
+
+            def call():
+                gdn.gdn_in_proj(dims, H, xh, w["w_in"], qkv, z, a, b, stream=stream)
+        else:
+            o = gi.make_hidden(T, sh.cv, 6).to(dev).reshape(T, sh.h_v, 128)
+            y = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+            n_out = H
+
+            def call():
+                gdn.gdn_out_proj(dims, H, o, w["w_out"], y, stream=stream)
+        k_in = H if args.kernel == "in_proj" else sh.cv
+        unit, per_call = "TFLOP", 2e-12 * T * n_out * k_in
     elif args.kernel == "prefill_host":
         # activations in pinned host memory, output back to it: the copies are
         # part of each call

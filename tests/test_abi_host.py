@@ -41,7 +41,8 @@ def test_header_declares_the_entry_points():
                  "gdn_state_copy", "gdn_state_reset", "gdn_decode_graph_create",
                  "gdn_decode_graph_launch", "gdn_decode_graph_destroy", "gdn_prefill_host",
                  "gdn_prefill_host_workspace_bytes", "gdn_prefill_host_segments",
-                 "gdn_prefill_segment_tokens_for", "gdn_selftest_wait_timeout"):
+                 "gdn_prefill_segment_tokens_for", "gdn_selftest_wait_timeout",
+                 "gdn_in_proj", "gdn_out_proj"):
         assert want in names
 
 
@@ -366,6 +367,31 @@ def test_prefill_rejects_bad_arguments(L):
     assert _prefill(L, d, ws_bytes=16) == WS
     assert _prefill(L, d, n_seqs=0) == OK                              # nothing to launch
     assert _prefill(L, d, T=0) == OK
+
+
+def test_projections_reject_bad_arguments(L):
+    d = gdn.make_dims()
+    inp = lambda dims, H, T, *ptrs: L.gdn_in_proj(dims, H, T, *ptrs, None, None)
+    outp = lambda dims, H, T, *ptrs: L.gdn_out_proj(dims, H, T, *ptrs, None, None)
+    six, three = [FAKE] * 6, [FAKE] * 3
+    D = ctypes.byref(d)
+    assert inp(None, 2048, 5, *six) == INVALID
+    assert inp(ctypes.byref(gdn.make_dims(d_k=64, d_v=64)), 2048, 5, *six) == UNSUP
+    assert inp(D, 0, 5, *six) == INVALID                   # hidden
+    assert inp(D, 2000, 5, *six) == UNSUP                  # not a multiple of 64
+    assert inp(D, 65536 + 64, 5, *six) == UNSUP
+    assert inp(D, 2048, -1, *six) == INVALID
+    assert inp(D, 2048, 1 << 31, *six) == INVALID
+    assert inp(D, 2048, 0, *six) == OK                     # nothing to launch
+    assert inp(D, 2048, 5, FAKE, FAKE, FAKE + 8, FAKE, FAKE, FAKE) == INVALID   # misaligned qkv
+    assert inp(D, 2048, 5, FAKE, None, FAKE, FAKE, FAKE, FAKE) == INVALID
+    # h_v must be a multiple of 8 (the a and b runs are 16-byte stores)
+    assert inp(ctypes.byref(gdn.make_dims(h_k=2, h_v=4)), 2048, 5, *six) == UNSUP
+    assert L.gdn_in_proj(D, 2048, 5, *six, FAKE + 2, None) == INVALID             # status word alignment
+    assert outp(D, 2048, 0, *three) == OK
+    assert outp(D, 2048, 5, FAKE, FAKE, None) == INVALID
+    assert outp(D, 96, 5, *three) == UNSUP
+    assert outp(ctypes.byref(gdn.make_dims(conv_w=3)), 2048, 5, *three) == UNSUP
 
 
 def test_noalloc_prefill_rejects_more_sequences_than_its_fixed_scratch(L):
