@@ -2,11 +2,12 @@
 """Throughput of the Gated DeltaNet layer's hot path on GB300, one JSON line.
 
 One step = one gdn_prefill of a single 32,768-token sequence (16 key / 32
-value heads, d = 128, seed 3) followed by 16 gdn_decode_step calls over a
-batch of 256 sequences (seed 4, exp(g) ~ U(0.5, 1)), all inputs seeded and
-synthetic and resident in HBM before the timed region.  Both inputs exceed
-the 129 MB L2 (prefill activations 0.77 GB, decode state 0.54 GB), so no L2
-flush is needed between iterations.
+value heads, d = 128, seed 3) followed by 256 gdn_decode_step calls over a
+batch of 256 sequences (seed 4, exp(g) ~ U(0.5, 1): the 256-sequence x
+256-step decode workload), all inputs seeded and synthetic and resident in
+HBM before the timed region.  Both inputs exceed the 129 MB L2 (prefill
+activations 0.77 GB, decode state 0.54 GB), so no L2 flush is needed between
+iterations.
 
   value            prefill tokens/s, summed over ranks (device time of the
                    gdn_prefill calls, CUDA events on the launching stream)
@@ -39,7 +40,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GDN prefill tokens/s (T=32K) & decode seq-steps/s (B=256); % TC/HBM roofline"
 PREFILL_T, PREFILL_SEED = 32768, 3
-DECODE_B, DECODE_CALLS, DECODE_SEED = 256, 16, 4
+DECODE_B, DECODE_CALLS, DECODE_SEED = 256, 256, 4
+PROJ_HIDDEN = 2048   # hidden size of the projections' row (the 35B-A3B hybrid's width)
 H_K, H_V, D = 16, 32, 128
 CC = 2 * H_K * D + H_V * D
 # effective FLOPs of the chunked form (C = 64) per token: per value head
@@ -211,17 +213,28 @@ def oracle_decode_sample(batch: int, threads: int) -> tuple[float, float]:
 
 
 def cpu_baseline() -> dict:
+    """The oracle on this host's cores, twice: all cores (OpenMP over independent
+    (sequence, value head) units) and one thread, each on a bounded sample."""
     import oracle
     threads = os.cpu_count() or 1
     oracle.build()
     pre_tps, pre_s = oracle_prefill_sample(PREFILL_T, threads)
     dec_sps, dec_s = oracle_decode_sample(DECODE_B, threads)
-    return {"value": round(pre_tps, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
+    cores = oracle.max_threads()
+    one_T = 4096
+    pre1_tps, pre1_s = oracle_prefill_sample(one_T, 1)
+    dec1_sps, dec1_s = oracle_decode_sample(DECODE_B, 1)
+    return {"value": round(pre_tps, 2), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
             "sample": f"prefill: the whole 32768-token sequence, all 32 value heads "
                       f"({pre_s:.1f} s); decode: one step of all 256 sequences "
                       f"({dec_s:.2f} s) = {dec_sps:.1f} seq-steps/s",
-            "decode_value": round(dec_sps, 2), "decode_unit": "seq-steps/s"}
+            "decode_value": round(dec_sps, 2), "decode_unit": "seq-steps/s",
+            "one_thread": {"value": round(pre1_tps, 2), "unit": "tokens/s", "cores": 1,
+                           "decode_value": round(dec1_sps, 2), "decode_unit": "seq-steps/s",
+                           "sample": f"prefill: the first {one_T} tokens of the sequence, all 32 "
+                                     f"value heads ({pre1_s:.1f} s); decode: one step of all 256 "
+                                     f"sequences ({dec1_s:.2f} s)"}}
 
 
 # ---- our arm --------------------------------------------------------------------
@@ -241,26 +254,29 @@ def _timed(call, iters: int, stream) -> float:
     return e0.elapsed_time(e1) / iters
 
 
-def next_rows(gdn, gi, dims, sh, dev, stream, hbm: float) -> dict:
+def next_rows(gdn, gi, dims, sh, dev, stream, hbm: float, tc_peak: float, prefill_with) -> dict:
     """The paths beyond the headline step, each timed on its own (not part of `value`):
-    4-token decode calls at B = 256, a 256-state snapshot copy, and a 64-step
-    decode graph at B = 3 against the same steps launched one by one."""
+    4- and 8-token decode calls at B = 256, a 256-state snapshot copy, a 64-step
+    decode graph at B = 3 against the same steps launched one by one, and the
+    projections around the layer at the prefill size (alone, and as in_proj ->
+    gdn_prefill -> out_proj)."""
     import torch
     res = {}
-    B, K = 256, 4
+    B = 256
     p = {k: v.to(dev) for k, v in gi.make_params(sh, DECODE_SEED).items()}
     st = gi.make_states(sh, B, DECODE_SEED, ssm_std=0.1 ** 0.5, conv_std=1.0)
     conv, ssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
-    x = {k: v.to(dev) for k, v in gi.make_tokens(sh, B * K, DECODE_SEED).items()}
-    out = torch.empty(B, K, sh.h_v, D, dtype=torch.bfloat16, device=dev)
-    ms = _timed(lambda: gdn.gdn_decode_multi(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"],
-                                             p["dt_bias"], p["conv_w"], p["norm_w"], None, B, conv,
-                                             ssm, out, K, stream=stream), 20, stream)
-    byts = B * (2 * STATE_BYTES + K * DECODE_TOKEN_BYTES)
-    res["decode_multi"] = {"workload": f"{B} sequences x {K} tokens per call",
-                           "value": round(B * K / (ms * 1e-3), 1), "unit": "seq-steps/s",
-                           "ms_per_call": round(ms, 4),
-                           "hbm_frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
+    for K, key in ((4, "decode_multi"), (8, "decode_multi_k8")):
+        x = {k: v.to(dev) for k, v in gi.make_tokens(sh, B * K, DECODE_SEED).items()}
+        out = torch.empty(B, K, sh.h_v, D, dtype=torch.bfloat16, device=dev)
+        ms = _timed(lambda: gdn.gdn_decode_multi(dims, x["qkv"], x["z"], x["a"], x["b"], p["A_log"],
+                                                 p["dt_bias"], p["conv_w"], p["norm_w"], None, B, conv,
+                                                 ssm, out, K, stream=stream), 20, stream)
+        byts = B * (2 * STATE_BYTES + K * DECODE_TOKEN_BYTES)
+        res[key] = {"workload": f"{B} sequences x {K} tokens per call",
+                    "value": round(B * K / (ms * 1e-3), 1), "unit": "seq-steps/s",
+                    "ms_per_call": round(ms, 4),
+                    "hbm_frac": round(byts / (ms * 1e-3) / 1e9 / hbm, 4)}
     bconv, bssm = torch.empty_like(conv), torch.empty_like(ssm)
     ms = _timed(lambda: gdn.gdn_state_copy(dims, conv, ssm, bconv, bssm, stream=stream), 20, stream)
     byts = 2 * B * STATE_BYTES
@@ -293,6 +309,37 @@ def next_rows(gdn, gi, dims, sh, dev, stream, hbm: float) -> dict:
                            "value": round(B3 * S / (ms_g * 1e-3), 1), "unit": "seq-steps/s",
                            "us_per_step": round(ms_g * 1e3 / S, 2),
                            "eager_us_per_step": round(ms_e * 1e3 / S, 2)}
+    del graph, conv, ssm, x, out
+
+    # the dense projections around the layer, at the prefill's 32768 tokens
+    H, T = PROJ_HIDDEN, PREFILL_T
+    bf = torch.bfloat16
+    w = {k: v.to(dev) for k, v in gi.make_proj_weights(sh, H, 6).items()}
+    xh = gi.make_hidden(T, H, 6).to(dev)
+    qkv = torch.empty(T, sh.cc, dtype=bf, device=dev)
+    z = torch.empty(T, sh.h_v, D, dtype=bf, device=dev)
+    a = torch.empty(T, sh.h_v, dtype=bf, device=dev)
+    b = torch.empty(T, sh.h_v, dtype=bf, device=dev)
+    o = gi.make_hidden(T, sh.cv, 7).to(dev).reshape(T, sh.h_v, D)
+    y = torch.empty(T, H, dtype=bf, device=dev)
+    n_in = gdn.in_proj_features(dims)
+    ms_in = _timed(lambda: gdn.gdn_in_proj(dims, H, xh, w["w_in"], qkv, z, a, b, stream=stream), 20, stream)
+    ms_out = _timed(lambda: gdn.gdn_out_proj(dims, H, o, w["w_out"], y, stream=stream), 20, stream)
+    for key, ms, n_out, k_in in (("in_proj", ms_in, n_in, H), ("out_proj", ms_out, H, sh.cv)):
+        tf = 2.0 * T * n_out * k_in / (ms * 1e-3) / 1e12
+        res[key] = {"workload": f"{T} tokens, {k_in} -> {n_out} features (hidden {H})",
+                    "value": round(tf, 1), "unit": "TFLOP/s", "ms_per_call": round(ms, 4),
+                    "tensor_frac": round(tf / tc_peak, 4),
+                    "peak_source": "measured bf16_tflops (burst)"}
+
+    def layer():
+        gdn.gdn_in_proj(dims, H, xh, w["w_in"], qkv, z, a, b, stream=stream)
+        prefill_with(qkv, z, a, b, o)
+        gdn.gdn_out_proj(dims, H, o, w["w_out"], y, stream=stream)
+    ms_l = _timed(layer, 10, stream)
+    res["projected_prefill"] = {"workload": f"in_proj -> gdn_prefill -> out_proj, 1 x {T} tokens, hidden {H}",
+                                "value": round(T / (ms_l * 1e-3), 1), "unit": "tokens/s",
+                                "ms_per_call": round(ms_l, 4)}
     return res
 
 
@@ -328,20 +375,24 @@ def run_ours(args) -> dict | None:
     st = gi.make_states(sh, DECODE_B, DECODE_SEED, ssm_std=0.1 ** 0.5, conv_std=1.0)
     dconv, dssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
     dtok_host = []
+    dall = gi.make_tokens(sh, DECODE_B * DECODE_CALLS, DECODE_SEED)   # call j: rows j*B .. (j+1)*B
     for j in range(DECODE_CALLS):
-        t = gi.make_tokens(sh, DECODE_B, DECODE_SEED, offset=j * DECODE_B)
+        t = {k: v[j * DECODE_B:(j + 1) * DECODE_B].contiguous() for k, v in dall.items()}
         g = gi.gate_controlled(sh, DECODE_B, DECODE_SEED, decay=(0.5, 1.0), beta=(0.0, 1.0), offset=j)
         t["a"], t["b"] = g["a"], g["b"]
         dtok_host.append(t)
+    del dall
     dtok = [{k: v.to(dev) for k, v in t.items()} for t in dtok_host]
     dout = torch.empty(DECODE_B, sh.h_v, D, dtype=torch.bfloat16, device=dev)
 
     stream = torch.cuda.current_stream(dev)
 
+    def prefill_with(qkv, z, a, b, o):
+        gdn.gdn_prefill(dims, qkv, z, a, b, params["A_log"], params["dt_bias"], params["conv_w"],
+                        params["norm_w"], cu, conv, ssm, o, ws, stream=stream)
+
     def prefill():
-        gdn.gdn_prefill(dims, x_dev["qkv"], x_dev["z"], x_dev["a"], x_dev["b"], params["A_log"],
-                        params["dt_bias"], params["conv_w"], params["norm_w"], cu, conv, ssm, out,
-                        ws, stream=stream)
+        prefill_with(x_dev["qkv"], x_dev["z"], x_dev["a"], x_dev["b"], out)
 
     def decode(j):
         t = dtok[j]
@@ -433,7 +484,8 @@ def run_ours(args) -> dict | None:
     e2e_dec_ms = aggregate_max(sum(e[2].elapsed_time(e[3]) for e in e2e_ev) / K, world)
     if rank != 0:
         return None
-    extra = next_rows(gdn, gi, dims, sh, dev, stream, float(peaks["hbm_gbs"]))
+    extra = next_rows(gdn, gi, dims, sh, dev, stream, float(peaks["hbm_gbs"]), float(peaks["bf16_tflops"]),
+                      prefill_with)
 
     # kernels one gdn_prefill call launches: the work list and the conv-state
     # hand-off, plus per head group the prep pass and the output scan; when the
@@ -459,7 +511,7 @@ def run_ours(args) -> dict | None:
         "ms_per_step": round(total_ms / K, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "prefill 1 x 32768 tokens + 16 decode steps x 256 sequences",
+        "config": {"workload": "prefill 1 x 32768 tokens + 256 decode steps x 256 sequences",
                    "h_k": H_K, "h_v": H_V, "d_k": D, "d_v": D, "conv_w": 4, "chunk": 64,
                    "prefill_tokens": PREFILL_T, "decode_batch": DECODE_B,
                    "decode_calls_per_step": DECODE_CALLS,
@@ -483,7 +535,10 @@ def run_ours(args) -> dict | None:
                                 "algorithmic_bytes_per_launch": dec_bytes},
                    "e2e": {"value": round(world * DECODE_B * DECODE_CALLS / (e2e_dec_ms * 1e-3), 1),
                            "unit": "seq-steps/s", "h2d_bytes_per_step": h2d_dec,
-                           "d2h_bytes_per_step": d2h_dec}},
+                           "d2h_bytes_per_step": d2h_dec,
+                           "call": "per decode call: torch copies of the step's tokens from pinned "
+                                   "host memory, gdn_decode_step on the device buffers, torch copy "
+                                   "of the output to pinned host memory (all on the launching stream)"}},
         "e2e": {"value": round(world * PREFILL_T / (e2e_pre_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre,
                 "call": "gdn_prefill_host (host activations in and output out, copies "
@@ -519,7 +574,7 @@ def run_reference(args) -> dict | None:
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(mean * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "prefill 1 x 32768 tokens + 16 decode steps x 256 sequences",
+        "config": {"workload": "prefill 1 x 32768 tokens + 256 decode steps x 256 sequences",
                    "h_k": H_K, "h_v": H_V, "d_k": D, "d_v": D, "conv_w": 4, "chunk": 64},
         "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.max_threads(),
                          "kind": "oracle",

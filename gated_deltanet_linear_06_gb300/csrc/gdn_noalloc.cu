@@ -11,8 +11,9 @@
 // GPU that loads the library holds until the process exits.
 //
 // Nothing here allocates: no cudaMalloc, no cudaFree, no allocating library
-// routine.  The array's device address is looked up once per device with
-// cudaGetSymbolAddress (its name is only a host-side stand-in in host code).
+// routine.  The array's device address is looked up with cudaGetSymbolAddress
+// once per context (its name is only a host-side stand-in in host code).
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -36,23 +37,59 @@ static_assert(256 + 256 + ((16 + 32 * (size_t)GDN_NOALLOC_MAX_SEQS + 255) / 256)
               "the fixed scratch must hold the work list of GDN_NOALLOC_MAX_SEQS sequences");
 
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+struct ScratchCache {
+  unsigned long long ctx_id = 0;   // the context the address belongs to (0: none yet)
+  void* addr = nullptr;
+};
+ScratchCache g_cache[kMaxDevices];
 
-// Device address of g_prefill_scratch on the current device (looked up on the
-// first call per device, then cached).
+using PfnCtxGetCurrent = CUresult (*)(CUcontext*);
+using PfnCtxGetId = CUresult (*)(CUcontext, unsigned long long*);
+
+// Id of the calling thread's current context (0 if there is none or the
+// driver cannot say).
+unsigned long long current_context_id() {
+  static PfnCtxGetCurrent get_current = nullptr;
+  static PfnCtxGetId get_id = nullptr;
+  static bool looked_up = false;
+  if (!looked_up) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PfnCtxGetCurrent>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PfnCtxGetId>(f);
+    looked_up = true;
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of g_prefill_scratch in the current context.  It is looked
+// up with cudaGetSymbolAddress on the first call in a context and cached
+// under the context's id, so a context that was rebuilt (after a
+// cudaDeviceReset, say) gets the address of its own copy of the array.
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchCache& c = g_cache[dev];
+  const unsigned long long id = current_context_id();
+  if (c.addr == nullptr || id == 0 || id != c.ctx_id) {
     void* addr = nullptr;
-    e = cudaGetSymbolAddress(&addr, g_prefill_scratch);
+    e = cudaGetSymbolAddress(&addr, g_prefill_scratch);   // also makes the primary context current
     if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = addr;
+    c.addr = addr;
+    c.ctx_id = current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = c.addr;
   return cudaSuccess;
 }
 
