@@ -260,10 +260,6 @@ gdn_status gdn_decode_graph_create(const gdn_dims* dims, int steps, const void* 
                               device_status, p);
   if (st != GDN_OK) return st;
   const bool f32 = out_dtype == GDN_DTYPE_F32;
-  // per-step strides of the step-major buffers, in elements
-  const size_t cc = (size_t)channels(dims), hv = (size_t)dims->h_v, dv = (size_t)dims->d_v;
-  const size_t qkv_step = (size_t)batch * cc, z_step = (size_t)batch * hv * dv;
-  const size_t ab_step = (size_t)batch * hv, out_step_bytes = z_step * (f32 ? 4 : 2);
 
   cudaStream_t s = nullptr;
   if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) != cudaSuccess) return GDN_ERR_CUDA;
@@ -272,15 +268,10 @@ gdn_status gdn_decode_graph_create(const gdn_dims* dims, int steps, const void* 
     cudaStreamDestroy(s);
     return GDN_ERR_CUDA;
   }
-  for (int t = 0; t < steps && err == cudaSuccess; ++t) {
-    gdn::DecodeArgs q = p;
-    q.qkv = p.qkv + t * qkv_step;
-    q.z = p.z + t * z_step;
-    q.a = p.a + t * ab_step;
-    q.b = p.b + t * ab_step;
-    q.out = static_cast<char*>(p.out) + t * out_step_bytes;
-    err = gdn::launch_decode(q, f32, s);
-  }
+  // the whole chain as one persistent launch (the state rows stay on chip
+  // through every step), then the conv state after the last step
+  err = gdn::launch_decode_chain(p, steps, f32, s);
+  if (err == cudaSuccess) err = gdn::launch_decode_chain_conv_state(p, p.qkv, steps, s);
   cudaGraph_t g = nullptr;
   const cudaError_t end = cudaStreamEndCapture(s, &g);
   cudaStreamDestroy(s);

@@ -368,53 +368,78 @@ __global__ void __launch_bounds__(kThreads, 3) decode_multi_kernel(DecodeArgs p)
 
   stage_batch(0);
 
+  // ---- gates of every (token, value head): their loads overlap the conv's ----
+  for (int i = tid; i < K * G; i += kThreads) {
+    const int t = i / G, g = i - t * G;
+    const int h = kh * G + g;
+    const size_t ab = ((size_t)bidx * K + t) * p.h_v + h;
+    const float gg = -__expf(p.A_log[h]) * softplus(bf16_to_f32(p.a[ab]) + p.dt_bias[h]);
+    s_decay[t][g] = __expf(gg);
+    s_beta[t][g] = sigmoid(bf16_to_f32(p.b[ab]));
+  }
+
   // ---- conv + SiLU over this CTA's channels for every token, the window shifting
-  //      one token at a time ----
+  //      one token at a time; every channel's inputs are loaded before any is used ----
   {
+    constexpr int kIt = ((2 + G) * kD + kThreads - 1) / kThreads;   // channels per thread
     float* cs = p.conv_state + (size_t)s * (kConvW - 1) * Cc;
-    for (int ci = tid; ci < (2 + G) * kD; ci += kThreads) {
-      int c;
-      if (ci < kD) c = kh * kD + ci;
-      else if (ci < 2 * kD) c = Cq + kh * kD + (ci - kD);
-      else c = 2 * Cq + kh * G * kD + (ci - 2 * kD);
-      float s0 = cs[c], s1 = cs[Cc + c], s2 = cs[2 * Cc + c];
-      const uint2 wr = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)c * kConvW);
-      const float w0 = bf16_to_f32(wr.x & 0xffffu), w1 = bf16_to_f32(wr.x >> 16);
-      const float w2 = bf16_to_f32(wr.y & 0xffffu), w3 = bf16_to_f32(wr.y >> 16);
-      float xs[kDecodeMaxSteps];  // every token's input issued before the first is used
+    int cidx[kIt];
+    float s0[kIt], s1[kIt], s2[kIt];
+    uint2 wr[kIt];
+    float xs[kIt][kDecodeMaxSteps];
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int ci = tid + it * kThreads;
+      cidx[it] = -1;
+      if (ci >= (2 + G) * kD) continue;
+      const int c = ci < kD ? kh * kD + ci : ci < 2 * kD ? Cq + kh * kD + (ci - kD) : 2 * Cq + kh * G * kD + (ci - 2 * kD);
+      cidx[it] = c;
+      s0[it] = cs[c];
+      s1[it] = cs[Cc + c];
+      s2[it] = cs[2 * Cc + c];
+      wr[it] = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)c * kConvW);
 #pragma unroll
       for (int t = 0; t < kDecodeMaxSteps; ++t)
-        if (t < K) xs[t] = bf16_to_f32(p.qkv[((size_t)bidx * K + t) * Cc + c]);
+        if (t < K) xs[it][t] = bf16_to_f32(p.qkv[((size_t)bidx * K + t) * Cc + c]);
+    }
+#pragma unroll
+    for (int it = 0; it < kIt; ++it) {
+      const int c = cidx[it];
+      if (c < 0) continue;
+      const int ci = tid + it * kThreads;
+      const float w0 = bf16_to_f32(wr[it].x & 0xffffu), w1 = bf16_to_f32(wr[it].x >> 16);
+      const float w2 = bf16_to_f32(wr[it].y & 0xffffu), w3 = bf16_to_f32(wr[it].y >> 16);
+      float a0 = s0[it], a1 = s1[it], a2 = s2[it];
 #pragma unroll
       for (int t = 0; t < kDecodeMaxSteps; ++t) {
         if (t >= K) break;
-        const float xt = xs[t];
-        float y = w0 * s0;
-        y = fmaf(w1, s1, y);
-        y = fmaf(w2, s2, y);
+        const float xt = xs[it][t];
+        float y = w0 * a0;
+        y = fmaf(w1, a1, y);
+        y = fmaf(w2, a2, y);
         y = fmaf(w3, xt, y);
         y = silu(y);
-        s0 = s1;
-        s1 = s2;
-        s2 = xt;
+        a0 = a1;
+        a1 = a2;
+        a2 = xt;
         if (p.conv_trace) {
           float* ct = p.conv_trace + ((size_t)bidx * K + t) * (kConvW - 1) * Cc;
-          ct[c] = s0;
-          ct[Cc + c] = s1;
-          ct[2 * Cc + c] = s2;
+          ct[c] = a0;
+          ct[Cc + c] = a1;
+          ct[2 * Cc + c] = a2;
         }
         if (ci < kD) sq[t][ci] = y;
         else if (ci < 2 * kD) sk[t][ci - kD] = y;
         else sv[t][(ci - 2 * kD) / kD][(ci - 2 * kD) % kD] = y;
       }
-      cs[c] = s0;
-      cs[Cc + c] = s1;
-      cs[2 * Cc + c] = s2;
+      cs[c] = a0;
+      cs[Cc + c] = a1;
+      cs[2 * Cc + c] = a2;
     }
   }
   __syncthreads();
 
-  // ---- L2 norms of q and k and k^ . q^ (a warp per token), gates ----
+  // ---- L2 norms of q and k and k^ . q^ (a warp per token) ----
   static_assert(kDecodeMaxSteps <= kWarps, "a warp per token");
   if (warp < K) {
     float rq, rk, kq;
@@ -424,14 +449,6 @@ __global__ void __launch_bounds__(kThreads, 3) decode_multi_kernel(DecodeArgs p)
       s_rk[warp] = rk;
       s_kq[warp] = kq;
     }
-  }
-  for (int i = tid; i < K * G; i += kThreads) {
-    const int t = i / G, g = i - t * G;
-    const int h = kh * G + g;
-    const size_t ab = ((size_t)bidx * K + t) * p.h_v + h;
-    const float gg = -__expf(p.A_log[h]) * softplus(bf16_to_f32(p.a[ab]) + p.dt_bias[h]);
-    s_decay[t][g] = __expf(gg);
-    s_beta[t][g] = sigmoid(bf16_to_f32(p.b[ab]));
   }
   __syncthreads();
   for (int i = tid; i < K * kD; i += kThreads) {
@@ -467,6 +484,22 @@ __global__ void __launch_bounds__(kThreads, 3) decode_multi_kernel(DecodeArgs p)
     }
     store_rows(batch_rows(nb), cur, rr, q);
   }
+  // this thread's z values for the output below, all loaded at once (its
+  // output rows share one d_v index, so one norm weight)
+  constexpr int kOut = kDecodeMaxSteps * G * kD / kThreads;
+  float zv[kOut];
+#pragma unroll
+  for (int k = 0; k < kOut; ++k) {
+    const int i = tid + k * kThreads;
+    zv[k] = 0.0f;
+    if (i < K * G * kD) {
+      const int t = i / (G * kD), rem = i - t * (G * kD);
+      const int vh = rem / kD, r = rem - vh * kD;
+      zv[k] = bf16_to_f32(p.z[(((size_t)bidx * K + t) * p.h_v + (size_t)kh * G + vh) * kD + r]);
+    }
+  }
+  static_assert(kThreads % kD == 0, "a thread's outputs share one d_v index");
+  const float nw = p.norm_w[tid % kD];
   __syncthreads();
 
   // ---- gated RMSNorm over d_v of each (token, value head) ----
@@ -481,15 +514,244 @@ __global__ void __launch_bounds__(kThreads, 3) decode_multi_kernel(DecodeArgs p)
     if (lane == 0) s_rstd[t][vh] = rsqrtf(ss * (1.0f / kD) + p.rms_eps);
   }
   __syncthreads();
-  for (int i = tid; i < K * G * kD; i += kThreads) {
+#pragma unroll
+  for (int k = 0; k < kOut; ++k) {
+    const int i = tid + k * kThreads;
+    if (i >= K * G * kD) break;
     const int t = i / (G * kD), rem = i - t * (G * kD);
     const int vh = rem / kD, r = rem - vh * kD;
     const size_t o_idx = (((size_t)bidx * K + t) * p.h_v + (size_t)kh * G + vh) * kD + r;
-    const float zz = bf16_to_f32(p.z[o_idx]);
-    const float val = so[t][vh][r] * s_rstd[t][vh] * p.norm_w[r] * silu(zz);
+    const float val = so[t][vh][r] * s_rstd[t][vh] * nw * silu(zv[k]);
     if (OUT_F32) reinterpret_cast<float*>(p.out)[o_idx] = val;
     else reinterpret_cast<uint16_t*>(p.out)[o_idx] = f32_to_bf16(val);
   }
+}
+
+// ---- a captured chain of steps, in one launch ----
+//
+// A chain of `steps` decode steps whose tokens are all known when it is
+// launched (gdn_decode_graph: the caller fills the step-major buffers first)
+// runs as one persistent launch.  A cluster of two CTAs owns one (sequence,
+// value head), each CTA 64 of its 128 state rows, 8 per warp -- the same
+// batches of 8 rows and lane layout as decode_kernel -- and keeps them in
+// registers through every step: the state crosses HBM once per launch instead of
+// once per step, and a step costs only its token's activations.
+//
+// Nothing outside a cluster is shared between steps: a step's conv window is
+// the raw inputs of the three tokens before it, which each thread keeps in
+// registers for its channels (from the conv state before the first step), so
+// no CTA writes the conv state during the chain; a small kernel writes it once
+// after the last step.  Each CTA conv-filters and normalises q and k (its key
+// head's 256 channels, recomputed by every CTA of the key head) and the 64 v
+// channels of its rows.  The gated RMSNorm needs all 128 outputs of the head:
+// each CTA forms the lane partial sums of o^2 that lanes 16 h .. 16 h + 15 of
+// the single step form, writes them into both CTAs' shared memory, and after a
+// cluster barrier both run the single step's butterfly over all 32 partials.
+// Every value is therefore computed by the same operations in the same order
+// as in decode_kernel: the chain gives bit for bit what the same single steps
+// give.  The next step's activations are loaded while a step computes.
+constexpr int kChainRows = kD / 2;   // state rows of a value head per CTA
+constexpr int kChainChannels = 2 * kD + kChainRows;   // conv channels a CTA filters
+
+template <int G, bool OUT_F32>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 2)
+    decode_chain_kernel(DecodeArgs p, int steps) {
+  const int half = blockIdx.x & 1;
+  const int pair = blockIdx.x >> 1;
+  const int bidx = pair / p.h_v;
+  const int h = pair - bidx * p.h_v;
+  const int kh = h / G, vh = h - kh * G;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int Cq = p.h_k * kD;
+  const int Cc = 2 * Cq + p.h_v * kD;
+  // per-step strides of the step-major buffers, in elements
+  const size_t qkv_step = (size_t)p.batch * Cc, z_step = (size_t)p.batch * p.h_v * kD;
+  const size_t ab_step = (size_t)p.batch * p.h_v;
+
+  int s = bidx;
+  if (p.slot) {   // both CTAs of the cluster see the same slot and leave together
+    s = p.slot[bidx];
+    if (s < 0 || s >= p.n_slots) {
+      if (tid == 0 && half == 0) record_status(p.status, GDN_ERR_DEVICE_BOUNDS);
+      return;
+    }
+  }
+
+  __shared__ __align__(16) float sq[kD], sk[kD], sv[kChainRows], so[kChainRows];
+  __shared__ float s_part[2][32];   // by step parity: the peer may be a step ahead
+  __shared__ float s_decay, s_beta, s_rstd, s_rq, s_rk, s_kq;
+
+  // this thread's conv channels (ci < kChainChannels): q and k of the key head,
+  // v of this half's rows; taps, and the window of raw inputs before the step
+  int chn[2];
+  float w[2][kConvW], win[2][kConvW - 1];
+  const float* cs = p.conv_state + (size_t)s * (kConvW - 1) * Cc;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int ci = tid + j * kThreads;
+    chn[j] = -1;
+    if (ci < kChainChannels) {
+      const int c = ci < kD ? kh * kD + ci
+                            : ci < 2 * kD ? Cq + kh * kD + (ci - kD) : 2 * Cq + h * kD + kChainRows * half + (ci - 2 * kD);
+      chn[j] = c;
+      const uint2 wr = *reinterpret_cast<const uint2*>(p.conv_w + (size_t)c * kConvW);
+      w[j][0] = bf16_to_f32(wr.x & 0xffffu);
+      w[j][1] = bf16_to_f32(wr.x >> 16);
+      w[j][2] = bf16_to_f32(wr.y & 0xffffu);
+      w[j][3] = bf16_to_f32(wr.y >> 16);
+#pragma unroll
+      for (int r = 0; r < kConvW - 1; ++r) win[j][r] = cs[(size_t)r * Cc + c];
+    }
+  }
+  const float A_exp_h = __expf(p.A_log[h]);   // as the single step forms it
+  const float dtb = p.dt_bias[h];
+  const int r_out = kChainRows * half + tid;   // this thread's output row (tid < 64)
+  const float nw = tid < kChainRows ? p.norm_w[r_out] : 0.0f;
+
+  // the state rows of this warp, in registers for the whole chain
+  const int rr = lane >> 3, q = lane & 7;
+  float* const rows = p.ssm_state + (((size_t)s * p.h_v + h) * kD + kChainRows * half + 8 * warp) * kD;
+  RowBatch cur;
+  load_rows(cur, rows, rr, q);
+
+  // step 0's activations; later steps' are loaded one step ahead
+  auto load_x = [&](int t, float (&x)[2], float& av, float& bv, float& zz) {
+    const uint16_t* xq = p.qkv + (size_t)t * qkv_step + (size_t)bidx * Cc;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) x[j] = chn[j] >= 0 ? bf16_to_f32(xq[chn[j]]) : 0.0f;
+    const size_t ab = (size_t)t * ab_step + (size_t)bidx * p.h_v + h;
+    av = (warp == 2 && lane == vh) ? bf16_to_f32(p.a[ab]) : 0.0f;
+    bv = (warp == 2 && lane == vh) ? bf16_to_f32(p.b[ab]) : 0.0f;
+    zz = tid < kChainRows ? bf16_to_f32(p.z[(size_t)t * z_step + ((size_t)bidx * p.h_v + h) * kD + r_out]) : 0.0f;
+  };
+  float x[2], av, bv, zz;
+  load_x(0, x, av, bv, zz);
+
+#pragma unroll 1
+  for (int t = 0; t < steps; ++t) {
+    float nx[2] = {0.0f, 0.0f}, nav = 0.0f, nbv = 0.0f, nzz = 0.0f;
+    if (t + 1 < steps) load_x(t + 1, nx, nav, nbv, nzz);
+
+    // ---- conv + SiLU, the window shifting by one token ----
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (chn[j] < 0) continue;
+      const int ci = tid + j * kThreads;
+      float y = w[j][0] * win[j][0];
+      y = fmaf(w[j][1], win[j][1], y);
+      y = fmaf(w[j][2], win[j][2], y);
+      y = fmaf(w[j][3], x[j], y);
+      y = silu(y);
+      win[j][0] = win[j][1];
+      win[j][1] = win[j][2];
+      win[j][2] = x[j];
+      if (ci < kD) sq[ci] = y;
+      else if (ci < 2 * kD) sk[ci - kD] = y;
+      else sv[ci - 2 * kD] = y;
+    }
+    __syncthreads();
+
+    // ---- L2 norms of q and k and k^ . q^, the gates of value head h ----
+    if (warp == 0) {
+      float rq, rk, kq;
+      token_norms(sq, sk, lane, p.l2_eps, rq, rk, kq);
+      if (lane == 0) {
+        s_rq = rq;
+        s_rk = rk;
+        s_kq = kq;
+      }
+    } else if (warp == 2 && lane == vh) {
+      const float g = -A_exp_h * softplus(av + dtb);
+      s_decay = __expf(g);
+      s_beta = sigmoid(bv);
+    }
+    __syncthreads();
+    if (tid < kD) {
+      sq[tid] *= s_rq;
+      sk[tid] *= s_rk;
+    }
+    __syncthreads();
+
+    // ---- this warp's 8 rows through the token ----
+    {
+      LaneCols qh, kk;
+      load_lane_cols(qh, sq, q);
+      load_lane_cols(kk, sk, q);
+      const float v[2] = {sv[8 * warp + rr], sv[8 * warp + 4 + rr]};
+      float o[2];
+      rows_token(cur, kk, qh, s_decay, s_beta, s_kq, v, o);
+      if (q == 0) {
+        so[8 * warp + rr] = o[0];
+        so[8 * warp + 4 + rr] = o[1];
+      }
+    }
+    __syncthreads();
+
+    // ---- gated RMSNorm: the single step's 32 lane partials, 16 from each CTA ----
+    if (warp == 0 && lane < 16) {
+      const float4 o4 = reinterpret_cast<const float4*>(so)[lane];
+      float ss = o4.x * o4.x;
+      ss = fmaf(o4.y, o4.y, ss);
+      ss = fmaf(o4.z, o4.z, ss);
+      ss = fmaf(o4.w, o4.w, ss);
+      float* mine = &s_part[t & 1][16 * half + lane];
+      *mine = ss;
+      const uint32_t local = static_cast<uint32_t>(__cvta_generic_to_shared(mine));
+      uint32_t remote;
+      asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(half ^ 1));
+      asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(ss) : "memory");
+    }
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+    if (warp == 0) {
+      const float ss = warp_sum(s_part[t & 1][lane]);
+      if (lane == 0) s_rstd = rsqrtf(ss * (1.0f / kD) + p.rms_eps);
+    }
+    __syncthreads();
+    if (tid < kChainRows) {
+      const size_t o_idx = (size_t)t * z_step + ((size_t)bidx * p.h_v + h) * kD + r_out;
+      const float val = so[tid] * s_rstd * nw * silu(zz);
+      if (OUT_F32) reinterpret_cast<float*>(p.out)[o_idx] = val;
+      else reinterpret_cast<uint16_t*>(p.out)[o_idx] = f32_to_bf16(val);
+    }
+    x[0] = nx[0];
+    x[1] = nx[1];
+    av = nav;
+    bv = nbv;
+    zz = nzz;
+  }
+  store_rows(rows, cur, rr, q);
+}
+
+// The conv state after a chain of `steps` steps: the raw inputs of its last
+// conv_w - 1 positions (rows of the starting conv state where the chain is
+// shorter than that).
+__global__ void __launch_bounds__(256) decode_chain_conv_state_kernel(DecodeArgs p, const uint16_t* qkv0,
+                                                                      int steps) {
+  const int Cc = 2 * p.h_k * kD + p.h_v * kD;
+  const int bidx = blockIdx.y, c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= Cc) return;
+  int s = bidx;
+  if (p.slot) {
+    s = p.slot[bidx];
+    if (s < 0 || s >= p.n_slots) return;   // the step kernels recorded it
+  }
+  float* cs = p.conv_state + (size_t)s * (kConvW - 1) * Cc;
+  float v[kConvW - 1];
+#pragma unroll
+  for (int r = 0; r < kConvW - 1; ++r) {
+    const int pos = steps - (kConvW - 1) + r;
+    v[r] = pos >= 0 ? bf16_to_f32(qkv0[((size_t)pos * p.batch + bidx) * Cc + c])
+                    : cs[(size_t)(kConvW - 1 + pos) * Cc + c];
+  }
+#pragma unroll
+  for (int r = 0; r < kConvW - 1; ++r) cs[(size_t)r * Cc + c] = v[r];
+}
+
+template <int G, bool OUT_F32>
+cudaError_t launch_chain_go(const DecodeArgs& p, int steps, cudaStream_t stream) {
+  decode_chain_kernel<G, OUT_F32><<<dim3((unsigned)(2 * p.batch * p.h_v)), dim3(kThreads), 0, stream>>>(p, steps);
+  return cudaGetLastError();
 }
 
 template <int G, bool OUT_F32>
@@ -537,6 +799,24 @@ cudaError_t launch_decode_multi(const DecodeArgs& p, bool out_f32, cudaStream_t 
     case 4: return launch_multi_g<4>(p, out_f32, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_decode_chain(const DecodeArgs& p, int steps, bool out_f32, cudaStream_t stream) {
+  if (steps < 1 || (long long)p.batch * p.h_v * 2 > 0x7fffffffLL) return cudaErrorInvalidValue;
+  switch (p.h_v / p.h_k) {
+    case 1: return out_f32 ? launch_chain_go<1, true>(p, steps, stream) : launch_chain_go<1, false>(p, steps, stream);
+    case 2: return out_f32 ? launch_chain_go<2, true>(p, steps, stream) : launch_chain_go<2, false>(p, steps, stream);
+    case 4: return out_f32 ? launch_chain_go<4, true>(p, steps, stream) : launch_chain_go<4, false>(p, steps, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_decode_chain_conv_state(const DecodeArgs& p, const uint16_t* qkv0, int steps,
+                                           cudaStream_t stream) {
+  const int Cc = 2 * p.h_k * kD + p.h_v * kD;
+  decode_chain_conv_state_kernel<<<dim3((unsigned)((Cc + 255) / 256), (unsigned)p.batch), 256, 0, stream>>>(
+      p, qkv0, steps);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream) {

@@ -110,6 +110,15 @@ cudaError_t launch_decode(const DecodeArgs& p, bool out_f32, cudaStream_t stream
 // p.steps tokens per sequence in one launch (1 <= steps <= kDecodeMaxSteps).
 constexpr int kDecodeMaxSteps = 8;
 cudaError_t launch_decode_multi(const DecodeArgs& p, bool out_f32, cudaStream_t stream);
+// A chain of `steps` single steps in one persistent launch: p's activations
+// and output are the chain's step-major buffers ([steps][batch][...]).  The
+// state rows stay in registers through the chain; the conv state is read (the
+// window before the first step) but not written --
+// launch_decode_chain_conv_state writes it afterwards.  The results are
+// bit-identical to `steps` launch_decode calls.
+cudaError_t launch_decode_chain(const DecodeArgs& p, int steps, bool out_f32, cudaStream_t stream);
+cudaError_t launch_decode_chain_conv_state(const DecodeArgs& p, const uint16_t* qkv0, int steps,
+                                           cudaStream_t stream);
 // n <= 65535 pairs per launch.
 cudaError_t launch_state_copy(const StateCopyArgs& p, cudaStream_t stream);
 // allow_split = false keeps every sequence in one segment (no transfer maps in

@@ -97,3 +97,65 @@ def test_graph_path_three_sequences_1024_steps_matches_oracle():
             np.testing.assert_array_equal(conv.cpu().double().numpy(), ref_conv)
     finally:
         g.close()
+
+
+@pytest.mark.parametrize("S,h_k,h_v,B", [(1, 16, 32, 2), (2, 32, 32, 2), (5, 8, 32, 2), (3, 16, 32, 2),
+                                         (6, 16, 32, 48)])
+def test_short_chains_and_head_groupings_equal_eager_steps_bitwise(S, h_k, h_v, B):
+    # chains shorter than the conv window (the conv state after the chain then
+    # keeps rows of the starting one), 1, 2 and 4 value heads per key head, and
+    # a batch of 48 whose 3072 CTAs run in several waves
+    sh = gi.Shape(h_k=h_k, h_v=h_v)
+    dims = dims_of(sh)
+    params = to_dev(gi.make_params(sh, 82))
+    st = gi.make_states(sh, B, 82, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    conv_g, ssm_g = st["conv_state"].to(DEV), st["ssm_state"].to(DEV)
+    conv_e, ssm_e = conv_g.clone(), ssm_g.clone()
+    t = gi.make_tokens(sh, S * B, 82)
+    bound = to_dev({k: v.reshape(S, B, *v.shape[1:]) for k, v in t.items()})
+    out_g = torch.empty(S, B, sh.h_v, sh.d_v, device=DEV)
+    out_e = torch.empty_like(out_g)
+    g = gdn.gdn_decode_graph_create(dims, S, bound["qkv"], bound["z"], bound["a"], bound["b"],
+                                    params["A_log"], params["dt_bias"], params["conv_w"],
+                                    params["norm_w"], None, B, conv_g, ssm_g, out_g)
+    try:
+        for launch in range(2):
+            g.launch()
+            for s in range(S):
+                gdn.gdn_decode_step(dims, bound["qkv"][s], bound["z"][s], bound["a"][s], bound["b"][s],
+                                    params["A_log"], params["dt_bias"], params["conv_w"],
+                                    params["norm_w"], None, B, conv_e, ssm_e, out_e[s])
+            assert torch.equal(out_g, out_e), f"launch {launch}"
+            assert torch.equal(ssm_g, ssm_e) and torch.equal(conv_g, conv_e), f"launch {launch}"
+    finally:
+        g.close()
+
+
+def test_graph_with_a_bad_slot_reports_it_and_leaves_that_entry_alone():
+    # entry 1's slot is out of range: it is skipped on the device (its output
+    # rows keep their NaN canary), the others decode as eager steps do
+    B, S, n = 3, 4, 3
+    dims = dims_of(SH)
+    params = to_dev(gi.make_params(SH, 83))
+    st = gi.make_states(SH, n, 83, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    slot = torch.tensor([2, 7, 0], dtype=torch.int32, device=DEV)
+    conv_g, ssm_g = st["conv_state"].to(DEV), st["ssm_state"].to(DEV)
+    conv_e, ssm_e = conv_g.clone(), ssm_g.clone()
+    t = gi.make_tokens(SH, S * B, 83)
+    bound = to_dev({k: v.reshape(S, B, *v.shape[1:]) for k, v in t.items()})
+    out_g = torch.full((S, B, SH.h_v, SH.d_v), float("nan"), device=DEV)
+    out_e = out_g.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    g = gdn.gdn_decode_graph_create(dims, S, bound["qkv"], bound["z"], bound["a"], bound["b"],
+                                    params["A_log"], params["dt_bias"], params["conv_w"],
+                                    params["norm_w"], slot, n, conv_g, ssm_g, out_g,
+                                    device_status=status)
+    try:
+        g.launch()
+    finally:
+        g.close()
+    assert gdn.gdn_read_device_status(status) == gdn.GDN_ERR_DEVICE_BOUNDS
+    _eager(dims, bound, params, conv_e, ssm_e, out_e, slot=slot, n_slots=n)
+    assert torch.isnan(out_g[:, 1]).all()
+    assert torch.equal(out_g[:, [0, 2]], out_e[:, [0, 2]])
+    assert torch.equal(ssm_g, ssm_e) and torch.equal(conv_g, conv_e)
