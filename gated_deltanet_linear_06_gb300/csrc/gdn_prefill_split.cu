@@ -864,6 +864,51 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 // completion whose successor needs something issued only after the wait, so a
 // barrier is never two phases on.
 constexpr int kXferWorkers = 256;                 // 8 warps: 2 per TMEM lane quarter
+constexpr float kNegligibleLogDecay = -160.0f;    // e^-160 < 1e-69
+
+// The last chunk j (0 <= j < n) of a segment such that the gamma_C of chunks
+// j .. n-1 sum to less than kNegligibleLogDecay, or -1.  rec: the gate-bearing
+// record of the segment's first chunk, stride bytes between chunks.  Every
+// thread of the block calls it and gets the same answer.  Each gamma_C <= 0, so
+// the suffix sums fall as j falls and the chunks are scanned from the end, a
+// block-sized tile at a time, until the sum crosses the bound.
+__device__ int decayed_prefix(const uint8_t* rec, size_t stride, int n) {
+  __shared__ float s_warp[32];
+  __shared__ int s_found;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (blockDim.x + 31) >> 5;
+  float run = 0.0f;   // the sum over the tiles already scanned (the same on every thread)
+  int found = -1;
+  for (int base = n - 1; base >= 0 && found < 0; base -= (int)blockDim.x) {
+    const int j = base - tid;   // thread i takes the i-th chunk from the tile's end
+    float g = 0.0f;
+    if (j >= 0) {
+      const float e = *reinterpret_cast<const float*>(rec + (size_t)j * stride + kRecGate + (C - 1) * 4);
+      g = e > 0.0f ? __logf(e) : -INFINITY;
+    }
+    // inclusive prefix sum over the tile in thread order
+    float x = g;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_warp[warp] = x;
+    __syncthreads();
+    float before = 0.0f;
+    for (int w = 0; w < warp; ++w) before += s_warp[w];
+    const float suffix = run + before + x;   // T_j for this thread's chunk
+    // the sums fall with the thread index: count those still above the bound
+    const int above = __syncthreads_count(j >= 0 && suffix >= kNegligibleLogDecay);
+    if (above < (int)blockDim.x && base - above >= 0) found = base - above;
+    float tile = 0.0f;
+    for (int w = 0; w < nw; ++w) tile += s_warp[w];
+    run += tile;
+    __syncthreads();   // s_warp is rewritten by the next tile
+  }
+  if (tid == 0) s_found = found;
+  __syncthreads();
+  return s_found;
+}
 constexpr int kXferThreads = kXferWorkers + 64;   // + the MMA warp and the copy warp
 struct XferLay {
   static constexpr uint32_t ST = 0;          // the tracked state, bf16 [128][128], K blocks 16 KB apart
@@ -895,7 +940,26 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
   const Seg sg = load_seg(p.seg_list, u);
   if (sg.sigma == sg.nsig - 1) return;   // the last segment needs no transfer map
   const int G = p.h_v / p.h_k, kh = h / G;
-  const int nch = (sg.len + C - 1) / C;
+
+  // ---- the decayed prefix of the segment ----
+  // Chunk c's transition of the state, e^{gamma_C} prod_t (I - beta_t k^_t k^_t^T),
+  // has 2-norm at most e^{gamma_C} (beta in (0, 1), |k^| <= 1).  So whatever the
+  // state holds before chunk j reaches the segment's end shrunk by at least
+  // e^{T_j}, T_j = the sum of gamma_C over chunks j .. end.  Where T_j <
+  // kNegligibleLogDecay that is below 1e-69 of its size, far under the smallest
+  // fp32 value: track S can start at the last such chunk from zero, and track X,
+  // the whole product, is zero.  Each chunk's e^{gamma_C} is its gate record's
+  // last e^gamma (0 once it underflows, read as -inf).
+  const int nch_all = (sg.len + C - 1) / C;
+  const int j0 = decayed_prefix(p.rec_v + ((size_t)sg.c0 * p.h_v + h) * kRecV, (size_t)p.h_v * kRecV, nch_all);
+  if (track_x && j0 >= 0) {   // X = 0: the zero map as its bf16 hi / lo tiles
+    uint4* xt = reinterpret_cast<uint4*>(xfer_ptr(p, sg.k0 + sg.sigma, h, 0));
+    for (int i = tid; i < 65536 / 16; i += kXferThreads) xt[i] = make_uint4(0, 0, 0, 0);
+    return;
+  }
+  const int jb = j0 > 0 ? j0 : 0;   // track S's first chunk
+  const int nch = nch_all - jb;
+  const int c0 = sg.c0 + jb;
 
   const Smem sm = smem_aligned(smem_raw);
   if (tid == 0) {
@@ -918,8 +982,8 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
   auto wt = [&](uint64_t* mb, uint32_t k) -> bool {   // the k-th completion of mb (parity k & 1)
     return tc::mbar_wait(mb, k & 1u, kWaitBudget);
   };
-  auto rec_kq = [&](int j) { return p.rec_kq + ((size_t)(sg.c0 + j) * p.h_k + kh) * kRecKQ; };
-  auto rec_v = [&](int j) { return p.rec_v + ((size_t)(sg.c0 + j) * p.h_v + h) * kRecV; };
+  auto rec_kq = [&](int j) { return p.rec_kq + ((size_t)(c0 + j) * p.h_k + kh) * kRecKQ; };
+  auto rec_v = [&](int j) { return p.rec_v + ((size_t)(c0 + j) * p.h_v + h) * kRecV; };
   bool ok = true;
 
   if (warp == kXferWorkers / 32) {

@@ -102,6 +102,22 @@ def test_prefill_segments_carry_state_with_near_unit_decay():
     print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
 
 
+def test_prefill_segments_with_fast_and_slow_decay_heads():
+    # value heads 0-15 decay fast (the default gate distribution: a segment's
+    # total log-decay is far below -160, so the transfer scan starts near the
+    # segment's end and the map is zero), heads 16-31 slowly (exp(g) in
+    # (0.99, 1): the whole segment is scanned); one call, both kinds of head
+    lengths = [6000, 37]
+    T = sum(lengths)
+    params, tok, st = _inputs(SH, lengths, 16, ssm_std=0.1 ** 0.5, conv_std=1.0, norm_w="uniform")
+    gc = gi.gate_controlled(SH, T, 16, decay=(0.99, 1.0), beta=(0.0, 0.2))
+    slow = slice(16, 32)
+    tok["a"][:, slow], tok["b"][:, slow] = gc["a"][:, slow], gc["b"][:, slow]
+    params["A_log"][slow], params["dt_bias"][slow] = gc["A_log"][slow], gc["dt_bias"][slow]
+    e = _check(SH, lengths, params, tok, st)
+    print(f"rel err out {e[0]:.2e} state {e[1]:.2e}")
+
+
 def test_prefill_zero_write_no_decay_keeps_state_bitwise_across_segments():
     # beta = 0 and exp(g) = 1: every chunk and every segment's transfer map is
     # exactly the identity, so the state comes back bit for bit, whether or not
