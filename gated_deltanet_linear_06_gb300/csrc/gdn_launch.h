@@ -52,6 +52,7 @@ struct PrefillArgs {
   int* seg_list;           // [count, pad x3][units][8]: the segments of every sequence
   int* multi_list;         // [count, pad x3][slots][4]: sequences longer than one segment
   float* xfer;             // per boundary slot and value head: transfer map, end state, initial state
+  int* xzero;              // per boundary slot and value head: 1 where the transfer map is exactly zero
   int* chunk_off;          // [n_seqs + 1]: first chunk record of each sequence (split path; else null)
   int2* chunk_list;        // [max_chunks]: (sequence, first token) of each chunk record, sequence -1 past the end
   uint8_t* rec_kq;         // [max_chunks][h_k] per-chunk key/query tile records

@@ -661,7 +661,7 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t align1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
 struct ScratchLayout {
-  size_t seg_list, multi_list, xfer, chunk_off, chunk_list, rec_kq, rec_v, total;
+  size_t seg_list, multi_list, xfer, xzero, chunk_off, chunk_list, rec_kq, rec_v, total;
   long long max_chunks;
 };
 // The scratch of one call.  The split path (records = true) has room for a
@@ -675,14 +675,15 @@ ScratchLayout scratch_layout(int n_seqs, int h_k, int h_v, long long total_token
   l.seg_list = 0;
   l.multi_list = align256(16 + (size_t)units * 32);
   l.xfer = l.multi_list + align256(16 + (size_t)slots * 16);
-  size_t end = l.xfer + (size_t)slots * h_v * 3 * kD * kD * sizeof(float);
+  l.xzero = l.xfer + (size_t)slots * h_v * 3 * kD * kD * sizeof(float);
+  size_t end = l.xzero + align256((size_t)slots * h_v * sizeof(int));
   l.max_chunks = records ? total_tokens / C + n_seqs : 0;
   l.chunk_off = align256(end);
   l.chunk_list = l.chunk_off + (records ? align256((size_t)(n_seqs + 1) * 4) : 0);
   l.rec_kq = align1024(l.chunk_list + (size_t)l.max_chunks * 8);
   l.rec_v = l.rec_kq + (size_t)l.max_chunks * h_k * kRecKQ;
   end = l.rec_v + (size_t)l.max_chunks * h_v * kRecV;
-  l.total = records ? end : l.xfer + (size_t)slots * h_v * 3 * kD * kD * sizeof(float);
+  l.total = records ? end : l.xzero + align256((size_t)slots * h_v * sizeof(int));
   return l;
 }
 }  // namespace
@@ -810,6 +811,7 @@ cudaError_t launch_prefill(const PrefillArgs& p_in, cudaStream_t stream, bool al
   p.seg_list = reinterpret_cast<int*>(scratch + l.seg_list);
   p.multi_list = reinterpret_cast<int*>(scratch + l.multi_list);
   p.xfer = reinterpret_cast<float*>(scratch + l.xfer);
+  p.xzero = reinterpret_cast<int*>(scratch + l.xzero);
   p.chunk_off = allow_split ? reinterpret_cast<int*>(scratch + l.chunk_off) : nullptr;
   p.chunk_list = allow_split ? reinterpret_cast<int2*>(scratch + l.chunk_list) : nullptr;
   p.rec_kq = allow_split ? reinterpret_cast<uint8_t*>(scratch + l.rec_kq) : nullptr;

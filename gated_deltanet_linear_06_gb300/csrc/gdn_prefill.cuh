@@ -356,10 +356,17 @@ __device__ __forceinline__ void ut_st4(float* M, int t, int s4, float a, float b
 }
 
 // acc[r][e] += sum_{k < nk} X[xr[r]][xc + k] Y[yr + k][yc + e] for two rows
-// (R = 2) or one, the sum in increasing k; nk a multiple of 4.
+// (R = 2) or one, the sum in increasing k; nk a multiple of 4.  Column pairs
+// run as packed fp32x2 multiply-adds, each element rounding as fmaf would.
 template <int R>
 __device__ __forceinline__ void ut_rowquad(const float* X, const int (&xr)[R], int xc, const float* Y, int yr,
                                            int yc, int nk, float (&acc)[R][4]) {
+  float2 a2[R][2];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    a2[r][0] = make_float2(acc[r][0], acc[r][1]);
+    a2[r][1] = make_float2(acc[r][2], acc[r][3]);
+  }
 #pragma unroll 2
   for (int k = 0; k < nk; k += 4) {
     float xk[R][4];
@@ -371,14 +378,19 @@ __device__ __forceinline__ void ut_rowquad(const float* X, const int (&xr)[R], i
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       const float4 y4 = ut_ld4(Y, yr + k + kk, yc);
+      const float2 ylo = make_float2(y4.x, y4.y), yhi = make_float2(y4.z, y4.w);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        acc[r][0] = fmaf(xk[r][kk], y4.x, acc[r][0]);
-        acc[r][1] = fmaf(xk[r][kk], y4.y, acc[r][1]);
-        acc[r][2] = fmaf(xk[r][kk], y4.z, acc[r][2]);
-        acc[r][3] = fmaf(xk[r][kk], y4.w, acc[r][3]);
+        const float2 x2 = make_float2(xk[r][kk], xk[r][kk]);
+        a2[r][0] = __ffma2_rn(x2, ylo, a2[r][0]);
+        a2[r][1] = __ffma2_rn(x2, yhi, a2[r][1]);
       }
     }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    acc[r][0] = a2[r][0].x; acc[r][1] = a2[r][0].y;
+    acc[r][2] = a2[r][1].x; acc[r][3] = a2[r][1].y;
   }
 }
 

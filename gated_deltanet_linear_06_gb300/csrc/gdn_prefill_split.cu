@@ -952,10 +952,13 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
   // last e^gamma (0 once it underflows, read as -inf).
   const int nch_all = (sg.len + C - 1) / C;
   const int j0 = decayed_prefix(p.rec_v + ((size_t)sg.c0 * p.h_v + h) * kRecV, (size_t)p.h_v * kRecV, nch_all);
-  if (track_x && j0 >= 0) {   // X = 0: the zero map as its bf16 hi / lo tiles
-    uint4* xt = reinterpret_cast<uint4*>(xfer_ptr(p, sg.k0 + sg.sigma, h, 0));
-    for (int i = tid; i < 65536 / 16; i += kXferThreads) xt[i] = make_uint4(0, 0, 0, 0);
-    return;
+  if (track_x) {   // the combine pass skips steps whose map is zero
+    if (tid == 0) p.xzero[(size_t)(sg.k0 + sg.sigma) * p.h_v + h] = j0 >= 0 ? 1 : 0;
+    if (j0 >= 0) {   // X = 0: the zero map as its bf16 hi / lo tiles
+      uint4* xt = reinterpret_cast<uint4*>(xfer_ptr(p, sg.k0 + sg.sigma, h, 0));
+      for (int i = tid; i < 65536 / 16; i += kXferThreads) xt[i] = make_uint4(0, 0, 0, 0);
+      return;
+    }
   }
   const int jb = j0 > 0 ? j0 : 0;   // track S's first chunk
   const int nch = nch_all - jb;
@@ -1227,6 +1230,16 @@ __global__ void __launch_bounds__(kCombThreads, 1) combine_kernel(const PrefillA
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = 32 * (warp & 3) + lane, col0 = 32 * (warp >> 2);   // TMEM lane = state row, 32 columns
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+  // Where every map of the sequence is exactly zero, each S_{sigma+1} is its
+  // S_sigma^0, which slot sigma already holds: only the initial state is saved.
+  int nonzero = 0;
+  for (int sg = tid; sg < steps; sg += kCombThreads) nonzero |= p.xzero[(size_t)(k0 + sg) * p.h_v + h] == 0;
+  if (!__syncthreads_or(nonzero)) {
+    float v[32];
+    load_state_row(p.ssm_state + ((size_t)n * p.h_v + h) * kD * kD, false, row, col0, v);
+    store_state_row(xfer_ptr(p, k0, h, 2), true, row, col0, v);
+    return;
+  }
   const Smem sm = smem_aligned(smem_raw);
   if (tid == 0) {
     tc::mbar_init(&mb_x[0], 1);
