@@ -947,8 +947,9 @@ __global__ void __launch_bounds__(kXferThreads, 2) xfer_kernel(const PrefillArgs
   // state holds before chunk j reaches the segment's end shrunk by at least
   // e^{T_j}, T_j = the sum of gamma_C over chunks j .. end.  Where T_j <
   // kNegligibleLogDecay that is below 1e-69 of its size, far under the smallest
-  // fp32 value: track S can start at the last such chunk from zero, and track X,
-  // the whole product, is zero.  Each chunk's e^{gamma_C} is its gate record's
+  // fp32 value: track S can start at the last such chunk from zero (the result
+  // then differs from the full scan by rounding only), and track X, the whole
+  // product, is zero.  Each chunk's e^{gamma_C} is its gate record's
   // last e^gamma (0 once it underflows, read as -inf).
   const int nch_all = (sg.len + C - 1) / C;
   const int j0 = decayed_prefix(p.rec_v + ((size_t)sg.c0 * p.h_v + h) * kRecV, (size_t)p.h_v * kRecV, nch_all);
