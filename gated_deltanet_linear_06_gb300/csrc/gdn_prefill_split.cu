@@ -39,26 +39,31 @@ namespace {
 // ============================== prep pass ==============================
 
 constexpr int kPrepThreads = 256;
+constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kMaxG = 4;   // value heads per key head on the compiled path
-// Shared memory (bytes from a 1024-aligned base).  Sized for two CTAs per SM.
+// Shared memory (bytes from a 1024-aligned base), sized for three CTAs per SM:
+// two raw staging blocks (k and q first, then the v rows of the value heads in
+// turn), the fp16 [K^ | Q^] tile of the Gram product and the gates.  The value
+// heads then run one after another in the Gram tile's space, with the bf16 K^
+// tile of their W products in the first staging block.
 struct PrepLay {
-  static constexpr uint32_t KQ = 0;             // bf16 [K^ | Q^], 64-column blocks 16 KB apart
-  static constexpr uint32_t KQ16 = 32768;       // fp16 copy of KQ (Gram operands), then head group 0's area
-  static constexpr uint32_t RAW = 66560;        // two staged raw blocks: q | k, then v of two heads;
-                                                // then head group 1's area
-  static constexpr uint32_t GATE = RAW + 2 * RAW_BLK;   // per head: fp32 gamma, beta, e^gamma [64]
+  static constexpr uint32_t KQ16 = 0;       // fp16 [K^ | Q^], 64-column blocks 16 KB apart; then a head's area
+  static constexpr uint32_t RAW = 32768;    // staging block b at RAW + b * RAW_STRIDE
+  static constexpr uint32_t RAW_STRIDE = (RAW_BLK + 1023) / 1024 * 1024;
+  static constexpr uint32_t KB = RAW;       // bf16 K^ [t][d_k], 64-column blocks 8 KB apart (head phase)
+  static constexpr uint32_t GATE = RAW + RAW_STRIDE + RAW_BLK;   // per value head: fp32 gamma, beta, e^gamma [64]
   static constexpr uint32_t BYTES = GATE + kMaxG * 3 * 64 * 4 + 1024;   // + slack to align the base
-  // A head group's area: the solve's A and T (fp32, 16 KB each) -- with the
+  // A value head's area: the solve's A and T (fp32, 16 KB each) -- with the
   // bf16 P tile over T's first 8 KB until the solve writes T --, then
   // T diag(beta e^gamma) over A, then -W [d_k][t] over A
-  __host__ __device__ static constexpr uint32_t area(int grp) { return grp == 0 ? KQ16 : RAW; }
+  static constexpr uint32_t AREA = KQ16;
 };
-static_assert(PrepLay::KQ16 + 2 * UT_BYTES <= PrepLay::RAW, "head group 0's A and T overlap the raw staging");
-static_assert(2 * UT_BYTES <= 2 * RAW_BLK, "head group 1's A and T exceed the raw staging");
+static_assert(2 * UT_BYTES <= PrepLay::RAW - PrepLay::KQ16, "a head's A and T fit the Gram tile's space");
+static_assert(16384 <= RAW_BLK, "the K^ tile fits a staging block");
 static_assert(16384 <= UT_BYTES, "-W goes over A");
 static_assert(PrepLay::RAW % 1024 == 0 && RAW_BLK % 128 == 0, "TMA destinations need 128-byte alignment");
-static_assert(2 * (PrepLay::BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
-constexpr uint32_t TP_G = 0, TP_W = 64, TP_COLS = 256;   // TMEM: Gram [K^;Q^]K^T, W^T per head group
+static_assert(3 * (PrepLay::BYTES + 1024) <= 228 * 1024, "three prep CTAs per SM");
+constexpr uint32_t TP_G = 0, TP_W = 64, TP_COLS = 128;   // TMEM: Gram [K^;Q^]K^T, W^T of the current head
 
 // This lane's 4 channels ch .. ch+3 of the conv weight as stored (bf16 [channel][tap]),
 // and unpacked to w[tap][channel].
@@ -81,17 +86,18 @@ __device__ __forceinline__ void conv_weights(const ConvW4& cw, float (&w)[kConvW
 }
 
 // One CTA per (chunk, key head): the state-free part of the chunk for the G
-// value heads that read this key head, stored as records.
-__global__ void __launch_bounds__(kPrepThreads, 2)
+// value heads that read this key head, stored as records.  Three CTAs share an
+// SM, so one CTA's waits (a raw block in flight, a product, a barrier behind
+// its slowest warp) leave the issue slots to the other two.
+__global__ void __launch_bounds__(kPrepThreads, 3)
     prep_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv) {
   using L_ = PrepLay;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t mbar;       // MMA completion
-  __shared__ __align__(8) uint64_t mbar_raw;   // staged raw q | k rows landed
-  __shared__ __align__(8) uint64_t mb_rv[2];   // a staging block's raw v rows landed
-  __shared__ __align__(8) uint64_t mb_w[2];    // a head group's W product done
-  __shared__ int rv_read[2];                   // warps done reading a staging block (cumulative)
-  __shared__ int rv_issued[2];                 // v copies issued into a staging block
+  __shared__ __align__(8) uint64_t mbar;       // the Gram product done
+  __shared__ __align__(8) uint64_t mb_raw[2];  // a staging block's raw rows landed
+  __shared__ __align__(8) uint64_t mb_w;       // a value head's W product done
+  __shared__ int raw_read[2];                  // warps done reading a staging block (cumulative)
+  __shared__ int raw_issued[2];                // raw loads issued into a staging block
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -105,17 +111,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   const int G = p.h_v / p.h_k;
   const int Cq = p.h_k * kD, Cc = 2 * Cq + p.h_v * kD;
   const float* cs_seq = p.conv_state + (size_t)n * (kConvW - 1) * Cc;   // this sequence's carried conv state
+  uint8_t* rkq = p.rec_kq + ((size_t)c * p.h_k + kh) * kRecKQ;
 
   const Smem sm = smem_aligned(smem_raw);
 
   if (tid == 0) {
     tc::mbar_init(&mbar, 1);
-    tc::mbar_init(&mbar_raw, 1);
-    for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&mb_rv[i], 1);
-      tc::mbar_init(&mb_w[i], 1);
-      rv_read[i] = 0;
-      rv_issued[i] = 0;
+    tc::mbar_init(&mb_w, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&mb_raw[b], 1);
+      raw_read[b] = 0;
+      raw_issued[b] = 1;   // k and q, issued below
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -124,60 +130,47 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base_s;
-  const int quarter = warp & 3, half = warp >> 2;   // TMEM lane quarter; CTA half (= head group)
+  const int quarter = warp & 3, half = warp >> 2;   // TMEM lane quarter; column half
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
   const int row = 32 * quarter + lane;
   const int y_raw = start + t0 - (kConvW - 1);      // first staged row (a chunk and its halo)
-  if (tid == 32) {   // raw q and k rows
-    mbar_expect_tx(&mbar_raw, 2 * RAW_BLK);
-    tma_load_2d(sm.base + L_::RAW, &tm_qkv, kh * kD, y_raw, &mbar_raw);
-    tma_load_2d(sm.base + L_::RAW + RAW_BLK, &tm_qkv, Cq + kh * kD, y_raw, &mbar_raw);
-  }
-  uint32_t phase = 0, raw_phase = 0;
-  bool raw_pending = true;
-  auto wait_mma = [&]() -> bool {
-    const bool ok = tc::mbar_wait(&mbar, phase, kWaitBudget);
-    phase ^= 1u;
-    const bool all_ok = __syncthreads_and(ok);
-    tc::fence_after_sync();
-    return all_ok;
-  };
-  auto wait_raw = [&]() -> bool {   // on a time-out the copy stays pending for the exit path
-    const bool ok_all = __syncthreads_and(tc::mbar_wait(&mbar_raw, raw_phase, kWaitBudget));
-    if (ok_all) {
-      raw_phase ^= 1u;
-      raw_pending = false;
+  // Staging block b takes the k (b = 0) or q (b = 1) rows, then the v rows of
+  // value heads kh*G + b, kh*G + b + 2, ...
+  auto raw_blk = [&](int b) { return sm.base + L_::RAW + b * L_::RAW_STRIDE; };
+  if (tid == 32) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      mbar_expect_tx(&mb_raw[b], RAW_BLK);
+      tma_load_2d(raw_blk(b), &tm_qkv, (b == 0 ? Cq : 0) + kh * kD, y_raw, &mb_raw[b]);
     }
-    return ok_all;
+  }
+  uint32_t raw_waited[2] = {0, 0};   // the same on every thread
+  auto wait_raw = [&](int b) -> bool {   // on a time-out the copy stays pending for the exit path
+    const bool all = __syncthreads_and(tc::mbar_wait(&mb_raw[b], raw_waited[b] & 1u, kWaitBudget));
+    if (all) ++raw_waited[b];
+    return all;
   };
-  // The two staging blocks take raw v rows as soon as the rows before them are
-  // read: block b holds value head 2r + b in round r.  The last of the eight
-  // warps to finish reading a block (its release number `rel`, counted from 0)
-  // issues the refill with value head g, if the key head has one.
-  auto release_blk = [&](int blk, int g, int rel) {
+  // Each warp done reading a staging block counts itself out; the last one of
+  // the block's release `rel` (counted from 0) issues its next raw load: the v
+  // rows of value head g = 2 rel + b, if the key head has it.
+  auto release_raw = [&](int b, int rel) {
     __syncwarp();
     if (lane == 0) {
       __threadfence_block();
-      if (atomicAdd(&rv_read[blk], 1) == (kPrepThreads / 32) * (rel + 1) - 1 && g < G) {
+      const int g = 2 * rel + b;
+      if (atomicAdd(&raw_read[b], 1) == kPrepWarps * (rel + 1) - 1 && g < G) {
         __threadfence_block();
         tc::fence_proxy_async();
-        mbar_expect_tx(&mb_rv[blk], RAW_BLK);
-        tma_load_2d(sm.base + L_::RAW + blk * RAW_BLK, &tm_qkv, 2 * Cq + (kh * G + g) * kD, y_raw, &mb_rv[blk]);
-        ++rv_issued[blk];
+        mbar_expect_tx(&mb_raw[b], RAW_BLK);
+        tma_load_2d(raw_blk(b), &tm_qkv, 2 * Cq + (kh * G + g) * kD, y_raw, &mb_raw[b]);
+        ++raw_issued[b];
       }
     }
   };
-  uint32_t rv_waited0 = 0, rv_waited1 = 0;   // the same on every thread
-  auto wait_rv = [&](int blk) -> bool {
-    uint32_t& w = blk == 0 ? rv_waited0 : rv_waited1;
-    const bool all = __syncthreads_and(tc::mbar_wait(&mb_rv[blk], w & 1u, kWaitBudget));
-    if (all) ++w;
-    return all;
-  };
   bool ok = true;
-  // this lane's q and k conv weights, in flight while the gates run
-  const ConvW4 cw_qk[2] = {conv_weights_load(p.conv_w, kh * kD + 4 * lane),
-                           conv_weights_load(p.conv_w, Cq + kh * kD + 4 * lane)};
+  // this lane's k and q conv weights, in flight while the gates run
+  const ConvW4 cw_kq[2] = {conv_weights_load(p.conv_w, Cq + kh * kD + 4 * lane),
+                           conv_weights_load(p.conv_w, kh * kD + 4 * lane)};
 
   // ---- gates and their cumulative sums, warp g for value head kh*G + g (meanwhile
   //      the raw rows land); the scan passes get e^gamma and e^{gamma_C - gamma} ----
@@ -222,38 +215,39 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     }
   }
 
-  // ---- conv + SiLU + L2 norms of q and k -> [K^ | Q^] in bf16 and fp16 ----
-  if (!wait_raw()) ok = false;
-  static_assert(C / 4 == 2 * (kPrepThreads / 32), "each warp takes two token quads of q and two of k");
-  if (ok) {
-    const float qscale = rsqrtf((float)kD);
+  // ---- conv + SiLU + L2 norms, k then q: into the fp16 Gram tile, and in bf16
+  //      straight into the record ----
+  static_assert(C / 4 == 2 * kPrepWarps, "each warp takes two token quads of each block");
+  const float qscale = rsqrtf((float)kD);
 #pragma unroll
-    for (int blk = 0; blk < 2; ++blk) {   // 0: q, 1: k
-      const int ch = (blk == 0 ? 0 : Cq) + kh * kD + 4 * lane;
-      float w[kConvW][4];
-      conv_weights(cw_qk[blk], w);
-#pragma unroll 1
-      for (int qd = 0; qd < 2; ++qd) {
-        const int tq = 4 * (warp + 8 * qd);
-        float y[4][4];
-        conv_quad_staged(sm.base + L_::RAW + blk * RAW_BLK, cs_seq + ch, Cc, t0, L, tq, lane, w, y);
-        float rn[4];
-        l2_rnorm4(y, p.l2_eps, blk == 0 ? qscale : 1.0f, lane, rn);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 r2 = make_float2(rn[i], rn[i]);
-          const float2 a = __fmul2_rn(make_float2(y[i][0], y[i][1]), r2);
-          const float2 b = __fmul2_rn(make_float2(y[i][2], y[i][3]), r2);
-          y[i][0] = a.x; y[i][1] = a.y; y[i][2] = b.x; y[i][3] = b.y;
-          const uint32_t o16 = tc::sw128_off(tq + i, 4 * lane, 16384) + (blk == 0 ? 8192u : 0u);
-          store_bf16x4(sm.base + L_::KQ, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
-          store_f16x4(sm.base + L_::KQ16, o16, y[i][0], y[i][1], y[i][2], y[i][3]);
-        }
-      }
-      release_blk(blk, blk, 0);   // q's block takes value head 0, k's value head 1
+  for (int blk = 0; blk < 2; ++blk) {   // 0: k, 1: q
+    if (!wait_raw(blk)) {
+      ok = false;
+      break;
     }
+    const int ch = (blk == 0 ? Cq : 0) + kh * kD + 4 * lane;
+    float w[kConvW][4];
+    conv_weights(cw_kq[blk], w);
+#pragma unroll 1
+    for (int qd = 0; qd < 2; ++qd) {
+      const int tq = 4 * (warp + kPrepWarps * qd);
+      float y[4][4];
+      conv_quad_staged(raw_blk(blk), cs_seq + ch, Cc, t0, L, tq, lane, w, y);
+      float rn[4];
+      l2_rnorm4(y, p.l2_eps, blk == 0 ? 1.0f : qscale, lane, rn);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 r2 = make_float2(rn[i], rn[i]);
+        const float2 a = __fmul2_rn(make_float2(y[i][0], y[i][1]), r2);
+        const float2 b = __fmul2_rn(make_float2(y[i][2], y[i][3]), r2);
+        const uint32_t o16 = tc::sw128_off(tq + i, 4 * lane, 16384) + (blk == 0 ? 0u : 8192u);
+        store_f16x4(sm.base + L_::KQ16, o16, a.x, a.y, b.x, b.y);
+        store_bf16x4(rkq, o16, a.x, a.y, b.x, b.y);
+      }
+    }
+    release_raw(blk, 0);   // k's block takes value head 0's v rows, q's value head 1's
   }
-  sync_for_mma();   // also: the raw q | k rows are read
+  sync_for_mma();   // the Gram tile is written
   if (ok && tid == 0) {
     // Gram [K^; Q^] K^T in fp16 (rows 0-63: K^K^T, 64-127: Q^K^T)
 #pragma unroll
@@ -262,62 +256,68 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
       tc::mma_bf16(tmem + TP_G, tc::sdesc_at(D_K, a), tc::sdesc_at(D_K, a), ID_GRAM, k > 0);
     }
     tc::mma_commit(&mbar);
-    bulk_store(p.rec_kq + ((size_t)c * p.h_k + kh) * kRecKQ, sm.base + L_::KQ, kRecKQ);
-    bulk_commit();
   }
 
-  // ---- conv + SiLU of v, two value heads at a time, straight into their records ----
+  // ---- conv + SiLU of v, a value head at a time, straight into its record ----
 #pragma unroll 1
-  for (int g0 = 0, rel = 1; g0 < G && ok; g0 += 2, ++rel) {
-    const int nv = min(2, G - g0);
-    // this lane's conv weights of the two heads
-    const ConvW4 cw_v[2] = {conv_weights_load(p.conv_w, 2 * Cq + (kh * G + g0) * kD + 4 * lane),
-                            conv_weights_load(p.conv_w, 2 * Cq + (kh * G + g0 + nv - 1) * kD + 4 * lane)};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      if (i >= nv) break;
-      if (!wait_rv(i)) { ok = false; break; }
-      const int h = kh * G + g0 + i;
-      const int ch = 2 * Cq + h * kD + 4 * lane;
-      float w[kConvW][4];
-      conv_weights(cw_v[i], w);
-      uint8_t* vh = p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecVH;
-#pragma unroll 1
-      for (int qd = 0; qd < 2; ++qd) {
-        const int tq = 4 * (warp + 8 * qd);
-        float y[4][4];
-        conv_quad_staged(sm.base + L_::RAW + i * RAW_BLK, cs_seq + ch, Cc, t0, L, tq, lane, w, y);
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
-      }
-      release_blk(i, g0 + 2 + i, rel);
+  for (int g = 0; g < G && ok; ++g) {
+    const int h = kh * G + g;
+    const int ch = 2 * Cq + h * kD + 4 * lane;
+    const ConvW4 cw_v = conv_weights_load(p.conv_w, ch);
+    if (!wait_raw(g & 1)) {
+      ok = false;
+      break;
     }
-  }
-  if (ok && !wait_mma()) ok = false;   // the Gram product (and KQ16 is free)
-
-  // ---- per value head, the two halves of the CTA (128 threads, a warp per TMEM
-  //      lane quarter) each take a head, synchronising on their own barrier ----
-  {
-    const int grp = half, gtid = tid & 127, bar = 1 + grp;
-    float* Af = sm.f32(L_::area(grp));
-    float* Tf = Af + UT_BYTES / 4;
-    uint8_t* ptile = sm.base + L_::area(grp) + UT_BYTES;
-    uint8_t* wn = sm.base + L_::area(grp);
-    const uint32_t tw = sm.addr + L_::area(grp);
-    const uint32_t tm_w = tmem + TP_W + 64 * grp;
-    uint32_t wphase = 0;
-    bool gok = ok;
+    float w[kConvW][4];
+    conv_weights(cw_v, w);
+    uint8_t* vh = p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecVH;
 #pragma unroll 1
-    for (int g = grp; g < G && gok; g += 2) {
+    for (int qd = 0; qd < 2; ++qd) {
+      const int tq = 4 * (warp + kPrepWarps * qd);
+      float y[4][4];
+      conv_quad_staged(raw_blk(g & 1), cs_seq + ch, Cc, t0, L, tq, lane, w, y);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
+    }
+    release_raw(g & 1, 1 + (g >> 1));
+  }
+  if (ok) {
+    // the bf16 K^ tile of the W products, back from this CTA's record into the
+    // first staging block (64-column blocks 16 KB apart there, 8 KB here), once
+    // every warp is done with the block
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = tid + j * kPrepThreads, kb = i >> 9, off = (i & 511) * 16;
+      *reinterpret_cast<uint4*>(sm.base + L_::KB + kb * 8192 + off) =
+          __ldcg(reinterpret_cast<const uint4*>(rkq + kb * 16384 + off));
+    }
+    // the Gram product (and its tile's space is free)
+    ok = __syncthreads_and(tc::mbar_wait(&mbar, 0, kWaitBudget));
+    tc::fence_after_sync();
+  }
+
+  // ---- per value head, one after another: a warp per TMEM lane quarter and
+  //      column half ----
+  {
+    float* Af = sm.f32(L_::AREA);
+    float* Tf = Af + UT_BYTES / 4;
+    uint8_t* ptile = sm.base + L_::AREA + UT_BYTES;
+    uint8_t* wn = sm.base + L_::AREA;
+    const uint32_t tw = sm.addr + L_::AREA;
+    const uint32_t tm_w = tmem + TP_W;
+    uint32_t wphase = 0;
+#pragma unroll 1
+    for (int g = 0; g < G && ok; ++g) {
       const int h = kh * G + g;
       uint8_t* rv = p.rec_v + ((size_t)c * p.h_v + h) * kRecV;
       const float* gam = sm.f32(L_::GATE + g * 3 * 64 * 4);
       const float* bet = gam + 64;
       const float* eg = gam + 128;
-      if (g >= 2) {   // this group's previous -W tile has left shared memory
-        if (gtid == 0) bulk_wait_read();
-        group_sync<128>(bar);
+      if (g >= 1) {   // the previous head's -W tile has left shared memory
+        if (tid == 0) bulk_wait_read();
+        __syncthreads();
       }
       // ---- A (fp32, below its diagonal: the solve reads nothing else) and P
       //      (bf16 tile, bulk-stored into the record) from the Gram rows: lane
@@ -327,17 +327,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         const int t = row & 63;
         const float gt = gam[t];
         const float bt = bet[t];
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          const int c0 = 32 * hf;
-          if (t < 32 && hf == 1) {
-            if (quarter >= 2) {
+        const int c0 = 32 * half;
+        if (t < 32 && half == 1) {
+          if (quarter >= 2) {
 #pragma unroll
-              for (int m = 0; m < 4; ++m)
-                *reinterpret_cast<uint4*>(ptile + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
-            }
-            continue;
+            for (int m = 0; m < 4; ++m)
+              *reinterpret_cast<uint4*>(ptile + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
           }
+        } else {
           float v[32];
           tc::tmem_ld32(tmem + lane_base + TP_G + c0, v);
           if (quarter < 2) {
@@ -360,22 +357,22 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
       }
       tc::fence_proxy_async();
-      group_sync<128>(bar);
-      if (gtid == 0) {
+      __syncthreads();
+      if (tid == 0) {
         bulk_store(rv + kRecP, ptile, 8192);
         bulk_commit();
       }
 
       // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) over A ----
-      solve_unit_lower<128>(Af, Tf, gtid, bar, [&] {   // the P tile has left T's rows
-        if (gtid == 0) bulk_wait_read();
-        group_sync<128>(bar);
+      solve_unit_lower<kPrepThreads>(Af, Tf, tid, 0, [&] {   // the P tile has left T's rows
+        if (tid == 0) bulk_wait_read();
+        __syncthreads();
       });
       {
-        float xb[4][8], xw[4][8];
+        float xb[2][8], xw[2][8];
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int e = gtid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
+        for (int q4 = 0; q4 < 2; ++q4) {
+          const int e = tid + q4 * kPrepThreads, t = e >> 3, c8 = (e & 7) * 8;
           const float4 lo = ut_ld4(Tf, t, c8), hi = ut_ld4(Tf, t, c8 + 4);
           const float tv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
@@ -385,61 +382,53 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
           }
         }
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int e = gtid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
+        for (int q4 = 0; q4 < 2; ++q4) {
+          const int e = tid + q4 * kPrepThreads, t = e >> 3, c8 = (e & 7) * 8;
           store_bf16x8(rv + kRecTB, tc::sw128_off(t, c8, 0), xb[q4]);
           store_bf16x8(wn, tc::sw128_off(t, c8, 0), xw[q4]);
         }
       }
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      group_sync<128>(bar);
-      tc::fence_after_sync();
-      if (gtid == 0) {
+      sync_for_mma();
+      if (tid == 0) {
         // W^T = K^T (T diag(beta e^gamma))^T
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tm_w, tc::sdesc_at(D_MN_KQ, sm.addr + L_::KQ + k * 2048), tc::sdesc_at(D_K, tw + k * 32),
+          tc::mma_bf16(tm_w, tc::sdesc_at(D_MN_V, sm.addr + L_::KB + k * 2048), tc::sdesc_at(D_K, tw + k * 32),
                        ID_MN_A, k > 0);
-        tc::mma_commit(&mb_w[grp]);
+        tc::mma_commit(&mb_w);
       }
-      gok = group_sync_and<128>(bar, tc::mbar_wait(&mb_w[grp], wphase, kWaitBudget));
+      ok = __syncthreads_and(tc::mbar_wait(&mb_w, wphase, kWaitBudget));
       wphase ^= 1u;
       tc::fence_after_sync();
-      if (!gok) break;
+      if (!ok) break;
 
-      // ---- -W tile [d_k][t] (over T diag(beta e^gamma), which the MMA has consumed):
-      //      a thread's TMEM lane is its d_k row, so each writes 64 contiguous bytes ----
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
+      // ---- -W tile [d_k][t] (over T diag(beta e^gamma), which the product has
+      //      consumed): a thread's TMEM lane is its d_k row, its 32 columns 64
+      //      contiguous bytes ----
+      {
         float v[32];
-        tc::tmem_ld32(tm_w + lane_base + 32 * hf, v);
+        tc::tmem_ld32(tm_w + lane_base + 32 * half, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = -v[i];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) store_bf16x8(wn, tc::sw128_off(row, 32 * hf + 8 * m, 0), v + 8 * m);
+        for (int m = 0; m < 4; ++m) store_bf16x8(wn, tc::sw128_off(row, 32 * half + 8 * m, 0), v + 8 * m);
       }
-      tc::fence_proxy_async();
-      group_sync<128>(bar);
-      if (gtid == 0) {
+      sync_for_mma();   // also: W^T is read before the next head's product overwrites it
+      if (tid == 0) {
         bulk_store(rv + kRecWN, wn, 16384);
         bulk_commit();
       }
     }
-    // this group's record copies have read their shared memory before it goes away
-    // (their global writes complete with the grid, before any later kernel reads them)
-    if (gtid == 0) bulk_wait_read();
-    ok = __syncthreads_and(gok) && ok;
   }
 
   if (tid == 0) {
     if (!ok) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
-    bulk_wait_read();   // the KQ record copy has read this CTA's shared memory
+    bulk_wait_read();   // the record copies have read this CTA's shared memory
   }
   // a raw copy still in flight after a time-out must land before the shared memory goes away
-  if (raw_pending) tc::mbar_wait(&mbar_raw, raw_phase, kWaitBudget);
-  if ((uint32_t)rv_issued[0] > rv_waited0) tc::mbar_wait(&mb_rv[0], rv_waited0 & 1u, kWaitBudget);
-  if ((uint32_t)rv_issued[1] > rv_waited1) tc::mbar_wait(&mb_rv[1], rv_waited1 & 1u, kWaitBudget);
+#pragma unroll
+  for (int b = 0; b < 2; ++b)
+    if ((uint32_t)raw_issued[b] > raw_waited[b]) tc::mbar_wait(&mb_raw[b], raw_waited[b] & 1u, kWaitBudget);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TP_COLS);
