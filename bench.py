@@ -542,7 +542,7 @@ def run_ours(args) -> dict | None:
         "e2e": {"value": round(world * PREFILL_T / (e2e_pre_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre,
                 "call": "gdn_prefill_host (host activations in and output out, copies "
-                        "overlapped with compute, 4096-token segments) + D2H of the final states"},
+                        "overlapped with compute, 5120-token segments) + D2H of the final states"},
         "gpu_launches": K * (prefill_kernels + DECODE_CALLS),
         "next_rows": extra,
         "clocks": clocks.summary(),

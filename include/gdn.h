@@ -197,7 +197,7 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
  * gdn_prefill with the activations in HOST memory: the call copies the inputs
  * in and the output out itself, overlapping the host link with the compute.
  *
- * The packed tokens are cut into segments of seg_tokens (0: 4096) tokens, fed
+ * The packed tokens are cut into segments of seg_tokens (0: 5120) tokens, fed
  * as a chunked-prefill scheduler would (llmxabe README, worker diagram): each
  * segment is one gdn_prefill call whose sequences continue from the states the
  * previous segment left.  Two library copy streams move segment i+1's inputs

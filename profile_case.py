@@ -5,7 +5,7 @@
   python profile_case.py --kernel decode_multi --batch 256 --steps 4
   python profile_case.py --kernel state_copy --batch 256
   python profile_case.py --kernel decode_graph --batch 3 --steps 64
-  python profile_case.py --kernel prefill_host --tokens 32768 --seg 4096
+  python profile_case.py --kernel prefill_host --tokens 32768 --seg 5120
   python profile_case.py --kernel in_proj --tokens 32768 --hidden 2048
   python profile_case.py --kernel out_proj --tokens 32768 --hidden 2048
 

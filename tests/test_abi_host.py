@@ -297,7 +297,7 @@ def test_prefill_host_segments_match_the_plain_model_and_tile_the_batch(L):
         cu = [0] + list(np.cumsum(lens).astype(int))
         T = cu[-1]
         got = gdn.gdn_prefill_host_segments(torch.tensor(cu, dtype=torch.int32), seg)
-        eff = min(seg if seg else 4096, T)
+        eff = min(seg if seg else 5120, T)
         assert got == _segments_model(cu, T, eff), (trial, cu, seg)
         # the segments tile [0, T) and each holds every token of its sequences' overlap
         assert got[0][0] == 0 and got[-1][1] == T
