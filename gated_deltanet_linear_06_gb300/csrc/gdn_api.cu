@@ -17,7 +17,7 @@
 
 namespace {
 
-constexpr int kVersion = 300;  // 0.3.0: the input and output projections around the layer
+constexpr int kVersion = 310;  // 0.3.1: the decode step from host buffers
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -232,6 +232,79 @@ gdn_status gdn_decode_multi(const gdn_dims* dims, const void* qkv, const void* z
                  cudaSuccess
              ? GDN_OK
              : GDN_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The device staging area of gdn_decode_step_host: the step's qkv, z, a, b and
+// its output, each 256-byte aligned.
+struct DecodeHostLayout {
+  size_t qkv, z, a, b, out, total;
+};
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+bool decode_host_layout(const gdn_dims* d, int batch, int out_dtype, DecodeHostLayout& l) {
+  if (check_dims(d) != GDN_OK || batch < 0 || (out_dtype != GDN_DTYPE_BF16 && out_dtype != GDN_DTYPE_F32))
+    return false;
+  const size_t B = (size_t)(batch > 0 ? batch : 1);
+  const size_t cc = 2ull * d->h_k * d->d_k + (size_t)d->h_v * d->d_v, zv = (size_t)d->h_v * d->d_v;
+  size_t off = 0;
+  l.qkv = off; off = round256(off + B * cc * 2);
+  l.z = off;   off = round256(off + B * zv * 2);
+  l.a = off;   off = round256(off + B * d->h_v * 2);
+  l.b = off;   off = round256(off + B * d->h_v * 2);
+  l.out = off; off = round256(off + B * zv * (out_dtype == GDN_DTYPE_F32 ? 4 : 2));
+  l.total = off;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t gdn_decode_step_host_workspace_bytes(const gdn_dims* dims, int batch, int out_dtype) {
+  DecodeHostLayout l;
+  return decode_host_layout(dims, batch, out_dtype, l) ? l.total : 0;
+}
+
+gdn_status gdn_decode_step_host(const gdn_dims* dims, const void* qkv, const void* z, const void* a,
+                                const void* b, const float* A_log, const float* dt_bias,
+                                const void* conv_w, const float* norm_w, const int32_t* slot,
+                                int n_slots, int batch, float* conv_state, float* ssm_state, void* out,
+                                int out_dtype, int32_t* device_status, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  gdn::TraceRange trace_range("gdn_decode_step_host");
+  DecodeHostLayout l;
+  if (!decode_host_layout(dims, batch, out_dtype, l)) {
+    const gdn_status st = check_dims(dims);
+    return st != GDN_OK ? st : GDN_ERR_INVALID_ARG;
+  }
+  if (batch == 0) return GDN_OK;
+  if (!qkv || !z || !a || !b || !out) return GDN_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < l.total)
+    return GDN_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  // every argument checked, against the staging buffers, before anything is enqueued
+  gdn::DecodeArgs p;
+  const gdn_status st = decode_args(dims, ws + l.qkv, ws + l.z, ws + l.a, ws + l.b, A_log, dt_bias, conv_w,
+                                    norm_w, slot, n_slots, batch, 1, conv_state, ssm_state, ws + l.out,
+                                    out_dtype, nullptr, nullptr, device_status, p);
+  if (st != GDN_OK) return st;
+  const size_t B = (size_t)batch;
+  const size_t cc = 2ull * dims->h_k * dims->d_k + (size_t)dims->h_v * dims->d_v;
+  const size_t zv = (size_t)dims->h_v * dims->d_v, hv = (size_t)dims->h_v;
+  const size_t out_bytes = B * zv * (out_dtype == GDN_DTYPE_F32 ? 4 : 2);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(ws + l.qkv, qkv, B * cc * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(ws + l.z, z, B * zv * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(ws + l.a, a, B * hv * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(ws + l.b, b, B * hv * 2, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (gdn::launch_decode(p, out_dtype == GDN_DTYPE_F32, s) != cudaSuccess) return GDN_ERR_CUDA;
+  if (cudaMemcpyAsync(out, ws + l.out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  return GDN_OK;
 }
 
 }  // extern "C"

@@ -194,6 +194,34 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
                            int32_t* device_status, void* stream);
 
 /*
+ * gdn_decode_step with the step's activations and output in HOST memory, for a
+ * serving loop that keeps each step's tokens on the host (llmxabe README,
+ * worker diagram: the worker owns the host side of every step).  On `stream`,
+ * in order: qkv, z, a and b are copied into the workspace, the step runs as
+ * gdn_decode_step does (same bits), and its output is copied to `out`.
+ *
+ *   qkv, z, a, b   HOST, layouts as for gdn_decode_step; pinned (page-locked)
+ *                  memory keeps the copies asynchronous, pageable memory still
+ *                  works (the copies then block the calling thread)
+ *   out            HOST [batch][h_v][d_v], bf16 or fp32 per out_dtype (output;
+ *                  written once the stream reaches the end of the call)
+ *   A_log, dt_bias, conv_w, norm_w, slot, conv_state, ssm_state, device_status
+ *                  DEVICE, as for gdn_decode_step
+ *   workspace      DEVICE, 256-byte aligned, >= the bytes below (staging for
+ *                  the step's inputs and output; not touched by other calls)
+ * Every argument is checked before anything is enqueued.  batch = 0 does
+ * nothing and returns GDN_OK.
+ */
+size_t gdn_decode_step_host_workspace_bytes(const gdn_dims* dims, int batch, int out_dtype);
+gdn_status gdn_decode_step_host(const gdn_dims* dims, const void* qkv, const void* z,
+                                const void* a, const void* b, const float* A_log,
+                                const float* dt_bias, const void* conv_w,
+                                const float* norm_w, const int32_t* slot, int n_slots,
+                                int batch, float* conv_state, float* ssm_state, void* out,
+                                int out_dtype, int32_t* device_status, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/*
  * gdn_prefill with the activations in HOST memory: the call copies the inputs
  * in and the output out itself, overlapping the host link with the compute.
  *

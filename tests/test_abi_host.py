@@ -42,7 +42,8 @@ def test_header_declares_the_entry_points():
                  "gdn_decode_graph_launch", "gdn_decode_graph_destroy", "gdn_prefill_host",
                  "gdn_prefill_host_workspace_bytes", "gdn_prefill_host_segments",
                  "gdn_prefill_segment_tokens_for", "gdn_selftest_wait_timeout",
-                 "gdn_in_proj", "gdn_out_proj"):
+                 "gdn_in_proj", "gdn_out_proj", "gdn_decode_step_host",
+                 "gdn_decode_step_host_workspace_bytes"):
         assert want in names
 
 
@@ -99,6 +100,19 @@ def _decode(L, dims, **kw):
                              args["out_dtype"], args["status"], args["stream"])
 
 
+def _decode_host(L, dims, **kw):
+    args = dict(qkv=FAKE, z=FAKE, a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE, conv_w=FAKE,
+                norm_w=FAKE, slot=None, n_slots=4, batch=4, conv_state=FAKE, ssm_state=FAKE,
+                out=FAKE, out_dtype=0, status=None, ws=0x100000, ws_bytes=1 << 40, stream=None)
+    args.update(kw)
+    return L.gdn_decode_step_host(ctypes.byref(dims) if dims is not None else None, args["qkv"],
+                                  args["z"], args["a"], args["b"], args["A_log"], args["dt_bias"],
+                                  args["conv_w"], args["norm_w"], args["slot"], args["n_slots"],
+                                  args["batch"], args["conv_state"], args["ssm_state"], args["out"],
+                                  args["out_dtype"], args["status"], args["ws"], args["ws_bytes"],
+                                  args["stream"])
+
+
 def _prefill(L, dims, **kw):
     args = dict(qkv=FAKE, z=FAKE, a=FAKE, b=FAKE, A_log=FAKE, dt_bias=FAKE, conv_w=FAKE,
                 norm_w=FAKE, cu=FAKE, n_seqs=2, T=100, conv_state=FAKE, ssm_state=FAKE,
@@ -124,6 +138,38 @@ def test_decode_rejects_bad_dims(L):
     assert _decode(L, gdn.make_dims(conv_w=3)) == UNSUP
     assert _decode(L, gdn.make_dims(h_k=4, h_v=32)) == UNSUP           # G = 8
     assert _decode(L, gdn.make_dims(h_k=128, h_v=128)) == UNSUP        # h_k > 64
+
+
+def test_decode_host_workspace_and_rejections(L):
+    # staging for qkv, z, a, b and the output, each 256-byte aligned; every
+    # rejection below returns before anything is enqueued (no GPU needed)
+    d = gdn.make_dims()
+    B = 5
+    cc, zv = 2 * 16 * 128 + 32 * 128, 32 * 128
+    r = lambda x: (x + 255) // 256 * 256
+    want = r(B * cc * 2) + r(B * zv * 2) + 2 * r(B * 32 * 2)
+    assert L.gdn_decode_step_host_workspace_bytes(ctypes.byref(d), B, 0) == want + r(B * zv * 2)
+    assert L.gdn_decode_step_host_workspace_bytes(ctypes.byref(d), B, 1) == want + r(B * zv * 4)
+    assert L.gdn_decode_step_host_workspace_bytes(ctypes.byref(d), -1, 0) == 0
+    assert L.gdn_decode_step_host_workspace_bytes(ctypes.byref(d), B, 2) == 0
+    assert L.gdn_decode_step_host_workspace_bytes(ctypes.byref(gdn.make_dims(d_k=64, d_v=64)), B, 0) == 0
+    assert _decode_host(L, None) == INVALID
+    assert _decode_host(L, gdn.make_dims(d_k=64, d_v=64)) == UNSUP
+    assert _decode_host(L, d, out_dtype=2) == INVALID
+    assert _decode_host(L, d, batch=-1) == INVALID
+    assert _decode_host(L, d, batch=0, qkv=None) == OK                  # nothing to do
+    for host in ("qkv", "z", "a", "b", "out"):
+        assert _decode_host(L, d, **{host: None}) == INVALID
+    assert _decode_host(L, d, ws=None) == WS
+    assert _decode_host(L, d, ws=0x100010) == WS                        # not 256-byte aligned
+    need = L.gdn_decode_step_host_workspace_bytes(ctypes.byref(d), 4, 0)
+    assert _decode_host(L, d, ws_bytes=need - 1) == WS
+    # the device arguments are checked as gdn_decode_step checks them
+    assert _decode_host(L, d, ws_bytes=need, A_log=None) == INVALID
+    assert _decode_host(L, d, ws_bytes=need, ssm_state=FAKE + 4) == INVALID
+    assert _decode_host(L, d, ws_bytes=need, n_slots=3) == INVALID     # fewer states than entries
+    assert _decode_host(L, d, ws_bytes=need, slot=FAKE + 8) == INVALID
+    assert _decode_host(L, d, ws_bytes=need, status=FAKE + 2) == INVALID
 
 
 def test_decode_rejects_bad_pointers_and_sizes(L):

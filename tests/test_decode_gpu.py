@@ -214,3 +214,35 @@ def test_decode_is_deterministic():
         res.append((out, ssm, conv))
     for x, y in zip(*res):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("out_dtype,use_slot", [(torch.float32, False), (torch.bfloat16, True)])
+def test_decode_from_host_buffers_equals_device_step_bitwise(out_dtype, use_slot):
+    # gdn_decode_step_host (pinned host qkv/z/a/b/out, copies inside the call)
+    # against gdn_decode_step on device copies of the same tokens: 8 steps of
+    # 6 sequences (seed 86); with use_slot the sequences live in slots 7..2 of
+    # an 8-slot pool.  The output starts as NaN on the host.
+    B, S, n = 6, 8, 8
+    dims = dims_of(SH)
+    params = to_dev(gi.make_params(SH, 86))
+    st = gi.make_states(SH, n, 86, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    slot = torch.tensor([7, 6, 5, 4, 3, 2], dtype=torch.int32, device=DEV) if use_slot else None
+    conv_h, ssm_h = st["conv_state"].to(DEV), st["ssm_state"].to(DEV)
+    conv_d, ssm_d = conv_h.clone(), ssm_h.clone()
+    toks = _tokens(SH, S, B, 86)
+    ws = torch.empty(gdn.gdn_decode_step_host_workspace_bytes(dims, B, out_dtype), dtype=torch.uint8,
+                     device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for s in range(S):
+        host = {k: v[s].contiguous().pin_memory() for k, v in toks.items()}
+        out_h = torch.full((B, SH.h_v, SH.d_v), float("nan"), dtype=out_dtype).pin_memory()
+        gdn.gdn_decode_step_host(dims, host["qkv"], host["z"], host["a"], host["b"], params["A_log"],
+                                 params["dt_bias"], params["conv_w"], params["norm_w"], slot, n,
+                                 conv_h, ssm_h, out_h, ws, device_status=status)
+        out_d = torch.empty(B, SH.h_v, SH.d_v, dtype=out_dtype, device=DEV)
+        _step(dims, {k: v[s].to(DEV) for k, v in toks.items()}, params, conv_d, ssm_d, out_d, slot=slot,
+              n_slots=n)
+        torch.cuda.synchronize()
+        assert torch.equal(out_h, out_d.cpu()), f"step {s}"
+    assert torch.equal(ssm_h, ssm_d) and torch.equal(conv_h, conv_d)
+    assert gdn.gdn_read_device_status(status) == 0
