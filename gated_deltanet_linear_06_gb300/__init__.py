@@ -260,28 +260,61 @@ def gdn_decode_step_host_workspace_bytes(dims: Dims, batch: int, out_dtype=torch
     return lib().gdn_decode_step_host_workspace_bytes(ctypes.byref(dims), int(batch), code)
 
 
-def gdn_decode_step_host(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,
-                         conv_state, ssm_state, out, workspace, device_status=None, stream=None):
-    """gdn_decode_step with qkv, z, a, b and out in (pinned) HOST memory: the
-    call copies them in and out on the stream itself."""
+def _decode_step_host_args(dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,
+                           conv_state, ssm_state, out, workspace, device_status, stream):
     bf, f32 = torch.bfloat16, torch.float32
     B = int(qkv.shape[0])
     Cc = 2 * dims.h_k * dims.d_k + dims.h_v * dims.d_v
     if out.dtype not in (bf, f32):
         raise ValueError("out: want a host bfloat16 or float32 tensor")
     out_dtype = GDN_DTYPE_F32 if out.dtype == f32 else GDN_DTYPE_BF16
-    st = lib().gdn_decode_step_host(
-        ctypes.byref(dims), _hptr(qkv, bf, "qkv", B * Cc), _hptr(z, bf, "z", B * dims.h_v * dims.d_v),
-        _hptr(a, bf, "a", B * dims.h_v), _hptr(b, bf, "b", B * dims.h_v),
-        _ptr(A_log, f32, "A_log", dims.h_v), _ptr(dt_bias, f32, "dt_bias", dims.h_v),
-        _ptr(conv_w, bf, "conv_w", Cc * dims.conv_w), _ptr(norm_w, f32, "norm_w", dims.d_v),
-        _ptr(slot, torch.int32, "slot", B), int(n_slots),
-        B, _ptr(conv_state, f32, "conv_state", int(n_slots) * (dims.conv_w - 1) * Cc),
-        _ptr(ssm_state, f32, "ssm_state", int(n_slots) * dims.h_v * dims.d_v * dims.d_k),
-        _hptr(out, out.dtype, "out", B * dims.h_v * dims.d_v), out_dtype,
-        _ptr(device_status, torch.int32, "device_status", 1), _ptr(workspace, torch.uint8, "workspace"),
-        workspace.numel() if isinstance(workspace, torch.Tensor) else 0, _stream(stream))
-    _check(st, "gdn_decode_step_host")
+    return (ctypes.byref(dims), _hptr(qkv, bf, "qkv", B * Cc), _hptr(z, bf, "z", B * dims.h_v * dims.d_v),
+            _hptr(a, bf, "a", B * dims.h_v), _hptr(b, bf, "b", B * dims.h_v),
+            _ptr(A_log, f32, "A_log", dims.h_v), _ptr(dt_bias, f32, "dt_bias", dims.h_v),
+            _ptr(conv_w, bf, "conv_w", Cc * dims.conv_w), _ptr(norm_w, f32, "norm_w", dims.d_v),
+            _ptr(slot, torch.int32, "slot", B), int(n_slots),
+            B, _ptr(conv_state, f32, "conv_state", int(n_slots) * (dims.conv_w - 1) * Cc),
+            _ptr(ssm_state, f32, "ssm_state", int(n_slots) * dims.h_v * dims.d_v * dims.d_k),
+            _hptr(out, out.dtype, "out", B * dims.h_v * dims.d_v), out_dtype,
+            _ptr(device_status, torch.int32, "device_status", 1), _ptr(workspace, torch.uint8, "workspace"),
+            workspace.numel() if isinstance(workspace, torch.Tensor) else 0, _stream(stream))
+
+
+def gdn_decode_step_host(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,
+                         conv_state, ssm_state, out, workspace, device_status=None, stream=None):
+    """gdn_decode_step with qkv, z, a, b and out in (pinned) HOST memory: the
+    call copies them in and out on the stream itself."""
+    _check(lib().gdn_decode_step_host(*_decode_step_host_args(
+        dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots, conv_state, ssm_state, out,
+        workspace, device_status, stream)), "gdn_decode_step_host")
+
+
+class PreparedCall:
+    """One library call whose arguments were checked and marshalled once:
+    calling the object runs the same C function on the same buffers again
+    (refill them in place between calls), at the cost of one ctypes call.
+    The tensors it was prepared with must outlive it."""
+    __slots__ = ("_fn", "_args", "_where", "_keep")
+
+    def __init__(self, fn, args, where, keep):
+        self._fn, self._args, self._where, self._keep = fn, args, where, keep
+
+    def __call__(self) -> None:
+        st = self._fn(*self._args)
+        if st != GDN_OK:
+            raise GdnError(st, self._where)
+
+
+def prepare_decode_step_host(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,
+                             conv_state, ssm_state, out, workspace, device_status=None,
+                             stream=None) -> PreparedCall:
+    """gdn_decode_step_host on these buffers and this stream, ready to call
+    once per step (a serving loop that refills the same pinned buffers)."""
+    args = _decode_step_host_args(dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,
+                                  conv_state, ssm_state, out, workspace, device_status, stream)
+    keep = (dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, conv_state, ssm_state, out,
+            workspace, device_status)
+    return PreparedCall(lib().gdn_decode_step_host, args, "gdn_decode_step_host", keep)
 
 
 def gdn_decode_multi(dims: Dims, qkv, z, a, b, A_log, dt_bias, conv_w, norm_w, slot, n_slots,

@@ -233,12 +233,26 @@ def test_decode_from_host_buffers_equals_device_step_bitwise(out_dtype, use_slot
     ws = torch.empty(gdn.gdn_decode_step_host_workspace_bytes(dims, B, out_dtype), dtype=torch.uint8,
                      device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    # steps 4..7 through a prepared call on fixed pinned buffers refilled in place
+    fixed = {k: torch.empty(v[0].shape, dtype=v.dtype).pin_memory() for k, v in toks.items()}
+    out_fixed = torch.empty(B, SH.h_v, SH.d_v, dtype=out_dtype).pin_memory()
+    prepared = gdn.prepare_decode_step_host(dims, fixed["qkv"], fixed["z"], fixed["a"], fixed["b"],
+                                            params["A_log"], params["dt_bias"], params["conv_w"],
+                                            params["norm_w"], slot, n, conv_h, ssm_h, out_fixed, ws,
+                                            device_status=status)
     for s in range(S):
-        host = {k: v[s].contiguous().pin_memory() for k, v in toks.items()}
-        out_h = torch.full((B, SH.h_v, SH.d_v), float("nan"), dtype=out_dtype).pin_memory()
-        gdn.gdn_decode_step_host(dims, host["qkv"], host["z"], host["a"], host["b"], params["A_log"],
-                                 params["dt_bias"], params["conv_w"], params["norm_w"], slot, n,
-                                 conv_h, ssm_h, out_h, ws, device_status=status)
+        if s < 4:
+            host = {k: v[s].contiguous().pin_memory() for k, v in toks.items()}
+            out_h = torch.full((B, SH.h_v, SH.d_v), float("nan"), dtype=out_dtype).pin_memory()
+            gdn.gdn_decode_step_host(dims, host["qkv"], host["z"], host["a"], host["b"], params["A_log"],
+                                     params["dt_bias"], params["conv_w"], params["norm_w"], slot, n,
+                                     conv_h, ssm_h, out_h, ws, device_status=status)
+        else:
+            for k, v in toks.items():
+                fixed[k].copy_(v[s])
+            out_fixed.fill_(float("nan"))
+            prepared()
+            out_h = out_fixed
         out_d = torch.empty(B, SH.h_v, SH.d_v, dtype=out_dtype, device=DEV)
         _step(dims, {k: v[s].to(DEV) for k, v in toks.items()}, params, conv_d, ssm_d, out_d, slot=slot,
               n_slots=n)
