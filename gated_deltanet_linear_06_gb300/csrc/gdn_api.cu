@@ -259,6 +259,25 @@ bool decode_host_layout(const gdn_dims* d, int batch, int out_dtype, DecodeHostL
   return true;
 }
 
+// The device address of `bytes` of page-locked host memory at p, or null when
+// p is not page-locked host memory the device can address (pageable memory,
+// device memory, null): both its first and its last byte must be.
+const void* mapped_host(const void* p, size_t bytes) {
+  if (!p || bytes == 0) return nullptr;
+  cudaPointerAttributes first, last;
+  if (cudaPointerGetAttributes(&first, p) != cudaSuccess ||
+      cudaPointerGetAttributes(&last, static_cast<const char*>(p) + bytes - 1) != cudaSuccess) {
+    cudaGetLastError();   // a refused query leaves no sticky error behind
+    return nullptr;
+  }
+  if (first.type != cudaMemoryTypeHost || last.type != cudaMemoryTypeHost || !first.devicePointer ||
+      !last.devicePointer ||
+      static_cast<const char*>(last.devicePointer) - static_cast<const char*>(first.devicePointer) !=
+          (ptrdiff_t)(bytes - 1))
+    return nullptr;
+  return first.devicePointer;
+}
+
 }  // namespace
 
 extern "C" {
@@ -296,6 +315,24 @@ gdn_status gdn_decode_step_host(const gdn_dims* dims, const void* qkv, const voi
   const size_t zv = (size_t)dims->h_v * dims->d_v, hv = (size_t)dims->h_v;
   const size_t out_bytes = B * zv * (out_dtype == GDN_DTYPE_F32 ? 4 : 2);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Page-locked buffers are read and written by the step's kernel in place, over
+  // the host link: no staging copies, whose fixed cost per copy is several
+  // microseconds.  Any other host memory goes through the staging area.
+  const void* mq = mapped_host(qkv, B * cc * 2);
+  const void* mz = mapped_host(z, B * zv * 2);
+  const void* ma = mapped_host(a, B * hv * 2);
+  const void* mb = mapped_host(b, B * hv * 2);
+  void* mo = const_cast<void*>(mapped_host(out, out_bytes));
+  if (mq && mz && ma && mb && mo && ((reinterpret_cast<uintptr_t>(mq) | reinterpret_cast<uintptr_t>(mz) |
+                                      reinterpret_cast<uintptr_t>(ma) | reinterpret_cast<uintptr_t>(mb) |
+                                      reinterpret_cast<uintptr_t>(mo)) & 15u) == 0) {
+    p.qkv = static_cast<const uint16_t*>(mq);
+    p.z = static_cast<const uint16_t*>(mz);
+    p.a = static_cast<const uint16_t*>(ma);
+    p.b = static_cast<const uint16_t*>(mb);
+    p.out = mo;
+    return gdn::launch_decode(p, out_dtype == GDN_DTYPE_F32, s) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
   if (cudaMemcpyAsync(ws + l.qkv, qkv, B * cc * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(ws + l.z, z, B * zv * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(ws + l.a, a, B * hv * 2, cudaMemcpyHostToDevice, s) != cudaSuccess ||

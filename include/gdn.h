@@ -196,19 +196,24 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
 /*
  * gdn_decode_step with the step's activations and output in HOST memory, for a
  * serving loop that keeps each step's tokens on the host (llmxabe README,
- * worker diagram: the worker owns the host side of every step).  On `stream`,
- * in order: qkv, z, a and b are copied into the workspace, the step runs as
- * gdn_decode_step does (same bits), and its output is copied to `out`.
+ * worker diagram: the worker owns the host side of every step).  The step
+ * runs on `stream` as gdn_decode_step does (same bits).  When all five host
+ * buffers are page-locked memory the device can address, its kernel reads the
+ * inputs and writes the output in place over the host link (no copies);
+ * otherwise qkv, z, a and b are first copied into the workspace and the output
+ * is copied to `out` after the step, on `stream`.
  *
- *   qkv, z, a, b   HOST, layouts as for gdn_decode_step; pinned (page-locked)
- *                  memory keeps the copies asynchronous, pageable memory still
- *                  works (the copies then block the calling thread)
+ *   qkv, z, a, b   HOST, layouts as for gdn_decode_step; page-locked memory
+ *                  (cudaHostAlloc, torch pin_memory) is used in place,
+ *                  pageable memory still works (the copies then block the
+ *                  calling thread)
  *   out            HOST [batch][h_v][d_v], bf16 or fp32 per out_dtype (output;
  *                  written once the stream reaches the end of the call)
  *   A_log, dt_bias, conv_w, norm_w, slot, conv_state, ssm_state, device_status
  *                  DEVICE, as for gdn_decode_step
  *   workspace      DEVICE, 256-byte aligned, >= the bytes below (staging for
- *                  the step's inputs and output; not touched by other calls)
+ *                  the step's inputs and output when they are copied; not
+ *                  touched by other calls)
  * Every argument is checked before anything is enqueued.  batch = 0 does
  * nothing and returns GDN_OK.
  */

@@ -216,17 +216,22 @@ def test_decode_is_deterministic():
         assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("out_dtype,use_slot", [(torch.float32, False), (torch.bfloat16, True)])
-def test_decode_from_host_buffers_equals_device_step_bitwise(out_dtype, use_slot):
-    # gdn_decode_step_host (pinned host qkv/z/a/b/out, copies inside the call)
-    # against gdn_decode_step on device copies of the same tokens: 8 steps of
-    # 6 sequences (seed 86); with use_slot the sequences live in slots 7..2 of
-    # an 8-slot pool.  The output starts as NaN on the host.
-    B, S, n = 6, 8, 8
+@pytest.mark.parametrize("out_dtype,use_slot,B,pinned", [(torch.float32, False, 6, True),
+                                                         (torch.bfloat16, True, 6, True),
+                                                         (torch.bfloat16, False, 70, True),
+                                                         (torch.float32, True, 100, False),
+                                                         (torch.bfloat16, False, 6, False)])
+def test_decode_from_host_buffers_equals_device_step_bitwise(out_dtype, use_slot, B, pinned):
+    # gdn_decode_step_host (host qkv/z/a/b/out) against gdn_decode_step on device
+    # copies of the same tokens: 8 steps of B sequences (seed 86); with use_slot
+    # the sequences live in slots B+1..2 of a (B+2)-slot pool.  Page-locked
+    # buffers are read and written in place by the kernel, pageable ones go
+    # through the staging copies.  The output starts as NaN on the host.
+    S, n = 8, B + 2
     dims = dims_of(SH)
     params = to_dev(gi.make_params(SH, 86))
     st = gi.make_states(SH, n, 86, ssm_std=0.1 ** 0.5, conv_std=1.0)
-    slot = torch.tensor([7, 6, 5, 4, 3, 2], dtype=torch.int32, device=DEV) if use_slot else None
+    slot = torch.arange(B + 1, 1, -1, dtype=torch.int32, device=DEV) if use_slot else None
     conv_h, ssm_h = st["conv_state"].to(DEV), st["ssm_state"].to(DEV)
     conv_d, ssm_d = conv_h.clone(), ssm_h.clone()
     toks = _tokens(SH, S, B, 86)
@@ -234,16 +239,17 @@ def test_decode_from_host_buffers_equals_device_step_bitwise(out_dtype, use_slot
                      device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     # steps 4..7 through a prepared call on fixed pinned buffers refilled in place
-    fixed = {k: torch.empty(v[0].shape, dtype=v.dtype).pin_memory() for k, v in toks.items()}
-    out_fixed = torch.empty(B, SH.h_v, SH.d_v, dtype=out_dtype).pin_memory()
+    host_mem = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    fixed = {k: host_mem(torch.empty(v[0].shape, dtype=v.dtype)) for k, v in toks.items()}
+    out_fixed = host_mem(torch.empty(B, SH.h_v, SH.d_v, dtype=out_dtype))
     prepared = gdn.prepare_decode_step_host(dims, fixed["qkv"], fixed["z"], fixed["a"], fixed["b"],
                                             params["A_log"], params["dt_bias"], params["conv_w"],
                                             params["norm_w"], slot, n, conv_h, ssm_h, out_fixed, ws,
                                             device_status=status)
     for s in range(S):
         if s < 4:
-            host = {k: v[s].contiguous().pin_memory() for k, v in toks.items()}
-            out_h = torch.full((B, SH.h_v, SH.d_v), float("nan"), dtype=out_dtype).pin_memory()
+            host = {k: host_mem(v[s].contiguous()) for k, v in toks.items()}
+            out_h = host_mem(torch.full((B, SH.h_v, SH.d_v), float("nan"), dtype=out_dtype))
             gdn.gdn_decode_step_host(dims, host["qkv"], host["z"], host["a"], host["b"], params["A_log"],
                                      params["dt_bias"], params["conv_w"], params["norm_w"], slot, n,
                                      conv_h, ssm_h, out_h, ws, device_status=status)
