@@ -33,11 +33,13 @@ def _segments(cu, T, seg):
     return out
 
 
-def _host_call(dims, tok, pd, cu_list, st, seg):
+def _host_call(dims, tok, pd, cu_list, st, seg, pinned=True):
+    # page-locked buffers let the library's copies run asynchronously; pageable ones still work
     T = tok["qkv"].shape[0]
     N = len(cu_list) - 1
-    host = {k: v.contiguous().pin_memory() for k, v in tok.items()}
-    out = torch.full((T, SH.h_v, SH.d_v), float("nan"), dtype=torch.bfloat16).pin_memory()
+    host_mem = (lambda t: t.pin_memory()) if pinned else (lambda t: t.clone())
+    host = {k: host_mem(v.contiguous()) for k, v in tok.items()}
+    out = host_mem(torch.full((T, SH.h_v, SH.d_v), float("nan"), dtype=torch.bfloat16))
     conv, ssm = st["conv_state"].clone().to(DEV), st["ssm_state"].clone().to(DEV)
     ws = torch.empty(gdn.gdn_prefill_host_workspace_bytes(dims, N, T, seg), dtype=torch.uint8,
                      device=DEV)
@@ -76,15 +78,16 @@ def _problem(lengths, seed):
     return cu_list, params, tok, st
 
 
-@pytest.mark.parametrize("seg", [1024, 320])
-def test_prefill_host_equals_segmented_device_calls_and_matches_oracle(seg):
+@pytest.mark.parametrize("seg,pinned", [(1024, True), (320, True), (320, False), (100, True)])
+def test_prefill_host_equals_segmented_device_calls_and_matches_oracle(seg, pinned):
     # lengths 5000, 3, 0, 1200, 2500 (seed 91, carried states): segment
-    # boundaries cut sequences, a 3-token sequence and an empty one sit inside
+    # boundaries cut sequences, a 3-token sequence and an empty one sit inside;
+    # 100-token segments start at token offsets that are no multiple of 8
     lengths = [5000, 3, 0, 1200, 2500]
     cu_list, params, tok, st = _problem(lengths, 91)
     dims = dims_of(SH)
     pd = to_dev(params)
-    out_h, conv_h, ssm_h = _host_call(dims, tok, pd, cu_list, st, seg)
+    out_h, conv_h, ssm_h = _host_call(dims, tok, pd, cu_list, st, seg, pinned)
     out_d, conv_d, ssm_d = _segmented_device_calls(dims, tok, pd, cu_list, st, seg)
     assert torch.equal(out_h, out_d)
     assert torch.equal(ssm_h, ssm_d) and torch.equal(conv_h, conv_d)
