@@ -214,8 +214,10 @@ gdn_status gdn_decode_step(const gdn_dims* dims, const void* qkv, const void* z,
  *   workspace      DEVICE, 256-byte aligned, >= the bytes below (staging for
  *                  the step's inputs and output when they are copied; not
  *                  touched by other calls)
- * Every argument is checked before anything is enqueued.  batch = 0 does
- * nothing and returns GDN_OK.
+ * The host buffers are read and written when the stream executes the call:
+ * leave the inputs unchanged and do not read `out` until the stream has passed
+ * it (as with any asynchronous copy).  Every argument is checked before
+ * anything is enqueued.  batch = 0 does nothing and returns GDN_OK.
  */
 size_t gdn_decode_step_host_workspace_bytes(const gdn_dims* dims, int batch, int out_dtype);
 gdn_status gdn_decode_step_host(const gdn_dims* dims, const void* qkv, const void* z,
