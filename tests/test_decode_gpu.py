@@ -266,3 +266,32 @@ def test_decode_from_host_buffers_equals_device_step_bitwise(out_dtype, use_slot
         assert torch.equal(out_h, out_d.cpu()), f"step {s}"
     assert torch.equal(ssm_h, ssm_d) and torch.equal(conv_h, conv_d)
     assert gdn.gdn_read_device_status(status) == 0
+
+
+def test_decode_from_host_buffers_flags_a_bad_slot():
+    # entry 1's slot is out of range: skipped on the device (its host output
+    # rows keep their NaN canary) and reported in the status word; the other
+    # entries decode as the device step does
+    B, n = 3, 4
+    dims = dims_of(SH)
+    params = to_dev(gi.make_params(SH, 87))
+    st = gi.make_states(SH, n, 87, ssm_std=0.1 ** 0.5, conv_std=1.0)
+    slot = torch.tensor([3, 9, 0], dtype=torch.int32, device=DEV)
+    conv_h, ssm_h = st["conv_state"].to(DEV), st["ssm_state"].to(DEV)
+    conv_d, ssm_d = conv_h.clone(), ssm_h.clone()
+    tok = gi.make_tokens(SH, B, 87)
+    host = {k: v.pin_memory() for k, v in tok.items()}
+    out_h = torch.full((B, SH.h_v, SH.d_v), float("nan")).pin_memory()
+    out_d = torch.full((B, SH.h_v, SH.d_v), float("nan"), device=DEV)
+    ws = torch.empty(gdn.gdn_decode_step_host_workspace_bytes(dims, B, torch.float32), dtype=torch.uint8,
+                     device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    gdn.gdn_decode_step_host(dims, host["qkv"], host["z"], host["a"], host["b"], params["A_log"],
+                             params["dt_bias"], params["conv_w"], params["norm_w"], slot, n, conv_h, ssm_h,
+                             out_h, ws, device_status=status)
+    _step(dims, to_dev(tok), params, conv_d, ssm_d, out_d, slot=slot, n_slots=n)
+    torch.cuda.synchronize()
+    assert gdn.gdn_read_device_status(status) == gdn.GDN_ERR_DEVICE_BOUNDS
+    assert torch.isnan(out_h[1]).all()
+    assert torch.equal(out_h[[0, 2]], out_d[[0, 2]].cpu())
+    assert torch.equal(ssm_h, ssm_d) and torch.equal(conv_h, conv_d)
