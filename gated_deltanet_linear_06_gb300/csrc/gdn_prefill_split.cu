@@ -42,10 +42,10 @@ constexpr int kPrepThreads = 256;
 constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kMaxG = 4;   // value heads per key head on the compiled path
 // Shared memory (bytes from a 1024-aligned base), sized for three CTAs per SM:
-// two raw staging blocks (k and q first, then the v rows of the value heads in
-// turn), the fp16 [K^ | Q^] tile of the Gram product and the gates.  The value
-// heads then run one after another in the Gram tile's space, with the bf16 K^
-// tile of their W products in the first staging block.
+// two raw staging blocks (k, then the bf16 K^ tile of the W products; q, then
+// the v rows of the value heads in turn), the fp16 [K^ | Q^] tile of the Gram
+// product and the gates.  The value heads then run one after another in the
+// Gram tile's space.
 struct PrepLay {
   static constexpr uint32_t KQ16 = 0;       // fp16 [K^ | Q^], 64-column blocks 16 KB apart; then a head's area
   static constexpr uint32_t RAW = 32768;    // staging block b at RAW + b * RAW_STRIDE
@@ -88,7 +88,9 @@ __device__ __forceinline__ void conv_weights(const ConvW4& cw, float (&w)[kConvW
 // One CTA per (chunk, key head): the state-free part of the chunk for the G
 // value heads that read this key head, stored as records.  Three CTAs share an
 // SM, so one CTA's waits (a raw block in flight, a product, a barrier behind
-// its slowest warp) leave the issue slots to the other two.
+// its slowest warp) leave the issue slots to the other two; within a CTA the v
+// conv of the value heads runs beside their solves, which keep only a few warps
+// busy.
 __global__ void __launch_bounds__(kPrepThreads, 3)
     prep_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv) {
   using L_ = PrepLay;
@@ -130,12 +132,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = tmem_base_s;
-  const int quarter = warp & 3, half = warp >> 2;   // TMEM lane quarter; column half
+  const int quarter = warp & 3;   // TMEM lane quarter
   const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
   const int row = 32 * quarter + lane;
   const int y_raw = start + t0 - (kConvW - 1);      // first staged row (a chunk and its halo)
-  // Staging block b takes the k (b = 0) or q (b = 1) rows, then the v rows of
-  // value heads kh*G + b, kh*G + b + 2, ...
+  // Staging block 0 takes the k rows (later the bf16 K^ tile), block 1 the q
+  // rows and then the v rows of each value head in turn.
   auto raw_blk = [&](int b) { return sm.base + L_::RAW + b * L_::RAW_STRIDE; };
   if (tid == 32) {
 #pragma unroll
@@ -150,20 +152,22 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     if (all) ++raw_waited[b];
     return all;
   };
-  // Each warp done reading a staging block counts itself out; the last one of
-  // the block's release `rel` (counted from 0) issues its next raw load: the v
-  // rows of value head g = 2 rel + b, if the key head has it.
-  auto release_raw = [&](int b, int rel) {
+  // the v rows of value head kh*G + g into block 1 (its earlier rows read)
+  auto load_v = [&](int g) {
+    tc::fence_proxy_async();
+    mbar_expect_tx(&mb_raw[1], RAW_BLK);
+    tma_load_2d(raw_blk(1), &tm_qkv, 2 * Cq + (kh * G + g) * kD, y_raw, &mb_raw[1]);
+    ++raw_issued[1];
+  };
+  // Each warp done reading the q rows counts itself out; the last one issues
+  // the first value head's v rows into the block.
+  auto release_q = [&]() {
     __syncwarp();
     if (lane == 0) {
       __threadfence_block();
-      const int g = 2 * rel + b;
-      if (atomicAdd(&raw_read[b], 1) == kPrepWarps * (rel + 1) - 1 && g < G) {
+      if (atomicAdd(&raw_read[1], 1) == kPrepWarps - 1) {
         __threadfence_block();
-        tc::fence_proxy_async();
-        mbar_expect_tx(&mb_raw[b], RAW_BLK);
-        tma_load_2d(raw_blk(b), &tm_qkv, 2 * Cq + (kh * G + g) * kD, y_raw, &mb_raw[b]);
-        ++raw_issued[b];
+        load_v(0);
       }
     }
   };
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         store_bf16x4(rkq, o16, a.x, a.y, b.x, b.y);
       }
     }
-    release_raw(blk, 0);   // k's block takes value head 0's v rows, q's value head 1's
+    if (blk == 1) release_q();
   }
   sync_for_mma();   // the Gram tile is written
   if (ok && tid == 0) {
@@ -258,49 +262,27 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     tc::mma_commit(&mbar);
   }
 
-  // ---- conv + SiLU of v, a value head at a time, straight into its record ----
-#pragma unroll 1
-  for (int g = 0; g < G && ok; ++g) {
-    const int h = kh * G + g;
-    const int ch = 2 * Cq + h * kD + 4 * lane;
-    const ConvW4 cw_v = conv_weights_load(p.conv_w, ch);
-    if (!wait_raw(g & 1)) {
-      ok = false;
-      break;
-    }
-    float w[kConvW][4];
-    conv_weights(cw_v, w);
-    uint8_t* vh = p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecVH;
-#pragma unroll 1
-    for (int qd = 0; qd < 2; ++qd) {
-      const int tq = 4 * (warp + kPrepWarps * qd);
-      float y[4][4];
-      conv_quad_staged(raw_blk(g & 1), cs_seq + ch, Cc, t0, L, tq, lane, w, y);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
-    }
-    release_raw(g & 1, 1 + (g >> 1));
-  }
   if (ok) {
-    // the bf16 K^ tile of the W products, back from this CTA's record into the
-    // first staging block (64-column blocks 16 KB apart there, 8 KB here), once
-    // every warp is done with the block
-    __syncthreads();
+    // the bf16 K^ tile of the W products, back from this CTA's record into block
+    // 0, whose k rows every warp has read (64-column blocks 16 KB apart there,
+    // 8 KB here)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int i = tid + j * kPrepThreads, kb = i >> 9, off = (i & 511) * 16;
       *reinterpret_cast<uint4*>(sm.base + L_::KB + kb * 8192 + off) =
           __ldcg(reinterpret_cast<const uint4*>(rkq + kb * 16384 + off));
     }
-    // the Gram product (and its tile's space is free)
-    ok = __syncthreads_and(tc::mbar_wait(&mbar, 0, kWaitBudget));
-    tc::fence_after_sync();
   }
+  sync_for_mma();   // the K^ tile is written (the W products read it)
 
-  // ---- per value head, one after another: a warp per TMEM lane quarter and
-  //      column half ----
-  {
+  // ---- two groups of four warps from here on, each on its own named barrier:
+  //      warps 0-3 take the value heads one after another (a warp per TMEM lane
+  //      quarter), warps 4-7 meanwhile the v conv of each value head, straight
+  //      into its record, through block 1.  The solve runs on at most four
+  //      warps, so the other four have the conv to do. ----
+  uint32_t v_waited = 0;   // v loads waited for (group 1's threads)
+  if (warp < 4) {
+    const int htid = tid;   // 0 .. 127
     float* Af = sm.f32(L_::AREA);
     float* Tf = Af + UT_BYTES / 4;
     uint8_t* ptile = sm.base + L_::AREA + UT_BYTES;
@@ -308,6 +290,10 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     const uint32_t tw = sm.addr + L_::AREA;
     const uint32_t tm_w = tmem + TP_W;
     uint32_t wphase = 0;
+    if (ok) {   // the Gram product (and its tile's space is free)
+      ok = group_sync_and<128>(1, tc::mbar_wait(&mbar, 0, kWaitBudget));
+      tc::fence_after_sync();
+    }
 #pragma unroll 1
     for (int g = 0; g < G && ok; ++g) {
       const int h = kh * G + g;
@@ -316,8 +302,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       const float* bet = gam + 64;
       const float* eg = gam + 128;
       if (g >= 1) {   // the previous head's -W tile has left shared memory
-        if (tid == 0) bulk_wait_read();
-        __syncthreads();
+        if (htid == 0) bulk_wait_read();
+        group_sync<128>(1);
       }
       // ---- A (fp32, below its diagonal: the solve reads nothing else) and P
       //      (bf16 tile, bulk-stored into the record) from the Gram rows: lane
@@ -327,14 +313,17 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         const int t = row & 63;
         const float gt = gam[t];
         const float bt = bet[t];
-        const int c0 = 32 * half;
-        if (t < 32 && half == 1) {
-          if (quarter >= 2) {
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const int c0 = 32 * hf;
+          if (t < 32 && hf == 1) {
+            if (quarter >= 2) {
 #pragma unroll
-            for (int m = 0; m < 4; ++m)
-              *reinterpret_cast<uint4*>(ptile + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
+              for (int m = 0; m < 4; ++m)
+                *reinterpret_cast<uint4*>(ptile + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
+            }
+            continue;
           }
-        } else {
           float v[32];
           tc::tmem_ld32(tmem + lane_base + TP_G + c0, v);
           if (quarter < 2) {
@@ -357,22 +346,22 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         }
       }
       tc::fence_proxy_async();
-      __syncthreads();
-      if (tid == 0) {
+      group_sync<128>(1);
+      if (htid == 0) {
         bulk_store(rv + kRecP, ptile, 8192);
         bulk_commit();
       }
 
       // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) over A ----
-      solve_unit_lower<kPrepThreads>(Af, Tf, tid, 0, [&] {   // the P tile has left T's rows
-        if (tid == 0) bulk_wait_read();
-        __syncthreads();
+      solve_unit_lower<128>(Af, Tf, htid, 1, [&] {   // the P tile has left T's rows
+        if (htid == 0) bulk_wait_read();
+        group_sync<128>(1);
       });
       {
-        float xb[2][8], xw[2][8];
+        float xb[4][8], xw[4][8];
 #pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-          const int e = tid + q4 * kPrepThreads, t = e >> 3, c8 = (e & 7) * 8;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int e = htid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
           const float4 lo = ut_ld4(Tf, t, c8), hi = ut_ld4(Tf, t, c8 + 4);
           const float tv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
@@ -382,14 +371,17 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
           }
         }
 #pragma unroll
-        for (int q4 = 0; q4 < 2; ++q4) {
-          const int e = tid + q4 * kPrepThreads, t = e >> 3, c8 = (e & 7) * 8;
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int e = htid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
           store_bf16x8(rv + kRecTB, tc::sw128_off(t, c8, 0), xb[q4]);
           store_bf16x8(wn, tc::sw128_off(t, c8, 0), xw[q4]);
         }
       }
-      sync_for_mma();
-      if (tid == 0) {
+      tc::fence_proxy_async();
+      tc::fence_before_sync();
+      group_sync<128>(1);
+      tc::fence_after_sync();
+      if (htid == 0) {
         // W^T = K^T (T diag(beta e^gamma))^T
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -397,38 +389,72 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
                        ID_MN_A, k > 0);
         tc::mma_commit(&mb_w);
       }
-      ok = __syncthreads_and(tc::mbar_wait(&mb_w, wphase, kWaitBudget));
+      ok = group_sync_and<128>(1, tc::mbar_wait(&mb_w, wphase, kWaitBudget));
       wphase ^= 1u;
       tc::fence_after_sync();
       if (!ok) break;
 
       // ---- -W tile [d_k][t] (over T diag(beta e^gamma), which the product has
-      //      consumed): a thread's TMEM lane is its d_k row, its 32 columns 64
+      //      consumed): a thread's TMEM lane is its d_k row, each 32 columns 64
       //      contiguous bytes ----
-      {
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
         float v[32];
-        tc::tmem_ld32(tm_w + lane_base + 32 * half, v);
+        tc::tmem_ld32(tm_w + lane_base + 32 * hf, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = -v[i];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) store_bf16x8(wn, tc::sw128_off(row, 32 * half + 8 * m, 0), v + 8 * m);
+        for (int m = 0; m < 4; ++m) store_bf16x8(wn, tc::sw128_off(row, 32 * hf + 8 * m, 0), v + 8 * m);
       }
-      sync_for_mma();   // also: W^T is read before the next head's product overwrites it
-      if (tid == 0) {
+      tc::fence_proxy_async();
+      tc::fence_before_sync();   // also: W^T is read before the next head's product overwrites it
+      group_sync<128>(1);
+      tc::fence_after_sync();
+      if (htid == 0) {
         bulk_store(rv + kRecWN, wn, 16384);
         bulk_commit();
       }
     }
+  } else {
+    const int vtid = tid - 128, vwarp = warp - 4;
+#pragma unroll 1
+    for (int g = 0; g < G && ok; ++g) {
+      const int h = kh * G + g;
+      const int ch = 2 * Cq + h * kD + 4 * lane;
+      const ConvW4 cw_v = conv_weights_load(p.conv_w, ch);
+      ok = group_sync_and<128>(2, tc::mbar_wait(&mb_raw[1], raw_waited[1] & 1u, kWaitBudget));
+      if (!ok) break;
+      ++raw_waited[1];
+      ++v_waited;
+      float w[kConvW][4];
+      conv_weights(cw_v, w);
+      uint8_t* vh = p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecVH;
+#pragma unroll 1
+      for (int qd = 0; qd < 4; ++qd) {
+        const int tq = 4 * (vwarp + 4 * qd);
+        float y[4][4];
+        conv_quad_staged(raw_blk(1), cs_seq + ch, Cc, t0, L, tq, lane, w, y);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
+      }
+      group_sync<128>(2);   // every warp of the group has read the block
+      if (vtid == 0 && g + 1 < G) load_v(g + 1);
+    }
   }
+  ok = __syncthreads_and(ok);
 
   if (tid == 0) {
     if (!ok) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
     bulk_wait_read();   // the record copies have read this CTA's shared memory
   }
-  // a raw copy still in flight after a time-out must land before the shared memory goes away
-#pragma unroll
-  for (int b = 0; b < 2; ++b)
-    if ((uint32_t)raw_issued[b] > raw_waited[b]) tc::mbar_wait(&mb_raw[b], raw_waited[b] & 1u, kWaitBudget);
+  // a raw copy still in flight after a time-out must land before the shared
+  // memory goes away: block 0's (k) was waited for by every thread or by none;
+  // block 1's by the v-conv group after the q rows
+  if ((uint32_t)raw_issued[0] > raw_waited[0]) tc::mbar_wait(&mb_raw[0], raw_waited[0] & 1u, kWaitBudget);
+  if (warp >= 4 || raw_waited[1] == 0) {
+    if ((uint32_t)raw_issued[1] > raw_waited[1]) tc::mbar_wait(&mb_raw[1], raw_waited[1] & 1u, kWaitBudget);
+  }
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, TP_COLS);
