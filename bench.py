@@ -104,6 +104,14 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.file = None
+        self.start = 0
+
+    def mark(self):
+        """Samples written before this call are left out of the summary (the
+        sampler starts ahead of the timed region)."""
+        if self.file is not None:
+            self.file.flush()
+            self.start = os.fstat(self.file.fileno()).st_size
 
     def __enter__(self):
         self.file = tempfile.TemporaryFile(mode="w+")
@@ -127,7 +135,7 @@ class ClockSampler:
     def summary(self) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.file.seek(0)
+        self.file.seek(self.start)
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.file:
@@ -421,9 +429,13 @@ def run_ours(args) -> dict | None:
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     t_all0, t_all1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
     with ClockSampler(local) as clocks:
+        # the sampler's process starts before the timed region, so that its
+        # start-up does not run inside it
+        time.sleep(0.5)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        clocks.mark()
         t_all0.record(stream)
         for k in range(K):
             ev[k][0].record(stream)
