@@ -116,7 +116,7 @@ __device__ __forceinline__ void stage_raw(const CUtensorMap* tm_qkv, uint8_t* ra
   tma_load_2d(raw + 2 * RAW_BLK, tm_qkv, 2 * Cq + h * kD, y, mbar);
 }
 
-// Every thread calls this; all agree on the verdict.
+// Every thread calls this; all agree on the answer.
 __device__ bool cu_seqlens_valid(const PrefillArgs& p) {
   int bad = 0;
   for (int i = threadIdx.x; i <= p.n_seqs; i += blockDim.x) {

@@ -501,7 +501,7 @@ static_assert(ScanLay::BYTES <= 227 * 1024, "shared memory");
 // TMEM columns: S, U / Vn^T, O1 (two buffers), O2
 constexpr uint32_t TS_S = 0, TS_U = 128, TS_O1 = 192, TS_O2 = 320, TS_COLS = 512;
 
-// Block-wide sync for the tensor core that also ANDs a per-thread verdict.
+// Block-wide sync for the tensor core that also ANDs a per-thread flag.
 __device__ __forceinline__ bool sync_for_mma_and(bool ok) {
   tc::fence_proxy_async();
   tc::fence_before_sync();
