@@ -53,8 +53,7 @@ struct PrepLay {
   static constexpr uint32_t KB = RAW;       // bf16 K^ [t][d_k], 64-column blocks 8 KB apart (head phase)
   static constexpr uint32_t GATE = RAW + RAW_STRIDE + RAW_BLK;   // per value head: fp32 gamma, beta, e^gamma [64]
   static constexpr uint32_t BYTES = GATE + kMaxG * 3 * 64 * 4 + 1024;   // + slack to align the base
-  // A value head's area: the solve's A and T (fp32, 16 KB each) -- with the
-  // bf16 P tile over T's first 8 KB until the solve writes T --, then
+  // A value head's area: the solve's A and T (fp32, 16 KB each), then
   // T diag(beta e^gamma) over A, then -W [d_k][t] over A
   static constexpr uint32_t AREA = KQ16;
 };
@@ -285,7 +284,6 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     const int htid = tid;   // 0 .. 127
     float* Af = sm.f32(L_::AREA);
     float* Tf = Af + UT_BYTES / 4;
-    uint8_t* ptile = sm.base + L_::AREA + UT_BYTES;
     uint8_t* wn = sm.base + L_::AREA;
     const uint32_t tw = sm.addr + L_::AREA;
     const uint32_t tm_w = tmem + TP_W;
@@ -306,10 +304,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         group_sync<128>(1);
       }
       // ---- A (fp32, below its diagonal: the solve reads nothing else) and P
-      //      (bf16 tile, bulk-stored into the record) from the Gram rows: lane
+      //      (bf16, stored straight into the record, so that the solve need not
+      //      wait for a copy out of shared memory) from the Gram rows: lane
       //      quarters 0-1 hold K^K^T rows, 2-3 Q^K^T rows; P's rows 0-31 are
       //      zero right of column 31 ----
       {
+        uint8_t* prec = rv + kRecP;
         const int t = row & 63;
         const float gt = gam[t];
         const float bt = bet[t];
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
             if (quarter >= 2) {
 #pragma unroll
               for (int m = 0; m < 4; ++m)
-                *reinterpret_cast<uint4*>(ptile + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(prec + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
             }
             continue;
           }
@@ -341,22 +341,14 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
               v[i] = keep_if_le(v[i] * __expf(gt - gam[s]), s, t);
             }
 #pragma unroll
-            for (int m = 0; m < 4; ++m) store_bf16x8(ptile, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
+            for (int m = 0; m < 4; ++m) store_bf16x8(prec, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
           }
         }
       }
-      tc::fence_proxy_async();
-      group_sync<128>(1);
-      if (htid == 0) {
-        bulk_store(rv + kRecP, ptile, 8192);
-        bulk_commit();
-      }
+      group_sync<128>(1);   // A is written
 
       // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) over A ----
-      solve_unit_lower<128>(Af, Tf, htid, 1, [&] {   // the P tile has left T's rows
-        if (htid == 0) bulk_wait_read();
-        group_sync<128>(1);
-      });
+      solve_unit_lower<128>(Af, Tf, htid, 1);
       {
         float xb[4][8], xw[4][8];
 #pragma unroll
