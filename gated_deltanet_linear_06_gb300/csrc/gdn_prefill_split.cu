@@ -279,7 +279,6 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   //      quarter), warps 4-7 meanwhile the v conv of each value head, straight
   //      into its record, through block 1.  The solve runs on at most four
   //      warps, so the other four have the conv to do. ----
-  uint32_t v_waited = 0;   // v loads waited for (group 1's threads)
   if (warp < 4) {
     const int htid = tid;   // 0 .. 127
     float* Af = sm.f32(L_::AREA);
@@ -417,7 +416,6 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       ok = group_sync_and<128>(2, tc::mbar_wait(&mb_raw[1], raw_waited[1] & 1u, kWaitBudget));
       if (!ok) break;
       ++raw_waited[1];
-      ++v_waited;
       float w[kConvW][4];
       conv_weights(cw_v, w);
       uint8_t* vh = p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecVH;
