@@ -222,6 +222,19 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   //      straight into the record ----
   static_assert(C / 4 == 2 * kPrepWarps, "each warp takes two token quads of each block");
   const float qscale = rsqrtf((float)kD);
+  // This lane's 4 columns (4 lane .. 4 lane + 3) in row tq + i of a tile in the
+  // 128-byte swizzle: tq is a multiple of 4 whose bits 0-2 are the same for
+  // every quad a warp takes, so the row-within-atom part of the offset is fixed
+  // per thread (quad_off) and the rest is (tq >> 3) * 1024 (tc::sw128_off, with
+  // the tile's 64-column block stride kb_stride).
+  auto quad_off = [&](int tq, int i, uint32_t kb_stride) -> uint32_t {
+    const int r7 = (tq & 7) + i;
+    return (uint32_t)(lane >> 4) * kb_stride + (uint32_t)r7 * 128u +
+           ((uint32_t)(((lane >> 1) & 7) ^ r7) << 4) + ((uint32_t)(lane & 1) << 3);
+  };
+  uint32_t qk_off[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) qk_off[i] = quad_off(4 * warp, i, 16384);
 #pragma unroll
   for (int blk = 0; blk < 2; ++blk) {   // 0: k, 1: q
     if (!wait_raw(blk)) {
@@ -243,7 +256,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         const float2 r2 = make_float2(rn[i], rn[i]);
         const float2 a = __fmul2_rn(make_float2(y[i][0], y[i][1]), r2);
         const float2 b = __fmul2_rn(make_float2(y[i][2], y[i][3]), r2);
-        const uint32_t o16 = tc::sw128_off(tq + i, 4 * lane, 16384) + (blk == 0 ? 0u : 8192u);
+        const uint32_t o16 = qk_off[i] + (uint32_t)(tq >> 3) * 1024u + (blk == 0 ? 0u : 8192u);
         store_f16x4(sm.base + L_::KQ16, o16, a.x, a.y, b.x, b.y);
         store_bf16x4(rkq, o16, a.x, a.y, b.x, b.y);
       }
@@ -408,6 +421,9 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     }
   } else {
     const int vtid = tid - 128, vwarp = warp - 4;
+    uint32_t v_off[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v_off[i] = quad_off(4 * vwarp, i, 8192);
 #pragma unroll 1
     for (int g = 0; g < G && ok; ++g) {
       const int h = kh * G + g;
@@ -426,7 +442,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
         conv_quad_staged(raw_blk(1), cs_seq + ch, Cc, t0, L, tq, lane, w, y);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          store_bf16x4(vh, tc::sw128_off(tq + q, 4 * lane, 8192), y[q][0], y[q][1], y[q][2], y[q][3]);
+          store_bf16x4(vh, v_off[q] + (uint32_t)(tq >> 3) * 1024u, y[q][0], y[q][1], y[q][2], y[q][3]);
       }
       group_sync<128>(2);   // every warp of the group has read the block
       if (vtid == 0 && g + 1 < G) load_v(g + 1);
