@@ -356,8 +356,11 @@ __device__ __forceinline__ void ut_st4(float* M, int t, int s4, float a, float b
 }
 
 // acc[r][e] += sum_{k < nk} X[xr[r]][xc + k] Y[yr + k][yc + e] for two rows
-// (R = 2) or one, the sum in increasing k; nk a multiple of 4.  Column pairs
-// run as packed fp32x2 multiply-adds, each element rounding as fmaf would.
+// (R = 2) or one, the sum in increasing k; nk a multiple of 8, yr a multiple
+// of 8, yc a multiple of 4.  Column pairs run as packed fp32x2 multiply-adds,
+// each element rounding as fmaf would.  Y's rows are taken 8 at a time: row
+// yr + k8 + j has its column group yc/4 at (yc/4 ^ j) * 4 in the layout above,
+// the same 8 offsets in every block of 8 rows.
 template <int R>
 __device__ __forceinline__ void ut_rowquad(const float* X, const int (&xr)[R], int xc, const float* Y, int yr,
                                            int yc, int nk, float (&acc)[R][4]) {
@@ -367,21 +370,24 @@ __device__ __forceinline__ void ut_rowquad(const float* X, const int (&xr)[R], i
     a2[r][0] = make_float2(acc[r][0], acc[r][1]);
     a2[r][1] = make_float2(acc[r][2], acc[r][3]);
   }
-#pragma unroll 2
-  for (int k = 0; k < nk; k += 4) {
-    float xk[R][4];
+  const int ycg = yc >> 2;
+#pragma unroll 1
+  for (int k8 = 0; k8 < nk; k8 += 8) {
+    float xk[R][8];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const float4 x4 = ut_ld4(X, xr[r], xc + k);
-      xk[r][0] = x4.x; xk[r][1] = x4.y; xk[r][2] = x4.z; xk[r][3] = x4.w;
+      const float4 x0 = ut_ld4(X, xr[r], xc + k8), x1 = ut_ld4(X, xr[r], xc + k8 + 4);
+      xk[r][0] = x0.x; xk[r][1] = x0.y; xk[r][2] = x0.z; xk[r][3] = x0.w;
+      xk[r][4] = x1.x; xk[r][5] = x1.y; xk[r][6] = x1.z; xk[r][7] = x1.w;
     }
+    const float* Yb = Y + (yr + k8) * 64;
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const float4 y4 = ut_ld4(Y, yr + k + kk, yc);
+    for (int j = 0; j < 8; ++j) {
+      const float4 y4 = *reinterpret_cast<const float4*>(Yb + j * 64 + ((ycg ^ j) << 2));
       const float2 ylo = make_float2(y4.x, y4.y), yhi = make_float2(y4.z, y4.w);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const float2 x2 = make_float2(xk[r][kk], xk[r][kk]);
+        const float2 x2 = make_float2(xk[r][j], xk[r][j]);
         a2[r][0] = __ffma2_rn(x2, ylo, a2[r][0]);
         a2[r][1] = __ffma2_rn(x2, yhi, a2[r][1]);
       }
