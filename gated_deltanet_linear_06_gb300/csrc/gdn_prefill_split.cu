@@ -772,8 +772,15 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       {
         float v[16], vs[16];
         tc::tmem_ld16(tmem + lane_base + TS_U + part * 16, v);
+        // (the multiplies two per packed fp32x2 instruction, each rounding as
+        // the scalar one would, here and below)
 #pragma unroll
-        for (int i = 0; i < 16; ++i) vs[i] = v[i] * egc[part * 16 + i];
+        for (int i = 0; i < 16; i += 4) {
+          const float4 e4 = *reinterpret_cast<const float4*>(egc + part * 16 + i);
+          const float2 a = __fmul2_rn(make_float2(v[i], v[i + 1]), make_float2(e4.x, e4.y));
+          const float2 b = __fmul2_rn(make_float2(v[i + 2], v[i + 3]), make_float2(e4.z, e4.w));
+          vs[i] = a.x; vs[i + 1] = a.y; vs[i + 2] = b.x; vs[i + 3] = b.y;
+        }
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
           const uint32_t off = tc::sw128_off(row, part * 16 + 8 * m, 0);
@@ -795,8 +802,12 @@ __global__ void __launch_bounds__(kOutThreads, 1)
 #pragma unroll
         for (int m = 0; m < 4; ++m)
           store_bf16x8(sm.base + M::S, tc::sw128_off(row, part * 32 + 8 * m, 16384), v + 8 * m);
+        const float2 dC2 = make_float2(dC, dC);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= dC;
+        for (int i = 0; i < 32; i += 2) {
+          const float2 a = __fmul2_rn(make_float2(v[i], v[i + 1]), dC2);
+          v[i] = a.x; v[i + 1] = a.y;
+        }
         tc::tmem_st32(ta, v);
         warp_signal(&mb_s, lane);
       }
@@ -808,9 +819,12 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         tc::tmem_ld16(tmem + lane_base + TS_O1 + 64 * (j & 1) + part * 16, o1);
         tc::tmem_ld16(tmem + lane_base + TS_O2 + part * 16, o2);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 16; i += 2) {
           const int t = part * 16 + i;
-          Ost[t * LDO + row] = fmaf(eg[t], o1[i], o2[i]);
+          const float2 o = __ffma2_rn(make_float2(eg[t], eg[t + 1]), make_float2(o1[i], o1[i + 1]),
+                                      make_float2(o2[i], o2[i + 1]));
+          Ost[t * LDO + row] = o.x;
+          Ost[(t + 1) * LDO + row] = o.y;
         }
       }
       tc::fence_before_sync();
@@ -828,10 +842,15 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         for (int i = 0; i < 4; ++i) {
           const float4 o4 = reinterpret_cast<const float4*>(Ost + (tq + i) * LDO)[lane];
           o[i][0] = o4.x; o[i][1] = o4.y; o[i][2] = o4.z; o[i][3] = o4.w;
-          ss[i] = o4.x * o4.x;
-          ss[i] = fmaf(o4.y, o4.y, ss[i]);
-          ss[i] = fmaf(o4.z, o4.z, ss[i]);
-          ss[i] = fmaf(o4.w, o4.w, ss[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {   // tokens i and i + 1, each summed in channel order
+          float2 q = __fmul2_rn(make_float2(o[i][0], o[i + 1][0]), make_float2(o[i][0], o[i + 1][0]));
+#pragma unroll
+          for (int e = 1; e < 4; ++e)
+            q = __ffma2_rn(make_float2(o[i][e], o[i + 1][e]), make_float2(o[i][e], o[i + 1][e]), q);
+          ss[i] = q.x;
+          ss[i + 1] = q.y;
         }
         const float r = rsqrtf(warp_sum4(ss, lane) * (1.0f / kD) + p.rms_eps);
         const float4 w4 = reinterpret_cast<const float4*>(nw)[lane];
@@ -842,9 +861,14 @@ __global__ void __launch_bounds__(kOutThreads, 1)
           float g[4] = {bf16_to_f32(zr.x & 0xffffu), bf16_to_f32(zr.x >> 16), bf16_to_f32(zr.y & 0xffffu),
                         bf16_to_f32(zr.y >> 16)};
           silu4(g);
+          const float2 r2 = make_float2(rstd, rstd);
+          const float2 p0 = __fmul2_rn(__fmul2_rn(__fmul2_rn(make_float2(o[i][0], o[i][1]), r2),
+                                                  make_float2(w4.x, w4.y)), make_float2(g[0], g[1]));
+          const float2 p1 = __fmul2_rn(__fmul2_rn(__fmul2_rn(make_float2(o[i][2], o[i][3]), r2),
+                                                  make_float2(w4.z, w4.w)), make_float2(g[2], g[3]));
           uint2 ov;
-          ov.x = pack_bf16x2(o[i][0] * rstd * w4.x * g[0], o[i][1] * rstd * w4.y * g[1]);
-          ov.y = pack_bf16x2(o[i][2] * rstd * w4.z * g[2], o[i][3] * rstd * w4.w * g[3]);
+          ov.x = pack_bf16x2(p0.x, p0.y);
+          ov.y = pack_bf16x2(p1.x, p1.y);
           if (tq + i < Le)
             *reinterpret_cast<uint2*>(p.out + ((size_t)(start + t0e + tq + i) * p.h_v + h) * kD + 4 * lane) = ov;
         }
