@@ -74,7 +74,7 @@ struct Lay {
   static constexpr uint32_t TB = 131072;   // T diag(beta) [t][s]
   static constexpr uint32_t TW = 139264;   // T diag(beta e^gamma) [t][s]
   static constexpr uint32_t P = 147456;    // P [t][s]
-  static constexpr uint32_t F32 = 155648;  // fp32: the solve's A and T, 16 KB each
+  static constexpr uint32_t F32 = 155648;  // fp32: the solve's A, then T over it (17 KB)
 };
 constexpr uint32_t F32_BYTES = 2 * UT_BYTES;
 // Staging of a chunk's raw inputs, loaded by TMA (2-D tensor maps over qkv and z):
@@ -161,8 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* bet = gam + 64;
   float* eg = gam + 128;
   float* egc = gam + 192;
-  float* Af = sm.f32(M::F32);
-  float* Tf = Af + UT_BYTES / 4;
+  float* Af = sm.f32(M::F32);   // A, then T over it (the solve runs in place)
+  const float* Tf = Af;
   float* Ost = sm.f32(M::OST);      // aliases the Vn tiles (used after them)
 
   if (tid == 0) {
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
 
     // ---- T = (I + A)^{-1} ----
-    solve_unit_lower<kThreads>(Af, Tf, tid, 0);
+    solve_unit_lower<kThreads>(Af, tid, 0);
     // T diag(beta) and T diag(beta e^gamma) as bf16 tiles [t][s]
     for (int e = tid; e < 64 * 8; e += kThreads) {
       const int t = e >> 3, c8 = (e & 7) * 8;

@@ -139,13 +139,20 @@ __device__ __forceinline__ void conv_quad_staged(const uint8_t* raw_blk, const f
                                                  float (&y)[4][4]) {
   constexpr int kRows = 4 + kConvW - 1;
   float2 x[kRows][2];   // channel pairs (0, 1) and (2, 3)
+  auto staged_row = [&](int r) {
+    const uint2 v2 = *reinterpret_cast<const uint2*>(raw_blk + (tq + r) * 256 + lane * 8);
+    x[r][0] = make_float2(bf16_to_f32(v2.x & 0xffffu), bf16_to_f32(v2.x >> 16));
+    x[r][1] = make_float2(bf16_to_f32(v2.y & 0xffffu), bf16_to_f32(v2.y >> 16));
+  };
+  // rows kConvW - 1 on hold tokens tq .. tq + 3 of the chunk; only the halo
+  // rows before them can lie before the sequence
 #pragma unroll
-  for (int r = 0; r < kRows; ++r) {
+  for (int r = kConvW - 1; r < kRows; ++r) staged_row(r);
+#pragma unroll
+  for (int r = 0; r < kConvW - 1; ++r) {
     const int tau = t0 + tq - (kConvW - 1) + r;   // position in the sequence
     if (tau >= 0) {
-      const uint2 v2 = *reinterpret_cast<const uint2*>(raw_blk + (tq + r) * 256 + lane * 8);
-      x[r][0] = make_float2(bf16_to_f32(v2.x & 0xffffu), bf16_to_f32(v2.x >> 16));
-      x[r][1] = make_float2(bf16_to_f32(v2.y & 0xffffu), bf16_to_f32(v2.y >> 16));
+      staged_row(r);
     } else {
       const float4 v4 = *reinterpret_cast<const float4*>(cs + (size_t)(kConvW - 1 + tau) * cs_stride);
       x[r][0] = make_float2(v4.x, v4.y);
@@ -156,17 +163,23 @@ __device__ __forceinline__ void conv_quad_staged(const uint8_t* raw_blk, const f
   // rounds as the scalar chain w0 x0, fma(w1, x1, .), ... would)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const bool live = tq + i < L;   // padding tokens of a partial chunk are zero
 #pragma unroll
     for (int pp = 0; pp < 2; ++pp) {
       float2 acc = __fmul2_rn(make_float2(w[0][2 * pp], w[0][2 * pp + 1]), x[i][pp]);
 #pragma unroll
       for (int j = 1; j < kConvW; ++j)
         acc = __ffma2_rn(make_float2(w[j][2 * pp], w[j][2 * pp + 1]), x[i + j][pp], acc);
-      y[i][2 * pp] = live ? acc.x : 0.0f;
-      y[i][2 * pp + 1] = live ? acc.y : 0.0f;
+      y[i][2 * pp] = acc.x;
+      y[i][2 * pp + 1] = acc.y;
     }
     silu4(y[i]);
+  }
+  // padding tokens of a partial chunk are zero (as SiLU of a zero conv would
+  // leave them); the same on the whole warp, taken in a sequence's last chunk only
+  if (tq + 4 > L) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (tq + i >= L) y[i][0] = y[i][1] = y[i][2] = y[i][3] = 0.0f;
   }
 }
 
@@ -342,11 +355,13 @@ __device__ __forceinline__ bool group_sync_and(int bar_id, bool ok) {
 }
 
 // ---- the UT solve's fp32 64 x 64 matrices (A, T) ----
-// Row-major, 64 floats a row, with the 16-byte column groups of row t
-// permuted by XOR with t mod 8: a warp reading or writing one column group of
-// 8 consecutive rows, or 8 column groups of one row, touches 32 distinct banks.
-constexpr uint32_t UT_BYTES = 64 * 64 * 4;
-__device__ __forceinline__ int ut_idx(int t, int s) { return t * 64 + ((((s >> 2) ^ (t & 7)) << 2) | (s & 3)); }
+// Row-major with rows UT_LD = 68 floats apart: a warp reading or writing one
+// 16-byte column group of 8 consecutive rows, or 8 column groups of one row,
+// touches 32 distinct banks, and every element's offset is its row's base plus
+// a constant (no per-access index arithmetic).
+constexpr int UT_LD = 68;
+constexpr uint32_t UT_BYTES = 64 * UT_LD * 4;
+__device__ __forceinline__ int ut_idx(int t, int s) { return t * UT_LD + s; }
 // columns s4 .. s4+3 of row t (s4 a multiple of 4)
 __device__ __forceinline__ float4 ut_ld4(const float* M, int t, int s4) {
   return *reinterpret_cast<const float4*>(M + ut_idx(t, s4));
@@ -356,11 +371,9 @@ __device__ __forceinline__ void ut_st4(float* M, int t, int s4, float a, float b
 }
 
 // acc[r][e] += sum_{k < nk} X[xr[r]][xc + k] Y[yr + k][yc + e] for two rows
-// (R = 2) or one, the sum in increasing k; nk a multiple of 8, yr a multiple
-// of 8, yc a multiple of 4.  Column pairs run as packed fp32x2 multiply-adds,
-// each element rounding as fmaf would.  Y's rows are taken 8 at a time: row
-// yr + k8 + j has its column group yc/4 at (yc/4 ^ j) * 4 in the layout above,
-// the same 8 offsets in every block of 8 rows.
+// (R = 2) or one, the sum in increasing k; nk a multiple of 8, xc and yc
+// multiples of 4.  Column pairs run as packed fp32x2 multiply-adds, each
+// element rounding as fmaf would; Y's rows are taken 8 at a time.
 template <int R>
 __device__ __forceinline__ void ut_rowquad(const float* X, const int (&xr)[R], int xc, const float* Y, int yr,
                                            int yc, int nk, float (&acc)[R][4]) {
@@ -370,20 +383,23 @@ __device__ __forceinline__ void ut_rowquad(const float* X, const int (&xr)[R], i
     a2[r][0] = make_float2(acc[r][0], acc[r][1]);
     a2[r][1] = make_float2(acc[r][2], acc[r][3]);
   }
-  const int ycg = yc >> 2;
+  const float* Xb[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) Xb[r] = X + ut_idx(xr[r], xc);
+  const float* Yb = Y + ut_idx(yr, yc);
 #pragma unroll 1
-  for (int k8 = 0; k8 < nk; k8 += 8) {
+  for (int k8 = 0; k8 < nk; k8 += 8, Yb += 8 * UT_LD) {
     float xk[R][8];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const float4 x0 = ut_ld4(X, xr[r], xc + k8), x1 = ut_ld4(X, xr[r], xc + k8 + 4);
+      const float4 x0 = *reinterpret_cast<const float4*>(Xb[r] + k8);
+      const float4 x1 = *reinterpret_cast<const float4*>(Xb[r] + k8 + 4);
       xk[r][0] = x0.x; xk[r][1] = x0.y; xk[r][2] = x0.z; xk[r][3] = x0.w;
       xk[r][4] = x1.x; xk[r][5] = x1.y; xk[r][6] = x1.z; xk[r][7] = x1.w;
     }
-    const float* Yb = Y + (yr + k8) * 64;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float4 y4 = *reinterpret_cast<const float4*>(Yb + j * 64 + ((ycg ^ j) << 2));
+      const float4 y4 = *reinterpret_cast<const float4*>(Yb + j * UT_LD);
       const float2 ylo = make_float2(y4.x, y4.y), yhi = make_float2(y4.z, y4.w);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
@@ -400,31 +416,31 @@ __device__ __forceinline__ void ut_rowquad(const float* X, const int (&xr)[R], i
   }
 }
 
-// T = (I + A)^{-1} for a strictly lower 64 x 64 matrix A (both in the layout
-// above; A is read only below its diagonal).  With L = I + A partitioned into
-// blocks, [L11 0; L21 L22]^{-1} = [T11 0; -T22 L21 T11, T22], applied twice:
+// T = (I + A)^{-1} for a strictly lower 64 x 64 matrix A, in place: M holds A
+// (read only below its diagonal) on entry and T on return, both in the layout
+// above.  With L = I + A partitioned into blocks, [L11 0; L21 L22]^{-1} =
+// [T11 0; -T22 L21 T11, T22], applied twice:
 //   1. the four 16 x 16 diagonal blocks by forward substitution (a column per
-//      thread, 64 threads);
+//      thread, 64 threads), written over A's diagonal blocks once every
+//      thread has read them;
 //   2. 16 -> 32: T10 = -T11 (A10 T00), T32 = -T33 (A32 T22);
 //   3. 32 -> 64: T[32:64][0:32] = -T[32:64][32:64] (A[32:64][0:32] T[0:32][0:32]).
-// Each product's left factor is staged in a block of T above the diagonal,
-// where the inverse is zero: T holds the inverse on and below its diagonal
-// only, and whoever reads it takes T[t][s] = 0 for s > t.  The products run as
-// 128 units of one or two rows x 4 columns, so every output's sum has the same
-// order whatever the thread count NT (>= 128); the unit -> thread maps keep
-// each warp's loop bounds uniform.  tid: the thread's index in its group of NT;
-// bar_id: the group's named barrier (0 for the whole CTA).  Every thread of
-// the group calls it; it ends with a group barrier.  before_t() runs on every
-// thread of the group after the diagonal blocks are solved and before anything
-// is written to Tf (a caller that keeps data there until then synchronises in
-// it).
-struct NoHook {
-  __device__ void operator()() const {}
-};
-template <int NT, typename BeforeT = NoHook>
-__device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, int tid, int bar_id,
-                                                 BeforeT before_t = {}) {
+// Each product's left factor is staged in a block above the diagonal, where A
+// holds nothing and the inverse is zero, and each product's result goes over
+// the block of A that the previous step consumed.  On return M holds the
+// inverse on and below its diagonal; above it, the 16 x 16 diagonal blocks are
+// exactly +0 (forward substitution) and the other blocks hold staging data, so
+// whoever reads T takes T[t][s] = 0 for s > t.  The products run as 128 units
+// of one or two rows x 4 columns, so every output's sum has the same order
+// whatever the thread count NT (>= 128); the unit -> thread maps keep each
+// warp's loop bounds uniform.  tid: the thread's index in its group of NT;
+// bar_id: the group's named barrier (0 for the whole CTA).  Every thread of the
+// group calls it; it ends with a group barrier.
+template <int NT>
+__device__ __forceinline__ void solve_unit_lower(float* M, int tid, int bar_id) {
   static_assert(NT >= 128 && NT % 32 == 0, "the products use 128 threads");
+  const float* Af = M;
+  float* Tf = M;
   const int b = tid >> 4, c = tid & 15;
   float x[16];
   if (tid < 64) {
@@ -442,7 +458,7 @@ __device__ __forceinline__ void solve_unit_lower(const float* Af, float* Tf, int
       x[r] = acc;
     }
   }
-  before_t();
+  group_sync<NT>(bar_id);   // every thread has read the diagonal blocks of A
   if (tid < 64) {
 #pragma unroll
     for (int r = 0; r < 16; ++r) Tf[ut_idx(16 * b + r, 16 * b + c)] = x[r];

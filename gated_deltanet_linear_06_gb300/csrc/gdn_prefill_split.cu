@@ -44,22 +44,22 @@ constexpr int kMaxG = 4;   // value heads per key head on the compiled path
 // Shared memory (bytes from a 1024-aligned base), sized for three CTAs per SM:
 // two raw staging blocks (k, then the bf16 K^ tile of the W products; q, then
 // the v rows of the value heads in turn), the fp16 [K^ | Q^] tile of the Gram
-// product and the gates.  The value heads then run one after another in the
-// Gram tile's space.
+// product and the gates.  The value heads then run in the Gram tile's space,
+// two at a time, one per slot.
 struct PrepLay {
-  static constexpr uint32_t KQ16 = 0;       // fp16 [K^ | Q^], 64-column blocks 16 KB apart; then a head's area
-  static constexpr uint32_t RAW = 32768;    // staging block b at RAW + b * RAW_STRIDE
+  static constexpr uint32_t KQ16 = 0;       // fp16 [K^ | Q^], 64-column blocks 16 KB apart; then two head slots
+  static constexpr uint32_t RAW = 34816;    // staging block b at RAW + b * RAW_STRIDE
   static constexpr uint32_t RAW_STRIDE = (RAW_BLK + 1023) / 1024 * 1024;
   static constexpr uint32_t KB = RAW;       // bf16 K^ [t][d_k], 64-column blocks 8 KB apart (head phase)
   static constexpr uint32_t GATE = RAW + RAW_STRIDE + RAW_BLK;   // per value head: fp32 gamma, beta, e^gamma [64]
   static constexpr uint32_t BYTES = GATE + kMaxG * 3 * 64 * 4 + 1024;   // + slack to align the base
-  // A value head's area: the solve's A and T (fp32, 16 KB each), then
-  // T diag(beta e^gamma) over A, then -W [d_k][t] over A
+  // Slot e of the head area, at AREA + e * UT_BYTES: a value head's A, T over it
+  // (fp32, 17 KB), then T diag(beta e^gamma), then -W [d_k][t]
   static constexpr uint32_t AREA = KQ16;
 };
-static_assert(2 * UT_BYTES <= PrepLay::RAW - PrepLay::KQ16, "a head's A and T fit the Gram tile's space");
+static_assert(2 * UT_BYTES <= PrepLay::RAW - PrepLay::KQ16, "two head slots fit the Gram tile's space");
 static_assert(16384 <= RAW_BLK, "the K^ tile fits a staging block");
-static_assert(16384 <= UT_BYTES, "-W goes over A");
+static_assert(16384 <= UT_BYTES && UT_BYTES % 1024 == 0, "-W fits a slot; slots keep the tiles' alignment");
 static_assert(PrepLay::RAW % 1024 == 0 && RAW_BLK % 128 == 0, "TMA destinations need 128-byte alignment");
 static_assert(3 * (PrepLay::BYTES + 1024) <= 228 * 1024, "three prep CTAs per SM");
 constexpr uint32_t TP_G = 0, TP_W = 64, TP_COLS = 128;   // TMEM: Gram [K^;Q^]K^T, W^T of the current head
@@ -84,21 +84,33 @@ __device__ __forceinline__ void conv_weights(const ConvW4& cw, float (&w)[kConvW
     }
 }
 
+// Bounded wait for a shared-memory counter that other threads of the CTA
+// raise (after a block-scope fence) to reach n; acquire ordering on success.
+__device__ __forceinline__ bool wait_count(const int* ctr, int n) {
+  const long long t0 = clock64();
+  while (*reinterpret_cast<const volatile int*>(ctr) < n)
+    if (clock64() - t0 > kWaitBudget) return false;
+  __threadfence_block();
+  return true;
+}
+
 // One CTA per (chunk, key head): the state-free part of the chunk for the G
 // value heads that read this key head, stored as records.  Three CTAs share an
 // SM, so one CTA's waits (a raw block in flight, a product, a barrier behind
-// its slowest warp) leave the issue slots to the other two; within a CTA the v
-// conv of the value heads runs beside their solves, which keep only a few warps
-// busy.
+// its slowest warp) leave the issue slots to the other two; within a CTA two
+// groups of four warps each take every other value head and the v conv of the
+// others, so that one group's solve, which keeps only a few warps busy, runs
+// beside the other's conv.
 __global__ void __launch_bounds__(kPrepThreads, 3)
     prep_kernel(const PrefillArgs p, const __grid_constant__ CUtensorMap tm_qkv) {
   using L_ = PrepLay;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t mbar;       // the Gram product done
   __shared__ __align__(8) uint64_t mb_raw[2];  // a staging block's raw rows landed
-  __shared__ __align__(8) uint64_t mb_w;       // a value head's W product done
+  __shared__ __align__(8) uint64_t mb_w[2];    // a value head's W product done (per group)
   __shared__ int raw_read[2];                  // warps done reading a staging block (cumulative)
   __shared__ int raw_issued[2];                // raw loads issued into a staging block
+  __shared__ int w_read;                       // value heads whose W^T has been read out of TMEM
   __shared__ uint32_t tmem_base_s;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -118,7 +130,9 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
 
   if (tid == 0) {
     tc::mbar_init(&mbar, 1);
-    tc::mbar_init(&mb_w, 1);
+    tc::mbar_init(&mb_w[0], 1);
+    tc::mbar_init(&mb_w[1], 1);
+    w_read = 0;
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&mb_raw[b], 1);
       raw_read[b] = 0;
@@ -145,18 +159,16 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
       tma_load_2d(raw_blk(b), &tm_qkv, (b == 0 ? Cq : 0) + kh * kD, y_raw, &mb_raw[b]);
     }
   }
-  uint32_t raw_waited[2] = {0, 0};   // the same on every thread
-  auto wait_raw = [&](int b) -> bool {   // on a time-out the copy stays pending for the exit path
-    const bool all = __syncthreads_and(tc::mbar_wait(&mb_raw[b], raw_waited[b] & 1u, kWaitBudget));
-    if (all) ++raw_waited[b];
-    return all;
-  };
+  // the k rows (block 0) or the q rows (block 1), each block's first load; on a
+  // time-out the copy stays pending for the exit path
+  auto wait_raw = [&](int b) -> bool { return __syncthreads_and(tc::mbar_wait(&mb_raw[b], 0, kWaitBudget)); };
   // the v rows of value head kh*G + g into block 1 (its earlier rows read)
   auto load_v = [&](int g) {
     tc::fence_proxy_async();
     mbar_expect_tx(&mb_raw[1], RAW_BLK);
     tma_load_2d(raw_blk(1), &tm_qkv, 2 * Cq + (kh * G + g) * kD, y_raw, &mb_raw[1]);
-    ++raw_issued[1];
+    __threadfence_block();
+    atomicAdd(&raw_issued[1], 1);   // the other group may wait for this count
   };
   // Each warp done reading the q rows counts itself out; the last one issues
   // the first value head's v rows into the block.
@@ -287,179 +299,198 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   }
   sync_for_mma();   // the K^ tile is written (the W products read it)
 
-  // ---- two groups of four warps from here on, each on its own named barrier:
-  //      warps 0-3 take the value heads one after another (a warp per TMEM lane
-  //      quarter), warps 4-7 meanwhile the v conv of each value head, straight
-  //      into its record, through block 1.  The solve runs on at most four
-  //      warps, so the other four have the conv to do. ----
-  if (warp < 4) {
-    const int htid = tid;   // 0 .. 127
-    float* Af = sm.f32(L_::AREA);
-    float* Tf = Af + UT_BYTES / 4;
-    uint8_t* wn = sm.base + L_::AREA;
-    const uint32_t tw = sm.addr + L_::AREA;
-    const uint32_t tm_w = tmem + TP_W;
-    uint32_t wphase = 0;
-    if (ok) {   // the Gram product (and its tile's space is free)
-      ok = group_sync_and<128>(1, tc::mbar_wait(&mbar, 0, kWaitBudget));
-      tc::fence_after_sync();
-    }
+  // ---- two groups of four warps from here on (e = 0: warps 0-3, e = 1: warps
+  //      4-7), each on its own named barrier (1 + e) and with its own slot of
+  //      the head area.  Step g of group e is value head g (A, P, the solve, T
+  //      diag(beta), W) when g % 2 == e, else the v conv of value head g, so
+  //      that each group does about half of both kinds of work.  The v rows of
+  //      the heads pass through staging block 1 in head order, each load issued
+  //      by the group that read the previous one; the W^T products take the
+  //      TMEM columns TP_W in head order, each issued once the group of the
+  //      head before has read its W^T out. ----
+  const int grp = warp >> 2, gtid = tid & 127, gwarp = warp & 3;
+  const int bar = 1 + grp;
+  float* M = sm.f32(L_::AREA + grp * UT_BYTES);   // A, T over it, then T diag(beta e^gamma), then -W
+  uint8_t* wn = sm.base + L_::AREA + grp * UT_BYTES;
+  const uint32_t tw = sm.addr + L_::AREA + grp * UT_BYTES;
+  const uint32_t tm_w = tmem + TP_W;
+  // one thread's bounded wait for a shared counter to reach n, then a barrier of
+  // the group that tells everyone whether it did
+  auto group_wait_count = [&](const int* ctr, int n) -> bool {
+    bool got = true;
+    if (gtid == 0) got = wait_count(ctr, n);
+    return group_sync_and<128>(bar, got);
+  };
+  bool gram_waited = false;
+  uint32_t wphase = 0;
+  int heads = 0;   // value heads this group has done
 #pragma unroll 1
-    for (int g = 0; g < G && ok; ++g) {
-      const int h = kh * G + g;
-      uint8_t* rv = p.rec_v + ((size_t)c * p.h_v + h) * kRecV;
-      const float* gam = sm.f32(L_::GATE + g * 3 * 64 * 4);
-      const float* bet = gam + 64;
-      const float* eg = gam + 128;
-      if (g >= 1) {   // the previous head's -W tile has left shared memory
-        if (htid == 0) bulk_wait_read();
-        group_sync<128>(1);
-      }
-      // ---- A (fp32, below its diagonal: the solve reads nothing else) and P
-      //      (bf16, stored straight into the record, so that the solve need not
-      //      wait for a copy out of shared memory) from the Gram rows: lane
-      //      quarters 0-1 hold K^K^T rows, 2-3 Q^K^T rows; P's rows 0-31 are
-      //      zero right of column 31 ----
-      {
-        uint8_t* prec = rv + kRecP;
-        const int t = row & 63;
-        const float gt = gam[t];
-        const float bt = bet[t];
-#pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          const int c0 = 32 * hf;
-          if (t < 32 && hf == 1) {
-            if (quarter >= 2) {
-#pragma unroll
-              for (int m = 0; m < 4; ++m)
-                *reinterpret_cast<uint4*>(prec + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
-            }
-            continue;
-          }
-          float v[32];
-          tc::tmem_ld32(tmem + lane_base + TP_G + c0, v);
-          if (quarter < 2) {
-#pragma unroll
-            for (int m = 0; m < 8; ++m) {
-              float a[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) a[e] = bt * __expf(gt - gam[c0 + 4 * m + e]) * v[4 * m + e];
-              ut_st4(Af, t, c0 + 4 * m, a[0], a[1], a[2], a[3]);
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int s = c0 + i;
-              v[i] = keep_if_le(v[i] * __expf(gt - gam[s]), s, t);
-            }
-#pragma unroll
-            for (int m = 0; m < 4; ++m) store_bf16x8(prec, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
-          }
-        }
-      }
-      group_sync<128>(1);   // A is written
-
-      // ---- T = (I + A)^{-1}; T diag(beta) -> record, T diag(beta e^gamma) over A ----
-      solve_unit_lower<128>(Af, Tf, htid, 1);
-      {
-        float xb[4][8], xw[4][8];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int e = htid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
-          const float4 lo = ut_ld4(Tf, t, c8), hi = ut_ld4(Tf, t, c8 + 4);
-          const float tv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            xb[q4][q] = keep_if_le(tv[q], c8 + q, t) * bet[c8 + q];   // T is zero above its diagonal
-            xw[q4][q] = xb[q4][q] * eg[c8 + q];
-          }
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int e = htid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
-          store_bf16x8(rv + kRecTB, tc::sw128_off(t, c8, 0), xb[q4]);
-          store_bf16x8(wn, tc::sw128_off(t, c8, 0), xw[q4]);
-        }
-      }
-      tc::fence_proxy_async();
-      tc::fence_before_sync();
-      group_sync<128>(1);
-      tc::fence_after_sync();
-      if (htid == 0) {
-        // W^T = K^T (T diag(beta e^gamma))^T
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc::mma_bf16(tm_w, tc::sdesc_at(D_MN_V, sm.addr + L_::KB + k * 2048), tc::sdesc_at(D_K, tw + k * 32),
-                       ID_MN_A, k > 0);
-        tc::mma_commit(&mb_w);
-      }
-      ok = group_sync_and<128>(1, tc::mbar_wait(&mb_w, wphase, kWaitBudget));
-      wphase ^= 1u;
-      tc::fence_after_sync();
-      if (!ok) break;
-
-      // ---- -W tile [d_k][t] (over T diag(beta e^gamma), which the product has
-      //      consumed): a thread's TMEM lane is its d_k row, each 32 columns 64
-      //      contiguous bytes ----
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        float v[32];
-        tc::tmem_ld32(tm_w + lane_base + 32 * hf, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = -v[i];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) store_bf16x8(wn, tc::sw128_off(row, 32 * hf + 8 * m, 0), v + 8 * m);
-      }
-      tc::fence_proxy_async();
-      tc::fence_before_sync();   // also: W^T is read before the next head's product overwrites it
-      group_sync<128>(1);
-      tc::fence_after_sync();
-      if (htid == 0) {
-        bulk_store(rv + kRecWN, wn, 16384);
-        bulk_commit();
-      }
-    }
-  } else {
-    const int vtid = tid - 128, vwarp = warp - 4;
-    uint32_t v_off[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v_off[i] = quad_off(4 * vwarp, i, 8192);
-#pragma unroll 1
-    for (int g = 0; g < G && ok; ++g) {
-      const int h = kh * G + g;
+  for (int g = 0; g < G && ok; ++g) {
+    const int h = kh * G + g;
+    uint8_t* rv = p.rec_v + ((size_t)c * p.h_v + h) * kRecV;
+    if ((g & 1) != grp) {
+      // ---- the v conv of value head g, straight into its record, from block 1
+      //      (its rows the (g + 2)-th load into the block: q, then v_0 .. v_g) ----
       const int ch = 2 * Cq + h * kD + 4 * lane;
       const ConvW4 cw_v = conv_weights_load(p.conv_w, ch);
-      ok = group_sync_and<128>(2, tc::mbar_wait(&mb_raw[1], raw_waited[1] & 1u, kWaitBudget));
+      ok = group_wait_count(&raw_issued[1], 2 + g);
+      if (ok) ok = group_sync_and<128>(bar, tc::mbar_wait(&mb_raw[1], (1 + g) & 1, kWaitBudget));
       if (!ok) break;
-      ++raw_waited[1];
       float w[kConvW][4];
       conv_weights(cw_v, w);
-      uint8_t* vh = p.rec_v + ((size_t)c * p.h_v + h) * kRecV + kRecVH;
+      uint8_t* vh = rv + kRecVH;
+      uint32_t v_off[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) v_off[i] = quad_off(4 * gwarp, i, 8192);
 #pragma unroll 1
       for (int qd = 0; qd < 4; ++qd) {
-        const int tq = 4 * (vwarp + 4 * qd);
+        const int tq = 4 * (gwarp + 4 * qd);
         float y[4][4];
         conv_quad_staged(raw_blk(1), cs_seq + ch, Cc, t0, L, tq, lane, w, y);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           store_bf16x4(vh, v_off[q] + (uint32_t)(tq >> 3) * 1024u, y[q][0], y[q][1], y[q][2], y[q][3]);
       }
-      group_sync<128>(2);   // every warp of the group has read the block
-      if (vtid == 0 && g + 1 < G) load_v(g + 1);
+      group_sync<128>(bar);   // every warp of the group has read the block
+      if (gtid == 0 && g + 1 < G) load_v(g + 1);
+      continue;
     }
+    // ---- value head g ----
+    if (!gram_waited) {   // the Gram product (and its tile's space is free)
+      ok = group_sync_and<128>(bar, tc::mbar_wait(&mbar, 0, kWaitBudget));
+      tc::fence_after_sync();
+      gram_waited = true;
+      if (!ok) break;
+    }
+    const float* gam = sm.f32(L_::GATE + g * 3 * 64 * 4);
+    const float* bet = gam + 64;
+    const float* eg = gam + 128;
+    if (heads >= 1) {   // this group's previous -W tile has left its slot
+      if (gtid == 0) bulk_wait_read();
+      group_sync<128>(bar);
+    }
+    // ---- A (fp32, below its diagonal: the solve reads nothing else) and P
+    //      (bf16, stored straight into the record) from the Gram rows: lane
+    //      quarters 0-1 hold K^K^T rows, 2-3 Q^K^T rows; P's rows 0-31 are
+    //      zero right of column 31 ----
+    {
+      uint8_t* prec = rv + kRecP;
+      const int t = row & 63;
+      const float gt = gam[t];
+      const float bt = bet[t];
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+        const int c0 = 32 * hf;
+        if (t < 32 && hf == 1) {
+          if (quarter >= 2) {
+#pragma unroll
+            for (int m = 0; m < 4; ++m)
+              *reinterpret_cast<uint4*>(prec + tc::sw128_off(t, c0 + 8 * m, 0)) = make_uint4(0, 0, 0, 0);
+          }
+          continue;
+        }
+        float v[32];
+        tc::tmem_ld32(tmem + lane_base + TP_G + c0, v);
+        if (quarter < 2) {
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            float a[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a[e] = bt * __expf(gt - gam[c0 + 4 * m + e]) * v[4 * m + e];
+            ut_st4(M, t, c0 + 4 * m, a[0], a[1], a[2], a[3]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int s = c0 + i;
+            v[i] = keep_if_le(v[i] * __expf(gt - gam[s]), s, t);
+          }
+#pragma unroll
+          for (int m = 0; m < 4; ++m) store_bf16x8(prec, tc::sw128_off(t, c0 + 8 * m, 0), v + 8 * m);
+        }
+      }
+    }
+    group_sync<128>(bar);   // A is written
+
+    // ---- T = (I + A)^{-1} in place; T diag(beta) -> record, T diag(beta e^gamma)
+    //      over T once every thread has read its rows ----
+    solve_unit_lower<128>(M, gtid, bar);
+    {
+      uint4 tw8[4];   // this thread's T diag(beta e^gamma) groups, bf16, held across the barrier
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int e = gtid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
+        const float4 lo = ut_ld4(M, t, c8), hi = ut_ld4(M, t, c8 + 4);
+        const float tv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        float xb[8], xw[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          xb[q] = keep_if_le(tv[q], c8 + q, t) * bet[c8 + q];   // T is zero above its diagonal
+          xw[q] = xb[q] * eg[c8 + q];
+        }
+        store_bf16x8(rv + kRecTB, tc::sw128_off(t, c8, 0), xb);
+        tw8[q4] = make_uint4(pack_bf16x2(xw[0], xw[1]), pack_bf16x2(xw[2], xw[3]), pack_bf16x2(xw[4], xw[5]),
+                             pack_bf16x2(xw[6], xw[7]));
+      }
+      group_sync<128>(bar);   // T is read
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int e = gtid + q4 * 128, t = e >> 3, c8 = (e & 7) * 8;
+        *reinterpret_cast<uint4*>(wn + tc::sw128_off(t, c8, 0)) = tw8[q4];
+      }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    // the W^T columns are free once value head g - 1's W^T has been read out
+    ok = group_wait_count(&w_read, g);
+    tc::fence_after_sync();
+    if (!ok) break;
+    if (gtid == 0) {
+      // W^T = K^T (T diag(beta e^gamma))^T
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        tc::mma_bf16(tm_w, tc::sdesc_at(D_MN_V, sm.addr + L_::KB + k * 2048), tc::sdesc_at(D_K, tw + k * 32),
+                     ID_MN_A, k > 0);
+      tc::mma_commit(&mb_w[grp]);
+    }
+    ok = group_sync_and<128>(bar, tc::mbar_wait(&mb_w[grp], wphase, kWaitBudget));
+    wphase ^= 1u;
+    tc::fence_after_sync();
+    if (!ok) break;
+
+    // ---- -W tile [d_k][t] over T diag(beta e^gamma), which the product has
+    //      consumed: a thread's TMEM lane is its d_k row, each 32 columns 64
+    //      contiguous bytes ----
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+      float v[32];
+      tc::tmem_ld32(tm_w + lane_base + 32 * hf, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = -v[i];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) store_bf16x8(wn, tc::sw128_off(row, 32 * hf + 8 * m, 0), v + 8 * m);
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();   // W^T is read before the next head's product overwrites it
+    group_sync<128>(bar);
+    tc::fence_after_sync();
+    if (gtid == 0) {
+      __threadfence_block();
+      atomicAdd(&w_read, 1);
+      bulk_store(rv + kRecWN, wn, 16384);
+      bulk_commit();
+    }
+    ++heads;
   }
   ok = __syncthreads_and(ok);
 
+  if (gtid == 0) bulk_wait_read();   // the record copies have read this CTA's shared memory
   if (tid == 0) {
     if (!ok) record_status(p.status, GDN_ERR_DEVICE_TIMEOUT);
-    bulk_wait_read();   // the record copies have read this CTA's shared memory
-  }
-  // a raw copy still in flight after a time-out must land before the shared
-  // memory goes away: block 0's (k) was waited for by every thread or by none;
-  // block 1's by the v-conv group after the q rows
-  if ((uint32_t)raw_issued[0] > raw_waited[0]) tc::mbar_wait(&mb_raw[0], raw_waited[0] & 1u, kWaitBudget);
-  if (warp >= 4 || raw_waited[1] == 0) {
-    if ((uint32_t)raw_issued[1] > raw_waited[1]) tc::mbar_wait(&mb_raw[1], raw_waited[1] & 1u, kWaitBudget);
+    // a raw copy still in flight after a time-out must land before the shared
+    // memory goes away: each load into a block was issued after the one before
+    // it had landed, so only the last one can be pending
+    for (int b = 0; b < 2; ++b) tc::mbar_wait(&mb_raw[b], (raw_issued[b] - 1) & 1, kWaitBudget);
   }
   tc::fence_before_sync();
   __syncthreads();
