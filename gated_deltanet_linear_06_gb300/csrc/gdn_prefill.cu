@@ -766,7 +766,10 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
 //   - chaining the groups' prep passes, 1.14 -> 1.28 ms at 32K tokens;
 //   - the transfer scans on high-priority streams, beside the later prep passes
 //     (those slowed by about as much as they absorbed, and the last group's
-//     chain then queued behind the other groups' output scans), 1.14 -> 1.29 ms.
+//     chain then queued behind the other groups' output scans), 1.14 -> 1.29 ms;
+//     again once the transfer scan skipped its decayed prefix (12 us a group),
+//     with the transfer and combine passes alone on high-priority streams forked
+//     after each prep pass, 0.768 -> 0.797 ms (slow decay 0.988 -> 1.102 ms).
 // The first group runs on the caller's stream, the others on side streams, per
 // device, created on first use and kept for the life of the process; the
 // caller's stream forks to them through one event and joins back through one
