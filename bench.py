@@ -569,7 +569,7 @@ def run_ours(args) -> dict | None:
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(pre_gbs, 1), "peak": hbm, "unit": "GB/s",
                      "frac": round(pre_gbs / hbm, 4), "traffic": _traffic("prefill", PREFILL_SRC),
-                     "kernel": "gdn_prefill (all its kernels: work list, transfer, combine, output, conv state)",
+                     "kernel": "gdn_prefill (all its kernels: work list, prep, transfer, combine, output, conv state)",
                      "algorithmic_bytes_per_launch": pre_bytes,
                      "peak_source": f"{peak_src} hbm_gbs",
                      "tensor": {"achieved": round(pre_tflops, 2), "peak": tc_peak, "unit": "TFLOP/s",
