@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
     }
   }
 
-  // ---- conv + SiLU + L2 norms, k then q: into the fp16 Gram tile, and in bf16
+  // ---- conv + SiLU + L2 norms, q then k: into the fp16 Gram tile, and in bf16
   //      straight into the record ----
   static_assert(C / 4 == 2 * kPrepWarps, "each warp takes two token quads of each block");
   const float qscale = rsqrtf((float)kD);
@@ -247,8 +247,11 @@ __global__ void __launch_bounds__(kPrepThreads, 3)
   uint32_t qk_off[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) qk_off[i] = quad_off(4 * warp, i, 16384);
+  // q first (block 1), so that its block is free for the first value head's v
+  // rows, loading behind the k conv
 #pragma unroll
-  for (int blk = 0; blk < 2; ++blk) {   // 0: k, 1: q
+  for (int bi = 0; bi < 2; ++bi) {
+    const int blk = 1 - bi;   // 0: k, 1: q
     if (!wait_raw(blk)) {
       ok = false;
       break;
