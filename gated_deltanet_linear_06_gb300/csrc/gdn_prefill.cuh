@@ -144,8 +144,8 @@ __device__ __forceinline__ void conv_quad_staged(const uint8_t* raw_blk, const f
     x[r][0] = make_float2(bf16_to_f32(v2.x & 0xffffu), bf16_to_f32(v2.x >> 16));
     x[r][1] = make_float2(bf16_to_f32(v2.y & 0xffffu), bf16_to_f32(v2.y >> 16));
   };
-  // rows kConvW - 1 on hold tokens tq .. tq + 3 of the chunk; only the halo
-  // rows before them can lie before the sequence
+  // rows kConvW - 1 .. kRows - 1 hold the chunk's tokens tq .. tq + 3, which lie
+  // in the sequence; only the halo rows before them can lie before it
 #pragma unroll
   for (int r = kConvW - 1; r < kRows; ++r) staged_row(r);
 #pragma unroll
